@@ -1,0 +1,269 @@
+"""CPU oracle for the fused Adam/AdamW shard step.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import this package; the library under
+``adamw_optimizer_step_persistent_gb300`` never does, and it shares no code
+with it.  The per-element arithmetic is plain C (``fadam_oracle.c``); this
+module only marshals numpy arrays and carries the per-step bookkeeping:
+
+* the step counters: every group advances, empty or not ("[PyTorch] Advance
+  FusedAdam step counter for empty param groups", Fix section);
+* the regular path advances each counter by one before the update
+  (distributed_fused_adam.py, ``step``), the capturable path by
+  ``noop != 1`` (same function, capturable branch), and with a set noop flag
+  nothing changes at all (DistAdamCapturableFunctor, early return);
+* an optional inf/nan screen of the scaled gradients that sets the noop flag
+  before any state is touched.
+
+Arrays: fp32 data are ``np.float32``; bf16 and fp16 data are ``np.uint16``
+bit patterns; remainders are ``np.int16``.  Every function is pinned by
+``tests/test_oracle_pins.py``; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass, field
+from typing import List, Optional
+
+import numpy as np
+
+from .build import build as _build
+
+DT_NONE, DT_F32, DT_BF16, DT_F16 = 0, 1, 2, 3
+MODE_L2, MODE_ADAMW = 0, 1
+
+_LIB = None
+
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+_f32 = ctypes.c_float
+_vp = ctypes.c_void_p
+
+
+def lib():
+    """Load (building first if needed) the oracle's C library."""
+    global _LIB
+    if _LIB is None:
+        L = ctypes.CDLL(_build())
+        L.oracle_bias_correction.restype = _f32
+        L.oracle_bias_correction.argtypes = [_f32, _i32]
+        L.oracle_adam_f32.restype = None
+        L.oracle_adam_f32.argtypes = [_i64, ctypes.c_int, ctypes.c_int, _i32, _f32, _f32,
+                                      _f32, _f32, _f32, _f32, _vp, _vp, _vp, _vp,
+                                      ctypes.c_int, _vp, ctypes.c_int]
+        L.oracle_adam_rem.restype = None
+        L.oracle_adam_rem.argtypes = [_i64, ctypes.c_int, ctypes.c_int, _i32, _f32, _f32,
+                                      _f32, _f32, _f32, _f32, _vp, _vp, _vp, _vp, _vp,
+                                      ctypes.c_int, _vp]
+        L.oracle_adam_f64.restype = None
+        L.oracle_adam_f64.argtypes = [_i64, ctypes.c_int, ctypes.c_int, _i32, _f32, _f32,
+                                      _f32, _f32, _f32, _f32, _vp, _vp, _vp, _vp]
+        L.oracle_any_nonfinite.restype = ctypes.c_int
+        L.oracle_any_nonfinite.argtypes = [_i64, _vp, ctypes.c_int, _f32]
+        L.oracle_rem_pack_n.restype = None
+        L.oracle_rem_pack_n.argtypes = [_i64, _vp, _vp, _vp]
+        L.oracle_rem_split_n.restype = None
+        L.oracle_rem_split_n.argtypes = [_i64, _vp, _vp, _vp]
+        for name in ("oracle_f32_to_bf16_n", "oracle_f32_to_f16_n", "oracle_bf16_to_f32_n",
+                     "oracle_f16_to_f32_n"):
+            getattr(L, name).restype = None
+            getattr(L, name).argtypes = [_i64, _vp, _vp]
+        _LIB = L
+    return _LIB
+
+
+def _ptr(a: Optional[np.ndarray]):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be contiguous"
+    return a.ctypes.data
+
+
+def _check(a: np.ndarray, dtype, n: int, what: str):
+    assert a.dtype == dtype, f"{what}: expected {np.dtype(dtype)}, got {a.dtype}"
+    assert a.size == n, f"{what}: expected {n} elements, got {a.size}"
+
+
+_G_NP = {DT_F32: np.float32, DT_BF16: np.uint16, DT_F16: np.uint16}
+
+
+# ---- scalar helpers ---------------------------------------------------------
+
+def bias_correction(beta: float, step: int) -> np.float32:
+    """1 - beta^step with beta a float, pow in double, rounded once to float."""
+    return np.float32(lib().oracle_bias_correction(float(np.float32(beta)), int(step)))
+
+
+def _map_n(fn, x, out_dtype):
+    x = np.ascontiguousarray(x)
+    out = np.empty(x.shape, dtype=out_dtype)
+    fn(x.size, _ptr(x), _ptr(out))
+    return out
+
+
+def f32_to_bf16(x) -> np.ndarray:
+    return _map_n(lib().oracle_f32_to_bf16_n, np.asarray(x, dtype=np.float32), np.uint16)
+
+
+def f32_to_f16(x) -> np.ndarray:
+    return _map_n(lib().oracle_f32_to_f16_n, np.asarray(x, dtype=np.float32), np.uint16)
+
+
+def bf16_to_f32(h) -> np.ndarray:
+    return _map_n(lib().oracle_bf16_to_f32_n, np.asarray(h, dtype=np.uint16), np.float32)
+
+
+def f16_to_f32(h) -> np.ndarray:
+    return _map_n(lib().oracle_f16_to_f32_n, np.asarray(h, dtype=np.uint16), np.float32)
+
+
+def rem_pack(hi, rem) -> np.ndarray:
+    """(bf16 high half, int16 remainder) -> fp32 bit patterns (uint32)."""
+    hi = np.ascontiguousarray(hi, dtype=np.uint16)
+    rem = np.ascontiguousarray(rem, dtype=np.int16)
+    out = np.empty(hi.shape, dtype=np.uint32)
+    lib().oracle_rem_pack_n(hi.size, _ptr(hi), _ptr(rem), _ptr(out))
+    return out
+
+
+def rem_split(bits):
+    """fp32 bit patterns (uint32) -> (bf16 high half, int16 remainder)."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint32)
+    hi = np.empty(bits.shape, dtype=np.uint16)
+    rem = np.empty(bits.shape, dtype=np.int16)
+    lib().oracle_rem_split_n(bits.size, _ptr(bits), _ptr(hi), _ptr(rem))
+    return hi, rem
+
+
+# ---- per-tensor update ------------------------------------------------------
+
+@dataclass
+class Group:
+    """Hyper-parameters of one param group (the functor's arguments)."""
+    mode: int = MODE_ADAMW
+    bias_correction: int = 1
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    weight_decay: float = 0.0
+    lr: float = 1e-3
+    grad_scale: float = 1.0
+
+
+def adam_f32(group: Group, step: int, p, m, v, g, g_dtype=DT_F32, p_out=None,
+             out_dtype=DT_NONE) -> None:
+    """Update one tensor with an fp32 master in place (p, m, v, p_out)."""
+    n = p.size
+    _check(p, np.float32, n, "p")
+    _check(m, np.float32, n, "m")
+    _check(v, np.float32, n, "v")
+    _check(g, _G_NP[g_dtype], n, "g")
+    if out_dtype != DT_NONE:
+        _check(p_out, np.float32 if out_dtype == DT_F32 else np.uint16, n, "p_out")
+    lib().oracle_adam_f32(n, group.mode, group.bias_correction, step, group.beta1,
+                          group.beta2, group.eps, group.weight_decay, group.lr,
+                          group.grad_scale, _ptr(p), _ptr(m), _ptr(v), _ptr(g), g_dtype,
+                          _ptr(p_out) if out_dtype != DT_NONE else None, out_dtype)
+
+
+def adam_rem(group: Group, step: int, p_hi, rem, m, v, g, g_dtype, p_out) -> None:
+    """Update one tensor whose master is bf16 high half + int16 remainder."""
+    n = p_hi.size
+    _check(p_hi, np.uint16, n, "p_hi")
+    _check(rem, np.int16, n, "rem")
+    _check(m, np.float32, n, "m")
+    _check(v, np.float32, n, "v")
+    _check(g, _G_NP[g_dtype], n, "g")
+    _check(p_out, np.uint16, n, "p_out")
+    lib().oracle_adam_rem(n, group.mode, group.bias_correction, step, group.beta1,
+                          group.beta2, group.eps, group.weight_decay, group.lr,
+                          group.grad_scale, _ptr(p_hi), _ptr(rem), _ptr(m), _ptr(v), _ptr(g),
+                          g_dtype, _ptr(p_out))
+
+
+def adam_f64(group: Group, step: int, p, m, v, g) -> None:
+    """Double-precision evaluation (error analysis only); arrays are float64."""
+    n = p.size
+    for a, w in ((p, "p"), (m, "m"), (v, "v"), (g, "g")):
+        _check(a, np.float64, n, w)
+    lib().oracle_adam_f64(n, group.mode, group.bias_correction, step, group.beta1,
+                          group.beta2, group.eps, group.weight_decay, group.lr,
+                          group.grad_scale, _ptr(p), _ptr(m), _ptr(v), _ptr(g))
+
+
+def any_nonfinite(g, g_dtype, grad_scale) -> bool:
+    g = np.ascontiguousarray(g)
+    return bool(lib().oracle_any_nonfinite(g.size, _ptr(g), g_dtype, float(grad_scale)))
+
+
+# ---- whole shard step -------------------------------------------------------
+
+@dataclass
+class Tensor:
+    """One tensor of the shard, as numpy arrays updated in place.
+
+    For an fp32 master set ``p``; for the remainder form set ``p_hi`` (bf16
+    bits) and ``rem`` and give ``p_out`` (bf16 bits, may be ``p_hi`` itself).
+    """
+    group: int
+    m: np.ndarray
+    v: np.ndarray
+    g: np.ndarray
+    g_dtype: int = DT_F32
+    p: Optional[np.ndarray] = None
+    p_hi: Optional[np.ndarray] = None
+    rem: Optional[np.ndarray] = None
+    p_out: Optional[np.ndarray] = None
+    out_dtype: int = DT_NONE
+
+
+@dataclass
+class Shard:
+    """A shard: param groups, tensors and the step counters.
+
+    ``step_slot[i]`` names the counter group i uses; groups may share one
+    counter (one optimizer-wide step) or own one each (one per group).
+    """
+    groups: List[Group]
+    tensors: List[Tensor]
+    steps: List[int] = field(default_factory=list)
+    step_slot: List[int] = field(default_factory=list)
+
+    def __post_init__(self):
+        if not self.step_slot:
+            self.step_slot = list(range(len(self.groups)))
+        if not self.steps:
+            self.steps = [0] * (max(self.step_slot) + 1 if self.step_slot else 0)
+
+
+def shard_step(shard: Shard, *, capturable: bool, noop: bool = False,
+               check_finite: bool = False, step_preadvanced: bool = False) -> bool:
+    """Apply one optimizer step to every tensor of the shard.
+
+    Returns the noop flag as it stands after the step (it can only go from
+    0 to 1, through the inf/nan screen).  With the flag set nothing changes:
+    neither the tensors nor, on either path, the step counters.
+    """
+    if check_finite and not noop:
+        for t in shard.tensors:
+            if any_nonfinite(t.g, t.g_dtype, shard.groups[t.group].grad_scale):
+                noop = True
+                break
+    if noop:
+        return True
+    if not (capturable and step_preadvanced):
+        for slot in sorted(set(shard.step_slot)):
+            shard.steps[slot] += 1
+    for t in shard.tensors:
+        grp = shard.groups[t.group]
+        step = shard.steps[shard.step_slot[t.group]]
+        if t.rem is not None:
+            adam_rem(grp, step, t.p_hi, t.rem, t.m, t.v, t.g, t.g_dtype, t.p_out)
+        else:
+            adam_f32(grp, step, t.p, t.m, t.v, t.g, t.g_dtype, t.p_out, t.out_dtype)
+    return False
+
+
+def group_steps(shard: Shard) -> List[int]:
+    """The step each group reports (its counter's value)."""
+    return [shard.steps[s] for s in shard.step_slot]

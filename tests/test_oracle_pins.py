@@ -1,0 +1,504 @@
+"""Pins of the CPU oracle to things other than itself (no GPU needed).
+
+Each test ties an oracle function to a hand-derived worked example, a closed
+form of the Adam recursion, an exhaustive or property check, a conversion
+done by numpy or torch, or a value printed on the pages.  None of them
+re-types the oracle's per-element sequence.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import DT_BF16, DT_F16, DT_F32, MODE_ADAMW, MODE_L2, Group
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+F32_EPS = 2.0 ** -24  # unit roundoff of fp32
+
+
+def _ulp(x):
+    return np.spacing(np.abs(np.asarray(x, dtype=np.float32))).astype(np.float64)
+
+
+# ---- worked examples ---------------------------------------------------------
+
+def _worked_examples():
+    rows = []
+    with open(os.path.join(GOLDEN, "worked_examples.txt")) as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, *kvs = line.split()
+            d = dict(kv.split("=") for kv in kvs)
+            rows.append((name, d))
+    return rows
+
+
+@pytest.mark.parametrize("name,d", _worked_examples(),
+                         ids=[r[0] for r in _worked_examples()])
+def test_worked_example_fp32_exact(name, d):
+    mode = MODE_ADAMW if d["mode"] == "adamw" else MODE_L2
+    grp = Group(mode=mode, bias_correction=int(d["bc"]), beta1=float(d["beta1"]),
+                beta2=float(d["beta2"]), eps=float(d["eps"]), weight_decay=float(d["wd"]),
+                lr=float(d["lr"]), grad_scale=float(d["gs"]))
+    p = np.array([float(d["p"])], np.float32)
+    m = np.array([float(d["m"])], np.float32)
+    v = np.array([float(d["v"])], np.float32)
+    g = np.array([float(d["g"])], np.float32)
+    oracle.adam_f32(grp, int(d["step"]), p, m, v, g, DT_F32)
+    assert p[0] == np.float32(d["p_new"]), (name, p[0])
+    assert m[0] == np.float32(d["m_new"]), (name, m[0])
+    assert v[0] == np.float32(d["v_new"]), (name, v[0])
+    # the double evaluation reaches the same exact values
+    p64, m64, v64 = (np.array([float(d[k])]) for k in ("p", "m", "v"))
+    oracle.adam_f64(grp, int(d["step"]), p64, m64, v64, np.array([float(d["g"])]))
+    assert (p64[0], m64[0], v64[0]) == (float(d["p_new"]), float(d["m_new"]), float(d["v_new"]))
+
+
+def test_worked_example_remainder_form():
+    # Example A on a master held as bf16 1.0 + remainder 0: the new master
+    # 0.9609375 has 8 significant bits, so it splits into 0x3F76 and 0.
+    grp = Group(mode=MODE_ADAMW, bias_correction=1, beta1=0.5, beta2=0.75, eps=0.5,
+                weight_decay=0.125, lr=0.0625, grad_scale=1.0)
+    hi = np.array([0x3F80], np.uint16)
+    rem = np.array([0], np.int16)
+    m = np.zeros(1, np.float32)
+    v = np.zeros(1, np.float32)
+    out = np.zeros(1, np.uint16)
+    oracle.adam_rem(grp, 1, hi, rem, m, v, np.array([0.5], np.float32), DT_F32, out)
+    assert out[0] == 0x3F76 and rem[0] == 0 and m[0] == 0.25 and v[0] == 0.0625
+
+
+# ---- remainders --------------------------------------------------------------
+
+def _remainder_rows():
+    rows = []
+    with open(os.path.join(GOLDEN, "remainder_split.txt")) as fh:
+        for line in fh:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                a, b, c = line.split()
+                rows.append((int(a, 16), int(b, 16), int(c)))
+    return rows
+
+
+def test_remainder_golden_rows():
+    rows = _remainder_rows()
+    bits = np.array([r[0] for r in rows], np.uint32)
+    hi, rem = oracle.rem_split(bits)
+    assert hi.tolist() == [r[1] for r in rows]
+    assert rem.tolist() == [r[2] for r in rows]
+    back = oracle.rem_pack(np.array([r[1] for r in rows], np.uint16),
+                           np.array([r[2] for r in rows], np.int16))
+    assert back.tolist() == [r[0] for r in rows]
+
+
+def test_remainder_roundtrip_all_2pow32():
+    """pack(split(x)) == x for every one of the 2^32 fp32 bit patterns.
+
+    A left inverse on a finite set of the same size is a bijection, so this
+    also gives split(pack(h, r)) == (h, r) for every (bf16, int16) pair.
+    """
+    L = oracle.lib()
+    chunk = 1 << 22
+    x = np.empty(chunk, np.uint32)
+    hi = np.empty(chunk, np.uint16)
+    rem = np.empty(chunk, np.int16)
+    back = np.empty(chunk, np.uint32)
+    base = np.arange(chunk, dtype=np.uint32)
+    for start in range(0, 1 << 32, chunk):
+        np.add(base, np.uint32(start), out=x)
+        L.oracle_rem_split_n(chunk, x.ctypes.data, hi.ctypes.data, rem.ctypes.data)
+        L.oracle_rem_pack_n(chunk, hi.ctypes.data, rem.ctypes.data, back.ctypes.data)
+        if not np.array_equal(back, x):
+            bad = np.nonzero(back != x)[0][0]
+            pytest.fail(f"round trip breaks at 0x{int(x[bad]):08X}")
+
+
+def test_remainder_high_half_is_nearest_bf16():
+    """The split's high half is a nearest bf16 to the master, ties away from 0."""
+    rng = np.random.default_rng(7)
+    bits = rng.integers(0, 1 << 32, size=1 << 20, dtype=np.uint64).astype(np.uint32)
+    # every midpoint and near-midpoint low half for random high halves
+    hs = rng.integers(0, 1 << 16, size=4096, dtype=np.uint64).astype(np.uint32)
+    lows = np.array([0x7FFF, 0x8000, 0x8001, 0x0000, 0xFFFF], np.uint32)
+    bits = np.concatenate([bits, ((hs[:, None] << 16) | lows[None, :]).ravel()])
+    hi, _ = oracle.rem_split(bits)
+    with np.errstate(invalid="ignore"):
+        x = bits.view(np.float32).astype(np.float64)
+        hv = (hi.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        trunc = ((bits >> 16) << 16).view(np.float32).astype(np.float64)
+        up = (((bits >> 16) + 1) << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    ok = np.isfinite(x) & np.isfinite(hv) & np.isfinite(up)
+    x, hv, trunc, up = x[ok], hv[ok], trunc[ok], up[ok]
+    other = np.where(hv == trunc, up, trunc)
+    dh, do = np.abs(x - hv), np.abs(x - other)
+    assert np.all(dh <= do)
+    tie = dh == do
+    assert np.all(np.abs(hv[tie]) >= np.abs(x[tie]))
+
+
+# ---- conversions -------------------------------------------------------------
+
+def _special_f32_bits():
+    rng = np.random.default_rng(11)
+    rnd = rng.integers(0, 1 << 32, size=1 << 22, dtype=np.uint64).astype(np.uint32)
+    # rounding-relevant low-bit patterns under every exponent
+    exps = np.arange(0, 256, dtype=np.uint32)
+    mhi = rng.integers(0, 1 << 23, size=64, dtype=np.uint64).astype(np.uint32) & 0x7FE000
+    lows = np.array([0, 1, 0xFFF, 0x1000, 0x1001, 0x1FFF, 0x7FFF, 0x8000, 0x8001, 0xFFFF],
+                    np.uint32)
+    grid = ((exps[:, None, None] << 23) | mhi[None, :, None] | lows[None, None, :]).ravel()
+    fixed = np.array([0, 0x7F800000, 0x7FC00000, 0x7F800001, 0x477FE000, 0x477FEFFF,
+                      0x477FF000, 0x477FF001, 0x38800000, 0x387FFFFF, 0x33000000, 0x33000001,
+                      0x337FFFFF, 0x33800000, 0x7F7FFFFF, 0x7F7F8000, 0x00000001], np.uint32)
+    return np.concatenate([rnd, grid, grid | 0x80000000, fixed, fixed | 0x80000000])
+
+
+def test_bf16_rounding_matches_torch():
+    x = _special_f32_bits().view(np.float32)
+    ours = oracle.f32_to_bf16(x)
+    ref = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(x)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.all(np.isnan(oracle.bf16_to_f32(ours[nan])))
+
+
+def test_f16_rounding_matches_numpy():
+    x = _special_f32_bits().view(np.float32)
+    ours = oracle.f32_to_f16(x)
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    nan = np.isnan(x)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.all(np.isnan(oracle.f16_to_f32(ours[nan])))
+
+
+def test_widening_all_16bit_patterns():
+    h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref_bf = torch.from_numpy(h.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+    ref_h = h.view(np.float16).astype(np.float32)
+    for ours, ref in ((oracle.bf16_to_f32(h), ref_bf), (oracle.f16_to_f32(h), ref_h)):
+        nan = np.isnan(ref)
+        assert np.array_equal(np.isnan(ours), nan)
+        assert np.array_equal(ours[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+# ---- bias correction -----------------------------------------------------------
+
+@pytest.mark.parametrize("beta", [0.5, 0.75, 0.9, 0.95, 0.999, 0.9999])
+def test_bias_correction_is_correctly_rounded(beta):
+    """1 - beta^k against its exact rational value rounded once to fp32."""
+    b = Fraction(float(np.float32(beta)))
+    for k in list(range(1, 40)) + [100, 1000]:
+        want = np.float32(float(1 - b ** k))
+        got = oracle.bias_correction(beta, k)
+        # double pow is within a few double ulps; after the one rounding to
+        # fp32 that can move the result by at most one fp32 ulp
+        assert abs(float(got) - float(want)) <= float(np.spacing(want)), (beta, k, got, want)
+    assert oracle.bias_correction(0.5, 3) == np.float32(0.875)
+    assert oracle.bias_correction(0.5, 24) == np.float32(1 - 2.0 ** -24)
+
+
+# ---- closed forms --------------------------------------------------------------
+
+def _rand_problem(n, seed, gscale=1e-3):
+    rng = np.random.default_rng(seed)
+    p = rng.standard_normal(n).astype(np.float32)
+    g = (rng.standard_normal(n) * gscale).astype(np.float32)
+    # a spread of magnitudes, including grads near and below eps
+    g[: n // 8] *= np.float32(1e-5)
+    g[n // 8: n // 4] *= np.float32(1e3)
+    return p, g
+
+
+@pytest.mark.parametrize("wd", [0.0, 0.1])
+def test_closed_form_adamw_step1(wd):
+    """AdamW, bias correction on, zero moments: m^ = sg and v^ = sg^2 at step 1,
+    so p1 = p0 - lr*(sg/(|sg|+eps) + wd*p0)."""
+    n = 50_000
+    p0, g = _rand_problem(n, 1)
+    grp = Group(mode=MODE_ADAMW, bias_correction=1, beta1=0.9, beta2=0.95, eps=1e-8,
+                weight_decay=wd, lr=1.6e-3, grad_scale=0.5)
+    p, m, v = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    oracle.adam_f32(grp, 1, p, m, v, g, DT_F32)
+    sg = g.astype(np.float64) * 0.5
+    eps = float(np.float32(1e-8))
+    lr, wdd = float(np.float32(1.6e-3)), float(np.float32(wd))
+    u = sg / (np.abs(sg) + eps) + wdd * p0
+    want = p0 - lr * u
+    tol = _ulp(want) + lr * (np.abs(u) + 1.0) * 32 * F32_EPS
+    assert np.all(np.abs(p - want) <= tol)
+
+
+def test_closed_form_l2_step1():
+    """L2 mode at step 1: s = g*gs + wd*p0 and p1 = p0 - lr*s/(|s|+eps)."""
+    n = 50_000
+    p0, g = _rand_problem(n, 2, gscale=1e-2)
+    grp = Group(mode=MODE_L2, bias_correction=1, beta1=0.9, beta2=0.95, eps=1e-8,
+                weight_decay=0.1, lr=1e-3, grad_scale=1.0 / 65536)
+    p, m, v = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    oracle.adam_f32(grp, 1, p, m, v, g, DT_F32)
+    s = g.astype(np.float64) * (1.0 / 65536) + float(np.float32(0.1)) * p0
+    lr = float(np.float32(1e-3))
+    want = p0 - lr * s / (np.abs(s) + float(np.float32(1e-8)))
+    assert np.all(np.abs(p - want) <= _ulp(want) + lr * 32 * F32_EPS)
+    # the first moment is the first moving average of s
+    assert np.allclose(m, (1 - float(np.float32(0.9))) * s, rtol=8 * F32_EPS, atol=0)
+
+
+@pytest.mark.parametrize("bc", [1, 0])
+def test_closed_form_constant_gradient_ten_steps(bc):
+    """Constant gradient, zero initial moments, wd = 0: after k steps
+    m_k = (1-b1^k) sg and v_k = (1-b2^k) sg^2 exactly, so each step moves p by
+    lr*sg/(|sg|+eps) with bias correction, and by
+    lr*(1-b1^k) sg/(sqrt(1-b2^k)|sg|+eps) without it."""
+    n, K = 20_000, 10
+    p0, g = _rand_problem(n, 3)
+    b1, b2 = float(np.float32(0.9)), float(np.float32(0.999))
+    grp = Group(mode=MODE_ADAMW, bias_correction=bc, beta1=0.9, beta2=0.999, eps=1e-8,
+                weight_decay=0.0, lr=1e-3, grad_scale=1.0)
+    p, m, v = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    sg = g.astype(np.float64)
+    want = p0.astype(np.float64)
+    lr, eps = float(np.float32(1e-3)), float(np.float32(1e-8))
+    for k in range(1, K + 1):
+        oracle.adam_f32(grp, k, p, m, v, g, DT_F32)
+        if bc:
+            want = want - lr * sg / (np.abs(sg) + eps)
+        else:
+            want = want - lr * (1 - b1 ** k) * sg / (math.sqrt(1 - b2 ** k) * np.abs(sg) + eps)
+        tol = K * _ulp(want) + lr * K * K * 16 * F32_EPS
+        assert np.all(np.abs(p - want) <= tol), k
+        assert np.allclose(m, (1 - b1 ** k) * sg, rtol=4 * k * F32_EPS, atol=1e-30)
+        assert np.allclose(v, (1 - b2 ** k) * sg * sg, rtol=4 * k * F32_EPS, atol=1e-37)
+
+
+def test_closed_form_adamw_decay_only():
+    """Zero gradient, AdamW: the moments stay zero and the update is pure
+    decay, p_k = p0 (1 - lr wd)^k."""
+    n, K = 10_000, 10
+    p0, _ = _rand_problem(n, 4)
+    grp = Group(mode=MODE_ADAMW, bias_correction=1, beta1=0.9, beta2=0.95, eps=1e-8,
+                weight_decay=0.1, lr=1.6e-3)
+    p, m, v = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    g = np.zeros(n, np.float32)
+    for k in range(1, K + 1):
+        oracle.adam_f32(grp, k, p, m, v, g, DT_F32)
+    a = float(np.float32(1.6e-3)) * float(np.float32(0.1))
+    want = p0.astype(np.float64) * (1 - a) ** K
+    assert np.all(np.abs(p - want) <= 2 * K * _ulp(want))
+    assert not m.any() and not v.any()
+
+
+def test_double_evaluation_closed_forms():
+    """The double evaluation meets the AdamW recursion with m^ = sg, v^ = sg^2
+    (constant gradient) to double rounding over ten steps."""
+    n = 20_000
+    p0, g = _rand_problem(n, 5)
+    grp = Group(mode=MODE_ADAMW, bias_correction=1, beta1=0.9, beta2=0.95, eps=1e-8,
+                weight_decay=0.1, lr=1e-3, grad_scale=1.0)
+    lr, wd, eps = (float(np.float32(x)) for x in (1e-3, 0.1, 1e-8))
+    pd, md, vd = p0.astype(np.float64), np.zeros(n), np.zeros(n)
+    sg = g.astype(np.float64)
+    want = p0.astype(np.float64)
+    for k in range(1, 11):
+        oracle.adam_f64(grp, k, pd, md, vd, sg)
+        want = want - lr * (sg / (np.abs(sg) + eps) + wd * want)
+        assert np.all(np.abs(pd - want) <= 1e-13 * (np.abs(want) + 1.0)), k
+
+
+def test_double_evaluation_agrees_with_fp32():
+    """fp32 and double evaluations stay within the fp32 rounding the
+    recursion accumulates: each step rounds p at the scale of |p| and the
+    moving averages at the scale of their two terms."""
+    n, K = 30_000, 10
+    p0, g = _rand_problem(n, 5)
+    for mode in (MODE_ADAMW, MODE_L2):
+        grp = Group(mode=mode, bias_correction=1, beta1=0.9, beta2=0.95, eps=1e-8,
+                    weight_decay=0.1, lr=1e-3, grad_scale=1.0)
+        p, m, v = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+        pd, md, vd = p0.astype(np.float64), np.zeros(n), np.zeros(n)
+        pscale = np.abs(p0).astype(np.float64)
+        sgmax = np.abs(g).astype(np.float64)
+        if mode == MODE_L2:
+            sgmax = sgmax + 0.1 * (np.abs(p0) + 0.02)
+        for k in range(1, K + 1):
+            oracle.adam_f32(grp, k, p, m, v, g, DT_F32)
+            oracle.adam_f64(grp, k, pd, md, vd, g.astype(np.float64))
+            pscale = np.maximum(pscale, np.abs(pd))
+        assert np.all(np.abs(p - pd) <= 2 * K * F32_EPS * pscale + 1e-3 * K * 64 * F32_EPS)
+        assert np.all(np.abs(m - md) <= 8 * K * F32_EPS * (np.abs(md) + sgmax))
+        assert np.all(np.abs(v - vd) <= 8 * K * F32_EPS * (np.abs(vd) + sgmax ** 2))
+
+
+# ---- dtypes of g and p_out -----------------------------------------------------
+
+@pytest.mark.parametrize("out_dtype", [DT_F32, DT_BF16, DT_F16])
+@pytest.mark.parametrize("g_dtype", [DT_F32, DT_BF16, DT_F16])
+def test_grad_widening_and_param_out_cast(g_dtype, out_dtype):
+    n = 4096
+    p0, g32 = _rand_problem(n, 6)
+    if g_dtype == DT_F32:
+        g, g_as_f32 = g32, g32
+    elif g_dtype == DT_BF16:
+        gt = torch.from_numpy(g32).to(torch.bfloat16)
+        g = gt.view(torch.int16).numpy().view(np.uint16)
+        g_as_f32 = gt.float().numpy()
+    else:
+        g = g32.astype(np.float16).view(np.uint16)
+        g_as_f32 = g32.astype(np.float16).astype(np.float32)
+    grp = Group(mode=MODE_ADAMW, weight_decay=0.1, lr=1e-3)
+    # the update with a low-precision grad equals the update with its exact fp32 value
+    p, m, v = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    out = np.zeros(n, np.float32 if out_dtype == DT_F32 else np.uint16)
+    oracle.adam_f32(grp, 1, p, m, v, g, g_dtype, out, out_dtype)
+    p2, m2, v2 = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    oracle.adam_f32(grp, 1, p2, m2, v2, g_as_f32, DT_F32)
+    assert np.array_equal(p, p2) and np.array_equal(m, m2) and np.array_equal(v, v2)
+    if out_dtype == DT_F32:
+        assert np.array_equal(out, p)
+    elif out_dtype == DT_BF16:
+        ref = torch.from_numpy(p.copy()).to(torch.bfloat16).view(torch.int16).numpy()
+        assert np.array_equal(out, ref.view(np.uint16))
+    else:
+        assert np.array_equal(out, p.astype(np.float16).view(np.uint16))
+
+
+def test_remainder_update_composes_pack_update_split():
+    n = 8192
+    rng = np.random.default_rng(8)
+    hi = torch.from_numpy(rng.standard_normal(n).astype(np.float32)).to(torch.bfloat16)
+    hi = hi.view(torch.int16).numpy().view(np.uint16).copy()
+    rem = rng.integers(-32768, 32768, size=n).astype(np.int16)
+    g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    grp = Group(mode=MODE_ADAMW, weight_decay=0.1, beta1=0.9, beta2=0.95, lr=1e-3)
+    m, v = np.zeros(n, np.float32), np.zeros(n, np.float32)
+    out = np.zeros(n, np.uint16)
+    r2 = rem.copy()
+    oracle.adam_rem(grp, 1, hi, r2, m, v, g, DT_F32, out)
+    master = oracle.rem_pack(hi, rem).view(np.float32).copy()
+    m3, v3 = np.zeros(n, np.float32), np.zeros(n, np.float32)
+    oracle.adam_f32(grp, 1, master, m3, v3, g, DT_F32)
+    h3, r3 = oracle.rem_split(master.view(np.uint32))
+    assert np.array_equal(out, h3) and np.array_equal(r2, r3)
+    assert np.array_equal(m, m3) and np.array_equal(v, v3)
+
+
+# ---- inf/nan screen ------------------------------------------------------------
+
+def test_nonfinite_screen_special_cases():
+    f = np.ones(100, np.float32)
+    assert not oracle.any_nonfinite(f, DT_F32, 1.0)
+    for bad in (np.inf, -np.inf, np.nan):
+        h = f.copy()
+        h[57] = bad
+        assert oracle.any_nonfinite(h, DT_F32, 1.0)
+    big = f.copy()
+    big[3] = 3e38
+    assert not oracle.any_nonfinite(big, DT_F32, 1.0)
+    assert oracle.any_nonfinite(big, DT_F32, 10.0)  # overflows once scaled
+    bf = np.full(10, 0x3F80, np.uint16)
+    assert not oracle.any_nonfinite(bf, DT_BF16, 1.0)
+    bf[9] = 0x7F80
+    assert oracle.any_nonfinite(bf, DT_BF16, 1.0)
+    h16 = np.full(10, 0x7BFF, np.uint16)  # 65504, the largest fp16
+    assert not oracle.any_nonfinite(h16, DT_F16, 1.0)
+    h16[0] = 0x7C00
+    assert oracle.any_nonfinite(h16, DT_F16, 1.0)
+    assert not oracle.any_nonfinite(np.zeros(0, np.float32), DT_F32, 1.0)
+
+
+# ---- shard step: noop and step counters ----------------------------------------
+
+def _small_shard(seed=9, with_empty=True, shared=False):
+    rng = np.random.default_rng(seed)
+    groups = [Group(mode=MODE_ADAMW, weight_decay=0.01), Group(mode=MODE_L2, weight_decay=0.0)]
+    if with_empty:
+        groups.append(Group(mode=MODE_ADAMW))
+    tensors = []
+    for i, n in enumerate([1000, 4097, 3]):
+        tensors.append(oracle.Tensor(group=i % 2, p=rng.standard_normal(n).astype(np.float32),
+                                     m=np.zeros(n, np.float32), v=np.zeros(n, np.float32),
+                                     g=(rng.standard_normal(n) * 1e-3).astype(np.float32)))
+    slot = [0] * len(groups) if shared else []
+    return oracle.Shard(groups=groups, tensors=tensors, step_slot=slot)
+
+
+def _snapshot(shard):
+    return [(t.p.copy(), t.m.copy(), t.v.copy()) for t in shard.tensors], list(shard.steps)
+
+
+@pytest.mark.parametrize("capturable", [False, True])
+def test_noop_leaves_everything_bit_identical(capturable):
+    sh = _small_shard()
+    oracle.shard_step(sh, capturable=capturable)
+    before, steps = _snapshot(sh)
+    assert oracle.shard_step(sh, capturable=capturable, noop=True) is True
+    after, steps2 = _snapshot(sh)
+    assert steps == steps2
+    for a, b in zip(before, after):
+        for x, y in zip(a, b):
+            assert x.tobytes() == y.tobytes()
+
+
+def test_nonfinite_grad_sets_noop_before_any_update():
+    sh = _small_shard()
+    oracle.shard_step(sh, capturable=True)
+    sh.tensors[2].g[1] = np.inf  # the last tensor: a late screen would be too late
+    before, steps = _snapshot(sh)
+    assert oracle.shard_step(sh, capturable=True, check_finite=True) is True
+    after, steps2 = _snapshot(sh)
+    assert steps == steps2 == [1, 1, 1]
+    for a, b in zip(before, after):
+        for x, y in zip(a, b):
+            assert x.tobytes() == y.tobytes()
+
+
+def _golden_empty_group():
+    with open(os.path.join(GOLDEN, "empty_group_steps.txt")) as fh:
+        rows = [ln.split() for ln in fh if ln.strip() and not ln.startswith("#")]
+    return {r[0]: (r[1], r[2]) for r in rows}
+
+
+@pytest.mark.parametrize("capturable", [False, True])
+def test_empty_group_advances_like_the_fixed_loop(capturable):
+    want_groups, want_state = _golden_empty_group()["fixed"]
+    rng = np.random.default_rng(0)
+    t = oracle.Tensor(group=0, p=rng.standard_normal(4).astype(np.float32),
+                      m=np.zeros(4, np.float32), v=np.zeros(4, np.float32),
+                      g=np.ones(4, np.float32))
+    sh = oracle.Shard(groups=[Group(), Group()], tensors=[t])
+    for _ in range(3):
+        oracle.shard_step(sh, capturable=capturable)
+    got = ",".join(str(s) for s in oracle.group_steps(sh))
+    assert got == want_groups == want_state
+
+
+def test_capturable_steps_count_only_applied_steps():
+    sh = _small_shard()
+    for k in range(5):
+        oracle.shard_step(sh, capturable=True, noop=(k == 2))
+    assert oracle.group_steps(sh) == [4, 4, 4]
+
+
+def test_shared_step_counter_advances_once_per_step():
+    sh = _small_shard(shared=True)
+    for _ in range(3):
+        oracle.shard_step(sh, capturable=True)
+    assert sh.steps == [3] and oracle.group_steps(sh) == [3, 3, 3]
+
+
+def test_preadvanced_counter_is_used_as_is():
+    a, b = _small_shard(), _small_shard()
+    b.steps = [1, 1, 1]
+    oracle.shard_step(a, capturable=True)
+    oracle.shard_step(b, capturable=True, step_preadvanced=True)
+    assert a.steps == b.steps == [1, 1, 1]
+    for ta, tb in zip(a.tensors, b.tensors):
+        assert ta.p.tobytes() == tb.p.tobytes()
