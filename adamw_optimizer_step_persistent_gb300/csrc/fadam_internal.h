@@ -1,0 +1,88 @@
+// Internal layout shared by the host planner (fadam_plan.cu) and the kernel
+// translation units (fadam_kernels_g*.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fadam.h"
+
+namespace fadam {
+
+// Threads per CTA of the update kernel.
+constexpr int kBlock = 256;
+// Elements per vector access (one 16-byte fp32 vector).
+constexpr int kVec = 4;
+// Largest work item, in elements (keeps in-item indices in 32 bits).
+constexpr int64_t kMaxItem = int64_t(1) << 26;
+// Work items are cut at multiples of this many elements.
+constexpr int64_t kCutQuantum = 32;
+
+// Item flags.
+constexpr uint16_t kItemVec = 1;  // every stream is vector-aligned at the item start
+
+// One contiguous run of one tensor: pointers already offset to the run start.
+struct alignas(16) Item {
+  void* p;
+  void* m;
+  void* v;
+  const void* g;
+  void* p_out;
+  int16_t* rem;
+  int32_t n;        // elements in the run
+  uint16_t group;   // param group
+  uint16_t flags;   // kItemVec
+};
+static_assert(sizeof(Item) == 64, "Item is one 64-byte record");
+
+// Group bits.
+constexpr uint32_t kGroupAdamW = 1;      // decoupled weight decay
+constexpr uint32_t kGroupBiasCorr = 2;   // bias correction on
+constexpr uint32_t kGroupOwnsStep = 4;   // advances *step_dev (first user of the pointer)
+
+// One param group as the kernel sees it (passed by value).
+struct alignas(16) KGroup {
+  float beta1, beta2, eps, wd;
+  float lr, grad_scale;   // regular plans
+  int32_t step;           // regular plans: the step of this update
+  uint32_t bits;          // kGroup*
+  const float* lr_dev;    // capturable plans
+  const float* gs_dev;
+  int32_t* step_dev;
+  int64_t reserved;
+};
+static_assert(sizeof(KGroup) == 64, "KGroup is one 64-byte record");
+
+// Per-plan device status block.
+struct KScratch {
+  unsigned int done;       // CTAs finished in the current launch (last one resets)
+  unsigned int bar_count;  // grid barrier arrivals
+  unsigned int bar_gen;    // grid barrier generation
+  int status;              // FADAM_OK or FADAM_ETIMEOUT
+};
+
+// Kernel flags.
+constexpr uint32_t kCapturable = FADAM_CAPTURABLE;
+constexpr uint32_t kCheckFinite = FADAM_CHECK_FINITE;
+constexpr uint32_t kPreadvanced = FADAM_STEP_PREADVANCED;
+
+// Everything one launch needs, passed as a __grid_constant__ parameter.
+struct alignas(16) KParams {
+  const Item* items;
+  const int32_t* cta_begin;  // grid+1 entries: CTA b runs items [cta_begin[b], cta_begin[b+1])
+  int32_t* noop;             // may be null
+  KScratch* scratch;
+  int32_t n_groups;
+  uint32_t flags;
+  int64_t reserved;
+  KGroup groups[FADAM_MAX_GROUPS];
+};
+
+// Kernel entry for the (g dtype, out dtype, remainders) combination, or
+// null when the combination does not exist.  Defined per g dtype in
+// fadam_kernels_g{f32,bf16,f16}.cu.
+const void* kernel_gf32(int out_dtype, bool remainders);
+const void* kernel_gbf16(int out_dtype, bool remainders);
+const void* kernel_gf16(int out_dtype, bool remainders);
+
+}  // namespace fadam

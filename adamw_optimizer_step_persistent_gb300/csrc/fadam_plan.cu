@@ -1,0 +1,727 @@
+// Host side of the C ABI: argument checks, the tensor-list packer that
+// builds the persistent grid's balanced work list, plan lifecycle and the
+// launches.  Every check runs before the first CUDA call, so a rejected call
+// launches nothing.
+//
+// The packer replaces the fixed-size chunk table of the page's
+// multi_tensor_apply (one CTA per chunk, several launches when the table is
+// full; "Enhance Distributed Fused Adam (#1794)", operator() reading
+// block_to_tensor / block_to_chunk) with one launch whose CTAs each take a
+// contiguous, equal-cost slice of the concatenated shard.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "fadam.h"
+#include "fadam_internal.h"
+
+using namespace fadam;
+
+namespace {
+
+// Bytes of work that justify one more CTA for small shards.
+constexpr double kMinCtaCost = 64.0 * 1024.0;
+// Fixed cost of one work item, in byte-equivalents (descriptor fetch, tail).
+constexpr double kItemOverhead = 4096.0;
+// Largest tensor the library accepts, in elements.
+constexpr int64_t kMaxNumel = int64_t(1) << 40;
+
+thread_local std::string t_last_error;
+
+fadam_status fail(fadam_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+fadam_status cuda_fail(cudaError_t e, const char* what) {
+  t_last_error = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  (void)cudaGetLastError();  // clear a non-sticky error so later calls start clean
+  return FADAM_ECUDA;
+}
+
+int elem_size(int32_t dt) {
+  switch (dt) {
+    case FADAM_DT_F32: return 4;
+    case FADAM_DT_BF16:
+    case FADAM_DT_F16: return 2;
+    default: return 0;
+  }
+}
+
+bool finite(float x) { return std::isfinite(x); }
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+  int prev = -1;
+  int want;
+  cudaError_t err = cudaSuccess;
+  explicit DeviceGuard(int dev) : want(dev) {
+    err = cudaGetDevice(&prev);
+    if (err == cudaSuccess && prev != want) err = cudaSetDevice(want);
+  }
+  ~DeviceGuard() {
+    if (prev >= 0 && prev != want) cudaSetDevice(prev);
+  }
+};
+
+struct Dtypes {
+  int32_t p, g, out;
+  bool rem;
+};
+
+fadam_status check_dtypes(const Dtypes& d, uint32_t flags) {
+  const uint32_t known = FADAM_CAPTURABLE | FADAM_REMAINDERS | FADAM_CHECK_FINITE |
+                         FADAM_STEP_PREADVANCED;
+  if (flags & ~known) return fail(FADAM_EINVAL, "unknown flag bits 0x%x", flags & ~known);
+  if ((flags & FADAM_STEP_PREADVANCED) && !(flags & FADAM_CAPTURABLE))
+    return fail(FADAM_EINVAL, "FADAM_STEP_PREADVANCED needs FADAM_CAPTURABLE");
+  if (d.g != FADAM_DT_F32 && d.g != FADAM_DT_BF16 && d.g != FADAM_DT_F16)
+    return fail(FADAM_EDTYPE, "g dtype %d is not fp32, bf16 or fp16", d.g);
+  if (d.out != FADAM_DT_NONE && elem_size(d.out) == 0)
+    return fail(FADAM_EDTYPE, "param-out dtype %d is not none, fp32, bf16 or fp16", d.out);
+  if (d.rem) {
+    if (d.p != FADAM_DT_BF16)
+      return fail(FADAM_EDTYPE, "remainder mode needs bf16 params (p dtype %d)", d.p);
+    if (d.out != FADAM_DT_BF16)
+      return fail(FADAM_EDTYPE, "remainder mode writes a bf16 param-out (out dtype %d)", d.out);
+  } else if (d.p != FADAM_DT_F32) {
+    return fail(FADAM_EDTYPE, "p dtype %d needs FADAM_REMAINDERS (only fp32 otherwise)", d.p);
+  }
+  return FADAM_OK;
+}
+
+fadam_status check_groups(const fadam_group* groups, int32_t n_groups, uint32_t flags,
+                          const std::vector<char>& has_tensor) {
+  if (n_groups < 1 || n_groups > FADAM_MAX_GROUPS)
+    return fail(FADAM_EINVAL, "n_groups %d outside 1..%d", n_groups, FADAM_MAX_GROUPS);
+  if (!groups) return fail(FADAM_EINVAL, "groups is NULL");
+  const bool capt = flags & FADAM_CAPTURABLE;
+  for (int32_t i = 0; i < n_groups; ++i) {
+    const fadam_group& g = groups[i];
+    if (g.mode != FADAM_MODE_L2 && g.mode != FADAM_MODE_ADAMW)
+      return fail(FADAM_EINVAL, "group %d: mode %d is neither L2 (0) nor AdamW (1)", i, g.mode);
+    if (g.bias_correction != 0 && g.bias_correction != 1)
+      return fail(FADAM_EINVAL, "group %d: bias_correction %d is not 0 or 1", i, g.bias_correction);
+    if (!(g.beta1 >= 0.0f && g.beta1 < 1.0f) || !(g.beta2 >= 0.0f && g.beta2 < 1.0f))
+      return fail(FADAM_EINVAL, "group %d: betas (%g, %g) outside [0, 1)", i, g.beta1, g.beta2);
+    if (!(g.eps >= 0.0f) || !finite(g.eps))
+      return fail(FADAM_EINVAL, "group %d: eps %g is not finite and >= 0", i, g.eps);
+    if (!finite(g.weight_decay))
+      return fail(FADAM_EINVAL, "group %d: weight_decay is not finite", i);
+    if (capt) {
+      if (!g.step_dev) return fail(FADAM_EINVAL, "group %d: capturable plan without step_dev", i);
+      if (reinterpret_cast<uintptr_t>(g.step_dev) % 4)
+        return fail(FADAM_EALIGN, "group %d: step_dev is not 4-byte aligned", i);
+      if (has_tensor[i] && (!g.lr_dev || !g.grad_scale_dev))
+        return fail(FADAM_EINVAL, "group %d: capturable plan needs lr_dev and grad_scale_dev", i);
+      if ((g.lr_dev && reinterpret_cast<uintptr_t>(g.lr_dev) % 4) ||
+          (g.grad_scale_dev && reinterpret_cast<uintptr_t>(g.grad_scale_dev) % 4))
+        return fail(FADAM_EALIGN, "group %d: lr_dev / grad_scale_dev not 4-byte aligned", i);
+    } else {
+      if (!finite(g.lr) || !finite(g.grad_scale))
+        return fail(FADAM_EINVAL, "group %d: lr or grad_scale is not finite", i);
+      if (g.bias_correction == 1 && g.step < 1)
+        return fail(FADAM_EINVAL, "group %d: step %d < 1 with bias correction (1-beta^step = 0)",
+                    i, g.step);
+    }
+  }
+  return FADAM_OK;
+}
+
+bool misaligned(const void* ptr, int esz) {
+  return reinterpret_cast<uintptr_t>(ptr) % static_cast<uintptr_t>(esz) != 0;
+}
+
+fadam_status check_tensors(const fadam_tensor* ts, int64_t n, int32_t n_groups, const Dtypes& d,
+                           std::vector<char>& has_tensor) {
+  if (n < 0) return fail(FADAM_EINVAL, "n_tensors %lld < 0", (long long)n);
+  if (n > 0 && !ts) return fail(FADAM_EINVAL, "tensors is NULL");
+  if (n > (int64_t(1) << 31)) return fail(FADAM_ELIMIT, "n_tensors %lld > 2^31", (long long)n);
+  const int psz = elem_size(d.p), gsz = elem_size(d.g), osz = elem_size(d.out);
+  for (int64_t i = 0; i < n; ++i) {
+    const fadam_tensor& t = ts[i];
+    if (t.group < 0 || t.group >= n_groups)
+      return fail(FADAM_EINVAL, "tensor %lld: group %d outside 0..%d", (long long)i, t.group,
+                  n_groups - 1);
+    if (t.numel < 0) return fail(FADAM_EINVAL, "tensor %lld: numel < 0", (long long)i);
+    if (t.numel > kMaxNumel)
+      return fail(FADAM_ELIMIT, "tensor %lld: numel %lld > 2^40", (long long)i, (long long)t.numel);
+    if (t.numel == 0) continue;
+    has_tensor[t.group] = 1;
+    if (!t.p || !t.m || !t.v || !t.g)
+      return fail(FADAM_EINVAL, "tensor %lld: p, m, v and g must be non-NULL", (long long)i);
+    if (d.out == FADAM_DT_NONE ? t.p_out != nullptr : t.p_out == nullptr)
+      return fail(FADAM_EINVAL, "tensor %lld: p_out must be %s for param-out dtype %d",
+                  (long long)i, d.out == FADAM_DT_NONE ? "NULL" : "non-NULL", d.out);
+    if (d.rem ? t.rem == nullptr : t.rem != nullptr)
+      return fail(FADAM_EINVAL, "tensor %lld: rem must be %s", (long long)i,
+                  d.rem ? "non-NULL in remainder mode" : "NULL outside remainder mode");
+    if (misaligned(t.p, psz) || misaligned(t.m, 4) || misaligned(t.v, 4) || misaligned(t.g, gsz) ||
+        (t.p_out && misaligned(t.p_out, osz)) || (t.rem && misaligned(t.rem, 2)))
+      return fail(FADAM_EALIGN, "tensor %lld: a pointer is not aligned to its element size",
+                  (long long)i);
+  }
+  return FADAM_OK;
+}
+
+// Algorithmic bytes per element: every stream read or written once.
+double bytes_per_elem(const Dtypes& d) {
+  const int gsz = elem_size(d.g);
+  if (d.rem) return 2 + 2 + 2 + 2 + 8 + 8 + gsz;  // p_hi R, p_out W, rem R+W, m, v, g
+  return 8 + 8 + 8 + gsz + elem_size(d.out);       // p, m, v R+W, g R, p_out W
+}
+
+struct PackItem {
+  int64_t tensor;
+  int64_t offset;
+  int64_t n;
+  bool vec;
+};
+
+struct Piece {
+  int64_t tensor, offset, n;
+  bool vec;
+};
+
+// Elements to skip at the start of a tensor so that every stream is
+// vector-aligned (all streams must agree), or -1 when they cannot agree.
+int64_t vector_head(const fadam_tensor& t, const Dtypes& d) {
+  const void* ptrs[6] = {t.p, t.m, t.v, t.g, t.p_out, t.rem};
+  const int esz[6] = {elem_size(d.p), 4, 4, elem_size(d.g), elem_size(d.out), 2};
+  int64_t r = -1;
+  for (int s = 0; s < 6; ++s) {
+    if (!ptrs[s] || esz[s] == 0) continue;
+    const int64_t rs = static_cast<int64_t>((reinterpret_cast<uintptr_t>(ptrs[s]) / esz[s]) % kVec);
+    if (r < 0) r = rs;
+    else if (r != rs) return -1;
+  }
+  return r < 0 ? 0 : (kVec - r) % kVec;
+}
+
+// Split the shard into pieces (aligned bodies, scalar heads) and cut them
+// into items so that CTA b's items cost about total/grid each.
+void pack(const fadam_tensor* ts, int64_t n, const Dtypes& d, int grid,
+          std::vector<PackItem>& items, std::vector<int32_t>& cta_begin) {
+  std::vector<Piece> pieces;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t len = ts[i].numel;
+    if (len <= 0) continue;
+    const int64_t h = vector_head(ts[i], d);
+    if (h < 0) {
+      pieces.push_back({i, 0, len, false});
+      continue;
+    }
+    if (h > 0) pieces.push_back({i, 0, std::min(h, len), false});
+    if (len > h) pieces.push_back({i, h, len - h, true});
+  }
+  const double bpe = bytes_per_elem(d);
+  double total = 0;
+  for (const Piece& p : pieces) total += p.n * bpe + kItemOverhead;
+  const double quota = total / grid;
+
+  items.clear();
+  cta_begin.assign(grid + 1, 0);
+  int b = 1;
+  double acc = 0;
+  for (const Piece& pc : pieces) {
+    int64_t off = pc.offset, left = pc.n;
+    while (left > 0) {
+      int64_t take = std::min(left, kMaxItem);
+      if (b < grid) {
+        const double room = quota * b - acc;
+        if (take * bpe + kItemOverhead > room) {
+          int64_t k = static_cast<int64_t>((room - kItemOverhead) / bpe);
+          k = k / kCutQuantum * kCutQuantum;
+          if (k <= 0) {  // nothing more fits in this CTA: close it
+            cta_begin[b++] = static_cast<int32_t>(items.size());
+            continue;
+          }
+          take = std::min(take, k);
+        }
+      }
+      items.push_back({pc.tensor, off, take, pc.vec});
+      acc += take * bpe + kItemOverhead;
+      off += take;
+      left -= take;
+      while (b < grid && acc >= quota * b) cta_begin[b++] = static_cast<int32_t>(items.size());
+    }
+  }
+  while (b <= grid) cta_begin[b++] = static_cast<int32_t>(items.size());
+  cta_begin[grid] = static_cast<int32_t>(items.size());
+}
+
+int choose_grid(double total_cost, int grid_max) {
+  const double want = std::ceil(total_cost / kMinCtaCost);
+  return static_cast<int>(std::max(1.0, std::min(want, static_cast<double>(grid_max))));
+}
+
+double total_cost(const fadam_tensor* ts, int64_t n, const Dtypes& d) {
+  double c = 0;
+  const double bpe = bytes_per_elem(d);
+  for (int64_t i = 0; i < n; ++i)
+    if (ts[i].numel > 0) c += ts[i].numel * bpe + kItemOverhead;
+  return c;
+}
+
+Item to_item(const fadam_tensor& t, const PackItem& pi, const Dtypes& d) {
+  auto adv = [&](const void* ptr, int esz) -> void* {
+    return ptr ? const_cast<char*>(static_cast<const char*>(ptr)) + pi.offset * esz : nullptr;
+  };
+  Item it;
+  it.p = adv(t.p, elem_size(d.p));
+  it.m = adv(t.m, 4);
+  it.v = adv(t.v, 4);
+  it.g = adv(t.g, elem_size(d.g));
+  it.p_out = adv(t.p_out, elem_size(d.out));
+  it.rem = static_cast<int16_t*>(adv(t.rem, 2));
+  it.n = static_cast<int32_t>(pi.n);
+  it.group = static_cast<uint16_t>(t.group);
+  it.flags = pi.vec ? kItemVec : 0;
+  return it;
+}
+
+const void* select_kernel(const Dtypes& d) {
+  switch (d.g) {
+    case FADAM_DT_F32: return kernel_gf32(d.out, d.rem);
+    case FADAM_DT_BF16: return kernel_gbf16(d.out, d.rem);
+    case FADAM_DT_F16: return kernel_gf16(d.out, d.rem);
+    default: return nullptr;
+  }
+}
+
+KGroup to_kgroup(const fadam_group& g, bool owns_step) {
+  KGroup k{};
+  k.beta1 = g.beta1;
+  k.beta2 = g.beta2;
+  k.eps = g.eps;
+  k.wd = g.weight_decay;
+  k.lr = g.lr;
+  k.grad_scale = g.grad_scale;
+  k.step = g.step;
+  k.bits = (g.mode == FADAM_MODE_ADAMW ? kGroupAdamW : 0u) |
+           (g.bias_correction ? kGroupBiasCorr : 0u) | (owns_step ? kGroupOwnsStep : 0u);
+  k.lr_dev = g.lr_dev;
+  k.gs_dev = g.grad_scale_dev;
+  k.step_dev = g.step_dev;
+  return k;
+}
+
+// A group owns its step counter when no earlier group uses the same pointer.
+void fill_kgroups(const fadam_group* groups, int32_t n_groups, uint32_t flags, KGroup* out) {
+  const bool capt = flags & FADAM_CAPTURABLE;
+  for (int32_t i = 0; i < n_groups; ++i) {
+    bool owns = capt;
+    for (int32_t j = 0; j < i && owns; ++j)
+      if (groups[j].step_dev == groups[i].step_dev) owns = false;
+    out[i] = to_kgroup(groups[i], owns);
+  }
+}
+
+struct HostPlan {
+  Dtypes d;
+  uint32_t flags = 0;
+  const void* kernel = nullptr;
+  int device = 0, sm_count = 0, blocks_per_sm = 0, grid = 1;
+  std::vector<Item> items;
+  std::vector<int32_t> cta_begin;
+  int64_t n_elements = 0;
+  double bytes = 0, check_bytes = 0;
+};
+
+// Checks, device query and packing shared by fadam_plan_create and
+// fadam_step_once.  Allocates no device memory.
+fadam_status prepare(const fadam_tensor* tensors, int64_t n_tensors, const fadam_group* groups,
+                     int32_t n_groups, const Dtypes& d, uint32_t flags, HostPlan& hp) {
+  fadam_status st = check_dtypes(d, flags);
+  if (st) return st;
+  if (n_groups < 1 || n_groups > FADAM_MAX_GROUPS)
+    return fail(FADAM_EINVAL, "n_groups %d outside 1..%d", n_groups, FADAM_MAX_GROUPS);
+  std::vector<char> has_tensor(n_groups, 0);
+  st = check_tensors(tensors, n_tensors, n_groups, d, has_tensor);
+  if (st) return st;
+  st = check_groups(groups, n_groups, flags, has_tensor);
+  if (st) return st;
+
+  hp.d = d;
+  hp.flags = flags;
+  hp.kernel = select_kernel(d);
+  if (!hp.kernel) return fail(FADAM_EDTYPE, "no kernel for this dtype combination");
+  cudaError_t e = cudaGetDevice(&hp.device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  e = cudaDeviceGetAttribute(&hp.sm_count, cudaDevAttrMultiProcessorCount, hp.device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&hp.blocks_per_sm, hp.kernel, kBlock, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  if (hp.blocks_per_sm < 1) return fail(FADAM_ECUDA, "kernel cannot be resident on this device");
+
+  const double cost = total_cost(tensors, n_tensors, d);
+  hp.grid = choose_grid(cost, hp.blocks_per_sm * hp.sm_count);
+  std::vector<PackItem> pitems;
+  pack(tensors, n_tensors, d, hp.grid, pitems, hp.cta_begin);
+  if (pitems.size() > size_t(INT32_MAX))
+    return fail(FADAM_ELIMIT, "more than 2^31 work items");
+  hp.items.reserve(pitems.size());
+  for (const PackItem& pi : pitems) hp.items.push_back(to_item(tensors[pi.tensor], pi, d));
+  const double bpe = bytes_per_elem(d);
+  for (int64_t i = 0; i < n_tensors; ++i) {
+    const int64_t ne = std::max<int64_t>(tensors[i].numel, 0);
+    hp.n_elements += ne;
+    double b = ne * bpe;
+    // a param-out that aliases the fp32 master is the same stream
+    if (!d.rem && tensors[i].p_out && tensors[i].p_out == tensors[i].p) b -= ne * 4.0;
+    hp.bytes += b;
+  }
+  if (flags & FADAM_CHECK_FINITE) hp.check_bytes = hp.n_elements * double(elem_size(d.g));
+  return FADAM_OK;
+}
+
+fadam_status launch(const void* kernel, const KParams& kp, int grid, bool cooperative,
+                    cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kBlock);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (cooperative) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  void* args[1] = {const_cast<KParams*>(&kp)};
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, kernel, args);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return FADAM_OK;
+}
+
+}  // namespace
+
+struct fadam_plan {
+  HostPlan hp;
+  std::vector<fadam_tensor> tensors;
+  std::vector<fadam_group> groups;
+  std::vector<char> has_tensor;
+  int32_t n_groups = 0;
+  Item* d_items = nullptr;
+  int32_t* d_cta = nullptr;
+  KScratch* d_scratch = nullptr;
+};
+
+namespace {
+
+void free_plan_memory(fadam_plan* p) {
+  if (p->d_items) cudaFree(p->d_items);
+  if (p->d_cta) cudaFree(p->d_cta);
+  if (p->d_scratch) cudaFree(p->d_scratch);
+  p->d_items = nullptr;
+  p->d_cta = nullptr;
+  p->d_scratch = nullptr;
+}
+
+void fill_params(KParams& kp, const Item* items, const int32_t* cta, int32_t* noop,
+                 KScratch* scratch, const fadam_group* groups, int32_t n_groups, uint32_t flags) {
+  memset(&kp, 0, sizeof kp);
+  kp.items = items;
+  kp.cta_begin = cta;
+  kp.noop = noop;
+  kp.scratch = scratch;
+  kp.n_groups = n_groups;
+  kp.flags = flags;
+  fill_kgroups(groups, n_groups, flags, kp.groups);
+}
+
+bool needs_launch(const HostPlan& hp) {
+  const bool owns_steps = (hp.flags & FADAM_CAPTURABLE) && !(hp.flags & FADAM_STEP_PREADVANCED);
+  return !hp.items.empty() || owns_steps;
+}
+
+}  // namespace
+
+extern "C" {
+
+fadam_status fadam_plan_create(const fadam_tensor* tensors, int64_t n_tensors,
+                               const fadam_group* groups, int32_t n_groups, int32_t p_dtype,
+                               int32_t g_dtype, int32_t out_dtype, uint32_t flags,
+                               fadam_plan** plan_out) {
+  t_last_error.clear();
+  if (!plan_out) return fail(FADAM_EINVAL, "plan_out is NULL");
+  *plan_out = nullptr;
+  const Dtypes d{p_dtype, g_dtype, out_dtype, (flags & FADAM_REMAINDERS) != 0};
+  fadam_plan* plan = new (std::nothrow) fadam_plan();
+  if (!plan) return fail(FADAM_EINVAL, "out of host memory");
+  fadam_status st = prepare(tensors, n_tensors, groups, n_groups, d, flags, plan->hp);
+  if (st) {
+    delete plan;
+    return st;
+  }
+  plan->tensors.assign(tensors, tensors + n_tensors);
+  plan->groups.assign(groups, groups + n_groups);
+  plan->n_groups = n_groups;
+  const HostPlan& hp = plan->hp;
+  cudaError_t e = cudaSuccess;
+  if (!hp.items.empty()) {
+    e = cudaMalloc(&plan->d_items, hp.items.size() * sizeof(Item));
+    if (e == cudaSuccess)
+      e = cudaMemcpy(plan->d_items, hp.items.data(), hp.items.size() * sizeof(Item),
+                     cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess) e = cudaMalloc(&plan->d_cta, hp.cta_begin.size() * sizeof(int32_t));
+  if (e == cudaSuccess)
+    e = cudaMemcpy(plan->d_cta, hp.cta_begin.data(), hp.cta_begin.size() * sizeof(int32_t),
+                   cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMalloc(&plan->d_scratch, sizeof(KScratch));
+  if (e == cudaSuccess) e = cudaMemset(plan->d_scratch, 0, sizeof(KScratch));
+  if (e != cudaSuccess) {
+    st = cuda_fail(e, "plan upload");
+    free_plan_memory(plan);
+    delete plan;
+    return st;
+  }
+  *plan_out = plan;
+  return FADAM_OK;
+}
+
+fadam_status fadam_plan_set_groups(fadam_plan* plan, const fadam_group* groups, int32_t n_groups) {
+  t_last_error.clear();
+  if (!plan) return fail(FADAM_EINVAL, "plan is NULL");
+  if (n_groups != plan->n_groups)
+    return fail(FADAM_EINVAL, "n_groups %d differs from the plan's %d", n_groups, plan->n_groups);
+  std::vector<char> has_tensor(n_groups, 0);
+  for (const fadam_tensor& t : plan->tensors)
+    if (t.numel > 0) has_tensor[t.group] = 1;
+  const fadam_status st = check_groups(groups, n_groups, plan->hp.flags, has_tensor);
+  if (st) return st;
+  plan->groups.assign(groups, groups + n_groups);
+  return FADAM_OK;
+}
+
+fadam_status fadam_step(fadam_plan* plan, int32_t* noop_dev, fadam_stream stream) {
+  if (!plan) return fail(FADAM_EINVAL, "plan is NULL");
+  const HostPlan& hp = plan->hp;
+  if ((hp.flags & FADAM_CHECK_FINITE) && !noop_dev)
+    return fail(FADAM_EINVAL, "FADAM_CHECK_FINITE needs a noop_dev flag to write");
+  if (noop_dev && reinterpret_cast<uintptr_t>(noop_dev) % 4)
+    return fail(FADAM_EALIGN, "noop_dev is not 4-byte aligned");
+  if (!needs_launch(hp)) return FADAM_OK;
+  DeviceGuard guard(hp.device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  KParams kp;
+  fill_params(kp, plan->d_items, plan->d_cta, noop_dev, plan->d_scratch, plan->groups.data(),
+              plan->n_groups, hp.flags);
+  return launch(hp.kernel, kp, hp.grid, (hp.flags & FADAM_CHECK_FINITE) != 0,
+                reinterpret_cast<cudaStream_t>(stream));
+}
+
+fadam_status fadam_step_host_grads(fadam_plan* plan, const void* const* g_host, int32_t* noop_dev,
+                                   int32_t* steps_host, fadam_stream stream) {
+  if (!plan) return fail(FADAM_EINVAL, "plan is NULL");
+  const HostPlan& hp = plan->hp;
+  const int gsz = elem_size(hp.d.g);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  bool any = false;
+  for (const fadam_tensor& t : plan->tensors) any |= t.numel > 0;
+  if (any && !g_host) return fail(FADAM_EINVAL, "g_host is NULL");
+  for (size_t i = 0; i < plan->tensors.size(); ++i)
+    if (plan->tensors[i].numel > 0 && !g_host[i])
+      return fail(FADAM_EINVAL, "g_host[%zu] is NULL", i);
+  DeviceGuard guard(hp.device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  for (size_t i = 0; i < plan->tensors.size(); ++i) {
+    const fadam_tensor& t = plan->tensors[i];
+    if (t.numel <= 0) continue;
+    const cudaError_t e = cudaMemcpyAsync(const_cast<void*>(t.g), g_host[i], size_t(t.numel) * gsz,
+                                          cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gradient upload");
+  }
+  fadam_status st = fadam_step(plan, noop_dev, stream);
+  if (st) return st;
+  if (steps_host) {
+    for (int32_t g = 0; g < plan->n_groups; ++g) {
+      const fadam_group& gr = plan->groups[g];
+      if (hp.flags & FADAM_CAPTURABLE) {
+        const cudaError_t e =
+            cudaMemcpyAsync(&steps_host[g], gr.step_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return cuda_fail(e, "step counter read");
+      } else {
+        steps_host[g] = gr.step;
+      }
+    }
+  }
+  const cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  return FADAM_OK;
+}
+
+fadam_status fadam_plan_status(fadam_plan* plan, int32_t* device_status) {
+  if (!plan || !device_status) return fail(FADAM_EINVAL, "plan or device_status is NULL");
+  DeviceGuard guard(plan->hp.device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  KScratch sc;
+  cudaError_t e = cudaMemcpy(&sc, plan->d_scratch, sizeof sc, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  *device_status = sc.status;
+  if (sc.status != FADAM_OK || sc.bar_count != 0 || sc.done != 0) {
+    e = cudaMemset(plan->d_scratch, 0, sizeof(KScratch));
+    if (e != cudaSuccess) return cuda_fail(e, "status reset");
+  }
+  return FADAM_OK;
+}
+
+fadam_status fadam_plan_get_info(const fadam_plan* plan, fadam_plan_info* info) {
+  if (!plan || !info) return fail(FADAM_EINVAL, "plan or info is NULL");
+  const HostPlan& hp = plan->hp;
+  memset(info, 0, sizeof *info);
+  info->n_tensors = static_cast<int64_t>(plan->tensors.size());
+  info->n_elements = hp.n_elements;
+  info->n_items = static_cast<int64_t>(hp.items.size());
+  info->grid = hp.grid;
+  info->block = kBlock;
+  info->blocks_per_sm = hp.blocks_per_sm;
+  info->sm_count = hp.sm_count;
+  info->n_groups = plan->n_groups;
+  info->device = hp.device;
+  info->bytes_per_step = hp.bytes;
+  info->check_bytes_per_step = hp.check_bytes;
+  return FADAM_OK;
+}
+
+fadam_status fadam_plan_destroy(fadam_plan* plan) {
+  if (!plan) return FADAM_OK;
+  {
+    DeviceGuard guard(plan->hp.device);
+    free_plan_memory(plan);
+  }
+  delete plan;
+  return FADAM_OK;
+}
+
+fadam_status fadam_step_once(const fadam_tensor* tensors, int64_t n_tensors, int32_t mode,
+                             int32_t bias_correction, float beta1, float beta2, float eps,
+                             float weight_decay, float lr, const float* lr_dev, int32_t step,
+                             int32_t* step_dev, float grad_scale, const float* grad_scale_dev,
+                             int32_t* noop_dev, int32_t g_dtype, int32_t out_dtype,
+                             fadam_stream stream) {
+  t_last_error.clear();
+  const int n_dev = (lr_dev != nullptr) + (step_dev != nullptr) + (grad_scale_dev != nullptr);
+  if (n_dev != 0 && n_dev != 3)
+    return fail(FADAM_EINVAL, "give all of lr_dev, step_dev, grad_scale_dev or none");
+  const uint32_t flags = n_dev == 3 ? FADAM_CAPTURABLE : 0u;
+  fadam_group grp{};
+  grp.mode = mode;
+  grp.bias_correction = bias_correction;
+  grp.beta1 = beta1;
+  grp.beta2 = beta2;
+  grp.eps = eps;
+  grp.weight_decay = weight_decay;
+  grp.lr = lr;
+  grp.grad_scale = grad_scale;
+  grp.step = step;
+  grp.lr_dev = lr_dev;
+  grp.grad_scale_dev = grad_scale_dev;
+  grp.step_dev = step_dev;
+  for (int64_t i = 0; i < n_tensors && tensors; ++i)
+    if (tensors[i].group != 0) return fail(FADAM_EINVAL, "one-shot tensors must all be group 0");
+  if (noop_dev && reinterpret_cast<uintptr_t>(noop_dev) % 4)
+    return fail(FADAM_EALIGN, "noop_dev is not 4-byte aligned");
+  HostPlan hp;
+  const Dtypes d{FADAM_DT_F32, g_dtype, out_dtype, false};
+  fadam_status st = prepare(tensors, n_tensors, &grp, 1, d, flags, hp);
+  if (st) return st;
+  if (!needs_launch(hp)) return FADAM_OK;
+  DeviceGuard guard(hp.device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Item* d_items = nullptr;
+  int32_t* d_cta = nullptr;
+  KScratch* d_scratch = nullptr;
+  cudaError_t e = cudaSuccess;
+  if (!hp.items.empty()) {
+    e = cudaMallocAsync(&d_items, hp.items.size() * sizeof(Item), s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(d_items, hp.items.data(), hp.items.size() * sizeof(Item),
+                          cudaMemcpyHostToDevice, s);
+  }
+  if (e == cudaSuccess) e = cudaMallocAsync(&d_cta, hp.cta_begin.size() * sizeof(int32_t), s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(d_cta, hp.cta_begin.data(), hp.cta_begin.size() * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMallocAsync(&d_scratch, sizeof(KScratch), s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(d_scratch, 0, sizeof(KScratch), s);
+  if (e == cudaSuccess) {
+    KParams kp;
+    fill_params(kp, d_items, d_cta, noop_dev, d_scratch, &grp, 1, flags);
+    st = launch(hp.kernel, kp, hp.grid, false, s);
+  } else {
+    st = cuda_fail(e, "one-shot upload");
+  }
+  if (d_items) cudaFreeAsync(d_items, s);
+  if (d_cta) cudaFreeAsync(d_cta, s);
+  if (d_scratch) cudaFreeAsync(d_scratch, s);
+  return st;
+}
+
+fadam_status fadam_pack_dry(const fadam_tensor* tensors, int64_t n_tensors, int32_t n_groups,
+                            int32_t p_dtype, int32_t g_dtype, int32_t out_dtype, uint32_t flags,
+                            int32_t grid, fadam_pack_item* items_out, int64_t max_items,
+                            int32_t* cta_begin_out, int64_t* n_items_out) {
+  t_last_error.clear();
+  const Dtypes d{p_dtype, g_dtype, out_dtype, (flags & FADAM_REMAINDERS) != 0};
+  fadam_status st = check_dtypes(d, flags);
+  if (st) return st;
+  if (n_groups < 1 || n_groups > FADAM_MAX_GROUPS)
+    return fail(FADAM_EINVAL, "n_groups %d outside 1..%d", n_groups, FADAM_MAX_GROUPS);
+  std::vector<char> has_tensor(n_groups, 0);
+  st = check_tensors(tensors, n_tensors, n_groups, d, has_tensor);
+  if (st) return st;
+  if (grid < 1) return fail(FADAM_EINVAL, "grid %d < 1", grid);
+  if (!n_items_out) return fail(FADAM_EINVAL, "n_items_out is NULL");
+  std::vector<PackItem> items;
+  std::vector<int32_t> cta;
+  pack(tensors, n_tensors, d, grid, items, cta);
+  *n_items_out = static_cast<int64_t>(items.size());
+  if (cta_begin_out) memcpy(cta_begin_out, cta.data(), cta.size() * sizeof(int32_t));
+  if (items_out) {
+    if (static_cast<int64_t>(items.size()) > max_items)
+      return fail(FADAM_ELIMIT, "%zu items do not fit in max_items %lld", items.size(),
+                  (long long)max_items);
+    for (size_t i = 0; i < items.size(); ++i) {
+      items_out[i].tensor = items[i].tensor;
+      items_out[i].offset = items[i].offset;
+      items_out[i].n = static_cast<int32_t>(items[i].n);
+      items_out[i].vec = items[i].vec ? 1 : 0;
+    }
+  }
+  return FADAM_OK;
+}
+
+const char* fadam_status_string(fadam_status status) {
+  switch (status) {
+    case FADAM_OK: return "ok";
+    case FADAM_EINVAL: return "invalid argument";
+    case FADAM_EDTYPE: return "unsupported dtype combination";
+    case FADAM_EALIGN: return "misaligned pointer";
+    case FADAM_ECUDA: return "CUDA runtime error";
+    case FADAM_ETIMEOUT: return "device-side wait timed out";
+    case FADAM_ELIMIT: return "size beyond a documented maximum";
+    default: return "unknown status";
+  }
+}
+
+const char* fadam_last_error(void) { return t_last_error.c_str(); }
+
+int32_t fadam_version(void) { return 10000; }
+
+}  // extern "C"

@@ -1,0 +1,253 @@
+"""Python face of the library: a shard optimizer over the C ABI.
+
+``FusedAdamShard`` holds one data-parallel rank's optimizer shard as lists
+of tensors per param group (the lists p, m, v, g, p_out of
+distributed_fused_adam.py's ``_local_step``), builds one plan for all of
+them and runs each step as a single persistent-grid launch.  It only
+marshals pointers and scalars; PyTorch supplies device memory and streams.
+
+Step counters ("[PyTorch] Advance FusedAdam step counter for empty param
+groups"): every group, empty or not, has one and it advances every applied
+step.  Regular shards keep them on the host and advance them before the
+launch, as ``step()`` of distributed_fused_adam.py does; capturable shards
+keep int32 device counters that the kernel advances by (noop != 1), so a
+captured step replays correctly.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Dict, List, Optional, Sequence
+
+import torch
+
+from . import _abi
+
+_DT = {torch.float32: _abi.DT_F32, torch.bfloat16: _abi.DT_BF16, torch.float16: _abi.DT_F16}
+
+
+def dtype_code(dt: Optional[torch.dtype]) -> int:
+    if dt is None:
+        return _abi.DT_NONE
+    if dt not in _DT:
+        raise TypeError(f"unsupported dtype {dt}")
+    return _DT[dt]
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+class FusedAdamShard:
+    """Fused Adam/AdamW over one shard: one kernel launch per step.
+
+    ``param_groups`` is a list of dicts with keys
+      params, exp_avgs, exp_avg_sqs, grads      lists of equal length
+      params_out (optional), remainders (remainder mode only)
+      lr, betas, eps, weight_decay, bias_correction, adam_w_mode
+    A group with empty lists is allowed; its step counter still advances.
+    ``params`` are fp32 masters, or in remainder mode the bf16 high halves
+    (``remainders`` then holds the int16 low halves and ``params_out`` the
+    bf16 tensors that receive the new high halves; they may be ``params``).
+    """
+
+    def __init__(self, param_groups: Sequence[Dict], *, capturable: bool = False,
+                 check_finite: bool = False, remainders: bool = False,
+                 shared_step: bool = False, step_preadvanced: bool = False,
+                 grad_scale: float = 1.0, device=None):
+        if check_finite and not capturable:
+            raise ValueError("check_finite needs capturable=True (the counters live on the device)")
+        self.capturable = capturable
+        self.device = torch.device(device) if device is not None else torch.device(
+            "cuda", torch.cuda.current_device())
+        self.groups = [dict(g) for g in param_groups]
+        if not 1 <= len(self.groups) <= _abi.MAX_GROUPS:
+            raise ValueError(f"1..{_abi.MAX_GROUPS} param groups supported")
+        self._keep: List[torch.Tensor] = []  # tensors the plan points into
+        flags = (_abi.CAPTURABLE if capturable else 0) | (_abi.REMAINDERS if remainders else 0)
+        flags |= (_abi.CHECK_FINITE if check_finite else 0)
+        flags |= (_abi.STEP_PREADVANCED if step_preadvanced else 0)
+        self.flags = flags
+
+        descs = []
+        g_dtype = out_dtype = None
+        p_dtype = torch.bfloat16 if remainders else torch.float32
+        for gi, g in enumerate(self.groups):
+            ps, ms, vs, gs = g["params"], g["exp_avgs"], g["exp_avg_sqs"], g["grads"]
+            outs = g.get("params_out") or [None] * len(ps)
+            rems = g.get("remainders") or [None] * len(ps)
+            if not (len(ps) == len(ms) == len(vs) == len(gs) == len(outs) == len(rems)):
+                raise ValueError(f"group {gi}: tensor lists differ in length")
+            for p, m, v, gr, o, r in zip(ps, ms, vs, gs, outs, rems):
+                for t in (p, m, v, gr, o, r):
+                    if t is not None and (not t.is_contiguous() or t.device != self.device):
+                        raise ValueError("tensors must be contiguous and on the shard's device")
+                if p.dtype != p_dtype or m.dtype != torch.float32 or v.dtype != torch.float32:
+                    raise TypeError(f"group {gi}: p must be {p_dtype}, m and v fp32")
+                g_dtype = g_dtype or gr.dtype
+                if gr.dtype != g_dtype:
+                    raise TypeError("every grad must have the same dtype")
+                if o is not None:
+                    out_dtype = out_dtype or o.dtype
+                    if o.dtype != out_dtype:
+                        raise TypeError("every param-out tensor must have the same dtype")
+                if not (p.numel() == m.numel() == v.numel() == gr.numel()):
+                    raise ValueError("p, m, v, g sizes differ")
+                descs.append(_abi.Tensor(p=_ptr(p), m=_ptr(m), v=_ptr(v), g=_ptr(gr),
+                                         p_out=_ptr(o), rem=_ptr(r), numel=p.numel(), group=gi))
+                self._keep += [t for t in (p, m, v, gr, o, r) if t is not None]
+        self.n_tensors = len(descs)
+        self.g_dtype = g_dtype or torch.float32
+        self.out_dtype = out_dtype
+
+        n = len(self.groups)
+        self.host_steps = [0] * n
+        self.host_lr = [float(g.get("lr", 1e-3)) for g in self.groups]
+        self.host_grad_scale = float(grad_scale)
+        if capturable:
+            dev = self.device
+            self.lr_dev = [torch.tensor([lr], dtype=torch.float32, device=dev) for lr in self.host_lr]
+            self.grad_scale_dev = torch.tensor([grad_scale], dtype=torch.float32, device=dev)
+            if shared_step:
+                one = torch.zeros(1, dtype=torch.int32, device=dev)
+                self.step_dev = [one] * n
+            else:
+                self.step_dev = [torch.zeros(1, dtype=torch.int32, device=dev) for _ in range(n)]
+            self.noop = torch.zeros(1, dtype=torch.int32, device=dev)
+        self._groups_c = (_abi.Group * n)()
+        self._fill_groups()
+
+        arr = (_abi.Tensor * max(1, len(descs)))(*descs)
+        plan = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            _abi.check(_abi.lib().fadam_plan_create(
+                arr, len(descs), self._groups_c, n, dtype_code(p_dtype), dtype_code(self.g_dtype),
+                dtype_code(out_dtype), flags, ctypes.byref(plan)), "fadam_plan_create")
+        self._plan = plan
+
+    # ---- scalars ---------------------------------------------------------------
+
+    def _fill_groups(self) -> None:
+        for i, g in enumerate(self.groups):
+            b1, b2 = g.get("betas", (0.9, 0.999))
+            c = self._groups_c[i]
+            c.mode = _abi.MODE_ADAMW if g.get("adam_w_mode", True) else _abi.MODE_L2
+            c.bias_correction = 1 if g.get("bias_correction", True) else 0
+            c.beta1, c.beta2 = float(b1), float(b2)
+            c.eps = float(g.get("eps", 1e-8))
+            c.weight_decay = float(g.get("weight_decay", 0.0))
+            c.lr = self.host_lr[i]
+            c.grad_scale = self.host_grad_scale
+            c.step = self.host_steps[i]
+            if self.capturable:
+                c.lr_dev = self.lr_dev[i].data_ptr()
+                c.grad_scale_dev = self.grad_scale_dev.data_ptr()
+                c.step_dev = self.step_dev[i].data_ptr()
+
+    def set_lr(self, group: int, lr: float) -> None:
+        """New learning rate for a group (a device write when capturable)."""
+        self.host_lr[group] = float(lr)
+        if self.capturable:
+            self.lr_dev[group].fill_(float(lr))
+
+    def set_grad_scale(self, scale: float) -> None:
+        self.host_grad_scale = float(scale)
+        if self.capturable:
+            self.grad_scale_dev.fill_(float(scale))
+
+    # ---- stepping ----------------------------------------------------------------
+
+    def step(self, found_inf: bool = False) -> None:
+        """One optimizer step on the current stream.
+
+        Regular shards: ``found_inf`` (a host bool, as the page's regular
+        path reads it) skips the step entirely; otherwise every group's
+        counter advances and one launch runs.  Capturable shards: one launch
+        that honours ``self.noop`` on the device; nothing here syncs, so the
+        call can be captured in a CUDA graph.
+        """
+        lib = _abi.lib()
+        if self.capturable:
+            _abi.check(lib.fadam_step(self._plan, self.noop.data_ptr(),
+                                      _stream_handle(self.device)), "fadam_step")
+            return
+        if found_inf:
+            return
+        self.host_steps = [s + 1 for s in self.host_steps]
+        self._fill_groups()
+        _abi.check(lib.fadam_plan_set_groups(self._plan, self._groups_c, len(self.groups)),
+                   "fadam_plan_set_groups")
+        _abi.check(lib.fadam_step(self._plan, None, _stream_handle(self.device)), "fadam_step")
+
+    def step_from_host(self, grads_host: Sequence[torch.Tensor]) -> List[int]:
+        """Copy host gradients (one per tensor, plan order) in, step, and
+        return the group step counters; waits for the stream."""
+        lib = _abi.lib()
+        if len(grads_host) != self.n_tensors:
+            raise ValueError("one host gradient per tensor")
+        ptrs = (ctypes.c_void_p * max(1, self.n_tensors))(*[g.data_ptr() for g in grads_host])
+        steps = (ctypes.c_int32 * len(self.groups))()
+        if not self.capturable:
+            self.host_steps = [s + 1 for s in self.host_steps]
+            self._fill_groups()
+            _abi.check(lib.fadam_plan_set_groups(self._plan, self._groups_c, len(self.groups)),
+                       "fadam_plan_set_groups")
+        noop = self.noop.data_ptr() if self.capturable else None
+        _abi.check(lib.fadam_step_host_grads(self._plan, ptrs, noop, steps,
+                                             _stream_handle(self.device)), "fadam_step_host_grads")
+        return list(steps)
+
+    # ---- state -------------------------------------------------------------------
+
+    def group_steps(self) -> List[int]:
+        """Each group's step counter (reads the device when capturable)."""
+        if self.capturable:
+            return [int(s.item()) for s in self.step_dev]
+        return list(self.host_steps)
+
+    def info(self) -> Dict[str, float]:
+        info = _abi.PlanInfo()
+        _abi.check(_abi.lib().fadam_plan_get_info(self._plan, ctypes.byref(info)),
+                   "fadam_plan_get_info")
+        return {name: getattr(info, name) for name, _ in _abi.PlanInfo._fields_}
+
+    def device_status(self) -> int:
+        st = ctypes.c_int32()
+        _abi.check(_abi.lib().fadam_plan_status(self._plan, ctypes.byref(st)), "fadam_plan_status")
+        return st.value
+
+    def close(self) -> None:
+        if getattr(self, "_plan", None):
+            _abi.lib().fadam_plan_destroy(self._plan)
+            self._plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def step_once(params, exp_avgs, exp_avg_sqs, grads, *, lr, betas, eps, weight_decay,
+              step, adam_w_mode=True, bias_correction=True, grad_scale=1.0, params_out=None,
+              lr_dev=None, step_dev=None, grad_scale_dev=None, noop=None) -> None:
+    """One-shot step through ``fadam_step_once`` (all tensors in one group)."""
+    descs = []
+    outs = params_out or [None] * len(params)
+    g_dtype = grads[0].dtype if grads else torch.float32
+    out_dtype = outs[0].dtype if outs and outs[0] is not None else None
+    for p, m, v, g, o in zip(params, exp_avgs, exp_avg_sqs, grads, outs):
+        descs.append(_abi.Tensor(p=_ptr(p), m=_ptr(m), v=_ptr(v), g=_ptr(g), p_out=_ptr(o),
+                                 rem=None, numel=p.numel(), group=0))
+    arr = (_abi.Tensor * max(1, len(descs)))(*descs)
+    dev = params[0].device if params else torch.device("cuda", torch.cuda.current_device())
+    b1, b2 = betas
+    _abi.check(_abi.lib().fadam_step_once(
+        arr, len(descs), _abi.MODE_ADAMW if adam_w_mode else _abi.MODE_L2,
+        1 if bias_correction else 0, float(b1), float(b2), float(eps), float(weight_decay),
+        float(lr), _ptr(lr_dev), int(step), _ptr(step_dev), float(grad_scale),
+        _ptr(grad_scale_dev), _ptr(noop), dtype_code(g_dtype), dtype_code(out_dtype),
+        _stream_handle(dev)), "fadam_step_once")

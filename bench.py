@@ -1,0 +1,387 @@
+"""Benchmark: fused Adam/AdamW shard step on GB300, capturable vs regular.
+
+Default workload: 201 fp32 tensors x 20,971,520 elements (the tensor list of
+the TE issue's adam_bench.py), AdamW, lr 1.6e-3, betas (0.9, 0.95),
+eps 1e-8, wd 0.1, no param-out copy: 28 algorithmic bytes per element,
+118.03 GB per step, far larger than the 129 MB L2, so no flush is needed
+between steps.
+
+One step = one fadam_step launch over the whole shard (a single persistent
+kernel).  Timed with CUDA events on the launching stream, per launch, after
+warm-up; the headline value is the capturable path's achieved HBM GB/s
+(algorithmic bytes / mean launch time).  Also measured: the regular path,
+a CUDA-graph replay of the capturable step, the in-kernel inf/nan screen,
+and an end-to-end number through fadam_step_host_grads (host gradients
+copied in from pinned memory, the step, the step counter read back).
+
+`--impl reference` times the CPU oracle instead (the reference arm): each
+step is a bounded sample of the same workload on the host cores.
+
+Multi-GPU (torchrun): every rank updates its own shard of the same size
+(weak scaling, no data-path collective); rank 0 prints the line with the
+maximum time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "Adam step achieved HBM GB/s (fraction of GB300 peak) + Gparams/s, capturable vs regular"
+
+
+# ---- distributed plumbing (timing only) ---------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value over ranks (timing reduction; not on the data path)."""
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(bytes_per_rank: float, elems_per_rank: float, world: int, seconds: float) -> dict:
+    """Whole-job throughput: every rank's bytes over the slowest rank's time."""
+    return {"gbs": world * bytes_per_rank / seconds / 1e9,
+            "gparams_per_s": world * elems_per_rank / seconds / 1e9}
+
+
+# ---- clocks -------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of the benchmark's GPU during timed work."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.rows = []
+        self.proc = None
+        self.thread = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = ["-i", str(device_index)]
+        self.cmd = ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}",
+                    "--format=csv,noheader,nounits", "-lms", "200"]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in self.rows:
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+                pw.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "power_w_max": max(pw), "reasons": sorted(reasons)}
+
+
+# ---- timing helpers -----------------------------------------------------------
+
+def time_launches(fn, steps: int, warmup: int, world: int):
+    """Per-launch CUDA-event times (ms) of `fn` on the current stream, plus
+    the bracketed wall time of the K timed steps (s)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        starts[i].record()
+        fn()
+        ends[i].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t0
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return per, wall
+
+
+def summarise(per_ms, bytes_per_step, elems, world, device):
+    mean_ms = statistics.mean(per_ms)
+    mean_ms = max_over_ranks(mean_ms, world, device)
+    agg = aggregate(bytes_per_step, elems, world, mean_ms / 1e3)
+    return {"ms_per_step": mean_ms, "min_ms": min(per_ms), "max_ms": max(per_ms),
+            "gbs": agg["gbs"], "gparams_per_s": agg["gparams_per_s"]}
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ---- CPU baseline (the oracle, as it stands) ----------------------------------
+
+def cpu_oracle_run(n_tensors: int, steps: int, threads: int, numel: int):
+    """Time the oracle on `n_tensors` tensors of the large-uniform recipe for
+    `steps` steps, tensors split into `threads` contiguous chunks run by a
+    thread pool (ctypes releases the GIL).  Returns (seconds per step, elems)."""
+    import oracle
+
+    spec = workloads.large_uniform(n_tensors=n_tensors, numel=numel)
+    shard = workloads.materialize(spec, "cpu")
+    g = spec.groups[0]
+    grp = oracle.Group(mode=oracle.MODE_ADAMW, bias_correction=1, beta1=g.betas[0],
+                       beta2=g.betas[1], eps=g.eps, weight_decay=g.weight_decay, lr=g.lr)
+    arrays = [(p.numpy(), m.numpy(), v.numpy(), gr.numpy())
+              for p, m, v, gr in zip(shard.params, shard.exp_avgs, shard.exp_avg_sqs, shard.grads)]
+    chunks = []
+    for p, m, v, gr in arrays:
+        bounds = np.linspace(0, p.size, threads + 1).astype(np.int64)
+        for a, b in zip(bounds[:-1], bounds[1:]):
+            if b > a:
+                chunks.append((p[a:b], m[a:b], v[a:b], gr[a:b]))
+    per_step = []
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        for k in range(1, steps + 1):
+            t0 = time.perf_counter()
+            list(pool.map(lambda c: oracle.adam_f32(grp, k, *c), chunks))
+            per_step.append(time.perf_counter() - t0)
+    return per_step, spec.n_elements
+
+
+def cpu_baseline(n_tensors=8, steps=10):
+    threads = os.cpu_count() or 1
+    per_step, elems = cpu_oracle_run(n_tensors, steps, threads, 320 * 65536)
+    sec = statistics.mean(per_step)
+    return {"value": elems * 28 / sec / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "gparams_per_s": elems / sec / 1e9,
+            "sample": f"{n_tensors} of the 201 tensors x 20,971,520 fp32 elements "
+                      f"({elems} elements, {elems * 28 / 1e9:.2f} GB per step), {steps} steps, "
+                      f"oracle per-tensor C loop on {threads} threads"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    threads = os.cpu_count() or 1
+    per_step, elems = cpu_oracle_run(args.ref_tensors, args.warmup + args.steps, threads,
+                                     320 * 65536)
+    timed = per_step[args.warmup:]
+    sec = statistics.mean(timed)
+    gbs = elems * 28 / sec / 1e9
+    sample = (f"each step: {args.ref_tensors} of the 201 tensors x 20,971,520 fp32 elements "
+              f"({elems} elements); oracle per-tensor C loop on {threads} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "large_uniform: 201 fp32 tensors x 20,971,520, AdamW "
+                                   "(bounded sample per step)", "sample_elements": elems},
+            "gparams_per_s": elems / sec / 1e9,
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- the GPU arm --------------------------------------------------------------
+
+def run_gpu(args):
+    from adamw_optimizer_step_persistent_gb300 import FusedAdamShard
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    device = torch.device("cuda", local)
+    spec = workloads.large_uniform(n_tensors=args.n_tensors, numel=args.numel,
+                                   seed=1237 + 1000 * rank)
+    shard = workloads.materialize(spec, device)
+    groups = shard.param_groups()
+    cap = FusedAdamShard(groups, capturable=True)
+    info = cap.info()
+    bytes_step = info["bytes_per_step"]
+    elems = info["n_elements"]
+    res = {}
+    variants = args.variants.split(",")
+    sampler = ClockSampler(local)
+    sampler.start()
+    if "capturable" in variants:
+        per, _ = time_launches(cap.step, args.steps, args.warmup, world)
+        res["capturable"] = summarise(per, bytes_step, elems, world, device)
+    if "regular" in variants:
+        reg = FusedAdamShard(groups, capturable=False)
+        per, _ = time_launches(reg.step, args.steps, args.warmup, world)
+        res["regular"] = summarise(per, bytes_step, elems, world, device)
+        reg.close()
+    if "graph" in variants:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            cap.step()
+        torch.cuda.current_stream().wait_stream(s)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cap.step()
+        per, _ = time_launches(graph.replay, args.steps, args.warmup, world)
+        res["graph_replay"] = summarise(per, bytes_step, elems, world, device)
+        del graph
+    if "check_finite" in variants:
+        chk = FusedAdamShard(groups, capturable=True, check_finite=True)
+        per, _ = time_launches(chk.step, args.steps, args.warmup, world)
+        r = summarise(per, bytes_step, elems, world, device)
+        r["gbs_including_screen"] = r["gbs"] * (bytes_step + chk.info()["check_bytes_per_step"]) / bytes_step
+        res["check_finite"] = r
+        chk.close()
+    clocks = sampler.stop()
+
+    e2e = None
+    if "e2e" in variants:
+        host = [g.cpu().pin_memory() for g in shard.grads]
+        for _ in range(max(1, args.warmup // 2)):
+            cap.step_from_host(host)
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            cap.step_from_host(host)
+        barrier(world)
+        sec = max_over_ranks((time.perf_counter() - t0) / args.steps, world, device)
+        agg = aggregate(bytes_step, elems, world, sec)
+        e2e = {"value": agg["gbs"], "unit": "GB/s", "ms_per_step": sec * 1e3,
+               "h2d_bytes_per_step": int(sum(g.numel() * g.element_size() for g in host)),
+               "d2h_bytes_per_step": 4 * len(groups),
+               "path": "fadam_step_host_grads: pinned host grads -> device, one launch, "
+                       "step counter -> host, stream sync"}
+        del host
+
+    head = res.get("capturable") or next(iter(res.values()))
+    peaks = measured_peaks()
+    achieved = bytes_step / (head["ms_per_step"] / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": head["gbs"], "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"large_uniform: {args.n_tensors} fp32 tensors x {args.numel}, "
+                               "AdamW lr 1.6e-3 betas (0.9,0.95) eps 1e-8 wd 0.1, no param-out",
+                   "elements_per_step": elems, "bytes_per_step": bytes_step,
+                   "bytes_per_element": bytes_step / elems, "grid": info["grid"],
+                   "block": info["block"], "items": info["n_items"],
+                   "l2": "inputs larger than L2 (no flush needed)",
+                   "parallelism": f"weak: one shard per GPU x {world}"},
+        "fraction_of_peak": head["gbs"] / world / peaks["hbm_gbs"],
+        "gparams_per_s": head["gparams_per_s"],
+        "variants": res,
+        "capturable_vs_regular": (res["capturable"]["ms_per_step"] / res["regular"]["ms_per_step"]
+                                  if "capturable" in res and "regular" in res else None),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "peak_source": peaks["source"], "traffic": args.traffic,
+                     "kernel": "fadam_update_kernel<f32 grad, no out, fp32 master>"},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    cap.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--n-tensors", type=int, default=201)
+    ap.add_argument("--numel", type=int, default=320 * 65536)
+    ap.add_argument("--variants", default="capturable,regular,graph,check_finite,e2e")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-tensors", type=int, default=4)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per launch for the headline kernel, if captured")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,278 @@
+/*
+ * fadam.h - C ABI of the multi-tensor fused Adam/AdamW update over one
+ * data-parallel rank's optimizer shard, for NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes (sources are web pages, cited by title and the
+ * construct on the page):
+ *   - "Enhance Distributed Fused Adam (#1794)" (apex patch),
+ *     DistAdamCapturableFunctor::local_step: per element, with sg the
+ *     scaled gradient,
+ *       L2 mode:    sg = g*grad_scale + wd*p
+ *       AdamW mode: sg = g*grad_scale
+ *       m' = beta1*m + (1-beta1)*sg          v' = beta2*v + (1-beta2)*sg^2
+ *       u  = (m'/bc1) / (sqrt(v'/bc2) + eps)  (+ wd*p in AdamW mode, old p)
+ *       p' = p - lr*u,   p_out = p' cast to the param-out dtype
+ *     with bc1 = 1-beta1^step, bc2 = 1-beta2^step when bias correction is
+ *     on (operator(), bias-correction block) and 1 otherwise; a noop flag
+ *     equal to 1 leaves everything untouched (operator(), early return).
+ *     lerp() is not defined on the page; it is read as the moving average
+ *     above.  Every operation is one IEEE fp32 operation, not contracted.
+ *   - "apex/contrib/optimizers/distributed_fused_adam.py":
+ *     step() (regular: the step counter advances by one before the update;
+ *     capturable: by (noop != 1), on the device), _local_step() (one call per
+ *     group over lists p, m, v, g, p_out), _local_step_with_param_remainders()
+ *     and _bf16_rem_to_fp32() (the fp32 master held as a bf16 high half plus
+ *     an int16 remainder).
+ *   - "[PyTorch] Advance FusedAdam step counter for empty param groups"
+ *     (TransformerEngine PR), Fix section: every param group's counter
+ *     advances, also a group that holds no tensor on this rank.
+ *
+ * Design: a plan packs the ragged tensor list once into a balanced work list
+ * for a persistent grid; each fadam_step() is then ONE kernel launch on the
+ * caller's stream, with no host synchronisation, no allocation and no
+ * host-to-device copy, so the capturable form can be captured in a CUDA
+ * graph.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_dev are device pointers (cudaMalloc, torch CUDA
+ *     storage); other pointers are host pointers unless stated.
+ *   - The caller owns all tensor memory.  A plan owns only its work list,
+ *     its copy of the descriptors and a small device status block.
+ *   - Argument checks run on the host before anything is launched.  A
+ *     failing check returns a non-zero status and launches nothing; the
+ *     message for the calling thread is available from fadam_last_error().
+ *   - No entry point traps or asserts on the device.  The only device-side
+ *     error (a bounded wait that gives up) is recorded in the plan's status
+ *     block and reported by fadam_plan_status().
+ *   - Calls on one plan must be ordered (one stream, or ordered streams):
+ *     the plan's device status block is shared by its launches.
+ */
+#ifndef FADAM_H_
+#define FADAM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t.  NULL means the legacy default stream. */
+typedef struct CUstream_st* fadam_stream;
+
+/* Opaque plan (packed work list for one shard). */
+typedef struct fadam_plan fadam_plan;
+
+/* Status codes returned by every entry point. */
+typedef int32_t fadam_status;
+#define FADAM_OK 0
+#define FADAM_EINVAL 1   /* an argument failed its check; nothing launched */
+#define FADAM_EDTYPE 2   /* unsupported dtype combination; nothing launched */
+#define FADAM_EALIGN 3   /* a pointer is not aligned to its element size */
+#define FADAM_ECUDA 4    /* a CUDA runtime call failed (see fadam_last_error) */
+#define FADAM_ETIMEOUT 5 /* a bounded device-side wait gave up (device status) */
+#define FADAM_ELIMIT 6   /* a size is beyond a documented maximum */
+
+/* Update mode ("mode" argument of the page's kernel; adam_w_mode). */
+#define FADAM_MODE_L2 0    /* L2: weight decay folded into the gradient */
+#define FADAM_MODE_ADAMW 1 /* decoupled weight decay */
+
+/* Element types. */
+#define FADAM_DT_NONE 0 /* no param-out copy */
+#define FADAM_DT_F32 1
+#define FADAM_DT_BF16 2
+#define FADAM_DT_F16 3
+
+/* Plan flags. */
+#define FADAM_CAPTURABLE 1u  /* lr, grad_scale, step read from device memory */
+#define FADAM_REMAINDERS 2u  /* master = bf16 p (high half) + int16 rem */
+#define FADAM_CHECK_FINITE 4u /* screen g*grad_scale for inf/nan first; sets noop */
+#define FADAM_STEP_PREADVANCED 8u /* capturable: *step_dev already advanced by the
+                                     caller; use it as is and do not write it */
+
+/* Maximum number of param groups in one plan. */
+#define FADAM_MAX_GROUPS 32
+
+/* One tensor (fragment) of the shard.  Every data pointer is a device
+ * pointer to numel contiguous elements, aligned at least to its element
+ * size.
+ *   p      fp32 master parameter, updated in place; in FADAM_REMAINDERS mode
+ *          the bf16 high half of the master (read only, unless p_out
+ *          aliases it)
+ *   m, v   fp32 first and second moments (exp_avg, exp_avg_sq), in place
+ *   g      gradient in the plan's g dtype, read only
+ *   p_out  param-out copy in the plan's out dtype; NULL iff the out dtype
+ *          is FADAM_DT_NONE; may alias p; required (bf16) in remainder mode
+ *   rem    int16 remainder, in place; non-NULL iff FADAM_REMAINDERS
+ *   group  index of the tensor's param group, 0 <= group < n_groups
+ * Tensors must not overlap one another, except that p_out may equal p. */
+typedef struct {
+  void* p;
+  void* m;
+  void* v;
+  const void* g;
+  void* p_out;
+  int16_t* rem;
+  int64_t numel;
+  int32_t group;
+  int32_t reserved; /* set to 0 */
+} fadam_tensor;
+
+/* One param group's hyper-parameters and scalars.
+ *   mode             FADAM_MODE_L2 or FADAM_MODE_ADAMW
+ *   bias_correction  0 or 1
+ *   beta1, beta2     in [0, 1)
+ *   eps              >= 0;  weight_decay: finite
+ * Regular plans read the host scalars lr, grad_scale and step (the step
+ * already advanced for this update, >= 1 when bias correction is on).
+ * Capturable plans read lr_dev, grad_scale_dev (fp32) and step_dev (int32)
+ * instead; step_dev is required for every group, empty or not, and groups
+ * may share one counter (it then advances once per step).  lr_dev and
+ * grad_scale_dev may be NULL only for a group with no tensor. */
+typedef struct {
+  int32_t mode;
+  int32_t bias_correction;
+  float beta1;
+  float beta2;
+  float eps;
+  float weight_decay;
+  float lr;
+  float grad_scale;
+  int32_t step;
+  int32_t reserved; /* set to 0 */
+  const float* lr_dev;
+  const float* grad_scale_dev;
+  int32_t* step_dev;
+} fadam_group;
+
+/* Read-only facts about a plan. */
+typedef struct {
+  int64_t n_tensors;
+  int64_t n_elements;     /* elements updated per step */
+  int64_t n_items;        /* work items in the packed list */
+  int32_t grid;           /* CTAs of the persistent launch */
+  int32_t block;          /* threads per CTA */
+  int32_t blocks_per_sm;  /* resident CTAs per SM at this block size */
+  int32_t sm_count;
+  int32_t n_groups;
+  int32_t device;
+  double bytes_per_step;  /* algorithmic HBM bytes of one update (each
+                             stream read or written once) */
+  double check_bytes_per_step; /* extra bytes of the FADAM_CHECK_FINITE screen */
+} fadam_plan_info;
+
+/* Build a plan for a shard: validates every descriptor, packs the ragged
+ * tensor list into a balanced work list for a persistent grid sized to the
+ * current device, uploads it (synchronously) and allocates the plan's
+ * device status block.  Call it before any stream capture.
+ *   tensors[n_tensors]  descriptors (host array, copied; n_tensors >= 0)
+ *   groups[n_groups]    1 <= n_groups <= FADAM_MAX_GROUPS (host array, copied)
+ *   p_dtype             FADAM_DT_F32, or FADAM_DT_BF16 with FADAM_REMAINDERS
+ *   g_dtype             FADAM_DT_F32, FADAM_DT_BF16 or FADAM_DT_F16
+ *   out_dtype           FADAM_DT_NONE, _F32, _BF16 or _F16 (_BF16 with remainders)
+ *   flags               FADAM_CAPTURABLE | FADAM_REMAINDERS |
+ *                       FADAM_CHECK_FINITE | FADAM_STEP_PREADVANCED
+ *   *plan_out           receives the plan (owned by the caller; free with
+ *                       fadam_plan_destroy)
+ * Errors: FADAM_EINVAL, FADAM_EDTYPE, FADAM_EALIGN, FADAM_ELIMIT, FADAM_ECUDA;
+ * on error *plan_out is set to NULL. */
+fadam_status fadam_plan_create(const fadam_tensor* tensors, int64_t n_tensors,
+                               const fadam_group* groups, int32_t n_groups,
+                               int32_t p_dtype, int32_t g_dtype, int32_t out_dtype,
+                               uint32_t flags, fadam_plan** plan_out);
+
+/* Replace the plan's param-group table (same n_groups as at creation).  This
+ * is how a regular plan receives each step's host lr, grad_scale and step;
+ * it copies the values on the host and touches no device memory, so it may
+ * be called between captured launches (the captured launch keeps the values
+ * it was captured with).  Errors: FADAM_EINVAL. */
+fadam_status fadam_plan_set_groups(fadam_plan* plan, const fadam_group* groups,
+                                   int32_t n_groups);
+
+/* One optimizer step over the whole shard: one persistent-grid kernel
+ * launch on `stream`, or none when there is nothing to do.
+ *   noop_dev  int32 device flag (may be NULL when FADAM_CHECK_FINITE is not
+ *             set).  When it equals 1 nothing is written: not p, m, v, rem,
+ *             p_out, nor the step counters; any other value counts as clear
+ *             (the page's kernel tests for 1).  The library only ever
+ *             writes 1 to it (with FADAM_CHECK_FINITE, when some
+ *             g*grad_scale is not finite; the screen runs over the whole
+ *             shard before any update).
+ * Capturable plans advance every group's *step_dev by (noop != 1) within
+ * the same launch and use step+1 in the bias correction (unless
+ * FADAM_STEP_PREADVANCED).  No host sync, no allocation: safe to capture.
+ * Errors: FADAM_EINVAL, FADAM_EALIGN, FADAM_ECUDA (launch failed). */
+fadam_status fadam_step(fadam_plan* plan, int32_t* noop_dev, fadam_stream stream);
+
+/* End-to-end step from host gradients: for every tensor, copies
+ * g_host[i] (a host buffer of numel elements of the g dtype; pinned memory
+ * makes the copy asynchronous) into the tensor's device g, runs
+ * fadam_step(), copies each group's step counter into steps_host[n_groups]
+ * (may be NULL), and waits for the stream.  Errors: as fadam_step. */
+fadam_status fadam_step_host_grads(fadam_plan* plan, const void* const* g_host,
+                                   int32_t* noop_dev, int32_t* steps_host,
+                                   fadam_stream stream);
+
+/* Read (synchronously) and clear the plan's device status word:
+ * *device_status = FADAM_OK, or FADAM_ETIMEOUT when a bounded wait of the
+ * FADAM_CHECK_FINITE grid barrier gave up (that step may be partly applied).
+ * Clearing also resets the barrier counters.  Errors: FADAM_EINVAL,
+ * FADAM_ECUDA. */
+fadam_status fadam_plan_status(fadam_plan* plan, int32_t* device_status);
+
+/* Facts about a plan.  Errors: FADAM_EINVAL. */
+fadam_status fadam_plan_get_info(const fadam_plan* plan, fadam_plan_info* info);
+
+/* Free a plan (waits for the device first).  NULL is accepted. */
+fadam_status fadam_plan_destroy(fadam_plan* plan);
+
+/* One-shot step mirroring the page's kernel signature: packs `tensors`
+ * (all in one param group), runs one step and frees its work list in
+ * stream order (cudaMallocAsync / cudaFreeAsync).  Regular when lr_dev,
+ * step_dev and grad_scale_dev are all NULL (host lr, step, grad_scale);
+ * capturable when all three are given.  out_dtype as in fadam_plan_create,
+ * p and g dtypes fp32 and g_dtype.  It copies pageable host memory, so it
+ * is not for stream capture.  Errors: as fadam_plan_create / fadam_step. */
+fadam_status fadam_step_once(const fadam_tensor* tensors, int64_t n_tensors, int32_t mode,
+                             int32_t bias_correction, float beta1, float beta2, float eps,
+                             float weight_decay, float lr, const float* lr_dev,
+                             int32_t step, int32_t* step_dev, float grad_scale,
+                             const float* grad_scale_dev, int32_t* noop_dev,
+                             int32_t g_dtype, int32_t out_dtype, fadam_stream stream);
+
+/* One work item of a dry-run packing (see fadam_pack_dry). */
+typedef struct {
+  int64_t tensor; /* index into the tensors array */
+  int64_t offset; /* first element of the run within the tensor */
+  int32_t n;      /* elements in the run */
+  int32_t vec;    /* 1 when every stream is 16-byte (fp32) / 8-byte (16-bit)
+                     aligned at the run start and the run takes the
+                     128-bit path */
+} fadam_pack_item;
+
+/* Host-only dry run of the packer, for inspection and tests; needs no GPU
+ * and dereferences no tensor pointer (their addresses only decide
+ * alignment).  Packs `tensors` for a grid of `grid` CTAs exactly as
+ * fadam_plan_create would, writes the item count to *n_items_out, the items
+ * to items_out[max_items] (may be NULL) and grid+1 CTA start indices to
+ * cta_begin_out (may be NULL): CTA b runs items
+ * [cta_begin_out[b], cta_begin_out[b+1]).  Errors: as fadam_plan_create's
+ * argument checks, FADAM_ELIMIT when the items exceed max_items. */
+fadam_status fadam_pack_dry(const fadam_tensor* tensors, int64_t n_tensors, int32_t n_groups,
+                            int32_t p_dtype, int32_t g_dtype, int32_t out_dtype, uint32_t flags,
+                            int32_t grid, fadam_pack_item* items_out, int64_t max_items,
+                            int32_t* cta_begin_out, int64_t* n_items_out);
+
+/* Static description of a status code. */
+const char* fadam_status_string(fadam_status status);
+
+/* Message of the last failure in the calling thread ("" when none). */
+const char* fadam_last_error(void);
+
+/* Library version, as major*10000 + minor*100 + patch. */
+int32_t fadam_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FADAM_H_ */

@@ -1,0 +1,195 @@
+"""Test helpers: hand the same seeded inputs to the oracle, and compare.
+
+Tolerances (GPU vs oracle):
+  fp32 p, m, v:        |d| <= 2e-6 * |x| + 1e-9   (x the oracle value)
+  bf16/fp16 param-out: at most 1 unit in the last place
+  noop, step counters, remainder round trip: bit-exact
+"""
+from __future__ import annotations
+
+from typing import Dict, List
+
+import numpy as np
+import torch
+
+import oracle
+import workloads
+
+RTOL, ATOL = 2e-6, 1e-9
+
+_ODT = {torch.float32: oracle.DT_F32, torch.bfloat16: oracle.DT_BF16, torch.float16: oracle.DT_F16}
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.float32:
+        return t.numpy().copy()
+    if t.dtype in (torch.bfloat16, torch.float16):
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    if t.dtype == torch.int16:
+        return t.numpy().copy()
+    raise TypeError(t.dtype)
+
+
+def oracle_groups(spec: workloads.ShardSpec) -> List[oracle.Group]:
+    out = []
+    for g in spec.groups:
+        out.append(oracle.Group(mode=oracle.MODE_ADAMW if g.adam_w_mode else oracle.MODE_L2,
+                                bias_correction=1 if g.bias_correction else 0,
+                                beta1=g.betas[0], beta2=g.betas[1], eps=g.eps,
+                                weight_decay=g.weight_decay, lr=g.lr,
+                                grad_scale=spec.grad_scale))
+    return out
+
+
+def oracle_shard(shard: workloads.Shard, idx: List[int] = None, elems: Dict[int, np.ndarray] = None,
+                 step_slot=None) -> oracle.Shard:
+    """Snapshot of the shard (or of sampled elements of it) as oracle arrays.
+
+    `idx` is the tensor order; `elems[i]`, when given, selects elements of
+    tensor i (the oracle then runs on the gathered samples only, which is
+    exact because every element updates independently).
+    """
+    spec = shard.spec
+    idx = shard.plan_order() if idx is None else idx
+    g_dt = _ODT[spec.g_dtype]
+    tensors = []
+    for i in idx:
+        sel = (lambda t: t) if elems is None else (lambda t, e=torch.as_tensor(elems[i], device=shard.params[i].device): t[e])
+        t = oracle.Tensor(group=spec.group_of[i], m=to_np(sel(shard.exp_avgs[i])),
+                          v=to_np(sel(shard.exp_avg_sqs[i])), g=to_np(sel(shard.grads[i])),
+                          g_dtype=g_dt)
+        if spec.remainders:
+            t.p_hi = to_np(sel(shard.params[i]))
+            t.rem = to_np(sel(shard.remainders[i]))
+            t.p_out = t.p_hi  # the new high half replaces the param in place
+            t.out_dtype = oracle.DT_BF16
+        else:
+            t.p = to_np(sel(shard.params[i]))
+            if spec.out_dtype is not None:
+                t.p_out = to_np(sel(shard.params_out[i]))
+                t.out_dtype = _ODT[spec.out_dtype]
+        tensors.append(t)
+    return oracle.Shard(groups=oracle_groups(spec), tensors=tensors,
+                        step_slot=list(step_slot) if step_slot else [])
+
+
+def refresh_grads(osh: oracle.Shard, shard: workloads.Shard, idx=None, elems=None) -> None:
+    idx = shard.plan_order() if idx is None else idx
+    for t, i in zip(osh.tensors, idx):
+        g = shard.grads[i]
+        if elems is not None:
+            g = g[torch.as_tensor(elems[i], device=g.device)]
+        t.g = to_np(g)
+
+
+def _ordered16(bits: np.ndarray) -> np.ndarray:
+    b = bits.astype(np.int32)
+    return np.where(b & 0x8000, -(b & 0x7FFF), b)
+
+
+class Report:
+    """Collects the worst deviations and the share of bit-identical values."""
+
+    def __init__(self):
+        self.n = 0
+        self.exact = 0
+        self.worst = 0.0
+
+    def f32(self, got: np.ndarray, want: np.ndarray, what: str) -> None:
+        got = got.astype(np.float64)
+        want = want.astype(np.float64)
+        both_nan = np.isnan(got) & np.isnan(want)
+        d = np.where(both_nan, 0.0, np.abs(got - want))
+        lim = RTOL * np.abs(want) + ATOL
+        bad = ~(d <= lim)
+        if bad.any():
+            k = int(np.argmax(bad))
+            raise AssertionError(f"{what}: {int(bad.sum())} of {got.size} outside tolerance; "
+                                 f"first at {k}: got {got[k]!r} want {want[k]!r}")
+        self.n += got.size
+        self.exact += int(np.sum((got == want) | both_nan))
+        with np.errstate(invalid="ignore", divide="ignore"):
+            rel = np.where(d > 0, d / np.maximum(lim, 1e-300), 0.0)
+        if rel.size:
+            self.worst = max(self.worst, float(rel.max()))
+
+    def ulp16(self, got: np.ndarray, want: np.ndarray, what: str) -> None:
+        d = np.abs(_ordered16(got) - _ordered16(want))
+        if (d > 1).any():
+            k = int(np.argmax(d > 1))
+            raise AssertionError(f"{what}: {int((d > 1).sum())} values beyond 1 ulp; first at "
+                                 f"{k}: got 0x{int(got[k]):04X} want 0x{int(want[k]):04X}")
+        self.n += got.size
+        self.exact += int(np.sum(d == 0))
+
+    @property
+    def exact_fraction(self) -> float:
+        return self.exact / max(1, self.n)
+
+
+def compare(shard: workloads.Shard, osh: oracle.Shard, idx=None, elems=None,
+            report: Report = None) -> Report:
+    """GPU shard vs oracle shard, element by element (or on the samples)."""
+    report = report or Report()
+    spec = shard.spec
+    idx = shard.plan_order() if idx is None else idx
+    for t, i in zip(osh.tensors, idx):
+        sel = (lambda x: x) if elems is None else (lambda x, e=torch.as_tensor(elems[i], device=shard.params[i].device): x[e])
+        report.f32(to_np(sel(shard.exp_avgs[i])), t.m, f"tensor {i} m")
+        report.f32(to_np(sel(shard.exp_avg_sqs[i])), t.v, f"tensor {i} v")
+        if spec.remainders:
+            hi = to_np(sel(shard.params[i]))
+            rem = to_np(sel(shard.remainders[i]))
+            got = oracle.rem_pack(hi, rem).view(np.float32)
+            want = oracle.rem_pack(t.p_hi, t.rem).view(np.float32)
+            report.f32(got, want, f"tensor {i} fp32 master (bf16 + remainder)")
+            report.ulp16(hi, t.p_hi, f"tensor {i} bf16 high half")
+        else:
+            report.f32(to_np(sel(shard.params[i])), t.p, f"tensor {i} p")
+            if spec.out_dtype == torch.float32:
+                report.f32(to_np(sel(shard.params_out[i])), t.p_out, f"tensor {i} p_out")
+            elif spec.out_dtype is not None:
+                report.ulp16(to_np(sel(shard.params_out[i])), t.p_out, f"tensor {i} p_out")
+    return report
+
+
+def sample_elements(spec: workloads.ShardSpec, per_tensor: int, seed: int) -> Dict[int, np.ndarray]:
+    """Seeded element samples per tensor (every element of small tensors),
+    always including each tensor's first and last element."""
+    rng = np.random.default_rng(seed)
+    out = {}
+    for i, n in enumerate(spec.sizes):
+        if n <= per_tensor:
+            out[i] = np.arange(n, dtype=np.int64)
+        else:
+            e = rng.choice(n, size=per_tensor - 2, replace=False)
+            out[i] = np.unique(np.concatenate([e, [0, n - 1]])).astype(np.int64)
+    return out
+
+
+def snapshot(shard: workloads.Shard) -> List[torch.Tensor]:
+    """Clones of every state tensor of the shard (on its device)."""
+    ts = []
+    for lst in (shard.params, shard.exp_avgs, shard.exp_avg_sqs, shard.params_out,
+                shard.remainders):
+        for t in lst:
+            if t is not None:
+                ts.append(t.clone())
+    return ts
+
+
+def state_equal(shard: workloads.Shard, snap: List[torch.Tensor]) -> bool:
+    k = 0
+    for lst in (shard.params, shard.exp_avgs, shard.exp_avg_sqs, shard.params_out,
+                shard.remainders):
+        for t in lst:
+            if t is not None:
+                a = t.view(torch.int16) if t.dtype != torch.int16 and t.element_size() == 2 else t
+                b = snap[k].view(torch.int16) if snap[k].element_size() == 2 and snap[k].dtype != torch.int16 else snap[k]
+                if t.dtype == torch.float32:
+                    a, b = t.view(torch.int32), snap[k].view(torch.int32)
+                if not torch.equal(a, b):
+                    return False
+                k += 1
+    return True

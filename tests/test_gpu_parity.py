@@ -1,0 +1,307 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Small versions of the five shard recipes, element by element over every
+tensor, several steps each, plus the edge cases: ragged and empty tensors,
+misaligned views, aliasing param-out, every grad/param-out dtype, noop and
+inf screens, shared and per-group step counters, graph replay, one-shot and
+host-gradient entry points.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from adamw_optimizer_step_persistent_gb300 import FusedAdamShard, _abi, step_once
+from tests import helpers
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _run(spec, steps, *, capturable=None, check_finite=False, fresh=True, shared_step=False):
+    """Run `steps` steps on the GPU and on the oracle from the same inputs."""
+    capturable = spec.capturable if capturable is None else capturable
+    shard = workloads.materialize(spec, DEV)
+    opt = FusedAdamShard(shard.param_groups(), capturable=capturable, check_finite=check_finite,
+                         remainders=spec.remainders, grad_scale=spec.grad_scale,
+                         shared_step=shared_step)
+    osh = helpers.oracle_shard(shard, step_slot=[0] * len(spec.groups) if shared_step else None)
+    for k in range(1, steps + 1):
+        if fresh and k > 1:
+            workloads.fresh_grads(shard, k)
+            helpers.refresh_grads(osh, shard)
+        opt.step()
+        oracle.shard_step(osh, capturable=capturable)
+    torch.cuda.synchronize()
+    return shard, opt, osh
+
+
+@pytest.mark.parametrize("name", ["tiny_adamw", "capturable_l2", "large_uniform",
+                                  "remainder_shard", "many_small"])
+def test_small_shards_match_oracle(name):
+    spec = workloads.small_versions()[name]
+    steps = 10 if name == "tiny_adamw" else 5
+    shard, opt, osh = _run(spec, steps)
+    rep = helpers.compare(shard, osh)
+    assert opt.group_steps() == oracle.group_steps(osh) == [steps] * len(spec.groups)
+    print(f"{name}: {rep.n} values, {rep.exact_fraction:.6f} bit-identical, "
+          f"worst {rep.worst:.3g} of tolerance")
+
+
+@pytest.mark.parametrize("name", ["tiny_adamw", "many_small"])
+def test_regular_and_capturable_are_bit_identical(name):
+    spec = workloads.small_versions()[name]
+    a, _, _ = _run(spec, 4, capturable=False)
+    b, opt_b, _ = _run(spec, 4, capturable=True)
+    for x, y in zip(helpers.snapshot(a), helpers.snapshot(b)):
+        assert torch.equal(x.view(torch.int32) if x.dtype == torch.float32 else x,
+                           y.view(torch.int32) if y.dtype == torch.float32 else y)
+    assert opt_b.group_steps() == [4] * len(spec.groups)
+
+
+def test_check_finite_without_inf_matches_plain_capturable():
+    spec = workloads.small_versions()["many_small"]
+    a, _, _ = _run(spec, 3, capturable=True)
+    b, opt_b, _ = _run(spec, 3, capturable=True, check_finite=True)
+    for x, y in zip(helpers.snapshot(a), helpers.snapshot(b)):
+        assert torch.equal(x, y)
+    assert opt_b.noop.item() == 0 and opt_b.device_status() == 0
+
+
+@pytest.mark.parametrize("screen", ["upstream_flag", "in_kernel_check"])
+def test_inf_gradient_skips_the_step_bit_exactly(screen):
+    """capturable L2 shard, bf16 grads and param-out: the step whose grads
+    hold a +inf changes nothing and does not advance the counter."""
+    spec = workloads.small_versions()["capturable_l2"]
+    shard = workloads.materialize(spec, DEV)
+    opt = FusedAdamShard(shard.param_groups(), capturable=True,
+                         check_finite=(screen == "in_kernel_check"), grad_scale=spec.grad_scale)
+    osh = helpers.oracle_shard(shard)
+    t_inf, e_inf = workloads.inf_position(spec)
+    for k in range(1, 6):
+        if k > 1:
+            workloads.fresh_grads(shard, k)
+            helpers.refresh_grads(osh, shard)
+        inject = k == spec.inf_at_step
+        if inject:
+            shard.grads[t_inf][e_inf] = float("inf")
+            before = helpers.snapshot(shard)
+            if screen == "upstream_flag":  # as the page's step(): found_inf copied to the flag
+                opt.noop.copy_(torch.isinf(shard.grads[t_inf]).any().to(torch.int32).view(1))
+        opt.step()
+        torch.cuda.synchronize()
+        if inject:
+            assert opt.noop.item() == 1
+            assert helpers.state_equal(shard, before)
+            assert opt.group_steps() == [k - 1]
+            oracle.shard_step(osh, capturable=True, noop=True)
+            opt.noop.zero_()
+        else:
+            oracle.shard_step(osh, capturable=True)
+    rep = helpers.compare(shard, osh)
+    assert opt.group_steps() == oracle.group_steps(osh) == [4]
+    assert rep.n > 0
+
+
+def test_graph_replay_matches_eager():
+    spec = workloads.small_versions()["many_small"]
+    a = workloads.materialize(spec, DEV)
+    b = workloads.materialize(spec, DEV)
+    oa = FusedAdamShard(a.param_groups(), capturable=True)
+    ob = FusedAdamShard(b.param_groups(), capturable=True)
+    for _ in range(3):
+        oa.step()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ob.step()  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ob.step()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    for x, y in zip(helpers.snapshot(a), helpers.snapshot(b)):
+        assert torch.equal(x, y)
+    assert ob.group_steps() == oa.group_steps() == [3, 3, 3]
+
+
+@pytest.mark.parametrize("g_dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("out_dtype", [None, torch.float32, torch.bfloat16, torch.float16])
+def test_dtype_combinations(g_dtype, out_dtype):
+    spec = workloads.large_uniform(n_tensors=3, numel=40_003)
+    spec.g_dtype, spec.out_dtype = g_dtype, out_dtype
+    shard, _, osh = _run(spec, 3, capturable=False)
+    helpers.compare(shard, osh)
+
+
+def _custom_shard(sizes, offsets_p, offsets_mvg, group_of, groups, out_alias=False,
+                  out_dtype=None):
+    """Tensors as views at chosen element offsets into fresh buffers."""
+    spec = workloads.ShardSpec("custom", groups, list(sizes), list(group_of), out_dtype=out_dtype,
+                               seed=99)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(99)
+    P, M, V, G, O = [], [], [], [], []
+    for n, op, oq in zip(sizes, offsets_p, offsets_mvg):
+        bp = torch.randn(n + op, generator=gen, device=DEV)
+        bm = torch.zeros(n + oq, device=DEV)
+        bv = torch.zeros(n + oq, device=DEV)
+        bg = torch.randn(n + oq, generator=gen, device=DEV) * 1e-3
+        P.append(bp[op:op + n])
+        M.append(bm[oq:oq + n])
+        V.append(bv[oq:oq + n])
+        G.append(bg[oq:oq + n])
+        if out_alias:
+            O.append(P[-1])
+        elif out_dtype is not None:
+            O.append(torch.zeros(n + op, dtype=out_dtype, device=DEV)[op:op + n])
+        else:
+            O.append(None)
+    return workloads.Shard(spec, P, M, V, G, O, [None] * len(sizes))
+
+
+def test_ragged_empty_and_misaligned_views():
+    g = workloads.GroupSpec(adam_w_mode=True, weight_decay=0.05, betas=(0.9, 0.95))
+    sizes = [0, 1, 3, 4, 5, 31, 1000, 4097, 70001, 0, 65536]
+    offs_p = [0, 1, 2, 3, 1, 0, 5, 3, 1, 0, 2]      # same residue as m, v, g: peeled head
+    offs_q = [0, 1, 2, 3, 2, 1, 5, 0, 1, 0, 2]      # some differ: whole tensor scalar
+    shard = _custom_shard(sizes, offs_p, offs_q, [0] * len(sizes), [g], out_dtype=torch.bfloat16)
+    opt = FusedAdamShard(shard.param_groups(), capturable=False)
+    osh = helpers.oracle_shard(shard)
+    for k in range(1, 4):
+        opt.step()
+        oracle.shard_step(osh, capturable=False)
+    torch.cuda.synchronize()
+    helpers.compare(shard, osh)
+
+
+def test_param_out_aliasing_the_master():
+    g = workloads.GroupSpec(adam_w_mode=False, weight_decay=0.1)
+    shard = _custom_shard([1234, 50000], [0, 0], [0, 0], [0, 0], [g], out_alias=True,
+                          out_dtype=torch.float32)
+    opt = FusedAdamShard(shard.param_groups(), capturable=False)
+    osh = helpers.oracle_shard(shard)
+    for t in osh.tensors:
+        t.p_out = t.p
+    for _ in range(3):
+        opt.step()
+        oracle.shard_step(osh, capturable=False)
+    torch.cuda.synchronize()
+    helpers.compare(shard, osh)
+    info = opt.info()
+    assert info["bytes_per_step"] == (1234 + 50000) * 28.0  # the alias is one stream
+
+
+def test_bias_correction_off_and_mixed_modes():
+    groups = [workloads.GroupSpec(adam_w_mode=True, weight_decay=0.1, bias_correction=False),
+              workloads.GroupSpec(adam_w_mode=False, weight_decay=0.1, bias_correction=True,
+                                  betas=(0.8, 0.9)),
+              workloads.GroupSpec(adam_w_mode=True, weight_decay=0.0, eps=1e-6)]
+    sizes = [5000, 777, 4096, 3, 100_000]
+    shard = _custom_shard(sizes, [0] * 5, [0] * 5, [0, 1, 2, 0, 1], groups)
+    for cap in (False, True):
+        sh = _custom_shard(sizes, [0] * 5, [0] * 5, [0, 1, 2, 0, 1], groups)
+        opt = FusedAdamShard(sh.param_groups(), capturable=cap)
+        osh = helpers.oracle_shard(sh)
+        for _ in range(4):
+            opt.step()
+            oracle.shard_step(osh, capturable=cap)
+        torch.cuda.synchronize()
+        helpers.compare(sh, osh)
+        assert opt.group_steps() == [4, 4, 4]
+    del shard
+
+
+def test_shared_step_counter_advances_once():
+    spec = workloads.small_versions()["many_small"]
+    shard, opt, osh = _run(spec, 3, shared_step=True)
+    helpers.compare(shard, osh)
+    assert opt.group_steps() == [3, 3, 3]
+    assert opt.step_dev[0].data_ptr() == opt.step_dev[2].data_ptr()
+
+
+def test_step_preadvanced_uses_counter_as_is():
+    spec = workloads.small_versions()["tiny_adamw"]
+    a, _, _ = _run(spec, 2, capturable=True, fresh=False)
+    b = workloads.materialize(spec, DEV)
+    ob = FusedAdamShard(b.param_groups(), capturable=True, step_preadvanced=True)
+    for k in (1, 2):
+        for s in ob.step_dev:
+            s.fill_(k)  # the caller advances, as the page's step() does
+        ob.step()
+    torch.cuda.synchronize()
+    for x, y in zip(helpers.snapshot(a), helpers.snapshot(b)):
+        assert torch.equal(x, y)
+    assert ob.group_steps() == [2, 2]
+
+
+def test_all_empty_plan_still_advances_capturable_steps():
+    groups = [dict(params=[], exp_avgs=[], exp_avg_sqs=[], grads=[], lr=1e-3) for _ in range(3)]
+    opt = FusedAdamShard(groups, capturable=True)
+    for _ in range(3):
+        opt.step()
+    torch.cuda.synchronize()
+    assert opt.group_steps() == [3, 3, 3]
+    reg = FusedAdamShard(groups, capturable=False)
+    for _ in range(3):
+        reg.step()
+    assert reg.group_steps() == [3, 3, 3]
+
+
+def test_step_once_regular_and_capturable():
+    spec = workloads.large_uniform(n_tensors=3, numel=10_007)
+    for cap in (False, True):
+        shard = workloads.materialize(spec, DEV)
+        osh = helpers.oracle_shard(shard)
+        g = spec.groups[0]
+        lr_dev = torch.tensor([g.lr], device=DEV) if cap else None
+        step_dev = torch.zeros(1, dtype=torch.int32, device=DEV) if cap else None
+        gs_dev = torch.tensor([1.0], device=DEV) if cap else None
+        for k in (1, 2):
+            step_once(shard.params, shard.exp_avgs, shard.exp_avg_sqs, shard.grads, lr=g.lr,
+                      betas=g.betas, eps=g.eps, weight_decay=g.weight_decay, step=k,
+                      lr_dev=lr_dev, step_dev=step_dev, grad_scale_dev=gs_dev)
+            oracle.shard_step(osh, capturable=cap)
+        torch.cuda.synchronize()
+        helpers.compare(shard, osh)
+        if cap:
+            assert step_dev.item() == 2
+
+
+def test_host_gradients_entry_point_matches_device_gradients():
+    spec = workloads.small_versions()["capturable_l2"]
+    a, _, _ = _run(spec, 2, fresh=False)
+    b = workloads.materialize(spec, DEV)
+    ob = FusedAdamShard(b.param_groups(), capturable=True, grad_scale=spec.grad_scale)
+    host = [g.cpu().pin_memory() for g in (b.grads[i] for i in b.plan_order())]
+    for gr in b.grads:
+        gr.zero_()  # the host copy is the only source of the grads
+    steps = [ob.step_from_host(host) for _ in range(2)]
+    assert steps == [[1], [2]]
+    for x, y in zip(helpers.snapshot(a), helpers.snapshot(b)):
+        assert torch.equal(x, y)
+
+
+def test_abi_rejects_bad_calls_without_launching():
+    L = _abi.lib()
+    spec = workloads.large_uniform(n_tensors=2, numel=1000)
+    shard = workloads.materialize(spec, DEV)
+    opt = FusedAdamShard(shard.param_groups(), capturable=True, check_finite=True)
+    snap = helpers.snapshot(shard)
+    # a check-finite plan refuses a missing noop flag, and a misaligned one
+    st = L.fadam_step(opt._plan, None, None)
+    assert st == _abi.EINVAL and b"noop" in L.fadam_last_error()
+    st = L.fadam_step(opt._plan, opt.noop.data_ptr() + 2, None)
+    assert st == _abi.EALIGN
+    torch.cuda.synchronize()
+    assert helpers.state_equal(shard, snap)
+    assert opt.group_steps() == [0] and opt.device_status() == 0
+    # set_groups refuses a different group count
+    grp = (_abi.Group * 2)()
+    assert L.fadam_plan_set_groups(opt._plan, grp, 2) == _abi.EINVAL

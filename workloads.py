@@ -1,0 +1,268 @@
+"""Seeded synthetic shards for the tests and the benchmark.
+
+This module only draws inputs: tensor sizes, layouts and random values.  It
+holds none of the optimizer's arithmetic and is shared by the CUDA-path
+tests, the oracle tests and bench.py, so both sides see the same inputs.
+
+Five shard recipes, all synthetic (no dataset or checkpoint is involved):
+
+1. ``tiny_adamw``: 4 fp32 tensors of 1000, 4097, 65536 and 3 elements
+   (separate allocations, ragged tails) plus one empty group; AdamW,
+   lr 1e-3, betas (0.9, 0.999), eps 1e-8, wd 0.01, host scalars.
+2. ``capturable_l2``: a GPT-style layer list, per layer 4096x4096,
+   4096x11008 (twice), 11008x4096 and two 4096 norm vectors, 8 layers
+   (1,216,413,696 elements); L2 mode, wd 0.1, betas (0.9, 0.95), eps 1e-8,
+   lr 1e-3 and grad_scale 1/65536 on the device, bf16 grads ~ N(0, 1e-2),
+   bf16 param-out copy; one seeded element is set to +inf at one step.
+3. ``large_uniform``: 201 fp32 tensors of 20,971,520 elements (the sizes of
+   the TE issue's adam_bench.py), p ~ N(0,1), g = N(0,1)*1e-3, AdamW,
+   lr 1.6e-3, betas (0.9, 0.95), eps 1e-8, wd 0.1, no param-out copy.
+4. ``remainder_shard``: one contiguous 1.2e9-element bucket cut into 512
+   views of log-uniform size in [4096, 16,777,216] scaled to sum to 1.2e9,
+   view starts rounded up to 64 elements (the 128-byte alignment rule of
+   distributed_fused_adam.py for 16-bit grads); bf16 high half + int16
+   remainder, bf16 grads ~ N(0, 1e-3), AdamW wd 0.1, betas (0.9, 0.95),
+   eps 1e-8, lr 1e-3 on the device; param-out is the bf16 high half itself.
+5. ``many_small``: 20,000 fp32 tensors in their own allocations, 30% of
+   log-uniform size in [1, 4096) and 70% in [4096, 1,048,576], shuffled;
+   group 0 AdamW wd 0.1 (the large ones), group 1 L2 wd 0 (the small ones),
+   group 2 empty; per-group device step counters.
+
+Every recipe takes a ``scale`` that shrinks the sizes for tests that the
+oracle must finish in seconds; ``scale=1`` is the full workload.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional
+
+import numpy as np
+import torch
+
+
+@dataclass
+class GroupSpec:
+    adam_w_mode: bool = True
+    lr: float = 1e-3
+    betas: tuple = (0.9, 0.999)
+    eps: float = 1e-8
+    weight_decay: float = 0.0
+    bias_correction: bool = True
+
+    def as_dict(self) -> Dict:
+        return dict(adam_w_mode=self.adam_w_mode, lr=self.lr, betas=self.betas, eps=self.eps,
+                    weight_decay=self.weight_decay, bias_correction=self.bias_correction)
+
+
+@dataclass
+class ShardSpec:
+    name: str
+    groups: List[GroupSpec]
+    sizes: List[int]                 # elements per tensor
+    group_of: List[int]              # param group of each tensor
+    g_dtype: torch.dtype = torch.float32
+    out_dtype: Optional[torch.dtype] = None
+    remainders: bool = False
+    capturable: bool = False
+    grad_std: float = 1e-3
+    grad_scale: float = 1.0
+    bucket_offsets: Optional[List[int]] = None  # views into one bucket (remainder shard)
+    bucket_len: int = 0
+    seed: int = 0
+    inf_at_step: Optional[int] = None  # step (1-based) whose grad holds one +inf
+    notes: Dict = field(default_factory=dict)
+
+    @property
+    def n_elements(self) -> int:
+        return int(sum(self.sizes))
+
+
+def _log_uniform(rng: np.random.Generator, lo: float, hi: float, n: int) -> np.ndarray:
+    return np.exp(rng.uniform(math.log(lo), math.log(hi), size=n))
+
+
+def tiny_adamw(seed: int = 1235) -> ShardSpec:
+    g = GroupSpec(adam_w_mode=True, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01)
+    return ShardSpec("tiny_adamw", [g, GroupSpec()], [1000, 4097, 65536, 3], [0, 0, 0, 0],
+                     grad_std=1e-3, seed=seed)
+
+
+def capturable_l2(layers: int = 8, hidden: int = 4096, ffn: int = 11008,
+                  seed: int = 1236) -> ShardSpec:
+    per_layer = [hidden * hidden, hidden * ffn, hidden * ffn, ffn * hidden, hidden, hidden]
+    sizes = per_layer * layers
+    g = GroupSpec(adam_w_mode=False, lr=1e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1)
+    return ShardSpec("capturable_l2", [g], sizes, [0] * len(sizes), g_dtype=torch.bfloat16,
+                     out_dtype=torch.bfloat16, capturable=True, grad_std=1e-2,
+                     grad_scale=1.0 / 65536, seed=seed, inf_at_step=3)
+
+
+def large_uniform(n_tensors: int = 201, numel: int = 320 * 65536, seed: int = 1237) -> ShardSpec:
+    g = GroupSpec(adam_w_mode=True, lr=1.6e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1)
+    return ShardSpec("large_uniform", [g], [numel] * n_tensors, [0] * n_tensors,
+                     grad_std=1e-3, seed=seed)
+
+
+def remainder_shard(total: int = 1_200_000_000, n_views: int = 512, lo: int = 4096,
+                    hi: int = 16_777_216, align: int = 64, seed: int = 1238) -> ShardSpec:
+    rng = np.random.default_rng(seed)
+    raw = _log_uniform(rng, lo, hi, n_views)
+    sizes = np.maximum(1, np.round(raw * (total / raw.sum()))).astype(np.int64)
+    sizes[-1] += total - int(sizes.sum())
+    offsets, pos = [], 0
+    for s in sizes:
+        pos = (pos + align - 1) // align * align
+        offsets.append(pos)
+        pos += int(s)
+    g = GroupSpec(adam_w_mode=True, lr=1e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1)
+    return ShardSpec("remainder_shard", [g], [int(s) for s in sizes], [0] * n_views,
+                     g_dtype=torch.bfloat16, out_dtype=torch.bfloat16, remainders=True,
+                     capturable=True, grad_std=1e-3, bucket_offsets=offsets, bucket_len=pos,
+                     seed=seed)
+
+
+def many_small(n_tensors: int = 20_000, frac_small: float = 0.3, small_hi: int = 4096,
+               large_hi: int = 1_048_576, seed: int = 1239) -> ShardSpec:
+    rng = np.random.default_rng(seed)
+    n_small = int(round(n_tensors * frac_small))
+    small = np.floor(_log_uniform(rng, 1, small_hi, n_small)).astype(np.int64)
+    large = np.floor(_log_uniform(rng, small_hi, large_hi, n_tensors - n_small)).astype(np.int64)
+    sizes = np.concatenate([small, large])
+    rng.shuffle(sizes)
+    sizes = np.clip(sizes, 1, large_hi)
+    group_of = [0 if s >= small_hi else 1 for s in sizes]
+    g0 = GroupSpec(adam_w_mode=True, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.1)
+    g1 = GroupSpec(adam_w_mode=False, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.0)
+    g2 = GroupSpec(adam_w_mode=True, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.1)
+    return ShardSpec("many_small", [g0, g1, g2], [int(s) for s in sizes], group_of,
+                     capturable=True, grad_std=1e-3, seed=seed)
+
+
+def small_versions() -> Dict[str, ShardSpec]:
+    """The same recipes at sizes the oracle finishes in seconds (several
+    CTAs' worth of work each, ragged tails included)."""
+    return {
+        "tiny_adamw": tiny_adamw(),
+        "capturable_l2": capturable_l2(layers=2, hidden=256, ffn=688),
+        "large_uniform": large_uniform(n_tensors=6, numel=65536 * 3 + 5),
+        "remainder_shard": remainder_shard(total=3_000_000, n_views=64, lo=64, hi=200_000),
+        "many_small": many_small(n_tensors=2000, large_hi=65536),
+    }
+
+
+def full_versions() -> Dict[str, ShardSpec]:
+    return {"tiny_adamw": tiny_adamw(), "capturable_l2": capturable_l2(),
+            "large_uniform": large_uniform(), "remainder_shard": remainder_shard(),
+            "many_small": many_small()}
+
+
+# ---- materialising a shard ----------------------------------------------------
+
+@dataclass
+class Shard:
+    """Tensors of one shard, per group, in plan order."""
+    spec: ShardSpec
+    params: List[torch.Tensor]
+    exp_avgs: List[torch.Tensor]
+    exp_avg_sqs: List[torch.Tensor]
+    grads: List[torch.Tensor]
+    params_out: List[Optional[torch.Tensor]]
+    remainders: List[Optional[torch.Tensor]]
+    buckets: Dict[str, torch.Tensor] = field(default_factory=dict)
+
+    def param_groups(self) -> List[Dict]:
+        """The per-group dicts FusedAdamShard takes."""
+        out = []
+        for gi, gs in enumerate(self.spec.groups):
+            idx = [i for i, g in enumerate(self.spec.group_of) if g == gi]
+            d = gs.as_dict()
+            d["params"] = [self.params[i] for i in idx]
+            d["exp_avgs"] = [self.exp_avgs[i] for i in idx]
+            d["exp_avg_sqs"] = [self.exp_avg_sqs[i] for i in idx]
+            d["grads"] = [self.grads[i] for i in idx]
+            if self.spec.out_dtype is not None:
+                d["params_out"] = [self.params_out[i] for i in idx]
+            if self.spec.remainders:
+                d["remainders"] = [self.remainders[i] for i in idx]
+            out.append(d)
+        return out
+
+    def plan_order(self) -> List[int]:
+        """Tensor indices in the order FusedAdamShard hands them to the plan."""
+        return [i for gi in range(len(self.spec.groups))
+                for i, g in enumerate(self.spec.group_of) if g == gi]
+
+
+def materialize(spec: ShardSpec, device="cuda") -> Shard:
+    """Draw the shard's tensors on `device` from the spec's seed.
+
+    p ~ N(0, 1) (for the remainder form: the bf16 rounding of such a draw as
+    the high half and a uniform int16 remainder), m = v = 0, and
+    g ~ N(0, grad_std^2) in the grad dtype.
+    """
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(spec.seed)
+    n = len(spec.sizes)
+    params, ms, vs, gs, outs, rems = [], [], [], [], [], []
+    buckets: Dict[str, torch.Tensor] = {}
+    if spec.bucket_offsets is not None:
+        L = spec.bucket_len
+        buckets["p"] = torch.zeros(L, dtype=torch.bfloat16, device=dev)
+        buckets["rem"] = torch.zeros(L, dtype=torch.int16, device=dev)
+        buckets["m"] = torch.zeros(L, dtype=torch.float32, device=dev)
+        buckets["v"] = torch.zeros(L, dtype=torch.float32, device=dev)
+        buckets["g"] = torch.zeros(L, dtype=spec.g_dtype, device=dev)
+    for i in range(n):
+        s = spec.sizes[i]
+        if spec.bucket_offsets is not None:
+            o = spec.bucket_offsets[i]
+            p = buckets["p"][o:o + s]
+            r = buckets["rem"][o:o + s]
+            m = buckets["m"][o:o + s]
+            v = buckets["v"][o:o + s]
+            g = buckets["g"][o:o + s]
+        else:
+            p = torch.empty(s, dtype=torch.bfloat16 if spec.remainders else torch.float32,
+                            device=dev)
+            r = torch.empty(s, dtype=torch.int16, device=dev) if spec.remainders else None
+            m = torch.zeros(s, dtype=torch.float32, device=dev)
+            v = torch.zeros(s, dtype=torch.float32, device=dev)
+            g = torch.empty(s, dtype=spec.g_dtype, device=dev)
+        if spec.remainders:
+            p.copy_(torch.randn(s, generator=gen, device=dev).to(torch.bfloat16))
+            r.copy_(torch.randint(-32768, 32768, (s,), generator=gen, device=dev,
+                                  dtype=torch.int32).to(torch.int16))
+        else:
+            p.copy_(torch.randn(s, generator=gen, device=dev))
+        g.copy_((torch.randn(s, generator=gen, device=dev) * spec.grad_std).to(spec.g_dtype))
+        params.append(p)
+        ms.append(m)
+        vs.append(v)
+        gs.append(g)
+        rems.append(r)
+        if spec.remainders:
+            outs.append(p)  # the new high half replaces the bf16 param in place
+        elif spec.out_dtype is not None:
+            outs.append(torch.zeros(s, dtype=spec.out_dtype, device=dev))
+        else:
+            outs.append(None)
+    return Shard(spec, params, ms, vs, gs, outs, rems, buckets)
+
+
+def inf_position(spec: ShardSpec) -> tuple:
+    """(tensor index, element index) of the seeded +inf gradient."""
+    rng = np.random.default_rng(spec.seed + 77)
+    t = int(rng.integers(0, len(spec.sizes)))
+    return t, int(rng.integers(0, spec.sizes[t]))
+
+
+def fresh_grads(shard: Shard, step: int) -> None:
+    """Redraw every gradient in place for `step` (same recipe, new seed)."""
+    spec = shard.spec
+    dev = shard.grads[0].device if shard.grads else torch.device("cpu")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(spec.seed * 7919 + step)
+    for g in shard.grads:
+        g.copy_((torch.randn(g.numel(), generator=gen, device=dev) * spec.grad_std).to(g.dtype))
