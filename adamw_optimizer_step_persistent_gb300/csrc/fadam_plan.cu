@@ -103,7 +103,7 @@ fadam_status check_dtypes(const Dtypes& d, uint32_t flags) {
 }
 
 fadam_status check_groups(const fadam_group* groups, int32_t n_groups, uint32_t flags,
-                          const std::vector<char>& has_tensor) {
+                          const std::vector<char>& has_tensor, bool check_host_step) {
   if (n_groups < 1 || n_groups > FADAM_MAX_GROUPS)
     return fail(FADAM_EINVAL, "n_groups %d outside 1..%d", n_groups, FADAM_MAX_GROUPS);
   if (!groups) return fail(FADAM_EINVAL, "groups is NULL");
@@ -132,7 +132,7 @@ fadam_status check_groups(const fadam_group* groups, int32_t n_groups, uint32_t 
     } else {
       if (!finite(g.lr) || !finite(g.grad_scale))
         return fail(FADAM_EINVAL, "group %d: lr or grad_scale is not finite", i);
-      if (g.bias_correction == 1 && g.step < 1)
+      if (check_host_step && g.bias_correction == 1 && g.step < 1)
         return fail(FADAM_EINVAL, "group %d: step %d < 1 with bias correction (1-beta^step = 0)",
                     i, g.step);
     }
@@ -226,9 +226,13 @@ void pack(const fadam_tensor* ts, int64_t n, const Dtypes& d, int grid,
     if (h > 0) pieces.push_back({i, 0, std::min(h, len), false});
     if (len > h) pieces.push_back({i, h, len - h, true});
   }
+  // Total cost, counting the overhead of every item the cuts can add (one
+  // per CTA boundary plus the kMaxItem splits): overestimating only leaves
+  // the last CTA a little short, underestimating would make it a straggler.
   const double bpe = bytes_per_elem(d);
-  double total = 0;
-  for (const Piece& p : pieces) total += p.n * bpe + kItemOverhead;
+  double total = kItemOverhead * (grid - 1);
+  for (const Piece& p : pieces)
+    total += p.n * bpe + kItemOverhead * double((p.n + kMaxItem - 1) / kMaxItem);
   const double quota = total / grid;
 
   items.clear();
@@ -343,7 +347,8 @@ struct HostPlan {
 // Checks, device query and packing shared by fadam_plan_create and
 // fadam_step_once.  Allocates no device memory.
 fadam_status prepare(const fadam_tensor* tensors, int64_t n_tensors, const fadam_group* groups,
-                     int32_t n_groups, const Dtypes& d, uint32_t flags, HostPlan& hp) {
+                     int32_t n_groups, const Dtypes& d, uint32_t flags, bool check_host_step,
+                     HostPlan& hp) {
   fadam_status st = check_dtypes(d, flags);
   if (st) return st;
   if (n_groups < 1 || n_groups > FADAM_MAX_GROUPS)
@@ -351,7 +356,7 @@ fadam_status prepare(const fadam_tensor* tensors, int64_t n_tensors, const fadam
   std::vector<char> has_tensor(n_groups, 0);
   st = check_tensors(tensors, n_tensors, n_groups, d, has_tensor);
   if (st) return st;
-  st = check_groups(groups, n_groups, flags, has_tensor);
+  st = check_groups(groups, n_groups, flags, has_tensor, check_host_step);
   if (st) return st;
 
   hp.d = d;
@@ -462,7 +467,8 @@ fadam_status fadam_plan_create(const fadam_tensor* tensors, int64_t n_tensors,
   const Dtypes d{p_dtype, g_dtype, out_dtype, (flags & FADAM_REMAINDERS) != 0};
   fadam_plan* plan = new (std::nothrow) fadam_plan();
   if (!plan) return fail(FADAM_EINVAL, "out of host memory");
-  fadam_status st = prepare(tensors, n_tensors, groups, n_groups, d, flags, plan->hp);
+  // the host step of a regular plan is per-step data: checked at launch
+  fadam_status st = prepare(tensors, n_tensors, groups, n_groups, d, flags, false, plan->hp);
   if (st) {
     delete plan;
     return st;
@@ -502,7 +508,7 @@ fadam_status fadam_plan_set_groups(fadam_plan* plan, const fadam_group* groups, 
   std::vector<char> has_tensor(n_groups, 0);
   for (const fadam_tensor& t : plan->tensors)
     if (t.numel > 0) has_tensor[t.group] = 1;
-  const fadam_status st = check_groups(groups, n_groups, plan->hp.flags, has_tensor);
+  const fadam_status st = check_groups(groups, n_groups, plan->hp.flags, has_tensor, false);
   if (st) return st;
   plan->groups.assign(groups, groups + n_groups);
   return FADAM_OK;
@@ -516,6 +522,11 @@ fadam_status fadam_step(fadam_plan* plan, int32_t* noop_dev, fadam_stream stream
   if (noop_dev && reinterpret_cast<uintptr_t>(noop_dev) % 4)
     return fail(FADAM_EALIGN, "noop_dev is not 4-byte aligned");
   if (!needs_launch(hp)) return FADAM_OK;
+  if (!(hp.flags & FADAM_CAPTURABLE))
+    for (int32_t i = 0; i < plan->n_groups; ++i)
+      if (plan->groups[i].bias_correction == 1 && plan->groups[i].step < 1)
+        return fail(FADAM_EINVAL, "group %d: step %d < 1 with bias correction (1-beta^step = 0)",
+                    i, plan->groups[i].step);
   DeviceGuard guard(hp.device);
   if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
   KParams kp;
@@ -638,7 +649,7 @@ fadam_status fadam_step_once(const fadam_tensor* tensors, int64_t n_tensors, int
     return fail(FADAM_EALIGN, "noop_dev is not 4-byte aligned");
   HostPlan hp;
   const Dtypes d{FADAM_DT_F32, g_dtype, out_dtype, false};
-  fadam_status st = prepare(tensors, n_tensors, &grp, 1, d, flags, hp);
+  fadam_status st = prepare(tensors, n_tensors, &grp, 1, d, flags, true, hp);
   if (st) return st;
   if (!needs_launch(hp)) return FADAM_OK;
   DeviceGuard guard(hp.device);

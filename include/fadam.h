@@ -123,7 +123,8 @@ typedef struct {
  *   beta1, beta2     in [0, 1)
  *   eps              >= 0;  weight_decay: finite
  * Regular plans read the host scalars lr, grad_scale and step (the step
- * already advanced for this update, >= 1 when bias correction is on).
+ * already advanced for this update, >= 1 when bias correction is on;
+ * fadam_step checks it, since a plan is normally made before the first step).
  * Capturable plans read lr_dev, grad_scale_dev (fp32) and step_dev (int32)
  * instead; step_dev is required for every group, empty or not, and groups
  * may share one counter (it then advances once per step).  lr_dev and
