@@ -101,7 +101,7 @@ class Report:
         want = want.astype(np.float64)
         both_nan = np.isnan(got) & np.isnan(want)
         d = np.where(both_nan, 0.0, np.abs(got - want))
-        lim = RTOL * np.abs(want) + ATOL
+        lim = np.where(both_nan, 0.0, RTOL * np.abs(want) + ATOL)
         bad = ~(d <= lim)
         if bad.any():
             k = int(np.argmax(bad))

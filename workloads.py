@@ -197,8 +197,9 @@ class Shard:
 def materialize(spec: ShardSpec, device="cuda") -> Shard:
     """Draw the shard's tensors on `device` from the spec's seed.
 
-    p ~ N(0, 1) (for the remainder form: the bf16 rounding of such a draw as
-    the high half and a uniform int16 remainder), m = v = 0, and
+    p ~ N(0, 1) (for the remainder form: the bf16 rounding of such a draw,
+    zero replaced by one, as the high half and a uniform int16 remainder),
+    m = v = 0, and
     g ~ N(0, grad_std^2) in the grad dtype.
     """
     dev = torch.device(device)
@@ -231,7 +232,11 @@ def materialize(spec: ShardSpec, device="cuda") -> Shard:
             v = torch.zeros(s, dtype=torch.float32, device=dev)
             g = torch.empty(s, dtype=spec.g_dtype, device=dev)
         if spec.remainders:
-            p.copy_(torch.randn(s, generator=gen, device=dev).to(torch.bfloat16))
+            hi = torch.randn(s, generator=gen, device=dev).to(torch.bfloat16)
+            # a zero high half with a negative remainder is the split of no
+            # finite master (it packs to a NaN pattern): draw nonzero halves
+            hi[hi == 0] = 1.0
+            p.copy_(hi)
             r.copy_(torch.randint(-32768, 32768, (s,), generator=gen, device=dev,
                                   dtype=torch.int32).to(torch.int16))
         else:
