@@ -736,3 +736,99 @@ const char* fadam_last_error(void) { return t_last_error.c_str(); }
 int32_t fadam_version(void) { return 10000; }
 
 }  // extern "C"
+
+// ---- one-call step without device allocation ----------------------------------
+//
+// The plan path keeps its work list and status block in memory it allocates
+// with cudaMalloc.  fadam_step_noalloc keeps them instead in one file-scope
+// device array, g_noalloc_arena, that every GPU loading this library holds
+// until the process exits.  Host code never uses the array's name as an
+// address: its device address is looked up once per device with
+// cudaGetSymbolAddress and handed to the kernel.
+
+#include <mutex>
+
+namespace {
+
+constexpr int64_t kNoAllocMaxItems = 4096;
+constexpr int32_t kNoAllocMaxCtas = 2048;
+constexpr size_t kArenaScratchOff = 0;
+constexpr size_t kArenaCtaOff = 256;
+constexpr size_t kArenaItemsOff =
+    kArenaCtaOff + ((size_t(kNoAllocMaxCtas) + 1) * sizeof(int32_t) + 255) / 256 * 256;
+constexpr size_t kArenaBytes = kArenaItemsOff + size_t(kNoAllocMaxItems) * sizeof(Item);
+static_assert(sizeof(KScratch) <= kArenaCtaOff, "status block fits its slot");
+
+constexpr int kMaxDevices = 64;
+std::mutex g_arena_mutex;
+void* g_arena_ptr[kMaxDevices] = {};
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_arena[kArenaBytes];
+
+namespace {
+
+// Device address of g_noalloc_arena on `dev` (which must be current),
+// looked up on the first call for that device.
+fadam_status arena_address(int dev, unsigned char** out) {
+  if (dev < 0 || dev >= kMaxDevices) return fail(FADAM_ELIMIT, "device %d beyond %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_arena_mutex);
+  if (!g_arena_ptr[dev]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_arena);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(g_noalloc_arena)");
+    g_arena_ptr[dev] = ptr;
+  }
+  *out = static_cast<unsigned char*>(g_arena_ptr[dev]);
+  return FADAM_OK;
+}
+
+}  // namespace
+
+extern "C" fadam_status fadam_step_noalloc(const fadam_tensor* tensors, int64_t n_tensors,
+                                           const fadam_group* groups, int32_t n_groups,
+                                           int32_t p_dtype, int32_t g_dtype, int32_t out_dtype,
+                                           uint32_t flags, int32_t* noop_dev,
+                                           fadam_stream stream) {
+  t_last_error.clear();
+  const Dtypes d{p_dtype, g_dtype, out_dtype, (flags & FADAM_REMAINDERS) != 0};
+  if ((flags & FADAM_CHECK_FINITE) && !noop_dev)
+    return fail(FADAM_EINVAL, "FADAM_CHECK_FINITE needs a noop_dev flag to write");
+  if (noop_dev && reinterpret_cast<uintptr_t>(noop_dev) % 4)
+    return fail(FADAM_EALIGN, "noop_dev is not 4-byte aligned");
+  HostPlan hp;
+  fadam_status st = prepare(tensors, n_tensors, groups, n_groups, d, flags, true, hp);
+  if (st) return st;
+  if (static_cast<int64_t>(hp.items.size()) > kNoAllocMaxItems)
+    return fail(FADAM_ELIMIT,
+                "fadam_step_noalloc: the shard packs into %zu work items, more than the %lld its "
+                "static device array holds; use fadam_plan_create/fadam_step",
+                hp.items.size(), (long long)kNoAllocMaxItems);
+  if (hp.grid > kNoAllocMaxCtas)
+    return fail(FADAM_ELIMIT, "fadam_step_noalloc: grid of %d CTAs exceeds %d", hp.grid,
+                kNoAllocMaxCtas);
+  if (!needs_launch(hp)) return FADAM_OK;
+  DeviceGuard guard(hp.device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  unsigned char* arena = nullptr;
+  st = arena_address(hp.device, &arena);
+  if (st) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Item* items = reinterpret_cast<Item*>(arena + kArenaItemsOff);
+  int32_t* cta = reinterpret_cast<int32_t*>(arena + kArenaCtaOff);
+  KScratch* scratch = reinterpret_cast<KScratch*>(arena + kArenaScratchOff);
+  cudaError_t e = cudaSuccess;
+  if (!hp.items.empty())
+    e = cudaMemcpyAsync(items, hp.items.data(), hp.items.size() * sizeof(Item),
+                        cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(cta, hp.cta_begin.data(), hp.cta_begin.size() * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, s);
+  // the counters and the status word must start at zero on every call
+  if (e == cudaSuccess) e = cudaMemsetAsync(scratch, 0, sizeof(KScratch), s);
+  if (e != cudaSuccess) return cuda_fail(e, "fadam_step_noalloc upload");
+  KParams kp;
+  fill_params(kp, items, cta, noop_dev, scratch, groups, n_groups, flags);
+  return launch(hp.kernel, kp, hp.grid, (flags & FADAM_CHECK_FINITE) != 0, s);
+}

@@ -240,6 +240,38 @@ fadam_status fadam_step_once(const fadam_tensor* tensors, int64_t n_tensors, int
                              const float* grad_scale_dev, int32_t* noop_dev,
                              int32_t g_dtype, int32_t out_dtype, fadam_stream stream);
 
+/* Step without any device allocation (no counterpart on the pages: this
+ * entry point exists for callers of this library, not for the method).
+ *
+ * Some callers cannot call cudaMalloc: code running while a framework's
+ * caching allocator has reserved nearly all device memory (a direct
+ * cudaMalloc can fail there), code inside another library's hooks that may
+ * only use memory handed to it, and latency-critical loops where
+ * cudaMalloc/cudaFree could synchronise the device.  This call packs the
+ * shard on the host, as fadam_plan_create does, and runs one step as
+ * fadam_step does, but keeps the work list and the status block in a
+ * static device array instead of allocated memory: about 264 KB that every
+ * GPU which loads this library holds until the process exits.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Limits: at most 4096 work items (roughly one per tensor plus one per CTA
+ * of the grid) and 2048 CTAs; a larger shard is rejected with FADAM_ELIMIT
+ * and a message from fadam_last_error(), before any device work.
+ * Arguments: as fadam_plan_create, plus noop_dev and stream as fadam_step;
+ * the step counters behave as in fadam_step.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any
+ * stream capture.  Each call copies its work list into the array and
+ * clears the status block on `stream` before the launch.  All calls share
+ * the one array and it keeps the last call's contents: calls whose work
+ * overlaps on the GPU (unordered streams, or concurrent host threads) race,
+ * so issue them in order on one stream.  Errors: as fadam_plan_create and
+ * fadam_step, FADAM_ELIMIT beyond the limits above. */
+fadam_status fadam_step_noalloc(const fadam_tensor* tensors, int64_t n_tensors,
+                                const fadam_group* groups, int32_t n_groups, int32_t p_dtype,
+                                int32_t g_dtype, int32_t out_dtype, uint32_t flags,
+                                int32_t* noop_dev, fadam_stream stream);
+
 /* One work item of a dry-run packing (see fadam_pack_dry). */
 typedef struct {
   int64_t tensor; /* index into the tensors array */
