@@ -44,7 +44,8 @@ class Group(ctypes.Structure):
 class PlanInfo(ctypes.Structure):
     """fadam_plan_info."""
     _fields_ = [("n_tensors", ctypes.c_int64), ("n_elements", ctypes.c_int64),
-                ("n_items", ctypes.c_int64), ("grid", ctypes.c_int32), ("block", ctypes.c_int32),
+                ("n_items", ctypes.c_int64), ("n_chunks", ctypes.c_int64),
+                ("grid", ctypes.c_int32), ("block", ctypes.c_int32),
                 ("blocks_per_sm", ctypes.c_int32), ("sm_count", ctypes.c_int32),
                 ("n_groups", ctypes.c_int32), ("device", ctypes.c_int32),
                 ("bytes_per_step", ctypes.c_double), ("check_bytes_per_step", ctypes.c_double)]

@@ -36,27 +36,33 @@ def _nvcc() -> str:
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
     deps.append(os.path.join(INCLUDE, "fadam.h"))
     deps.append(os.path.abspath(__file__))
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link libfadam.so if it is missing or out of date."""
-    if not force and not _stale():
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, defines=(), lib: str = LIB) -> str:
+    """Compile and link libfadam.so if it is missing or out of date.
+
+    `defines` (e.g. ["FADAM_UNROLL=4"]) override the kernel's compile-time
+    tuning defaults; `lib` puts such a build elsewhere.
+    """
+    if not force and not defines and not _stale(lib):
+        return lib
+    out_dir = os.path.dirname(os.path.abspath(lib))
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if os.environ.get("FADAM_PTXAS_VERBOSE") == "1" else []
+    extra += [f"-D{d}" for d in defines]
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(out_dir, os.path.splitext(src)[0] + ".o")
         objs.append(obj)
         cmd = [nvcc, *NVCC_FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c",
                os.path.join(CSRC, src), "-o", obj]
@@ -73,12 +79,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
             failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-shared",
            "-Xcompiler", "-fPIC", *objs, "-o", tmp]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -10,7 +10,10 @@
 namespace fadam {
 
 // Threads per CTA of the update kernel.
-constexpr int kBlock = 256;
+#ifndef FADAM_BLOCK
+#define FADAM_BLOCK 1024
+#endif
+constexpr int kBlock = FADAM_BLOCK;
 // Elements per vector access (one 16-byte fp32 vector).
 constexpr int kVec = 4;
 // Largest work item, in elements (keeps in-item indices in 32 bits).
@@ -18,8 +21,14 @@ constexpr int64_t kMaxItem = int64_t(1) << 26;
 // Work items are cut at multiples of this many elements.
 constexpr int64_t kCutQuantum = 32;
 
+// Tiles of the bulk pipeline: kBlock 4-element vectors each (one per
+// thread); a chunk, the unit CTAs pull from the shared work counter, is at
+// most kChunkTiles tiles of one item.
+constexpr int kChunkTiles = 16;
+
 // Item flags.
-constexpr uint16_t kItemVec = 1;  // every stream is vector-aligned at the item start
+constexpr uint16_t kItemVec = 1;   // every stream is aligned to one 4-element vector
+constexpr uint16_t kItemBulk = 2;  // ... and to 16 bytes (bulk copies allowed)
 
 // One contiguous run of one tensor: pointers already offset to the run start.
 struct alignas(16) Item {
@@ -31,7 +40,7 @@ struct alignas(16) Item {
   int16_t* rem;
   int32_t n;        // elements in the run
   uint16_t group;   // param group
-  uint16_t flags;   // kItemVec
+  uint16_t flags;   // kItemVec, kItemBulk
 };
 static_assert(sizeof(Item) == 64, "Item is one 64-byte record");
 
@@ -54,11 +63,23 @@ struct alignas(16) KGroup {
 static_assert(sizeof(KGroup) == 64, "KGroup is one 64-byte record");
 
 // Per-plan device status block.
+// One chunk of bulk tiles: tiles [tile0, tile0 + ntiles) of item `item`.
+struct alignas(16) Chunk {
+  int32_t item;
+  int32_t tile0;
+  int32_t ntiles;
+  int32_t reserved;
+};
+
 struct KScratch {
-  unsigned int done;       // CTAs finished in the current launch (last one resets)
-  unsigned int bar_count;  // grid barrier arrivals
-  unsigned int bar_gen;    // grid barrier generation
-  int status;              // FADAM_OK or FADAM_ETIMEOUT
+  unsigned int done;         // CTAs finished in the current launch (last one resets all)
+  unsigned int bar_count;    // grid barrier arrivals
+  unsigned int bar_gen;      // grid barrier generation
+  int status;                // FADAM_OK or FADAM_ETIMEOUT
+  unsigned int next_update;  // next chunk of the update's bulk pass
+  unsigned int next_scan;    // next chunk of the inf/nan screen's bulk pass
+  unsigned int next_tail_update;  // next item whose tail the update takes
+  unsigned int next_tail_scan;    // next item whose tail the screen takes
 };
 
 // Kernel flags.
@@ -72,17 +93,25 @@ struct alignas(16) KParams {
   const int32_t* cta_begin;  // grid+1 entries: CTA b runs items [cta_begin[b], cta_begin[b+1])
   int32_t* noop;             // may be null
   KScratch* scratch;
+  const Chunk* chunks;       // bulk tiles, pulled dynamically by the CTAs
+  int32_t n_chunks;
   int32_t n_groups;
   uint32_t flags;
-  int64_t reserved;
+  int32_t reserved;
   KGroup groups[FADAM_MAX_GROUPS];
 };
 
-// Kernel entry for the (g dtype, out dtype, remainders) combination, or
-// null when the combination does not exist.  Defined per g dtype in
+// A kernel and the dynamic shared memory (bulk-copy tiles) it launches with.
+struct KernelEntry {
+  const void* fn;
+  size_t smem;
+};
+
+// Kernel entry for the (g dtype, out dtype, remainders) combination, or a
+// null fn when the combination does not exist.  Defined per g dtype in
 // fadam_kernels_g{f32,bf16,f16}.cu.
-const void* kernel_gf32(int out_dtype, bool remainders);
-const void* kernel_gbf16(int out_dtype, bool remainders);
-const void* kernel_gf16(int out_dtype, bool remainders);
+KernelEntry kernel_gf32(int out_dtype, bool remainders);
+KernelEntry kernel_gbf16(int out_dtype, bool remainders);
+KernelEntry kernel_gf16(int out_dtype, bool remainders);
 
 }  // namespace fadam

@@ -6,14 +6,25 @@
 //   1. prologue: each param group's scalars are read once (host values for
 //      regular plans, device values for capturable ones) and the bias
 //      corrections 1 - beta^step are computed once, into shared memory;
-//   2. optional inf/nan screen of g*grad_scale over the CTA's items, then a
-//      bounded grid barrier (cooperative launch), then the noop flag is read;
-//   3. the update: per item, 128-bit streaming loads of p, m, v and g for
-//      kUnroll vectors per thread, all issued before any arithmetic, then
-//      the element math and 128-bit streaming stores; a scalar loop takes
-//      the ragged tail and runs whose pointers are not vector-aligned;
-//   4. capturable plans: the last CTA to finish advances each step counter
-//      by (noop != 1).
+//   2. optional inf/nan screen of g*grad_scale over the CTA's items (the
+//      same two passes, copying only g), then a bounded grid barrier
+//      (cooperative launch), then the noop flag is read;
+//   3. the update, in two passes.  The bulk pass treats every
+//      16-byte-aligned item as tiles of kTile 4-element vectors, grouped in
+//      chunks of up to kChunkTiles tiles that the CTAs pull from one
+//      launch-wide counter (so an SM that gets more bandwidth takes more
+//      chunks).  In each CTA thread 0 copies the tiles of p, m, v, g (and
+//      the remainders) into shared memory with cp.async.bulk, kStages tiles
+//      ahead and across chunk boundaries, each tile completing on its own
+//      mbarrier; every thread updates one vector of the tile from shared
+//      memory and writes the results straight to global memory with
+//      streaming 128-bit stores.  A tail pass then takes the at most 7
+//      trailing elements of every bulk item (warps pull 32 items at a time
+//      from another counter, one item per lane), and the rest pass the
+//      CTA's statically assigned items that are not 16-byte aligned, with
+//      the whole CTA (128-bit streaming loads, then element by element);
+//   4. the last CTA to finish resets the work counters and, for capturable
+//      plans, advances each step counter by (noop != 1).
 //
 // Element math follows "Enhance Distributed Fused Adam (#1794)",
 // DistAdamCapturableFunctor::local_step, one IEEE fp32 operation per step
@@ -32,10 +43,26 @@
 
 namespace fadam {
 
-// Vectors per thread per iteration of the aligned loop.
-constexpr int kUnroll = 2;
-// Iterations of the grid-barrier wait before it gives up (about a second).
-constexpr unsigned kBarrierSpinLimit = 1u << 21;
+// Vectors per thread per iteration of the 128-bit load loop.
+#ifndef FADAM_UNROLL
+#define FADAM_UNROLL 1
+#endif
+constexpr int kUnroll = FADAM_UNROLL;
+// Resident CTAs per SM the register allocation must allow (unset: let the
+// compiler choose; an explicit 1 changes its choice).
+#ifdef FADAM_MIN_BLOCKS
+#define FADAM_BOUNDS __launch_bounds__(kBlock, FADAM_MIN_BLOCKS)
+#else
+#define FADAM_BOUNDS __launch_bounds__(kBlock)
+#endif
+// Wall time after which a grid-barrier or mbarrier wait gives up.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 // ---- scalar state -----------------------------------------------------------
 
@@ -136,6 +163,17 @@ __device__ __forceinline__ void store_out1(void* base, int i, float x) {
   }
 }
 
+__device__ __forceinline__ void unpack4(const uint2& r, unsigned short (&o)[4]) {
+  o[0] = static_cast<unsigned short>(r.x & 0xFFFFu);
+  o[1] = static_cast<unsigned short>(r.x >> 16);
+  o[2] = static_cast<unsigned short>(r.y & 0xFFFFu);
+  o[3] = static_cast<unsigned short>(r.y >> 16);
+}
+
+__device__ __forceinline__ uint2 pack4(const unsigned short (&h)[4]) {
+  return make_uint2(h[0] | (static_cast<unsigned>(h[1]) << 16), h[2] | (static_cast<unsigned>(h[3]) << 16));
+}
+
 // ---- the update of one element ---------------------------------------------
 
 // p' for the fp32 master x; m and v are updated in place.
@@ -171,143 +209,434 @@ __device__ __forceinline__ void rem_split(float x, unsigned short& hi, unsigned 
   hi = static_cast<unsigned short>((b >> 16) + (rem_bits >> 15));
 }
 
-// ---- one work item ------------------------------------------------------------
-
+// One 4-element vector of the fp32-master form, in registers.
 template <bool ADAMW, int GT, int OT>
-__device__ __forceinline__ void run_item_f32(const Item& it, const Scal& s) {
-  const int n = it.n;
-  int scalar_from = 0;
-  if (it.flags & kItemVec) {
-    const int nv = n / kVec;
-    float4* p4 = reinterpret_cast<float4*>(it.p);
-    float4* m4 = reinterpret_cast<float4*>(it.m);
-    float4* v4 = reinterpret_cast<float4*>(it.v);
-    for (int base = threadIdx.x; base < nv; base += kBlock * kUnroll) {
-      float4 P[kUnroll], M[kUnroll], V[kUnroll];
-      typename Raw4<GT>::T G[kUnroll];
+__device__ __forceinline__ void update4_f32(float4 P, float4 M, float4 V,
+                                            const typename Raw4<GT>::T& G, const Scal& s,
+                                            float4* p4, float4* m4, float4* v4, void* out, int i) {
+  float g[4];
+  widen4<GT>(G, g);
+  float x[4] = {P.x, P.y, P.z, P.w};
+  float m[4] = {M.x, M.y, M.z, M.w};
+  float v[4] = {V.x, V.y, V.z, V.w};
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int i = base + u * kBlock;
-        if (i < nv) {
-          P[u] = __ldcs(p4 + i);
-          M[u] = __ldcs(m4 + i);
-          V[u] = __ldcs(v4 + i);
-          G[u] = load4<GT>(it.g, i);
-        }
-      }
+  for (int e = 0; e < 4; ++e) x[e] = adam_elem<ADAMW>(x[e], m[e], v[e], g[e], s);
+  __stcs(p4 + i, make_float4(x[0], x[1], x[2], x[3]));
+  __stcs(m4 + i, make_float4(m[0], m[1], m[2], m[3]));
+  __stcs(v4 + i, make_float4(v[0], v[1], v[2], v[3]));
+  store_out4<OT>(out, i, x);
+}
+
+// One 4-element vector of the remainder form: H the bf16 high halves, R the
+// remainders; the new remainders go to rem, the new high halves to out.
+template <bool ADAMW, int GT>
+__device__ __forceinline__ void update4_rem(const uint2& H, const uint2& R, float4 M, float4 V,
+                                            const typename Raw4<GT>::T& G, const Scal& s,
+                                            uint2* r4, float4* m4, float4* v4, uint2* o4, int i) {
+  float g[4];
+  widen4<GT>(G, g);
+  unsigned short hh[4], rr[4], oh[4], orr[4];
+  unpack4(H, hh);
+  unpack4(R, rr);
+  float m[4] = {M.x, M.y, M.z, M.w};
+  float v[4] = {V.x, V.y, V.z, V.w};
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int i = base + u * kBlock;
-        if (i < nv) {
-          float g[4];
-          widen4<GT>(G[u], g);
-          float x[4] = {P[u].x, P[u].y, P[u].z, P[u].w};
-          float m[4] = {M[u].x, M[u].y, M[u].z, M[u].w};
-          float v[4] = {V[u].x, V[u].y, V[u].z, V[u].w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) x[e] = adam_elem<ADAMW>(x[e], m[e], v[e], g[e], s);
-          __stcs(p4 + i, make_float4(x[0], x[1], x[2], x[3]));
-          __stcs(m4 + i, make_float4(m[0], m[1], m[2], m[3]));
-          __stcs(v4 + i, make_float4(v[0], v[1], v[2], v[3]));
-          store_out4<OT>(it.p_out, i, x);
-        }
-      }
-    }
-    scalar_from = nv * kVec;
+  for (int e = 0; e < 4; ++e) {
+    const float x = adam_elem<ADAMW>(rem_pack(hh[e], rr[e]), m[e], v[e], g[e], s);
+    rem_split(x, oh[e], orr[e]);
   }
-  float* p = reinterpret_cast<float*>(it.p);
-  float* mp = reinterpret_cast<float*>(it.m);
-  float* vp = reinterpret_cast<float*>(it.v);
-  for (int i = scalar_from + threadIdx.x; i < n; i += kBlock) {
-    float m = __ldcs(mp + i), v = __ldcs(vp + i);
-    const float x = adam_elem<ADAMW>(__ldcs(p + i), m, v, load1<GT>(it.g, i), s);
-    __stcs(p + i, x);
-    __stcs(mp + i, m);
-    __stcs(vp + i, v);
-    store_out1<OT>(it.p_out, i, x);
+  __stcs(r4 + i, pack4(orr));
+  __stcs(m4 + i, make_float4(m[0], m[1], m[2], m[3]));
+  __stcs(v4 + i, make_float4(v[0], v[1], v[2], v[3]));
+  __stcs(o4 + i, pack4(oh));
+}
+
+// ---- bulk-copy pipeline -----------------------------------------------------
+
+#ifndef FADAM_BULK
+#define FADAM_BULK 1
+#endif
+#ifndef FADAM_STAGES
+#define FADAM_STAGES 2
+#endif
+constexpr int kStages = FADAM_STAGES;
+constexpr int kTile = kBlock;  // vectors per tile: one per thread
+
+// Byte layout of one tile in shared memory, by stream (per vector of 4
+// elements): p 16 (or the bf16 high halves 8 and the remainders 8), m 16,
+// v 16, g 16 or 8.
+constexpr int kOffM = 16 * kTile;
+constexpr int kOffV = 32 * kTile;
+constexpr int kOffG = 48 * kTile;
+template <int GT>
+__host__ __device__ constexpr int g_vec_bytes() { return GT == FADAM_DT_F32 ? 16 : 8; }
+template <int GT>
+__host__ __device__ constexpr unsigned tile_bytes() { return static_cast<unsigned>(kTile * (48 + g_vec_bytes<GT>())); }
+template <int GT>
+__host__ __device__ constexpr size_t smem_bytes() { return FADAM_BULK ? size_t(kStages) * tile_bytes<GT>() : 0; }
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for the phase of `parity` to complete, for at most kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+
+// Global -> shared bulk copy completing on `bar` (16-byte aligned, size a
+// multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ Item load_item(const Item* items, int k) {
+  const int4* src = reinterpret_cast<const int4*>(items + k);
+  int4 w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) w[j] = __ldg(src + j);
+  Item it;
+  memcpy(&it, w, sizeof(Item));
+  return it;
+}
+
+// Vectors of an item that go through the bulk pipeline: all of them when
+// every stream is 16-byte aligned, rounded down to an even count so that
+// 8-byte-per-vector streams still copy whole 16-byte units; none otherwise.
+__device__ __forceinline__ int bulk_vectors(const Item& it) {
+  return (it.flags & kItemBulk) ? ((it.n / kVec) & ~1) : 0;
+}
+
+__device__ __forceinline__ int bulk_tiles(const Item& it) {
+  return (bulk_vectors(it) + kTile - 1) / kTile;
+}
+
+// What a pipeline pass moves through shared memory.
+enum class Pass { kUpdate, kScan };  // kScan: only g, for the inf/nan screen
+
+template <int GT, Pass PASS>
+__host__ __device__ constexpr unsigned bytes_per_vector() {
+  return PASS == Pass::kScan ? g_vec_bytes<GT>() : 48u + g_vec_bytes<GT>();
+}
+
+// Vectors in one tile: one per thread for the update; four per thread for
+// the screen, which moves only g and would otherwise keep too few bytes in
+// flight.
+template <Pass PASS>
+__host__ __device__ constexpr int tile_vectors() { return PASS == Pass::kScan ? 4 * kTile : kTile; }
+
+// Thread 0 of the CTA: start the copies of vectors [v0, v0 + len) of `it`
+// into buffer `slot % kStages`.
+template <int GT, bool REM, Pass PASS>
+__device__ __forceinline__ void issue_tile(const Item& it, int v0, unsigned len, unsigned slot,
+                                           unsigned char* smem, uint64_t* full) {
+  constexpr int GB = g_vec_bytes<GT>();
+  const unsigned b = slot % kStages;
+  unsigned char* st = smem + size_t(b) * tile_bytes<GT>();
+  uint64_t* bar = full + b;
+  mbar_expect_tx(bar, len * bytes_per_vector<GT, PASS>());
+  if constexpr (PASS == Pass::kScan) {
+    bulk_load(st, static_cast<const char*>(it.g) + size_t(v0) * GB, len * GB, bar);
+  } else {
+    if constexpr (REM) {
+      bulk_load(st, static_cast<const char*>(it.p) + size_t(v0) * 8, len * 8, bar);
+      bulk_load(st + 8 * kTile, reinterpret_cast<const char*>(it.rem) + size_t(v0) * 8, len * 8, bar);
+    } else {
+      bulk_load(st, static_cast<const char*>(it.p) + size_t(v0) * 16, len * 16, bar);
+    }
+    bulk_load(st + kOffM, static_cast<const char*>(it.m) + size_t(v0) * 16, len * 16, bar);
+    bulk_load(st + kOffV, static_cast<const char*>(it.v) + size_t(v0) * 16, len * 16, bar);
+    bulk_load(st + kOffG, static_cast<const char*>(it.g) + size_t(v0) * GB, len * GB, bar);
   }
 }
 
-// Remainder form: p is the bf16 high half (read), rem the int16 low half
-// (read and written), p_out receives the new bf16 high half (it may alias p).
-template <bool ADAMW, int GT>
-__device__ __forceinline__ void run_item_rem(const Item& it, const Scal& s) {
-  const int n = it.n;
-  int scalar_from = 0;
-  if (it.flags & kItemVec) {
-    const int nv = n / kVec;
-    const uint2* h4 = reinterpret_cast<const uint2*>(it.p);
-    uint2* r4 = reinterpret_cast<uint2*>(it.rem);
-    float4* m4 = reinterpret_cast<float4*>(it.m);
-    float4* v4 = reinterpret_cast<float4*>(it.v);
-    uint2* o4 = reinterpret_cast<uint2*>(it.p_out);
-    for (int base = threadIdx.x; base < nv; base += kBlock * kUnroll) {
-      uint2 H[kUnroll], R[kUnroll];
-      float4 M[kUnroll], V[kUnroll];
-      typename Raw4<GT>::T G[kUnroll];
+// The producer side of the pipeline, kept by thread 0 only: it pulls chunks
+// of tiles from the launch-wide counter (so faster SMs take more of them)
+// and copies their tiles kStages ahead of the consumers, announcing each
+// tile's (item, tile) in a small shared ring before its copies start.  When
+// the chunks run out it announces the end with an arrival that carries no
+// bytes.
+struct Producer {
+  Item it;
+  int item, v, vend;  // vectors [v, vend) of the current chunk remain
+  unsigned slot;
+  bool finished;
+};
+
+struct TileTag {
+  int item;  // -1: no more tiles
+  int v0;
+  int len;
+};
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+template <int GT, bool REM, Pass PASS>
+__device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, unsigned* counter,
+                                             unsigned char* smem, uint64_t* full, TileTag* tags) {
+  if (pr.finished) return;
+  while (pr.v >= pr.vend) {
+    const unsigned c = atomicAdd(counter, 1u);
+    if (c >= static_cast<unsigned>(kp.n_chunks)) {
+      const unsigned b = pr.slot % kStages;
+      tags[b] = TileTag{-1, 0, 0};
+      mbar_arrive(full + b);  // completes the phase with no copy
+      ++pr.slot;
+      pr.finished = true;
+      return;
+    }
+    const Chunk ch = kp.chunks[c];
+    if (ch.item != pr.item) {
+      pr.item = ch.item;
+      pr.it = load_item(kp.items, ch.item);
+    }
+    pr.v = ch.tile0 * kTile;
+    pr.vend = min((ch.tile0 + ch.ntiles) * kTile, bulk_vectors(pr.it));
+  }
+  const int len = min(tile_vectors<PASS>(), pr.vend - pr.v);
+  tags[pr.slot % kStages] = TileTag{pr.item, pr.v, len};
+  issue_tile<GT, REM, PASS>(pr.it, pr.v, static_cast<unsigned>(len), pr.slot, smem, full);
+  pr.v += len;
+  ++pr.slot;
+}
+
+// Consume one tile from shared memory.
+template <bool ADAMW, int GT, int OT, bool REM>
+__device__ __forceinline__ void update_tile(const Item& it, const Scal& s, const unsigned char* st,
+                                            int v0, int len) {
+  const int t = threadIdx.x;
+  if (t >= len) return;
+  const int i = v0 + t;
+  const float4 M = reinterpret_cast<const float4*>(st + kOffM)[t];
+  const float4 V = reinterpret_cast<const float4*>(st + kOffV)[t];
+  const typename Raw4<GT>::T G = reinterpret_cast<const typename Raw4<GT>::T*>(st + kOffG)[t];
+  if constexpr (REM) {
+    const uint2 H = reinterpret_cast<const uint2*>(st)[t];
+    const uint2 R = reinterpret_cast<const uint2*>(st + 8 * kTile)[t];
+    update4_rem<ADAMW, GT>(H, R, M, V, G, s, reinterpret_cast<uint2*>(it.rem),
+                           reinterpret_cast<float4*>(it.m), reinterpret_cast<float4*>(it.v),
+                           reinterpret_cast<uint2*>(it.p_out), i);
+  } else {
+    const float4 P = reinterpret_cast<const float4*>(st)[t];
+    update4_f32<ADAMW, GT, OT>(P, M, V, G, s, reinterpret_cast<float4*>(it.p),
+                               reinterpret_cast<float4*>(it.m), reinterpret_cast<float4*>(it.v),
+                               it.p_out, i);
+  }
+}
+
+template <int GT>
+__device__ __forceinline__ bool scan_tile(const unsigned char* st, int len, float gs) {
+  bool bad = false;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int i = base + u * kBlock;
-        if (i < nv) {
-          H[u] = __ldcs(h4 + i);
-          R[u] = __ldcs(r4 + i);
-          M[u] = __ldcs(m4 + i);
-          V[u] = __ldcs(v4 + i);
-          G[u] = load4<GT>(it.g, i);
+  for (int q = 0; q < tile_vectors<Pass::kScan>() / kTile; ++q) {
+    const int t = threadIdx.x + q * kTile;
+    if (t < len) {
+      float g[4];
+      widen4<GT>(reinterpret_cast<const typename Raw4<GT>::T*>(st)[t], g);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) bad |= !isfinite(__fmul_rn(g[e], gs));
+    }
+  }
+  return bad;
+}
+
+// Phase A: the bulk tiles of the whole shard, pulled chunk by chunk from
+// the launch-wide counter, as one continuous pipeline per CTA (the copies
+// of the next chunk start while the current one is consumed).  `bad`
+// collects the scan's finding; a wait that gives up sets `timed_out` and
+// ends the pass for the CTA.
+template <int GT, int OT, bool REM, Pass PASS>
+__device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp, unsigned* counter,
+                                          unsigned char* smem, uint64_t* full, TileTag* tags,
+                                          Producer& pr, unsigned& stage, bool& bad,
+                                          bool& timed_out) {
+  if (threadIdx.x == 0) {
+    pr.item = -1;
+    pr.v = 0;
+    pr.vend = 0;
+    pr.slot = stage;
+    pr.finished = false;
+    for (int q = 0; q < kStages; ++q) produce_next<GT, REM, PASS>(pr, kp, counter, smem, full, tags);
+  }
+  int cur_item = -1;
+  Item it;
+  for (;; ++stage) {
+    const unsigned b = stage % kStages;
+    const bool ok = mbar_wait(full + b, (stage / kStages) & 1u);
+    TileTag tag{-1, 0, 0};
+    if (ok) {
+      tag = tags[b];
+      if (tag.item >= 0) {
+        if (tag.item != cur_item) {
+          cur_item = tag.item;
+          it = load_item(kp.items, tag.item);
         }
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int i = base + u * kBlock;
-        if (i < nv) {
-          float g[4];
-          widen4<GT>(G[u], g);
-          const unsigned short hh[4] = {
-              static_cast<unsigned short>(H[u].x & 0xFFFFu), static_cast<unsigned short>(H[u].x >> 16),
-              static_cast<unsigned short>(H[u].y & 0xFFFFu), static_cast<unsigned short>(H[u].y >> 16)};
-          const unsigned short rr[4] = {
-              static_cast<unsigned short>(R[u].x & 0xFFFFu), static_cast<unsigned short>(R[u].x >> 16),
-              static_cast<unsigned short>(R[u].y & 0xFFFFu), static_cast<unsigned short>(R[u].y >> 16)};
-          float m[4] = {M[u].x, M[u].y, M[u].z, M[u].w};
-          float v[4] = {V[u].x, V[u].y, V[u].z, V[u].w};
-          unsigned short oh[4], orr[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float x = adam_elem<ADAMW>(rem_pack(hh[e], rr[e]), m[e], v[e], g[e], s);
-            rem_split(x, oh[e], orr[e]);
-          }
-          __stcs(r4 + i, make_uint2(orr[0] | (static_cast<unsigned>(orr[1]) << 16),
-                                    orr[2] | (static_cast<unsigned>(orr[3]) << 16)));
-          __stcs(m4 + i, make_float4(m[0], m[1], m[2], m[3]));
-          __stcs(v4 + i, make_float4(v[0], v[1], v[2], v[3]));
-          __stcs(o4 + i, make_uint2(oh[0] | (static_cast<unsigned>(oh[1]) << 16),
-                                    oh[2] | (static_cast<unsigned>(oh[3]) << 16)));
+        const unsigned char* st = smem + size_t(b) * tile_bytes<GT>();
+        const SGroup& G = sgrp[it.group];
+        const Scal s{G.beta1, G.omb1, G.beta2, G.omb2, G.bc1, G.bc2, G.eps, G.wd, G.lr, G.gs};
+        if constexpr (PASS == Pass::kScan) {
+          bad |= scan_tile<GT>(st, tag.len, s.gs);
+        } else {
+          if (G.bits & kGroupAdamW) update_tile<true, GT, OT, REM>(it, s, st, tag.v0, tag.len);
+          else update_tile<false, GT, OT, REM>(it, s, st, tag.v0, tag.len);
         }
       }
     }
-    scalar_from = nv * kVec;
+    // every thread is done with buffer b; a timeout anywhere stops the CTA
+    if (__syncthreads_or(!ok)) {
+      timed_out = true;
+      ++stage;
+      return;
+    }
+    if (tag.item < 0) {  // the end marker (the same for every thread)
+      ++stage;
+      return;
+    }
+    if (threadIdx.x == 0) {
+      // order the generic-proxy reads of the buffer before its async refill
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      produce_next<GT, REM, PASS>(pr, kp, counter, smem, full, tags);
+    }
   }
+}
+
+// ---- element-wise paths (tails, runs not 16-byte aligned) -------------------
+
+template <bool ADAMW, int GT, int OT>
+__device__ __forceinline__ void update_elem_f32(const Item& it, const Scal& s, int i) {
+  float* p = reinterpret_cast<float*>(it.p);
+  float* mp = reinterpret_cast<float*>(it.m);
+  float* vp = reinterpret_cast<float*>(it.v);
+  float m = __ldcs(mp + i), v = __ldcs(vp + i);
+  const float x = adam_elem<ADAMW>(__ldcs(p + i), m, v, load1<GT>(it.g, i), s);
+  __stcs(p + i, x);
+  __stcs(mp + i, m);
+  __stcs(vp + i, v);
+  store_out1<OT>(it.p_out, i, x);
+}
+
+template <bool ADAMW, int GT>
+__device__ __forceinline__ void update_elem_rem(const Item& it, const Scal& s, int i) {
   const unsigned short* hp = reinterpret_cast<const unsigned short*>(it.p);
   unsigned short* rp = reinterpret_cast<unsigned short*>(it.rem);
   float* mp = reinterpret_cast<float*>(it.m);
   float* vp = reinterpret_cast<float*>(it.v);
   unsigned short* op = reinterpret_cast<unsigned short*>(it.p_out);
-  for (int i = scalar_from + threadIdx.x; i < n; i += kBlock) {
-    float m = __ldcs(mp + i), v = __ldcs(vp + i);
-    const float x0 = rem_pack(__ldcs(hp + i), __ldcs(rp + i));
-    const float x = adam_elem<ADAMW>(x0, m, v, load1<GT>(it.g, i), s);
-    unsigned short oh, orr;
-    rem_split(x, oh, orr);
-    __stcs(rp + i, orr);
-    __stcs(mp + i, m);
-    __stcs(vp + i, v);
-    __stcs(op + i, oh);
-  }
+  float m = __ldcs(mp + i), v = __ldcs(vp + i);
+  const float x0 = rem_pack(__ldcs(hp + i), __ldcs(rp + i));
+  const float x = adam_elem<ADAMW>(x0, m, v, load1<GT>(it.g, i), s);
+  unsigned short oh, orr;
+  rem_split(x, oh, orr);
+  __stcs(rp + i, orr);
+  __stcs(mp + i, m);
+  __stcs(vp + i, v);
+  __stcs(op + i, oh);
 }
 
-// True when this thread saw a non-finite g*grad_scale in the item.
+template <bool ADAMW, int GT, int OT, bool REM>
+__device__ __forceinline__ void update_elem(const Item& it, const Scal& s, int i) {
+  if constexpr (REM) update_elem_rem<ADAMW, GT>(it, s, i);
+  else update_elem_f32<ADAMW, GT, OT>(it, s, i);
+}
+
+// A whole item not aligned for bulk copies, by the whole CTA: 128-bit
+// streaming loads when every stream is vector-aligned, then element by
+// element for the rest.
+template <bool ADAMW, int GT, int OT, bool REM>
+__device__ __forceinline__ void simt_item(const Item& it, const Scal& s) {
+  const int n = it.n;
+  int scalar_from = 0;
+  if (it.flags & kItemVec) {
+    const int nv = n / kVec;
+    for (int base = threadIdx.x; base < nv; base += kBlock * kUnroll) {
+      if constexpr (REM) {
+        const uint2* h4 = reinterpret_cast<const uint2*>(it.p);
+        uint2* r4 = reinterpret_cast<uint2*>(it.rem);
+        float4* m4 = reinterpret_cast<float4*>(it.m);
+        float4* v4 = reinterpret_cast<float4*>(it.v);
+        uint2* o4 = reinterpret_cast<uint2*>(it.p_out);
+        uint2 H[kUnroll], R[kUnroll];
+        float4 M[kUnroll], V[kUnroll];
+        typename Raw4<GT>::T G[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int i = base + u * kBlock;
+          if (i < nv) {
+            H[u] = __ldcs(h4 + i);
+            R[u] = __ldcs(r4 + i);
+            M[u] = __ldcs(m4 + i);
+            V[u] = __ldcs(v4 + i);
+            G[u] = load4<GT>(it.g, i);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int i = base + u * kBlock;
+          if (i < nv) update4_rem<ADAMW, GT>(H[u], R[u], M[u], V[u], G[u], s, r4, m4, v4, o4, i);
+        }
+      } else {
+        float4* p4 = reinterpret_cast<float4*>(it.p);
+        float4* m4 = reinterpret_cast<float4*>(it.m);
+        float4* v4 = reinterpret_cast<float4*>(it.v);
+        float4 P[kUnroll], M[kUnroll], V[kUnroll];
+        typename Raw4<GT>::T G[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int i = base + u * kBlock;
+          if (i < nv) {
+            P[u] = __ldcs(p4 + i);
+            M[u] = __ldcs(m4 + i);
+            V[u] = __ldcs(v4 + i);
+            G[u] = load4<GT>(it.g, i);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int i = base + u * kBlock;
+          if (i < nv) update4_f32<ADAMW, GT, OT>(P[u], M[u], V[u], G[u], s, p4, m4, v4, it.p_out, i);
+        }
+      }
+    }
+    scalar_from = nv * kVec;
+  }
+  for (int i = scalar_from + threadIdx.x; i < n; i += kBlock) update_elem<ADAMW, GT, OT, REM>(it, s, i);
+}
+
+// True when this thread saw a non-finite g*grad_scale in the item (by the
+// whole CTA).
 template <int GT>
-__device__ __forceinline__ bool scan_item(const Item& it, float gs) {
+__device__ __forceinline__ bool simt_scan(const Item& it, float gs) {
   bool bad = false;
   const int n = it.n;
   int scalar_from = 0;
@@ -326,19 +655,92 @@ __device__ __forceinline__ bool scan_item(const Item& it, float gs) {
   return bad;
 }
 
-__device__ __forceinline__ Item load_item(const Item* items, int k) {
-  const int4* src = reinterpret_cast<const int4*>(items + k);
-  int4 w[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) w[j] = __ldg(src + j);
-  Item it;
-  memcpy(&it, w, sizeof(Item));
-  return it;
+// Phase B, tails: the at most 7 trailing elements of every bulk item.
+// Warps pull 32 items at a time from a launch-wide counter and each lane
+// takes one item's tail, so the many small latencies overlap across the
+// whole GPU.
+template <int GT, int OT, bool REM, Pass PASS>
+__device__ __forceinline__ bool tail_pass(const KParams& kp, const SGroup* sgrp, unsigned* counter,
+                                          int n_items) {
+  const int lane = threadIdx.x % 32;
+  bool bad = false;
+  for (;;) {
+    unsigned base = 0;
+    if (lane == 0) base = atomicAdd(counter, 32u);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (base >= static_cast<unsigned>(n_items)) break;
+    const int k = static_cast<int>(base) + lane;
+    if (k >= n_items) continue;
+    const Item it = load_item(kp.items, k);
+    if (!(it.flags & kItemBulk)) continue;
+    const SGroup& G = sgrp[it.group];
+    const Scal s{G.beta1, G.omb1, G.beta2, G.omb2, G.bc1, G.bc2, G.eps, G.wd, G.lr, G.gs};
+    for (int i = bulk_vectors(it) * kVec; i < it.n; ++i) {
+      if constexpr (PASS == Pass::kScan) {
+        bad |= !isfinite(__fmul_rn(load1<GT>(it.g, i), s.gs));
+      } else {
+        if (G.bits & kGroupAdamW) update_elem<true, GT, OT, REM>(it, s, i);
+        else update_elem<false, GT, OT, REM>(it, s, i);
+      }
+    }
+  }
+  return bad;
+}
+
+// Phase B, the rest: this CTA's items that are not 16-byte aligned, by the
+// whole CTA (128-bit streaming loads when vector-aligned, then element by
+// element).  Without the bulk pipeline every item goes this way.  The
+// threads first test kBlock items' flags at once, so a range of bulk items
+// is skipped in a few loads.
+template <int GT, int OT, bool REM, Pass PASS>
+__device__ __forceinline__ bool rest_pass(const KParams& kp, const SGroup* sgrp, int item_begin,
+                                          int item_end) {
+  __shared__ int s_count;
+  __shared__ int s_list[kBlock];
+  bool bad = false;
+  for (int base = item_begin; base < item_end; base += kBlock) {
+    if (threadIdx.x == 0) s_count = 0;
+    __syncthreads();
+    const int k = base + threadIdx.x;
+    if (k < item_end) {
+      const uint16_t flags = __ldg(&kp.items[k].flags);
+      if (!(FADAM_BULK && (flags & kItemBulk))) s_list[atomicAdd(&s_count, 1)] = k;
+    }
+    __syncthreads();
+    const int count = s_count;
+    for (int q = 0; q < count; ++q) {
+      const Item it = load_item(kp.items, s_list[q]);
+      const SGroup& G = sgrp[it.group];
+      const Scal s{G.beta1, G.omb1, G.beta2, G.omb2, G.bc1, G.bc2, G.eps, G.wd, G.lr, G.gs};
+      if constexpr (PASS == Pass::kScan) {
+        bad |= simt_scan<GT>(it, s.gs);
+      } else {
+        if (G.bits & kGroupAdamW) simt_item<true, GT, OT, REM>(it, s);
+        else simt_item<false, GT, OT, REM>(it, s);
+      }
+    }
+    __syncthreads();  // s_list is reused
+  }
+  return bad;
+}
+
+// One full pass: the bulk tiles of the shard (dynamically shared), then
+// the rest of this CTA's items.
+template <int GT, int OT, bool REM, Pass PASS>
+__device__ __forceinline__ void run_pass(const KParams& kp, const SGroup* sgrp, int item_begin,
+                                         int item_end, unsigned* counter, unsigned* tail_counter,
+                                         int n_items, unsigned char* smem, uint64_t* full,
+                                         TileTag* tags, Producer& pr, unsigned& stage, bool& bad,
+                                         bool& timed_out) {
+  if (FADAM_BULK && kp.n_chunks > 0 && !timed_out)
+    bulk_pass<GT, OT, REM, PASS>(kp, sgrp, counter, smem, full, tags, pr, stage, bad, timed_out);
+  if (FADAM_BULK) bad |= tail_pass<GT, OT, REM, PASS>(kp, sgrp, tail_counter, n_items);
+  bad |= rest_pass<GT, OT, REM, PASS>(kp, sgrp, item_begin, item_end);
 }
 
 // Grid-wide barrier for a cooperative launch.  The wait is bounded: after
-// kBarrierSpinLimit polls it records FADAM_ETIMEOUT in the status block and
-// returns false instead of hanging.
+// kWaitLimitNs it records FADAM_ETIMEOUT in the status block and returns
+// false instead of hanging.
 __device__ __forceinline__ bool grid_barrier(KScratch* sc) {
   __shared__ int s_ok;
   __syncthreads();
@@ -352,9 +754,9 @@ __device__ __forceinline__ bool grid_barrier(KScratch* sc) {
       __threadfence();
       atomicAdd(&sc->bar_gen, 1u);
     } else {
-      unsigned spins = 0;
+      const unsigned long long t0 = global_ns();
       while (ld_acquire_u32(&sc->bar_gen) == gen) {
-        if (++spins > kBarrierSpinLimit) {
+        if (global_ns() - t0 > kWaitLimitNs) {
           atomicExch(&sc->status, FADAM_ETIMEOUT);
           ok = 0;
           break;
@@ -372,14 +774,24 @@ __device__ __forceinline__ bool grid_barrier(KScratch* sc) {
 // ---- the kernel ---------------------------------------------------------------
 
 template <int GT, int OT, bool REM>
-__global__ void __launch_bounds__(kBlock) fadam_update_kernel(const __grid_constant__ KParams kp) {
+__global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams kp) {
   __shared__ SGroup sgrp[FADAM_MAX_GROUPS];
   __shared__ int s_noop;
+  __shared__ __align__(8) uint64_t s_full[kStages];
+  __shared__ TileTag s_tags[kStages];
+  __shared__ Producer s_prod;  // used by thread 0 only
+  extern __shared__ __align__(128) unsigned char s_tiles[];
   const bool capturable = (kp.flags & kCapturable) != 0;
   const int tid = threadIdx.x;
 
   // 1. prologue: scalars once per CTA
-  if (tid == 0) s_noop = kp.noop ? (__ldcg(kp.noop) == 1) : 0;  // only 1 means set
+  if (tid == 0) {
+    s_noop = kp.noop ? (__ldcg(kp.noop) == 1) : 0;  // only 1 means set
+    if (FADAM_BULK) {
+      for (int b = 0; b < kStages; ++b) mbar_init(&s_full[b], 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+  }
   if (tid < kp.n_groups) {
     const KGroup& G = kp.groups[tid];
     SGroup s;
@@ -415,17 +827,17 @@ __global__ void __launch_bounds__(kBlock) fadam_update_kernel(const __grid_const
 
   const int item_begin = __ldg(kp.cta_begin + blockIdx.x);
   const int item_end = __ldg(kp.cta_begin + blockIdx.x + 1);
-  bool barrier_ok = true;
+  const int n_items = __ldg(kp.cta_begin + gridDim.x);
+  unsigned stage = 0;  // tiles through the pipeline so far (buffer and parity)
+  bool barrier_ok = true, timed_out = false;
 
   // 2. optional inf/nan screen over the whole shard before any update
   if (kp.flags & kCheckFinite) {
     bool bad = false;
-    if (!s_noop) {
-      for (int k = item_begin; k < item_end; ++k) {
-        const Item it = load_item(kp.items, k);
-        bad |= scan_item<GT>(it, sgrp[it.group].gs);
-      }
-    }
+    if (!s_noop)
+      run_pass<GT, OT, REM, Pass::kScan>(kp, sgrp, item_begin, item_end, &kp.scratch->next_scan,
+                                         &kp.scratch->next_tail_scan, n_items, s_tiles, s_full,
+                                         s_tags, s_prod, stage, bad, timed_out);
     if (__syncthreads_or(bad) && tid == 0) atomicExch(kp.noop, 1);
     barrier_ok = grid_barrier(kp.scratch);
     if (tid == 0) s_noop = (ld_acquire_s32(kp.noop) == 1);
@@ -434,50 +846,53 @@ __global__ void __launch_bounds__(kBlock) fadam_update_kernel(const __grid_const
 
   // 3. the update
   if (!s_noop && barrier_ok) {
-    for (int k = item_begin; k < item_end; ++k) {
-      const Item it = load_item(kp.items, k);
-      const SGroup& G = sgrp[it.group];
-      const Scal s{G.beta1, G.omb1, G.beta2, G.omb2, G.bc1, G.bc2, G.eps, G.wd, G.lr, G.gs};
-      if constexpr (REM) {
-        if (G.bits & kGroupAdamW) run_item_rem<true, GT>(it, s);
-        else run_item_rem<false, GT>(it, s);
-      } else {
-        if (G.bits & kGroupAdamW) run_item_f32<true, GT, OT>(it, s);
-        else run_item_f32<false, GT, OT>(it, s);
-      }
-    }
+    bool unused = false;
+    run_pass<GT, OT, REM, Pass::kUpdate>(kp, sgrp, item_begin, item_end, &kp.scratch->next_update,
+                                         &kp.scratch->next_tail_update, n_items, s_tiles, s_full,
+                                         s_tags, s_prod, stage, unused, timed_out);
   }
+  if (__syncthreads_or(timed_out) && tid == 0) atomicExch(&kp.scratch->status, FADAM_ETIMEOUT);
 
-  // 4. capturable: the last CTA to finish advances the step counters
-  if (capturable && !(kp.flags & kPreadvanced)) {
-    __syncthreads();
-    if (tid == 0) {
+  // 4. the last CTA to finish resets the work counters for the next launch
+  //    and, for capturable plans, advances the step counters
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(&kp.scratch->done, 1u);
+    if (prev == gridDim.x - 1) {
       __threadfence();
-      const unsigned prev = atomicAdd(&kp.scratch->done, 1u);
-      if (prev == gridDim.x - 1) {
-        __threadfence();
+      if (capturable && !(kp.flags & kPreadvanced)) {
         const int adv = (s_noop || !barrier_ok) ? 0 : 1;
         for (int g = 0; g < kp.n_groups; ++g)
           if (sgrp[g].bits & kGroupOwnsStep) *kp.groups[g].step_dev = sgrp[g].step_old + adv;
-        atomicExch(&kp.scratch->done, 0u);
       }
+      atomicExch(&kp.scratch->next_update, 0u);
+      atomicExch(&kp.scratch->next_scan, 0u);
+      atomicExch(&kp.scratch->next_tail_update, 0u);
+      atomicExch(&kp.scratch->next_tail_scan, 0u);
+      atomicExch(&kp.scratch->done, 0u);
     }
   }
 }
 
 // Entry for one g dtype: every out dtype, with and without remainders.
 template <int GT>
-const void* kernel_for(int out_dtype, bool remainders) {
+KernelEntry kernel_for(int out_dtype, bool remainders) {
+  const size_t smem = smem_bytes<GT>();
   if (remainders)
     return out_dtype == FADAM_DT_BF16
-               ? reinterpret_cast<const void*>(&fadam_update_kernel<GT, FADAM_DT_BF16, true>)
-               : nullptr;
+               ? KernelEntry{reinterpret_cast<const void*>(&fadam_update_kernel<GT, FADAM_DT_BF16, true>), smem}
+               : KernelEntry{nullptr, 0};
   switch (out_dtype) {
-    case FADAM_DT_NONE: return reinterpret_cast<const void*>(&fadam_update_kernel<GT, FADAM_DT_NONE, false>);
-    case FADAM_DT_F32: return reinterpret_cast<const void*>(&fadam_update_kernel<GT, FADAM_DT_F32, false>);
-    case FADAM_DT_BF16: return reinterpret_cast<const void*>(&fadam_update_kernel<GT, FADAM_DT_BF16, false>);
-    case FADAM_DT_F16: return reinterpret_cast<const void*>(&fadam_update_kernel<GT, FADAM_DT_F16, false>);
-    default: return nullptr;
+    case FADAM_DT_NONE:
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<GT, FADAM_DT_NONE, false>), smem};
+    case FADAM_DT_F32:
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<GT, FADAM_DT_F32, false>), smem};
+    case FADAM_DT_BF16:
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<GT, FADAM_DT_BF16, false>), smem};
+    case FADAM_DT_F16:
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<GT, FADAM_DT_F16, false>), smem};
+    default: return {nullptr, 0};
   }
 }
 

@@ -5,7 +5,7 @@
 
 namespace fadam {
 
-const void* kernel_gbf16(int out_dtype, bool remainders) {
+KernelEntry kernel_gbf16(int out_dtype, bool remainders) {
   return kernel_for<FADAM_DT_BF16>(out_dtype, remainders);
 }
 

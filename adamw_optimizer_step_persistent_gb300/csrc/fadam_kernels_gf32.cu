@@ -5,7 +5,7 @@
 
 namespace fadam {
 
-const void* kernel_gf32(int out_dtype, bool remainders) {
+KernelEntry kernel_gf32(int out_dtype, bool remainders) {
   return kernel_for<FADAM_DT_F32>(out_dtype, remainders);
 }
 

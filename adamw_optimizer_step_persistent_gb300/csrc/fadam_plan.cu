@@ -30,6 +30,9 @@ namespace {
 constexpr double kMinCtaCost = 64.0 * 1024.0;
 // Fixed cost of one work item, in byte-equivalents (descriptor fetch, tail).
 constexpr double kItemOverhead = 4096.0;
+// Most chunks a plan's work list holds (chunks grow past kChunkTiles tiles
+// beyond that).
+constexpr int64_t kPlanMaxChunks = 65536;
 // Largest tensor the library accepts, in elements.
 constexpr int64_t kMaxNumel = int64_t(1) << 40;
 
@@ -187,27 +190,39 @@ struct PackItem {
   int64_t tensor;
   int64_t offset;
   int64_t n;
-  bool vec;
+  int level;  // 0 scalar, 1 vector-aligned, 2 also 16-byte aligned
 };
 
 struct Piece {
   int64_t tensor, offset, n;
-  bool vec;
+  int level;
 };
 
-// Elements to skip at the start of a tensor so that every stream is
-// vector-aligned (all streams must agree), or -1 when they cannot agree.
-int64_t vector_head(const fadam_tensor& t, const Dtypes& d) {
+struct Head {
+  int64_t h;  // elements to peel off the start of the tensor
+  int level;  // alignment of the rest, as in PackItem
+};
+
+// How many leading elements to peel so that the rest of the tensor is as
+// aligned as possible: every stream 16-byte aligned (bulk copies), else
+// every stream aligned to one 4-element vector, else nothing (scalar path).
+Head body_alignment(const fadam_tensor& t, const Dtypes& d) {
   const void* ptrs[6] = {t.p, t.m, t.v, t.g, t.p_out, t.rem};
   const int esz[6] = {elem_size(d.p), 4, 4, elem_size(d.g), elem_size(d.out), 2};
+  for (int64_t h = 0; h < 8; ++h) {
+    bool ok = true;
+    for (int s = 0; s < 6 && ok; ++s)
+      if (ptrs[s] && esz[s] && (reinterpret_cast<uintptr_t>(ptrs[s]) + h * esz[s]) % 16 != 0) ok = false;
+    if (ok) return {h, 2};
+  }
   int64_t r = -1;
   for (int s = 0; s < 6; ++s) {
     if (!ptrs[s] || esz[s] == 0) continue;
     const int64_t rs = static_cast<int64_t>((reinterpret_cast<uintptr_t>(ptrs[s]) / esz[s]) % kVec);
     if (r < 0) r = rs;
-    else if (r != rs) return -1;
+    else if (r != rs) return {0, 0};
   }
-  return r < 0 ? 0 : (kVec - r) % kVec;
+  return {r < 0 ? 0 : (kVec - r) % kVec, 1};
 }
 
 // Split the shard into pieces (aligned bodies, scalar heads) and cut them
@@ -218,13 +233,13 @@ void pack(const fadam_tensor* ts, int64_t n, const Dtypes& d, int grid,
   for (int64_t i = 0; i < n; ++i) {
     const int64_t len = ts[i].numel;
     if (len <= 0) continue;
-    const int64_t h = vector_head(ts[i], d);
-    if (h < 0) {
-      pieces.push_back({i, 0, len, false});
+    const Head hd = body_alignment(ts[i], d);
+    if (hd.level == 0) {
+      pieces.push_back({i, 0, len, 0});
       continue;
     }
-    if (h > 0) pieces.push_back({i, 0, std::min(h, len), false});
-    if (len > h) pieces.push_back({i, h, len - h, true});
+    if (hd.h > 0) pieces.push_back({i, 0, std::min(hd.h, len), 0});
+    if (len > hd.h) pieces.push_back({i, hd.h, len - hd.h, hd.level});
   }
   // Total cost, counting the overhead of every item the cuts can add (one
   // per CTA boundary plus the kMaxItem splits): overestimating only leaves
@@ -255,7 +270,7 @@ void pack(const fadam_tensor* ts, int64_t n, const Dtypes& d, int grid,
           take = std::min(take, k);
         }
       }
-      items.push_back({pc.tensor, off, take, pc.vec});
+      items.push_back({pc.tensor, off, take, pc.level});
       acc += take * bpe + kItemOverhead;
       off += take;
       left -= take;
@@ -292,16 +307,16 @@ Item to_item(const fadam_tensor& t, const PackItem& pi, const Dtypes& d) {
   it.rem = static_cast<int16_t*>(adv(t.rem, 2));
   it.n = static_cast<int32_t>(pi.n);
   it.group = static_cast<uint16_t>(t.group);
-  it.flags = pi.vec ? kItemVec : 0;
+  it.flags = static_cast<uint16_t>((pi.level >= 1 ? kItemVec : 0) | (pi.level >= 2 ? kItemBulk : 0));
   return it;
 }
 
-const void* select_kernel(const Dtypes& d) {
+KernelEntry select_kernel(const Dtypes& d) {
   switch (d.g) {
     case FADAM_DT_F32: return kernel_gf32(d.out, d.rem);
     case FADAM_DT_BF16: return kernel_gbf16(d.out, d.rem);
     case FADAM_DT_F16: return kernel_gf16(d.out, d.rem);
-    default: return nullptr;
+    default: return {nullptr, 0};
   }
 }
 
@@ -333,13 +348,42 @@ void fill_kgroups(const fadam_group* groups, int32_t n_groups, uint32_t flags, K
   }
 }
 
+// Chunks of bulk tiles for the dynamically shared bulk pass: kChunkTiles
+// tiles each, or more when that keeps the list within max_chunks.  An item
+// is bulk-copied when every stream is 16-byte aligned (kItemBulk); its
+// tiles cover its vectors rounded down to an even count.
+void build_chunks(const std::vector<Item>& items, int64_t max_chunks, std::vector<Chunk>& chunks) {
+  int64_t total_tiles = 0;
+  auto tiles_of = [](const Item& it) -> int64_t {
+    if (!(it.flags & kItemBulk)) return 0;
+    const int64_t bv = (it.n / kVec) & ~int64_t(1);
+    return (bv + kBlock - 1) / kBlock;
+  };
+  for (const Item& it : items) total_tiles += tiles_of(it);
+  int64_t per = kChunkTiles;
+  // every item with tiles needs at least one chunk of its own
+  int64_t bulk_items = 0;
+  for (const Item& it : items) bulk_items += tiles_of(it) > 0;
+  const int64_t budget = std::max<int64_t>(1, max_chunks - bulk_items);
+  per = std::max<int64_t>(per, (total_tiles + budget - 1) / budget);
+  chunks.clear();
+  for (size_t k = 0; k < items.size(); ++k) {
+    const int64_t nt = tiles_of(items[k]);
+    for (int64_t t = 0; t < nt; t += per)
+      chunks.push_back(Chunk{static_cast<int32_t>(k), static_cast<int32_t>(t),
+                             static_cast<int32_t>(std::min(per, nt - t)), 0});
+  }
+}
+
 struct HostPlan {
   Dtypes d;
   uint32_t flags = 0;
   const void* kernel = nullptr;
+  size_t smem = 0;  // dynamic shared memory of a launch
   int device = 0, sm_count = 0, blocks_per_sm = 0, grid = 1;
   std::vector<Item> items;
   std::vector<int32_t> cta_begin;
+  std::vector<Chunk> chunks;
   int64_t n_elements = 0;
   double bytes = 0, check_bytes = 0;
 };
@@ -348,7 +392,7 @@ struct HostPlan {
 // fadam_step_once.  Allocates no device memory.
 fadam_status prepare(const fadam_tensor* tensors, int64_t n_tensors, const fadam_group* groups,
                      int32_t n_groups, const Dtypes& d, uint32_t flags, bool check_host_step,
-                     HostPlan& hp) {
+                     int64_t max_chunks, HostPlan& hp) {
   fadam_status st = check_dtypes(d, flags);
   if (st) return st;
   if (n_groups < 1 || n_groups > FADAM_MAX_GROUPS)
@@ -361,13 +405,18 @@ fadam_status prepare(const fadam_tensor* tensors, int64_t n_tensors, const fadam
 
   hp.d = d;
   hp.flags = flags;
-  hp.kernel = select_kernel(d);
+  const KernelEntry ke = select_kernel(d);
+  hp.kernel = ke.fn;
+  hp.smem = ke.smem;
   if (!hp.kernel) return fail(FADAM_EDTYPE, "no kernel for this dtype combination");
   cudaError_t e = cudaGetDevice(&hp.device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   e = cudaDeviceGetAttribute(&hp.sm_count, cudaDevAttrMultiProcessorCount, hp.device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&hp.blocks_per_sm, hp.kernel, kBlock, 0);
+  e = cudaFuncSetAttribute(hp.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(hp.smem));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(dynamic shared memory)");
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&hp.blocks_per_sm, hp.kernel, kBlock, hp.smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
   if (hp.blocks_per_sm < 1) return fail(FADAM_ECUDA, "kernel cannot be resident on this device");
 
@@ -379,6 +428,7 @@ fadam_status prepare(const fadam_tensor* tensors, int64_t n_tensors, const fadam
     return fail(FADAM_ELIMIT, "more than 2^31 work items");
   hp.items.reserve(pitems.size());
   for (const PackItem& pi : pitems) hp.items.push_back(to_item(tensors[pi.tensor], pi, d));
+  build_chunks(hp.items, max_chunks, hp.chunks);
   const double bpe = bytes_per_elem(d);
   for (int64_t i = 0; i < n_tensors; ++i) {
     const int64_t ne = std::max<int64_t>(tensors[i].numel, 0);
@@ -392,12 +442,12 @@ fadam_status prepare(const fadam_tensor* tensors, int64_t n_tensors, const fadam
   return FADAM_OK;
 }
 
-fadam_status launch(const void* kernel, const KParams& kp, int grid, bool cooperative,
+fadam_status launch(const void* kernel, size_t smem, const KParams& kp, int grid, bool cooperative,
                     cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kBlock);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   if (cooperative) {
@@ -421,6 +471,7 @@ struct fadam_plan {
   std::vector<char> has_tensor;
   int32_t n_groups = 0;
   Item* d_items = nullptr;
+  Chunk* d_chunks = nullptr;
   int32_t* d_cta = nullptr;
   KScratch* d_scratch = nullptr;
 };
@@ -429,18 +480,23 @@ namespace {
 
 void free_plan_memory(fadam_plan* p) {
   if (p->d_items) cudaFree(p->d_items);
+  if (p->d_chunks) cudaFree(p->d_chunks);
   if (p->d_cta) cudaFree(p->d_cta);
   if (p->d_scratch) cudaFree(p->d_scratch);
   p->d_items = nullptr;
+  p->d_chunks = nullptr;
   p->d_cta = nullptr;
   p->d_scratch = nullptr;
 }
 
-void fill_params(KParams& kp, const Item* items, const int32_t* cta, int32_t* noop,
-                 KScratch* scratch, const fadam_group* groups, int32_t n_groups, uint32_t flags) {
+void fill_params(KParams& kp, const Item* items, const int32_t* cta, const Chunk* chunks,
+                 int32_t n_chunks, int32_t* noop, KScratch* scratch, const fadam_group* groups,
+                 int32_t n_groups, uint32_t flags) {
   memset(&kp, 0, sizeof kp);
   kp.items = items;
   kp.cta_begin = cta;
+  kp.chunks = chunks;
+  kp.n_chunks = n_chunks;
   kp.noop = noop;
   kp.scratch = scratch;
   kp.n_groups = n_groups;
@@ -468,7 +524,8 @@ fadam_status fadam_plan_create(const fadam_tensor* tensors, int64_t n_tensors,
   fadam_plan* plan = new (std::nothrow) fadam_plan();
   if (!plan) return fail(FADAM_EINVAL, "out of host memory");
   // the host step of a regular plan is per-step data: checked at launch
-  fadam_status st = prepare(tensors, n_tensors, groups, n_groups, d, flags, false, plan->hp);
+  fadam_status st = prepare(tensors, n_tensors, groups, n_groups, d, flags, false, kPlanMaxChunks,
+                            plan->hp);
   if (st) {
     delete plan;
     return st;
@@ -482,6 +539,12 @@ fadam_status fadam_plan_create(const fadam_tensor* tensors, int64_t n_tensors,
     e = cudaMalloc(&plan->d_items, hp.items.size() * sizeof(Item));
     if (e == cudaSuccess)
       e = cudaMemcpy(plan->d_items, hp.items.data(), hp.items.size() * sizeof(Item),
+                     cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess && !hp.chunks.empty()) {
+    e = cudaMalloc(&plan->d_chunks, hp.chunks.size() * sizeof(Chunk));
+    if (e == cudaSuccess)
+      e = cudaMemcpy(plan->d_chunks, hp.chunks.data(), hp.chunks.size() * sizeof(Chunk),
                      cudaMemcpyHostToDevice);
   }
   if (e == cudaSuccess) e = cudaMalloc(&plan->d_cta, hp.cta_begin.size() * sizeof(int32_t));
@@ -530,9 +593,9 @@ fadam_status fadam_step(fadam_plan* plan, int32_t* noop_dev, fadam_stream stream
   DeviceGuard guard(hp.device);
   if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
   KParams kp;
-  fill_params(kp, plan->d_items, plan->d_cta, noop_dev, plan->d_scratch, plan->groups.data(),
-              plan->n_groups, hp.flags);
-  return launch(hp.kernel, kp, hp.grid, (hp.flags & FADAM_CHECK_FINITE) != 0,
+  fill_params(kp, plan->d_items, plan->d_cta, plan->d_chunks, static_cast<int32_t>(hp.chunks.size()),
+              noop_dev, plan->d_scratch, plan->groups.data(), plan->n_groups, hp.flags);
+  return launch(hp.kernel, hp.smem, kp, hp.grid, (hp.flags & FADAM_CHECK_FINITE) != 0,
                 reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -598,6 +661,7 @@ fadam_status fadam_plan_get_info(const fadam_plan* plan, fadam_plan_info* info) 
   info->n_tensors = static_cast<int64_t>(plan->tensors.size());
   info->n_elements = hp.n_elements;
   info->n_items = static_cast<int64_t>(hp.items.size());
+  info->n_chunks = static_cast<int64_t>(hp.chunks.size());
   info->grid = hp.grid;
   info->block = kBlock;
   info->blocks_per_sm = hp.blocks_per_sm;
@@ -649,13 +713,14 @@ fadam_status fadam_step_once(const fadam_tensor* tensors, int64_t n_tensors, int
     return fail(FADAM_EALIGN, "noop_dev is not 4-byte aligned");
   HostPlan hp;
   const Dtypes d{FADAM_DT_F32, g_dtype, out_dtype, false};
-  fadam_status st = prepare(tensors, n_tensors, &grp, 1, d, flags, true, hp);
+  fadam_status st = prepare(tensors, n_tensors, &grp, 1, d, flags, true, kPlanMaxChunks, hp);
   if (st) return st;
   if (!needs_launch(hp)) return FADAM_OK;
   DeviceGuard guard(hp.device);
   if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   Item* d_items = nullptr;
+  Chunk* d_chunks = nullptr;
   int32_t* d_cta = nullptr;
   KScratch* d_scratch = nullptr;
   cudaError_t e = cudaSuccess;
@@ -663,6 +728,12 @@ fadam_status fadam_step_once(const fadam_tensor* tensors, int64_t n_tensors, int
     e = cudaMallocAsync(&d_items, hp.items.size() * sizeof(Item), s);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(d_items, hp.items.data(), hp.items.size() * sizeof(Item),
+                          cudaMemcpyHostToDevice, s);
+  }
+  if (e == cudaSuccess && !hp.chunks.empty()) {
+    e = cudaMallocAsync(&d_chunks, hp.chunks.size() * sizeof(Chunk), s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(d_chunks, hp.chunks.data(), hp.chunks.size() * sizeof(Chunk),
                           cudaMemcpyHostToDevice, s);
   }
   if (e == cudaSuccess) e = cudaMallocAsync(&d_cta, hp.cta_begin.size() * sizeof(int32_t), s);
@@ -673,12 +744,14 @@ fadam_status fadam_step_once(const fadam_tensor* tensors, int64_t n_tensors, int
   if (e == cudaSuccess) e = cudaMemsetAsync(d_scratch, 0, sizeof(KScratch), s);
   if (e == cudaSuccess) {
     KParams kp;
-    fill_params(kp, d_items, d_cta, noop_dev, d_scratch, &grp, 1, flags);
-    st = launch(hp.kernel, kp, hp.grid, false, s);
+    fill_params(kp, d_items, d_cta, d_chunks, static_cast<int32_t>(hp.chunks.size()), noop_dev,
+                d_scratch, &grp, 1, flags);
+    st = launch(hp.kernel, hp.smem, kp, hp.grid, false, s);
   } else {
     st = cuda_fail(e, "one-shot upload");
   }
   if (d_items) cudaFreeAsync(d_items, s);
+  if (d_chunks) cudaFreeAsync(d_chunks, s);
   if (d_cta) cudaFreeAsync(d_cta, s);
   if (d_scratch) cudaFreeAsync(d_scratch, s);
   return st;
@@ -712,7 +785,7 @@ fadam_status fadam_pack_dry(const fadam_tensor* tensors, int64_t n_tensors, int3
       items_out[i].tensor = items[i].tensor;
       items_out[i].offset = items[i].offset;
       items_out[i].n = static_cast<int32_t>(items[i].n);
-      items_out[i].vec = items[i].vec ? 1 : 0;
+      items_out[i].vec = items[i].level;
     }
   }
   return FADAM_OK;
@@ -751,12 +824,14 @@ int32_t fadam_version(void) { return 10000; }
 namespace {
 
 constexpr int64_t kNoAllocMaxItems = 4096;
+constexpr int64_t kNoAllocMaxChunks = 4096;
 constexpr int32_t kNoAllocMaxCtas = 2048;
 constexpr size_t kArenaScratchOff = 0;
 constexpr size_t kArenaCtaOff = 256;
 constexpr size_t kArenaItemsOff =
     kArenaCtaOff + ((size_t(kNoAllocMaxCtas) + 1) * sizeof(int32_t) + 255) / 256 * 256;
-constexpr size_t kArenaBytes = kArenaItemsOff + size_t(kNoAllocMaxItems) * sizeof(Item);
+constexpr size_t kArenaChunksOff = kArenaItemsOff + size_t(kNoAllocMaxItems) * sizeof(Item);
+constexpr size_t kArenaBytes = kArenaChunksOff + size_t(kNoAllocMaxChunks) * sizeof(Chunk);
 static_assert(sizeof(KScratch) <= kArenaCtaOff, "status block fits its slot");
 
 constexpr int kMaxDevices = 64;
@@ -798,7 +873,8 @@ extern "C" fadam_status fadam_step_noalloc(const fadam_tensor* tensors, int64_t 
   if (noop_dev && reinterpret_cast<uintptr_t>(noop_dev) % 4)
     return fail(FADAM_EALIGN, "noop_dev is not 4-byte aligned");
   HostPlan hp;
-  fadam_status st = prepare(tensors, n_tensors, groups, n_groups, d, flags, true, hp);
+  fadam_status st = prepare(tensors, n_tensors, groups, n_groups, d, flags, true, kNoAllocMaxChunks,
+                            hp);
   if (st) return st;
   if (static_cast<int64_t>(hp.items.size()) > kNoAllocMaxItems)
     return fail(FADAM_ELIMIT,
@@ -816,11 +892,15 @@ extern "C" fadam_status fadam_step_noalloc(const fadam_tensor* tensors, int64_t 
   if (st) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   Item* items = reinterpret_cast<Item*>(arena + kArenaItemsOff);
+  Chunk* chunks = reinterpret_cast<Chunk*>(arena + kArenaChunksOff);
   int32_t* cta = reinterpret_cast<int32_t*>(arena + kArenaCtaOff);
   KScratch* scratch = reinterpret_cast<KScratch*>(arena + kArenaScratchOff);
   cudaError_t e = cudaSuccess;
   if (!hp.items.empty())
     e = cudaMemcpyAsync(items, hp.items.data(), hp.items.size() * sizeof(Item),
+                        cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && !hp.chunks.empty())
+    e = cudaMemcpyAsync(chunks, hp.chunks.data(), hp.chunks.size() * sizeof(Chunk),
                         cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(cta, hp.cta_begin.data(), hp.cta_begin.size() * sizeof(int32_t),
@@ -829,6 +909,7 @@ extern "C" fadam_status fadam_step_noalloc(const fadam_tensor* tensors, int64_t 
   if (e == cudaSuccess) e = cudaMemsetAsync(scratch, 0, sizeof(KScratch), s);
   if (e != cudaSuccess) return cuda_fail(e, "fadam_step_noalloc upload");
   KParams kp;
-  fill_params(kp, items, cta, noop_dev, scratch, groups, n_groups, flags);
-  return launch(hp.kernel, kp, hp.grid, (flags & FADAM_CHECK_FINITE) != 0, s);
+  fill_params(kp, items, cta, chunks, static_cast<int32_t>(hp.chunks.size()), noop_dev, scratch,
+              groups, n_groups, flags);
+  return launch(hp.kernel, hp.smem, kp, hp.grid, (flags & FADAM_CHECK_FINITE) != 0, s);
 }

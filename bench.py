@@ -263,11 +263,18 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     init_dist(world, "nccl")
     device = torch.device("cuda", local)
-    spec = workloads.large_uniform(n_tensors=args.n_tensors, numel=args.numel,
-                                   seed=1237 + 1000 * rank)
+    if args.workload == "large_uniform":
+        spec = workloads.large_uniform(n_tensors=args.n_tensors or 201, numel=args.numel,
+                                       seed=1237 + 1000 * rank)
+    elif args.workload == "many_small" and args.n_tensors:
+        spec = workloads.many_small(n_tensors=args.n_tensors, seed=1239 + 1000 * rank)
+    else:
+        spec = workloads.full_versions()[args.workload]
+        spec.seed += 1000 * rank
     shard = workloads.materialize(spec, device)
     groups = shard.param_groups()
-    cap = FusedAdamShard(groups, capturable=True)
+    kw = dict(remainders=spec.remainders, grad_scale=spec.grad_scale)
+    cap = FusedAdamShard(groups, capturable=True, **kw)
     info = cap.info()
     bytes_step = info["bytes_per_step"]
     elems = info["n_elements"]
@@ -279,7 +286,7 @@ def run_gpu(args):
         per, _ = time_launches(cap.step, args.steps, args.warmup, world)
         res["capturable"] = summarise(per, bytes_step, elems, world, device)
     if "regular" in variants:
-        reg = FusedAdamShard(groups, capturable=False)
+        reg = FusedAdamShard(groups, capturable=False, **kw)
         per, _ = time_launches(reg.step, args.steps, args.warmup, world)
         res["regular"] = summarise(per, bytes_step, elems, world, device)
         reg.close()
@@ -296,7 +303,7 @@ def run_gpu(args):
         res["graph_replay"] = summarise(per, bytes_step, elems, world, device)
         del graph
     if "check_finite" in variants:
-        chk = FusedAdamShard(groups, capturable=True, check_finite=True)
+        chk = FusedAdamShard(groups, capturable=True, check_finite=True, **kw)
         per, _ = time_launches(chk.step, args.steps, args.warmup, world)
         r = summarise(per, bytes_step, elems, world, device)
         r["gbs_including_screen"] = r["gbs"] * (bytes_step + chk.info()["check_bytes_per_step"]) / bytes_step
@@ -306,7 +313,7 @@ def run_gpu(args):
 
     e2e = None
     if "e2e" in variants:
-        host = [g.cpu().pin_memory() for g in shard.grads]
+        host = [shard.grads[i].cpu().pin_memory() for i in shard.plan_order()]
         for _ in range(max(1, args.warmup // 2)):
             cap.step_from_host(host)
         barrier(world)
@@ -331,8 +338,10 @@ def run_gpu(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"large_uniform: {args.n_tensors} fp32 tensors x {args.numel}, "
-                               "AdamW lr 1.6e-3 betas (0.9,0.95) eps 1e-8 wd 0.1, no param-out",
+        "config": {"workload": (f"large_uniform: {args.n_tensors or 201} fp32 tensors x {args.numel}, "
+                                "AdamW lr 1.6e-3 betas (0.9,0.95) eps 1e-8 wd 0.1, no param-out"
+                                if args.workload == "large_uniform" else
+                                f"{spec.name}: {len(spec.sizes)} tensors, {spec.n_elements} elements"),
                    "elements_per_step": elems, "bytes_per_step": bytes_step,
                    "bytes_per_element": bytes_step / elems, "grid": info["grid"],
                    "block": info["block"], "items": info["n_items"],
@@ -346,13 +355,13 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "peak_source": peaks["source"], "traffic": args.traffic,
-                     "kernel": "fadam_update_kernel<f32 grad, no out, fp32 master>"},
+                     "kernel": "fadam_update_kernel (bulk-copy pipeline)"},
         "clocks": clocks,
         "gpu_launches": args.steps,
     }
     if e2e:
         line["e2e"] = e2e
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "large_uniform":
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -368,7 +377,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--n-tensors", type=int, default=201)
+    ap.add_argument("--workload", default="large_uniform",
+                    choices=["large_uniform", "capturable_l2", "remainder_shard", "many_small"])
+    ap.add_argument("--n-tensors", type=int, default=None,
+                    help="tensor count of large_uniform (201) or many_small (20000)")
     ap.add_argument("--numel", type=int, default=320 * 65536)
     ap.add_argument("--variants", default="capturable,regular,graph,check_finite,e2e")
     ap.add_argument("--no-cpu-baseline", action="store_true")

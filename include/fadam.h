@@ -150,6 +150,7 @@ typedef struct {
   int64_t n_tensors;
   int64_t n_elements;     /* elements updated per step */
   int64_t n_items;        /* work items in the packed list */
+  int64_t n_chunks;       /* chunks of bulk-copy tiles the CTAs share out */
   int32_t grid;           /* CTAs of the persistent launch */
   int32_t block;          /* threads per CTA */
   int32_t blocks_per_sm;  /* resident CTAs per SM at this block size */
@@ -250,13 +251,15 @@ fadam_status fadam_step_once(const fadam_tensor* tensors, int64_t n_tensors, int
  * cudaMalloc/cudaFree could synchronise the device.  This call packs the
  * shard on the host, as fadam_plan_create does, and runs one step as
  * fadam_step does, but keeps the work list and the status block in a
- * static device array instead of allocated memory: about 264 KB that every
+ * static device array instead of allocated memory: about 330 KB that every
  * GPU which loads this library holds until the process exits.  It calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *
  * Limits: at most 4096 work items (roughly one per tensor plus one per CTA
  * of the grid) and 2048 CTAs; a larger shard is rejected with FADAM_ELIMIT
- * and a message from fadam_last_error(), before any device work.
+ * and a message from fadam_last_error(), before any device work.  Its list
+ * of tile chunks is capped at 4096 entries by making chunks larger, which
+ * can leave the CTAs a little less evenly loaded than a plan's.
  * Arguments: as fadam_plan_create, plus noop_dev and stream as fadam_step;
  * the step counters behave as in fadam_step.
  * The first call on a device looks up the array's device address (once per
@@ -277,9 +280,9 @@ typedef struct {
   int64_t tensor; /* index into the tensors array */
   int64_t offset; /* first element of the run within the tensor */
   int32_t n;      /* elements in the run */
-  int32_t vec;    /* 1 when every stream is 16-byte (fp32) / 8-byte (16-bit)
-                     aligned at the run start and the run takes the
-                     128-bit path */
+  int32_t vec;    /* alignment of every stream at the run start: 0 none
+                     (scalar path), 1 one 4-element vector (128-bit loads),
+                     2 also 16 bytes (bulk copies through shared memory) */
 } fadam_pack_item;
 
 /* Host-only dry run of the packer, for inspection and tests; needs no GPU

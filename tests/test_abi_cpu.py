@@ -248,15 +248,16 @@ def test_pack_covers_and_balances_full_workloads(recipe):
     assert max(costs) <= quota * 1.0001 + slack, (max(costs), quota)
     # the last CTA may end short by the overhead the packer reserved for cuts
     assert min(costs[:-1]) >= quota * 0.9999 - slack, (min(costs), quota)
-    # every run of an aligned allocation is vectorised and starts on a cut
-    assert all(vec == 1 for *_, vec in items)
+    # every run of a 256-byte aligned allocation takes the bulk-copy path and
+    # starts on a cut
+    assert all(vec == 2 for *_, vec in items)
     assert all(off % CUT == 0 for _, off, _, _ in items)
 
 
 def test_pack_peels_heads_and_falls_back_to_scalar():
     base = 1 << 40
     ts = [
-        # all streams one fp32 element past a 16-byte boundary: peel 3, then vector
+        # all streams one fp32 element past a 16-byte boundary: peel 3, then bulk
         _abi.Tensor(p=base + 4, m=base + 4096 + 4, v=base + 8192 + 4, g=base + 12288 + 4,
                     numel=1001, group=0),
         # residues disagree: the whole tensor runs scalar
@@ -268,19 +269,30 @@ def test_pack_peels_heads_and_falls_back_to_scalar():
     ]
     items, cta = _dry(ts, 1)
     _check_cover(ts, items)
-    assert items[0] == (0, 0, 3, 0) and items[1] == (0, 3, 998, 1)
+    assert items[0] == (0, 0, 3, 0) and items[1] == (0, 3, 998, 2)
     assert items[2] == (1, 0, 500, 0)
-    assert items[3][0] == 3 and items[3][3] == 1  # a 2-element aligned run: vector path, tail only
+    assert items[3][0] == 3 and items[3][3] == 2  # a 2-element aligned run: tail only
     assert cta == [0, len(items)]
 
 
-def test_pack_bf16_streams_align_at_8_bytes():
+def test_pack_peels_up_to_seven_for_16_byte_alignment():
     base = 1 << 40
-    # fp32 p/m/v at +8 bytes (residue 2 elements) and bf16 g at +4 bytes (residue 2)
+    # fp32 p/m/v at +8 bytes and bf16 g at +4 bytes: 6 elements later every
+    # stream sits on a 16-byte boundary
     t = _abi.Tensor(p=base + 8, m=base + 4096 + 8, v=base + 8192 + 8, g=base + 12288 + 4,
                     numel=100, group=0)
     items, _ = _dry([t], 1, g=_abi.DT_BF16)
-    assert items[0] == (0, 0, 2, 0) and items[1] == (0, 2, 98, 1)
+    assert items[0] == (0, 0, 6, 0) and items[1] == (0, 6, 94, 2)
+
+
+def test_pack_vector_level_when_16_bytes_is_out_of_reach():
+    base = 1 << 40
+    # two 16-bit streams that agree modulo one vector (8 bytes) but not
+    # modulo 16 bytes: 128-bit loads yes, bulk copies no
+    t = _abi.Tensor(p=base, m=base + 4096, v=base + 8192, g=base + 12288, p_out=base + 16384 + 8,
+                    numel=100, group=0)
+    items, _ = _dry([t], 1, g=_abi.DT_BF16, out=_abi.DT_BF16)
+    assert items == [(0, 0, 100, 1)]
 
 
 def test_pack_empty_shard():
