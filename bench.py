@@ -176,6 +176,47 @@ def summarise(per_ms, bytes_per_step, elems, world, device):
             "gbs": agg["gbs"], "gparams_per_s": agg["gparams_per_s"]}
 
 
+PROFILE = os.path.join(ROOT, "profiles", "fadam_update_kernel_large_uniform_8x20971520.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "include", "fadam.h")] + sorted(
+    os.path.join(ROOT, "adamw_optimizer_step_persistent_gb300", "csrc", f)
+    for f in os.listdir(os.path.join(ROOT, "adamw_optimizer_step_persistent_gb300", "csrc"))
+    if f.endswith((".cu", ".cuh", ".h")))
+
+
+def kernel_source_hash() -> str:
+    """sha256 over the CUDA library's sources (decides whether a stored ncu
+    traffic figure still describes the kernel that runs)."""
+    import hashlib
+    h = hashlib.sha256()
+    for path in KERNEL_SOURCES:
+        with open(path, "rb") as fh:
+            h.update(os.path.relpath(path, ROOT).encode())
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(elements: int):
+    """DRAM bytes per launch from the committed ncu summary of the headline
+    kernel, scaled from its capture case by elements, or None when the
+    kernel sources changed since the capture."""
+    try:
+        with open(PROFILE) as fh:
+            text = fh.read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line and line.split(":", 1)[0].strip() in ("source_sha256", "traffic_bytes_per_element"):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return float(fields["traffic_bytes_per_element"]) * elements
+    except (KeyError, ValueError):
+        return None
+
+
 def measured_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -354,7 +395,8 @@ def run_gpu(args):
                                   if "capturable" in res and "regular" in res else None),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "peak_source": peaks["source"], "traffic": args.traffic,
+                     "peak_source": peaks["source"],
+                     "traffic": (profiled_traffic(elems) if args.workload == "large_uniform" else None),
                      "kernel": "fadam_update_kernel (bulk-copy pipeline)"},
         "clocks": clocks,
         "gpu_launches": args.steps,
@@ -385,8 +427,6 @@ def main(argv=None):
     ap.add_argument("--variants", default="capturable,regular,graph,check_finite,e2e")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tensors", type=int, default=4)
-    ap.add_argument("--traffic", type=float, default=None,
-                    help="ncu dram bytes per launch for the headline kernel, if captured")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
