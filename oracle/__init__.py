@@ -55,6 +55,10 @@ def lib():
         L.oracle_adam_rem.argtypes = [_i64, ctypes.c_int, ctypes.c_int, _i32, _f32, _f32,
                                       _f32, _f32, _f32, _f32, _vp, _vp, _vp, _vp, _vp,
                                       ctypes.c_int, _vp]
+        L.oracle_adam_state.restype = None
+        L.oracle_adam_state.argtypes = [_i64, ctypes.c_int, ctypes.c_int, _i32, _f32, _f32,
+                                        _f32, _f32, _f32, _f32, _vp, _vp, _vp, ctypes.c_int,
+                                        _vp, ctypes.c_int, _vp, ctypes.c_int]
         L.oracle_adam_f64.restype = None
         L.oracle_adam_f64.argtypes = [_i64, ctypes.c_int, ctypes.c_int, _i32, _f32, _f32,
                                       _f32, _f32, _f32, _f32, _vp, _vp, _vp, _vp]
@@ -166,6 +170,24 @@ def adam_f32(group: Group, step: int, p, m, v, g, g_dtype=DT_F32, p_out=None,
                           _ptr(p_out) if out_dtype != DT_NONE else None, out_dtype)
 
 
+_S_NP = {DT_F32: np.float32, DT_BF16: np.uint16, DT_F16: np.uint16}
+
+
+def adam_state(group: Group, step: int, p, m, v, state_dtype, g, g_dtype=DT_F32, p_out=None,
+               out_dtype=DT_NONE) -> None:
+    """Update one tensor whose p, m, v all have `state_dtype` (in place)."""
+    n = p.size
+    for a, w in ((p, "p"), (m, "m"), (v, "v")):
+        _check(a, _S_NP[state_dtype], n, w)
+    _check(g, _G_NP[g_dtype], n, "g")
+    if out_dtype != DT_NONE:
+        _check(p_out, np.float32 if out_dtype == DT_F32 else np.uint16, n, "p_out")
+    lib().oracle_adam_state(n, group.mode, group.bias_correction, step, group.beta1,
+                            group.beta2, group.eps, group.weight_decay, group.lr,
+                            group.grad_scale, _ptr(p), _ptr(m), _ptr(v), state_dtype, _ptr(g),
+                            g_dtype, _ptr(p_out) if out_dtype != DT_NONE else None, out_dtype)
+
+
 def adam_rem(group: Group, step: int, p_hi, rem, m, v, g, g_dtype, p_out) -> None:
     """Update one tensor whose master is bf16 high half + int16 remainder."""
     n = p_hi.size
@@ -202,8 +224,9 @@ def any_nonfinite(g, g_dtype, grad_scale) -> bool:
 class Tensor:
     """One tensor of the shard, as numpy arrays updated in place.
 
-    For an fp32 master set ``p``; for the remainder form set ``p_hi`` (bf16
-    bits) and ``rem`` and give ``p_out`` (bf16 bits, may be ``p_hi`` itself).
+    For an fp32 master set ``p``; for 16-bit state set ``p``, ``m``, ``v`` as
+    uint16 bits and ``state_dtype``; for the remainder form set ``p_hi``
+    (bf16 bits) and ``rem`` and give ``p_out`` (bf16 bits, may be ``p_hi``).
     """
     group: int
     m: np.ndarray
@@ -215,6 +238,7 @@ class Tensor:
     rem: Optional[np.ndarray] = None
     p_out: Optional[np.ndarray] = None
     out_dtype: int = DT_NONE
+    state_dtype: int = DT_F32  # dtype of p, m and v (fp32 master form)
 
 
 @dataclass
@@ -259,6 +283,9 @@ def shard_step(shard: Shard, *, capturable: bool, noop: bool = False,
         step = shard.steps[shard.step_slot[t.group]]
         if t.rem is not None:
             adam_rem(grp, step, t.p_hi, t.rem, t.m, t.v, t.g, t.g_dtype, t.p_out)
+        elif t.state_dtype != DT_F32:
+            adam_state(grp, step, t.p, t.m, t.v, t.state_dtype, t.g, t.g_dtype, t.p_out,
+                       t.out_dtype)
         else:
             adam_f32(grp, step, t.p, t.m, t.v, t.g, t.g_dtype, t.p_out, t.out_dtype)
     return False

@@ -166,13 +166,16 @@ float oracle_bias_correction(float beta, int32_t step) {
   return (float)(1.0 - pow((double)beta, (double)step));
 }
 
-static float grad_at(const void* g, int g_dtype, int64_t i) {
-  switch (g_dtype) {
-    case ORC_DT_F32: return ((const float*)g)[i];
-    case ORC_DT_BF16: return oracle_bf16_to_f32(((const uint16_t*)g)[i]);
-    default: return oracle_f16_to_f32(((const uint16_t*)g)[i]);
+/* Element i of an array of the given dtype, widened to float (exact). */
+static float value_at(const void* a, int dtype, int64_t i) {
+  switch (dtype) {
+    case ORC_DT_F32: return ((const float*)a)[i];
+    case ORC_DT_BF16: return oracle_bf16_to_f32(((const uint16_t*)a)[i]);
+    default: return oracle_f16_to_f32(((const uint16_t*)a)[i]);
   }
 }
+
+static float grad_at(const void* g, int g_dtype, int64_t i) { return value_at(g, g_dtype, i); }
 
 static void put_out(void* out, int out_dtype, int64_t i, float x) {
   switch (out_dtype) {
@@ -232,6 +235,32 @@ void oracle_adam_f32(int64_t n, int mode, int bias_correction, int32_t step,
     float x = update_one(mode, beta1, beta2, eps, wd, lr, grad_scale, bc1, bc2, p[i],
                          &m[i], &v[i], grad_at(g, g_dtype, i));
     p[i] = x;
+    if (p_out) put_out(p_out, out_dtype, i, x);
+  }
+}
+
+/* One tensor whose master and moments are all of `state_dtype` (fp32,
+ * bf16 or fp16), as the functor's one type T for p, m and v: each value is
+ * widened to float, the update runs in float as above, and p, m, v are
+ * rounded back to the state dtype (to nearest, ties to even) when stored.
+ * p_out receives the float result cast to its own dtype. */
+void oracle_adam_state(int64_t n, int mode, int bias_correction, int32_t step, float beta1,
+                       float beta2, float eps, float wd, float lr, float grad_scale, void* p,
+                       void* m, void* v, int state_dtype, const void* g, int g_dtype,
+                       void* p_out, int out_dtype) {
+  float bc1 = 1.0f, bc2 = 1.0f;
+  if (bias_correction == 1) {
+    bc1 = oracle_bias_correction(beta1, step);
+    bc2 = oracle_bias_correction(beta2, step);
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    float mi = value_at(m, state_dtype, i);
+    float vi = value_at(v, state_dtype, i);
+    float x = update_one(mode, beta1, beta2, eps, wd, lr, grad_scale, bc1, bc2,
+                         value_at(p, state_dtype, i), &mi, &vi, grad_at(g, g_dtype, i));
+    put_out(p, state_dtype, i, x);
+    put_out(m, state_dtype, i, mi);
+    put_out(v, state_dtype, i, vi);
     if (p_out) put_out(p_out, out_dtype, i, x);
   }
 }

@@ -502,3 +502,67 @@ def test_preadvanced_counter_is_used_as_is():
     assert a.steps == b.steps == [1, 1, 1]
     for ta, tb in zip(a.tensors, b.tensors):
         assert ta.p.tobytes() == tb.p.tobytes()
+
+
+# ---- 16-bit optimizer state (p, m, v of one dtype T) ----------------------------
+
+@pytest.mark.parametrize("state_dtype", [DT_BF16, DT_F16])
+@pytest.mark.parametrize("name,d", _worked_examples(), ids=[r[0] for r in _worked_examples()])
+def test_worked_example_16bit_state_exact(name, d, state_dtype):
+    """Every value of the worked examples has at most 8 significant bits, so
+    it is exact in bf16 and fp16 as well and the 16-bit state path must give
+    the same results bit for bit."""
+    mode = MODE_ADAMW if d["mode"] == "adamw" else MODE_L2
+    grp = Group(mode=mode, bias_correction=int(d["bc"]), beta1=float(d["beta1"]),
+                beta2=float(d["beta2"]), eps=float(d["eps"]), weight_decay=float(d["wd"]),
+                lr=float(d["lr"]), grad_scale=float(d["gs"]))
+    conv = oracle.f32_to_bf16 if state_dtype == DT_BF16 else oracle.f32_to_f16
+    back = oracle.bf16_to_f32 if state_dtype == DT_BF16 else oracle.f16_to_f32
+    p, m, v = (conv(np.array([float(d[k])], np.float32)) for k in ("p", "m", "v"))
+    g = np.array([float(d["g"])], np.float32)
+    oracle.adam_state(grp, int(d["step"]), p, m, v, state_dtype, g, DT_F32)
+    assert back(p)[0] == np.float32(d["p_new"]), name
+    assert back(m)[0] == np.float32(d["m_new"]), name
+    assert back(v)[0] == np.float32(d["v_new"]), name
+
+
+@pytest.mark.parametrize("state_dtype", [DT_BF16, DT_F16])
+def test_16bit_state_is_widen_update_round(state_dtype):
+    """The 16-bit state update equals the fp32 update of the widened values,
+    each result rounded to the state dtype by torch's own conversion."""
+    n = 20_000
+    rng = np.random.default_rng(12)
+    tdt = torch.bfloat16 if state_dtype == DT_BF16 else torch.float16
+
+    def to16(x):
+        return torch.from_numpy(np.asarray(x, np.float32)).to(tdt).view(torch.int16).numpy().view(np.uint16)
+
+    def to32(b):
+        return torch.from_numpy(b.view(np.int16).copy()).view(tdt).float().numpy()
+
+    p = to16(rng.standard_normal(n))
+    m = to16(rng.standard_normal(n) * 1e-3)
+    v = to16(np.abs(rng.standard_normal(n)) * 1e-6)
+    g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    grp = Group(mode=MODE_ADAMW, weight_decay=0.1, beta1=0.9, beta2=0.95, lr=1e-3)
+    p32, m32, v32 = to32(p), to32(m), to32(v)
+    out = np.zeros(n, np.uint16)
+    oracle.adam_state(grp, 3, p, m, v, state_dtype, g, DT_F32, out, DT_BF16)
+    oracle.adam_f32(grp, 3, p32, m32, v32, g, DT_F32)
+    assert np.array_equal(p, to16(p32)) and np.array_equal(m, to16(m32))
+    assert np.array_equal(v, to16(v32))
+    ref_out = torch.from_numpy(p32.copy()).to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(out, ref_out.view(np.uint16))
+
+
+def test_fp32_state_through_the_generic_path_matches_adam_f32():
+    n = 5000
+    p0, g = _rand_problem(n, 13)
+    grp = Group(mode=MODE_L2, weight_decay=0.1, lr=1e-3)
+    a = [p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)]
+    b = [p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)]
+    for k in (1, 2, 3):
+        oracle.adam_f32(grp, k, *a, g, DT_F32)
+        oracle.adam_state(grp, k, *b, DT_F32, g, DT_F32)
+    for x, y in zip(a, b):
+        assert x.tobytes() == y.tobytes()
