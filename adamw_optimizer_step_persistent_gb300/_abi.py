@@ -20,6 +20,7 @@ MODE_L2, MODE_ADAMW = 0, 1
 DT_NONE, DT_F32, DT_BF16, DT_F16 = 0, 1, 2, 3
 # plan flags
 CAPTURABLE, REMAINDERS, CHECK_FINITE, STEP_PREADVANCED = 1, 2, 4, 8
+TEST_BARRIER_TIMEOUT = 0x80000000  # diagnostic: the screen's grid barrier runs out
 MAX_GROUPS = 32
 
 

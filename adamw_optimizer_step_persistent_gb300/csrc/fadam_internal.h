@@ -86,6 +86,7 @@ struct KScratch {
 constexpr uint32_t kCapturable = FADAM_CAPTURABLE;
 constexpr uint32_t kCheckFinite = FADAM_CHECK_FINITE;
 constexpr uint32_t kPreadvanced = FADAM_STEP_PREADVANCED;
+constexpr uint32_t kTestBarrierTimeout = FADAM_TEST_BARRIER_TIMEOUT;
 
 // Everything one launch needs, passed as a __grid_constant__ parameter.
 struct alignas(16) KParams {
@@ -107,11 +108,19 @@ struct KernelEntry {
   size_t smem;
 };
 
-// Kernel entry for the (g dtype, out dtype, remainders) combination, or a
-// null fn when the combination does not exist.  Defined per g dtype in
-// fadam_kernels_g{f32,bf16,f16}.cu.
-KernelEntry kernel_gf32(int out_dtype, bool remainders);
-KernelEntry kernel_gbf16(int out_dtype, bool remainders);
-KernelEntry kernel_gf16(int out_dtype, bool remainders);
+// Kernel entry for the (state dtype, g dtype, out dtype, remainders)
+// combination, or a null fn when the combination does not exist.  One
+// function per (state, g) pair, each in fadam_kernels_s<state>_g<g>.cu.
+#define FADAM_DECLARE_KERNELS(S, G) KernelEntry kernel_s##S##_g##G(int out_dtype, bool remainders);
+FADAM_DECLARE_KERNELS(f32, f32)
+FADAM_DECLARE_KERNELS(f32, bf16)
+FADAM_DECLARE_KERNELS(f32, f16)
+FADAM_DECLARE_KERNELS(bf16, f32)
+FADAM_DECLARE_KERNELS(bf16, bf16)
+FADAM_DECLARE_KERNELS(bf16, f16)
+FADAM_DECLARE_KERNELS(f16, f32)
+FADAM_DECLARE_KERNELS(f16, bf16)
+FADAM_DECLARE_KERNELS(f16, f16)
+#undef FADAM_DECLARE_KERNELS
 
 }  // namespace fadam

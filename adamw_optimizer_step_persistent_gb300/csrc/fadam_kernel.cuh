@@ -26,6 +26,10 @@
 //   4. the last CTA to finish resets the work counters and, for capturable
 //      plans, advances each step counter by (noop != 1).
 //
+// p, m and v share one state dtype ST (fp32, bf16 or fp16; the functor's one
+// type T), widened to float for the update and rounded back (nearest-even)
+// when stored; the remainder form keeps fp32 m and v.
+//
 // Element math follows "Enhance Distributed Fused Adam (#1794)",
 // DistAdamCapturableFunctor::local_step, one IEEE fp32 operation per step
 // of the printed expression (__f*_rn intrinsics: correctly rounded and never
@@ -209,21 +213,24 @@ __device__ __forceinline__ void rem_split(float x, unsigned short& hi, unsigned 
   hi = static_cast<unsigned short>((b >> 16) + (rem_bits >> 15));
 }
 
-// One 4-element vector of the fp32-master form, in registers.
-template <bool ADAMW, int GT, int OT>
-__device__ __forceinline__ void update4_f32(float4 P, float4 M, float4 V,
-                                            const typename Raw4<GT>::T& G, const Scal& s,
-                                            float4* p4, float4* m4, float4* v4, void* out, int i) {
-  float g[4];
+// One 4-element vector whose p, m, v have dtype ST, in registers: widened
+// to float, updated, rounded back to ST (nearest-even) when stored.
+template <bool ADAMW, int ST, int GT, int OT>
+__device__ __forceinline__ void update4_state(const typename Raw4<ST>::T& P,
+                                              const typename Raw4<ST>::T& M,
+                                              const typename Raw4<ST>::T& V,
+                                              const typename Raw4<GT>::T& G, const Scal& s, void* p,
+                                              void* m, void* v, void* out, int i) {
+  float g[4], x[4], mm[4], vv[4];
   widen4<GT>(G, g);
-  float x[4] = {P.x, P.y, P.z, P.w};
-  float m[4] = {M.x, M.y, M.z, M.w};
-  float v[4] = {V.x, V.y, V.z, V.w};
+  widen4<ST>(P, x);
+  widen4<ST>(M, mm);
+  widen4<ST>(V, vv);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) x[e] = adam_elem<ADAMW>(x[e], m[e], v[e], g[e], s);
-  __stcs(p4 + i, make_float4(x[0], x[1], x[2], x[3]));
-  __stcs(m4 + i, make_float4(m[0], m[1], m[2], m[3]));
-  __stcs(v4 + i, make_float4(v[0], v[1], v[2], v[3]));
+  for (int e = 0; e < 4; ++e) x[e] = adam_elem<ADAMW>(x[e], mm[e], vv[e], g[e], s);
+  store_out4<ST>(p, i, x);
+  store_out4<ST>(m, i, mm);
+  store_out4<ST>(v, i, vv);
   store_out4<OT>(out, i, x);
 }
 
@@ -262,18 +269,37 @@ __device__ __forceinline__ void update4_rem(const uint2& H, const uint2& R, floa
 constexpr int kStages = FADAM_STAGES;
 constexpr int kTile = kBlock;  // vectors per tile: one per thread
 
-// Byte layout of one tile in shared memory, by stream (per vector of 4
-// elements): p 16 (or the bf16 high halves 8 and the remainders 8), m 16,
-// v 16, g 16 or 8.
-constexpr int kOffM = 16 * kTile;
-constexpr int kOffV = 32 * kTile;
-constexpr int kOffG = 48 * kTile;
-template <int GT>
-__host__ __device__ constexpr int g_vec_bytes() { return GT == FADAM_DT_F32 ? 16 : 8; }
-template <int GT>
-__host__ __device__ constexpr unsigned tile_bytes() { return static_cast<unsigned>(kTile * (48 + g_vec_bytes<GT>())); }
-template <int GT>
-__host__ __device__ constexpr size_t smem_bytes() { return FADAM_BULK ? size_t(kStages) * tile_bytes<GT>() : 0; }
+template <int DT>
+__host__ __device__ constexpr int vec_bytes() { return DT == FADAM_DT_F32 ? 16 : 8; }
+
+// Byte layout of one update tile in shared memory, stream after stream, for
+// p, m, v of dtype ST (or, in remainder form, the bf16 high halves and the
+// int16 remainders with fp32 m and v) and g of dtype GT.
+template <int ST, int GT, bool REM>
+struct Layout {
+  static constexpr int kP = REM ? 8 : vec_bytes<ST>();    // bytes per vector of p
+  static constexpr int kR = REM ? 8 : 0;                  // ... of the remainders
+  static constexpr int kMV = REM ? 16 : vec_bytes<ST>();  // ... of m and of v
+  static constexpr int kG = vec_bytes<GT>();              // ... of g
+  static constexpr unsigned per_vector = kP + kR + 2 * kMV + kG;
+  // vectors of an update tile: two per thread when a vector carries at most
+  // 40 bytes (16-bit state), so every tile keeps about 64 KB in flight
+  static constexpr int update_vectors = (per_vector <= 40 ? 2 : 1) * kTile;
+  static constexpr int off_r = kP * update_vectors;
+  static constexpr int off_m = (kP + kR) * update_vectors;
+  static constexpr int off_v = off_m + kMV * update_vectors;
+  static constexpr int off_g = off_v + kMV * update_vectors;
+  static constexpr unsigned update_tile = per_vector * update_vectors;
+  // the screen copies only g, four vectors per thread
+  static constexpr int scan_vectors = 4 * kTile;
+  static constexpr unsigned scan_tile = scan_vectors * kG;
+  static constexpr unsigned stage = update_tile > scan_tile ? update_tile : scan_tile;
+};
+
+template <int ST, int GT, bool REM>
+__host__ __device__ constexpr size_t smem_bytes() {
+  return FADAM_BULK ? size_t(kStages) * Layout<ST, GT, REM>::stage : 0;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -343,39 +369,34 @@ __device__ __forceinline__ int bulk_tiles(const Item& it) {
 // What a pipeline pass moves through shared memory.
 enum class Pass { kUpdate, kScan };  // kScan: only g, for the inf/nan screen
 
-template <int GT, Pass PASS>
-__host__ __device__ constexpr unsigned bytes_per_vector() {
-  return PASS == Pass::kScan ? g_vec_bytes<GT>() : 48u + g_vec_bytes<GT>();
+// Vectors in one tile of a pass (Layout::update_vectors or ::scan_vectors).
+template <int ST, int GT, bool REM, Pass PASS>
+__host__ __device__ constexpr int tile_vectors() {
+  return PASS == Pass::kScan ? Layout<ST, GT, REM>::scan_vectors
+                             : Layout<ST, GT, REM>::update_vectors;
 }
-
-// Vectors in one tile: one per thread for the update; four per thread for
-// the screen, which moves only g and would otherwise keep too few bytes in
-// flight.
-template <Pass PASS>
-__host__ __device__ constexpr int tile_vectors() { return PASS == Pass::kScan ? 4 * kTile : kTile; }
 
 // Thread 0 of the CTA: start the copies of vectors [v0, v0 + len) of `it`
 // into buffer `slot % kStages`.
-template <int GT, bool REM, Pass PASS>
+template <int ST, int GT, bool REM, Pass PASS>
 __device__ __forceinline__ void issue_tile(const Item& it, int v0, unsigned len, unsigned slot,
                                            unsigned char* smem, uint64_t* full) {
-  constexpr int GB = g_vec_bytes<GT>();
+  using L = Layout<ST, GT, REM>;
   const unsigned b = slot % kStages;
-  unsigned char* st = smem + size_t(b) * tile_bytes<GT>();
+  unsigned char* st = smem + size_t(b) * L::stage;
   uint64_t* bar = full + b;
-  mbar_expect_tx(bar, len * bytes_per_vector<GT, PASS>());
+  const size_t v = static_cast<size_t>(v0);
   if constexpr (PASS == Pass::kScan) {
-    bulk_load(st, static_cast<const char*>(it.g) + size_t(v0) * GB, len * GB, bar);
+    mbar_expect_tx(bar, len * L::kG);
+    bulk_load(st, static_cast<const char*>(it.g) + v * L::kG, len * L::kG, bar);
   } else {
-    if constexpr (REM) {
-      bulk_load(st, static_cast<const char*>(it.p) + size_t(v0) * 8, len * 8, bar);
-      bulk_load(st + 8 * kTile, reinterpret_cast<const char*>(it.rem) + size_t(v0) * 8, len * 8, bar);
-    } else {
-      bulk_load(st, static_cast<const char*>(it.p) + size_t(v0) * 16, len * 16, bar);
-    }
-    bulk_load(st + kOffM, static_cast<const char*>(it.m) + size_t(v0) * 16, len * 16, bar);
-    bulk_load(st + kOffV, static_cast<const char*>(it.v) + size_t(v0) * 16, len * 16, bar);
-    bulk_load(st + kOffG, static_cast<const char*>(it.g) + size_t(v0) * GB, len * GB, bar);
+    mbar_expect_tx(bar, len * L::per_vector);
+    bulk_load(st, static_cast<const char*>(it.p) + v * L::kP, len * L::kP, bar);
+    if constexpr (REM)
+      bulk_load(st + L::off_r, reinterpret_cast<const char*>(it.rem) + v * L::kR, len * L::kR, bar);
+    bulk_load(st + L::off_m, static_cast<const char*>(it.m) + v * L::kMV, len * L::kMV, bar);
+    bulk_load(st + L::off_v, static_cast<const char*>(it.v) + v * L::kMV, len * L::kMV, bar);
+    bulk_load(st + L::off_g, static_cast<const char*>(it.g) + v * L::kG, len * L::kG, bar);
   }
 }
 
@@ -402,7 +423,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-template <int GT, bool REM, Pass PASS>
+template <int ST, int GT, bool REM, Pass PASS>
 __device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, unsigned* counter,
                                              unsigned char* smem, uint64_t* full, TileTag* tags) {
   if (pr.finished) return;
@@ -424,34 +445,40 @@ __device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, un
     pr.v = ch.tile0 * kTile;
     pr.vend = min((ch.tile0 + ch.ntiles) * kTile, bulk_vectors(pr.it));
   }
-  const int len = min(tile_vectors<PASS>(), pr.vend - pr.v);
+  const int len = min(tile_vectors<ST, GT, REM, PASS>(), pr.vend - pr.v);
   tags[pr.slot % kStages] = TileTag{pr.item, pr.v, len};
-  issue_tile<GT, REM, PASS>(pr.it, pr.v, static_cast<unsigned>(len), pr.slot, smem, full);
+  issue_tile<ST, GT, REM, PASS>(pr.it, pr.v, static_cast<unsigned>(len), pr.slot, smem, full);
   pr.v += len;
   ++pr.slot;
 }
 
-// Consume one tile from shared memory.
-template <bool ADAMW, int GT, int OT, bool REM>
+// Consume one tile from shared memory: thread t takes vectors t, t + kTile,
+// ... of it.
+template <bool ADAMW, int ST, int GT, int OT, bool REM>
 __device__ __forceinline__ void update_tile(const Item& it, const Scal& s, const unsigned char* st,
                                             int v0, int len) {
-  const int t = threadIdx.x;
-  if (t >= len) return;
-  const int i = v0 + t;
-  const float4 M = reinterpret_cast<const float4*>(st + kOffM)[t];
-  const float4 V = reinterpret_cast<const float4*>(st + kOffV)[t];
-  const typename Raw4<GT>::T G = reinterpret_cast<const typename Raw4<GT>::T*>(st + kOffG)[t];
-  if constexpr (REM) {
-    const uint2 H = reinterpret_cast<const uint2*>(st)[t];
-    const uint2 R = reinterpret_cast<const uint2*>(st + 8 * kTile)[t];
-    update4_rem<ADAMW, GT>(H, R, M, V, G, s, reinterpret_cast<uint2*>(it.rem),
-                           reinterpret_cast<float4*>(it.m), reinterpret_cast<float4*>(it.v),
-                           reinterpret_cast<uint2*>(it.p_out), i);
-  } else {
-    const float4 P = reinterpret_cast<const float4*>(st)[t];
-    update4_f32<ADAMW, GT, OT>(P, M, V, G, s, reinterpret_cast<float4*>(it.p),
-                               reinterpret_cast<float4*>(it.m), reinterpret_cast<float4*>(it.v),
-                               it.p_out, i);
+  using L = Layout<ST, GT, REM>;
+#pragma unroll
+  for (int q = 0; q < L::update_vectors / kTile; ++q) {
+    const int t = threadIdx.x + q * kTile;
+    if (t >= len) return;
+    const int i = v0 + t;
+    const typename Raw4<GT>::T G = reinterpret_cast<const typename Raw4<GT>::T*>(st + L::off_g)[t];
+    if constexpr (REM) {
+      const uint2 H = reinterpret_cast<const uint2*>(st)[t];
+      const uint2 R = reinterpret_cast<const uint2*>(st + L::off_r)[t];
+      const float4 M = reinterpret_cast<const float4*>(st + L::off_m)[t];
+      const float4 V = reinterpret_cast<const float4*>(st + L::off_v)[t];
+      update4_rem<ADAMW, GT>(H, R, M, V, G, s, reinterpret_cast<uint2*>(it.rem),
+                             reinterpret_cast<float4*>(it.m), reinterpret_cast<float4*>(it.v),
+                             reinterpret_cast<uint2*>(it.p_out), i);
+    } else {
+      using S4 = typename Raw4<ST>::T;
+      const S4 P = reinterpret_cast<const S4*>(st)[t];
+      const S4 M = reinterpret_cast<const S4*>(st + L::off_m)[t];
+      const S4 V = reinterpret_cast<const S4*>(st + L::off_v)[t];
+      update4_state<ADAMW, ST, GT, OT>(P, M, V, G, s, it.p, it.m, it.v, it.p_out, i);
+    }
   }
 }
 
@@ -459,7 +486,7 @@ template <int GT>
 __device__ __forceinline__ bool scan_tile(const unsigned char* st, int len, float gs) {
   bool bad = false;
 #pragma unroll
-  for (int q = 0; q < tile_vectors<Pass::kScan>() / kTile; ++q) {
+  for (int q = 0; q < 4; ++q) {  // Layout::scan_vectors = 4 * kTile
     const int t = threadIdx.x + q * kTile;
     if (t < len) {
       float g[4];
@@ -476,7 +503,7 @@ __device__ __forceinline__ bool scan_tile(const unsigned char* st, int len, floa
 // of the next chunk start while the current one is consumed).  `bad`
 // collects the scan's finding; a wait that gives up sets `timed_out` and
 // ends the pass for the CTA.
-template <int GT, int OT, bool REM, Pass PASS>
+template <int ST, int GT, int OT, bool REM, Pass PASS>
 __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp, unsigned* counter,
                                           unsigned char* smem, uint64_t* full, TileTag* tags,
                                           Producer& pr, unsigned& stage, bool& bad,
@@ -487,7 +514,7 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
     pr.vend = 0;
     pr.slot = stage;
     pr.finished = false;
-    for (int q = 0; q < kStages; ++q) produce_next<GT, REM, PASS>(pr, kp, counter, smem, full, tags);
+    for (int q = 0; q < kStages; ++q) produce_next<ST, GT, REM, PASS>(pr, kp, counter, smem, full, tags);
   }
   int cur_item = -1;
   Item it;
@@ -502,14 +529,14 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
           cur_item = tag.item;
           it = load_item(kp.items, tag.item);
         }
-        const unsigned char* st = smem + size_t(b) * tile_bytes<GT>();
+        const unsigned char* st = smem + size_t(b) * Layout<ST, GT, REM>::stage;
         const SGroup& G = sgrp[it.group];
         const Scal s{G.beta1, G.omb1, G.beta2, G.omb2, G.bc1, G.bc2, G.eps, G.wd, G.lr, G.gs};
         if constexpr (PASS == Pass::kScan) {
           bad |= scan_tile<GT>(st, tag.len, s.gs);
         } else {
-          if (G.bits & kGroupAdamW) update_tile<true, GT, OT, REM>(it, s, st, tag.v0, tag.len);
-          else update_tile<false, GT, OT, REM>(it, s, st, tag.v0, tag.len);
+          if (G.bits & kGroupAdamW) update_tile<true, ST, GT, OT, REM>(it, s, st, tag.v0, tag.len);
+          else update_tile<false, ST, GT, OT, REM>(it, s, st, tag.v0, tag.len);
         }
       }
     }
@@ -526,23 +553,20 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
     if (threadIdx.x == 0) {
       // order the generic-proxy reads of the buffer before its async refill
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      produce_next<GT, REM, PASS>(pr, kp, counter, smem, full, tags);
+      produce_next<ST, GT, REM, PASS>(pr, kp, counter, smem, full, tags);
     }
   }
 }
 
 // ---- element-wise paths (tails, runs not 16-byte aligned) -------------------
 
-template <bool ADAMW, int GT, int OT>
-__device__ __forceinline__ void update_elem_f32(const Item& it, const Scal& s, int i) {
-  float* p = reinterpret_cast<float*>(it.p);
-  float* mp = reinterpret_cast<float*>(it.m);
-  float* vp = reinterpret_cast<float*>(it.v);
-  float m = __ldcs(mp + i), v = __ldcs(vp + i);
-  const float x = adam_elem<ADAMW>(__ldcs(p + i), m, v, load1<GT>(it.g, i), s);
-  __stcs(p + i, x);
-  __stcs(mp + i, m);
-  __stcs(vp + i, v);
+template <bool ADAMW, int ST, int GT, int OT>
+__device__ __forceinline__ void update_elem_state(const Item& it, const Scal& s, int i) {
+  float m = load1<ST>(it.m, i), v = load1<ST>(it.v, i);
+  const float x = adam_elem<ADAMW>(load1<ST>(it.p, i), m, v, load1<GT>(it.g, i), s);
+  store_out1<ST>(it.p, i, x);
+  store_out1<ST>(it.m, i, m);
+  store_out1<ST>(it.v, i, v);
   store_out1<OT>(it.p_out, i, x);
 }
 
@@ -564,16 +588,16 @@ __device__ __forceinline__ void update_elem_rem(const Item& it, const Scal& s, i
   __stcs(op + i, oh);
 }
 
-template <bool ADAMW, int GT, int OT, bool REM>
+template <bool ADAMW, int ST, int GT, int OT, bool REM>
 __device__ __forceinline__ void update_elem(const Item& it, const Scal& s, int i) {
   if constexpr (REM) update_elem_rem<ADAMW, GT>(it, s, i);
-  else update_elem_f32<ADAMW, GT, OT>(it, s, i);
+  else update_elem_state<ADAMW, ST, GT, OT>(it, s, i);
 }
 
 // A whole item not aligned for bulk copies, by the whole CTA: 128-bit
 // streaming loads when every stream is vector-aligned, then element by
 // element for the rest.
-template <bool ADAMW, int GT, int OT, bool REM>
+template <bool ADAMW, int ST, int GT, int OT, bool REM>
 __device__ __forceinline__ void simt_item(const Item& it, const Scal& s) {
   const int n = it.n;
   int scalar_from = 0;
@@ -606,31 +630,29 @@ __device__ __forceinline__ void simt_item(const Item& it, const Scal& s) {
           if (i < nv) update4_rem<ADAMW, GT>(H[u], R[u], M[u], V[u], G[u], s, r4, m4, v4, o4, i);
         }
       } else {
-        float4* p4 = reinterpret_cast<float4*>(it.p);
-        float4* m4 = reinterpret_cast<float4*>(it.m);
-        float4* v4 = reinterpret_cast<float4*>(it.v);
-        float4 P[kUnroll], M[kUnroll], V[kUnroll];
+        typename Raw4<ST>::T P[kUnroll], M[kUnroll], V[kUnroll];
         typename Raw4<GT>::T G[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int i = base + u * kBlock;
           if (i < nv) {
-            P[u] = __ldcs(p4 + i);
-            M[u] = __ldcs(m4 + i);
-            V[u] = __ldcs(v4 + i);
+            P[u] = load4<ST>(it.p, i);
+            M[u] = load4<ST>(it.m, i);
+            V[u] = load4<ST>(it.v, i);
             G[u] = load4<GT>(it.g, i);
           }
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int i = base + u * kBlock;
-          if (i < nv) update4_f32<ADAMW, GT, OT>(P[u], M[u], V[u], G[u], s, p4, m4, v4, it.p_out, i);
+          if (i < nv)
+            update4_state<ADAMW, ST, GT, OT>(P[u], M[u], V[u], G[u], s, it.p, it.m, it.v, it.p_out, i);
         }
       }
     }
     scalar_from = nv * kVec;
   }
-  for (int i = scalar_from + threadIdx.x; i < n; i += kBlock) update_elem<ADAMW, GT, OT, REM>(it, s, i);
+  for (int i = scalar_from + threadIdx.x; i < n; i += kBlock) update_elem<ADAMW, ST, GT, OT, REM>(it, s, i);
 }
 
 // True when this thread saw a non-finite g*grad_scale in the item (by the
@@ -659,7 +681,7 @@ __device__ __forceinline__ bool simt_scan(const Item& it, float gs) {
 // Warps pull 32 items at a time from a launch-wide counter and each lane
 // takes one item's tail, so the many small latencies overlap across the
 // whole GPU.
-template <int GT, int OT, bool REM, Pass PASS>
+template <int ST, int GT, int OT, bool REM, Pass PASS>
 __device__ __forceinline__ bool tail_pass(const KParams& kp, const SGroup* sgrp, unsigned* counter,
                                           int n_items) {
   const int lane = threadIdx.x % 32;
@@ -679,8 +701,8 @@ __device__ __forceinline__ bool tail_pass(const KParams& kp, const SGroup* sgrp,
       if constexpr (PASS == Pass::kScan) {
         bad |= !isfinite(__fmul_rn(load1<GT>(it.g, i), s.gs));
       } else {
-        if (G.bits & kGroupAdamW) update_elem<true, GT, OT, REM>(it, s, i);
-        else update_elem<false, GT, OT, REM>(it, s, i);
+        if (G.bits & kGroupAdamW) update_elem<true, ST, GT, OT, REM>(it, s, i);
+        else update_elem<false, ST, GT, OT, REM>(it, s, i);
       }
     }
   }
@@ -692,7 +714,7 @@ __device__ __forceinline__ bool tail_pass(const KParams& kp, const SGroup* sgrp,
 // element).  Without the bulk pipeline every item goes this way.  The
 // threads first test kBlock items' flags at once, so a range of bulk items
 // is skipped in a few loads.
-template <int GT, int OT, bool REM, Pass PASS>
+template <int ST, int GT, int OT, bool REM, Pass PASS>
 __device__ __forceinline__ bool rest_pass(const KParams& kp, const SGroup* sgrp, int item_begin,
                                           int item_end) {
   __shared__ int s_count;
@@ -715,8 +737,8 @@ __device__ __forceinline__ bool rest_pass(const KParams& kp, const SGroup* sgrp,
       if constexpr (PASS == Pass::kScan) {
         bad |= simt_scan<GT>(it, s.gs);
       } else {
-        if (G.bits & kGroupAdamW) simt_item<true, GT, OT, REM>(it, s);
-        else simt_item<false, GT, OT, REM>(it, s);
+        if (G.bits & kGroupAdamW) simt_item<true, ST, GT, OT, REM>(it, s);
+        else simt_item<false, ST, GT, OT, REM>(it, s);
       }
     }
     __syncthreads();  // s_list is reused
@@ -726,22 +748,24 @@ __device__ __forceinline__ bool rest_pass(const KParams& kp, const SGroup* sgrp,
 
 // One full pass: the bulk tiles of the shard (dynamically shared), then
 // the rest of this CTA's items.
-template <int GT, int OT, bool REM, Pass PASS>
+template <int ST, int GT, int OT, bool REM, Pass PASS>
 __device__ __forceinline__ void run_pass(const KParams& kp, const SGroup* sgrp, int item_begin,
                                          int item_end, unsigned* counter, unsigned* tail_counter,
                                          int n_items, unsigned char* smem, uint64_t* full,
                                          TileTag* tags, Producer& pr, unsigned& stage, bool& bad,
                                          bool& timed_out) {
   if (FADAM_BULK && kp.n_chunks > 0 && !timed_out)
-    bulk_pass<GT, OT, REM, PASS>(kp, sgrp, counter, smem, full, tags, pr, stage, bad, timed_out);
-  if (FADAM_BULK) bad |= tail_pass<GT, OT, REM, PASS>(kp, sgrp, tail_counter, n_items);
-  bad |= rest_pass<GT, OT, REM, PASS>(kp, sgrp, item_begin, item_end);
+    bulk_pass<ST, GT, OT, REM, PASS>(kp, sgrp, counter, smem, full, tags, pr, stage, bad, timed_out);
+  if (FADAM_BULK) bad |= tail_pass<ST, GT, OT, REM, PASS>(kp, sgrp, tail_counter, n_items);
+  bad |= rest_pass<ST, GT, OT, REM, PASS>(kp, sgrp, item_begin, item_end);
 }
 
 // Grid-wide barrier for a cooperative launch.  The wait is bounded: after
 // kWaitLimitNs it records FADAM_ETIMEOUT in the status block and returns
 // false instead of hanging.
-__device__ __forceinline__ bool grid_barrier(KScratch* sc) {
+// `extra` > 0 (diagnostic) makes the barrier wait for that many CTAs more
+// than the grid has, so that every wait runs out.
+__device__ __forceinline__ bool grid_barrier(KScratch* sc, unsigned extra) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -749,7 +773,7 @@ __device__ __forceinline__ bool grid_barrier(KScratch* sc) {
     const unsigned gen = ld_acquire_u32(&sc->bar_gen);
     __threadfence();
     const unsigned arrived = atomicAdd(&sc->bar_count, 1u);
-    if (arrived == gridDim.x - 1) {
+    if (arrived == gridDim.x + extra - 1) {
       atomicExch(&sc->bar_count, 0u);
       __threadfence();
       atomicAdd(&sc->bar_gen, 1u);
@@ -773,7 +797,7 @@ __device__ __forceinline__ bool grid_barrier(KScratch* sc) {
 
 // ---- the kernel ---------------------------------------------------------------
 
-template <int GT, int OT, bool REM>
+template <int ST, int GT, int OT, bool REM>
 __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams kp) {
   __shared__ SGroup sgrp[FADAM_MAX_GROUPS];
   __shared__ int s_noop;
@@ -835,11 +859,11 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
   if (kp.flags & kCheckFinite) {
     bool bad = false;
     if (!s_noop)
-      run_pass<GT, OT, REM, Pass::kScan>(kp, sgrp, item_begin, item_end, &kp.scratch->next_scan,
+      run_pass<ST, GT, OT, REM, Pass::kScan>(kp, sgrp, item_begin, item_end, &kp.scratch->next_scan,
                                          &kp.scratch->next_tail_scan, n_items, s_tiles, s_full,
                                          s_tags, s_prod, stage, bad, timed_out);
     if (__syncthreads_or(bad) && tid == 0) atomicExch(kp.noop, 1);
-    barrier_ok = grid_barrier(kp.scratch);
+    barrier_ok = grid_barrier(kp.scratch, (kp.flags & kTestBarrierTimeout) ? 1u : 0u);
     if (tid == 0) s_noop = (ld_acquire_s32(kp.noop) == 1);
     __syncthreads();
   }
@@ -847,7 +871,7 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
   // 3. the update
   if (!s_noop && barrier_ok) {
     bool unused = false;
-    run_pass<GT, OT, REM, Pass::kUpdate>(kp, sgrp, item_begin, item_end, &kp.scratch->next_update,
+    run_pass<ST, GT, OT, REM, Pass::kUpdate>(kp, sgrp, item_begin, item_end, &kp.scratch->next_update,
                                          &kp.scratch->next_tail_update, n_items, s_tiles, s_full,
                                          s_tags, s_prod, stage, unused, timed_out);
   }
@@ -875,23 +899,25 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
   }
 }
 
-// Entry for one g dtype: every out dtype, with and without remainders.
-template <int GT>
+// Entry for one (state dtype, g dtype): every out dtype, and the remainder
+// form (bf16 high half + int16 remainder, fp32 m and v) under fp32 state.
+template <int ST, int GT>
 KernelEntry kernel_for(int out_dtype, bool remainders) {
-  const size_t smem = smem_bytes<GT>();
-  if (remainders)
-    return out_dtype == FADAM_DT_BF16
-               ? KernelEntry{reinterpret_cast<const void*>(&fadam_update_kernel<GT, FADAM_DT_BF16, true>), smem}
-               : KernelEntry{nullptr, 0};
+  if (remainders) {
+    if (ST != FADAM_DT_F32 || out_dtype != FADAM_DT_BF16) return {nullptr, 0};
+    return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_BF16, true>),
+            smem_bytes<ST, GT, true>()};
+  }
+  const size_t smem = smem_bytes<ST, GT, false>();
   switch (out_dtype) {
     case FADAM_DT_NONE:
-      return {reinterpret_cast<const void*>(&fadam_update_kernel<GT, FADAM_DT_NONE, false>), smem};
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_NONE, false>), smem};
     case FADAM_DT_F32:
-      return {reinterpret_cast<const void*>(&fadam_update_kernel<GT, FADAM_DT_F32, false>), smem};
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_F32, false>), smem};
     case FADAM_DT_BF16:
-      return {reinterpret_cast<const void*>(&fadam_update_kernel<GT, FADAM_DT_BF16, false>), smem};
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_BF16, false>), smem};
     case FADAM_DT_F16:
-      return {reinterpret_cast<const void*>(&fadam_update_kernel<GT, FADAM_DT_F16, false>), smem};
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_F16, false>), smem};
     default: return {nullptr, 0};
   }
 }

@@ -80,16 +80,21 @@ struct DeviceGuard {
 };
 
 struct Dtypes {
-  int32_t p, g, out;
+  int32_t p, g, out;  // p: the state dtype of p, m, v (bf16 high half in remainder form)
   bool rem;
 };
 
+// Element size of m and v: the state dtype, or fp32 in the remainder form.
+int mv_size(const Dtypes& d) { return d.rem ? 4 : elem_size(d.p); }
+
 fadam_status check_dtypes(const Dtypes& d, uint32_t flags) {
   const uint32_t known = FADAM_CAPTURABLE | FADAM_REMAINDERS | FADAM_CHECK_FINITE |
-                         FADAM_STEP_PREADVANCED;
+                         FADAM_STEP_PREADVANCED | FADAM_TEST_BARRIER_TIMEOUT;
   if (flags & ~known) return fail(FADAM_EINVAL, "unknown flag bits 0x%x", flags & ~known);
   if ((flags & FADAM_STEP_PREADVANCED) && !(flags & FADAM_CAPTURABLE))
     return fail(FADAM_EINVAL, "FADAM_STEP_PREADVANCED needs FADAM_CAPTURABLE");
+  if ((flags & FADAM_TEST_BARRIER_TIMEOUT) && !(flags & FADAM_CHECK_FINITE))
+    return fail(FADAM_EINVAL, "FADAM_TEST_BARRIER_TIMEOUT needs FADAM_CHECK_FINITE");
   if (d.g != FADAM_DT_F32 && d.g != FADAM_DT_BF16 && d.g != FADAM_DT_F16)
     return fail(FADAM_EDTYPE, "g dtype %d is not fp32, bf16 or fp16", d.g);
   if (d.out != FADAM_DT_NONE && elem_size(d.out) == 0)
@@ -99,8 +104,8 @@ fadam_status check_dtypes(const Dtypes& d, uint32_t flags) {
       return fail(FADAM_EDTYPE, "remainder mode needs bf16 params (p dtype %d)", d.p);
     if (d.out != FADAM_DT_BF16)
       return fail(FADAM_EDTYPE, "remainder mode writes a bf16 param-out (out dtype %d)", d.out);
-  } else if (d.p != FADAM_DT_F32) {
-    return fail(FADAM_EDTYPE, "p dtype %d needs FADAM_REMAINDERS (only fp32 otherwise)", d.p);
+  } else if (elem_size(d.p) == 0) {
+    return fail(FADAM_EDTYPE, "state dtype %d (p, m, v) is not fp32, bf16 or fp16", d.p);
   }
   return FADAM_OK;
 }
@@ -171,7 +176,8 @@ fadam_status check_tensors(const fadam_tensor* ts, int64_t n, int32_t n_groups, 
     if (d.rem ? t.rem == nullptr : t.rem != nullptr)
       return fail(FADAM_EINVAL, "tensor %lld: rem must be %s", (long long)i,
                   d.rem ? "non-NULL in remainder mode" : "NULL outside remainder mode");
-    if (misaligned(t.p, psz) || misaligned(t.m, 4) || misaligned(t.v, 4) || misaligned(t.g, gsz) ||
+    if (misaligned(t.p, psz) || misaligned(t.m, mv_size(d)) || misaligned(t.v, mv_size(d)) ||
+        misaligned(t.g, gsz) ||
         (t.p_out && misaligned(t.p_out, osz)) || (t.rem && misaligned(t.rem, 2)))
       return fail(FADAM_EALIGN, "tensor %lld: a pointer is not aligned to its element size",
                   (long long)i);
@@ -183,7 +189,7 @@ fadam_status check_tensors(const fadam_tensor* ts, int64_t n, int32_t n_groups, 
 double bytes_per_elem(const Dtypes& d) {
   const int gsz = elem_size(d.g);
   if (d.rem) return 2 + 2 + 2 + 2 + 8 + 8 + gsz;  // p_hi R, p_out W, rem R+W, m, v, g
-  return 8 + 8 + 8 + gsz + elem_size(d.out);       // p, m, v R+W, g R, p_out W
+  return 6.0 * elem_size(d.p) + gsz + elem_size(d.out);  // p, m, v R+W, g R, p_out W
 }
 
 struct PackItem {
@@ -208,7 +214,7 @@ struct Head {
 // every stream aligned to one 4-element vector, else nothing (scalar path).
 Head body_alignment(const fadam_tensor& t, const Dtypes& d) {
   const void* ptrs[6] = {t.p, t.m, t.v, t.g, t.p_out, t.rem};
-  const int esz[6] = {elem_size(d.p), 4, 4, elem_size(d.g), elem_size(d.out), 2};
+  const int esz[6] = {elem_size(d.p), mv_size(d), mv_size(d), elem_size(d.g), elem_size(d.out), 2};
   for (int64_t h = 0; h < 8; ++h) {
     bool ok = true;
     for (int s = 0; s < 6 && ok; ++s)
@@ -300,8 +306,8 @@ Item to_item(const fadam_tensor& t, const PackItem& pi, const Dtypes& d) {
   };
   Item it;
   it.p = adv(t.p, elem_size(d.p));
-  it.m = adv(t.m, 4);
-  it.v = adv(t.v, 4);
+  it.m = adv(t.m, mv_size(d));
+  it.v = adv(t.v, mv_size(d));
   it.g = adv(t.g, elem_size(d.g));
   it.p_out = adv(t.p_out, elem_size(d.out));
   it.rem = static_cast<int16_t*>(adv(t.rem, 2));
@@ -312,10 +318,19 @@ Item to_item(const fadam_tensor& t, const PackItem& pi, const Dtypes& d) {
 }
 
 KernelEntry select_kernel(const Dtypes& d) {
-  switch (d.g) {
-    case FADAM_DT_F32: return kernel_gf32(d.out, d.rem);
-    case FADAM_DT_BF16: return kernel_gbf16(d.out, d.rem);
-    case FADAM_DT_F16: return kernel_gf16(d.out, d.rem);
+  // the remainder form keeps fp32 m and v: its kernels sit with fp32 state
+  const int32_t st = d.rem ? FADAM_DT_F32 : d.p;
+  const int key = st * 4 + d.g;
+  switch (key) {
+    case FADAM_DT_F32 * 4 + FADAM_DT_F32: return kernel_sf32_gf32(d.out, d.rem);
+    case FADAM_DT_F32 * 4 + FADAM_DT_BF16: return kernel_sf32_gbf16(d.out, d.rem);
+    case FADAM_DT_F32 * 4 + FADAM_DT_F16: return kernel_sf32_gf16(d.out, d.rem);
+    case FADAM_DT_BF16 * 4 + FADAM_DT_F32: return kernel_sbf16_gf32(d.out, d.rem);
+    case FADAM_DT_BF16 * 4 + FADAM_DT_BF16: return kernel_sbf16_gbf16(d.out, d.rem);
+    case FADAM_DT_BF16 * 4 + FADAM_DT_F16: return kernel_sbf16_gf16(d.out, d.rem);
+    case FADAM_DT_F16 * 4 + FADAM_DT_F32: return kernel_sf16_gf32(d.out, d.rem);
+    case FADAM_DT_F16 * 4 + FADAM_DT_BF16: return kernel_sf16_gbf16(d.out, d.rem);
+    case FADAM_DT_F16 * 4 + FADAM_DT_F16: return kernel_sf16_gf16(d.out, d.rem);
     default: return {nullptr, 0};
   }
 }
@@ -434,8 +449,8 @@ fadam_status prepare(const fadam_tensor* tensors, int64_t n_tensors, const fadam
     const int64_t ne = std::max<int64_t>(tensors[i].numel, 0);
     hp.n_elements += ne;
     double b = ne * bpe;
-    // a param-out that aliases the fp32 master is the same stream
-    if (!d.rem && tensors[i].p_out && tensors[i].p_out == tensors[i].p) b -= ne * 4.0;
+    // a param-out that aliases the master (same dtype) is the same stream
+    if (!d.rem && tensors[i].p_out && tensors[i].p_out == tensors[i].p) b -= ne * double(elem_size(d.out));
     hp.bytes += b;
   }
   if (flags & FADAM_CHECK_FINITE) hp.check_bytes = hp.n_elements * double(elem_size(d.g));

@@ -49,15 +49,18 @@ class FusedAdamShard:
       params_out (optional), remainders (remainder mode only)
       lr, betas, eps, weight_decay, bias_correction, adam_w_mode
     A group with empty lists is allowed; its step counter still advances.
-    ``params`` are fp32 masters, or in remainder mode the bf16 high halves
-    (``remainders`` then holds the int16 low halves and ``params_out`` the
-    bf16 tensors that receive the new high halves; they may be ``params``).
+    ``params`` are the masters and set the state dtype: fp32, bf16 or fp16,
+    with ``exp_avgs`` and ``exp_avg_sqs`` of the same dtype (updated in
+    float, rounded back on store); in remainder mode they are the bf16 high
+    halves (``remainders`` then holds the int16 low halves, the moments are
+    fp32, and ``params_out`` the bf16 tensors that receive the new high
+    halves; they may be ``params``).
     """
 
     def __init__(self, param_groups: Sequence[Dict], *, capturable: bool = False,
                  check_finite: bool = False, remainders: bool = False,
                  shared_step: bool = False, step_preadvanced: bool = False,
-                 grad_scale: float = 1.0, device=None):
+                 grad_scale: float = 1.0, device=None, extra_flags: int = 0):
         if check_finite and not capturable:
             raise ValueError("check_finite needs capturable=True (the counters live on the device)")
         self.capturable = capturable
@@ -70,11 +73,12 @@ class FusedAdamShard:
         flags = (_abi.CAPTURABLE if capturable else 0) | (_abi.REMAINDERS if remainders else 0)
         flags |= (_abi.CHECK_FINITE if check_finite else 0)
         flags |= (_abi.STEP_PREADVANCED if step_preadvanced else 0)
+        flags |= int(extra_flags)
         self.flags = flags
 
         descs = []
         g_dtype = out_dtype = None
-        p_dtype = torch.bfloat16 if remainders else torch.float32
+        p_dtype = torch.bfloat16 if remainders else None
         for gi, g in enumerate(self.groups):
             ps, ms, vs, gs = g["params"], g["exp_avgs"], g["exp_avg_sqs"], g["grads"]
             outs = g.get("params_out") or [None] * len(ps)
@@ -85,8 +89,10 @@ class FusedAdamShard:
                 for t in (p, m, v, gr, o, r):
                     if t is not None and (not t.is_contiguous() or t.device != self.device):
                         raise ValueError("tensors must be contiguous and on the shard's device")
-                if p.dtype != p_dtype or m.dtype != torch.float32 or v.dtype != torch.float32:
-                    raise TypeError(f"group {gi}: p must be {p_dtype}, m and v fp32")
+                p_dtype = p_dtype or p.dtype
+                mv_dtype = torch.float32 if remainders else p_dtype
+                if p.dtype != p_dtype or m.dtype != mv_dtype or v.dtype != mv_dtype:
+                    raise TypeError(f"group {gi}: p must be {p_dtype}, m and v {mv_dtype}")
                 g_dtype = g_dtype or gr.dtype
                 if gr.dtype != g_dtype:
                     raise TypeError("every grad must have the same dtype")
@@ -100,6 +106,8 @@ class FusedAdamShard:
                                          p_out=_ptr(o), rem=_ptr(r), numel=p.numel(), group=gi))
                 self._keep += [t for t in (p, m, v, gr, o, r) if t is not None]
         self.n_tensors = len(descs)
+        p_dtype = p_dtype or torch.float32
+        self.state_dtype = p_dtype
         self.g_dtype = g_dtype or torch.float32
         self.out_dtype = out_dtype
 

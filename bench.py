@@ -420,7 +420,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="large_uniform",
-                    choices=["large_uniform", "capturable_l2", "remainder_shard", "many_small"])
+                    choices=["large_uniform", "capturable_l2", "remainder_shard", "many_small",
+                             "large_uniform_bf16_state"])
     ap.add_argument("--n-tensors", type=int, default=None,
                     help="tensor count of large_uniform (201) or many_small (20000)")
     ap.add_argument("--numel", type=int, default=320 * 65536)

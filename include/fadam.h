@@ -88,6 +88,12 @@ typedef int32_t fadam_status;
 #define FADAM_CHECK_FINITE 4u /* screen g*grad_scale for inf/nan first; sets noop */
 #define FADAM_STEP_PREADVANCED 8u /* capturable: *step_dev already advanced by the
                                      caller; use it as is and do not write it */
+/* Diagnostic, for testing the failure path: with FADAM_CHECK_FINITE, the
+ * grid barrier after the inf/nan screen waits for one more CTA than the
+ * launch has, so every CTA's wait runs out after its limit (about 2 s).
+ * The step then updates nothing, advances no counter, and
+ * fadam_plan_status() reports FADAM_ETIMEOUT.  Never set in normal use. */
+#define FADAM_TEST_BARRIER_TIMEOUT 0x80000000u
 
 /* Maximum number of param groups in one plan. */
 #define FADAM_MAX_GROUPS 32

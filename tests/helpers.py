@@ -2,7 +2,8 @@
 
 Tolerances (GPU vs oracle):
   fp32 p, m, v:        |d| <= 2e-6 * |x| + 1e-9   (x the oracle value)
-  bf16/fp16 param-out: at most 1 unit in the last place
+  bf16/fp16 param-out, and p, m, v kept in a 16-bit state dtype: at most
+                       1 unit in the last place
   noop, step counters, remainder round trip: bit-exact
 """
 from __future__ import annotations
@@ -66,6 +67,7 @@ def oracle_shard(shard: workloads.Shard, idx: List[int] = None, elems: Dict[int,
             t.out_dtype = oracle.DT_BF16
         else:
             t.p = to_np(sel(shard.params[i]))
+            t.state_dtype = _ODT[spec.state_dtype]
             if spec.out_dtype is not None:
                 t.p_out = to_np(sel(shard.params_out[i]))
                 t.out_dtype = _ODT[spec.out_dtype]
@@ -134,8 +136,18 @@ def compare(shard: workloads.Shard, osh: oracle.Shard, idx=None, elems=None,
     report = report or Report()
     spec = shard.spec
     idx = shard.plan_order() if idx is None else idx
+    state16 = not spec.remainders and spec.state_dtype != torch.float32
     for t, i in zip(osh.tensors, idx):
         sel = (lambda x: x) if elems is None else (lambda x, e=torch.as_tensor(elems[i], device=shard.params[i].device): x[e])
+        if state16:  # 16-bit p, m, v: within one unit in the last place
+            report.ulp16(to_np(sel(shard.exp_avgs[i])), t.m, f"tensor {i} m")
+            report.ulp16(to_np(sel(shard.exp_avg_sqs[i])), t.v, f"tensor {i} v")
+            report.ulp16(to_np(sel(shard.params[i])), t.p, f"tensor {i} p")
+            if spec.out_dtype == torch.float32:
+                report.f32(to_np(sel(shard.params_out[i])), t.p_out, f"tensor {i} p_out")
+            elif spec.out_dtype is not None:
+                report.ulp16(to_np(sel(shard.params_out[i])), t.p_out, f"tensor {i} p_out")
+            continue
         report.f32(to_np(sel(shard.exp_avgs[i])), t.m, f"tensor {i} m")
         report.f32(to_np(sel(shard.exp_avg_sqs[i])), t.v, f"tensor {i} v")
         if spec.remainders:

@@ -77,13 +77,14 @@ def _create(tensors, groups, p=_abi.DT_F32, g=_abi.DT_F32, out=_abi.DT_NONE, fla
 
 @pytest.mark.parametrize("case,want", [
     ("no_groups", _abi.EINVAL), ("too_many_groups", _abi.EINVAL), ("bad_g_dtype", _abi.EDTYPE),
-    ("rem_needs_bf16_p", _abi.EDTYPE), ("bf16_p_needs_rem", _abi.EDTYPE),
+    ("rem_needs_bf16_p", _abi.EDTYPE), ("bad_state_dtype", _abi.EDTYPE),
     ("rem_needs_bf16_out", _abi.EDTYPE), ("unknown_flag", _abi.EINVAL),
     ("preadvanced_needs_capturable", _abi.EINVAL), ("group_out_of_range", _abi.EINVAL),
     ("negative_numel", _abi.EINVAL), ("null_p", _abi.EINVAL), ("out_ptr_without_dtype", _abi.EINVAL),
     ("missing_out_ptr", _abi.EINVAL), ("rem_without_flag", _abi.EINVAL),
     ("misaligned_m", _abi.EALIGN), ("misaligned_bf16_g", _abi.EALIGN),
     ("numel_beyond_max", _abi.ELIMIT), ("bad_mode", _abi.EINVAL), ("beta_one", _abi.EINVAL),
+    ("misaligned_16bit_state_m", _abi.EALIGN), ("timeout_diag_needs_screen", _abi.EINVAL),
     ("negative_eps", _abi.EINVAL), ("nan_lr", _abi.EINVAL),
     ("capturable_without_step_dev", _abi.EINVAL), ("capturable_without_lr_dev", _abi.EINVAL),
     ("misaligned_step_dev", _abi.EALIGN),
@@ -98,8 +99,8 @@ def test_plan_create_rejects(case, want):
         kw["g"] = 7
     elif case == "rem_needs_bf16_p":
         kw.update(flags=_abi.REMAINDERS, out=_abi.DT_BF16)
-    elif case == "bf16_p_needs_rem":
-        kw["p"] = _abi.DT_BF16
+    elif case == "bad_state_dtype":
+        kw["p"] = 9
     elif case == "rem_needs_bf16_out":
         kw.update(flags=_abi.REMAINDERS, p=_abi.DT_BF16, out=_abi.DT_F32)
     elif case == "unknown_flag":
@@ -125,6 +126,11 @@ def test_plan_create_rejects(case, want):
         kw["g"] = _abi.DT_BF16
     elif case == "numel_beyond_max":
         t = [_tensor(numel=(1 << 40) + 1)]
+    elif case == "misaligned_16bit_state_m":
+        t = [_tensor(m=FAKE + 1)]
+        kw["p"] = _abi.DT_BF16
+    elif case == "timeout_diag_needs_screen":
+        kw["flags"] = _abi.TEST_BARRIER_TIMEOUT
     elif case == "bad_mode":
         g = [_group(mode=2)]
     elif case == "beta_one":
@@ -306,3 +312,13 @@ def test_pack_splits_huge_tensor_into_bounded_items():
     _check_cover(t, items)
     assert max(n for _, _, n, _ in items) <= 1 << 26
     assert len(items) >= 32
+
+
+def test_pack_16bit_state_aligns_every_stream_to_16_bytes():
+    base = 1 << 40
+    # bf16 p, m, v and fp32 g: p, m, v at +4 bytes (2 elements), g at +8 bytes
+    # (2 elements): 6 elements later all four sit on 16-byte boundaries
+    t = _abi.Tensor(p=base + 4, m=base + 4096 + 4, v=base + 8192 + 4, g=base + 12288 + 8,
+                    numel=200, group=0)
+    items, _ = _dry([t], 1, p=_abi.DT_BF16)
+    assert items[0] == (0, 0, 6, 0) and items[1] == (0, 6, 194, 2)

@@ -305,3 +305,57 @@ def test_abi_rejects_bad_calls_without_launching():
     # set_groups refuses a different group count
     grp = (_abi.Group * 2)()
     assert L.fadam_plan_set_groups(opt._plan, grp, 2) == _abi.EINVAL
+
+
+def test_grid_barrier_wait_runs_out_and_reports_timeout():
+    """The screen's grid barrier is told to wait for one CTA more than the
+    launch has (a flag nothing sets): every wait gives up after its limit,
+    nothing is updated, no counter moves, the status reads FADAM_ETIMEOUT,
+    and the next ordinary step on the same context works."""
+    spec = workloads.small_versions()["tiny_adamw"]
+    shard = workloads.materialize(spec, DEV)
+    bad = FusedAdamShard(shard.param_groups(), capturable=True, check_finite=True,
+                         extra_flags=_abi.TEST_BARRIER_TIMEOUT)
+    snap = helpers.snapshot(shard)
+    bad.step()
+    torch.cuda.synchronize()
+    assert helpers.state_equal(shard, snap)
+    assert bad.group_steps() == [0, 0] and bad.noop.item() == 0
+    assert bad.device_status() == _abi.ETIMEOUT
+    assert bad.device_status() == _abi.OK  # reading clears it
+    bad.close()
+    good = FusedAdamShard(shard.param_groups(), capturable=True, check_finite=True)
+    osh = helpers.oracle_shard(shard)
+    good.step()
+    oracle.shard_step(osh, capturable=True)
+    torch.cuda.synchronize()
+    helpers.compare(shard, osh)
+    assert good.group_steps() == [1, 1] and good.device_status() == _abi.OK
+
+
+@pytest.mark.parametrize("state_dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("g_dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("out_dtype", [None, torch.float32, torch.bfloat16])
+def test_16bit_state_matches_oracle(state_dtype, g_dtype, out_dtype):
+    """p, m, v in one 16-bit dtype (the functor's single type T), several
+    steps, ragged sizes, both modes and bias corrections."""
+    spec = workloads.large_uniform(n_tensors=3, numel=40_003, state_dtype=state_dtype,
+                                   g_dtype=g_dtype)
+    spec.sizes = [40_003, 7, 131_072 + 5]
+    spec.group_of = [0, 1, 1]
+    spec.groups = [spec.groups[0], workloads.GroupSpec(adam_w_mode=False, weight_decay=0.05,
+                                                       bias_correction=False)]
+    spec.out_dtype = out_dtype
+    for capturable in (False, True):
+        shard, opt, osh = _run(spec, 4, capturable=capturable)
+        rep = helpers.compare(shard, osh)
+        assert opt.group_steps() == [4, 4]
+        assert rep.exact_fraction == 1.0, rep.exact_fraction
+
+
+def test_16bit_state_shard_full_oracle_and_graph():
+    spec = workloads.small_versions()["many_small"]
+    spec.state_dtype = torch.bfloat16
+    shard, opt, osh = _run(spec, 3)
+    helpers.compare(shard, osh)
+    assert opt.group_steps() == [3, 3, 3]

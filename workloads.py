@@ -17,6 +17,8 @@ Five shard recipes, all synthetic (no dataset or checkpoint is involved):
 3. ``large_uniform``: 201 fp32 tensors of 20,971,520 elements (the sizes of
    the TE issue's adam_bench.py), p ~ N(0,1), g = N(0,1)*1e-3, AdamW,
    lr 1.6e-3, betas (0.9, 0.95), eps 1e-8, wd 0.1, no param-out copy.
+   A variant keeps p, m, v in bf16 or fp16 (``state_dtype``), with bf16
+   grads: 14 bytes per element.
 4. ``remainder_shard``: one contiguous 1.2e9-element bucket cut into 512
    views of log-uniform size in [4096, 16,777,216] scaled to sum to 1.2e9,
    view starts rounded up to 64 elements (the 128-byte alignment rule of
@@ -28,8 +30,8 @@ Five shard recipes, all synthetic (no dataset or checkpoint is involved):
    group 0 AdamW wd 0.1 (the large ones), group 1 L2 wd 0 (the small ones),
    group 2 empty; per-group device step counters.
 
-Every recipe takes a ``scale`` that shrinks the sizes for tests that the
-oracle must finish in seconds; ``scale=1`` is the full workload.
+Every recipe takes size arguments that shrink it for tests the oracle must
+finish in seconds (``small_versions``); the defaults are the full workloads.
 """
 from __future__ import annotations
 
@@ -64,6 +66,7 @@ class ShardSpec:
     g_dtype: torch.dtype = torch.float32
     out_dtype: Optional[torch.dtype] = None
     remainders: bool = False
+    state_dtype: torch.dtype = torch.float32  # p, m, v (fp32 unless 16-bit state)
     capturable: bool = False
     grad_std: float = 1e-3
     grad_scale: float = 1.0
@@ -98,10 +101,13 @@ def capturable_l2(layers: int = 8, hidden: int = 4096, ffn: int = 11008,
                      grad_scale=1.0 / 65536, seed=seed, inf_at_step=3)
 
 
-def large_uniform(n_tensors: int = 201, numel: int = 320 * 65536, seed: int = 1237) -> ShardSpec:
+def large_uniform(n_tensors: int = 201, numel: int = 320 * 65536, seed: int = 1237,
+                  state_dtype: torch.dtype = torch.float32,
+                  g_dtype: torch.dtype = torch.float32) -> ShardSpec:
     g = GroupSpec(adam_w_mode=True, lr=1.6e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1)
-    return ShardSpec("large_uniform", [g], [numel] * n_tensors, [0] * n_tensors,
-                     grad_std=1e-3, seed=seed)
+    name = "large_uniform" if state_dtype == torch.float32 else "large_uniform_16bit_state"
+    return ShardSpec(name, [g], [numel] * n_tensors, [0] * n_tensors, g_dtype=g_dtype,
+                     state_dtype=state_dtype, grad_std=1e-3, seed=seed)
 
 
 def remainder_shard(total: int = 1_200_000_000, n_views: int = 512, lo: int = 4096,
@@ -154,7 +160,9 @@ def small_versions() -> Dict[str, ShardSpec]:
 def full_versions() -> Dict[str, ShardSpec]:
     return {"tiny_adamw": tiny_adamw(), "capturable_l2": capturable_l2(),
             "large_uniform": large_uniform(), "remainder_shard": remainder_shard(),
-            "many_small": many_small()}
+            "many_small": many_small(),
+            "large_uniform_bf16_state": large_uniform(state_dtype=torch.bfloat16,
+                                                      g_dtype=torch.bfloat16)}
 
 
 # ---- materialising a shard ----------------------------------------------------
@@ -225,11 +233,11 @@ def materialize(spec: ShardSpec, device="cuda") -> Shard:
             v = buckets["v"][o:o + s]
             g = buckets["g"][o:o + s]
         else:
-            p = torch.empty(s, dtype=torch.bfloat16 if spec.remainders else torch.float32,
-                            device=dev)
+            sdt = torch.float32 if spec.remainders else spec.state_dtype
+            p = torch.empty(s, dtype=torch.bfloat16 if spec.remainders else sdt, device=dev)
             r = torch.empty(s, dtype=torch.int16, device=dev) if spec.remainders else None
-            m = torch.zeros(s, dtype=torch.float32, device=dev)
-            v = torch.zeros(s, dtype=torch.float32, device=dev)
+            m = torch.zeros(s, dtype=sdt, device=dev)
+            v = torch.zeros(s, dtype=sdt, device=dev)
             g = torch.empty(s, dtype=spec.g_dtype, device=dev)
         if spec.remainders:
             hi = torch.randn(s, generator=gen, device=dev).to(torch.bfloat16)
@@ -240,7 +248,7 @@ def materialize(spec: ShardSpec, device="cuda") -> Shard:
             r.copy_(torch.randint(-32768, 32768, (s,), generator=gen, device=dev,
                                   dtype=torch.int32).to(torch.int16))
         else:
-            p.copy_(torch.randn(s, generator=gen, device=dev))
+            p.copy_(torch.randn(s, generator=gen, device=dev).to(p.dtype))
         g.copy_((torch.randn(s, generator=gen, device=dev) * spec.grad_std).to(spec.g_dtype))
         params.append(p)
         ms.append(m)
