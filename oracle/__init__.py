@@ -62,6 +62,8 @@ def lib():
         L.oracle_adam_f64.restype = None
         L.oracle_adam_f64.argtypes = [_i64, ctypes.c_int, ctypes.c_int, _i32, _f32, _f32,
                                       _f32, _f32, _f32, _f32, _vp, _vp, _vp, _vp]
+        L.oracle_sumsq.restype = ctypes.c_double
+        L.oracle_sumsq.argtypes = [_i64, _vp, ctypes.c_int]
         L.oracle_any_nonfinite.restype = ctypes.c_int
         L.oracle_any_nonfinite.argtypes = [_i64, _vp, ctypes.c_int, _f32]
         L.oracle_rem_pack_n.restype = None
@@ -213,6 +215,12 @@ def adam_f64(group: Group, step: int, p, m, v, g) -> None:
                           group.grad_scale, _ptr(p), _ptr(m), _ptr(v), _ptr(g))
 
 
+def sumsq(g, g_dtype) -> float:
+    """Sum of squares of one gradient tensor, in double."""
+    g = np.ascontiguousarray(g)
+    return float(lib().oracle_sumsq(g.size, _ptr(g), g_dtype))
+
+
 def any_nonfinite(g, g_dtype, grad_scale) -> bool:
     g = np.ascontiguousarray(g)
     return bool(lib().oracle_any_nonfinite(g.size, _ptr(g), g_dtype, float(grad_scale)))
@@ -294,3 +302,44 @@ def shard_step(shard: Shard, *, capturable: bool, noop: bool = False,
 def group_steps(shard: Shard) -> List[int]:
     """The step each group reports (its counter's value)."""
     return [shard.steps[s] for s in shard.step_slot]
+
+
+# ---- gradient norm and clipping ---------------------------------------------
+#
+# "apex/contrib/optimizers/distributed_fused_adam.py": _local_grad_norm (sum
+# of squares of the local gradient shard), grad_norm (all-reduced, square
+# root, times the grad scale), clip_grad_norm (clip_coef = max_norm /
+# (total_norm + 1e-6), clamped to at most 1, multiplied into the grad
+# scale) and step() (found_inf = not isfinite(grad norm), copied into the
+# noop flag).  Readings: with one grad scale per group the squared norm is
+# sum_g scale_g^2 * sum_{i in g} g_i^2, accumulated in double (the norm of
+# the scaled gradient; with one scale for all groups this is the page's
+# norm times scale); the norm is that square root rounded once to float;
+# the clip arithmetic is in float, one IEEE operation at a time.
+
+
+def shard_sumsq(shard: "Shard") -> float:
+    """Squared norm of the scaled gradient of the shard (before any
+    all-reduce across ranks)."""
+    per_group = [0.0] * len(shard.groups)
+    for t in shard.tensors:
+        per_group[t.group] += sumsq(t.g, t.g_dtype)
+    total = 0.0
+    for grp, s in zip(shard.groups, per_group):
+        gs = float(np.float32(grp.grad_scale))
+        total += gs * gs * s
+    return total
+
+
+def clip_from_sumsq(total_sumsq: float, max_norm: float, grad_scale: float):
+    """(norm, found_inf, clip coefficient, new grad scale) from the squared
+    norm summed over all ranks; max_norm <= 0 means no clipping."""
+    import math
+    with np.errstate(over="ignore", invalid="ignore"):
+        norm = np.float32(math.sqrt(total_sumsq)) if total_sumsq < math.inf else np.float32(math.inf)
+        found_inf = not np.isfinite(norm)
+        if max_norm <= 0:
+            return norm, found_inf, np.float32(1.0), np.float32(grad_scale)
+        coef = np.float32(max_norm) / (norm + np.float32(1e-6))
+        coef = min(coef, np.float32(1.0))
+        return norm, found_inf, np.float32(coef), np.float32(grad_scale) * np.float32(coef)

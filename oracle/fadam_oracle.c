@@ -316,6 +316,17 @@ void oracle_adam_f64(int64_t n, int mode, int bias_correction, int32_t step, flo
   }
 }
 
+/* Sum of squares of a gradient tensor, each element widened exactly and
+ * squared and added in double, one after the other. */
+double oracle_sumsq(int64_t n, const void* g, int g_dtype) {
+  double s = 0.0;
+  for (int64_t i = 0; i < n; ++i) {
+    double x = (double)grad_at(g, g_dtype, i);
+    s += x * x;
+  }
+  return s;
+}
+
 /* Inf/NaN screen of a gradient tensor: 1 when some grad*grad_scale (the
  * scaled gradient the update would consume) is not finite, else 0. */
 int oracle_any_nonfinite(int64_t n, const void* g, int g_dtype, float grad_scale) {

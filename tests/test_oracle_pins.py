@@ -566,3 +566,53 @@ def test_fp32_state_through_the_generic_path_matches_adam_f32():
         oracle.adam_state(grp, k, *b, DT_F32, g, DT_F32)
     for x, y in zip(a, b):
         assert x.tobytes() == y.tobytes()
+
+
+# ---- gradient norm and clipping --------------------------------------------------
+
+def test_sumsq_against_numpy_and_exact_cases():
+    rng = np.random.default_rng(14)
+    g = rng.standard_normal(100_003).astype(np.float32)
+    want = float(np.sum(g.astype(np.float64) ** 2))  # numpy's pairwise float64 sum
+    assert oracle.sumsq(g, DT_F32) == pytest.approx(want, rel=1e-13)
+    # constant vectors: n * c^2 exactly
+    assert oracle.sumsq(np.full(1000, 0.5, np.float32), DT_F32) == 250.0
+    assert oracle.sumsq(np.full(7, 0x4000, np.uint16), DT_BF16) == 28.0  # bf16 2.0
+    assert oracle.sumsq(np.full(9, 0x3C00, np.uint16), DT_F16) == 9.0    # fp16 1.0
+    assert oracle.sumsq(np.zeros(0, np.float32), DT_F32) == 0.0
+    bad = g.copy()
+    bad[5] = np.inf
+    assert oracle.sumsq(bad, DT_F32) == np.inf
+
+
+def test_shard_norm_is_the_norm_of_the_scaled_concatenation():
+    rng = np.random.default_rng(15)
+    gs = [0.5, 2.0]
+    groups = [Group(grad_scale=gs[0]), Group(grad_scale=gs[1]), Group()]
+    tensors, cat = [], []
+    for i, n in enumerate([1000, 17, 4096, 3]):
+        g = rng.standard_normal(n).astype(np.float32)
+        tensors.append(oracle.Tensor(group=i % 2, p=np.zeros(n, np.float32),
+                                     m=np.zeros(n, np.float32), v=np.zeros(n, np.float32), g=g))
+        cat.append(g.astype(np.float64) * gs[i % 2])
+    sh = oracle.Shard(groups=groups, tensors=tensors)
+    want = np.linalg.norm(np.concatenate(cat)) ** 2
+    assert oracle.shard_sumsq(sh) == pytest.approx(want, rel=1e-12)
+
+
+def test_clip_coefficient_cases():
+    # below the threshold: coefficient clamped to 1, scale unchanged
+    norm, inf, coef, gs = oracle.clip_from_sumsq(9.0, max_norm=5.0, grad_scale=0.25)
+    assert norm == np.float32(3.0) and not inf and coef == np.float32(1.0) and gs == np.float32(0.25)
+    # above: max_norm / (norm + 1e-6), in float
+    norm, inf, coef, gs = oracle.clip_from_sumsq(100.0, max_norm=1.0, grad_scale=1.0)
+    assert norm == np.float32(10.0)
+    assert coef == np.float32(1.0) / (np.float32(10.0) + np.float32(1e-6))
+    assert coef == pytest.approx(0.1, rel=1e-6) and gs == coef
+    # a non-finite squared norm sets found_inf
+    for bad in (np.inf, np.nan):
+        assert oracle.clip_from_sumsq(bad, 1.0, 1.0)[1]
+    # a norm beyond the float range is not finite either
+    assert oracle.clip_from_sumsq(1e80, 1.0, 1.0)[1]
+    # no clipping requested
+    assert oracle.clip_from_sumsq(16.0, 0.0, 0.5)[2:] == (np.float32(1.0), np.float32(0.5))
