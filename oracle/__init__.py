@@ -336,7 +336,7 @@ def clip_from_sumsq(total_sumsq: float, max_norm: float, grad_scale: float):
     norm summed over all ranks; max_norm <= 0 means no clipping."""
     import math
     with np.errstate(over="ignore", invalid="ignore"):
-        norm = np.float32(math.sqrt(total_sumsq)) if total_sumsq < math.inf else np.float32(math.inf)
+        norm = np.float32(math.sqrt(total_sumsq))  # inf and NaN propagate
         found_inf = not np.isfinite(norm)
         if max_norm <= 0:
             return norm, found_inf, np.float32(1.0), np.float32(grad_scale)

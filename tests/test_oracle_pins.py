@@ -612,6 +612,8 @@ def test_clip_coefficient_cases():
     # a non-finite squared norm sets found_inf
     for bad in (np.inf, np.nan):
         assert oracle.clip_from_sumsq(bad, 1.0, 1.0)[1]
+    assert np.isnan(oracle.clip_from_sumsq(np.nan, 1.0, 1.0)[0])
+    assert np.isinf(oracle.clip_from_sumsq(np.inf, 1.0, 1.0)[0])
     # a norm beyond the float range is not finite either
     assert oracle.clip_from_sumsq(1e80, 1.0, 1.0)[1]
     # no clipping requested
