@@ -77,6 +77,8 @@ SIGNATURES = [
                               ctypes.POINTER(_i64)]),
     ("fadam_step_noalloc", _i32, [ctypes.POINTER(Tensor), _i64, ctypes.POINTER(Group), _i32, _i32,
                                   _i32, _i32, _u32, _vp, _vp]),
+    ("fadam_grad_sumsq", _i32, [_vp, _vp, _vp]),
+    ("fadam_clip_apply", _i32, [_vp, _vp, _f32, _vp, _vp, _vp]),
     ("fadam_status_string", ctypes.c_char_p, [_i32]),
     ("fadam_last_error", ctypes.c_char_p, []),
     ("fadam_version", _i32, []),

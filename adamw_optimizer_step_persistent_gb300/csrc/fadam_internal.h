@@ -87,6 +87,9 @@ constexpr uint32_t kCapturable = FADAM_CAPTURABLE;
 constexpr uint32_t kCheckFinite = FADAM_CHECK_FINITE;
 constexpr uint32_t kPreadvanced = FADAM_STEP_PREADVANCED;
 constexpr uint32_t kTestBarrierTimeout = FADAM_TEST_BARRIER_TIMEOUT;
+// Launch-only flag (never a plan flag): compute the squared gradient norm
+// instead of the update.
+constexpr uint32_t kNormOnly = 1u << 30;
 
 // Everything one launch needs, passed as a __grid_constant__ parameter.
 struct alignas(16) KParams {
@@ -95,6 +98,8 @@ struct alignas(16) KParams {
   int32_t* noop;             // may be null
   KScratch* scratch;
   const Chunk* chunks;       // bulk tiles, pulled dynamically by the CTAs
+  double* partials;          // norm launches: weighted sums of squares, one per chunk then one per item
+  double* sumsq_out;         // norm launches: sum_g grad_scale_g^2 * sum g^2
   int32_t n_chunks;
   int32_t n_groups;
   uint32_t flags;

@@ -367,13 +367,14 @@ __device__ __forceinline__ int bulk_tiles(const Item& it) {
 }
 
 // What a pipeline pass moves through shared memory.
-enum class Pass { kUpdate, kScan };  // kScan: only g, for the inf/nan screen
+// kScan: only g, for the inf/nan screen; kNorm: only g, for the squared norm
+enum class Pass { kUpdate, kScan, kNorm };
 
 // Vectors in one tile of a pass (Layout::update_vectors or ::scan_vectors).
 template <int ST, int GT, bool REM, Pass PASS>
 __host__ __device__ constexpr int tile_vectors() {
-  return PASS == Pass::kScan ? Layout<ST, GT, REM>::scan_vectors
-                             : Layout<ST, GT, REM>::update_vectors;
+  return PASS == Pass::kUpdate ? Layout<ST, GT, REM>::update_vectors
+                               : Layout<ST, GT, REM>::scan_vectors;
 }
 
 // Thread 0 of the CTA: start the copies of vectors [v0, v0 + len) of `it`
@@ -386,7 +387,7 @@ __device__ __forceinline__ void issue_tile(const Item& it, int v0, unsigned len,
   unsigned char* st = smem + size_t(b) * L::stage;
   uint64_t* bar = full + b;
   const size_t v = static_cast<size_t>(v0);
-  if constexpr (PASS == Pass::kScan) {
+  if constexpr (PASS != Pass::kUpdate) {
     mbar_expect_tx(bar, len * L::kG);
     bulk_load(st, static_cast<const char*>(it.g) + v * L::kG, len * L::kG, bar);
   } else {
@@ -409,6 +410,7 @@ __device__ __forceinline__ void issue_tile(const Item& it, int v0, unsigned len,
 struct Producer {
   Item it;
   int item, v, vend;  // vectors [v, vend) of the current chunk remain
+  int chunk;
   unsigned slot;
   bool finished;
 };
@@ -417,6 +419,7 @@ struct TileTag {
   int item;  // -1: no more tiles
   int v0;
   int len;
+  int chunk;
 };
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -431,13 +434,14 @@ __device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, un
     const unsigned c = atomicAdd(counter, 1u);
     if (c >= static_cast<unsigned>(kp.n_chunks)) {
       const unsigned b = pr.slot % kStages;
-      tags[b] = TileTag{-1, 0, 0};
+      tags[b] = TileTag{-1, 0, 0, -1};
       mbar_arrive(full + b);  // completes the phase with no copy
       ++pr.slot;
       pr.finished = true;
       return;
     }
     const Chunk ch = kp.chunks[c];
+    pr.chunk = static_cast<int>(c);
     if (ch.item != pr.item) {
       pr.item = ch.item;
       pr.it = load_item(kp.items, ch.item);
@@ -446,7 +450,7 @@ __device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, un
     pr.vend = min((ch.tile0 + ch.ntiles) * kTile, bulk_vectors(pr.it));
   }
   const int len = min(tile_vectors<ST, GT, REM, PASS>(), pr.vend - pr.v);
-  tags[pr.slot % kStages] = TileTag{pr.item, pr.v, len};
+  tags[pr.slot % kStages] = TileTag{pr.item, pr.v, len, pr.chunk};
   issue_tile<ST, GT, REM, PASS>(pr.it, pr.v, static_cast<unsigned>(len), pr.slot, smem, full);
   pr.v += len;
   ++pr.slot;
@@ -498,6 +502,134 @@ __device__ __forceinline__ bool scan_tile(const unsigned char* st, int len, floa
   return bad;
 }
 
+// Squares of 4 widened values: in float when the sum is in a safe range,
+// else exactly in double (overflow, NaN, or nonzero values whose squares
+// would underflow).  Returns true when the double path was needed.
+__device__ __forceinline__ bool square4(const float (&g)[4], float& f, double& d) {
+  const float v = __fadd_rn(__fadd_rn(__fmul_rn(g[0], g[0]), __fmul_rn(g[1], g[1])),
+                            __fadd_rn(__fmul_rn(g[2], g[2]), __fmul_rn(g[3], g[3])));
+  const bool tiny_nonzero = v < 1e-30f && (g[0] != 0.0f || g[1] != 0.0f || g[2] != 0.0f || g[3] != 0.0f);
+  if (!(v <= 1e30f) || tiny_nonzero) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) d += static_cast<double>(g[e]) * static_cast<double>(g[e]);
+    return true;
+  }
+  f = __fadd_rn(f, v);
+  return false;
+}
+
+// A thread's running sum of squares over the tiles of one chunk: float with
+// Kahan compensation, plus a double part for the rare values square4 sends
+// there (and for float sums that grow large).  At the end of a chunk the
+// CTA reduces all threads' sums in a fixed order into the chunk's slot, so
+// the result does not depend on which CTA took which chunk.
+struct NormAcc {
+  float sum, comp;
+  double dsum;
+  int chunk;
+  int group;
+};
+
+__device__ __forceinline__ void norm_reset(NormAcc& na) {
+  na.sum = 0.0f;
+  na.comp = 0.0f;
+  na.dsum = 0.0;
+}
+
+__device__ __forceinline__ void norm_add(NormAcc& na, float f, double d, bool special) {
+  const float y = __fsub_rn(f, na.comp);
+  const float t = __fadd_rn(na.sum, y);
+  na.comp = __fsub_rn(__fsub_rn(t, na.sum), y);
+  na.sum = t;
+  if (special) na.dsum += d;
+  if (na.sum > 1e30f) {  // keep the float part far from overflow
+    na.dsum += static_cast<double>(na.sum) - static_cast<double>(na.comp);
+    na.sum = 0.0f;
+    na.comp = 0.0f;
+  }
+}
+
+// Sum of one double per thread over the whole CTA, in a fixed order; the
+// result is valid in thread 0.  Every thread must call it.
+__device__ __forceinline__ double cta_sum(double x, double* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = x;
+  __syncthreads();
+  double total = 0.0;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < kBlock / 32; ++w) total += red[w];
+  __syncthreads();  // red is reused
+  return total;
+}
+
+// Sum over the CTA of one float and one double per thread, in a fixed
+// order (deterministic): each warp reduces its floats in float (five
+// roundings), the doubles only when some thread holds one, and warp 0 adds
+// the 32 warp sums in double.  The result is valid in thread 0; every thread
+// must call it.
+__device__ __forceinline__ double cta_sum_mixed(float xf, double xd, double* red, double* redd) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) xf = __fadd_rn(xf, __shfl_xor_sync(0xffffffffu, xf, o));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x / 32;
+  if (lane == 0) red[warp] = static_cast<double>(xf);
+  const bool any_d = __syncthreads_or(xd != 0.0);
+  if (any_d) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) xd += __shfl_xor_sync(0xffffffffu, xd, o);
+    if (lane == 0) redd[warp] = xd;
+    __syncthreads();
+  }
+  double total = 0.0;
+  if (warp == 0) {
+    double y = red[lane] + (any_d ? redd[lane] : 0.0);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+    total = y;
+  }
+  __syncthreads();  // red and redd are reused
+  return total;
+}
+
+// Close the current chunk: its weighted sum of squares into its slot.
+__device__ __forceinline__ void norm_close(NormAcc& na, const SGroup* sgrp, double* slots,
+                                           double* red) {
+  if (na.chunk < 0) return;
+  const double total = cta_sum_mixed(na.sum, na.dsum, red, red + kBlock / 32);
+  if (threadIdx.x == 0) {
+    const double gs = sgrp[na.group].gs;
+    slots[na.chunk] = gs * gs * total;
+    __threadfence();
+  }
+  norm_reset(na);
+  na.chunk = -1;
+}
+
+// Every thread of the CTA calls this for the same tile.
+template <int GT>
+__device__ __forceinline__ void norm_tile(const unsigned char* st, const TileTag& tag, int group,
+                                          NormAcc& na, const SGroup* sgrp, double* slots,
+                                          double* red) {
+  if (tag.chunk != na.chunk) {
+    norm_close(na, sgrp, slots, red);
+    na.chunk = tag.chunk;
+    na.group = group;
+  }
+  float f = 0.0f;
+  double d = 0.0;
+  bool special = false;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {  // Layout::scan_vectors = 4 * kTile
+    const int t = threadIdx.x + q * kTile;
+    if (t < tag.len) {
+      float g[4];
+      widen4<GT>(reinterpret_cast<const typename Raw4<GT>::T*>(st)[t], g);
+      special |= square4(g, f, d);
+    }
+  }
+  norm_add(na, f, d, special);
+}
+
 // Phase A: the bulk tiles of the whole shard, pulled chunk by chunk from
 // the launch-wide counter, as one continuous pipeline per CTA (the copies
 // of the next chunk start while the current one is consumed).  `bad`
@@ -506,8 +638,9 @@ __device__ __forceinline__ bool scan_tile(const unsigned char* st, int len, floa
 template <int ST, int GT, int OT, bool REM, Pass PASS>
 __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp, unsigned* counter,
                                           unsigned char* smem, uint64_t* full, TileTag* tags,
-                                          Producer& pr, unsigned& stage, bool& bad,
+                                          Producer& pr, double* red, unsigned& stage, bool& bad,
                                           bool& timed_out) {
+  NormAcc na{0.0f, 0.0f, 0.0, -1, 0};
   if (threadIdx.x == 0) {
     pr.item = -1;
     pr.v = 0;
@@ -521,7 +654,16 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
   for (;; ++stage) {
     const unsigned b = stage % kStages;
     const bool ok = mbar_wait(full + b, (stage / kStages) & 1u);
-    TileTag tag{-1, 0, 0};
+    if constexpr (PASS == Pass::kNorm) {
+      // the norm's per-chunk reductions are CTA-wide: decide a timeout for
+      // every thread before any of them touches the tile
+      if (__syncthreads_or(!ok)) {
+        timed_out = true;
+        ++stage;
+        return;
+      }
+    }
+    TileTag tag{-1, 0, 0, -1};
     if (ok) {
       tag = tags[b];
       if (tag.item >= 0) {
@@ -534,6 +676,8 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
         const Scal s{G.beta1, G.omb1, G.beta2, G.omb2, G.bc1, G.bc2, G.eps, G.wd, G.lr, G.gs};
         if constexpr (PASS == Pass::kScan) {
           bad |= scan_tile<GT>(st, tag.len, s.gs);
+        } else if constexpr (PASS == Pass::kNorm) {
+          norm_tile<GT>(st, tag, it.group, na, sgrp, kp.partials, red);
         } else {
           if (G.bits & kGroupAdamW) update_tile<true, ST, GT, OT, REM>(it, s, st, tag.v0, tag.len);
           else update_tile<false, ST, GT, OT, REM>(it, s, st, tag.v0, tag.len);
@@ -548,6 +692,7 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
     }
     if (tag.item < 0) {  // the end marker (the same for every thread)
       ++stage;
+      if constexpr (PASS == Pass::kNorm) norm_close(na, sgrp, kp.partials, red);
       return;
     }
     if (threadIdx.x == 0) {
@@ -697,13 +842,21 @@ __device__ __forceinline__ bool tail_pass(const KParams& kp, const SGroup* sgrp,
     if (!(it.flags & kItemBulk)) continue;
     const SGroup& G = sgrp[it.group];
     const Scal s{G.beta1, G.omb1, G.beta2, G.omb2, G.bc1, G.bc2, G.eps, G.wd, G.lr, G.gs};
+    double sq = 0.0;
     for (int i = bulk_vectors(it) * kVec; i < it.n; ++i) {
       if constexpr (PASS == Pass::kScan) {
         bad |= !isfinite(__fmul_rn(load1<GT>(it.g, i), s.gs));
+      } else if constexpr (PASS == Pass::kNorm) {
+        const double x = load1<GT>(it.g, i);
+        sq += x * x;
       } else {
         if (G.bits & kGroupAdamW) update_elem<true, ST, GT, OT, REM>(it, s, i);
         else update_elem<false, ST, GT, OT, REM>(it, s, i);
       }
+    }
+    if constexpr (PASS == Pass::kNorm) {  // the item's slot, after the chunk slots
+      kp.partials[kp.n_chunks + k] = static_cast<double>(G.gs) * G.gs * sq;
+      __threadfence();
     }
   }
   return bad;
@@ -716,7 +869,7 @@ __device__ __forceinline__ bool tail_pass(const KParams& kp, const SGroup* sgrp,
 // is skipped in a few loads.
 template <int ST, int GT, int OT, bool REM, Pass PASS>
 __device__ __forceinline__ bool rest_pass(const KParams& kp, const SGroup* sgrp, int item_begin,
-                                          int item_end) {
+                                          int item_end, double* red) {
   __shared__ int s_count;
   __shared__ int s_list[kBlock];
   bool bad = false;
@@ -736,6 +889,17 @@ __device__ __forceinline__ bool rest_pass(const KParams& kp, const SGroup* sgrp,
       const Scal s{G.beta1, G.omb1, G.beta2, G.omb2, G.bc1, G.bc2, G.eps, G.wd, G.lr, G.gs};
       if constexpr (PASS == Pass::kScan) {
         bad |= simt_scan<GT>(it, s.gs);
+      } else if constexpr (PASS == Pass::kNorm) {
+        double sq = 0.0;
+        for (int i = threadIdx.x; i < it.n; i += kBlock) {
+          const double x = load1<GT>(it.g, i);
+          sq += x * x;
+        }
+        const double total = cta_sum(sq, red);
+        if (threadIdx.x == 0) {
+          kp.partials[kp.n_chunks + s_list[q]] = static_cast<double>(G.gs) * G.gs * total;
+          __threadfence();
+        }
       } else {
         if (G.bits & kGroupAdamW) simt_item<true, ST, GT, OT, REM>(it, s);
         else simt_item<false, ST, GT, OT, REM>(it, s);
@@ -752,12 +916,13 @@ template <int ST, int GT, int OT, bool REM, Pass PASS>
 __device__ __forceinline__ void run_pass(const KParams& kp, const SGroup* sgrp, int item_begin,
                                          int item_end, unsigned* counter, unsigned* tail_counter,
                                          int n_items, unsigned char* smem, uint64_t* full,
-                                         TileTag* tags, Producer& pr, unsigned& stage, bool& bad,
-                                         bool& timed_out) {
+                                         TileTag* tags, Producer& pr, double* red,
+                                         unsigned& stage, bool& bad, bool& timed_out) {
   if (FADAM_BULK && kp.n_chunks > 0 && !timed_out)
-    bulk_pass<ST, GT, OT, REM, PASS>(kp, sgrp, counter, smem, full, tags, pr, stage, bad, timed_out);
+    bulk_pass<ST, GT, OT, REM, PASS>(kp, sgrp, counter, smem, full, tags, pr, red, stage, bad,
+                                     timed_out);
   if (FADAM_BULK) bad |= tail_pass<ST, GT, OT, REM, PASS>(kp, sgrp, tail_counter, n_items);
-  bad |= rest_pass<ST, GT, OT, REM, PASS>(kp, sgrp, item_begin, item_end);
+  bad |= rest_pass<ST, GT, OT, REM, PASS>(kp, sgrp, item_begin, item_end, red);
 }
 
 // Grid-wide barrier for a cooperative launch.  The wait is bounded: after
@@ -804,6 +969,7 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
   __shared__ __align__(8) uint64_t s_full[kStages];
   __shared__ TileTag s_tags[kStages];
   __shared__ Producer s_prod;  // used by thread 0 only
+  __shared__ double s_red[2 * (kBlock / 32)];  // norm launches: partials per warp
   extern __shared__ __align__(128) unsigned char s_tiles[];
   const bool capturable = (kp.flags & kCapturable) != 0;
   const int tid = threadIdx.x;
@@ -855,13 +1021,24 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
   unsigned stage = 0;  // tiles through the pipeline so far (buffer and parity)
   bool barrier_ok = true, timed_out = false;
 
+  const bool norm_only = (kp.flags & kNormOnly) != 0;
+  if (norm_only) {
+    // squared gradient norm instead of the update: one weighted partial per
+    // chunk of tiles and per item (tails, unaligned items), summed by the
+    // last CTA below in a fixed order
+    bool unused = false;
+    run_pass<ST, GT, OT, REM, Pass::kNorm>(kp, sgrp, item_begin, item_end, &kp.scratch->next_scan,
+                                           &kp.scratch->next_tail_scan, n_items, s_tiles, s_full,
+                                           s_tags, s_prod, s_red, stage, unused, timed_out);
+  }
+
   // 2. optional inf/nan screen over the whole shard before any update
-  if (kp.flags & kCheckFinite) {
+  if (!norm_only && (kp.flags & kCheckFinite)) {
     bool bad = false;
     if (!s_noop)
       run_pass<ST, GT, OT, REM, Pass::kScan>(kp, sgrp, item_begin, item_end, &kp.scratch->next_scan,
                                          &kp.scratch->next_tail_scan, n_items, s_tiles, s_full,
-                                         s_tags, s_prod, stage, bad, timed_out);
+                                         s_tags, s_prod, s_red, stage, bad, timed_out);
     if (__syncthreads_or(bad) && tid == 0) atomicExch(kp.noop, 1);
     barrier_ok = grid_barrier(kp.scratch, (kp.flags & kTestBarrierTimeout) ? 1u : 0u);
     if (tid == 0) s_noop = (ld_acquire_s32(kp.noop) == 1);
@@ -869,23 +1046,37 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
   }
 
   // 3. the update
-  if (!s_noop && barrier_ok) {
+  if (!norm_only && !s_noop && barrier_ok) {
     bool unused = false;
     run_pass<ST, GT, OT, REM, Pass::kUpdate>(kp, sgrp, item_begin, item_end, &kp.scratch->next_update,
                                          &kp.scratch->next_tail_update, n_items, s_tiles, s_full,
-                                         s_tags, s_prod, stage, unused, timed_out);
+                                         s_tags, s_prod, s_red, stage, unused, timed_out);
   }
   if (__syncthreads_or(timed_out) && tid == 0) atomicExch(&kp.scratch->status, FADAM_ETIMEOUT);
 
   // 4. the last CTA to finish resets the work counters for the next launch
-  //    and, for capturable plans, advances the step counters
+  //    and, for capturable plans, advances the step counters; for a norm
+  //    launch it sums the partials
+  __shared__ int s_last;
   __syncthreads();
   if (tid == 0) {
     __threadfence();
-    const unsigned prev = atomicAdd(&kp.scratch->done, 1u);
-    if (prev == gridDim.x - 1) {
+    s_last = atomicAdd(&kp.scratch->done, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (norm_only && s_last) {
+    __threadfence();
+    const int n_slots = (FADAM_BULK ? kp.n_chunks : 0) + n_items;
+    const int base = FADAM_BULK ? 0 : kp.n_chunks;
+    double x = 0.0;
+    for (int i = tid; i < n_slots; i += kBlock) x += __ldcg(kp.partials + base + i);
+    const double total = cta_sum(x, s_red);
+    if (tid == 0) *kp.sumsq_out = total;
+  }
+  if (tid == 0) {
+    if (s_last) {
       __threadfence();
-      if (capturable && !(kp.flags & kPreadvanced)) {
+      if (!norm_only && capturable && !(kp.flags & kPreadvanced)) {
         const int adv = (s_noop || !barrier_ok) ? 0 : 1;
         for (int g = 0; g < kp.n_groups; ++g)
           if (sgrp[g].bits & kGroupOwnsStep) *kp.groups[g].step_dev = sgrp[g].step_old + adv;

@@ -489,6 +489,7 @@ struct fadam_plan {
   Chunk* d_chunks = nullptr;
   int32_t* d_cta = nullptr;
   KScratch* d_scratch = nullptr;
+  double* d_partials = nullptr;  // gradient-norm launches: per-chunk and per-item partials
 };
 
 namespace {
@@ -498,10 +499,12 @@ void free_plan_memory(fadam_plan* p) {
   if (p->d_chunks) cudaFree(p->d_chunks);
   if (p->d_cta) cudaFree(p->d_cta);
   if (p->d_scratch) cudaFree(p->d_scratch);
+  if (p->d_partials) cudaFree(p->d_partials);
   p->d_items = nullptr;
   p->d_chunks = nullptr;
   p->d_cta = nullptr;
   p->d_scratch = nullptr;
+  p->d_partials = nullptr;
 }
 
 void fill_params(KParams& kp, const Item* items, const int32_t* cta, const Chunk* chunks,
@@ -568,6 +571,9 @@ fadam_status fadam_plan_create(const fadam_tensor* tensors, int64_t n_tensors,
                    cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMalloc(&plan->d_scratch, sizeof(KScratch));
   if (e == cudaSuccess) e = cudaMemset(plan->d_scratch, 0, sizeof(KScratch));
+  // gradient-norm launches: one partial per tile chunk and per item
+  if (e == cudaSuccess)
+    e = cudaMalloc(&plan->d_partials, (hp.chunks.size() + hp.items.size() + 1) * sizeof(double));
   if (e != cudaSuccess) {
     st = cuda_fail(e, "plan upload");
     free_plan_memory(plan);
@@ -770,6 +776,88 @@ fadam_status fadam_step_once(const fadam_tensor* tensors, int64_t n_tensors, int
   if (d_cta) cudaFreeAsync(d_cta, s);
   if (d_scratch) cudaFreeAsync(d_scratch, s);
   return st;
+}
+
+}  // extern "C"
+
+namespace {
+
+struct ClipArgs {
+  const double* sumsq;
+  float* norm_out;
+  int32_t* noop;
+  float max_norm;
+  int32_t n_scales;
+  float* scales[FADAM_MAX_GROUPS];
+};
+
+// One thread: the norm from the squared norm, found_inf into the noop flag,
+// and the clip coefficient multiplied into each distinct grad_scale.
+__global__ void fadam_clip_kernel(const __grid_constant__ ClipArgs a) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  const float norm = __double2float_rn(sqrt(__ldcg(a.sumsq)));
+  if (a.norm_out) *a.norm_out = norm;
+  if (a.noop) *a.noop = isfinite(norm) ? 0 : 1;
+  if (a.max_norm > 0.0f) {
+    float coef = __fdiv_rn(a.max_norm, __fadd_rn(norm, 1e-6f));
+    if (coef > 1.0f) coef = 1.0f;  // a NaN coefficient stays NaN, as torch.clamp keeps it
+    for (int i = 0; i < a.n_scales; ++i) *a.scales[i] = __fmul_rn(*a.scales[i], coef);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+fadam_status fadam_grad_sumsq(fadam_plan* plan, double* sumsq_dev, fadam_stream stream) {
+  if (!plan) return fail(FADAM_EINVAL, "plan is NULL");
+  if (!sumsq_dev || reinterpret_cast<uintptr_t>(sumsq_dev) % 8)
+    return fail(FADAM_EINVAL, "sumsq_dev must be a non-NULL, 8-byte aligned device pointer");
+  const HostPlan& hp = plan->hp;
+  DeviceGuard guard(hp.device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  KParams kp;
+  fill_params(kp, plan->d_items, plan->d_cta, plan->d_chunks, static_cast<int32_t>(hp.chunks.size()),
+              nullptr, plan->d_scratch, plan->groups.data(), plan->n_groups,
+              (hp.flags & FADAM_CAPTURABLE) | kNormOnly);
+  kp.partials = plan->d_partials;
+  kp.sumsq_out = sumsq_dev;
+  return launch(hp.kernel, hp.smem, kp, hp.grid, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fadam_status fadam_clip_apply(fadam_plan* plan, const double* sumsq_dev, float max_norm,
+                              float* norm_dev, int32_t* noop_dev, fadam_stream stream) {
+  if (!plan) return fail(FADAM_EINVAL, "plan is NULL");
+  if (!sumsq_dev || reinterpret_cast<uintptr_t>(sumsq_dev) % 8)
+    return fail(FADAM_EINVAL, "sumsq_dev must be a non-NULL, 8-byte aligned device pointer");
+  if ((norm_dev && reinterpret_cast<uintptr_t>(norm_dev) % 4) ||
+      (noop_dev && reinterpret_cast<uintptr_t>(noop_dev) % 4))
+    return fail(FADAM_EALIGN, "norm_dev / noop_dev not 4-byte aligned");
+  if (!std::isfinite(max_norm)) return fail(FADAM_EINVAL, "max_norm is not finite");
+  ClipArgs a{};
+  a.sumsq = sumsq_dev;
+  a.norm_out = norm_dev;
+  a.noop = noop_dev;
+  a.max_norm = max_norm;
+  if (plan->hp.flags & FADAM_CAPTURABLE) {
+    for (int32_t g = 0; g < plan->n_groups; ++g) {
+      float* gs = const_cast<float*>(plan->groups[g].grad_scale_dev);
+      if (!gs) continue;
+      bool seen = false;
+      for (int32_t j = 0; j < a.n_scales; ++j) seen |= a.scales[j] == gs;
+      if (!seen) a.scales[a.n_scales++] = gs;
+    }
+  }
+  DeviceGuard guard(plan->hp.device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  void* args[1] = {&a};
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(&fadam_clip_kernel), args);
+  if (e != cudaSuccess) return cuda_fail(e, "clip kernel launch");
+  return FADAM_OK;
 }
 
 fadam_status fadam_pack_dry(const fadam_tensor* tensors, int64_t n_tensors, int32_t n_groups,

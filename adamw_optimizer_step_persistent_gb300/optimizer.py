@@ -208,6 +208,45 @@ class FusedAdamShard:
                                              _stream_handle(self.device)), "fadam_step_host_grads")
         return list(steps)
 
+    # ---- gradient norm and clipping ------------------------------------------
+
+    def grad_norm_sq(self) -> torch.Tensor:
+        """Squared L2 norm of this shard's scaled gradient, as a float64
+        device tensor (all-reduce it across data-parallel ranks before
+        clip_apply).  One launch, no sync."""
+        if not hasattr(self, "_sumsq"):
+            self._sumsq = torch.zeros(1, dtype=torch.float64, device=self.device)
+        if not self.capturable:  # the plan reads the current host grad_scale
+            self._fill_groups()
+            _abi.check(_abi.lib().fadam_plan_set_groups(self._plan, self._groups_c,
+                                                        len(self.groups)), "fadam_plan_set_groups")
+        _abi.check(_abi.lib().fadam_grad_sumsq(self._plan, self._sumsq.data_ptr(),
+                                               _stream_handle(self.device)), "fadam_grad_sumsq")
+        return self._sumsq
+
+    def clip_apply(self, sumsq: torch.Tensor, max_norm: float) -> torch.Tensor:
+        """Norm from the (all-reduced) squared norm; found_inf into the noop
+        flag; capturable shards scale the device grad_scale by the clip
+        coefficient.  Returns the norm as a float32 device tensor."""
+        if not hasattr(self, "_norm"):
+            self._norm = torch.zeros(1, dtype=torch.float32, device=self.device)
+        noop = self.noop.data_ptr() if self.capturable else None
+        _abi.check(_abi.lib().fadam_clip_apply(self._plan, sumsq.data_ptr(), float(max_norm),
+                                               self._norm.data_ptr(), noop,
+                                               _stream_handle(self.device)), "fadam_clip_apply")
+        if not self.capturable and max_norm > 0:
+            # regular shards keep grad_scale on the host (the page's .item() path)
+            import numpy as np
+            norm = np.float32(self._norm.item())
+            coef = np.float32(max_norm) / (norm + np.float32(1e-6))
+            coef = min(coef, np.float32(1.0))
+            self.host_grad_scale = float(np.float32(self.host_grad_scale) * np.float32(coef))
+        return self._norm
+
+    def clip_grad_norm(self, max_norm: float) -> torch.Tensor:
+        """Single-rank clip: grad_norm_sq then clip_apply."""
+        return self.clip_apply(self.grad_norm_sq(), max_norm)
+
     # ---- state -------------------------------------------------------------------
 
     def group_steps(self) -> List[int]:

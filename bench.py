@@ -350,6 +350,12 @@ def run_gpu(args):
         r["gbs_including_screen"] = r["gbs"] * (bytes_step + chk.info()["check_bytes_per_step"]) / bytes_step
         res["check_finite"] = r
         chk.close()
+    if "norm" in variants:
+        per, _ = time_launches(cap.grad_norm_sq, args.steps, args.warmup, world)
+        gbytes = elems * shard.grads[0].element_size()
+        r = summarise(per, gbytes, elems, world, device)
+        r["bytes_per_step"] = gbytes
+        res["grad_norm"] = r
     clocks = sampler.stop()
 
     e2e = None
@@ -371,7 +377,7 @@ def run_gpu(args):
                        "step counter -> host, stream sync"}
         del host
 
-    head = res.get("capturable") or next(iter(res.values()))
+    head = res.get("capturable") or res.get("regular") or next(iter(res.values()))
     peaks = measured_peaks()
     achieved = bytes_step / (head["ms_per_step"] / 1e3) / 1e9
     line = {
@@ -425,7 +431,7 @@ def main(argv=None):
     ap.add_argument("--n-tensors", type=int, default=None,
                     help="tensor count of large_uniform (201) or many_small (20000)")
     ap.add_argument("--numel", type=int, default=320 * 65536)
-    ap.add_argument("--variants", default="capturable,regular,graph,check_finite,e2e")
+    ap.add_argument("--variants", default="capturable,regular,graph,check_finite,norm,e2e")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tensors", type=int, default=4)
     args = ap.parse_args(argv)

@@ -220,6 +220,32 @@ fadam_status fadam_step_host_grads(fadam_plan* plan, const void* const* g_host,
                                    int32_t* noop_dev, int32_t* steps_host,
                                    fadam_stream stream);
 
+/* Gradient norm, step one: the squared L2 norm of the shard's scaled
+ * gradient, sum over groups of grad_scale^2 * sum of g^2 over the group's
+ * tensors ("apex/contrib/optimizers/distributed_fused_adam.py",
+ * _local_grad_norm and grad_norm), written as one double to *sumsq_dev by
+ * one launch on `stream`.  grad_scale is the host value of regular plans
+ * and *grad_scale_dev of capturable ones.  Accumulation: float within a
+ * tile, exactly in double wherever a float partial would overflow,
+ * underflow or is not finite, double across tiles and CTAs (a fixed order:
+ * the result is deterministic).  Across data-parallel ranks, all-reduce
+ * (sum) *sumsq_dev before step two.  No allocation, no host sync: safe to
+ * capture.  Errors: FADAM_EINVAL (NULL or misaligned sumsq_dev),
+ * FADAM_ECUDA. */
+fadam_status fadam_grad_sumsq(fadam_plan* plan, double* sumsq_dev, fadam_stream stream);
+
+/* Gradient norm, step two (same source, clip_grad_norm and step()): from
+ * the squared norm (summed over ranks), one thread on `stream` writes
+ * norm = sqrt(*sumsq_dev) rounded to float into *norm_dev (may be NULL),
+ * found_inf = (norm is not finite) as 0 or 1 into *noop_dev (may be NULL:
+ * the page copies found_inf into its noop buffer), and, when max_norm > 0,
+ * multiplies each distinct grad_scale_dev of a capturable plan by
+ * min(1, max_norm / (norm + 1e-6)) (float arithmetic; a NaN coefficient is
+ * kept).  Regular plans keep grad_scale on the host: read *norm_dev and
+ * scale it there.  Errors: FADAM_EINVAL, FADAM_EALIGN, FADAM_ECUDA. */
+fadam_status fadam_clip_apply(fadam_plan* plan, const double* sumsq_dev, float max_norm,
+                              float* norm_dev, int32_t* noop_dev, fadam_stream stream);
+
 /* Read (synchronously) and clear the plan's device status word:
  * *device_status = FADAM_OK, or FADAM_ETIMEOUT when a bounded wait of the
  * FADAM_CHECK_FINITE grid barrier gave up (that step may be partly applied).

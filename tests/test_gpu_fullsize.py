@@ -113,3 +113,17 @@ def test_tensor_beyond_2_pow_31_elements():
     opt.close()
     del shard, opt
     _free()
+
+
+def test_large_uniform_norm_full_size():
+    """Squared norm of the 201 x 20,971,520 shard against the oracle run
+    tensor by tensor on the host."""
+    spec = workloads.large_uniform()
+    shard = workloads.materialize(spec, DEV)
+    opt = FusedAdamShard(shard.param_groups(), capturable=True)
+    got = opt.grad_norm_sq().item()
+    want = sum(oracle.sumsq(helpers.to_np(g), oracle.DT_F32) for g in shard.grads)
+    assert got == pytest.approx(want, rel=2e-6)
+    opt.close()
+    del shard, opt
+    _free()
