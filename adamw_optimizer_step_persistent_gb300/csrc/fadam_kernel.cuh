@@ -502,50 +502,83 @@ __device__ __forceinline__ bool scan_tile(const unsigned char* st, int len, floa
   return bad;
 }
 
-// Squares of 4 widened values: in float when the sum is in a safe range,
-// else exactly in double (overflow, NaN, or nonzero values whose squares
-// would underflow).  Returns true when the double path was needed.
-__device__ __forceinline__ bool square4(const float (&g)[4], float& f, double& d) {
+// Sum of the squares of 4 widened values in float.  `special` is set when
+// that sum is outside the range where float serves (overflow, NaN, or
+// nonzero values whose squares underflow); such vectors are redone exactly
+// in double by square_tile_exact.
+__device__ __forceinline__ float square4(const float (&g)[4], bool& special) {
   const float v = __fadd_rn(__fadd_rn(__fmul_rn(g[0], g[0]), __fmul_rn(g[1], g[1])),
                             __fadd_rn(__fmul_rn(g[2], g[2]), __fmul_rn(g[3], g[3])));
   const bool tiny_nonzero = v < 1e-30f && (g[0] != 0.0f || g[1] != 0.0f || g[2] != 0.0f || g[3] != 0.0f);
-  if (!(v <= 1e30f) || tiny_nonzero) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) d += static_cast<double>(g[e]) * static_cast<double>(g[e]);
-    return true;
+  special |= !(v <= 1e30f) || tiny_nonzero;
+  return v;
+}
+
+struct SqPart {
+  float f;
+  double d;
+};
+
+// The rare case, kept out of line so that no double arithmetic sits in the
+// streaming loop: the thread's vectors of one tile again, the in-range ones
+// summed in float as before and the others squared exactly in double.
+template <int GT>
+__device__ __noinline__ SqPart square_tile_exact(const unsigned char* st, int len) {
+  SqPart r{0.0f, 0.0};
+  for (int q = 0; q < 4; ++q) {
+    const int t = threadIdx.x + q * kTile;
+    if (t < len) {
+      float g[4];
+      widen4<GT>(reinterpret_cast<const typename Raw4<GT>::T*>(st)[t], g);
+      bool sp = false;
+      const float v = square4(g, sp);
+      if (sp) {
+        for (int e = 0; e < 4; ++e) r.d += static_cast<double>(g[e]) * static_cast<double>(g[e]);
+      } else {
+        r.f = __fadd_rn(r.f, v);
+      }
+    }
   }
-  f = __fadd_rn(f, v);
-  return false;
+  return r;
 }
 
 // A thread's running sum of squares over the tiles of one chunk: float with
-// Kahan compensation, plus a double part for the rare values square4 sends
-// there (and for float sums that grow large).  At the end of a chunk the
-// CTA reduces all threads' sums in a fixed order into the chunk's slot, so
-// the result does not depend on which CTA took which chunk.
+// Kahan compensation, in registers, plus a double part for the rare values
+// square4 sends there (and for float sums that grow large).  The double
+// part lives in shared memory (one slot per thread, `has_d` says it is
+// nonzero), so the out-of-line code that touches it takes no reference to
+// the registers.  At the end of a chunk the CTA reduces all threads' sums in
+// a fixed order into the chunk's slot, so the result does not depend on
+// which CTA took which chunk.
 struct NormAcc {
   float sum, comp;
-  double dsum;
+  bool has_d;
   int chunk;
   int group;
 };
 
-__device__ __forceinline__ void norm_reset(NormAcc& na) {
-  na.sum = 0.0f;
-  na.comp = 0.0f;
-  na.dsum = 0.0;
+static __device__ __noinline__ float2 norm_fold(float sum, float comp, double d, double* dpart) {
+  double x = *dpart + d;
+  if (sum > 1e30f) {  // keep the float part far from overflow
+    x += static_cast<double>(sum) - static_cast<double>(comp);
+    sum = 0.0f;
+    comp = 0.0f;
+  }
+  *dpart = x;
+  return make_float2(sum, comp);
 }
 
-__device__ __forceinline__ void norm_add(NormAcc& na, float f, double d, bool special) {
+__device__ __forceinline__ void norm_add(NormAcc& na, float f, double d, bool special,
+                                         double* dpart) {
   const float y = __fsub_rn(f, na.comp);
   const float t = __fadd_rn(na.sum, y);
   na.comp = __fsub_rn(__fsub_rn(t, na.sum), y);
   na.sum = t;
-  if (special) na.dsum += d;
-  if (na.sum > 1e30f) {  // keep the float part far from overflow
-    na.dsum += static_cast<double>(na.sum) - static_cast<double>(na.comp);
-    na.sum = 0.0f;
-    na.comp = 0.0f;
+  if (special || na.sum > 1e30f) {
+    const float2 sc = norm_fold(na.sum, na.comp, d, dpart);
+    na.sum = sc.x;
+    na.comp = sc.y;
+    na.has_d = true;
   }
 }
 
@@ -563,71 +596,91 @@ __device__ __forceinline__ double cta_sum(double x, double* red) {
   return total;
 }
 
-// Sum over the CTA of one float and one double per thread, in a fixed
-// order (deterministic): each warp reduces its floats in float (five
-// roundings), the doubles only when some thread holds one, and warp 0 adds
-// the 32 warp sums in double.  The result is valid in thread 0; every thread
-// must call it.
-__device__ __forceinline__ double cta_sum_mixed(float xf, double xd, double* red, double* redd) {
+// The per-chunk reduction rides on the bulk pipeline's one CTA barrier per
+// tile.  When a chunk ends, each warp reduces its threads' sums (float sums
+// in float, five roundings; the double parts only when the warp holds one)
+// into red[warp] of one of two buffers; after the next barrier warp 0 adds
+// the 32 warp partials in double, in a fixed order, into the chunk's slot.
+// The buffers alternate, so a chunk that ends in the following tile writes
+// the other one while warp 0 still reads.  The result does not depend on
+// which CTA took which chunk.
+struct NormPending {
+  int chunk;  // -1: nothing to publish
+  float gs;
+};
+
+__device__ __forceinline__ void norm_warp_close(NormAcc& na, double* red_buf, double* dpart) {
+  float xf = na.sum;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) xf = __fadd_rn(xf, __shfl_xor_sync(0xffffffffu, xf, o));
-  const int lane = threadIdx.x & 31, warp = threadIdx.x / 32;
-  if (lane == 0) red[warp] = static_cast<double>(xf);
-  const bool any_d = __syncthreads_or(xd != 0.0);
-  if (any_d) {
+  double xd = 0.0;
+  if (__any_sync(0xffffffffu, na.has_d)) {
+    if (na.has_d) {
+      xd = *dpart;
+      *dpart = 0.0;
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) xd += __shfl_xor_sync(0xffffffffu, xd, o);
-    if (lane == 0) redd[warp] = xd;
-    __syncthreads();
   }
-  double total = 0.0;
-  if (warp == 0) {
-    double y = red[lane] + (any_d ? redd[lane] : 0.0);
+  if ((threadIdx.x & 31) == 0) red_buf[threadIdx.x / 32] = static_cast<double>(xf) + xd;
+  na.sum = 0.0f;
+  na.comp = 0.0f;
+  na.has_d = false;
+}
+
+// Warp 0, after a CTA barrier that follows every warp's norm_warp_close.
+__device__ __forceinline__ void norm_publish(const double* red_buf, float gs, double* slot) {
+  if (threadIdx.x < 32) {
+    double y = red_buf[threadIdx.x];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
-    total = y;
+    // thread 0 writes every chunk slot; its fence before the completion
+    // count at the end of the launch publishes them all
+    if (threadIdx.x == 0) *slot = static_cast<double>(gs) * gs * y;
   }
-  __syncthreads();  // red and redd are reused
-  return total;
 }
 
-// Close the current chunk: its weighted sum of squares into its slot.
-__device__ __forceinline__ void norm_close(NormAcc& na, const SGroup* sgrp, double* slots,
-                                           double* red) {
-  if (na.chunk < 0) return;
-  const double total = cta_sum_mixed(na.sum, na.dsum, red, red + kBlock / 32);
-  if (threadIdx.x == 0) {
-    const double gs = sgrp[na.group].gs;
-    slots[na.chunk] = gs * gs * total;
-    __threadfence();
-  }
-  norm_reset(na);
-  na.chunk = -1;
-}
-
-// Every thread of the CTA calls this for the same tile.
+// Every thread of the CTA calls this for the same tile (the warp-level
+// close needs whole warps).  A chunk that ends here becomes `pend`.
 template <int GT>
 __device__ __forceinline__ void norm_tile(const unsigned char* st, const TileTag& tag, int group,
-                                          NormAcc& na, const SGroup* sgrp, double* slots,
-                                          double* red) {
+                                          NormAcc& na, const SGroup* sgrp, double* red,
+                                          double* dpart, unsigned& closes, NormPending& pend) {
   if (tag.chunk != na.chunk) {
-    norm_close(na, sgrp, slots, red);
+    if (na.chunk >= 0) {
+      norm_warp_close(na, red + (closes & 1u) * (kBlock / 32), dpart);
+      pend = NormPending{na.chunk, sgrp[na.group].gs};
+      ++closes;
+    }
     na.chunk = tag.chunk;
     na.group = group;
   }
+  // Squares summed with fused multiply-adds; the range test is made once on
+  // the thread's tile sum: overflow or NaN, or a tiny sum while some input
+  // is nonzero (squares that may have underflowed).  Either sends the
+  // thread's vectors of this tile to the exact path.
   float f = 0.0f;
-  double d = 0.0;
-  bool special = false;
+  unsigned nz = 0u;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {  // Layout::scan_vectors = 4 * kTile
     const int t = threadIdx.x + q * kTile;
     if (t < tag.len) {
       float g[4];
       widen4<GT>(reinterpret_cast<const typename Raw4<GT>::T*>(st)[t], g);
-      special |= square4(g, f, d);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) f = __fmaf_rn(g[e], g[e], f);
+      nz |= __float_as_uint(g[0]) | __float_as_uint(g[1]) | __float_as_uint(g[2]) |
+            __float_as_uint(g[3]);
     }
   }
-  norm_add(na, f, d, special);
+  const bool special = !(f <= 1e30f) || (f < 1e-30f && (nz & 0x7fffffffu) != 0u);
+  double d = 0.0;
+  if (special) {
+    const SqPart r = square_tile_exact<GT>(st, tag.len);
+    f = r.f;
+    d = r.d;
+  }
+  norm_add(na, f, d, special, dpart);
 }
 
 // Phase A: the bulk tiles of the whole shard, pulled chunk by chunk from
@@ -640,7 +693,15 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
                                           unsigned char* smem, uint64_t* full, TileTag* tags,
                                           Producer& pr, double* red, unsigned& stage, bool& bad,
                                           bool& timed_out) {
-  NormAcc na{0.0f, 0.0f, 0.0, -1, 0};
+  NormAcc na{0.0f, 0.0f, false, -1, 0};
+  NormPending pend{-1, 0.0f};
+  double* dpart = nullptr;
+  if constexpr (PASS == Pass::kNorm) {
+    __shared__ double s_dpart[kBlock];
+    dpart = s_dpart + threadIdx.x;
+    *dpart = 0.0;
+  }
+  unsigned closes = 0;
   if (threadIdx.x == 0) {
     pr.item = -1;
     pr.v = 0;
@@ -653,16 +714,9 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
   Item it;
   for (;; ++stage) {
     const unsigned b = stage % kStages;
-    const bool ok = mbar_wait(full + b, (stage / kStages) & 1u);
-    if constexpr (PASS == Pass::kNorm) {
-      // the norm's per-chunk reductions are CTA-wide: decide a timeout for
-      // every thread before any of them touches the tile
-      if (__syncthreads_or(!ok)) {
-        timed_out = true;
-        ++stage;
-        return;
-      }
-    }
+    bool ok = mbar_wait(full + b, (stage / kStages) & 1u);
+    // the norm's chunk closes are warp-wide: one decision per warp
+    if constexpr (PASS == Pass::kNorm) ok = __all_sync(0xffffffffu, ok);
     TileTag tag{-1, 0, 0, -1};
     if (ok) {
       tag = tags[b];
@@ -677,7 +731,7 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
         if constexpr (PASS == Pass::kScan) {
           bad |= scan_tile<GT>(st, tag.len, s.gs);
         } else if constexpr (PASS == Pass::kNorm) {
-          norm_tile<GT>(st, tag, it.group, na, sgrp, kp.partials, red);
+          norm_tile<GT>(st, tag, it.group, na, sgrp, red, dpart, closes, pend);
         } else {
           if (G.bits & kGroupAdamW) update_tile<true, ST, GT, OT, REM>(it, s, st, tag.v0, tag.len);
           else update_tile<false, ST, GT, OT, REM>(it, s, st, tag.v0, tag.len);
@@ -690,9 +744,22 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
       ++stage;
       return;
     }
+    if constexpr (PASS == Pass::kNorm) {
+      if (pend.chunk >= 0) {
+        norm_publish(red + ((closes - 1u) & 1u) * (kBlock / 32), pend.gs, kp.partials + pend.chunk);
+        pend.chunk = -1;
+      }
+    }
     if (tag.item < 0) {  // the end marker (the same for every thread)
       ++stage;
-      if constexpr (PASS == Pass::kNorm) norm_close(na, sgrp, kp.partials, red);
+      if constexpr (PASS == Pass::kNorm) {
+        if (na.chunk >= 0) {
+          double* buf = red + (closes & 1u) * (kBlock / 32);
+          norm_warp_close(na, buf, dpart);
+          __syncthreads();
+          norm_publish(buf, sgrp[na.group].gs, kp.partials + na.chunk);
+        }
+      }
       return;
     }
     if (threadIdx.x == 0) {

@@ -307,6 +307,10 @@ def run_gpu(args):
     if args.workload == "large_uniform":
         spec = workloads.large_uniform(n_tensors=args.n_tensors or 201, numel=args.numel,
                                        seed=1237 + 1000 * rank)
+    elif args.workload == "large_uniform_bf16_state" and args.n_tensors:
+        spec = workloads.large_uniform(n_tensors=args.n_tensors, numel=args.numel,
+                                       seed=1237 + 1000 * rank, state_dtype=torch.bfloat16,
+                                       g_dtype=torch.bfloat16)
     elif args.workload == "many_small" and args.n_tensors:
         spec = workloads.many_small(n_tensors=args.n_tensors, seed=1239 + 1000 * rank)
     else:
@@ -429,7 +433,7 @@ def main(argv=None):
                     choices=["large_uniform", "capturable_l2", "remainder_shard", "many_small",
                              "large_uniform_bf16_state"])
     ap.add_argument("--n-tensors", type=int, default=None,
-                    help="tensor count of large_uniform (201) or many_small (20000)")
+                    help="tensor count of large_uniform[_bf16_state] (201) or many_small (20000)")
     ap.add_argument("--numel", type=int, default=320 * 65536)
     ap.add_argument("--variants", default="capturable,regular,graph,check_finite,norm,e2e")
     ap.add_argument("--no-cpu-baseline", action="store_true")
