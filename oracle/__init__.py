@@ -15,6 +15,10 @@ module only marshals numpy arrays and carries the per-step bookkeeping:
 * an optional inf/nan screen of the scaled gradients that sets the noop flag
   before any state is touched.
 
+Around the step, the one-GPU stand-in for the data-parallel exchange (the
+reduce-scatter that fills this rank's gradient shard, the all-gather of the
+param-out shard) is plain numpy float32 arithmetic in this module.
+
 Arrays: fp32 data are ``np.float32``; bf16 and fp16 data are ``np.uint16``
 bit patterns; remainders are ``np.int16``.  Every function is pinned by
 ``tests/test_oracle_pins.py``; none is "parity unpinned".
@@ -343,3 +347,69 @@ def clip_from_sumsq(total_sumsq: float, max_norm: float, grad_scale: float):
         coef = np.float32(max_norm) / (norm + np.float32(1e-6))
         coef = min(coef, np.float32(1.0))
         return norm, found_inf, np.float32(coef), np.float32(grad_scale) * np.float32(coef)
+
+
+# ---- the data-parallel exchange around the step (one-GPU stand-in) ------------
+#
+# "apex/contrib/optimizers/distributed_fused_adam.py": _start_bucket_grad_sync
+# (each rank's gradient bucket is reduce-scattered into this rank's shard
+# buffer, which has the grad sync dtype; ReduceOp.AVG when average_grad_sync,
+# SUM otherwise), _finish_bucket_grad_sync (the synced shard becomes the
+# gradient shard the local step reads) and _start_bucket_param_sync (every
+# rank's param shard is all-gathered into each rank's param bucket).
+# Readings: this rank's shard receives, element by element, the R ranks'
+# values widened to float and added in rank order 0, 1, ..., R-1, one IEEE
+# float addition at a time; the average divides that sum by R (one IEEE float
+# division); the result is rounded once to the grad dtype (nearest-even),
+# which is what the shard buffer holds.  The exchange runs whether or not the
+# step is then skipped.  The all-gather puts this rank's param-out shard,
+# byte for byte, at this rank's place in every rank's param bucket.
+
+def _widen(x, dtype) -> np.ndarray:
+    if dtype == DT_F32:
+        return np.asarray(x, dtype=np.float32)
+    return bf16_to_f32(x) if dtype == DT_BF16 else f16_to_f32(x)
+
+
+def _narrow(x, dtype) -> np.ndarray:
+    if dtype == DT_F32:
+        return np.asarray(x, dtype=np.float32).copy()
+    return f32_to_bf16(x) if dtype == DT_BF16 else f32_to_f16(x)
+
+
+def reduce_sources(sources, g_dtype: int, average: bool) -> np.ndarray:
+    """This rank's gradient shard from the R ranks' contributions to it
+    (``sources[r]``: rank r's values for this shard, in the grad dtype)."""
+    if len(sources) < 1:
+        raise ValueError("at least one source")
+    with np.errstate(over="ignore", invalid="ignore"):
+        acc = _widen(sources[0], g_dtype).copy()
+        for s in sources[1:]:
+            acc = acc + _widen(s, g_dtype)  # float32 + float32: one IEEE addition
+        if average:
+            acc = acc / np.float32(len(sources))
+    return _narrow(acc, g_dtype)
+
+
+def exchange_step(shard: Shard, sources, *, average: bool, capturable: bool,
+                  noop: bool = False, check_finite: bool = False,
+                  step_preadvanced: bool = False) -> bool:
+    """Reduce-scatter stand-in, then the shard step.  ``sources[i]`` lists the
+    R contributions for tensor i; each tensor's ``g`` is overwritten with the
+    reduced shard (the exchange happens even if the step is then skipped).
+    Returns the noop flag after the step; the all-gather side is
+    ``gather_param_out``."""
+    for t, src in zip(shard.tensors, sources):
+        t.g[...] = reduce_sources(src, t.g_dtype, average)
+    return shard_step(shard, capturable=capturable, noop=noop, check_finite=check_finite,
+                      step_preadvanced=step_preadvanced)
+
+
+def gather_param_out(p_out_shard, n_ranks: int, rank: int) -> np.ndarray:
+    """Every rank's bucket receives this rank's param-out shard at offset
+    rank * shard size; returns what this rank contributes to one bucket of
+    R shards (other ranks' places left zero)."""
+    shard = np.asarray(p_out_shard)
+    out = np.zeros(shard.size * n_ranks, dtype=shard.dtype)
+    out[rank * shard.size:(rank + 1) * shard.size] = shard
+    return out

@@ -618,3 +618,152 @@ def test_clip_coefficient_cases():
     assert oracle.clip_from_sumsq(1e80, 1.0, 1.0)[1]
     # no clipping requested
     assert oracle.clip_from_sumsq(16.0, 0.0, 0.5)[2:] == (np.float32(1.0), np.float32(0.5))
+
+
+# ---- the data-parallel exchange (one-GPU stand-in) -----------------------------
+
+def _golden_reduce_rows():
+    rows = []
+    path = os.path.join(os.path.dirname(__file__), "golden", "reduce_sources.txt")
+    with open(path) as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, srcs = line.split("|")
+            dt, op, expected = head.split()
+            rows.append((dt, op, float(expected), [float(x) for x in srcs.split()]))
+    return rows
+
+
+_DT = {"f32": DT_F32, "bf16": DT_BF16, "f16": DT_F16}
+
+
+def _to_dtype(x, dt):
+    x = np.asarray(x, np.float32)
+    if dt == DT_F32:
+        return x
+    return oracle.f32_to_bf16(x) if dt == DT_BF16 else oracle.f32_to_f16(x)
+
+
+def _from_dtype(x, dt):
+    if dt == DT_F32:
+        return np.asarray(x, np.float32)
+    return oracle.bf16_to_f32(x) if dt == DT_BF16 else oracle.f16_to_f32(x)
+
+
+@pytest.mark.parametrize("row", _golden_reduce_rows(), ids=lambda r: f"{r[0]}-{r[1]}-{r[2]}")
+def test_reduce_sources_golden_rows(row):
+    dts, op, expected, values = row
+    dt = _DT[dts]
+    srcs = [_to_dtype([v], dt) for v in values]
+    for s, v in zip(srcs, values):  # the fixture's inputs are exact in their dtype
+        assert _from_dtype(s, dt)[0] == np.float32(v) or (np.isnan(v) and np.isnan(_from_dtype(s, dt)[0]))
+    got = _from_dtype(oracle.reduce_sources(srcs, dt, op == "avg"), dt)[0]
+    if np.isnan(expected):
+        assert np.isnan(got)
+    else:
+        assert got == np.float32(expected) and np.signbit(got) == np.signbit(np.float32(expected))
+
+
+def _round_f32_exact(q):
+    """Nearest float32 to the rational q, ties to even, by exact comparison
+    (independent of the oracle's float arithmetic)."""
+    from fractions import Fraction
+    r0 = np.float32(float(q))
+    cands = [np.nextafter(r0, np.float32(-np.inf)), r0, np.nextafter(r0, np.float32(np.inf))]
+    best = None
+    for c in cands:
+        d = abs(Fraction(float(c)) - q)
+        key = (d, int(np.asarray(c, np.float32).view(np.uint32)) & 1)
+        if best is None or key < best[0]:
+            best = (key, c)
+    return best[1]
+
+
+def test_reduce_sources_average_is_correctly_rounded_when_the_sum_is_exact():
+    """Small-integer contributions: the float sum is exact, so the average
+    must be the nearest float to the exact rational sum / R."""
+    from fractions import Fraction
+    rng = np.random.default_rng(16)
+    for r in (3, 5, 6, 7, 12):
+        srcs = [rng.integers(-1000, 1000, 500).astype(np.float32) for _ in range(r)]
+        got = oracle.reduce_sources(srcs, DT_F32, True)
+        total = np.sum(np.stack(srcs).astype(np.int64), axis=0)
+        for i in range(0, 500, 7):
+            want = _round_f32_exact(Fraction(int(total[i]), r))
+            assert got[i] == want, (r, i)
+
+
+def test_reduce_sources_invariants():
+    rng = np.random.default_rng(17)
+    x = rng.standard_normal(4096).astype(np.float32)
+    # one rank, sum or average: the values themselves
+    for avg in (False, True):
+        assert oracle.reduce_sources([x], DT_F32, avg).tobytes() == x.tobytes()
+    # two equal contributions averaged: x + x = 2x exactly, halved exactly
+    assert oracle.reduce_sources([x, x], DT_F32, True).tobytes() == x.tobytes()
+    # x and -x cancel to +0
+    z = oracle.reduce_sources([x, -x], DT_F32, False)
+    assert not np.any(z) and not np.any(np.signbit(z))
+    # 16-bit: the result is the nearest-even rounding of the float result
+    xb = oracle.f32_to_bf16(x)
+    yb = oracle.f32_to_bf16(rng.standard_normal(4096).astype(np.float32))
+    f = oracle.bf16_to_f32(xb) + oracle.bf16_to_f32(yb)
+    assert np.array_equal(oracle.reduce_sources([xb, yb], DT_BF16, False), oracle.f32_to_bf16(f))
+
+
+def _exchange_shard(seed, n=(3000, 17, 1024)):
+    rng = np.random.default_rng(seed)
+    tensors = []
+    for i, k in enumerate(n):
+        tensors.append(oracle.Tensor(group=i % 2, p=rng.standard_normal(k).astype(np.float32),
+                                     m=np.zeros(k, np.float32), v=np.zeros(k, np.float32),
+                                     g=np.zeros(k, np.uint16), g_dtype=DT_BF16,
+                                     p_out=np.zeros(k, np.uint16), out_dtype=DT_BF16))
+    groups = [Group(mode=MODE_ADAMW, weight_decay=0.1, lr=1e-3), Group(mode=MODE_L2, lr=1e-3)]
+    return oracle.Shard(groups=groups, tensors=tensors)
+
+
+def test_exchange_with_one_rank_is_the_plain_step():
+    a, b = _exchange_shard(18), _exchange_shard(18)
+    rng = np.random.default_rng(19)
+    srcs = [[oracle.f32_to_bf16(rng.standard_normal(t.g.size).astype(np.float32) * 1e-2)]
+            for t in a.tensors]
+    for t, s in zip(b.tensors, srcs):
+        t.g[...] = s[0]
+    oracle.exchange_step(a, srcs, average=True, capturable=True)
+    oracle.shard_step(b, capturable=True)
+    for ta, tb in zip(a.tensors, b.tensors):
+        for k in ("p", "m", "v", "g", "p_out"):
+            assert getattr(ta, k).tobytes() == getattr(tb, k).tobytes()
+    assert a.steps == b.steps
+
+
+def test_exchange_noop_and_screen():
+    rng = np.random.default_rng(20)
+    sh = _exchange_shard(21)
+    before = [(t.p.copy(), t.m.copy(), t.v.copy()) for t in sh.tensors]
+    srcs = [[oracle.f32_to_bf16(rng.standard_normal(t.g.size).astype(np.float32))
+             for _ in range(3)] for t in sh.tensors]
+    # a set flag: the exchange still fills the gradient shard; nothing else moves
+    assert oracle.exchange_step(sh, srcs, average=True, capturable=True, noop=True)
+    for t, s, (p, m, v) in zip(sh.tensors, srcs, before):
+        assert t.g.tobytes() == oracle.reduce_sources(s, DT_BF16, True).tobytes()
+        assert t.p.tobytes() == p.tobytes() and t.m.tobytes() == m.tobytes()
+    assert sh.steps == [0, 0]
+    # an inf in one rank's contribution reaches the shard and the screen skips the step
+    srcs[1][2][5] = 0x7F80  # bf16 +inf
+    assert oracle.exchange_step(sh, srcs, average=True, capturable=True, check_finite=True)
+    assert sh.steps == [0, 0]
+    assert np.isinf(oracle.bf16_to_f32(sh.tensors[1].g)[5])
+
+
+def test_gather_places_each_rank_shard():
+    rng = np.random.default_rng(22)
+    r, s = 4, 1000
+    shards = [oracle.f32_to_bf16(rng.standard_normal(s).astype(np.float32)) for _ in range(r)]
+    bucket = np.zeros(r * s, np.uint16)
+    for k in range(r):
+        bucket |= oracle.gather_param_out(shards[k], r, k)
+    assert bucket.tobytes() == np.concatenate(shards).tobytes()
