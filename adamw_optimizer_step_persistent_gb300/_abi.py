@@ -22,6 +22,8 @@ DT_NONE, DT_F32, DT_BF16, DT_F16 = 0, 1, 2, 3
 CAPTURABLE, REMAINDERS, CHECK_FINITE, STEP_PREADVANCED = 1, 2, 4, 8
 TEST_BARRIER_TIMEOUT = 0x80000000  # diagnostic: the screen's grid barrier runs out
 MAX_GROUPS = 32
+MAX_SOURCES = 16
+MAX_DESTS = 16
 
 
 class Tensor(ctypes.Structure):
@@ -79,6 +81,10 @@ SIGNATURES = [
                                   _i32, _i32, _u32, _vp, _vp]),
     ("fadam_grad_sumsq", _i32, [_vp, _vp, _vp]),
     ("fadam_clip_apply", _i32, [_vp, _vp, _f32, _vp, _vp, _vp]),
+    ("fadam_plan_set_exchange", _i32, [_vp, _vp, ctypes.POINTER(_vp), _i32, _i32, _vp,
+                                       ctypes.POINTER(_vp), _i32]),
+    ("fadam_grad_reduce", _i32, [_vp, _vp]),
+    ("fadam_step_reduce", _i32, [_vp, _vp, _vp]),
     ("fadam_status_string", ctypes.c_char_p, [_i32]),
     ("fadam_last_error", ctypes.c_char_p, []),
     ("fadam_version", _i32, []),

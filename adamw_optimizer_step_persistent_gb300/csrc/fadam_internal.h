@@ -87,9 +87,12 @@ constexpr uint32_t kCapturable = FADAM_CAPTURABLE;
 constexpr uint32_t kCheckFinite = FADAM_CHECK_FINITE;
 constexpr uint32_t kPreadvanced = FADAM_STEP_PREADVANCED;
 constexpr uint32_t kTestBarrierTimeout = FADAM_TEST_BARRIER_TIMEOUT;
-// Launch-only flag (never a plan flag): compute the squared gradient norm
-// instead of the update.
+// Launch-only flags (never plan flags): compute the squared gradient norm
+// instead of the update; write the gradient shard from the exchange sources
+// (alone, or before the update with a grid barrier between).
 constexpr uint32_t kNormOnly = 1u << 30;
+constexpr uint32_t kReduceOnly = 1u << 29;
+constexpr uint32_t kReduceFirst = 1u << 28;
 
 // Everything one launch needs, passed as a __grid_constant__ parameter.
 struct alignas(16) KParams {
@@ -104,6 +107,14 @@ struct alignas(16) KParams {
   int32_t n_groups;
   uint32_t flags;
   int32_t reserved;
+  // the data-parallel exchange: byte offsets from the shard's g to each
+  // source's, and from p_out to each extra destination
+  int32_t n_sources;
+  int32_t average;
+  int32_t n_dests;
+  int32_t reserved2;
+  int64_t src_delta[FADAM_MAX_SOURCES];
+  int64_t dst_delta[FADAM_MAX_DESTS];
   KGroup groups[FADAM_MAX_GROUPS];
 };
 

@@ -146,24 +146,48 @@ __device__ __forceinline__ unsigned short narrow(float x) {
   }
 }
 
-template <int OT>
-__device__ __forceinline__ void store_out4(void* base, int i, const float (&x)[4]) {
-  if constexpr (OT == FADAM_DT_F32) {
-    __stcs(reinterpret_cast<float4*>(base) + i, make_float4(x[0], x[1], x[2], x[3]));
-  } else if constexpr (OT == FADAM_DT_BF16 || OT == FADAM_DT_F16) {
+// 4 floats rounded to dtype DT (nearest-even for 16-bit types).
+template <int DT>
+__device__ __forceinline__ typename Raw4<DT>::T pack_out4(const float (&x)[4]) {
+  if constexpr (DT == FADAM_DT_F32) {
+    return make_float4(x[0], x[1], x[2], x[3]);
+  } else {
     uint2 w;
-    w.x = static_cast<unsigned>(narrow<OT>(x[0])) | (static_cast<unsigned>(narrow<OT>(x[1])) << 16);
-    w.y = static_cast<unsigned>(narrow<OT>(x[2])) | (static_cast<unsigned>(narrow<OT>(x[3])) << 16);
-    __stcs(reinterpret_cast<uint2*>(base) + i, w);
+    w.x = static_cast<unsigned>(narrow<DT>(x[0])) | (static_cast<unsigned>(narrow<DT>(x[1])) << 16);
+    w.y = static_cast<unsigned>(narrow<DT>(x[2])) | (static_cast<unsigned>(narrow<DT>(x[3])) << 16);
+    return w;
   }
 }
 
+// Extra destinations of the param-out copy (the all-gather side of the
+// data-parallel exchange): the same element lands at the same byte offset
+// from each destination's start as from p_out's.
+struct Dests {
+  int n;
+  const int64_t* delta;
+};
+
+template <class T>
+__device__ __forceinline__ void store_all(T* base, int i, const T& x, const Dests* d) {
+  __stcs(base + i, x);
+  if (d)
+    for (int k = 0; k < d->n; ++k)
+      __stcs(reinterpret_cast<T*>(reinterpret_cast<char*>(base) + d->delta[k]) + i, x);
+}
+
 template <int OT>
-__device__ __forceinline__ void store_out1(void* base, int i, float x) {
+__device__ __forceinline__ void store_out4(void* base, int i, const float (&x)[4],
+                                           const Dests* d = nullptr) {
+  if constexpr (OT == FADAM_DT_F32 || OT == FADAM_DT_BF16 || OT == FADAM_DT_F16)
+    store_all(reinterpret_cast<typename Raw4<OT>::T*>(base), i, pack_out4<OT>(x), d);
+}
+
+template <int OT>
+__device__ __forceinline__ void store_out1(void* base, int i, float x, const Dests* d = nullptr) {
   if constexpr (OT == FADAM_DT_F32) {
-    __stcs(reinterpret_cast<float*>(base) + i, x);
+    store_all(reinterpret_cast<float*>(base), i, x, d);
   } else if constexpr (OT == FADAM_DT_BF16 || OT == FADAM_DT_F16) {
-    __stcs(reinterpret_cast<unsigned short*>(base) + i, narrow<OT>(x));
+    store_all(reinterpret_cast<unsigned short*>(base), i, narrow<OT>(x), d);
   }
 }
 
@@ -220,7 +244,7 @@ __device__ __forceinline__ void update4_state(const typename Raw4<ST>::T& P,
                                               const typename Raw4<ST>::T& M,
                                               const typename Raw4<ST>::T& V,
                                               const typename Raw4<GT>::T& G, const Scal& s, void* p,
-                                              void* m, void* v, void* out, int i) {
+                                              void* m, void* v, void* out, int i, const Dests& d) {
   float g[4], x[4], mm[4], vv[4];
   widen4<GT>(G, g);
   widen4<ST>(P, x);
@@ -231,7 +255,7 @@ __device__ __forceinline__ void update4_state(const typename Raw4<ST>::T& P,
   store_out4<ST>(p, i, x);
   store_out4<ST>(m, i, mm);
   store_out4<ST>(v, i, vv);
-  store_out4<OT>(out, i, x);
+  store_out4<OT>(out, i, x, &d);
 }
 
 // One 4-element vector of the remainder form: H the bf16 high halves, R the
@@ -239,7 +263,8 @@ __device__ __forceinline__ void update4_state(const typename Raw4<ST>::T& P,
 template <bool ADAMW, int GT>
 __device__ __forceinline__ void update4_rem(const uint2& H, const uint2& R, float4 M, float4 V,
                                             const typename Raw4<GT>::T& G, const Scal& s,
-                                            uint2* r4, float4* m4, float4* v4, uint2* o4, int i) {
+                                            uint2* r4, float4* m4, float4* v4, uint2* o4, int i,
+                                            const Dests& d) {
   float g[4];
   widen4<GT>(G, g);
   unsigned short hh[4], rr[4], oh[4], orr[4];
@@ -255,7 +280,7 @@ __device__ __forceinline__ void update4_rem(const uint2& H, const uint2& R, floa
   __stcs(r4 + i, pack4(orr));
   __stcs(m4 + i, make_float4(m[0], m[1], m[2], m[3]));
   __stcs(v4 + i, make_float4(v[0], v[1], v[2], v[3]));
-  __stcs(o4 + i, pack4(oh));
+  store_all(o4, i, pack4(oh), &d);
 }
 
 // ---- bulk-copy pipeline -----------------------------------------------------
@@ -367,8 +392,18 @@ __device__ __forceinline__ int bulk_tiles(const Item& it) {
 }
 
 // What a pipeline pass moves through shared memory.
-// kScan: only g, for the inf/nan screen; kNorm: only g, for the squared norm
-enum class Pass { kUpdate, kScan, kNorm };
+// kScan: only g, for the inf/nan screen; kNorm: only g, for the squared norm;
+// kReduce: the exchange sources' slices of g, reduced into the shard's g.
+enum class Pass { kUpdate, kScan, kNorm, kReduce };
+
+// Vectors of a reduce tile: as many as the R source slices fit in one stage
+// (at most the screen's 4 per thread), a multiple of one warp.
+template <int ST, int GT, bool REM>
+__host__ __device__ constexpr int reduce_vectors(int n_sources) {
+  using L = Layout<ST, GT, REM>;
+  const int v = static_cast<int>(L::stage / (static_cast<unsigned>(n_sources) * L::kG));
+  return (v < 4 * kTile ? v : 4 * kTile) & ~31;
+}
 
 // Vectors in one tile of a pass (Layout::update_vectors or ::scan_vectors).
 template <int ST, int GT, bool REM, Pass PASS>
@@ -380,14 +415,21 @@ __host__ __device__ constexpr int tile_vectors() {
 // Thread 0 of the CTA: start the copies of vectors [v0, v0 + len) of `it`
 // into buffer `slot % kStages`.
 template <int ST, int GT, bool REM, Pass PASS>
-__device__ __forceinline__ void issue_tile(const Item& it, int v0, unsigned len, unsigned slot,
-                                           unsigned char* smem, uint64_t* full) {
+__device__ __forceinline__ void issue_tile(const KParams& kp, const Item& it, int v0, unsigned len,
+                                           unsigned slot, unsigned char* smem, uint64_t* full) {
   using L = Layout<ST, GT, REM>;
   const unsigned b = slot % kStages;
   unsigned char* st = smem + size_t(b) * L::stage;
   uint64_t* bar = full + b;
   const size_t v = static_cast<size_t>(v0);
-  if constexpr (PASS != Pass::kUpdate) {
+  if constexpr (PASS == Pass::kReduce) {
+    // source r's slice at r * (vectors of a reduce tile) in the stage
+    const size_t stride = size_t(reduce_vectors<ST, GT, REM>(kp.n_sources)) * L::kG;
+    mbar_expect_tx(bar, static_cast<unsigned>(kp.n_sources) * len * L::kG);
+    const char* g = static_cast<const char*>(it.g) + v * L::kG;
+    for (int r = 0; r < kp.n_sources; ++r)
+      bulk_load(st + size_t(r) * stride, g + kp.src_delta[r], len * L::kG, bar);
+  } else if constexpr (PASS != Pass::kUpdate) {
     mbar_expect_tx(bar, len * L::kG);
     bulk_load(st, static_cast<const char*>(it.g) + v * L::kG, len * L::kG, bar);
   } else {
@@ -449,18 +491,23 @@ __device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, un
     pr.v = ch.tile0 * kTile;
     pr.vend = min((ch.tile0 + ch.ntiles) * kTile, bulk_vectors(pr.it));
   }
-  const int len = min(tile_vectors<ST, GT, REM, PASS>(), pr.vend - pr.v);
+  int tv;
+  if constexpr (PASS == Pass::kReduce) tv = reduce_vectors<ST, GT, REM>(kp.n_sources);
+  else tv = tile_vectors<ST, GT, REM, PASS>();
+  const int len = min(tv, pr.vend - pr.v);
   tags[pr.slot % kStages] = TileTag{pr.item, pr.v, len, pr.chunk};
-  issue_tile<ST, GT, REM, PASS>(pr.it, pr.v, static_cast<unsigned>(len), pr.slot, smem, full);
+  issue_tile<ST, GT, REM, PASS>(kp, pr.it, pr.v, static_cast<unsigned>(len), pr.slot, smem, full);
   pr.v += len;
   ++pr.slot;
 }
 
 // Consume one tile from shared memory: thread t takes vectors t, t + kTile,
-// ... of it.
-template <bool ADAMW, int ST, int GT, int OT, bool REM>
+// ... of it.  DESTS: param-out also goes to the exchange destinations (a
+// separate instance, so the plain step carries no destination loop).
+template <bool ADAMW, int ST, int GT, int OT, bool REM, bool DESTS>
 __device__ __forceinline__ void update_tile(const Item& it, const Scal& s, const unsigned char* st,
-                                            int v0, int len) {
+                                            int v0, int len, const Dests& d0) {
+  const Dests d{DESTS ? d0.n : 0, d0.delta};
   using L = Layout<ST, GT, REM>;
 #pragma unroll
   for (int q = 0; q < L::update_vectors / kTile; ++q) {
@@ -475,15 +522,78 @@ __device__ __forceinline__ void update_tile(const Item& it, const Scal& s, const
       const float4 V = reinterpret_cast<const float4*>(st + L::off_v)[t];
       update4_rem<ADAMW, GT>(H, R, M, V, G, s, reinterpret_cast<uint2*>(it.rem),
                              reinterpret_cast<float4*>(it.m), reinterpret_cast<float4*>(it.v),
-                             reinterpret_cast<uint2*>(it.p_out), i);
+                             reinterpret_cast<uint2*>(it.p_out), i, d);
     } else {
       using S4 = typename Raw4<ST>::T;
       const S4 P = reinterpret_cast<const S4*>(st)[t];
       const S4 M = reinterpret_cast<const S4*>(st + L::off_m)[t];
       const S4 V = reinterpret_cast<const S4*>(st + L::off_v)[t];
-      update4_state<ADAMW, ST, GT, OT>(P, M, V, G, s, it.p, it.m, it.v, it.p_out, i);
+      update4_state<ADAMW, ST, GT, OT>(P, M, V, G, s, it.p, it.m, it.v, it.p_out, i, d);
     }
   }
+}
+
+// ---- the reduce-scatter stand-in ---------------------------------------------
+//
+// "apex/contrib/optimizers/distributed_fused_adam.py", _start_bucket_grad_sync:
+// this rank's shard of g from the R ranks' contributions, widened to float
+// and added in rank order (one IEEE addition each), divided by R for
+// ReduceOp.AVG (one IEEE division), rounded once to the grad dtype.  With
+// the screen on, the reduced g*grad_scale is tested as the update will use
+// it.
+
+template <int GT>
+__device__ __forceinline__ float stored_value(float x) {
+  if constexpr (GT == FADAM_DT_F32) return x;
+  else if constexpr (GT == FADAM_DT_BF16) return bf16_to_f32(narrow<GT>(x));
+  else return f16_to_f32(narrow<GT>(x));
+}
+
+// One tile: source r's vectors at r * stride in the stage.
+template <int ST, int GT, bool REM>
+__device__ __forceinline__ bool reduce_tile(const KParams& kp, const Item& it,
+                                            const unsigned char* st, int v0, int len, float gs,
+                                            bool screen) {
+  using L = Layout<ST, GT, REM>;
+  using G4 = typename Raw4<GT>::T;
+  const size_t stride = size_t(reduce_vectors<ST, GT, REM>(kp.n_sources)) * L::kG;
+  const float rn = static_cast<float>(kp.n_sources);
+  bool bad = false;
+  for (int t = threadIdx.x; t < len; t += kBlock) {
+    float acc[4];
+    widen4<GT>(reinterpret_cast<const G4*>(st)[t], acc);
+    for (int r = 1; r < kp.n_sources; ++r) {
+      float x[4];
+      widen4<GT>(reinterpret_cast<const G4*>(st + size_t(r) * stride)[t], x);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
+    }
+    if (kp.average) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[e] = __fdiv_rn(acc[e], rn);
+    }
+    const G4 w = pack_out4<GT>(acc);
+    __stcs(reinterpret_cast<G4*>(const_cast<void*>(it.g)) + v0 + t, w);
+    if (screen) {
+      float y[4];
+      widen4<GT>(w, y);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) bad |= !isfinite(__fmul_rn(y[e], gs));
+    }
+  }
+  return bad;
+}
+
+// One element, straight from global memory (tails, unaligned items).
+template <int GT>
+__device__ __forceinline__ bool reduce_elem(const KParams& kp, const Item& it, int i, float gs,
+                                            bool screen) {
+  const char* g = static_cast<const char*>(it.g);
+  float acc = load1<GT>(g + kp.src_delta[0], i);
+  for (int r = 1; r < kp.n_sources; ++r) acc = __fadd_rn(acc, load1<GT>(g + kp.src_delta[r], i));
+  if (kp.average) acc = __fdiv_rn(acc, static_cast<float>(kp.n_sources));
+  store_out1<GT>(const_cast<void*>(it.g), i, acc);
+  return screen && !isfinite(__fmul_rn(stored_value<GT>(acc), gs));
 }
 
 template <int GT>
@@ -693,6 +803,8 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
                                           unsigned char* smem, uint64_t* full, TileTag* tags,
                                           Producer& pr, double* red, unsigned& stage, bool& bad,
                                           bool& timed_out) {
+  const Dests dst{kp.n_dests, kp.dst_delta};
+  const bool screen = (kp.flags & kCheckFinite) != 0;  // reduce pass: screen the result
   NormAcc na{0.0f, 0.0f, false, -1, 0};
   NormPending pend{-1, 0.0f};
   double* dpart = nullptr;
@@ -732,9 +844,17 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
           bad |= scan_tile<GT>(st, tag.len, s.gs);
         } else if constexpr (PASS == Pass::kNorm) {
           norm_tile<GT>(st, tag, it.group, na, sgrp, red, dpart, closes, pend);
+        } else if constexpr (PASS == Pass::kReduce) {
+          bad |= reduce_tile<ST, GT, REM>(kp, it, st, tag.v0, tag.len, s.gs, screen);
         } else {
-          if (G.bits & kGroupAdamW) update_tile<true, ST, GT, OT, REM>(it, s, st, tag.v0, tag.len);
-          else update_tile<false, ST, GT, OT, REM>(it, s, st, tag.v0, tag.len);
+          const bool aw = (G.bits & kGroupAdamW) != 0;
+          if (dst.n == 0) {
+            if (aw) update_tile<true, ST, GT, OT, REM, false>(it, s, st, tag.v0, tag.len, dst);
+            else update_tile<false, ST, GT, OT, REM, false>(it, s, st, tag.v0, tag.len, dst);
+          } else {
+            if (aw) update_tile<true, ST, GT, OT, REM, true>(it, s, st, tag.v0, tag.len, dst);
+            else update_tile<false, ST, GT, OT, REM, true>(it, s, st, tag.v0, tag.len, dst);
+          }
         }
       }
     }
@@ -773,17 +893,19 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
 // ---- element-wise paths (tails, runs not 16-byte aligned) -------------------
 
 template <bool ADAMW, int ST, int GT, int OT>
-__device__ __forceinline__ void update_elem_state(const Item& it, const Scal& s, int i) {
+__device__ __forceinline__ void update_elem_state(const Item& it, const Scal& s, int i,
+                                                  const Dests& d) {
   float m = load1<ST>(it.m, i), v = load1<ST>(it.v, i);
   const float x = adam_elem<ADAMW>(load1<ST>(it.p, i), m, v, load1<GT>(it.g, i), s);
   store_out1<ST>(it.p, i, x);
   store_out1<ST>(it.m, i, m);
   store_out1<ST>(it.v, i, v);
-  store_out1<OT>(it.p_out, i, x);
+  store_out1<OT>(it.p_out, i, x, &d);
 }
 
 template <bool ADAMW, int GT>
-__device__ __forceinline__ void update_elem_rem(const Item& it, const Scal& s, int i) {
+__device__ __forceinline__ void update_elem_rem(const Item& it, const Scal& s, int i,
+                                                const Dests& d) {
   const unsigned short* hp = reinterpret_cast<const unsigned short*>(it.p);
   unsigned short* rp = reinterpret_cast<unsigned short*>(it.rem);
   float* mp = reinterpret_cast<float*>(it.m);
@@ -797,20 +919,20 @@ __device__ __forceinline__ void update_elem_rem(const Item& it, const Scal& s, i
   __stcs(rp + i, orr);
   __stcs(mp + i, m);
   __stcs(vp + i, v);
-  __stcs(op + i, oh);
+  store_all(op, i, oh, &d);
 }
 
 template <bool ADAMW, int ST, int GT, int OT, bool REM>
-__device__ __forceinline__ void update_elem(const Item& it, const Scal& s, int i) {
-  if constexpr (REM) update_elem_rem<ADAMW, GT>(it, s, i);
-  else update_elem_state<ADAMW, ST, GT, OT>(it, s, i);
+__device__ __forceinline__ void update_elem(const Item& it, const Scal& s, int i, const Dests& d) {
+  if constexpr (REM) update_elem_rem<ADAMW, GT>(it, s, i, d);
+  else update_elem_state<ADAMW, ST, GT, OT>(it, s, i, d);
 }
 
 // A whole item not aligned for bulk copies, by the whole CTA: 128-bit
 // streaming loads when every stream is vector-aligned, then element by
 // element for the rest.
 template <bool ADAMW, int ST, int GT, int OT, bool REM>
-__device__ __forceinline__ void simt_item(const Item& it, const Scal& s) {
+__device__ __forceinline__ void simt_item(const Item& it, const Scal& s, const Dests& d) {
   const int n = it.n;
   int scalar_from = 0;
   if (it.flags & kItemVec) {
@@ -839,7 +961,7 @@ __device__ __forceinline__ void simt_item(const Item& it, const Scal& s) {
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int i = base + u * kBlock;
-          if (i < nv) update4_rem<ADAMW, GT>(H[u], R[u], M[u], V[u], G[u], s, r4, m4, v4, o4, i);
+          if (i < nv) update4_rem<ADAMW, GT>(H[u], R[u], M[u], V[u], G[u], s, r4, m4, v4, o4, i, d);
         }
       } else {
         typename Raw4<ST>::T P[kUnroll], M[kUnroll], V[kUnroll];
@@ -858,13 +980,15 @@ __device__ __forceinline__ void simt_item(const Item& it, const Scal& s) {
         for (int u = 0; u < kUnroll; ++u) {
           const int i = base + u * kBlock;
           if (i < nv)
-            update4_state<ADAMW, ST, GT, OT>(P[u], M[u], V[u], G[u], s, it.p, it.m, it.v, it.p_out, i);
+            update4_state<ADAMW, ST, GT, OT>(P[u], M[u], V[u], G[u], s, it.p, it.m, it.v, it.p_out, i,
+                                             d);
         }
       }
     }
     scalar_from = nv * kVec;
   }
-  for (int i = scalar_from + threadIdx.x; i < n; i += kBlock) update_elem<ADAMW, ST, GT, OT, REM>(it, s, i);
+  for (int i = scalar_from + threadIdx.x; i < n; i += kBlock)
+    update_elem<ADAMW, ST, GT, OT, REM>(it, s, i, d);
 }
 
 // True when this thread saw a non-finite g*grad_scale in the item (by the
@@ -897,6 +1021,8 @@ template <int ST, int GT, int OT, bool REM, Pass PASS>
 __device__ __forceinline__ bool tail_pass(const KParams& kp, const SGroup* sgrp, unsigned* counter,
                                           int n_items) {
   const int lane = threadIdx.x % 32;
+  const Dests dst{kp.n_dests, kp.dst_delta};
+  const bool screen = (kp.flags & kCheckFinite) != 0;
   bool bad = false;
   for (;;) {
     unsigned base = 0;
@@ -916,9 +1042,11 @@ __device__ __forceinline__ bool tail_pass(const KParams& kp, const SGroup* sgrp,
       } else if constexpr (PASS == Pass::kNorm) {
         const double x = load1<GT>(it.g, i);
         sq += x * x;
+      } else if constexpr (PASS == Pass::kReduce) {
+        bad |= reduce_elem<GT>(kp, it, i, s.gs, screen);
       } else {
-        if (G.bits & kGroupAdamW) update_elem<true, ST, GT, OT, REM>(it, s, i);
-        else update_elem<false, ST, GT, OT, REM>(it, s, i);
+        if (G.bits & kGroupAdamW) update_elem<true, ST, GT, OT, REM>(it, s, i, dst);
+        else update_elem<false, ST, GT, OT, REM>(it, s, i, dst);
       }
     }
     if constexpr (PASS == Pass::kNorm) {  // the item's slot, after the chunk slots
@@ -939,6 +1067,8 @@ __device__ __forceinline__ bool rest_pass(const KParams& kp, const SGroup* sgrp,
                                           int item_end, double* red) {
   __shared__ int s_count;
   __shared__ int s_list[kBlock];
+  const Dests dst{kp.n_dests, kp.dst_delta};
+  const bool screen = (kp.flags & kCheckFinite) != 0;
   bool bad = false;
   for (int base = item_begin; base < item_end; base += kBlock) {
     if (threadIdx.x == 0) s_count = 0;
@@ -967,9 +1097,11 @@ __device__ __forceinline__ bool rest_pass(const KParams& kp, const SGroup* sgrp,
           kp.partials[kp.n_chunks + s_list[q]] = static_cast<double>(G.gs) * G.gs * total;
           __threadfence();
         }
+      } else if constexpr (PASS == Pass::kReduce) {
+        for (int i = threadIdx.x; i < it.n; i += kBlock) bad |= reduce_elem<GT>(kp, it, i, s.gs, screen);
       } else {
-        if (G.bits & kGroupAdamW) simt_item<true, ST, GT, OT, REM>(it, s);
-        else simt_item<false, ST, GT, OT, REM>(it, s);
+        if (G.bits & kGroupAdamW) simt_item<true, ST, GT, OT, REM>(it, s, dst);
+        else simt_item<false, ST, GT, OT, REM>(it, s, dst);
       }
     }
     __syncthreads();  // s_list is reused
@@ -1099,8 +1231,33 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
                                            s_tags, s_prod, s_red, stage, unused, timed_out);
   }
 
+  // 1b. the reduce-scatter stand-in: this rank's g from the exchange
+  //     sources (alone, or before the update; it runs even when the step
+  //     is then skipped), screened in the same pass when the plan asks
+  const bool reduce_only = (kp.flags & kReduceOnly) != 0;
+  const bool reduce_first = (kp.flags & kReduceFirst) != 0;
+  const bool updates = !norm_only && !reduce_only;
+  if (reduce_only || reduce_first) {
+    bool bad = false;
+    run_pass<ST, GT, OT, REM, Pass::kReduce>(kp, sgrp, item_begin, item_end, &kp.scratch->next_scan,
+                                             &kp.scratch->next_tail_scan, n_items, s_tiles, s_full,
+                                             s_tags, s_prod, s_red, stage, bad, timed_out);
+    // the update copies g with the async proxy: order this thread's
+    // generic-proxy stores of g before that
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    if (reduce_first) {
+      if (__syncthreads_or(bad) && tid == 0) atomicExch(kp.noop, 1);
+      barrier_ok = grid_barrier(kp.scratch, (kp.flags & kTestBarrierTimeout) ? 1u : 0u);
+      if (tid == 0) {
+        s_noop = kp.noop ? (ld_acquire_s32(kp.noop) == 1) : 0;
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      __syncthreads();
+    }
+  }
+
   // 2. optional inf/nan screen over the whole shard before any update
-  if (!norm_only && (kp.flags & kCheckFinite)) {
+  if (updates && !reduce_first && (kp.flags & kCheckFinite)) {
     bool bad = false;
     if (!s_noop)
       run_pass<ST, GT, OT, REM, Pass::kScan>(kp, sgrp, item_begin, item_end, &kp.scratch->next_scan,
@@ -1113,7 +1270,7 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
   }
 
   // 3. the update
-  if (!norm_only && !s_noop && barrier_ok) {
+  if (updates && !s_noop && barrier_ok) {
     bool unused = false;
     run_pass<ST, GT, OT, REM, Pass::kUpdate>(kp, sgrp, item_begin, item_end, &kp.scratch->next_update,
                                          &kp.scratch->next_tail_update, n_items, s_tiles, s_full,
@@ -1143,7 +1300,7 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
   if (tid == 0) {
     if (s_last) {
       __threadfence();
-      if (!norm_only && capturable && !(kp.flags & kPreadvanced)) {
+      if (updates && capturable && !(kp.flags & kPreadvanced)) {
         const int adv = (s_noop || !barrier_ok) ? 0 : 1;
         for (int g = 0; g < kp.n_groups; ++g)
           if (sgrp[g].bits & kGroupOwnsStep) *kp.groups[g].step_dev = sgrp[g].step_old + adv;

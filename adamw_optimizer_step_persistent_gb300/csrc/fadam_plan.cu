@@ -490,6 +490,10 @@ struct fadam_plan {
   int32_t* d_cta = nullptr;
   KScratch* d_scratch = nullptr;
   double* d_partials = nullptr;  // gradient-norm launches: per-chunk and per-item partials
+  // the data-parallel exchange (fadam_plan_set_exchange): byte offsets
+  int32_t n_sources = 0, average = 0, n_dests = 0;
+  int64_t src_delta[FADAM_MAX_SOURCES] = {};
+  int64_t dst_delta[FADAM_MAX_DESTS] = {};
 };
 
 namespace {
@@ -520,6 +524,14 @@ void fill_params(KParams& kp, const Item* items, const int32_t* cta, const Chunk
   kp.n_groups = n_groups;
   kp.flags = flags;
   fill_kgroups(groups, n_groups, flags, kp.groups);
+}
+
+void fill_exchange(KParams& kp, const fadam_plan* plan) {
+  kp.n_sources = plan->n_sources;
+  kp.average = plan->average;
+  kp.n_dests = plan->n_dests;
+  for (int r = 0; r < plan->n_sources; ++r) kp.src_delta[r] = plan->src_delta[r];
+  for (int d = 0; d < plan->n_dests; ++d) kp.dst_delta[d] = plan->dst_delta[d];
 }
 
 bool needs_launch(const HostPlan& hp) {
@@ -616,8 +628,91 @@ fadam_status fadam_step(fadam_plan* plan, int32_t* noop_dev, fadam_stream stream
   KParams kp;
   fill_params(kp, plan->d_items, plan->d_cta, plan->d_chunks, static_cast<int32_t>(hp.chunks.size()),
               noop_dev, plan->d_scratch, plan->groups.data(), plan->n_groups, hp.flags);
+  fill_exchange(kp, plan);
+  kp.n_sources = 0;  // the plain step reads g as it stands
   return launch(hp.kernel, hp.smem, kp, hp.grid, (hp.flags & FADAM_CHECK_FINITE) != 0,
                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+fadam_status fadam_plan_set_exchange(fadam_plan* plan, const void* g_shard,
+                                     const void* const* sources, int32_t n_sources,
+                                     int32_t average, const void* out_shard,
+                                     void* const* dests, int32_t n_dests) {
+  t_last_error.clear();
+  if (!plan) return fail(FADAM_EINVAL, "plan is NULL");
+  if (n_sources < 0 || n_sources > FADAM_MAX_SOURCES)
+    return fail(FADAM_EINVAL, "n_sources %d outside 0..%d", n_sources, FADAM_MAX_SOURCES);
+  if (n_dests < 0 || n_dests > FADAM_MAX_DESTS)
+    return fail(FADAM_EINVAL, "n_dests %d outside 0..%d", n_dests, FADAM_MAX_DESTS);
+  if (average != 0 && average != 1) return fail(FADAM_EINVAL, "average must be 0 or 1");
+  int64_t src[FADAM_MAX_SOURCES] = {}, dst[FADAM_MAX_DESTS] = {};
+  if (n_sources > 0) {
+    if (!g_shard || !sources) return fail(FADAM_EINVAL, "g_shard and sources are needed");
+    for (int32_t r = 0; r < n_sources; ++r) {
+      if (!sources[r]) return fail(FADAM_EINVAL, "sources[%d] is NULL", r);
+      src[r] = static_cast<int64_t>(reinterpret_cast<uintptr_t>(sources[r]) -
+                                    reinterpret_cast<uintptr_t>(g_shard));
+      if (src[r] % 16) return fail(FADAM_EALIGN, "sources[%d] - g_shard is not a multiple of 16 bytes", r);
+    }
+  }
+  if (n_dests > 0) {
+    if (plan->hp.d.out == FADAM_DT_NONE && !plan->hp.d.rem)
+      return fail(FADAM_EINVAL, "exchange destinations need a param-out dtype");
+    if (!out_shard || !dests) return fail(FADAM_EINVAL, "out_shard and dests are needed");
+    for (int32_t d = 0; d < n_dests; ++d) {
+      if (!dests[d]) return fail(FADAM_EINVAL, "dests[%d] is NULL", d);
+      dst[d] = static_cast<int64_t>(reinterpret_cast<uintptr_t>(dests[d]) -
+                                    reinterpret_cast<uintptr_t>(out_shard));
+      if (dst[d] % 16) return fail(FADAM_EALIGN, "dests[%d] - out_shard is not a multiple of 16 bytes", d);
+    }
+  }
+  plan->n_sources = n_sources;
+  plan->average = average;
+  plan->n_dests = n_dests;
+  for (int r = 0; r < FADAM_MAX_SOURCES; ++r) plan->src_delta[r] = src[r];
+  for (int d = 0; d < FADAM_MAX_DESTS; ++d) plan->dst_delta[d] = dst[d];
+  return FADAM_OK;
+}
+
+fadam_status fadam_grad_reduce(fadam_plan* plan, fadam_stream stream) {
+  t_last_error.clear();
+  if (!plan) return fail(FADAM_EINVAL, "plan is NULL");
+  if (plan->n_sources < 1) return fail(FADAM_EINVAL, "no exchange sources set");
+  const HostPlan& hp = plan->hp;
+  if (hp.items.empty()) return FADAM_OK;
+  DeviceGuard guard(hp.device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  KParams kp;
+  fill_params(kp, plan->d_items, plan->d_cta, plan->d_chunks, static_cast<int32_t>(hp.chunks.size()),
+              nullptr, plan->d_scratch, plan->groups.data(), plan->n_groups,
+              (hp.flags & FADAM_CAPTURABLE) | kReduceOnly);
+  fill_exchange(kp, plan);
+  return launch(hp.kernel, hp.smem, kp, hp.grid, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fadam_status fadam_step_reduce(fadam_plan* plan, int32_t* noop_dev, fadam_stream stream) {
+  t_last_error.clear();
+  if (!plan) return fail(FADAM_EINVAL, "plan is NULL");
+  if (plan->n_sources < 1) return fail(FADAM_EINVAL, "no exchange sources set");
+  const HostPlan& hp = plan->hp;
+  if ((hp.flags & FADAM_CHECK_FINITE) && !noop_dev)
+    return fail(FADAM_EINVAL, "FADAM_CHECK_FINITE needs a noop_dev flag to write");
+  if (noop_dev && reinterpret_cast<uintptr_t>(noop_dev) % 4)
+    return fail(FADAM_EALIGN, "noop_dev is not 4-byte aligned");
+  if (!needs_launch(hp)) return FADAM_OK;
+  if (!(hp.flags & FADAM_CAPTURABLE))
+    for (int32_t i = 0; i < plan->n_groups; ++i)
+      if (plan->groups[i].bias_correction == 1 && plan->groups[i].step < 1)
+        return fail(FADAM_EINVAL, "group %d: step %d < 1 with bias correction (1-beta^step = 0)",
+                    i, plan->groups[i].step);
+  DeviceGuard guard(hp.device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  KParams kp;
+  fill_params(kp, plan->d_items, plan->d_cta, plan->d_chunks, static_cast<int32_t>(hp.chunks.size()),
+              noop_dev, plan->d_scratch, plan->groups.data(), plan->n_groups,
+              hp.flags | kReduceFirst);
+  fill_exchange(kp, plan);
+  return launch(hp.kernel, hp.smem, kp, hp.grid, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
 fadam_status fadam_step_host_grads(fadam_plan* plan, const void* const* g_host, int32_t* noop_dev,

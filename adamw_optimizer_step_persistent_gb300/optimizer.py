@@ -247,6 +247,57 @@ class FusedAdamShard:
         """Single-rank clip: grad_norm_sq then clip_apply."""
         return self.clip_apply(self.grad_norm_sq(), max_norm)
 
+    # ---- the data-parallel exchange (one-GPU stand-in) ----------------------------
+
+    def set_exchange(self, g_shard: torch.Tensor, sources: Sequence[torch.Tensor], *,
+                     average: bool = True, out_shard: Optional[torch.Tensor] = None,
+                     dests: Sequence[torch.Tensor] = ()) -> None:
+        """Register the reduce-scatter sources and the param all-gather
+        destinations (fadam_plan_set_exchange).  Every tensor's gradient is
+        a view of ``g_shard`` and each source is laid out like it (same
+        dtype, at least as many elements); every param-out copy is a view of
+        ``out_shard`` and each destination is laid out like it."""
+        for s in sources:
+            if s.dtype != g_shard.dtype or s.numel() < g_shard.numel() or s.device != g_shard.device:
+                raise ValueError("each source needs g_shard's dtype, device and at least its size")
+        if dests and out_shard is None:
+            raise ValueError("destinations need out_shard")
+        for d in dests:
+            if d.dtype != out_shard.dtype or d.numel() < out_shard.numel() or d.device != out_shard.device:
+                raise ValueError("each destination needs out_shard's dtype, device and at least its size")
+        src = (ctypes.c_void_p * max(1, len(sources)))(*[s.data_ptr() for s in sources])
+        dst = (ctypes.c_void_p * max(1, len(dests)))(*[d.data_ptr() for d in dests])
+        _abi.check(_abi.lib().fadam_plan_set_exchange(
+            self._plan, g_shard.data_ptr() if sources else None, src, len(sources), int(average),
+            out_shard.data_ptr() if dests else None, dst, len(dests)), "fadam_plan_set_exchange")
+        # the plan holds raw pointers: keep the buffers alive with it
+        self._exchange = (g_shard, list(sources), out_shard, list(dests))
+
+    def grad_reduce(self) -> None:
+        """The reduce-scatter stand-in alone: every tensor's gradient from the
+        sources.  One launch, no sync."""
+        _abi.check(_abi.lib().fadam_grad_reduce(self._plan, _stream_handle(self.device)),
+                   "fadam_grad_reduce")
+
+    def step_reduce(self, found_inf: bool = False) -> None:
+        """The reduce-scatter stand-in fused with the step (one launch).  The
+        gradient shard is written even when the step is skipped: regular
+        shards with ``found_inf`` run the reduction alone."""
+        lib = _abi.lib()
+        if self.capturable:
+            _abi.check(lib.fadam_step_reduce(self._plan, self.noop.data_ptr(),
+                                             _stream_handle(self.device)), "fadam_step_reduce")
+            return
+        if found_inf:
+            self.grad_reduce()
+            return
+        self.host_steps = [s + 1 for s in self.host_steps]
+        self._fill_groups()
+        _abi.check(lib.fadam_plan_set_groups(self._plan, self._groups_c, len(self.groups)),
+                   "fadam_plan_set_groups")
+        _abi.check(lib.fadam_step_reduce(self._plan, None, _stream_handle(self.device)),
+                   "fadam_step_reduce")
+
     # ---- state -------------------------------------------------------------------
 
     def group_steps(self) -> List[int]:

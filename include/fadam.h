@@ -98,6 +98,11 @@ typedef int32_t fadam_status;
 /* Maximum number of param groups in one plan. */
 #define FADAM_MAX_GROUPS 32
 
+/* Maximum numbers of gradient sources and extra param-out destinations of
+ * the data-parallel exchange (fadam_plan_set_exchange). */
+#define FADAM_MAX_SOURCES 16
+#define FADAM_MAX_DESTS 16
+
 /* One tensor (fragment) of the shard.  Every data pointer is a device
  * pointer to numel contiguous elements, aligned at least to its element
  * size.
@@ -197,7 +202,9 @@ fadam_status fadam_plan_set_groups(fadam_plan* plan, const fadam_group* groups,
                                    int32_t n_groups);
 
 /* One optimizer step over the whole shard: one persistent-grid kernel
- * launch on `stream`, or none when there is nothing to do.
+ * launch on `stream`, or none when there is nothing to do.  With exchange
+ * destinations set (fadam_plan_set_exchange), param-out is also written to
+ * every destination.
  *   noop_dev  int32 device flag (may be NULL when FADAM_CHECK_FINITE is not
  *             set).  When it equals 1 nothing is written: not p, m, v, rem,
  *             p_out, nor the step counters; any other value counts as clear
@@ -226,9 +233,10 @@ fadam_status fadam_step_host_grads(fadam_plan* plan, const void* const* g_host,
  * _local_grad_norm and grad_norm), written as one double to *sumsq_dev by
  * one launch on `stream`.  grad_scale is the host value of regular plans
  * and *grad_scale_dev of capturable ones.  Accumulation: float within a
- * tile, exactly in double wherever a float partial would overflow,
- * underflow or is not finite, double across tiles and CTAs (a fixed order:
- * the result is deterministic).  Across data-parallel ranks, all-reduce
+ * thread's share of a chunk of tiles (Kahan-compensated) and within a warp,
+ * exactly in double wherever a float partial would overflow, underflow or is
+ * not finite, double across warps, chunks and CTAs (a fixed order: the
+ * result is deterministic).  Across data-parallel ranks, all-reduce
  * (sum) *sumsq_dev before step two.  No allocation, no host sync: safe to
  * capture.  Errors: FADAM_EINVAL (NULL or misaligned sumsq_dev),
  * FADAM_ECUDA. */
@@ -245,6 +253,62 @@ fadam_status fadam_grad_sumsq(fadam_plan* plan, double* sumsq_dev, fadam_stream 
  * scale it there.  Errors: FADAM_EINVAL, FADAM_EALIGN, FADAM_ECUDA. */
 fadam_status fadam_clip_apply(fadam_plan* plan, const double* sumsq_dev, float max_norm,
                               float* norm_dev, int32_t* noop_dev, fadam_stream stream);
+
+/* The data-parallel exchange around the step, on one GPU
+ * ("apex/contrib/optimizers/distributed_fused_adam.py":
+ * _start_bucket_grad_sync, the reduce-scatter of every rank's gradient
+ * bucket into this rank's shard with ReduceOp.AVG or SUM, and
+ * _start_bucket_param_sync, the all-gather of every rank's param shard).
+ * A data-parallel group of R ranks is stood in for by R device buffers: the
+ * plan's gradients are this rank's shard (the tensors' g pointers all lie in
+ * one shard buffer starting at g_shard), and sources[r] is where rank r's
+ * contribution to that shard starts, laid out like the shard; each tensor's
+ * contribution from rank r is read at g + (sources[r] - g_shard).  Likewise
+ * the tensors' p_out pointers lie in one buffer starting at out_shard, and
+ * dests[d] is another buffer laid out like it (another rank's place for this
+ * shard in its param bucket); every p_out value is also written at
+ * p_out + (dests[d] - out_shard).
+ *   g_shard, sources[n_sources]   0 <= n_sources <= FADAM_MAX_SOURCES
+ *                                 (host array of device pointers, copied);
+ *                                 every sources[r] - g_shard a multiple of 16
+ *                                 bytes.  The sources are only read.
+ *   average                       1: the sum divided by R (ReduceOp.AVG);
+ *                                 0: the sum.
+ *   out_shard, dests[n_dests]     0 <= n_dests <= FADAM_MAX_DESTS, each
+ *                                 dests[d] - out_shard a multiple of 16
+ *                                 bytes; needs a param-out dtype.
+ * The reduction: the R values of an element widened to float and added in
+ * rank order one IEEE addition at a time, divided by R (one IEEE division)
+ * when averaging, rounded once (nearest-even) to the grad dtype and stored
+ * in the shard's g.  Buffers are owned by the caller and must stay valid
+ * while the plan is used; the pointers are copied on the host (no device
+ * memory is touched, so this may be called between captured launches;
+ * captured launches keep the pointers they were captured with).
+ * n_sources = 0 and n_dests = 0 remove the exchange.  Errors: FADAM_EINVAL
+ * (counts out of range, NULL pointers, destinations without a param-out
+ * dtype), FADAM_EALIGN (a difference not a multiple of 16 bytes). */
+fadam_status fadam_plan_set_exchange(fadam_plan* plan, const void* g_shard,
+                                     const void* const* sources, int32_t n_sources,
+                                     int32_t average, const void* out_shard,
+                                     void* const* dests, int32_t n_dests);
+
+/* The reduce-scatter stand-in alone: one launch that writes this rank's
+ * gradient shard (every tensor's g) from the plan's sources, as described
+ * at fadam_plan_set_exchange.  It touches nothing else (no state, no step
+ * counter, no noop flag), so it can feed fadam_grad_sumsq and
+ * fadam_clip_apply before fadam_step.  Safe to capture.  Errors:
+ * FADAM_EINVAL (no sources set), FADAM_ECUDA. */
+fadam_status fadam_grad_reduce(fadam_plan* plan, fadam_stream stream);
+
+/* The reduce-scatter stand-in fused with the step: one cooperative launch
+ * that first writes the gradient shard from the sources (as
+ * fadam_grad_reduce; with FADAM_CHECK_FINITE the inf/nan screen of the
+ * reduced g*grad_scale happens in the same pass), waits at a bounded grid
+ * barrier, then runs the step exactly as fadam_step (param-out also to the
+ * plan's destinations).  The gradient shard is written even when the step
+ * is skipped (a set noop flag).  Errors: as fadam_step, and FADAM_EINVAL
+ * when no sources are set. */
+fadam_status fadam_step_reduce(fadam_plan* plan, int32_t* noop_dev, fadam_stream stream);
 
 /* Read (synchronously) and clear the plan's device status word:
  * *device_status = FADAM_OK, or FADAM_ETIMEOUT when a bounded wait of the

@@ -1,0 +1,190 @@
+"""GPU parity of the data-parallel exchange stand-in (fadam_plan_set_exchange,
+fadam_grad_reduce, fadam_step_reduce) against the oracle: the reduced
+gradient shard bit for bit, the fused step element by element, the
+param-out copies in every destination, a set noop flag, the inf/nan screen
+of the reduced gradient, graph replay, the norm of the reduced shard, and the
+argument checks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from adamw_optimizer_step_persistent_gb300 import FusedAdamShard
+from adamw_optimizer_step_persistent_gb300._abi import FadamError
+from tests import helpers
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+NAMES = ["exchange_shard", "exchange_packed_sum"]
+
+
+def _make(name, capturable=True, check_finite=False):
+    spec = workloads.exchange_versions()[name]
+    shard = workloads.materialize(spec, DEV)
+    opt = FusedAdamShard(shard.param_groups(), capturable=capturable, check_finite=check_finite)
+    opt.set_exchange(shard.buckets["g"], list(shard.sources), average=spec.exchange_average,
+                     out_shard=shard.buckets["p_out"], dests=list(shard.dests))
+    return spec, shard, opt
+
+
+def _oracle_sources(shard, idx=None):
+    """Per tensor (plan order): the R ranks' contributions to its fragment."""
+    idx = shard.plan_order() if idx is None else idx
+    out = []
+    for i in idx:
+        o, n = shard.offsets[i], shard.spec.sizes[i]
+        out.append([helpers.to_np(shard.sources[r, o:o + n]) for r in range(shard.sources.shape[0])])
+    return out
+
+
+def _check_reduced(shard, osh):
+    for t, i in zip(osh.tensors, shard.plan_order()):
+        got = helpers.to_np(shard.grads[i])
+        assert got.tobytes() == t.g.tobytes(), f"tensor {i}: reduced gradient differs"
+
+
+def _check_dests(shard):
+    o = shard.buckets["p_out"]
+    for d in range(shard.dests.shape[0]):
+        assert torch.equal(shard.dests[d].view(torch.int16), o.view(torch.int16)), f"destination {d}"
+
+
+@pytest.mark.parametrize("capturable", [True, False])
+@pytest.mark.parametrize("name", NAMES)
+def test_step_reduce_matches_oracle(name, capturable):
+    spec, shard, opt = _make(name, capturable=capturable)
+    osh = helpers.oracle_shard(shard)
+    src = _oracle_sources(shard)
+    rep = helpers.Report()
+    for k in range(3):
+        opt.step_reduce()
+        oracle.exchange_step(osh, src, average=spec.exchange_average, capturable=capturable)
+        torch.cuda.synchronize()
+        _check_reduced(shard, osh)
+        helpers.compare(shard, osh, report=rep)
+        _check_dests(shard)
+        # the next step's contributions: rank r's buffer rolled by one rank
+        shard.sources.copy_(torch.roll(shard.sources, 1, dims=0))
+        src = _oracle_sources(shard)
+    assert opt.group_steps() == [3]
+    assert rep.exact_fraction == 1.0, rep.exact_fraction
+    opt.close()
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_grad_reduce_alone_touches_only_g(name):
+    spec, shard, opt = _make(name)
+    snap = helpers.snapshot(shard)
+    dests = shard.dests.clone()
+    opt.grad_reduce()
+    torch.cuda.synchronize()
+    osh = helpers.oracle_shard(shard)
+    for t, s in zip(osh.tensors, _oracle_sources(shard)):
+        t.g[...] = oracle.reduce_sources(s, oracle.DT_BF16, spec.exchange_average)
+    _check_reduced(shard, osh)
+    assert helpers.state_equal(shard, snap)
+    assert torch.equal(dests, shard.dests)
+    assert opt.group_steps() == [0]
+    opt.close()
+
+
+def test_noop_still_reduces():
+    spec, shard, opt = _make("exchange_shard")
+    snap = helpers.snapshot(shard)
+    opt.noop.fill_(1)
+    opt.step_reduce()
+    torch.cuda.synchronize()
+    osh = helpers.oracle_shard(shard)
+    assert oracle.exchange_step(osh, _oracle_sources(shard), average=True, capturable=True, noop=True)
+    _check_reduced(shard, osh)
+    assert helpers.state_equal(shard, snap)
+    assert opt.group_steps() == [0]
+    opt.close()
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_screen_of_the_reduced_gradient(name):
+    spec, shard, opt = _make(name, check_finite=True)
+    opt.step_reduce()  # finite: one step applied
+    torch.cuda.synchronize()
+    assert opt.noop.item() == 0 and opt.group_steps() == [1]
+    snap = helpers.snapshot(shard)
+    # an inf in one rank's contribution, in a fragment's tail element
+    i = shard.plan_order()[-1]
+    shard.sources[1, shard.offsets[i] + spec.sizes[i] - 1] = float("inf")
+    opt.step_reduce()
+    torch.cuda.synchronize()
+    assert opt.noop.item() == 1 and opt.group_steps() == [1]
+    assert helpers.state_equal(shard, snap)
+    assert torch.isinf(shard.grads[i][-1].float())
+    opt.close()
+
+
+def test_graph_replay_equals_eager():
+    spec, a, oa = _make("exchange_shard")
+    _, b, ob = _make("exchange_shard")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ob.step_reduce()
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ob.step_reduce()
+    for _ in range(4):
+        oa.step_reduce()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    for x, y in zip(helpers.snapshot(a), helpers.snapshot(b)):
+        assert torch.equal(x.view(torch.int8), y.view(torch.int8))
+    assert torch.equal(a.dests, b.dests) and oa.group_steps() == ob.group_steps() == [4]
+    oa.close()
+    ob.close()
+
+
+def test_norm_of_the_reduced_shard():
+    spec, shard, opt = _make("exchange_shard")
+    opt.grad_reduce()
+    got = opt.grad_norm_sq().item()
+    osh = helpers.oracle_shard(shard)
+    want = oracle.shard_sumsq(osh)
+    assert got == pytest.approx(want, rel=2e-6)
+    opt.close()
+
+
+def test_plain_step_writes_destinations():
+    spec, shard, opt = _make("exchange_packed_sum")
+    opt.step()  # no reduction: g as it stands (zeros), param-out to every destination
+    torch.cuda.synchronize()
+    _check_dests(shard)
+    assert shard.buckets["p_out"].abs().sum().item() > 0
+    opt.close()
+
+
+def test_exchange_argument_checks():
+    spec, shard, opt = _make("exchange_shard")
+    g = shard.buckets["g"]
+    with pytest.raises(ValueError):  # a source smaller than the shard
+        opt.set_exchange(g, [shard.sources[0, :10]])
+    with pytest.raises(FadamError):  # 17 sources
+        opt.set_exchange(g, [shard.sources[0]] * 17)
+    with pytest.raises(FadamError):  # a source start 2 bytes off
+        opt.set_exchange(g, [shard.sources.reshape(-1)[1:1 + g.numel()]])
+    with pytest.raises(ValueError):
+        opt.set_exchange(g, [shard.sources[0]], dests=[shard.dests[0]])  # dests without out_shard
+    opt.set_exchange(g, [])  # no exchange: the reduce entry points refuse
+    with pytest.raises(FadamError):
+        opt.grad_reduce()
+    with pytest.raises(FadamError):
+        opt.step_reduce()
+    opt.close()
+    # destinations on a plan without a param-out copy
+    lspec = workloads.large_uniform(n_tensors=1, numel=4096)
+    lsh = workloads.materialize(lspec, DEV)
+    lopt = FusedAdamShard(lsh.param_groups(), capturable=True)
+    with pytest.raises(FadamError):
+        out = torch.zeros(4096, dtype=torch.bfloat16, device=DEV)
+        lopt.set_exchange(lsh.grads[0], [], out_shard=out, dests=[out.clone()])
+    lopt.close()

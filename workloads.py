@@ -29,6 +29,15 @@ Five shard recipes, all synthetic (no dataset or checkpoint is involved):
    log-uniform size in [1, 4096) and 70% in [4096, 1,048,576], shuffled;
    group 0 AdamW wd 0.1 (the large ones), group 1 L2 wd 0 (the small ones),
    group 2 empty; per-group device step counters.
+6. ``exchange_shard``: the one-GPU stand-in for one data-parallel rank of
+   R = 8 with its exchange: the GPT-style layer list of ``capturable_l2``
+   as fragments of one gradient shard buffer and one bf16 param-out shard
+   buffer (fragment starts rounded up to 64 elements, the 128-byte rule for
+   16-bit grads), fp32 p, m, v, AdamW wd 0.1, betas (0.9, 0.95), eps 1e-8,
+   lr 1e-3 on the device; R source buffers laid out like the gradient shard
+   (each rank's bf16 gradient for this shard, ~ N(0, 1e-2)), averaged into
+   the shard, and R - 1 destination buffers laid out like the param-out
+   shard (the other ranks' places for it).
 
 Every recipe takes size arguments that shrink it for tests the oracle must
 finish in seconds (``small_versions``); the defaults are the full workloads.
@@ -74,6 +83,10 @@ class ShardSpec:
     bucket_len: int = 0
     seed: int = 0
     inf_at_step: Optional[int] = None  # step (1-based) whose grad holds one +inf
+    exchange_ranks: int = 0    # > 0: gradients and param-out as views of one shard buffer each,
+    exchange_dests: int = 0    # with this many source and destination buffers
+    exchange_average: bool = True  # ReduceOp.AVG (else SUM)
+    exchange_align: int = 64   # fragment starts rounded up to this many elements
     notes: Dict = field(default_factory=dict)
 
     @property
@@ -145,6 +158,27 @@ def many_small(n_tensors: int = 20_000, frac_small: float = 0.3, small_hi: int =
                      capturable=True, grad_std=1e-3, seed=seed)
 
 
+def exchange_shard(layers: int = 8, hidden: int = 4096, ffn: int = 11008, ranks: int = 8,
+                   dests: Optional[int] = None, seed: int = 1240) -> ShardSpec:
+    per_layer = [hidden * hidden, hidden * ffn, hidden * ffn, ffn * hidden, hidden, hidden]
+    sizes = per_layer * layers
+    g = GroupSpec(adam_w_mode=True, lr=1e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1)
+    return ShardSpec("exchange_shard", [g], sizes, [0] * len(sizes), g_dtype=torch.bfloat16,
+                     out_dtype=torch.bfloat16, capturable=True, grad_std=1e-2, seed=seed,
+                     exchange_ranks=ranks, exchange_dests=ranks - 1 if dests is None else dests)
+
+
+def exchange_offsets(sizes: List[int], align: int = 64) -> List[int]:
+    """Fragment starts in the shard buffer, each rounded up to `align`
+    elements."""
+    out, o = [], 0
+    for n in sizes:
+        o = (o + align - 1) // align * align
+        out.append(o)
+        o += n
+    return out
+
+
 def small_versions() -> Dict[str, ShardSpec]:
     """The same recipes at sizes the oracle finishes in seconds (several
     CTAs' worth of work each, ragged tails included)."""
@@ -155,6 +189,19 @@ def small_versions() -> Dict[str, ShardSpec]:
         "remainder_shard": remainder_shard(total=3_000_000, n_views=64, lo=64, hi=200_000),
         "many_small": many_small(n_tensors=2000, large_hi=65536),
     }
+
+
+def exchange_versions(full: bool = False) -> Dict[str, ShardSpec]:
+    """The exchange recipe: small (three ranks, a non-power-of-two average,
+    ragged fragments) or at full size."""
+    if full:
+        return {"exchange_shard": exchange_shard()}
+    # the second one sums, and packs its fragments with no alignment
+    # padding (odd starts, ragged tails: the element-wise paths)
+    packed = exchange_shard(layers=1, hidden=300, ffn=1001, ranks=5, dests=2)
+    packed.name, packed.exchange_average, packed.exchange_align = "exchange_packed_sum", False, 1
+    return {"exchange_shard": exchange_shard(layers=2, hidden=256, ffn=688, ranks=3),
+            "exchange_packed_sum": packed}
 
 
 def full_versions() -> Dict[str, ShardSpec]:
@@ -178,6 +225,11 @@ class Shard:
     params_out: List[Optional[torch.Tensor]]
     remainders: List[Optional[torch.Tensor]]
     buckets: Dict[str, torch.Tensor] = field(default_factory=dict)
+    # exchange recipes: [R, L] sources laid out like buckets["g"], [D, L]
+    # destinations laid out like buckets["p_out"], fragment starts
+    sources: Optional[torch.Tensor] = None
+    dests: Optional[torch.Tensor] = None
+    offsets: Optional[List[int]] = None
 
     def param_groups(self) -> List[Dict]:
         """The per-group dicts FusedAdamShard takes."""
@@ -216,6 +268,12 @@ def materialize(spec: ShardSpec, device="cuda") -> Shard:
     n = len(spec.sizes)
     params, ms, vs, gs, outs, rems = [], [], [], [], [], []
     buckets: Dict[str, torch.Tensor] = {}
+    xoff = None
+    if spec.exchange_ranks > 0:
+        xoff = exchange_offsets(spec.sizes, spec.exchange_align)
+        L = (xoff[-1] + spec.sizes[-1]) if spec.sizes else 0
+        buckets["g"] = torch.zeros(L, dtype=spec.g_dtype, device=dev)
+        buckets["p_out"] = torch.zeros(L, dtype=spec.out_dtype, device=dev)
     if spec.bucket_offsets is not None:
         L = spec.bucket_len
         buckets["p"] = torch.zeros(L, dtype=torch.bfloat16, device=dev)
@@ -239,6 +297,8 @@ def materialize(spec: ShardSpec, device="cuda") -> Shard:
             m = torch.zeros(s, dtype=sdt, device=dev)
             v = torch.zeros(s, dtype=sdt, device=dev)
             g = torch.empty(s, dtype=spec.g_dtype, device=dev)
+            if xoff is not None:
+                g = buckets["g"][xoff[i]:xoff[i] + s]
         if spec.remainders:
             hi = torch.randn(s, generator=gen, device=dev).to(torch.bfloat16)
             # a zero high half with a negative remainder is the split of no
@@ -257,11 +317,24 @@ def materialize(spec: ShardSpec, device="cuda") -> Shard:
         rems.append(r)
         if spec.remainders:
             outs.append(p)  # the new high half replaces the bf16 param in place
+        elif xoff is not None:
+            outs.append(buckets["p_out"][xoff[i]:xoff[i] + s])
         elif spec.out_dtype is not None:
             outs.append(torch.zeros(s, dtype=spec.out_dtype, device=dev))
         else:
             outs.append(None)
-    return Shard(spec, params, ms, vs, gs, outs, rems, buckets)
+    sources = dests = None
+    if xoff is not None:
+        # rows padded to 64 elements, so every row starts 128-byte aligned
+        L = buckets["g"].numel()
+        Lp = (L + 63) // 64 * 64
+        sources = torch.empty(spec.exchange_ranks, Lp, dtype=spec.g_dtype, device=dev)
+        for r in range(spec.exchange_ranks):
+            sources[r].copy_((torch.randn(Lp, generator=gen, device=dev) * spec.grad_std)
+                             .to(spec.g_dtype))
+        sources = sources[:, :L]
+        dests = torch.zeros(spec.exchange_dests, Lp, dtype=spec.out_dtype, device=dev)[:, :L]
+    return Shard(spec, params, ms, vs, gs, outs, rems, buckets, sources, dests, xoff)
 
 
 def inf_position(spec: ShardSpec) -> tuple:
