@@ -112,7 +112,7 @@ struct alignas(16) KParams {
   int32_t n_sources;
   int32_t average;
   int32_t n_dests;
-  int32_t reserved2;
+  float avg_mul;  // 1/R when averaging over a power-of-two R (exact), else 0
   int64_t src_delta[FADAM_MAX_SOURCES];
   int64_t dst_delta[FADAM_MAX_DESTS];
   KGroup groups[FADAM_MAX_GROUPS];

@@ -315,8 +315,10 @@ struct Layout {
   static constexpr int off_v = off_m + kMV * update_vectors;
   static constexpr int off_g = off_v + kMV * update_vectors;
   static constexpr unsigned update_tile = per_vector * update_vectors;
-  // the screen copies only g, four vectors per thread
-  static constexpr int scan_vectors = 4 * kTile;
+  // the g-only passes (screen, norm) fill the same stage with g: at least
+  // four vectors per thread, more for 16-bit grads
+  static constexpr int scan_per_thread = update_tile / kG / kTile > 4 ? update_tile / kG / kTile : 4;
+  static constexpr int scan_vectors = scan_per_thread * kTile;
   static constexpr unsigned scan_tile = scan_vectors * kG;
   static constexpr unsigned stage = update_tile > scan_tile ? update_tile : scan_tile;
 };
@@ -397,12 +399,12 @@ __device__ __forceinline__ int bulk_tiles(const Item& it) {
 enum class Pass { kUpdate, kScan, kNorm, kReduce };
 
 // Vectors of a reduce tile: as many as the R source slices fit in one stage
-// (at most the screen's 4 per thread), a multiple of one warp.
+// (at most as many as a screen tile), a multiple of one warp.
 template <int ST, int GT, bool REM>
 __host__ __device__ constexpr int reduce_vectors(int n_sources) {
   using L = Layout<ST, GT, REM>;
   const int v = static_cast<int>(L::stage / (static_cast<unsigned>(n_sources) * L::kG));
-  return (v < 4 * kTile ? v : 4 * kTile) & ~31;
+  return (v < L::scan_vectors ? v : L::scan_vectors) & ~31;
 }
 
 // Vectors in one tile of a pass (Layout::update_vectors or ::scan_vectors).
@@ -448,11 +450,18 @@ __device__ __forceinline__ void issue_tile(const KParams& kp, const Item& it, in
 // and copies their tiles kStages ahead of the consumers, announcing each
 // tile's (item, tile) in a small shared ring before its copies start.  When
 // the chunks run out it announces the end with an arrival that carries no
-// bytes.
+// bytes.  The g-only passes take chunks in batches of consecutive indices,
+// up to kBatchMax while much work remains and down to one near the end (so
+// the CTAs still finish together); a batch's chunk records arrive in one
+// round trip.
+constexpr int kBatchMax = 8;
+
 struct Producer {
   Item it;
-  int item, v, vend;  // vectors [v, vend) of the current chunk remain
+  Chunk recs[kBatchMax];  // the current batch's chunk records
+  int item, v, vend;      // vectors [v, vend) of the current chunk remain
   int chunk;
+  int next, batch0, batch_end;  // chunks [next, batch_end) of the batch remain
   unsigned slot;
   bool finished;
 };
@@ -468,13 +477,34 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// Thread 0: take the next batch of chunks, or return false when none is left.
+__device__ __forceinline__ bool next_batch(Producer& pr, const KParams& kp, unsigned* counter,
+                                           int kmax) {
+  const int remaining = kp.n_chunks - pr.batch_end;  // as this CTA last saw it
+  const int k = max(1, min(kmax, remaining / (2 * static_cast<int>(gridDim.x))));
+  const unsigned c0 = atomicAdd(counter, static_cast<unsigned>(k));
+  if (c0 >= static_cast<unsigned>(kp.n_chunks)) return false;
+  const int cnt = min(k, kp.n_chunks - static_cast<int>(c0));
+  for (int j = 0; j < cnt; ++j)  // independent 16-byte copies, one wait
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(smem_addr(&pr.recs[j])),
+                 "l"(kp.chunks + c0 + j)
+                 : "memory");
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  pr.next = static_cast<int>(c0);
+  pr.batch0 = static_cast<int>(c0);
+  pr.batch_end = static_cast<int>(c0) + cnt;
+  return true;
+}
+
 template <int ST, int GT, bool REM, Pass PASS>
 __device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, unsigned* counter,
                                              unsigned char* smem, uint64_t* full, TileTag* tags) {
   if (pr.finished) return;
   while (pr.v >= pr.vend) {
-    const unsigned c = atomicAdd(counter, 1u);
-    if (c >= static_cast<unsigned>(kp.n_chunks)) {
+    // the update's chunks are long (16 tiles): one at a time keeps the
+    // CTAs on neighbouring chunks; the g-only passes' chunks are 2-4 tiles
+    if (pr.next >= pr.batch_end &&
+        !next_batch(pr, kp, counter, PASS == Pass::kUpdate ? 1 : kBatchMax)) {
       const unsigned b = pr.slot % kStages;
       tags[b] = TileTag{-1, 0, 0, -1};
       mbar_arrive(full + b);  // completes the phase with no copy
@@ -482,8 +512,8 @@ __device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, un
       pr.finished = true;
       return;
     }
-    const Chunk ch = kp.chunks[c];
-    pr.chunk = static_cast<int>(c);
+    const Chunk ch = pr.recs[pr.next - pr.batch0];
+    pr.chunk = pr.next++;
     if (ch.item != pr.item) {
       pr.item = ch.item;
       pr.it = load_item(kp.items, ch.item);
@@ -569,8 +599,15 @@ __device__ __forceinline__ bool reduce_tile(const KParams& kp, const Item& it,
       for (int e = 0; e < 4; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
     }
     if (kp.average) {
+      // dividing by a power of two is multiplying by its exact reciprocal
+      // (the same correctly rounded result)
+      if (kp.avg_mul != 0.0f) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[e] = __fdiv_rn(acc[e], rn);
+        for (int e = 0; e < 4; ++e) acc[e] = __fmul_rn(acc[e], kp.avg_mul);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] = __fdiv_rn(acc[e], rn);
+      }
     }
     const G4 w = pack_out4<GT>(acc);
     __stcs(reinterpret_cast<G4*>(const_cast<void*>(it.g)) + v0 + t, w);
@@ -591,16 +628,18 @@ __device__ __forceinline__ bool reduce_elem(const KParams& kp, const Item& it, i
   const char* g = static_cast<const char*>(it.g);
   float acc = load1<GT>(g + kp.src_delta[0], i);
   for (int r = 1; r < kp.n_sources; ++r) acc = __fadd_rn(acc, load1<GT>(g + kp.src_delta[r], i));
-  if (kp.average) acc = __fdiv_rn(acc, static_cast<float>(kp.n_sources));
+  if (kp.average)
+    acc = kp.avg_mul != 0.0f ? __fmul_rn(acc, kp.avg_mul)
+                             : __fdiv_rn(acc, static_cast<float>(kp.n_sources));
   store_out1<GT>(const_cast<void*>(it.g), i, acc);
   return screen && !isfinite(__fmul_rn(stored_value<GT>(acc), gs));
 }
 
-template <int GT>
+template <int Q, int GT>
 __device__ __forceinline__ bool scan_tile(const unsigned char* st, int len, float gs) {
   bool bad = false;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {  // Layout::scan_vectors = 4 * kTile
+  for (int q = 0; q < Q; ++q) {  // Q = Layout::scan_per_thread
     const int t = threadIdx.x + q * kTile;
     if (t < len) {
       float g[4];
@@ -632,10 +671,10 @@ struct SqPart {
 // The rare case, kept out of line so that no double arithmetic sits in the
 // streaming loop: the thread's vectors of one tile again, the in-range ones
 // summed in float as before and the others squared exactly in double.
-template <int GT>
+template <int Q, int GT>
 __device__ __noinline__ SqPart square_tile_exact(const unsigned char* st, int len) {
   SqPart r{0.0f, 0.0};
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < Q; ++q) {
     const int t = threadIdx.x + q * kTile;
     if (t < len) {
       float g[4];
@@ -752,7 +791,7 @@ __device__ __forceinline__ void norm_publish(const double* red_buf, float gs, do
 
 // Every thread of the CTA calls this for the same tile (the warp-level
 // close needs whole warps).  A chunk that ends here becomes `pend`.
-template <int GT>
+template <int Q, int GT>
 __device__ __forceinline__ void norm_tile(const unsigned char* st, const TileTag& tag, int group,
                                           NormAcc& na, const SGroup* sgrp, double* red,
                                           double* dpart, unsigned& closes, NormPending& pend) {
@@ -772,7 +811,7 @@ __device__ __forceinline__ void norm_tile(const unsigned char* st, const TileTag
   float f = 0.0f;
   unsigned nz = 0u;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {  // Layout::scan_vectors = 4 * kTile
+  for (int q = 0; q < Q; ++q) {  // Q = Layout::scan_per_thread
     const int t = threadIdx.x + q * kTile;
     if (t < tag.len) {
       float g[4];
@@ -786,7 +825,7 @@ __device__ __forceinline__ void norm_tile(const unsigned char* st, const TileTag
   const bool special = !(f <= 1e30f) || (f < 1e-30f && (nz & 0x7fffffffu) != 0u);
   double d = 0.0;
   if (special) {
-    const SqPart r = square_tile_exact<GT>(st, tag.len);
+    const SqPart r = square_tile_exact<Q, GT>(st, tag.len);
     f = r.f;
     d = r.d;
   }
@@ -820,6 +859,7 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
     pr.vend = 0;
     pr.slot = stage;
     pr.finished = false;
+    pr.next = pr.batch0 = pr.batch_end = 0;
     for (int q = 0; q < kStages; ++q) produce_next<ST, GT, REM, PASS>(pr, kp, counter, smem, full, tags);
   }
   int cur_item = -1;
@@ -841,9 +881,10 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
         const SGroup& G = sgrp[it.group];
         const Scal s{G.beta1, G.omb1, G.beta2, G.omb2, G.bc1, G.bc2, G.eps, G.wd, G.lr, G.gs};
         if constexpr (PASS == Pass::kScan) {
-          bad |= scan_tile<GT>(st, tag.len, s.gs);
+          bad |= scan_tile<Layout<ST, GT, REM>::scan_per_thread, GT>(st, tag.len, s.gs);
         } else if constexpr (PASS == Pass::kNorm) {
-          norm_tile<GT>(st, tag, it.group, na, sgrp, red, dpart, closes, pend);
+          norm_tile<Layout<ST, GT, REM>::scan_per_thread, GT>(st, tag, it.group, na, sgrp, red,
+                                                              dpart, closes, pend);
         } else if constexpr (PASS == Pass::kReduce) {
           bad |= reduce_tile<ST, GT, REM>(kp, it, st, tag.v0, tag.len, s.gs, screen);
         } else {

@@ -530,6 +530,8 @@ void fill_exchange(KParams& kp, const fadam_plan* plan) {
   kp.n_sources = plan->n_sources;
   kp.average = plan->average;
   kp.n_dests = plan->n_dests;
+  const int r_n = plan->n_sources;
+  kp.avg_mul = (plan->average && r_n > 0 && (r_n & (r_n - 1)) == 0) ? 1.0f / static_cast<float>(r_n) : 0.0f;
   for (int r = 0; r < plan->n_sources; ++r) kp.src_delta[r] = plan->src_delta[r];
   for (int d = 0; d < plan->n_dests; ++d) kp.dst_delta[d] = plan->dst_delta[d];
 }

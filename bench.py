@@ -311,6 +311,9 @@ def run_gpu(args):
         spec = workloads.large_uniform(n_tensors=args.n_tensors, numel=args.numel,
                                        seed=1237 + 1000 * rank, state_dtype=torch.bfloat16,
                                        g_dtype=torch.bfloat16)
+    elif args.workload == "exchange_shard":
+        spec = workloads.exchange_versions(full=True)["exchange_shard"]
+        spec.seed += 1000 * rank
     elif args.workload == "many_small" and args.n_tensors:
         spec = workloads.many_small(n_tensors=args.n_tensors, seed=1239 + 1000 * rank)
     else:
@@ -319,19 +322,45 @@ def run_gpu(args):
     shard = workloads.materialize(spec, device)
     groups = shard.param_groups()
     kw = dict(remainders=spec.remainders, grad_scale=spec.grad_scale)
-    cap = FusedAdamShard(groups, capturable=True, **kw)
+
+    def make(capturable, **more):
+        opt = FusedAdamShard(groups, capturable=capturable, **kw, **more)
+        if spec.exchange_ranks:  # the data-parallel exchange stand-in
+            opt.set_exchange(shard.buckets["g"], list(shard.sources),
+                             average=spec.exchange_average, out_shard=shard.buckets["p_out"],
+                             dests=list(shard.dests))
+        return opt
+
+    cap = make(True)
     info = cap.info()
     bytes_step = info["bytes_per_step"]
     elems = info["n_elements"]
+    if spec.exchange_ranks:
+        gsz = shard.buckets["g"].element_size()
+        # every step also writes the param-out copy to each destination
+        bytes_step += elems * spec.exchange_dests * shard.buckets["p_out"].element_size()
+        # fused: the R sources are read and the shard's g written, instead of g read
+        exchange_bytes = bytes_step + elems * spec.exchange_ranks * gsz
+        reduce_bytes = elems * (spec.exchange_ranks + 1) * gsz
     res = {}
     variants = args.variants.split(",")
     sampler = ClockSampler(local)
     sampler.start()
+    if spec.exchange_ranks and "exchange" in variants:
+        per, _ = time_launches(cap.step_reduce, args.steps, args.warmup, world)
+        r = summarise(per, exchange_bytes, elems, world, device)
+        r["bytes_per_step"] = exchange_bytes
+        res["exchange"] = r
+    if spec.exchange_ranks and "reduce" in variants:
+        per, _ = time_launches(cap.grad_reduce, args.steps, args.warmup, world)
+        r = summarise(per, reduce_bytes, elems, world, device)
+        r["bytes_per_step"] = reduce_bytes
+        res["reduce"] = r
     if "capturable" in variants:
         per, _ = time_launches(cap.step, args.steps, args.warmup, world)
         res["capturable"] = summarise(per, bytes_step, elems, world, device)
     if "regular" in variants:
-        reg = FusedAdamShard(groups, capturable=False, **kw)
+        reg = make(False)
         per, _ = time_launches(reg.step, args.steps, args.warmup, world)
         res["regular"] = summarise(per, bytes_step, elems, world, device)
         reg.close()
@@ -348,7 +377,7 @@ def run_gpu(args):
         res["graph_replay"] = summarise(per, bytes_step, elems, world, device)
         del graph
     if "check_finite" in variants:
-        chk = FusedAdamShard(groups, capturable=True, check_finite=True, **kw)
+        chk = make(True, check_finite=True)
         per, _ = time_launches(chk.step, args.steps, args.warmup, world)
         r = summarise(per, bytes_step, elems, world, device)
         r["gbs_including_screen"] = r["gbs"] * (bytes_step + chk.info()["check_bytes_per_step"]) / bytes_step
@@ -381,9 +410,11 @@ def run_gpu(args):
                        "step counter -> host, stream sync"}
         del host
 
-    head = res.get("capturable") or res.get("regular") or next(iter(res.values()))
+    head = (res.get("exchange") or res.get("capturable") or res.get("regular")
+            or next(iter(res.values())))
+    head_bytes = head.get("bytes_per_step", bytes_step)
     peaks = measured_peaks()
-    achieved = bytes_step / (head["ms_per_step"] / 1e3) / 1e9
+    achieved = head_bytes / (head["ms_per_step"] / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": head["gbs"], "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
@@ -392,9 +423,12 @@ def run_gpu(args):
         "config": {"workload": (f"large_uniform: {args.n_tensors or 201} fp32 tensors x {args.numel}, "
                                 "AdamW lr 1.6e-3 betas (0.9,0.95) eps 1e-8 wd 0.1, no param-out"
                                 if args.workload == "large_uniform" else
-                                f"{spec.name}: {len(spec.sizes)} tensors, {spec.n_elements} elements"),
-                   "elements_per_step": elems, "bytes_per_step": bytes_step,
-                   "bytes_per_element": bytes_step / elems, "grid": info["grid"],
+                                f"{spec.name}: {len(spec.sizes)} tensors, {spec.n_elements} elements"
+                                + (f", fp32 state, bf16 g and param-out, {spec.exchange_ranks} ranks "
+                                   f"averaged into the shard, {spec.exchange_dests} destinations"
+                                   if spec.exchange_ranks else "")),
+                   "elements_per_step": elems, "bytes_per_step": head_bytes,
+                   "bytes_per_element": head_bytes / elems, "grid": info["grid"],
                    "block": info["block"], "items": info["n_items"],
                    "l2": "inputs larger than L2 (no flush needed)",
                    "parallelism": f"weak: one shard per GPU x {world}"},
@@ -431,11 +465,12 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="large_uniform",
                     choices=["large_uniform", "capturable_l2", "remainder_shard", "many_small",
-                             "large_uniform_bf16_state"])
+                             "large_uniform_bf16_state", "exchange_shard"])
     ap.add_argument("--n-tensors", type=int, default=None,
                     help="tensor count of large_uniform[_bf16_state] (201) or many_small (20000)")
     ap.add_argument("--numel", type=int, default=320 * 65536)
-    ap.add_argument("--variants", default="capturable,regular,graph,check_finite,norm,e2e")
+    ap.add_argument("--variants", default="capturable,regular,graph,check_finite,norm,e2e",
+                    help="also exchange,reduce on the exchange_shard workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tensors", type=int, default=4)
     args = ap.parse_args(argv)

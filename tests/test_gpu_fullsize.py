@@ -127,3 +127,38 @@ def test_large_uniform_norm_full_size():
     opt.close()
     del shard, opt
     _free()
+
+
+def test_exchange_shard_full_size():
+    """Eight ranks' bf16 gradients averaged into the 1.2e9-element shard and
+    stepped in one launch, param-out to the seven other ranks' places, for
+    two steps; sampled elements against the oracle (the reduced gradient
+    bit for bit), destinations byte-equal over the whole shard."""
+    spec = workloads.exchange_versions(full=True)["exchange_shard"]
+    shard = workloads.materialize(spec, DEV)
+    opt = FusedAdamShard(shard.param_groups(), capturable=True)
+    opt.set_exchange(shard.buckets["g"], list(shard.sources), average=True,
+                     out_shard=shard.buckets["p_out"], dests=list(shard.dests))
+    order = shard.plan_order()
+    elems = helpers.sample_elements(spec, 4096, seed=spec.seed + 5)
+    osh = helpers.oracle_shard(shard, elems=elems)
+    src = []
+    for i in order:
+        e = torch.as_tensor(elems[i], device=DEV) + shard.offsets[i]
+        src.append([helpers.to_np(shard.sources[r][e]) for r in range(spec.exchange_ranks)])
+    for _ in range(2):
+        opt.step_reduce()
+        oracle.exchange_step(osh, src, average=True, capturable=True)
+    torch.cuda.synchronize()
+    for t, i in zip(osh.tensors, order):
+        got = helpers.to_np(shard.grads[i][torch.as_tensor(elems[i], device=DEV)])
+        assert got.tobytes() == t.g.tobytes(), f"tensor {i}: reduced gradient differs"
+    rep = helpers.compare(shard, osh, elems=elems)
+    assert rep.exact_fraction == 1.0
+    out = shard.buckets["p_out"].view(torch.int16)
+    for d in range(spec.exchange_dests):
+        assert torch.equal(shard.dests[d].view(torch.int16), out), f"destination {d}"
+    assert opt.group_steps() == [2]
+    opt.close()
+    del shard, opt
+    _free()
