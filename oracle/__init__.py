@@ -251,6 +251,7 @@ class Tensor:
     p_out: Optional[np.ndarray] = None
     out_dtype: int = DT_NONE
     state_dtype: int = DT_F32  # dtype of p, m and v (fp32 master form)
+    scales: Optional[np.ndarray] = None  # scaled 16-bit state: float32[3] (p, m, v)
 
 
 @dataclass
@@ -295,6 +296,9 @@ def shard_step(shard: Shard, *, capturable: bool, noop: bool = False,
         step = shard.steps[shard.step_slot[t.group]]
         if t.rem is not None:
             adam_rem(grp, step, t.p_hi, t.rem, t.m, t.v, t.g, t.g_dtype, t.p_out)
+        elif t.scales is not None:
+            adam_scaled(grp, step, t.p, t.m, t.v, t.scales, t.state_dtype, t.g, t.g_dtype,
+                        t.p_out, t.out_dtype)
         elif t.state_dtype != DT_F32:
             adam_state(grp, step, t.p, t.m, t.v, t.state_dtype, t.g, t.g_dtype, t.p_out,
                        t.out_dtype)
@@ -413,3 +417,65 @@ def gather_param_out(p_out_shard, n_ranks: int, rank: int) -> np.ndarray:
     out = np.zeros(shard.size * n_ranks, dtype=shard.dtype)
     out[rank * shard.size:(rank + 1) * shard.size] = shard
     return out
+
+
+# ---- scaled optimizer state -----------------------------------------------------
+#
+# "apex/contrib/optimizers/distributed_fused_adam.py": _local_step_with_scaled_states
+# (per fragment: the fp16/bf16 param, exp_avg and exp_avg_sq are copied to
+# fp32 and multiplied by their scales, the Adam step runs on the fp32
+# buffers with the param buffer as its own param-out, the param-out of the
+# param sync dtype is the cast of the new fp32 param, then every buffer is
+# rescaled and copied back) and _apply_state_scale (absmax = max(-min, max)
+# of the buffer; scale = absmax / (finfo(dtype).max / 2); rscale = 1 / scale
+# where scale > 0, else 0; buffer *= rscale).  Readings: every product,
+# quotient and reciprocal is one IEEE float operation; absmax is the largest
+# magnitude as a float (+0 when every value is a zero of either sign; NaN
+# when any value is NaN, as aminmax propagates it); the copies to the state
+# dtype round to nearest even; empty tensors are skipped (the page skips
+# fragments with no local elements).
+
+def max_scaled_state(state_dtype: int) -> np.float32:
+    """finfo(dtype).max / 2 for the 16-bit state dtype, as a float."""
+    if state_dtype == DT_BF16:
+        return np.float32(bf16_to_f32(np.array([0x7F7F], np.uint16))[0]) / np.float32(2)
+    if state_dtype == DT_F16:
+        return np.float32(65504.0) / np.float32(2)
+    raise ValueError("scaled states need a 16-bit state dtype")
+
+
+def state_scale(buf, state_dtype: int):
+    """(scale, rscale) of an fp32 buffer, as _apply_state_scale computes them."""
+    with np.errstate(invalid="ignore", over="ignore", divide="ignore"):
+        a = np.abs(np.asarray(buf, np.float32))
+        absmax = np.float32(np.max(a)) if a.size else np.float32(0)  # NaN propagates
+        scale = absmax / max_scaled_state(state_dtype)
+        rscale = np.float32(1) / scale if scale > 0 else np.float32(0)
+    return np.float32(scale), np.float32(rscale)
+
+
+def adam_scaled(group: Group, step: int, p16, m16, v16, scales, state_dtype: int, g,
+                g_dtype=DT_F32, p_out=None, out_dtype=DT_NONE) -> None:
+    """One step of a tensor in scaled 16-bit state.  ``p16, m16, v16``: uint16
+    bits of the state dtype, updated in place; ``scales``: float32[3] (param,
+    exp_avg, exp_avg_sq), updated in place."""
+    if np.asarray(p16).size == 0:
+        return
+    with np.errstate(invalid="ignore", over="ignore"):
+        bufs = [_widen(x, state_dtype) * np.float32(s) for x, s in zip((p16, m16, v16), scales)]
+    p, m, v = (np.ascontiguousarray(b, np.float32) for b in bufs)
+    adam_f32(group, step, p, m, v, g, g_dtype, p_out, out_dtype)
+    for k, (buf, dst) in enumerate(((p, p16), (m, m16), (v, v16))):
+        scale, rscale = state_scale(buf, state_dtype)
+        with np.errstate(invalid="ignore", over="ignore"):
+            dst[...] = _narrow(buf * rscale, state_dtype)
+        scales[k] = scale
+
+
+def scale_state(x, state_dtype: int):
+    """A new scaled state from fp32 values (how the page stores the params
+    at construction): (16-bit bits, scale)."""
+    buf = np.asarray(x, np.float32)
+    scale, rscale = state_scale(buf, state_dtype)
+    with np.errstate(invalid="ignore", over="ignore"):
+        return _narrow(buf * rscale, state_dtype), scale
