@@ -20,6 +20,7 @@ MODE_L2, MODE_ADAMW = 0, 1
 DT_NONE, DT_F32, DT_BF16, DT_F16 = 0, 1, 2, 3
 # plan flags
 CAPTURABLE, REMAINDERS, CHECK_FINITE, STEP_PREADVANCED = 1, 2, 4, 8
+SCALED_STATES = 16
 TEST_BARRIER_TIMEOUT = 0x80000000  # diagnostic: the screen's grid barrier runs out
 MAX_GROUPS = 32
 MAX_SOURCES = 16
@@ -85,6 +86,7 @@ SIGNATURES = [
                                        ctypes.POINTER(_vp), _i32]),
     ("fadam_grad_reduce", _i32, [_vp, _vp]),
     ("fadam_step_reduce", _i32, [_vp, _vp, _vp]),
+    ("fadam_plan_set_state_scales", _i32, [_vp, _vp]),
     ("fadam_status_string", ctypes.c_char_p, [_i32]),
     ("fadam_last_error", ctypes.c_char_p, []),
     ("fadam_version", _i32, []),

@@ -41,6 +41,7 @@ struct alignas(16) Item {
   int32_t n;        // elements in the run
   uint16_t group;   // param group
   uint16_t flags;   // kItemVec, kItemBulk
+  int32_t tensor;   // index of the tensor the run belongs to
 };
 static_assert(sizeof(Item) == 64, "Item is one 64-byte record");
 
@@ -80,6 +81,8 @@ struct KScratch {
   unsigned int next_scan;    // next chunk of the inf/nan screen's bulk pass
   unsigned int next_tail_update;  // next item whose tail the update takes
   unsigned int next_tail_scan;    // next item whose tail the screen takes
+  unsigned int next_rescale;      // scaled state: next chunk of the rescale pass
+  unsigned int next_tail_rescale; // ... and next item whose tail it takes
 };
 
 // Kernel flags.
@@ -87,6 +90,7 @@ constexpr uint32_t kCapturable = FADAM_CAPTURABLE;
 constexpr uint32_t kCheckFinite = FADAM_CHECK_FINITE;
 constexpr uint32_t kPreadvanced = FADAM_STEP_PREADVANCED;
 constexpr uint32_t kTestBarrierTimeout = FADAM_TEST_BARRIER_TIMEOUT;
+constexpr uint32_t kScaledStates = FADAM_SCALED_STATES;
 // Launch-only flags (never plan flags): compute the squared gradient norm
 // instead of the update; write the gradient shard from the exchange sources
 // (alone, or before the update with a grid barrier between).
@@ -115,6 +119,13 @@ struct alignas(16) KParams {
   float avg_mul;  // 1/R when averaging over a power-of-two R (exact), else 0
   int64_t src_delta[FADAM_MAX_SOURCES];
   int64_t dst_delta[FADAM_MAX_DESTS];
+  // scaled state: 3 scales per tensor (p, m, v), the new-value absmax of
+  // each (1 + largest |x| bit pattern; 0 = no element seen), and the scale
+  // target (half the state dtype's largest finite value)
+  float* scales;
+  unsigned* absmax;
+  int32_t n_tensors;
+  float max_scaled;
   KGroup groups[FADAM_MAX_GROUPS];
 };
 
@@ -138,5 +149,16 @@ FADAM_DECLARE_KERNELS(f16, f32)
 FADAM_DECLARE_KERNELS(f16, bf16)
 FADAM_DECLARE_KERNELS(f16, f16)
 #undef FADAM_DECLARE_KERNELS
+
+// Scaled 16-bit state instances (state dtype bf16 or fp16), one function per
+// (state, g) pair, each in fadam_kernels_scaled_s<state>_g<g>.cu.
+#define FADAM_DECLARE_SCALED(S, G) KernelEntry scaled_kernel_s##S##_g##G(int out_dtype);
+FADAM_DECLARE_SCALED(bf16, f32)
+FADAM_DECLARE_SCALED(bf16, bf16)
+FADAM_DECLARE_SCALED(bf16, f16)
+FADAM_DECLARE_SCALED(f16, f32)
+FADAM_DECLARE_SCALED(f16, bf16)
+FADAM_DECLARE_SCALED(f16, f16)
+#undef FADAM_DECLARE_SCALED
 
 }  // namespace fadam

@@ -202,6 +202,30 @@ __device__ __forceinline__ uint2 pack4(const unsigned short (&h)[4]) {
   return make_uint2(h[0] | (static_cast<unsigned>(h[1]) << 16), h[2] | (static_cast<unsigned>(h[3]) << 16));
 }
 
+// What a pipeline pass moves through shared memory.
+// kScan: only g, for the inf/nan screen; kNorm: only g, for the squared norm;
+// kReduce: the exchange sources' slices of g, reduced into the shard's g;
+// kScaledA / kScaledB: the two update passes of a scaled 16-bit state (A
+// writes param-out and takes each tensor's absmax of the new values, B
+// stores the rescaled state).
+enum class Pass { kUpdate, kScan, kNorm, kReduce, kScaledA, kScaledB };
+
+__host__ __device__ constexpr bool update_like(Pass p) {
+  return p == Pass::kUpdate || p == Pass::kScaledA || p == Pass::kScaledB;
+}
+
+// A scaled tensor's factors for one pass: the stored scales of p, m, v
+// (to unscale) and, in the rescale pass, the reciprocals of the new ones.
+struct StateScale {
+  float s[3];
+  float r[3];
+};
+
+// Scaled state, absmax slots: 1 + the largest |x| bit pattern seen (NaN's
+// patterns sort above inf's, so a NaN wins as it does in a min/max scan;
+// 0 means no element seen).
+__device__ __forceinline__ unsigned abs_bits(float x) { return __float_as_uint(x) & 0x7fffffffu; }
+
 // ---- the update of one element ---------------------------------------------
 
 // p' for the fp32 master x; m and v are updated in place.
@@ -239,23 +263,67 @@ __device__ __forceinline__ void rem_split(float x, unsigned short& hi, unsigned 
 
 // One 4-element vector whose p, m, v have dtype ST, in registers: widened
 // to float, updated, rounded back to ST (nearest-even) when stored.
-template <bool ADAMW, int ST, int GT, int OT>
+// Scaled state (PASS kScaledA / kScaledB): the widened values are first
+// multiplied by the tensor's scales; pass A then writes only param-out and
+// folds |p'|, |m'|, |v'| into the thread's maxima `mx` (bit patterns), pass
+// B only the state, each new value times its new reciprocal scale.
+template <bool ADAMW, int ST, int GT, int OT, Pass PASS = Pass::kUpdate>
 __device__ __forceinline__ void update4_state(const typename Raw4<ST>::T& P,
                                               const typename Raw4<ST>::T& M,
                                               const typename Raw4<ST>::T& V,
                                               const typename Raw4<GT>::T& G, const Scal& s, void* p,
-                                              void* m, void* v, void* out, int i, const Dests& d) {
+                                              void* m, void* v, void* out, int i, const Dests& d,
+                                              const StateScale* sc = nullptr,
+                                              unsigned* mx = nullptr) {
   float g[4], x[4], mm[4], vv[4];
   widen4<GT>(G, g);
   widen4<ST>(P, x);
   widen4<ST>(M, mm);
   widen4<ST>(V, vv);
+  if constexpr (PASS == Pass::kScaledA || PASS == Pass::kScaledB) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[e] = __fmul_rn(x[e], sc->s[0]);
+      mm[e] = __fmul_rn(mm[e], sc->s[1]);
+      vv[e] = __fmul_rn(vv[e], sc->s[2]);
+    }
+  }
 #pragma unroll
   for (int e = 0; e < 4; ++e) x[e] = adam_elem<ADAMW>(x[e], mm[e], vv[e], g[e], s);
-  store_out4<ST>(p, i, x);
-  store_out4<ST>(m, i, mm);
-  store_out4<ST>(v, i, vv);
-  store_out4<OT>(out, i, x, &d);
+  if constexpr (PASS == Pass::kScaledA) {
+    store_out4<OT>(out, i, x, &d);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      mx[0] = max(mx[0], abs_bits(x[e]));
+      mx[1] = max(mx[1], abs_bits(mm[e]));
+      mx[2] = max(mx[2], abs_bits(vv[e]));
+    }
+  } else if constexpr (PASS == Pass::kScaledB) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[e] = __fmul_rn(x[e], sc->r[0]);
+      mm[e] = __fmul_rn(mm[e], sc->r[1]);
+      vv[e] = __fmul_rn(vv[e], sc->r[2]);
+    }
+    store_out4<ST>(p, i, x);
+    store_out4<ST>(m, i, mm);
+    store_out4<ST>(v, i, vv);
+  } else {
+    store_out4<ST>(p, i, x);
+    store_out4<ST>(m, i, mm);
+    store_out4<ST>(v, i, vv);
+    store_out4<OT>(out, i, x, &d);
+  }
+}
+
+// Pass A: a warp's maxima into the tensor's absmax slots (1 + bits).
+__device__ __forceinline__ void flush_absmax(const KParams& kp, int t, unsigned (&mx)[3]) {
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const unsigned w = __reduce_max_sync(0xffffffffu, mx[k]);
+    if ((threadIdx.x & 31) == 0) atomicMax(kp.absmax + 3 * t + k, w + 1u);
+    mx[k] = 0u;
+  }
 }
 
 // One 4-element vector of the remainder form: H the bf16 high halves, R the
@@ -393,10 +461,6 @@ __device__ __forceinline__ int bulk_tiles(const Item& it) {
   return (bulk_vectors(it) + kTile - 1) / kTile;
 }
 
-// What a pipeline pass moves through shared memory.
-// kScan: only g, for the inf/nan screen; kNorm: only g, for the squared norm;
-// kReduce: the exchange sources' slices of g, reduced into the shard's g.
-enum class Pass { kUpdate, kScan, kNorm, kReduce };
 
 // Vectors of a reduce tile: as many as the R source slices fit in one stage
 // (at most as many as a screen tile), a multiple of one warp.
@@ -410,7 +474,7 @@ __host__ __device__ constexpr int reduce_vectors(int n_sources) {
 // Vectors in one tile of a pass (Layout::update_vectors or ::scan_vectors).
 template <int ST, int GT, bool REM, Pass PASS>
 __host__ __device__ constexpr int tile_vectors() {
-  return PASS == Pass::kUpdate ? Layout<ST, GT, REM>::update_vectors
+  return update_like(PASS) ? Layout<ST, GT, REM>::update_vectors
                                : Layout<ST, GT, REM>::scan_vectors;
 }
 
@@ -431,7 +495,7 @@ __device__ __forceinline__ void issue_tile(const KParams& kp, const Item& it, in
     const char* g = static_cast<const char*>(it.g) + v * L::kG;
     for (int r = 0; r < kp.n_sources; ++r)
       bulk_load(st + size_t(r) * stride, g + kp.src_delta[r], len * L::kG, bar);
-  } else if constexpr (PASS != Pass::kUpdate) {
+  } else if constexpr (!update_like(PASS)) {
     mbar_expect_tx(bar, len * L::kG);
     bulk_load(st, static_cast<const char*>(it.g) + v * L::kG, len * L::kG, bar);
   } else {
@@ -456,9 +520,11 @@ __device__ __forceinline__ void issue_tile(const KParams& kp, const Item& it, in
 // round trip.
 constexpr int kBatchMax = 8;
 
+
 struct Producer {
   Item it;
   Chunk recs[kBatchMax];  // the current batch's chunk records
+  StateScale sc;          // scaled-state passes: the current item's factors
   int item, v, vend;      // vectors [v, vend) of the current chunk remain
   int chunk;
   int next, batch0, batch_end;  // chunks [next, batch_end) of the batch remain
@@ -471,7 +537,27 @@ struct TileTag {
   int v0;
   int len;
   int chunk;
+  StateScale sc;  // scaled-state passes only
 };
+
+// The factors of tensor t: the stored scales, and for the rescale pass the
+// reciprocal of each new scale (absmax / target; the reciprocal only where
+// the scale is positive, else 0).  Read after the grid barrier that
+// follows the absmax pass.
+__device__ __forceinline__ StateScale tensor_scales(const KParams& kp, int t, bool rescale) {
+  StateScale sc;
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    sc.s[k] = __ldcg(kp.scales + 3 * t + k);
+    sc.r[k] = 0.0f;
+    if (rescale) {
+      const unsigned a = __ldcg(kp.absmax + 3 * t + k);
+      const float scale = a ? __fdiv_rn(__uint_as_float(a - 1u), kp.max_scaled) : 0.0f;
+      sc.r[k] = scale > 0.0f ? __fdiv_rn(1.0f, scale) : 0.0f;
+    }
+  }
+  return sc;
+}
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
@@ -504,7 +590,7 @@ __device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, un
     // the update's chunks are long (16 tiles): one at a time keeps the
     // CTAs on neighbouring chunks; the g-only passes' chunks are 2-4 tiles
     if (pr.next >= pr.batch_end &&
-        !next_batch(pr, kp, counter, PASS == Pass::kUpdate ? 1 : kBatchMax)) {
+        !next_batch(pr, kp, counter, update_like(PASS) ? 1 : kBatchMax)) {
       const unsigned b = pr.slot % kStages;
       tags[b] = TileTag{-1, 0, 0, -1};
       mbar_arrive(full + b);  // completes the phase with no copy
@@ -517,6 +603,8 @@ __device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, un
     if (ch.item != pr.item) {
       pr.item = ch.item;
       pr.it = load_item(kp.items, ch.item);
+      if constexpr (PASS == Pass::kScaledA || PASS == Pass::kScaledB)
+        pr.sc = tensor_scales(kp, pr.it.tensor, PASS == Pass::kScaledB);
     }
     pr.v = ch.tile0 * kTile;
     pr.vend = min((ch.tile0 + ch.ntiles) * kTile, bulk_vectors(pr.it));
@@ -525,7 +613,12 @@ __device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, un
   if constexpr (PASS == Pass::kReduce) tv = reduce_vectors<ST, GT, REM>(kp.n_sources);
   else tv = tile_vectors<ST, GT, REM, PASS>();
   const int len = min(tv, pr.vend - pr.v);
-  tags[pr.slot % kStages] = TileTag{pr.item, pr.v, len, pr.chunk};
+  TileTag& tg = tags[pr.slot % kStages];
+  tg.item = pr.item;
+  tg.v0 = pr.v;
+  tg.len = len;
+  tg.chunk = pr.chunk;
+  if constexpr (PASS == Pass::kScaledA || PASS == Pass::kScaledB) tg.sc = pr.sc;
   issue_tile<ST, GT, REM, PASS>(kp, pr.it, pr.v, static_cast<unsigned>(len), pr.slot, smem, full);
   pr.v += len;
   ++pr.slot;
@@ -534,9 +627,10 @@ __device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, un
 // Consume one tile from shared memory: thread t takes vectors t, t + kTile,
 // ... of it.  DESTS: param-out also goes to the exchange destinations (a
 // separate instance, so the plain step carries no destination loop).
-template <bool ADAMW, int ST, int GT, int OT, bool REM, bool DESTS>
+template <bool ADAMW, int ST, int GT, int OT, bool REM, bool DESTS, Pass PASS = Pass::kUpdate>
 __device__ __forceinline__ void update_tile(const Item& it, const Scal& s, const unsigned char* st,
-                                            int v0, int len, const Dests& d0) {
+                                            int v0, int len, const Dests& d0,
+                                            const StateScale* sc = nullptr, unsigned* mx = nullptr) {
   const Dests d{DESTS ? d0.n : 0, d0.delta};
   using L = Layout<ST, GT, REM>;
 #pragma unroll
@@ -558,7 +652,8 @@ __device__ __forceinline__ void update_tile(const Item& it, const Scal& s, const
       const S4 P = reinterpret_cast<const S4*>(st)[t];
       const S4 M = reinterpret_cast<const S4*>(st + L::off_m)[t];
       const S4 V = reinterpret_cast<const S4*>(st + L::off_v)[t];
-      update4_state<ADAMW, ST, GT, OT>(P, M, V, G, s, it.p, it.m, it.v, it.p_out, i, d);
+      update4_state<ADAMW, ST, GT, OT, PASS>(P, M, V, G, s, it.p, it.m, it.v, it.p_out, i, d, sc,
+                                             mx);
     }
   }
 }
@@ -844,6 +939,7 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
                                           bool& timed_out) {
   const Dests dst{kp.n_dests, kp.dst_delta};
   const bool screen = (kp.flags & kCheckFinite) != 0;  // reduce pass: screen the result
+  unsigned mx[3] = {0u, 0u, 0u};                        // scaled pass A: |new value| maxima
   NormAcc na{0.0f, 0.0f, false, -1, 0};
   NormPending pend{-1, 0.0f};
   double* dpart = nullptr;
@@ -867,13 +963,16 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
   for (;; ++stage) {
     const unsigned b = stage % kStages;
     bool ok = mbar_wait(full + b, (stage / kStages) & 1u);
-    // the norm's chunk closes are warp-wide: one decision per warp
-    if constexpr (PASS == Pass::kNorm) ok = __all_sync(0xffffffffu, ok);
+    // the norm's chunk closes and the absmax flushes are warp-wide: one
+    // decision per warp
+    if constexpr (PASS == Pass::kNorm || PASS == Pass::kScaledA) ok = __all_sync(0xffffffffu, ok);
     TileTag tag{-1, 0, 0, -1};
     if (ok) {
       tag = tags[b];
       if (tag.item >= 0) {
         if (tag.item != cur_item) {
+          if constexpr (PASS == Pass::kScaledA)
+            if (cur_item >= 0) flush_absmax(kp, it.tensor, mx);
           cur_item = tag.item;
           it = load_item(kp.items, tag.item);
         }
@@ -887,6 +986,12 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
                                                               dpart, closes, pend);
         } else if constexpr (PASS == Pass::kReduce) {
           bad |= reduce_tile<ST, GT, REM>(kp, it, st, tag.v0, tag.len, s.gs, screen);
+        } else if constexpr (PASS == Pass::kScaledA || PASS == Pass::kScaledB) {
+          const StateScale sc = tag.sc;
+          if (G.bits & kGroupAdamW)
+            update_tile<true, ST, GT, OT, REM, true, PASS>(it, s, st, tag.v0, tag.len, dst, &sc, mx);
+          else
+            update_tile<false, ST, GT, OT, REM, true, PASS>(it, s, st, tag.v0, tag.len, dst, &sc, mx);
         } else {
           const bool aw = (G.bits & kGroupAdamW) != 0;
           if (dst.n == 0) {
@@ -913,6 +1018,8 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
     }
     if (tag.item < 0) {  // the end marker (the same for every thread)
       ++stage;
+      if constexpr (PASS == Pass::kScaledA)
+        if (cur_item >= 0) flush_absmax(kp, it.tensor, mx);
       if constexpr (PASS == Pass::kNorm) {
         if (na.chunk >= 0) {
           double* buf = red + (closes & 1u) * (kBlock / 32);
@@ -933,15 +1040,32 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
 
 // ---- element-wise paths (tails, runs not 16-byte aligned) -------------------
 
-template <bool ADAMW, int ST, int GT, int OT>
+template <bool ADAMW, int ST, int GT, int OT, Pass PASS>
 __device__ __forceinline__ void update_elem_state(const Item& it, const Scal& s, int i,
-                                                  const Dests& d) {
-  float m = load1<ST>(it.m, i), v = load1<ST>(it.v, i);
-  const float x = adam_elem<ADAMW>(load1<ST>(it.p, i), m, v, load1<GT>(it.g, i), s);
-  store_out1<ST>(it.p, i, x);
-  store_out1<ST>(it.m, i, m);
-  store_out1<ST>(it.v, i, v);
-  store_out1<OT>(it.p_out, i, x, &d);
+                                                  const Dests& d, const StateScale* sc,
+                                                  unsigned* mx) {
+  float m = load1<ST>(it.m, i), v = load1<ST>(it.v, i), x0 = load1<ST>(it.p, i);
+  if constexpr (PASS == Pass::kScaledA || PASS == Pass::kScaledB) {
+    x0 = __fmul_rn(x0, sc->s[0]);
+    m = __fmul_rn(m, sc->s[1]);
+    v = __fmul_rn(v, sc->s[2]);
+  }
+  const float x = adam_elem<ADAMW>(x0, m, v, load1<GT>(it.g, i), s);
+  if constexpr (PASS == Pass::kScaledA) {
+    store_out1<OT>(it.p_out, i, x, &d);
+    mx[0] = max(mx[0], abs_bits(x));
+    mx[1] = max(mx[1], abs_bits(m));
+    mx[2] = max(mx[2], abs_bits(v));
+  } else if constexpr (PASS == Pass::kScaledB) {
+    store_out1<ST>(it.p, i, __fmul_rn(x, sc->r[0]));
+    store_out1<ST>(it.m, i, __fmul_rn(m, sc->r[1]));
+    store_out1<ST>(it.v, i, __fmul_rn(v, sc->r[2]));
+  } else {
+    store_out1<ST>(it.p, i, x);
+    store_out1<ST>(it.m, i, m);
+    store_out1<ST>(it.v, i, v);
+    store_out1<OT>(it.p_out, i, x, &d);
+  }
 }
 
 template <bool ADAMW, int GT>
@@ -963,17 +1087,19 @@ __device__ __forceinline__ void update_elem_rem(const Item& it, const Scal& s, i
   store_all(op, i, oh, &d);
 }
 
-template <bool ADAMW, int ST, int GT, int OT, bool REM>
-__device__ __forceinline__ void update_elem(const Item& it, const Scal& s, int i, const Dests& d) {
+template <bool ADAMW, int ST, int GT, int OT, bool REM, Pass PASS = Pass::kUpdate>
+__device__ __forceinline__ void update_elem(const Item& it, const Scal& s, int i, const Dests& d,
+                                            const StateScale* sc = nullptr, unsigned* mx = nullptr) {
   if constexpr (REM) update_elem_rem<ADAMW, GT>(it, s, i, d);
-  else update_elem_state<ADAMW, ST, GT, OT>(it, s, i, d);
+  else update_elem_state<ADAMW, ST, GT, OT, PASS>(it, s, i, d, sc, mx);
 }
 
 // A whole item not aligned for bulk copies, by the whole CTA: 128-bit
 // streaming loads when every stream is vector-aligned, then element by
 // element for the rest.
-template <bool ADAMW, int ST, int GT, int OT, bool REM>
-__device__ __forceinline__ void simt_item(const Item& it, const Scal& s, const Dests& d) {
+template <bool ADAMW, int ST, int GT, int OT, bool REM, Pass PASS = Pass::kUpdate>
+__device__ __forceinline__ void simt_item(const Item& it, const Scal& s, const Dests& d,
+                                          const StateScale* sc = nullptr, unsigned* mx = nullptr) {
   const int n = it.n;
   int scalar_from = 0;
   if (it.flags & kItemVec) {
@@ -1021,15 +1147,15 @@ __device__ __forceinline__ void simt_item(const Item& it, const Scal& s, const D
         for (int u = 0; u < kUnroll; ++u) {
           const int i = base + u * kBlock;
           if (i < nv)
-            update4_state<ADAMW, ST, GT, OT>(P[u], M[u], V[u], G[u], s, it.p, it.m, it.v, it.p_out, i,
-                                             d);
+            update4_state<ADAMW, ST, GT, OT, PASS>(P[u], M[u], V[u], G[u], s, it.p, it.m, it.v,
+                                                   it.p_out, i, d, sc, mx);
         }
       }
     }
     scalar_from = nv * kVec;
   }
   for (int i = scalar_from + threadIdx.x; i < n; i += kBlock)
-    update_elem<ADAMW, ST, GT, OT, REM>(it, s, i, d);
+    update_elem<ADAMW, ST, GT, OT, REM, PASS>(it, s, i, d, sc, mx);
 }
 
 // True when this thread saw a non-finite g*grad_scale in the item (by the
@@ -1077,6 +1203,10 @@ __device__ __forceinline__ bool tail_pass(const KParams& kp, const SGroup* sgrp,
     const SGroup& G = sgrp[it.group];
     const Scal s{G.beta1, G.omb1, G.beta2, G.omb2, G.bc1, G.bc2, G.eps, G.wd, G.lr, G.gs};
     double sq = 0.0;
+    StateScale sc;
+    unsigned mx[3] = {0u, 0u, 0u};
+    if constexpr (PASS == Pass::kScaledA || PASS == Pass::kScaledB)
+      sc = tensor_scales(kp, it.tensor, PASS == Pass::kScaledB);
     for (int i = bulk_vectors(it) * kVec; i < it.n; ++i) {
       if constexpr (PASS == Pass::kScan) {
         bad |= !isfinite(__fmul_rn(load1<GT>(it.g, i), s.gs));
@@ -1085,10 +1215,17 @@ __device__ __forceinline__ bool tail_pass(const KParams& kp, const SGroup* sgrp,
         sq += x * x;
       } else if constexpr (PASS == Pass::kReduce) {
         bad |= reduce_elem<GT>(kp, it, i, s.gs, screen);
+      } else if constexpr (PASS == Pass::kScaledA || PASS == Pass::kScaledB) {
+        if (G.bits & kGroupAdamW) update_elem<true, ST, GT, OT, REM, PASS>(it, s, i, dst, &sc, mx);
+        else update_elem<false, ST, GT, OT, REM, PASS>(it, s, i, dst, &sc, mx);
       } else {
         if (G.bits & kGroupAdamW) update_elem<true, ST, GT, OT, REM>(it, s, i, dst);
         else update_elem<false, ST, GT, OT, REM>(it, s, i, dst);
       }
+    }
+    if constexpr (PASS == Pass::kScaledA) {  // this lane's item alone: no warp reduction
+      if (bulk_vectors(it) * kVec < it.n)
+        for (int k = 0; k < 3; ++k) atomicMax(kp.absmax + 3 * it.tensor + k, mx[k] + 1u);
     }
     if constexpr (PASS == Pass::kNorm) {  // the item's slot, after the chunk slots
       kp.partials[kp.n_chunks + k] = static_cast<double>(G.gs) * G.gs * sq;
@@ -1140,6 +1277,12 @@ __device__ __forceinline__ bool rest_pass(const KParams& kp, const SGroup* sgrp,
         }
       } else if constexpr (PASS == Pass::kReduce) {
         for (int i = threadIdx.x; i < it.n; i += kBlock) bad |= reduce_elem<GT>(kp, it, i, s.gs, screen);
+      } else if constexpr (PASS == Pass::kScaledA || PASS == Pass::kScaledB) {
+        const StateScale sc = tensor_scales(kp, it.tensor, PASS == Pass::kScaledB);
+        unsigned mx[3] = {0u, 0u, 0u};
+        if (G.bits & kGroupAdamW) simt_item<true, ST, GT, OT, REM, PASS>(it, s, dst, &sc, mx);
+        else simt_item<false, ST, GT, OT, REM, PASS>(it, s, dst, &sc, mx);
+        if constexpr (PASS == Pass::kScaledA) flush_absmax(kp, it.tensor, mx);
       } else {
         if (G.bits & kGroupAdamW) simt_item<true, ST, GT, OT, REM>(it, s, dst);
         else simt_item<false, ST, GT, OT, REM>(it, s, dst);
@@ -1202,7 +1345,9 @@ __device__ __forceinline__ bool grid_barrier(KScratch* sc, unsigned extra) {
 
 // ---- the kernel ---------------------------------------------------------------
 
-template <int ST, int GT, int OT, bool REM>
+// SCALED: the scaled 16-bit state instances (their own kernels, so the
+// plain ones carry none of the two-pass code).
+template <int ST, int GT, int OT, bool REM, bool SCALED = false>
 __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams kp) {
   __shared__ SGroup sgrp[FADAM_MAX_GROUPS];
   __shared__ int s_noop;
@@ -1310,12 +1455,32 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
     __syncthreads();
   }
 
-  // 3. the update
+  // 3. the update (scaled 16-bit state: the absmax pass, a bounded grid
+  //    barrier, the rescale pass)
+  bool scaled_done = false;
   if (updates && !s_noop && barrier_ok) {
     bool unused = false;
-    run_pass<ST, GT, OT, REM, Pass::kUpdate>(kp, sgrp, item_begin, item_end, &kp.scratch->next_update,
-                                         &kp.scratch->next_tail_update, n_items, s_tiles, s_full,
-                                         s_tags, s_prod, s_red, stage, unused, timed_out);
+    if constexpr (SCALED) {
+      run_pass<ST, GT, OT, REM, Pass::kScaledA>(kp, sgrp, item_begin, item_end,
+                                                &kp.scratch->next_update,
+                                                &kp.scratch->next_tail_update, n_items, s_tiles,
+                                                s_full, s_tags, s_prod, s_red, stage, unused,
+                                                timed_out);
+      barrier_ok = grid_barrier(kp.scratch, 0u);
+      if (barrier_ok)
+        run_pass<ST, GT, OT, REM, Pass::kScaledB>(kp, sgrp, item_begin, item_end,
+                                                  &kp.scratch->next_rescale,
+                                                  &kp.scratch->next_tail_rescale, n_items, s_tiles,
+                                                  s_full, s_tags, s_prod, s_red, stage, unused,
+                                                  timed_out);
+      scaled_done = barrier_ok;
+    } else {
+      run_pass<ST, GT, OT, REM, Pass::kUpdate>(kp, sgrp, item_begin, item_end,
+                                               &kp.scratch->next_update,
+                                               &kp.scratch->next_tail_update, n_items, s_tiles,
+                                               s_full, s_tags, s_prod, s_red, stage, unused,
+                                               timed_out);
+    }
   }
   if (__syncthreads_or(timed_out) && tid == 0) atomicExch(&kp.scratch->status, FADAM_ETIMEOUT);
 
@@ -1338,6 +1503,20 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
     const double total = cta_sum(x, s_red);
     if (tid == 0) *kp.sumsq_out = total;
   }
+  if (scaled_done && s_last) {
+    // the new scales replace the old (tensors that had no element keep
+    // theirs), unless some wait gave up; the absmax slots are cleared for
+    // the next step either way
+    __threadfence();
+    const bool ok = ld_acquire_s32(&kp.scratch->status) == FADAM_OK;
+    for (int j = tid; j < 3 * kp.n_tensors; j += kBlock) {
+      const unsigned a = __ldcg(kp.absmax + j);
+      if (a) {
+        if (ok) kp.scales[j] = __fdiv_rn(__uint_as_float(a - 1u), kp.max_scaled);
+        kp.absmax[j] = 0u;
+      }
+    }
+  }
   if (tid == 0) {
     if (s_last) {
       __threadfence();
@@ -1350,6 +1529,8 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
       atomicExch(&kp.scratch->next_scan, 0u);
       atomicExch(&kp.scratch->next_tail_update, 0u);
       atomicExch(&kp.scratch->next_tail_scan, 0u);
+      atomicExch(&kp.scratch->next_rescale, 0u);
+      atomicExch(&kp.scratch->next_tail_rescale, 0u);
       atomicExch(&kp.scratch->done, 0u);
     }
   }
@@ -1374,6 +1555,24 @@ KernelEntry kernel_for(int out_dtype, bool remainders) {
       return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_BF16, false>), smem};
     case FADAM_DT_F16:
       return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_F16, false>), smem};
+    default: return {nullptr, 0};
+  }
+}
+
+// The scaled 16-bit state instance for a (state dtype, g dtype, out dtype)
+// combination; the state dtype is bf16 or fp16.
+template <int ST, int GT>
+KernelEntry scaled_kernel_for(int out_dtype) {
+  const size_t smem = smem_bytes<ST, GT, false>();
+  switch (out_dtype) {
+    case FADAM_DT_NONE:
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_NONE, false, true>), smem};
+    case FADAM_DT_F32:
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_F32, false, true>), smem};
+    case FADAM_DT_BF16:
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_BF16, false, true>), smem};
+    case FADAM_DT_F16:
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_F16, false, true>), smem};
     default: return {nullptr, 0};
   }
 }

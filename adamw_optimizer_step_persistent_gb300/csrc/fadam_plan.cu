@@ -89,7 +89,7 @@ int mv_size(const Dtypes& d) { return d.rem ? 4 : elem_size(d.p); }
 
 fadam_status check_dtypes(const Dtypes& d, uint32_t flags) {
   const uint32_t known = FADAM_CAPTURABLE | FADAM_REMAINDERS | FADAM_CHECK_FINITE |
-                         FADAM_STEP_PREADVANCED | FADAM_TEST_BARRIER_TIMEOUT;
+                         FADAM_STEP_PREADVANCED | FADAM_TEST_BARRIER_TIMEOUT | FADAM_SCALED_STATES;
   if (flags & ~known) return fail(FADAM_EINVAL, "unknown flag bits 0x%x", flags & ~known);
   if ((flags & FADAM_STEP_PREADVANCED) && !(flags & FADAM_CAPTURABLE))
     return fail(FADAM_EINVAL, "FADAM_STEP_PREADVANCED needs FADAM_CAPTURABLE");
@@ -107,6 +107,8 @@ fadam_status check_dtypes(const Dtypes& d, uint32_t flags) {
   } else if (elem_size(d.p) == 0) {
     return fail(FADAM_EDTYPE, "state dtype %d (p, m, v) is not fp32, bf16 or fp16", d.p);
   }
+  if ((flags & FADAM_SCALED_STATES) && (d.rem || (d.p != FADAM_DT_BF16 && d.p != FADAM_DT_F16)))
+    return fail(FADAM_EDTYPE, "scaled states need a bf16 or fp16 state and no remainders");
   return FADAM_OK;
 }
 
@@ -314,13 +316,25 @@ Item to_item(const fadam_tensor& t, const PackItem& pi, const Dtypes& d) {
   it.n = static_cast<int32_t>(pi.n);
   it.group = static_cast<uint16_t>(t.group);
   it.flags = static_cast<uint16_t>((pi.level >= 1 ? kItemVec : 0) | (pi.level >= 2 ? kItemBulk : 0));
+  it.tensor = static_cast<int32_t>(pi.tensor);
   return it;
 }
 
-KernelEntry select_kernel(const Dtypes& d) {
+KernelEntry select_kernel(const Dtypes& d, bool scaled) {
   // the remainder form keeps fp32 m and v: its kernels sit with fp32 state
   const int32_t st = d.rem ? FADAM_DT_F32 : d.p;
   const int key = st * 4 + d.g;
+  if (scaled) {
+    switch (key) {
+      case FADAM_DT_BF16 * 4 + FADAM_DT_F32: return scaled_kernel_sbf16_gf32(d.out);
+      case FADAM_DT_BF16 * 4 + FADAM_DT_BF16: return scaled_kernel_sbf16_gbf16(d.out);
+      case FADAM_DT_BF16 * 4 + FADAM_DT_F16: return scaled_kernel_sbf16_gf16(d.out);
+      case FADAM_DT_F16 * 4 + FADAM_DT_F32: return scaled_kernel_sf16_gf32(d.out);
+      case FADAM_DT_F16 * 4 + FADAM_DT_BF16: return scaled_kernel_sf16_gbf16(d.out);
+      case FADAM_DT_F16 * 4 + FADAM_DT_F16: return scaled_kernel_sf16_gf16(d.out);
+      default: return {nullptr, 0};
+    }
+  }
   switch (key) {
     case FADAM_DT_F32 * 4 + FADAM_DT_F32: return kernel_sf32_gf32(d.out, d.rem);
     case FADAM_DT_F32 * 4 + FADAM_DT_BF16: return kernel_sf32_gbf16(d.out, d.rem);
@@ -420,7 +434,7 @@ fadam_status prepare(const fadam_tensor* tensors, int64_t n_tensors, const fadam
 
   hp.d = d;
   hp.flags = flags;
-  const KernelEntry ke = select_kernel(d);
+  const KernelEntry ke = select_kernel(d, (flags & FADAM_SCALED_STATES) != 0);
   hp.kernel = ke.fn;
   hp.smem = ke.smem;
   if (!hp.kernel) return fail(FADAM_EDTYPE, "no kernel for this dtype combination");
@@ -494,11 +508,16 @@ struct fadam_plan {
   int32_t n_sources = 0, average = 0, n_dests = 0;
   int64_t src_delta[FADAM_MAX_SOURCES] = {};
   int64_t dst_delta[FADAM_MAX_DESTS] = {};
+  // scaled state: the caller's scales and the plan's absmax workspace
+  float* scales = nullptr;
+  unsigned* d_absmax = nullptr;
 };
 
 namespace {
 
 void free_plan_memory(fadam_plan* p) {
+  if (p->d_absmax) cudaFree(p->d_absmax);
+  p->d_absmax = nullptr;
   if (p->d_items) cudaFree(p->d_items);
   if (p->d_chunks) cudaFree(p->d_chunks);
   if (p->d_cta) cudaFree(p->d_cta);
@@ -524,6 +543,16 @@ void fill_params(KParams& kp, const Item* items, const int32_t* cta, const Chunk
   kp.n_groups = n_groups;
   kp.flags = flags;
   fill_kgroups(groups, n_groups, flags, kp.groups);
+}
+
+void fill_scaled(KParams& kp, const fadam_plan* plan) {
+  if (!(plan->hp.flags & FADAM_SCALED_STATES)) return;
+  kp.scales = plan->scales;
+  kp.absmax = plan->d_absmax;
+  kp.n_tensors = static_cast<int32_t>(plan->tensors.size());
+  // half the largest finite value of the state dtype
+  kp.max_scaled = plan->hp.d.p == FADAM_DT_F16 ? 0x1.ffcp+14f   // 65504 / 2
+                                                : 0x1.fep+126f;  // 0x7F7F as bf16, / 2
 }
 
 void fill_exchange(KParams& kp, const fadam_plan* plan) {
@@ -588,6 +617,11 @@ fadam_status fadam_plan_create(const fadam_tensor* tensors, int64_t n_tensors,
   // gradient-norm launches: one partial per tile chunk and per item
   if (e == cudaSuccess)
     e = cudaMalloc(&plan->d_partials, (hp.chunks.size() + hp.items.size() + 1) * sizeof(double));
+  // scaled state: three absmax slots per tensor, zero between steps
+  if (e == cudaSuccess && (flags & FADAM_SCALED_STATES) && n_tensors > 0) {
+    e = cudaMalloc(&plan->d_absmax, size_t(n_tensors) * 3 * sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMemset(plan->d_absmax, 0, size_t(n_tensors) * 3 * sizeof(unsigned));
+  }
   if (e != cudaSuccess) {
     st = cuda_fail(e, "plan upload");
     free_plan_memory(plan);
@@ -627,13 +661,29 @@ fadam_status fadam_step(fadam_plan* plan, int32_t* noop_dev, fadam_stream stream
                     i, plan->groups[i].step);
   DeviceGuard guard(hp.device);
   if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  const bool scaled = (hp.flags & FADAM_SCALED_STATES) != 0;
+  if (scaled && !plan->scales)
+    return fail(FADAM_EINVAL, "a scaled-state plan needs fadam_plan_set_state_scales first");
   KParams kp;
   fill_params(kp, plan->d_items, plan->d_cta, plan->d_chunks, static_cast<int32_t>(hp.chunks.size()),
               noop_dev, plan->d_scratch, plan->groups.data(), plan->n_groups, hp.flags);
   fill_exchange(kp, plan);
+  fill_scaled(kp, plan);
   kp.n_sources = 0;  // the plain step reads g as it stands
-  return launch(hp.kernel, hp.smem, kp, hp.grid, (hp.flags & FADAM_CHECK_FINITE) != 0,
+  return launch(hp.kernel, hp.smem, kp, hp.grid, (hp.flags & FADAM_CHECK_FINITE) != 0 || scaled,
                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+fadam_status fadam_plan_set_state_scales(fadam_plan* plan, float* scales_dev) {
+  t_last_error.clear();
+  if (!plan) return fail(FADAM_EINVAL, "plan is NULL");
+  if (!(plan->hp.flags & FADAM_SCALED_STATES))
+    return fail(FADAM_EINVAL, "the plan was not created with FADAM_SCALED_STATES");
+  if (!scales_dev) return fail(FADAM_EINVAL, "scales_dev is NULL");
+  if (reinterpret_cast<uintptr_t>(scales_dev) % 4)
+    return fail(FADAM_EALIGN, "scales_dev is not 4-byte aligned");
+  plan->scales = scales_dev;
+  return FADAM_OK;
 }
 
 fadam_status fadam_plan_set_exchange(fadam_plan* plan, const void* g_shard,
@@ -709,11 +759,14 @@ fadam_status fadam_step_reduce(fadam_plan* plan, int32_t* noop_dev, fadam_stream
                     i, plan->groups[i].step);
   DeviceGuard guard(hp.device);
   if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  if ((hp.flags & FADAM_SCALED_STATES) && !plan->scales)
+    return fail(FADAM_EINVAL, "a scaled-state plan needs fadam_plan_set_state_scales first");
   KParams kp;
   fill_params(kp, plan->d_items, plan->d_cta, plan->d_chunks, static_cast<int32_t>(hp.chunks.size()),
               noop_dev, plan->d_scratch, plan->groups.data(), plan->n_groups,
               hp.flags | kReduceFirst);
   fill_exchange(kp, plan);
+  fill_scaled(kp, plan);
   return launch(hp.kernel, hp.smem, kp, hp.grid, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -1068,6 +1121,8 @@ extern "C" fadam_status fadam_step_noalloc(const fadam_tensor* tensors, int64_t 
                                            fadam_stream stream) {
   t_last_error.clear();
   const Dtypes d{p_dtype, g_dtype, out_dtype, (flags & FADAM_REMAINDERS) != 0};
+  if (flags & FADAM_SCALED_STATES)
+    return fail(FADAM_EINVAL, "scaled states need a plan (fadam_plan_set_state_scales)");
   if ((flags & FADAM_CHECK_FINITE) && !noop_dev)
     return fail(FADAM_EINVAL, "FADAM_CHECK_FINITE needs a noop_dev flag to write");
   if (noop_dev && reinterpret_cast<uintptr_t>(noop_dev) % 4)

@@ -60,7 +60,8 @@ class FusedAdamShard:
     def __init__(self, param_groups: Sequence[Dict], *, capturable: bool = False,
                  check_finite: bool = False, remainders: bool = False,
                  shared_step: bool = False, step_preadvanced: bool = False,
-                 grad_scale: float = 1.0, device=None, extra_flags: int = 0):
+                 grad_scale: float = 1.0, device=None, extra_flags: int = 0,
+                 state_scales: Optional[torch.Tensor] = None):
         if check_finite and not capturable:
             raise ValueError("check_finite needs capturable=True (the counters live on the device)")
         self.capturable = capturable
@@ -73,6 +74,7 @@ class FusedAdamShard:
         flags = (_abi.CAPTURABLE if capturable else 0) | (_abi.REMAINDERS if remainders else 0)
         flags |= (_abi.CHECK_FINITE if check_finite else 0)
         flags |= (_abi.STEP_PREADVANCED if step_preadvanced else 0)
+        flags |= (_abi.SCALED_STATES if state_scales is not None else 0)
         flags |= int(extra_flags)
         self.flags = flags
 
@@ -135,6 +137,18 @@ class FusedAdamShard:
                 arr, len(descs), self._groups_c, n, dtype_code(p_dtype), dtype_code(self.g_dtype),
                 dtype_code(out_dtype), flags, ctypes.byref(plan)), "fadam_plan_create")
         self._plan = plan
+        self.state_scales = None
+        if state_scales is not None:
+            # scaled 16-bit state: one fp32 scale per tensor for p, m and v,
+            # in the order the tensors were given ([n_tensors, 3])
+            if (state_scales.dtype != torch.float32 or state_scales.device != self.device
+                    or not state_scales.is_contiguous()
+                    or tuple(state_scales.shape) != (self.n_tensors, 3)):
+                raise ValueError("state_scales must be a contiguous fp32 [n_tensors, 3] "
+                                 "tensor on the shard's device")
+            _abi.check(_abi.lib().fadam_plan_set_state_scales(self._plan, state_scales.data_ptr()),
+                       "fadam_plan_set_state_scales")
+            self.state_scales = state_scales
 
     # ---- scalars ---------------------------------------------------------------
 

@@ -311,6 +311,9 @@ def run_gpu(args):
         spec = workloads.large_uniform(n_tensors=args.n_tensors, numel=args.numel,
                                        seed=1237 + 1000 * rank, state_dtype=torch.bfloat16,
                                        g_dtype=torch.bfloat16)
+    elif args.workload == "scaled_state_shard":
+        spec = workloads.scaled_versions(full=True)["scaled_state_shard"]
+        spec.seed += 1000 * rank
     elif args.workload == "exchange_shard":
         spec = workloads.exchange_versions(full=True)["exchange_shard"]
         spec.seed += 1000 * rank
@@ -324,6 +327,8 @@ def run_gpu(args):
     kw = dict(remainders=spec.remainders, grad_scale=spec.grad_scale)
 
     def make(capturable, **more):
+        if spec.scaled_state:  # each plan steps its own copy of the scales
+            more["state_scales"] = shard.state_scales[shard.plan_order()].contiguous()
         opt = FusedAdamShard(groups, capturable=capturable, **kw, **more)
         if spec.exchange_ranks:  # the data-parallel exchange stand-in
             opt.set_exchange(shard.buckets["g"], list(shard.sources),
@@ -335,6 +340,10 @@ def run_gpu(args):
     info = cap.info()
     bytes_step = info["bytes_per_step"]
     elems = info["n_elements"]
+    if spec.scaled_state:
+        # the rescale depends on every new value of a tensor: a second pass
+        # reads p, m, v and g again (24 B per element for fp16 state, bf16 g)
+        bytes_step += elems * (3 * shard.params[0].element_size() + shard.grads[0].element_size())
     if spec.exchange_ranks:
         gsz = shard.buckets["g"].element_size()
         # every step also writes the param-out copy to each destination
@@ -465,7 +474,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="large_uniform",
                     choices=["large_uniform", "capturable_l2", "remainder_shard", "many_small",
-                             "large_uniform_bf16_state", "exchange_shard"])
+                             "large_uniform_bf16_state", "exchange_shard", "scaled_state_shard"])
     ap.add_argument("--n-tensors", type=int, default=None,
                     help="tensor count of large_uniform[_bf16_state] (201) or many_small (20000)")
     ap.add_argument("--numel", type=int, default=320 * 65536)

@@ -88,6 +88,8 @@ typedef int32_t fadam_status;
 #define FADAM_CHECK_FINITE 4u /* screen g*grad_scale for inf/nan first; sets noop */
 #define FADAM_STEP_PREADVANCED 8u /* capturable: *step_dev already advanced by the
                                      caller; use it as is and do not write it */
+#define FADAM_SCALED_STATES 16u /* 16-bit p, m, v stored with one fp32 scale each
+                                   per tensor (fadam_plan_set_state_scales) */
 /* Diagnostic, for testing the failure path: with FADAM_CHECK_FINITE, the
  * grid barrier after the inf/nan screen waits for one more CTA than the
  * launch has, so every CTA's wait runs out after its limit (about 2 s).
@@ -309,6 +311,32 @@ fadam_status fadam_grad_reduce(fadam_plan* plan, fadam_stream stream);
  * is skipped (a set noop flag).  Errors: as fadam_step, and FADAM_EINVAL
  * when no sources are set. */
 fadam_status fadam_step_reduce(fadam_plan* plan, int32_t* noop_dev, fadam_stream stream);
+
+/* Scaled optimizer state ("apex/contrib/optimizers/distributed_fused_adam.py",
+ * _local_step_with_scaled_states and _apply_state_scale): with
+ * FADAM_SCALED_STATES the plan's p, m and v (state dtype bf16 or fp16, not
+ * the remainder form) hold scaled values, and each tensor has three fp32
+ * scales.  A step widens each value and multiplies it by its scale, runs
+ * the fp32 update (param-out, if any, is the cast of the new fp32 param),
+ * then rescales each of the tensor's three buffers: absmax = the largest
+ * magnitude of the new values (NaN if any is NaN), scale = absmax /
+ * (largest finite value of the state dtype / 2), reciprocal = 1 / scale
+ * where scale > 0 else 0, stored value = new value * reciprocal rounded to
+ * nearest even; the new scales replace the old.  Tensors with no elements
+ * keep their scales.  Each product, quotient and reciprocal is one IEEE
+ * float operation.  For bf16 that target is about 1.7e38, so a buffer whose
+ * absmax is below about 0.5 gets a subnormal scale whose reciprocal is
+ * infinite (the page's operations do the same).
+ *   scales_dev   device float array of 3 * n_tensors: tensor i's scales of
+ *                p, m, v at [3i], [3i+1], [3i+2] (i in the order given to
+ *                fadam_plan_create), 4-byte aligned, read and rewritten by
+ *                every applied step (left as is by a skipped one).
+ * The pointer is copied on the host; a scaled plan's steps fail with
+ * FADAM_EINVAL until it is set.  A scaled step is one cooperative launch
+ * with two passes over the shard and a bounded grid barrier between
+ * (the new scales depend on every new value of a tensor).  Errors:
+ * FADAM_EINVAL (not a scaled plan, NULL), FADAM_EALIGN. */
+fadam_status fadam_plan_set_state_scales(fadam_plan* plan, float* scales_dev);
 
 /* Read (synchronously) and clear the plan's device status word:
  * *device_status = FADAM_OK, or FADAM_ETIMEOUT when a bounded wait of the

@@ -44,7 +44,7 @@ def oracle_groups(spec: workloads.ShardSpec) -> List[oracle.Group]:
 
 
 def oracle_shard(shard: workloads.Shard, idx: List[int] = None, elems: Dict[int, np.ndarray] = None,
-                 step_slot=None) -> oracle.Shard:
+                 step_slot=None, scales: torch.Tensor = None) -> oracle.Shard:
     """Snapshot of the shard (or of sampled elements of it) as oracle arrays.
 
     `idx` is the tensor order; `elems[i]`, when given, selects elements of
@@ -68,6 +68,8 @@ def oracle_shard(shard: workloads.Shard, idx: List[int] = None, elems: Dict[int,
         else:
             t.p = to_np(sel(shard.params[i]))
             t.state_dtype = _ODT[spec.state_dtype]
+            if scales is not None:  # [n, 3] in the order of idx
+                t.scales = to_np(scales[len(tensors)]).copy()
             if spec.out_dtype is not None:
                 t.p_out = to_np(sel(shard.params_out[i]))
                 t.out_dtype = _ODT[spec.out_dtype]
@@ -88,6 +90,13 @@ def refresh_grads(osh: oracle.Shard, shard: workloads.Shard, idx=None, elems=Non
 def _ordered16(bits: np.ndarray) -> np.ndarray:
     b = bits.astype(np.int32)
     return np.where(b & 0x8000, -(b & 0x7FFF), b)
+
+
+def _is_nan16(bits: np.ndarray, dtype) -> np.ndarray:
+    b = bits.astype(np.int32)
+    if dtype == torch.bfloat16:
+        return ((b & 0x7F80) == 0x7F80) & ((b & 0x7F) != 0)
+    return ((b & 0x7C00) == 0x7C00) & ((b & 0x3FF) != 0)
 
 
 class Report:
@@ -116,8 +125,10 @@ class Report:
         if rel.size:
             self.worst = max(self.worst, float(rel.max()))
 
-    def ulp16(self, got: np.ndarray, want: np.ndarray, what: str) -> None:
+    def ulp16(self, got: np.ndarray, want: np.ndarray, what: str, dtype=None) -> None:
         d = np.abs(_ordered16(got) - _ordered16(want))
+        if dtype is not None:  # two NaNs match whatever their payloads
+            d = np.where(_is_nan16(got, dtype) & _is_nan16(want, dtype), 0, d)
         if (d > 1).any():
             k = int(np.argmax(d > 1))
             raise AssertionError(f"{what}: {int((d > 1).sum())} values beyond 1 ulp; first at "
@@ -140,9 +151,10 @@ def compare(shard: workloads.Shard, osh: oracle.Shard, idx=None, elems=None,
     for t, i in zip(osh.tensors, idx):
         sel = (lambda x: x) if elems is None else (lambda x, e=torch.as_tensor(elems[i], device=shard.params[i].device): x[e])
         if state16:  # 16-bit p, m, v: within one unit in the last place
-            report.ulp16(to_np(sel(shard.exp_avgs[i])), t.m, f"tensor {i} m")
-            report.ulp16(to_np(sel(shard.exp_avg_sqs[i])), t.v, f"tensor {i} v")
-            report.ulp16(to_np(sel(shard.params[i])), t.p, f"tensor {i} p")
+            sdt = spec.state_dtype
+            report.ulp16(to_np(sel(shard.exp_avgs[i])), t.m, f"tensor {i} m", sdt)
+            report.ulp16(to_np(sel(shard.exp_avg_sqs[i])), t.v, f"tensor {i} v", sdt)
+            report.ulp16(to_np(sel(shard.params[i])), t.p, f"tensor {i} p", sdt)
             if spec.out_dtype == torch.float32:
                 report.f32(to_np(sel(shard.params_out[i])), t.p_out, f"tensor {i} p_out")
             elif spec.out_dtype is not None:

@@ -162,3 +162,34 @@ def test_exchange_shard_full_size():
     opt.close()
     del shard, opt
     _free()
+
+
+def test_scaled_state_full_size():
+    """The 1.2e9-element fp16 scaled-state shard, two regular steps.  The
+    rescale depends on every element of a tensor, so the oracle runs whole
+    tensors: the first layer's 4096x4096 and 4096x11008 matrices and both
+    norm vectors, against every one of their elements and their scales."""
+    spec = workloads.scaled_versions(full=True)["scaled_state_shard"]
+    shard = workloads.materialize(spec, DEV)
+    order = shard.plan_order()
+    scales = shard.state_scales[order].contiguous()
+    opt = FusedAdamShard(shard.param_groups(), state_scales=scales)
+    pos = [0, 1, 4, 5]
+    idx = [order[k] for k in pos]
+    osh = helpers.oracle_shard(shard, idx=idx, scales=scales[pos])
+    for k in (1, 2):
+        if k > 1:
+            workloads.fresh_grads(shard, k)
+            helpers.refresh_grads(osh, shard, idx=idx)
+        opt.step()
+        oracle.shard_step(osh, capturable=False)
+    torch.cuda.synchronize()
+    rep = helpers.compare(shard, osh, idx=idx)
+    assert rep.exact_fraction == 1.0
+    got = helpers.to_np(scales)
+    for k, t in zip(pos, osh.tensors):
+        assert got[k].tobytes() == t.scales.tobytes(), k
+    assert opt.group_steps() == [2]
+    opt.close()
+    del shard, opt
+    _free()

@@ -38,6 +38,14 @@ Five shard recipes, all synthetic (no dataset or checkpoint is involved):
    (each rank's bf16 gradient for this shard, ~ N(0, 1e-2)), averaged into
    the shard, and R - 1 destination buffers laid out like the param-out
    shard (the other ranks' places for it).
+7. ``scaled_state_shard``: the GPT-style layer list with p, m, v stored as
+   fp16 values and one fp32 scale each per tensor (the page's scaled state,
+   meant for fp16 optimizer states), bf16 grads ~ N(0, 1e-2), bf16
+   param-out, AdamW wd 0.1, betas (0.9, 0.95), eps 1e-8, lr 1e-3, host
+   scalars (the page's scaled path is the regular one).  The stored values
+   are draws of N(0, 1000^2) (|.| for v) rounded to the state dtype and the
+   scales 1e-3, 1e-6 and 1e-9 (p ~ N(0, 1), m ~ N(0, 1e-6), v ~ 1e-6):
+   valid scaled states, not the output of a rescale.
 
 Every recipe takes size arguments that shrink it for tests the oracle must
 finish in seconds (``small_versions``); the defaults are the full workloads.
@@ -87,6 +95,8 @@ class ShardSpec:
     exchange_dests: int = 0    # with this many source and destination buffers
     exchange_average: bool = True  # ReduceOp.AVG (else SUM)
     exchange_align: int = 64   # fragment starts rounded up to this many elements
+    scaled_state: bool = False  # p, m, v in state_dtype with one fp32 scale each per tensor
+    scale_of: tuple = (1e-3, 1e-6, 1e-9)  # the scales drawn states are stored with
     notes: Dict = field(default_factory=dict)
 
     @property
@@ -168,6 +178,33 @@ def exchange_shard(layers: int = 8, hidden: int = 4096, ffn: int = 11008, ranks:
                      exchange_ranks=ranks, exchange_dests=ranks - 1 if dests is None else dests)
 
 
+def scaled_state_shard(layers: int = 8, hidden: int = 4096, ffn: int = 11008,
+                       state_dtype: torch.dtype = torch.float16, seed: int = 1241) -> ShardSpec:
+    per_layer = [hidden * hidden, hidden * ffn, hidden * ffn, ffn * hidden, hidden, hidden]
+    sizes = per_layer * layers
+    g = GroupSpec(adam_w_mode=True, lr=1e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1)
+    return ShardSpec("scaled_state_shard", [g], sizes, [0] * len(sizes), g_dtype=torch.bfloat16,
+                     out_dtype=torch.bfloat16, state_dtype=state_dtype, grad_std=1e-2, seed=seed,
+                     scaled_state=True)
+
+
+def scaled_versions(full: bool = False) -> Dict[str, ShardSpec]:
+    """The scaled-state recipe: full size, or small ones (fp16 with an empty
+    tensor and ragged sizes; bf16 with moments large enough that bf16's
+    scale target keeps the reciprocals finite; bf16 with Adam-sized moments,
+    whose reciprocals overflow as on the page)."""
+    if full:
+        return {"scaled_state_shard": scaled_state_shard()}
+    f16 = scaled_state_shard(layers=2, hidden=256, ffn=689)
+    f16.sizes = f16.sizes[:5] + [0] + f16.sizes[5:] + [3, 4097]
+    f16.group_of = [0] * len(f16.sizes)
+    b16 = scaled_state_shard(layers=1, hidden=320, ffn=1000, state_dtype=torch.bfloat16)
+    b16.name, b16.scale_of = "scaled_bf16", (1e-3, 1e-3, 1e-3)
+    b16_small = scaled_state_shard(layers=1, hidden=128, ffn=300, state_dtype=torch.bfloat16)
+    b16_small.name = "scaled_bf16_small_moments"
+    return {"scaled_state_shard": f16, "scaled_bf16": b16, "scaled_bf16_small_moments": b16_small}
+
+
 def exchange_offsets(sizes: List[int], align: int = 64) -> List[int]:
     """Fragment starts in the shard buffer, each rounded up to `align`
     elements."""
@@ -230,6 +267,8 @@ class Shard:
     sources: Optional[torch.Tensor] = None
     dests: Optional[torch.Tensor] = None
     offsets: Optional[List[int]] = None
+    # scaled-state recipes: [n_tensors, 3] fp32 scales (p, m, v), spec order
+    state_scales: Optional[torch.Tensor] = None
 
     def param_groups(self) -> List[Dict]:
         """The per-group dicts FusedAdamShard takes."""
@@ -307,6 +346,10 @@ def materialize(spec: ShardSpec, device="cuda") -> Shard:
             p.copy_(hi)
             r.copy_(torch.randint(-32768, 32768, (s,), generator=gen, device=dev,
                                   dtype=torch.int32).to(torch.int16))
+        elif spec.scaled_state:
+            p.copy_((torch.randn(s, generator=gen, device=dev) * 1000).to(p.dtype))
+            m.copy_((torch.randn(s, generator=gen, device=dev) * 1000).to(m.dtype))
+            v.copy_((torch.randn(s, generator=gen, device=dev) * 1000).abs().to(v.dtype))
         else:
             p.copy_(torch.randn(s, generator=gen, device=dev).to(p.dtype))
         g.copy_((torch.randn(s, generator=gen, device=dev) * spec.grad_std).to(spec.g_dtype))
@@ -334,7 +377,10 @@ def materialize(spec: ShardSpec, device="cuda") -> Shard:
                              .to(spec.g_dtype))
         sources = sources[:, :L]
         dests = torch.zeros(spec.exchange_dests, Lp, dtype=spec.out_dtype, device=dev)[:, :L]
-    return Shard(spec, params, ms, vs, gs, outs, rems, buckets, sources, dests, xoff)
+    scales = None
+    if spec.scaled_state:
+        scales = torch.tensor([list(spec.scale_of)] * n, dtype=torch.float32, device=dev).reshape(n, 3)
+    return Shard(spec, params, ms, vs, gs, outs, rems, buckets, sources, dests, xoff, scales)
 
 
 def inf_position(spec: ShardSpec) -> tuple:
