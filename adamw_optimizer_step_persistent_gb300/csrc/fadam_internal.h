@@ -97,6 +97,10 @@ constexpr uint32_t kScaledStates = FADAM_SCALED_STATES;
 constexpr uint32_t kNormOnly = 1u << 30;
 constexpr uint32_t kReduceOnly = 1u << 29;
 constexpr uint32_t kReduceFirst = 1u << 28;
+// Launch-only: the gradients are read from pinned host memory (zero copy):
+// tensor t's g lives at host_g[t] instead of dev_g[t], every item goes the
+// element-wise way (plain loads; no bulk copies from host memory).
+constexpr uint32_t kHostGrads = 1u << 27;
 
 // Everything one launch needs, passed as a __grid_constant__ parameter.
 struct alignas(16) KParams {
@@ -126,6 +130,10 @@ struct alignas(16) KParams {
   unsigned* absmax;
   int32_t n_tensors;
   float max_scaled;
+  // host-gradient launches: per tensor, the device-accessible address of
+  // the host gradient and the tensor's own device g
+  const char* const* host_g;
+  const char* const* dev_g;
   KGroup groups[FADAM_MAX_GROUPS];
 };
 

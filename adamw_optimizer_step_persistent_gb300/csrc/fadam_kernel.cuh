@@ -1245,6 +1245,8 @@ __device__ __forceinline__ bool rest_pass(const KParams& kp, const SGroup* sgrp,
                                           int item_end, double* red) {
   __shared__ int s_count;
   __shared__ int s_list[kBlock];
+  // host-gradient launches take every item here, reading g from host memory
+  const bool host_g = (kp.flags & kHostGrads) != 0;
   const Dests dst{kp.n_dests, kp.dst_delta};
   const bool screen = (kp.flags & kCheckFinite) != 0;
   bool bad = false;
@@ -1254,12 +1256,14 @@ __device__ __forceinline__ bool rest_pass(const KParams& kp, const SGroup* sgrp,
     const int k = base + threadIdx.x;
     if (k < item_end) {
       const uint16_t flags = __ldg(&kp.items[k].flags);
-      if (!(FADAM_BULK && (flags & kItemBulk))) s_list[atomicAdd(&s_count, 1)] = k;
+      if (host_g || !(FADAM_BULK && (flags & kItemBulk))) s_list[atomicAdd(&s_count, 1)] = k;
     }
     __syncthreads();
     const int count = s_count;
     for (int q = 0; q < count; ++q) {
-      const Item it = load_item(kp.items, s_list[q]);
+      Item it = load_item(kp.items, s_list[q]);
+      if (host_g)  // the same element offset within the tensor, in host memory
+        it.g = kp.host_g[it.tensor] + (static_cast<const char*>(it.g) - kp.dev_g[it.tensor]);
       const SGroup& G = sgrp[it.group];
       const Scal s{G.beta1, G.omb1, G.beta2, G.omb2, G.bc1, G.bc2, G.eps, G.wd, G.lr, G.gs};
       if constexpr (PASS == Pass::kScan) {
@@ -1301,10 +1305,11 @@ __device__ __forceinline__ void run_pass(const KParams& kp, const SGroup* sgrp, 
                                          int n_items, unsigned char* smem, uint64_t* full,
                                          TileTag* tags, Producer& pr, double* red,
                                          unsigned& stage, bool& bad, bool& timed_out) {
-  if (FADAM_BULK && kp.n_chunks > 0 && !timed_out)
+  const bool bulk = FADAM_BULK && !(kp.flags & kHostGrads);
+  if (bulk && kp.n_chunks > 0 && !timed_out)
     bulk_pass<ST, GT, OT, REM, PASS>(kp, sgrp, counter, smem, full, tags, pr, red, stage, bad,
                                      timed_out);
-  if (FADAM_BULK) bad |= tail_pass<ST, GT, OT, REM, PASS>(kp, sgrp, tail_counter, n_items);
+  if (bulk) bad |= tail_pass<ST, GT, OT, REM, PASS>(kp, sgrp, tail_counter, n_items);
   bad |= rest_pass<ST, GT, OT, REM, PASS>(kp, sgrp, item_begin, item_end, red);
 }
 

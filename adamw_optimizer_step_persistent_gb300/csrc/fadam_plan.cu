@@ -511,6 +511,11 @@ struct fadam_plan {
   // scaled state: the caller's scales and the plan's absmax workspace
   float* scales = nullptr;
   unsigned* d_absmax = nullptr;
+  // host-gradient steps: per tensor its device g, and the host gradient's
+  // device-accessible address (written by each call)
+  const char** d_dev_g = nullptr;
+  const char** d_host_g = nullptr;
+  std::vector<const char*> host_g;
 };
 
 namespace {
@@ -518,6 +523,9 @@ namespace {
 void free_plan_memory(fadam_plan* p) {
   if (p->d_absmax) cudaFree(p->d_absmax);
   p->d_absmax = nullptr;
+  if (p->d_dev_g) cudaFree(p->d_dev_g);
+  if (p->d_host_g) cudaFree(p->d_host_g);
+  p->d_dev_g = p->d_host_g = nullptr;
   if (p->d_items) cudaFree(p->d_items);
   if (p->d_chunks) cudaFree(p->d_chunks);
   if (p->d_cta) cudaFree(p->d_cta);
@@ -617,6 +625,18 @@ fadam_status fadam_plan_create(const fadam_tensor* tensors, int64_t n_tensors,
   // gradient-norm launches: one partial per tile chunk and per item
   if (e == cudaSuccess)
     e = cudaMalloc(&plan->d_partials, (hp.chunks.size() + hp.items.size() + 1) * sizeof(double));
+  // host-gradient steps: the tensors' device g pointers, and room for the
+  // host ones
+  if (e == cudaSuccess && n_tensors > 0) {
+    std::vector<const char*> dev_g(n_tensors);
+    for (int64_t i = 0; i < n_tensors; ++i) dev_g[i] = static_cast<const char*>(tensors[i].g);
+    e = cudaMalloc(&plan->d_dev_g, size_t(n_tensors) * sizeof(char*));
+    if (e == cudaSuccess)
+      e = cudaMemcpy(plan->d_dev_g, dev_g.data(), size_t(n_tensors) * sizeof(char*),
+                     cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMalloc(&plan->d_host_g, size_t(n_tensors) * sizeof(char*));
+    plan->host_g.assign(size_t(n_tensors), nullptr);
+  }
   // scaled state: three absmax slots per tensor, zero between steps
   if (e == cudaSuccess && (flags & FADAM_SCALED_STATES) && n_tensors > 0) {
     e = cudaMalloc(&plan->d_absmax, size_t(n_tensors) * 3 * sizeof(unsigned));
@@ -646,7 +666,18 @@ fadam_status fadam_plan_set_groups(fadam_plan* plan, const fadam_group* groups, 
   return FADAM_OK;
 }
 
+namespace {
+fadam_status step_launch(fadam_plan* plan, int32_t* noop_dev, fadam_stream stream,
+                         uint32_t extra_flags);
+}  // namespace
+
 fadam_status fadam_step(fadam_plan* plan, int32_t* noop_dev, fadam_stream stream) {
+  return step_launch(plan, noop_dev, stream, 0u);
+}
+
+namespace {
+fadam_status step_launch(fadam_plan* plan, int32_t* noop_dev, fadam_stream stream,
+                         uint32_t extra_flags) {
   if (!plan) return fail(FADAM_EINVAL, "plan is NULL");
   const HostPlan& hp = plan->hp;
   if ((hp.flags & FADAM_CHECK_FINITE) && !noop_dev)
@@ -666,13 +697,17 @@ fadam_status fadam_step(fadam_plan* plan, int32_t* noop_dev, fadam_stream stream
     return fail(FADAM_EINVAL, "a scaled-state plan needs fadam_plan_set_state_scales first");
   KParams kp;
   fill_params(kp, plan->d_items, plan->d_cta, plan->d_chunks, static_cast<int32_t>(hp.chunks.size()),
-              noop_dev, plan->d_scratch, plan->groups.data(), plan->n_groups, hp.flags);
+              noop_dev, plan->d_scratch, plan->groups.data(), plan->n_groups,
+              hp.flags | extra_flags);
   fill_exchange(kp, plan);
   fill_scaled(kp, plan);
   kp.n_sources = 0;  // the plain step reads g as it stands
+  kp.host_g = plan->d_host_g;
+  kp.dev_g = plan->d_dev_g;
   return launch(hp.kernel, hp.smem, kp, hp.grid, (hp.flags & FADAM_CHECK_FINITE) != 0 || scaled,
                 reinterpret_cast<cudaStream_t>(stream));
 }
+}  // namespace
 
 fadam_status fadam_plan_set_state_scales(fadam_plan* plan, float* scales_dev) {
   t_last_error.clear();
@@ -784,14 +819,40 @@ fadam_status fadam_step_host_grads(fadam_plan* plan, const void* const* g_host, 
       return fail(FADAM_EINVAL, "g_host[%zu] is NULL", i);
   DeviceGuard guard(hp.device);
   if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
-  for (size_t i = 0; i < plan->tensors.size(); ++i) {
-    const fadam_tensor& t = plan->tensors[i];
-    if (t.numel <= 0) continue;
-    const cudaError_t e = cudaMemcpyAsync(const_cast<void*>(t.g), g_host[i], size_t(t.numel) * gsz,
-                                          cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(e, "gradient upload");
+  // zero copy when every host gradient is page-locked and mapped for this
+  // device: the update reads it over the host link itself, so the transfer
+  // and the update of the other streams overlap
+  bool mapped = any && plan->d_host_g != nullptr;
+  for (size_t i = 0; mapped && i < plan->tensors.size(); ++i) {
+    plan->host_g[i] = nullptr;
+    if (plan->tensors[i].numel <= 0) continue;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, g_host[i]) != cudaSuccess || a.type != cudaMemoryTypeHost ||
+        a.devicePointer == nullptr || reinterpret_cast<uintptr_t>(a.devicePointer) % 16 !=
+                                          reinterpret_cast<uintptr_t>(plan->tensors[i].g) % 16) {
+      cudaGetLastError();  // clear the query's error for unregistered memory
+      mapped = false;
+      break;
+    }
+    plan->host_g[i] = static_cast<const char*>(a.devicePointer);
   }
-  fadam_status st = fadam_step(plan, noop_dev, stream);
+  fadam_status st = FADAM_OK;
+  if (mapped) {
+    const cudaError_t e = cudaMemcpyAsync(plan->d_host_g, plan->host_g.data(),
+                                          plan->host_g.size() * sizeof(char*),
+                                          cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "host gradient table upload");
+    st = step_launch(plan, noop_dev, stream, kHostGrads);
+  } else {
+    for (size_t i = 0; i < plan->tensors.size(); ++i) {
+      const fadam_tensor& t = plan->tensors[i];
+      if (t.numel <= 0) continue;
+      const cudaError_t e = cudaMemcpyAsync(const_cast<void*>(t.g), g_host[i],
+                                            size_t(t.numel) * gsz, cudaMemcpyHostToDevice, s);
+      if (e != cudaSuccess) return cuda_fail(e, "gradient upload");
+    }
+    st = fadam_step(plan, noop_dev, stream);
+  }
   if (st) return st;
   if (steps_host) {
     for (int32_t g = 0; g < plan->n_groups; ++g) {

@@ -312,11 +312,9 @@ def run_gpu(args):
                                        seed=1237 + 1000 * rank, state_dtype=torch.bfloat16,
                                        g_dtype=torch.bfloat16)
     elif args.workload == "scaled_state_shard":
-        spec = workloads.scaled_versions(full=True)["scaled_state_shard"]
-        spec.seed += 1000 * rank
+        spec = workloads.scaled_state_shard(layers=args.layers or 8, seed=1241 + 1000 * rank)
     elif args.workload == "exchange_shard":
-        spec = workloads.exchange_versions(full=True)["exchange_shard"]
-        spec.seed += 1000 * rank
+        spec = workloads.exchange_shard(layers=args.layers or 8, seed=1240 + 1000 * rank)
     elif args.workload == "many_small" and args.n_tensors:
         spec = workloads.many_small(n_tensors=args.n_tensors, seed=1239 + 1000 * rank)
     else:
@@ -415,8 +413,9 @@ def run_gpu(args):
         e2e = {"value": agg["gbs"], "unit": "GB/s", "ms_per_step": sec * 1e3,
                "h2d_bytes_per_step": int(sum(g.numel() * g.element_size() for g in host)),
                "d2h_bytes_per_step": 4 * len(groups),
-               "path": "fadam_step_host_grads: pinned host grads -> device, one launch, "
-                       "step counter -> host, stream sync"}
+               "path": "fadam_step_host_grads: pinned host grads read in place by the update "
+                       "(zero copy over the host link, overlapping the p/m/v traffic), one "
+                       "launch, step counter -> host, stream sync"}
         del host
 
     head = (res.get("exchange") or res.get("capturable") or res.get("regular")
@@ -478,6 +477,8 @@ def main(argv=None):
     ap.add_argument("--n-tensors", type=int, default=None,
                     help="tensor count of large_uniform[_bf16_state] (201) or many_small (20000)")
     ap.add_argument("--numel", type=int, default=320 * 65536)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="layers of the exchange_shard / scaled_state_shard layer list (8)")
     ap.add_argument("--variants", default="capturable,regular,graph,check_finite,norm,e2e",
                     help="also exchange,reduce on the exchange_shard workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")

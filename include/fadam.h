@@ -220,11 +220,16 @@ fadam_status fadam_plan_set_groups(fadam_plan* plan, const fadam_group* groups,
  * Errors: FADAM_EINVAL, FADAM_EALIGN, FADAM_ECUDA (launch failed). */
 fadam_status fadam_step(fadam_plan* plan, int32_t* noop_dev, fadam_stream stream);
 
-/* End-to-end step from host gradients: for every tensor, copies
- * g_host[i] (a host buffer of numel elements of the g dtype; pinned memory
- * makes the copy asynchronous) into the tensor's device g, runs
- * fadam_step(), copies each group's step counter into steps_host[n_groups]
- * (may be NULL), and waits for the stream.  Errors: as fadam_step. */
+/* End-to-end step from host gradients g_host[i] (a host buffer of numel
+ * elements of the g dtype per tensor).  When every buffer is page-locked and
+ * mapped for the device (cudaHostAlloc / cudaHostRegister, or torch's
+ * pin_memory), with the same address alignment modulo 16 bytes as the
+ * tensor's device g, the step reads the gradients over the host link
+ * itself (zero copy: the transfer overlaps the update of p, m and v, and
+ * the tensors' device g buffers are not written).  Otherwise each buffer is
+ * copied into the tensor's device g first (cudaMemcpyAsync) and fadam_step()
+ * runs.  Then each group's step counter is copied into steps_host[n_groups]
+ * (may be NULL), and the call waits for the stream.  Errors: as fadam_step. */
 fadam_status fadam_step_host_grads(fadam_plan* plan, const void* const* g_host,
                                    int32_t* noop_dev, int32_t* steps_host,
                                    fadam_stream stream);

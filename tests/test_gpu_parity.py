@@ -274,18 +274,53 @@ def test_step_once_regular_and_capturable():
             assert step_dev.item() == 2
 
 
-def test_host_gradients_entry_point_matches_device_gradients():
-    spec = workloads.small_versions()["capturable_l2"]
-    a, _, _ = _run(spec, 2, fresh=False)
+@pytest.mark.parametrize("name", ["capturable_l2", "remainder_shard", "many_small"])
+def test_host_gradients_entry_point_matches_device_gradients(name):
+    """Pinned host gradients are read in place (zero copy) by every item
+    form: bf16 grads with a param-out copy, the remainder form, and the
+    many-small shard's ragged and unaligned tensors."""
+    spec = workloads.small_versions()[name]
+    a, _, _ = _run(spec, 2, capturable=True, fresh=False)
     b = workloads.materialize(spec, DEV)
-    ob = FusedAdamShard(b.param_groups(), capturable=True, grad_scale=spec.grad_scale)
+    ob = FusedAdamShard(b.param_groups(), capturable=True, grad_scale=spec.grad_scale,
+                        remainders=spec.remainders)
     host = [g.cpu().pin_memory() for g in (b.grads[i] for i in b.plan_order())]
     for gr in b.grads:
         gr.zero_()  # the host copy is the only source of the grads
     steps = [ob.step_from_host(host) for _ in range(2)]
+    assert steps == [[1] * len(spec.groups), [2] * len(spec.groups)]
+    for x, y in zip(helpers.snapshot(a), helpers.snapshot(b)):
+        assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("memory", ["pageable", "misaligned_pinned"])
+def test_host_gradients_copy_path(memory):
+    """Host gradients that cannot be read in place (pageable, or pinned at
+    another 16-byte alignment than the device gradient) are copied in
+    first; the result is the same, and the device gradients hold them."""
+    spec = workloads.small_versions()["capturable_l2"]
+    a, _, _ = _run(spec, 2, fresh=False)
+    b = workloads.materialize(spec, DEV)
+    ob = FusedAdamShard(b.param_groups(), capturable=True, grad_scale=spec.grad_scale)
+    if memory == "pageable":
+        host = [g.cpu() for g in (b.grads[i] for i in b.plan_order())]
+    else:
+        host = []
+        for i in b.plan_order():
+            g = b.grads[i]
+            buf = torch.empty(g.numel() + 8, dtype=g.dtype).pin_memory()
+            view = buf[1:1 + g.numel()]  # 2 bytes off the pinned allocation's alignment
+            view.copy_(g.cpu())
+            host.append(view)
+    want = [g.clone() for g in b.grads]
+    for gr in b.grads:
+        gr.zero_()
+    steps = [ob.step_from_host(host) for _ in range(2)]
     assert steps == [[1], [2]]
     for x, y in zip(helpers.snapshot(a), helpers.snapshot(b)):
         assert torch.equal(x, y)
+    for g, w in zip(b.grads, want):
+        assert torch.equal(g, w)  # the copy path filled the device gradients
 
 
 def test_abi_rejects_bad_calls_without_launching():
