@@ -116,13 +116,14 @@ template <int DT>
 __device__ __forceinline__ void widen4(const typename Raw4<DT>::T& r, float (&o)[4]) {
   if constexpr (DT == FADAM_DT_F32) {
     o[0] = r.x; o[1] = r.y; o[2] = r.z; o[3] = r.w;
+  } else if constexpr (DT == FADAM_DT_BF16) {
+    // a bf16 is the top half of its float: one shift or one mask per value
+    o[0] = __uint_as_float(r.x << 16); o[1] = __uint_as_float(r.x & 0xFFFF0000u);
+    o[2] = __uint_as_float(r.y << 16); o[3] = __uint_as_float(r.y & 0xFFFF0000u);
   } else {
-    const unsigned short h0 = r.x & 0xFFFFu, h1 = r.x >> 16, h2 = r.y & 0xFFFFu, h3 = r.y >> 16;
-    if constexpr (DT == FADAM_DT_BF16) {
-      o[0] = bf16_to_f32(h0); o[1] = bf16_to_f32(h1); o[2] = bf16_to_f32(h2); o[3] = bf16_to_f32(h3);
-    } else {
-      o[0] = f16_to_f32(h0); o[1] = f16_to_f32(h1); o[2] = f16_to_f32(h2); o[3] = f16_to_f32(h3);
-    }
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&r.y));
+    o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
   }
 }
 
@@ -146,16 +147,26 @@ __device__ __forceinline__ unsigned short narrow(float x) {
   }
 }
 
+// Two floats rounded to dtype DT (nearest-even) in one 32-bit word, the
+// first in the low half: one paired conversion instead of two and a pack.
+template <int DT>
+__device__ __forceinline__ unsigned narrow2(float lo, float hi) {
+  if constexpr (DT == FADAM_DT_BF16) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const unsigned*>(&h);
+  } else {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const unsigned*>(&h);
+  }
+}
+
 // 4 floats rounded to dtype DT (nearest-even for 16-bit types).
 template <int DT>
 __device__ __forceinline__ typename Raw4<DT>::T pack_out4(const float (&x)[4]) {
   if constexpr (DT == FADAM_DT_F32) {
     return make_float4(x[0], x[1], x[2], x[3]);
   } else {
-    uint2 w;
-    w.x = static_cast<unsigned>(narrow<DT>(x[0])) | (static_cast<unsigned>(narrow<DT>(x[1])) << 16);
-    w.y = static_cast<unsigned>(narrow<DT>(x[2])) | (static_cast<unsigned>(narrow<DT>(x[3])) << 16);
-    return w;
+    return make_uint2(narrow2<DT>(x[0], x[1]), narrow2<DT>(x[2], x[3]));
   }
 }
 
