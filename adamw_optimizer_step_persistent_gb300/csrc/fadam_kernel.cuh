@@ -14,7 +14,7 @@
 //      chunks of up to kChunkTiles tiles that the CTAs pull from one
 //      launch-wide counter (so an SM that gets more bandwidth takes more
 //      chunks).  In each CTA thread 0 copies the tiles of p, m, v, g (and
-//      the remainders) into shared memory with cp.async.bulk, kStages tiles
+//      the remainders) into shared memory with cp.async.bulk, 2-3 tiles
 //      ahead and across chunk boundaries, each tile completing on its own
 //      mbarrier; every thread updates one vector of the tile from shared
 //      memory and writes the results straight to global memory with
@@ -367,11 +367,23 @@ __device__ __forceinline__ void update4_rem(const uint2& H, const uint2& R, floa
 #ifndef FADAM_BULK
 #define FADAM_BULK 1
 #endif
+// Tiles in flight per CTA: up to kMaxStages, as many as fit in
+// kStageBudget bytes of dynamic shared memory (at least two).  Three 64 KB
+// stages and the static shared memory fit the 227 KB a CTA may use; with
+// one 1024-thread CTA per SM (the register file allows no second one) that
+// space would otherwise sit idle.  Layouts with larger tiles keep two.
 #ifndef FADAM_STAGES
-#define FADAM_STAGES 2
+#define FADAM_STAGES 3
 #endif
-constexpr int kStages = FADAM_STAGES;
+constexpr int kMaxStages = FADAM_STAGES;
+constexpr unsigned kStageBudget = 192u * 1024u;
 constexpr int kTile = kBlock;  // vectors per tile: one per thread
+
+// Vectors of one tile a thread has in flight at once (the tile loop's unroll).
+#ifndef FADAM_VEC_UNROLL
+#define FADAM_VEC_UNROLL 2
+#endif
+constexpr int kVecUnroll = FADAM_VEC_UNROLL;
 
 template <int DT>
 __host__ __device__ constexpr int vec_bytes() { return DT == FADAM_DT_F32 ? 16 : 8; }
@@ -400,11 +412,23 @@ struct Layout {
   static constexpr int scan_vectors = scan_per_thread * kTile;
   static constexpr unsigned scan_tile = scan_vectors * kG;
   static constexpr unsigned stage = update_tile > scan_tile ? update_tile : scan_tile;
+  // buffers of the pipeline that fit the budget (at least two)
+  static constexpr int stages = kStageBudget / stage >= unsigned(kMaxStages) ? kMaxStages : 2;
 };
 
-template <int ST, int GT, bool REM>
+// Pipeline buffers of one kernel instance; every pass of an instance uses
+// the same count, so the stage counter carries from pass to pass.  The
+// scaled-state instances keep two: their spilled registers live in L1,
+// which shares the SM's memory with these buffers, and a third 64 KB stage
+// cost them more than it gained.
+template <int ST, int GT, bool REM, bool SCALED>
+__host__ __device__ constexpr int pipeline_stages() {
+  return SCALED ? 2 : Layout<ST, GT, REM>::stages;
+}
+
+template <int ST, int GT, bool REM, bool SCALED = false>
 __host__ __device__ constexpr size_t smem_bytes() {
-  return FADAM_BULK ? size_t(kStages) * Layout<ST, GT, REM>::stage : 0;
+  return FADAM_BULK ? size_t(pipeline_stages<ST, GT, REM, SCALED>()) * Layout<ST, GT, REM>::stage : 0;
 }
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -490,12 +514,12 @@ __host__ __device__ constexpr int tile_vectors() {
 }
 
 // Thread 0 of the CTA: start the copies of vectors [v0, v0 + len) of `it`
-// into buffer `slot % kStages`.
-template <int ST, int GT, bool REM, Pass PASS>
+// into buffer `slot % NS` (NS: the instance's pipeline stages).
+template <int ST, int GT, bool REM, Pass PASS, int NS>
 __device__ __forceinline__ void issue_tile(const KParams& kp, const Item& it, int v0, unsigned len,
                                            unsigned slot, unsigned char* smem, uint64_t* full) {
   using L = Layout<ST, GT, REM>;
-  const unsigned b = slot % kStages;
+  const unsigned b = slot % NS;
   unsigned char* st = smem + size_t(b) * L::stage;
   uint64_t* bar = full + b;
   const size_t v = static_cast<size_t>(v0);
@@ -522,7 +546,7 @@ __device__ __forceinline__ void issue_tile(const KParams& kp, const Item& it, in
 
 // The producer side of the pipeline, kept by thread 0 only: it pulls chunks
 // of tiles from the launch-wide counter (so faster SMs take more of them)
-// and copies their tiles kStages ahead of the consumers, announcing each
+// and copies their tiles Layout::stages ahead of the consumers, announcing each
 // tile's (item, tile) in a small shared ring before its copies start.  When
 // the chunks run out it announces the end with an arrival that carries no
 // bytes.  The g-only passes take chunks in batches of consecutive indices,
@@ -593,7 +617,7 @@ __device__ __forceinline__ bool next_batch(Producer& pr, const KParams& kp, unsi
   return true;
 }
 
-template <int ST, int GT, bool REM, Pass PASS>
+template <int ST, int GT, bool REM, Pass PASS, int NS>
 __device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, unsigned* counter,
                                              unsigned char* smem, uint64_t* full, TileTag* tags) {
   if (pr.finished) return;
@@ -602,7 +626,7 @@ __device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, un
     // CTAs on neighbouring chunks; the g-only passes' chunks are 2-4 tiles
     if (pr.next >= pr.batch_end &&
         !next_batch(pr, kp, counter, update_like(PASS) ? 1 : kBatchMax)) {
-      const unsigned b = pr.slot % kStages;
+      const unsigned b = pr.slot % NS;
       tags[b] = TileTag{-1, 0, 0, -1};
       mbar_arrive(full + b);  // completes the phase with no copy
       ++pr.slot;
@@ -624,13 +648,13 @@ __device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, un
   if constexpr (PASS == Pass::kReduce) tv = reduce_vectors<ST, GT, REM>(kp.n_sources);
   else tv = tile_vectors<ST, GT, REM, PASS>();
   const int len = min(tv, pr.vend - pr.v);
-  TileTag& tg = tags[pr.slot % kStages];
+  TileTag& tg = tags[pr.slot % NS];
   tg.item = pr.item;
   tg.v0 = pr.v;
   tg.len = len;
   tg.chunk = pr.chunk;
   if constexpr (PASS == Pass::kScaledA || PASS == Pass::kScaledB) tg.sc = pr.sc;
-  issue_tile<ST, GT, REM, PASS>(kp, pr.it, pr.v, static_cast<unsigned>(len), pr.slot, smem, full);
+  issue_tile<ST, GT, REM, PASS, NS>(kp, pr.it, pr.v, static_cast<unsigned>(len), pr.slot, smem, full);
   pr.v += len;
   ++pr.slot;
 }
@@ -644,7 +668,10 @@ __device__ __forceinline__ void update_tile(const Item& it, const Scal& s, const
                                             const StateScale* sc = nullptr, unsigned* mx = nullptr) {
   const Dests d{DESTS ? d0.n : 0, d0.delta};
   using L = Layout<ST, GT, REM>;
-#pragma unroll
+  // the scaled passes take their vectors one at a time: interleaving two
+  // spills more of their larger working set than it hides
+  constexpr int kU = (PASS == Pass::kScaledA || PASS == Pass::kScaledB) ? 1 : kVecUnroll;
+#pragma unroll kU
   for (int q = 0; q < L::update_vectors / kTile; ++q) {
     const int t = threadIdx.x + q * kTile;
     if (t >= len) return;
@@ -852,19 +879,37 @@ __device__ __forceinline__ double cta_sum(double x, double* red) {
 }
 
 // The per-chunk reduction rides on the bulk pipeline's one CTA barrier per
-// tile.  When a chunk ends, each warp reduces its threads' sums (float sums
-// in float, five roundings; the double parts only when the warp holds one)
-// into red[warp] of one of two buffers; after the next barrier warp 0 adds
-// the 32 warp partials in double, in a fixed order, into the chunk's slot.
-// The buffers alternate, so a chunk that ends in the following tile writes
-// the other one while warp 0 still reads.  The result does not depend on
-// which CTA took which chunk.
+// tile.  When a chunk ends, each warp reduces its threads' float sums in
+// float (five roundings) into f[warp] of one of two buffers, and its double
+// parts into d[warp] (zero unless some thread of the warp holds one); after
+// the next barrier warp 0 adds the 32 warp partials, again in float and in
+// a fixed order, and folds in the double parts and grad_scale^2 in double,
+// into the chunk's slot.  Every partial is a sum of squares (nonnegative),
+// so each of these roundings adds at most 2^-24 of the chunk's sum.  The
+// double arithmetic stays with one thread per chunk: this GPU's FP64 rate
+// is a small fraction of its FP32 rate, and 32 warps converting and adding
+// in double at every close held the whole CTA at the next barrier.  The
+// buffers alternate, so a chunk that ends in the following tile writes the
+// other one while warp 0 still reads.  The result does not depend on which
+// CTA took which chunk.
 struct NormPending {
   int chunk;  // -1: nothing to publish
   float gs;
 };
 
-__device__ __forceinline__ void norm_warp_close(NormAcc& na, double* red_buf, double* dpart) {
+struct NormBuf {
+  float* f;
+  double* d;
+};
+
+// Buffer k % 2 of the warp partials in `red` (3 * kBlock / 32 doubles: the
+// two double halves, then the two float halves).
+__device__ __forceinline__ NormBuf norm_buf(double* red, unsigned k) {
+  constexpr int W = kBlock / 32;
+  return NormBuf{reinterpret_cast<float*>(red + 2 * W) + (k & 1u) * W, red + (k & 1u) * W};
+}
+
+__device__ __forceinline__ void norm_warp_close(NormAcc& na, const NormBuf& buf, double* dpart) {
   float xf = na.sum;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) xf = __fadd_rn(xf, __shfl_xor_sync(0xffffffffu, xf, o));
@@ -877,21 +922,29 @@ __device__ __forceinline__ void norm_warp_close(NormAcc& na, double* red_buf, do
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) xd += __shfl_xor_sync(0xffffffffu, xd, o);
   }
-  if ((threadIdx.x & 31) == 0) red_buf[threadIdx.x / 32] = static_cast<double>(xf) + xd;
+  if ((threadIdx.x & 31) == 0) {
+    buf.f[threadIdx.x / 32] = xf;
+    buf.d[threadIdx.x / 32] = xd;
+  }
   na.sum = 0.0f;
   na.comp = 0.0f;
   na.has_d = false;
 }
 
 // Warp 0, after a CTA barrier that follows every warp's norm_warp_close.
-__device__ __forceinline__ void norm_publish(const double* red_buf, float gs, double* slot) {
+__device__ __forceinline__ void norm_publish(const NormBuf& buf, float gs, double* slot) {
   if (threadIdx.x < 32) {
-    double y = red_buf[threadIdx.x];
+    float y = buf.f[threadIdx.x];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+    for (int o = 16; o > 0; o >>= 1) y = __fadd_rn(y, __shfl_xor_sync(0xffffffffu, y, o));
+    double yd = buf.d[threadIdx.x];
+    if (__any_sync(0xffffffffu, __double_as_longlong(yd) != 0)) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) yd += __shfl_xor_sync(0xffffffffu, yd, o);
+    }
     // thread 0 writes every chunk slot; its fence before the completion
     // count at the end of the launch publishes them all
-    if (threadIdx.x == 0) *slot = static_cast<double>(gs) * gs * y;
+    if (threadIdx.x == 0) *slot = static_cast<double>(gs) * gs * (static_cast<double>(y) + yd);
   }
 }
 
@@ -903,7 +956,7 @@ __device__ __forceinline__ void norm_tile(const unsigned char* st, const TileTag
                                           double* dpart, unsigned& closes, NormPending& pend) {
   if (tag.chunk != na.chunk) {
     if (na.chunk >= 0) {
-      norm_warp_close(na, red + (closes & 1u) * (kBlock / 32), dpart);
+      norm_warp_close(na, norm_buf(red, closes), dpart);
       pend = NormPending{na.chunk, sgrp[na.group].gs};
       ++closes;
     }
@@ -943,7 +996,7 @@ __device__ __forceinline__ void norm_tile(const unsigned char* st, const TileTag
 // of the next chunk start while the current one is consumed).  `bad`
 // collects the scan's finding; a wait that gives up sets `timed_out` and
 // ends the pass for the CTA.
-template <int ST, int GT, int OT, bool REM, Pass PASS>
+template <int ST, int GT, int OT, bool REM, Pass PASS, int NS>
 __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp, unsigned* counter,
                                           unsigned char* smem, uint64_t* full, TileTag* tags,
                                           Producer& pr, double* red, unsigned& stage, bool& bad,
@@ -967,13 +1020,13 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
     pr.slot = stage;
     pr.finished = false;
     pr.next = pr.batch0 = pr.batch_end = 0;
-    for (int q = 0; q < kStages; ++q) produce_next<ST, GT, REM, PASS>(pr, kp, counter, smem, full, tags);
+    for (int q = 0; q < NS; ++q) produce_next<ST, GT, REM, PASS, NS>(pr, kp, counter, smem, full, tags);
   }
   int cur_item = -1;
   Item it;
   for (;; ++stage) {
-    const unsigned b = stage % kStages;
-    bool ok = mbar_wait(full + b, (stage / kStages) & 1u);
+    const unsigned b = stage % NS;
+    bool ok = mbar_wait(full + b, (stage / NS) & 1u);
     // the norm's chunk closes and the absmax flushes are warp-wide: one
     // decision per warp
     if constexpr (PASS == Pass::kNorm || PASS == Pass::kScaledA) ok = __all_sync(0xffffffffu, ok);
@@ -1023,7 +1076,7 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
     }
     if constexpr (PASS == Pass::kNorm) {
       if (pend.chunk >= 0) {
-        norm_publish(red + ((closes - 1u) & 1u) * (kBlock / 32), pend.gs, kp.partials + pend.chunk);
+        norm_publish(norm_buf(red, closes - 1u), pend.gs, kp.partials + pend.chunk);
         pend.chunk = -1;
       }
     }
@@ -1033,7 +1086,7 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
         if (cur_item >= 0) flush_absmax(kp, it.tensor, mx);
       if constexpr (PASS == Pass::kNorm) {
         if (na.chunk >= 0) {
-          double* buf = red + (closes & 1u) * (kBlock / 32);
+          const NormBuf buf = norm_buf(red, closes);
           norm_warp_close(na, buf, dpart);
           __syncthreads();
           norm_publish(buf, sgrp[na.group].gs, kp.partials + na.chunk);
@@ -1044,7 +1097,7 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
     if (threadIdx.x == 0) {
       // order the generic-proxy reads of the buffer before its async refill
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      produce_next<ST, GT, REM, PASS>(pr, kp, counter, smem, full, tags);
+      produce_next<ST, GT, REM, PASS, NS>(pr, kp, counter, smem, full, tags);
     }
   }
 }
@@ -1310,7 +1363,7 @@ __device__ __forceinline__ bool rest_pass(const KParams& kp, const SGroup* sgrp,
 
 // One full pass: the bulk tiles of the shard (dynamically shared), then
 // the rest of this CTA's items.
-template <int ST, int GT, int OT, bool REM, Pass PASS>
+template <int ST, int GT, int OT, bool REM, Pass PASS, int NS>
 __device__ __forceinline__ void run_pass(const KParams& kp, const SGroup* sgrp, int item_begin,
                                          int item_end, unsigned* counter, unsigned* tail_counter,
                                          int n_items, unsigned char* smem, uint64_t* full,
@@ -1318,7 +1371,7 @@ __device__ __forceinline__ void run_pass(const KParams& kp, const SGroup* sgrp, 
                                          unsigned& stage, bool& bad, bool& timed_out) {
   const bool bulk = FADAM_BULK && !(kp.flags & kHostGrads);
   if (bulk && kp.n_chunks > 0 && !timed_out)
-    bulk_pass<ST, GT, OT, REM, PASS>(kp, sgrp, counter, smem, full, tags, pr, red, stage, bad,
+    bulk_pass<ST, GT, OT, REM, PASS, NS>(kp, sgrp, counter, smem, full, tags, pr, red, stage, bad,
                                      timed_out);
   if (bulk) bad |= tail_pass<ST, GT, OT, REM, PASS>(kp, sgrp, tail_counter, n_items);
   bad |= rest_pass<ST, GT, OT, REM, PASS>(kp, sgrp, item_begin, item_end, red);
@@ -1367,11 +1420,12 @@ template <int ST, int GT, int OT, bool REM, bool SCALED = false>
 __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams kp) {
   __shared__ SGroup sgrp[FADAM_MAX_GROUPS];
   __shared__ int s_noop;
-  __shared__ __align__(8) uint64_t s_full[kStages];
-  __shared__ TileTag s_tags[kStages];
+  __shared__ __align__(8) uint64_t s_full[kMaxStages];
+  __shared__ TileTag s_tags[kMaxStages];
   __shared__ Producer s_prod;  // used by thread 0 only
-  __shared__ double s_red[2 * (kBlock / 32)];  // norm launches: partials per warp
+  __shared__ double s_red[3 * (kBlock / 32)];  // norm launches: partials per warp
   extern __shared__ __align__(128) unsigned char s_tiles[];
+  constexpr int NS = pipeline_stages<ST, GT, REM, SCALED>();
   const bool capturable = (kp.flags & kCapturable) != 0;
   const int tid = threadIdx.x;
 
@@ -1379,7 +1433,7 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
   if (tid == 0) {
     s_noop = kp.noop ? (__ldcg(kp.noop) == 1) : 0;  // only 1 means set
     if (FADAM_BULK) {
-      for (int b = 0; b < kStages; ++b) mbar_init(&s_full[b], 1);
+      for (int b = 0; b < NS; ++b) mbar_init(&s_full[b], 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
   }
@@ -1405,7 +1459,9 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
       s.step_old = G.step;
       step = G.step;
     }
-    if (G.bits & kGroupBiasCorr) {
+    // launches that only read g (norm, reduction) skip the double pow:
+    // this GPU's FP64 rate makes it a few microseconds per CTA
+    if ((G.bits & kGroupBiasCorr) && !(kp.flags & (kNormOnly | kReduceOnly))) {
       s.bc1 = static_cast<float>(1.0 - pow(static_cast<double>(G.beta1), static_cast<double>(step)));
       s.bc2 = static_cast<float>(1.0 - pow(static_cast<double>(G.beta2), static_cast<double>(step)));
     } else {
@@ -1428,7 +1484,7 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
     // chunk of tiles and per item (tails, unaligned items), summed by the
     // last CTA below in a fixed order
     bool unused = false;
-    run_pass<ST, GT, OT, REM, Pass::kNorm>(kp, sgrp, item_begin, item_end, &kp.scratch->next_scan,
+    run_pass<ST, GT, OT, REM, Pass::kNorm, NS>(kp, sgrp, item_begin, item_end, &kp.scratch->next_scan,
                                            &kp.scratch->next_tail_scan, n_items, s_tiles, s_full,
                                            s_tags, s_prod, s_red, stage, unused, timed_out);
   }
@@ -1441,7 +1497,7 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
   const bool updates = !norm_only && !reduce_only;
   if (reduce_only || reduce_first) {
     bool bad = false;
-    run_pass<ST, GT, OT, REM, Pass::kReduce>(kp, sgrp, item_begin, item_end, &kp.scratch->next_scan,
+    run_pass<ST, GT, OT, REM, Pass::kReduce, NS>(kp, sgrp, item_begin, item_end, &kp.scratch->next_scan,
                                              &kp.scratch->next_tail_scan, n_items, s_tiles, s_full,
                                              s_tags, s_prod, s_red, stage, bad, timed_out);
     // the update copies g with the async proxy: order this thread's
@@ -1462,7 +1518,7 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
   if (updates && !reduce_first && (kp.flags & kCheckFinite)) {
     bool bad = false;
     if (!s_noop)
-      run_pass<ST, GT, OT, REM, Pass::kScan>(kp, sgrp, item_begin, item_end, &kp.scratch->next_scan,
+      run_pass<ST, GT, OT, REM, Pass::kScan, NS>(kp, sgrp, item_begin, item_end, &kp.scratch->next_scan,
                                          &kp.scratch->next_tail_scan, n_items, s_tiles, s_full,
                                          s_tags, s_prod, s_red, stage, bad, timed_out);
     if (__syncthreads_or(bad) && tid == 0) atomicExch(kp.noop, 1);
@@ -1477,21 +1533,21 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
   if (updates && !s_noop && barrier_ok) {
     bool unused = false;
     if constexpr (SCALED) {
-      run_pass<ST, GT, OT, REM, Pass::kScaledA>(kp, sgrp, item_begin, item_end,
+      run_pass<ST, GT, OT, REM, Pass::kScaledA, NS>(kp, sgrp, item_begin, item_end,
                                                 &kp.scratch->next_update,
                                                 &kp.scratch->next_tail_update, n_items, s_tiles,
                                                 s_full, s_tags, s_prod, s_red, stage, unused,
                                                 timed_out);
       barrier_ok = grid_barrier(kp.scratch, 0u);
       if (barrier_ok)
-        run_pass<ST, GT, OT, REM, Pass::kScaledB>(kp, sgrp, item_begin, item_end,
+        run_pass<ST, GT, OT, REM, Pass::kScaledB, NS>(kp, sgrp, item_begin, item_end,
                                                   &kp.scratch->next_rescale,
                                                   &kp.scratch->next_tail_rescale, n_items, s_tiles,
                                                   s_full, s_tags, s_prod, s_red, stage, unused,
                                                   timed_out);
       scaled_done = barrier_ok;
     } else {
-      run_pass<ST, GT, OT, REM, Pass::kUpdate>(kp, sgrp, item_begin, item_end,
+      run_pass<ST, GT, OT, REM, Pass::kUpdate, NS>(kp, sgrp, item_begin, item_end,
                                                &kp.scratch->next_update,
                                                &kp.scratch->next_tail_update, n_items, s_tiles,
                                                s_full, s_tags, s_prod, s_red, stage, unused,
@@ -1579,7 +1635,7 @@ KernelEntry kernel_for(int out_dtype, bool remainders) {
 // combination; the state dtype is bf16 or fp16.
 template <int ST, int GT>
 KernelEntry scaled_kernel_for(int out_dtype) {
-  const size_t smem = smem_bytes<ST, GT, false>();
+  const size_t smem = smem_bytes<ST, GT, false, true>();
   switch (out_dtype) {
     case FADAM_DT_NONE:
       return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_NONE, false, true>), smem};

@@ -315,6 +315,8 @@ def run_gpu(args):
         spec = workloads.scaled_state_shard(layers=args.layers or 8, seed=1241 + 1000 * rank)
     elif args.workload == "exchange_shard":
         spec = workloads.exchange_shard(layers=args.layers or 8, seed=1240 + 1000 * rank)
+    elif args.workload == "capturable_l2" and args.layers:
+        spec = workloads.capturable_l2(layers=args.layers, seed=1236 + 1000 * rank)
     elif args.workload == "many_small" and args.n_tensors:
         spec = workloads.many_small(n_tensors=args.n_tensors, seed=1239 + 1000 * rank)
     else:
@@ -478,7 +480,8 @@ def main(argv=None):
                     help="tensor count of large_uniform[_bf16_state] (201) or many_small (20000)")
     ap.add_argument("--numel", type=int, default=320 * 65536)
     ap.add_argument("--layers", type=int, default=None,
-                    help="layers of the exchange_shard / scaled_state_shard layer list (8)")
+                    help="layers of the capturable_l2 / exchange_shard / scaled_state_shard "
+                         "layer list (8)")
     ap.add_argument("--variants", default="capturable,regular,graph,check_finite,norm,e2e",
                     help="also exchange,reduce on the exchange_shard workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
