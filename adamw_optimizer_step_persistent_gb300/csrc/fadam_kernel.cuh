@@ -784,6 +784,15 @@ __device__ __forceinline__ bool scan_tile(const unsigned char* st, int len, floa
   return bad;
 }
 
+// OR of the raw words of 4 elements (zero only when every element is +0).
+template <int DT>
+__device__ __forceinline__ unsigned raw_or4(const typename Raw4<DT>::T& r) {
+  if constexpr (DT == FADAM_DT_F32)
+    return __float_as_uint(r.x) | __float_as_uint(r.y) | __float_as_uint(r.z) | __float_as_uint(r.w);
+  else
+    return r.x | r.y;
+}
+
 // Sum of the squares of 4 widened values in float.  `special` is set when
 // that sum is outside the range where float serves (overflow, NaN, or
 // nonzero values whose squares underflow); such vectors are redone exactly
@@ -963,25 +972,44 @@ __device__ __forceinline__ void norm_tile(const unsigned char* st, const TileTag
     na.chunk = tag.chunk;
     na.group = group;
   }
-  // Squares summed with fused multiply-adds; the range test is made once on
-  // the thread's tile sum: overflow or NaN, or a tiny sum while some input
-  // is nonzero (squares that may have underflowed).  Either sends the
-  // thread's vectors of this tile to the exact path.
-  float f = 0.0f;
+  // Squares summed with fused multiply-adds in two independent chains (the
+  // thread's even and odd vectors), added once per tile; full tiles skip
+  // the per-vector bounds test.  The range test is made once on the
+  // thread's tile sum: overflow or NaN, or a tiny sum while some input is
+  // nonzero (squares that may have underflowed; the raw words are OR-ed
+  // and the sign bits masked off).  Either sends the thread's vectors of
+  // this tile to the exact path.
+  using R4 = typename Raw4<GT>::T;
+  const R4* src = reinterpret_cast<const R4*>(st);
+  float f2[2] = {0.0f, 0.0f};
   unsigned nz = 0u;
+  if (tag.len == Q * kTile) {
 #pragma unroll
-  for (int q = 0; q < Q; ++q) {  // Q = Layout::scan_per_thread
-    const int t = threadIdx.x + q * kTile;
-    if (t < tag.len) {
+    for (int q = 0; q < Q; ++q) {  // Q = Layout::scan_per_thread
+      const R4 r = src[threadIdx.x + q * kTile];
       float g[4];
-      widen4<GT>(reinterpret_cast<const typename Raw4<GT>::T*>(st)[t], g);
+      widen4<GT>(r, g);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) f = __fmaf_rn(g[e], g[e], f);
-      nz |= __float_as_uint(g[0]) | __float_as_uint(g[1]) | __float_as_uint(g[2]) |
-            __float_as_uint(g[3]);
+      for (int e = 0; e < 4; ++e) f2[q & 1] = __fmaf_rn(g[e], g[e], f2[q & 1]);
+      nz |= raw_or4<GT>(r);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      const int t = threadIdx.x + q * kTile;
+      if (t < tag.len) {
+        const R4 r = src[t];
+        float g[4];
+        widen4<GT>(r, g);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f2[q & 1] = __fmaf_rn(g[e], g[e], f2[q & 1]);
+        nz |= raw_or4<GT>(r);
+      }
     }
   }
-  const bool special = !(f <= 1e30f) || (f < 1e-30f && (nz & 0x7fffffffu) != 0u);
+  float f = __fadd_rn(f2[0], f2[1]);
+  const unsigned mag = GT == FADAM_DT_F32 ? 0x7fffffffu : 0x7fff7fffu;
+  const bool special = !(f <= 1e30f) || (f < 1e-30f && (nz & mag) != 0u);
   double d = 0.0;
   if (special) {
     const SqPart r = square_tile_exact<Q, GT>(st, tag.len);

@@ -33,6 +33,8 @@ constexpr double kItemOverhead = 4096.0;
 // Most chunks a plan's work list holds (chunks grow past kChunkTiles tiles
 // beyond that).
 constexpr int64_t kPlanMaxChunks = 65536;
+// Smallest chunk of the tapered end of a chunk list, in tiles.
+constexpr int64_t kTaperMinTiles = 4;
 // Largest tensor the library accepts, in elements.
 constexpr int64_t kMaxNumel = int64_t(1) << 40;
 
@@ -377,11 +379,18 @@ void fill_kgroups(const fadam_group* groups, int32_t n_groups, uint32_t flags, K
   }
 }
 
-// Chunks of bulk tiles for the dynamically shared bulk pass: kChunkTiles
-// tiles each, or more when that keeps the list within max_chunks.  An item
-// is bulk-copied when every stream is 16-byte aligned (kItemBulk); its
-// tiles cover its vectors rounded down to an even count.
-void build_chunks(const std::vector<Item>& items, int64_t max_chunks, std::vector<Chunk>& chunks) {
+// Chunks of bulk tiles for the dynamically shared bulk pass, in the order
+// the CTAs take them: kChunkTiles tiles each (or more when that keeps the
+// list within max_chunks), tapering towards the end of the list so that the
+// CTAs finish together: a chunk that starts with R tiles left in the list
+// gets about R / (2 grid) of them, down to kTaperMinTiles (guided
+// self-scheduling; smaller chunks would leave the g-only passes, which
+// read a chunk in tiles of 4-8 update tiles' worth of g, with partial
+// tiles).  The tapered list is used when it fits max_chunks.  An item is
+// bulk-copied when every stream is 16-byte aligned (kItemBulk); its tiles
+// cover its vectors rounded down to an even count.
+void build_chunks(const std::vector<Item>& items, int64_t max_chunks, int grid,
+                  std::vector<Chunk>& chunks) {
   int64_t total_tiles = 0;
   auto tiles_of = [](const Item& it) -> int64_t {
     if (!(it.flags & kItemBulk)) return 0;
@@ -395,12 +404,22 @@ void build_chunks(const std::vector<Item>& items, int64_t max_chunks, std::vecto
   for (const Item& it : items) bulk_items += tiles_of(it) > 0;
   const int64_t budget = std::max<int64_t>(1, max_chunks - bulk_items);
   per = std::max<int64_t>(per, (total_tiles + budget - 1) / budget);
-  chunks.clear();
-  for (size_t k = 0; k < items.size(); ++k) {
-    const int64_t nt = tiles_of(items[k]);
-    for (int64_t t = 0; t < nt; t += per)
-      chunks.push_back(Chunk{static_cast<int32_t>(k), static_cast<int32_t>(t),
-                             static_cast<int32_t>(std::min(per, nt - t)), 0});
+  for (int taper = 1; taper >= 0; --taper) {
+    chunks.clear();
+    int64_t left = total_tiles;  // tiles from the next chunk to the end
+    for (size_t k = 0; k < items.size(); ++k) {
+      const int64_t nt = tiles_of(items[k]);
+      for (int64_t t = 0; t < nt;) {
+        int64_t size = per;
+        if (taper) size = std::min(per, std::max<int64_t>(kTaperMinTiles, left / (2 * int64_t(grid))));
+        size = std::min(size, nt - t);
+        chunks.push_back(Chunk{static_cast<int32_t>(k), static_cast<int32_t>(t),
+                               static_cast<int32_t>(size), 0});
+        t += size;
+        left -= size;
+      }
+    }
+    if (int64_t(chunks.size()) <= max_chunks) return;
   }
 }
 
@@ -457,7 +476,7 @@ fadam_status prepare(const fadam_tensor* tensors, int64_t n_tensors, const fadam
     return fail(FADAM_ELIMIT, "more than 2^31 work items");
   hp.items.reserve(pitems.size());
   for (const PackItem& pi : pitems) hp.items.push_back(to_item(tensors[pi.tensor], pi, d));
-  build_chunks(hp.items, max_chunks, hp.chunks);
+  build_chunks(hp.items, max_chunks, hp.grid, hp.chunks);
   const double bpe = bytes_per_elem(d);
   for (int64_t i = 0; i < n_tensors; ++i) {
     const int64_t ne = std::max<int64_t>(tensors[i].numel, 0);
