@@ -712,20 +712,26 @@ __device__ __forceinline__ float stored_value(float x) {
   else return f16_to_f32(narrow<GT>(x));
 }
 
-// One tile: source r's vectors at r * stride in the stage.
-template <int ST, int GT, bool REM>
+// One tile: source r's vectors at r * stride in the stage.  R > 0: the
+// number of sources, fixed at compile time (the source loop unrolled, the
+// slice offsets constants); R == 0: kp.n_sources.  Either way the sources
+// are added in rank order.
+template <int ST, int GT, bool REM, int R>
 __device__ __forceinline__ bool reduce_tile(const KParams& kp, const Item& it,
                                             const unsigned char* st, int v0, int len, float gs,
                                             bool screen) {
   using L = Layout<ST, GT, REM>;
   using G4 = typename Raw4<GT>::T;
-  const size_t stride = size_t(reduce_vectors<ST, GT, REM>(kp.n_sources)) * L::kG;
-  const float rn = static_cast<float>(kp.n_sources);
+  const int nr = R > 0 ? R : kp.n_sources;
+  const size_t stride = size_t(reduce_vectors<ST, GT, REM>(nr)) * L::kG;
+  const float rn = static_cast<float>(nr);
   bool bad = false;
   for (int t = threadIdx.x; t < len; t += kBlock) {
     float acc[4];
     widen4<GT>(reinterpret_cast<const G4*>(st)[t], acc);
-    for (int r = 1; r < kp.n_sources; ++r) {
+#pragma unroll
+    for (int r = 1; r < (R > 0 ? R : FADAM_MAX_SOURCES); ++r) {
+      if (R == 0 && r >= nr) break;
       float x[4];
       widen4<GT>(reinterpret_cast<const G4*>(st + size_t(r) * stride)[t], x);
 #pragma unroll
@@ -752,6 +758,20 @@ __device__ __forceinline__ bool reduce_tile(const KParams& kp, const Item& it,
     }
   }
   return bad;
+}
+
+// The reduce tile for the launch's source count: common data-parallel
+// degrees get an unrolled instance, any other count the generic loop.
+template <int ST, int GT, bool REM>
+__device__ __forceinline__ bool reduce_tile_any(const KParams& kp, const Item& it,
+                                                const unsigned char* st, int v0, int len, float gs,
+                                                bool screen) {
+  switch (kp.n_sources) {
+    case 2: return reduce_tile<ST, GT, REM, 2>(kp, it, st, v0, len, gs, screen);
+    case 4: return reduce_tile<ST, GT, REM, 4>(kp, it, st, v0, len, gs, screen);
+    case 8: return reduce_tile<ST, GT, REM, 8>(kp, it, st, v0, len, gs, screen);
+    default: return reduce_tile<ST, GT, REM, 0>(kp, it, st, v0, len, gs, screen);
+  }
 }
 
 // One element, straight from global memory (tails, unaligned items).
@@ -1077,7 +1097,7 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
           norm_tile<Layout<ST, GT, REM>::scan_per_thread, GT>(st, tag, it.group, na, sgrp, red,
                                                               dpart, closes, pend);
         } else if constexpr (PASS == Pass::kReduce) {
-          bad |= reduce_tile<ST, GT, REM>(kp, it, st, tag.v0, tag.len, s.gs, screen);
+          bad |= reduce_tile_any<ST, GT, REM>(kp, it, st, tag.v0, tag.len, s.gs, screen);
         } else if constexpr (PASS == Pass::kScaledA || PASS == Pass::kScaledB) {
           const StateScale sc = tag.sc;
           if (G.bits & kGroupAdamW)

@@ -34,7 +34,10 @@ constexpr double kItemOverhead = 4096.0;
 // beyond that).
 constexpr int64_t kPlanMaxChunks = 65536;
 // Smallest chunk of the tapered end of a chunk list, in tiles.
-constexpr int64_t kTaperMinTiles = 4;
+#ifndef FADAM_TAPER_MIN_TILES
+#define FADAM_TAPER_MIN_TILES 4
+#endif
+constexpr int64_t kTaperMinTiles = FADAM_TAPER_MIN_TILES;
 // Largest tensor the library accepts, in elements.
 constexpr int64_t kMaxNumel = int64_t(1) << 40;
 
