@@ -78,6 +78,8 @@ SIGNATURES = [
     ("fadam_pack_dry", _i32, [ctypes.POINTER(Tensor), _i64, _i32, _i32, _i32, _i32, _u32, _i32,
                               ctypes.POINTER(PackItem), _i64, ctypes.POINTER(_i32),
                               ctypes.POINTER(_i64)]),
+    ("fadam_chunk_dry", _i32, [ctypes.POINTER(Tensor), _i64, _i32, _i32, _i32, _i32, _u32, _i32,
+                               _i64, ctypes.POINTER(_i32), _i64, ctypes.POINTER(_i64)]),
     ("fadam_step_noalloc", _i32, [ctypes.POINTER(Tensor), _i64, ctypes.POINTER(Group), _i32, _i32,
                                   _i32, _i32, _u32, _vp, _vp]),
     ("fadam_grad_sumsq", _i32, [_vp, _vp, _vp]),

@@ -1127,6 +1127,44 @@ fadam_status fadam_pack_dry(const fadam_tensor* tensors, int64_t n_tensors, int3
   return FADAM_OK;
 }
 
+fadam_status fadam_chunk_dry(const fadam_tensor* tensors, int64_t n_tensors, int32_t n_groups,
+                             int32_t p_dtype, int32_t g_dtype, int32_t out_dtype, uint32_t flags,
+                             int32_t grid, int64_t max_chunks, int32_t* chunks_out,
+                             int64_t max_out, int64_t* n_chunks_out) {
+  t_last_error.clear();
+  const Dtypes d{p_dtype, g_dtype, out_dtype, (flags & FADAM_REMAINDERS) != 0};
+  fadam_status st = check_dtypes(d, flags);
+  if (st) return st;
+  if (n_groups < 1 || n_groups > FADAM_MAX_GROUPS)
+    return fail(FADAM_EINVAL, "n_groups %d outside 1..%d", n_groups, FADAM_MAX_GROUPS);
+  std::vector<char> has_tensor(n_groups, 0);
+  st = check_tensors(tensors, n_tensors, n_groups, d, has_tensor);
+  if (st) return st;
+  if (grid < 1) return fail(FADAM_EINVAL, "grid %d < 1", grid);
+  if (max_chunks < 1) return fail(FADAM_EINVAL, "max_chunks %lld < 1", (long long)max_chunks);
+  if (!n_chunks_out) return fail(FADAM_EINVAL, "n_chunks_out is NULL");
+  std::vector<PackItem> pitems;
+  std::vector<int32_t> cta;
+  pack(tensors, n_tensors, d, grid, pitems, cta);
+  std::vector<Item> items;
+  items.reserve(pitems.size());
+  for (const PackItem& pi : pitems) items.push_back(to_item(tensors[pi.tensor], pi, d));
+  std::vector<Chunk> chunks;
+  build_chunks(items, max_chunks, grid, chunks);
+  *n_chunks_out = static_cast<int64_t>(chunks.size());
+  if (chunks_out) {
+    if (static_cast<int64_t>(chunks.size()) > max_out)
+      return fail(FADAM_ELIMIT, "%zu chunks do not fit in max_out %lld", chunks.size(),
+                  (long long)max_out);
+    for (size_t i = 0; i < chunks.size(); ++i) {
+      chunks_out[3 * i] = chunks[i].item;
+      chunks_out[3 * i + 1] = chunks[i].tile0;
+      chunks_out[3 * i + 2] = chunks[i].ntiles;
+    }
+  }
+  return FADAM_OK;
+}
+
 const char* fadam_status_string(fadam_status status) {
   switch (status) {
     case FADAM_OK: return "ok";

@@ -427,6 +427,25 @@ fadam_status fadam_pack_dry(const fadam_tensor* tensors, int64_t n_tensors, int3
                             int32_t grid, fadam_pack_item* items_out, int64_t max_items,
                             int32_t* cta_begin_out, int64_t* n_items_out);
 
+/* Host-only dry run of the chunk list, for inspection and tests; needs no
+ * GPU and dereferences no tensor pointer.  Packs `tensors` for a grid of
+ * `grid` CTAs as fadam_pack_dry does, then builds the list of bulk-tile
+ * chunks the CTAs of a launch take in order, at most `max_chunks` long (a
+ * plan uses 65536, fadam_step_noalloc 4096): 16 tiles a chunk (more when
+ * that keeps the list within max_chunks), tapering at the end of the list
+ * to about R / (2 grid) tiles, at least 4, for a chunk that starts with R
+ * tiles left; the tapered list is used when it fits max_chunks.  A tile
+ * here is 1024 vectors of 4 elements (a pass may copy several at once);
+ * only items whose streams are all 16-byte aligned have tiles.  Writes the chunk
+ * count to *n_chunks_out and, when chunks_out is not NULL, each chunk as
+ * three int32 (item index as in fadam_pack_dry, first tile, tiles) to
+ * chunks_out[3 * max_out].  Errors: as fadam_pack_dry, FADAM_EINVAL for
+ * max_chunks < 1, FADAM_ELIMIT when the chunks exceed max_out. */
+fadam_status fadam_chunk_dry(const fadam_tensor* tensors, int64_t n_tensors, int32_t n_groups,
+                             int32_t p_dtype, int32_t g_dtype, int32_t out_dtype, uint32_t flags,
+                             int32_t grid, int64_t max_chunks, int32_t* chunks_out,
+                             int64_t max_out, int64_t* n_chunks_out);
+
 /* Static description of a status code. */
 const char* fadam_status_string(fadam_status status);
 

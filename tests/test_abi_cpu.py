@@ -322,3 +322,103 @@ def test_pack_16bit_state_aligns_every_stream_to_16_bytes():
                     numel=200, group=0)
     items, _ = _dry([t], 1, p=_abi.DT_BF16)
     assert items[0] == (0, 0, 6, 0) and items[1] == (0, 6, 194, 2)
+
+
+# ---- the chunk list -------------------------------------------------------------
+
+PLAN_MAX_CHUNKS = 65536
+NOALLOC_MAX_CHUNKS = 4096
+TAPER_MIN = 4
+
+
+def _chunks(tensors, grid, max_chunks, g=_abi.DT_F32):
+    arr = (_abi.Tensor * max(1, len(tensors)))(*tensors)
+    n = ctypes.c_int64()
+    st = L.fadam_chunk_dry(arr, len(tensors), 1, _abi.DT_F32, g, _abi.DT_NONE, 0, grid,
+                           max_chunks, None, 0, ctypes.byref(n))
+    assert st == _abi.OK, L.fadam_last_error()
+    out = (ctypes.c_int32 * max(3, 3 * n.value))()
+    st = L.fadam_chunk_dry(arr, len(tensors), 1, _abi.DT_F32, g, _abi.DT_NONE, 0, grid,
+                           max_chunks, out, n.value, ctypes.byref(n))
+    assert st == _abi.OK, L.fadam_last_error()
+    return [tuple(out[3 * i:3 * i + 3]) for i in range(n.value)]
+
+
+def _tiles_of(item):
+    _, _, n, vec = item
+    return ((n // 4) & ~1) // -1024 * -1 if vec == 2 else 0
+
+
+def _check_chunk_cover(items, chunks):
+    """Every tile of every bulk item in exactly one chunk, items in order."""
+    nxt = {}
+    for k, t0, nt in chunks:
+        assert nt >= 1 and nxt.get(k, 0) == t0
+        nxt[k] = t0 + nt
+    for k, it in enumerate(items):
+        assert nxt.get(k, 0) == _tiles_of(it), k
+    order = [k for k, _, _ in chunks]
+    assert order == sorted(order)
+
+
+@pytest.mark.parametrize("recipe", ["large_uniform", "many_small", "capturable_l2"])
+def test_chunk_list_covers_every_tile_and_tapers(recipe):
+    spec = workloads.full_versions()[recipe]
+    tensors = _aligned_tensors(spec.sizes)
+    grid = 152
+    gdt = _abi.DT_BF16 if spec.g_dtype != workloads.torch.float32 else _abi.DT_F32
+    items, _ = _dry(tensors, grid, g=gdt)
+    chunks = _chunks(tensors, grid, PLAN_MAX_CHUNKS, g=gdt)
+    _check_chunk_cover(items, chunks)
+    assert len(chunks) <= PLAN_MAX_CHUNKS
+    sizes = [nt for _, _, nt in chunks]
+    last = {k: t0 + nt for k, t0, nt in chunks}
+    # each chunk takes min(16, max(4, tiles left / (2 grid))) tiles, cut
+    # short only by the end of its item
+    left = sum(sizes)
+    for k, t0, nt in chunks:
+        want = min(16, max(TAPER_MIN, left // (2 * grid)))
+        assert nt == want or t0 + nt == last[k], (k, t0, nt, want, left)
+        left -= nt
+    # the end of the list is in small chunks: the CTAs finish together
+    assert max(sizes[-grid:]) <= TAPER_MIN
+    assert max(sizes) == 16
+
+
+def test_chunk_list_keeps_to_the_noalloc_limit():
+    # 201 x 20,971,520 has about a million tiles: 4096 chunks need bigger
+    # chunks than 16 tiles, so the list is untapered and grown to fit
+    spec = workloads.full_versions()["large_uniform"]
+    tensors = _aligned_tensors(spec.sizes)
+    items, _ = _dry(tensors, 152)
+    chunks = _chunks(tensors, 152, NOALLOC_MAX_CHUNKS)
+    _check_chunk_cover(items, chunks)
+    assert len(chunks) <= NOALLOC_MAX_CHUNKS
+    assert max(nt for _, _, nt in chunks) > 16
+
+
+def test_chunk_list_small_and_empty_shards():
+    assert _chunks([], 4, PLAN_MAX_CHUNKS) == []
+    tensors = _aligned_tensors([1000, 4097, 65536, 3])
+    items, _ = _dry(tensors, 4)
+    chunks = _chunks(tensors, 4, PLAN_MAX_CHUNKS)
+    _check_chunk_cover(items, chunks)
+    # 65536 elements are 16 tiles: near the end of the list, so tapered
+    assert all(nt <= TAPER_MIN for _, _, nt in chunks)
+
+
+def test_chunk_dry_rejects_bad_arguments():
+    tensors = _aligned_tensors([4096])
+    arr = (_abi.Tensor * 1)(*tensors)
+    n = ctypes.c_int64()
+    assert L.fadam_chunk_dry(arr, 1, 1, _abi.DT_F32, _abi.DT_F32, _abi.DT_NONE, 0, 4, 0, None, 0,
+                             ctypes.byref(n)) == _abi.EINVAL
+    assert L.fadam_chunk_dry(arr, 1, 1, _abi.DT_F32, _abi.DT_F32, _abi.DT_NONE, 0, 0, 16, None,
+                             0, ctypes.byref(n)) == _abi.EINVAL
+    assert L.fadam_chunk_dry(arr, 1, 1, _abi.DT_F32, _abi.DT_F32, _abi.DT_NONE, 0, 4, 16, None,
+                             0, None) == _abi.EINVAL
+    out = (ctypes.c_int32 * 3)()
+    tensors = _aligned_tensors([1 << 20])
+    arr = (_abi.Tensor * 1)(*tensors)
+    assert L.fadam_chunk_dry(arr, 1, 1, _abi.DT_F32, _abi.DT_F32, _abi.DT_NONE, 0, 4, 16, out, 1,
+                             ctypes.byref(n)) == _abi.ELIMIT
