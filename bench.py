@@ -183,15 +183,26 @@ KERNEL_SOURCES = [os.path.join(ROOT, "include", "fadam.h")] + sorted(
     if f.endswith((".cu", ".cuh", ".h")))
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and with whitespace runs collapsed, so
+    that edits to comments alone keep the hash (string literals in these
+    sources hold no comment markers)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
-    """sha256 over the CUDA library's sources (decides whether a stored ncu
-    traffic figure still describes the kernel that runs)."""
+    """sha256 over the code of the CUDA library's sources, comments left out
+    (decides whether a stored ncu traffic figure still describes the kernel
+    that runs)."""
     import hashlib
     h = hashlib.sha256()
     for path in KERNEL_SOURCES:
-        with open(path, "rb") as fh:
+        with open(path, encoding="utf-8") as fh:
             h.update(os.path.relpath(path, ROOT).encode())
-            h.update(fh.read())
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()
 
 

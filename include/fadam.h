@@ -108,10 +108,11 @@ typedef int32_t fadam_status;
 /* One tensor (fragment) of the shard.  Every data pointer is a device
  * pointer to numel contiguous elements, aligned at least to its element
  * size.
- *   p      fp32 master parameter, updated in place; in FADAM_REMAINDERS mode
- *          the bf16 high half of the master (read only, unless p_out
- *          aliases it)
- *   m, v   fp32 first and second moments (exp_avg, exp_avg_sq), in place
+ *   p      master parameter in the plan's state dtype (fp32, bf16 or fp16),
+ *          updated in place; in FADAM_REMAINDERS mode the bf16 high half of
+ *          the master (read only, unless p_out aliases it)
+ *   m, v   first and second moments (exp_avg, exp_avg_sq) in the state
+ *          dtype (fp32 in FADAM_REMAINDERS mode), in place
  *   g      gradient in the plan's g dtype, read only
  *   p_out  param-out copy in the plan's out dtype; NULL iff the out dtype
  *          is FADAM_DT_NONE; may alias p; required (bf16) in remainder mode
@@ -181,11 +182,17 @@ typedef struct {
  * device status block.  Call it before any stream capture.
  *   tensors[n_tensors]  descriptors (host array, copied; n_tensors >= 0)
  *   groups[n_groups]    1 <= n_groups <= FADAM_MAX_GROUPS (host array, copied)
- *   p_dtype             FADAM_DT_F32, or FADAM_DT_BF16 with FADAM_REMAINDERS
+ *   p_dtype             state dtype of p, m and v: FADAM_DT_F32, _BF16 or
+ *                       _F16 (the optimizer's `dtype`; 16-bit values are
+ *                       widened for the update and rounded to nearest-even
+ *                       on store); FADAM_DT_BF16 with FADAM_REMAINDERS
+ *                       (then m and v are fp32)
  *   g_dtype             FADAM_DT_F32, FADAM_DT_BF16 or FADAM_DT_F16
  *   out_dtype           FADAM_DT_NONE, _F32, _BF16 or _F16 (_BF16 with remainders)
  *   flags               FADAM_CAPTURABLE | FADAM_REMAINDERS |
- *                       FADAM_CHECK_FINITE | FADAM_STEP_PREADVANCED
+ *                       FADAM_CHECK_FINITE | FADAM_STEP_PREADVANCED |
+ *                       FADAM_SCALED_STATES (bf16 or fp16 state only; set
+ *                       the scales with fadam_plan_set_state_scales)
  *   *plan_out           receives the plan (owned by the caller; free with
  *                       fadam_plan_destroy)
  * Errors: FADAM_EINVAL, FADAM_EDTYPE, FADAM_EALIGN, FADAM_ELIMIT, FADAM_ECUDA;
