@@ -83,7 +83,7 @@ SIGNATURES = [
     ("fadam_step_noalloc", _i32, [ctypes.POINTER(Tensor), _i64, ctypes.POINTER(Group), _i32, _i32,
                                   _i32, _i32, _u32, _vp, _vp]),
     ("fadam_grad_sumsq", _i32, [_vp, _vp, _vp]),
-    ("fadam_clip_apply", _i32, [_vp, _vp, _f32, _vp, _vp, _vp]),
+    ("fadam_clip_apply", _i32, [_vp, _vp, _f32, _vp, _vp, _vp, _vp]),
     ("fadam_plan_set_exchange", _i32, [_vp, _vp, ctypes.POINTER(_vp), _i32, _i32, _vp,
                                        ctypes.POINTER(_vp), _i32]),
     ("fadam_grad_reduce", _i32, [_vp, _vp]),

@@ -1022,20 +1022,29 @@ struct ClipArgs {
   float max_norm;
   int32_t n_scales;
   float* scales[FADAM_MAX_GROUPS];
+  // regular plans: each group's host grad_scale in, the clipped one out
+  int32_t n_host;
+  float* host_out;
+  float host_in[FADAM_MAX_GROUPS];
 };
 
 // One thread: the norm from the squared norm, found_inf into the noop flag,
-// and the clip coefficient multiplied into each distinct grad_scale.
+// and the clip coefficient multiplied into each distinct device grad_scale
+// (capturable plans) or into each group's host grad_scale, written out for
+// the caller to keep (regular plans).
 __global__ void fadam_clip_kernel(const __grid_constant__ ClipArgs a) {
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   const float norm = __double2float_rn(sqrt(__ldcg(a.sumsq)));
   if (a.norm_out) *a.norm_out = norm;
   if (a.noop) *a.noop = isfinite(norm) ? 0 : 1;
+  float coef = 1.0f;
   if (a.max_norm > 0.0f) {
-    float coef = __fdiv_rn(a.max_norm, __fadd_rn(norm, 1e-6f));
+    coef = __fdiv_rn(a.max_norm, __fadd_rn(norm, 1e-6f));
     if (coef > 1.0f) coef = 1.0f;  // a NaN coefficient stays NaN, as torch.clamp keeps it
     for (int i = 0; i < a.n_scales; ++i) *a.scales[i] = __fmul_rn(*a.scales[i], coef);
   }
+  for (int i = 0; i < a.n_host; ++i)
+    a.host_out[i] = a.max_norm > 0.0f ? __fmul_rn(a.host_in[i], coef) : a.host_in[i];
 }
 
 }  // namespace
@@ -1059,13 +1068,16 @@ fadam_status fadam_grad_sumsq(fadam_plan* plan, double* sumsq_dev, fadam_stream 
 }
 
 fadam_status fadam_clip_apply(fadam_plan* plan, const double* sumsq_dev, float max_norm,
-                              float* norm_dev, int32_t* noop_dev, fadam_stream stream) {
+                              float* norm_dev, int32_t* noop_dev, float* grad_scales_out_dev,
+                              fadam_stream stream) {
   if (!plan) return fail(FADAM_EINVAL, "plan is NULL");
   if (!sumsq_dev || reinterpret_cast<uintptr_t>(sumsq_dev) % 8)
     return fail(FADAM_EINVAL, "sumsq_dev must be a non-NULL, 8-byte aligned device pointer");
   if ((norm_dev && reinterpret_cast<uintptr_t>(norm_dev) % 4) ||
       (noop_dev && reinterpret_cast<uintptr_t>(noop_dev) % 4))
     return fail(FADAM_EALIGN, "norm_dev / noop_dev not 4-byte aligned");
+  if (grad_scales_out_dev && reinterpret_cast<uintptr_t>(grad_scales_out_dev) % 4)
+    return fail(FADAM_EALIGN, "grad_scales_out_dev not 4-byte aligned");
   if (!std::isfinite(max_norm)) return fail(FADAM_EINVAL, "max_norm is not finite");
   ClipArgs a{};
   a.sumsq = sumsq_dev;
@@ -1080,6 +1092,10 @@ fadam_status fadam_clip_apply(fadam_plan* plan, const double* sumsq_dev, float m
       for (int32_t j = 0; j < a.n_scales; ++j) seen |= a.scales[j] == gs;
       if (!seen) a.scales[a.n_scales++] = gs;
     }
+  } else if (grad_scales_out_dev) {
+    a.n_host = plan->n_groups;
+    a.host_out = grad_scales_out_dev;
+    for (int32_t g = 0; g < plan->n_groups; ++g) a.host_in[g] = plan->groups[g].grad_scale;
   }
   DeviceGuard guard(plan->hp.device);
   if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");

@@ -240,21 +240,28 @@ class FusedAdamShard:
 
     def clip_apply(self, sumsq: torch.Tensor, max_norm: float) -> torch.Tensor:
         """Norm from the (all-reduced) squared norm; found_inf into the noop
-        flag; capturable shards scale the device grad_scale by the clip
-        coefficient.  Returns the norm as a float32 device tensor."""
+        flag; the clip coefficient multiplied into the grad scale by the
+        same launch: on the device for capturable shards, and for regular
+        shards into a device copy of each group's host grad scale, which is
+        read back (one sync, as the page's .item() path).  Returns the norm
+        as a float32 device tensor."""
         if not hasattr(self, "_norm"):
             self._norm = torch.zeros(1, dtype=torch.float32, device=self.device)
+            self._scales_out = torch.zeros(len(self.groups), dtype=torch.float32,
+                                           device=self.device)
         noop = self.noop.data_ptr() if self.capturable else None
+        scales_out = None
+        if not self.capturable:
+            self._fill_groups()  # the plan scales the current host grad scale
+            _abi.check(_abi.lib().fadam_plan_set_groups(self._plan, self._groups_c,
+                                                        len(self.groups)), "fadam_plan_set_groups")
+            scales_out = self._scales_out.data_ptr()
         _abi.check(_abi.lib().fadam_clip_apply(self._plan, sumsq.data_ptr(), float(max_norm),
-                                               self._norm.data_ptr(), noop,
+                                               self._norm.data_ptr(), noop, scales_out,
                                                _stream_handle(self.device)), "fadam_clip_apply")
-        if not self.capturable and max_norm > 0:
-            # regular shards keep grad_scale on the host (the page's .item() path)
-            import numpy as np
-            norm = np.float32(self._norm.item())
-            coef = np.float32(max_norm) / (norm + np.float32(1e-6))
-            coef = min(coef, np.float32(1.0))
-            self.host_grad_scale = float(np.float32(self.host_grad_scale) * np.float32(coef))
+        if not self.capturable:
+            # every group shares the binding's one host grad scale
+            self.host_grad_scale = float(self._scales_out[0].item())
         return self._norm
 
     def clip_grad_norm(self, max_norm: float) -> torch.Tensor:

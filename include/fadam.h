@@ -263,10 +263,16 @@ fadam_status fadam_grad_sumsq(fadam_plan* plan, double* sumsq_dev, fadam_stream 
  * the page copies found_inf into its noop buffer), and, when max_norm > 0,
  * multiplies each distinct grad_scale_dev of a capturable plan by
  * min(1, max_norm / (norm + 1e-6)) (float arithmetic; a NaN coefficient is
- * kept).  Regular plans keep grad_scale on the host: read *norm_dev and
- * scale it there.  Errors: FADAM_EINVAL, FADAM_EALIGN, FADAM_ECUDA. */
+ * kept).  Regular plans keep grad_scale on the host (the page reads the
+ * norm with .item()): when grad_scales_out_dev is not NULL, the same
+ * launch writes each group's grad_scale (as last set with
+ * fadam_plan_set_groups) times that coefficient into
+ * grad_scales_out_dev[n_groups] (unchanged when max_norm <= 0), for the
+ * caller to read back and pass to fadam_plan_set_groups; capturable plans
+ * ignore it.  Errors: FADAM_EINVAL, FADAM_EALIGN, FADAM_ECUDA. */
 fadam_status fadam_clip_apply(fadam_plan* plan, const double* sumsq_dev, float max_norm,
-                              float* norm_dev, int32_t* noop_dev, fadam_stream stream);
+                              float* norm_dev, int32_t* noop_dev, float* grad_scales_out_dev,
+                              fadam_stream stream);
 
 /* The data-parallel exchange around the step, on one GPU
  * ("apex/contrib/optimizers/distributed_fused_adam.py":

@@ -89,7 +89,7 @@ def test_clip_scales_device_grad_scale(max_norm):
     assert opt.noop.item() == 0
 
 
-def test_regular_shard_clips_on_the_host():
+def test_regular_shard_clips_its_host_grad_scale():
     spec = workloads.small_versions()["tiny_adamw"]
     shard = workloads.materialize(spec, DEV)
     opt = _opt(spec, shard, capturable=False)
@@ -97,6 +97,14 @@ def test_regular_shard_clips_on_the_host():
     want = oracle.shard_sumsq(helpers.oracle_shard(shard))
     _, _, _, o_gs = oracle.clip_from_sumsq(want, 1e-3, 1.0)
     assert opt.host_grad_scale == pytest.approx(float(o_gs), rel=2e-6)
+    # a second clip sees the gradient times the clipped scale and scales
+    # that scale again; max_norm <= 0 keeps it
+    opt.clip_grad_norm(1e-3)
+    _, _, _, o_gs2 = oracle.clip_from_sumsq(want * float(o_gs) ** 2, 1e-3, float(o_gs))
+    assert opt.host_grad_scale == pytest.approx(float(o_gs2), rel=4e-6)
+    before = opt.host_grad_scale
+    opt.clip_grad_norm(0.0)
+    assert opt.host_grad_scale == before
 
 
 def test_norm_clip_step_in_one_graph_matches_eager():
