@@ -406,9 +406,12 @@ struct Layout {
   static constexpr int off_v = off_m + kMV * update_vectors;
   static constexpr int off_g = off_v + kMV * update_vectors;
   static constexpr unsigned update_tile = per_vector * update_vectors;
-  // the g-only passes (screen, norm) fill the same stage with g: at least
-  // four vectors per thread, more for 16-bit grads
-  static constexpr int scan_per_thread = update_tile / kG / kTile > 4 ? update_tile / kG / kTile : 4;
+  // the g-only passes (screen, norm, reduce) fill a stage of at least
+  // 64 KB with g: four vectors per thread for fp32 grads, eight for 16-bit
+  // ones (more when the update's tile is larger)
+  static constexpr unsigned kScanBytes = 65536u;
+  static constexpr unsigned scan_target = update_tile > kScanBytes ? update_tile : kScanBytes;
+  static constexpr int scan_per_thread = static_cast<int>(scan_target / kG / kTile);
   static constexpr int scan_vectors = scan_per_thread * kTile;
   static constexpr unsigned scan_tile = scan_vectors * kG;
   static constexpr unsigned stage = update_tile > scan_tile ? update_tile : scan_tile;
