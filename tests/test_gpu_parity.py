@@ -394,3 +394,40 @@ def test_16bit_state_shard_full_oracle_and_graph():
     shard, opt, osh = _run(spec, 3)
     helpers.compare(shard, osh)
     assert opt.group_steps() == [3, 3, 3]
+
+
+@pytest.mark.parametrize("name", ["tiny_adamw", "capturable_l2", "remainder_shard", "many_small"])
+def test_plan_work_lists_match_the_host_dry_runs(name):
+    # the packer and the chunk list a plan uploads are the ones the host-only
+    # dry runs (fadam_pack_dry, fadam_chunk_dry) describe for the plan's grid
+    spec = workloads.small_versions()[name]
+    shard = workloads.materialize(spec, DEV)
+    groups = shard.param_groups()
+    opt = FusedAdamShard(groups, capturable=spec.capturable, remainders=spec.remainders,
+                         grad_scale=spec.grad_scale)
+    info = opt.info()
+    descs = []
+    for gi, g in enumerate(groups):
+        outs = g.get("params_out") or [None] * len(g["params"])
+        rems = g.get("remainders") or [None] * len(g["params"])
+        for p, m, v, gr, o, r in zip(g["params"], g["exp_avgs"], g["exp_avg_sqs"], g["grads"],
+                                     outs, rems):
+            descs.append(_abi.Tensor(p=p.data_ptr(), m=m.data_ptr(), v=v.data_ptr(),
+                                     g=gr.data_ptr(), p_out=o.data_ptr() if o is not None else None,
+                                     rem=r.data_ptr() if r is not None else None,
+                                     numel=p.numel(), group=gi))
+    arr = (_abi.Tensor * max(1, len(descs)))(*descs)
+    codes = {None: _abi.DT_NONE, torch.float32: _abi.DT_F32, torch.bfloat16: _abi.DT_BF16,
+             torch.float16: _abi.DT_F16}
+    p_dt = _abi.DT_BF16 if spec.remainders else codes[spec.state_dtype]
+    g_dt, o_dt = codes[spec.g_dtype], codes[spec.out_dtype]
+    flags = _abi.REMAINDERS if spec.remainders else 0
+    L = _abi.lib()
+    n = ctypes.c_int64()
+    assert L.fadam_pack_dry(arr, len(descs), len(groups), p_dt, g_dt, o_dt, flags, info["grid"],
+                            None, 0, None, ctypes.byref(n)) == _abi.OK, L.fadam_last_error()
+    assert n.value == info["n_items"]
+    assert L.fadam_chunk_dry(arr, len(descs), len(groups), p_dt, g_dt, o_dt, flags, info["grid"],
+                             65536, None, 0, ctypes.byref(n)) == _abi.OK, L.fadam_last_error()
+    assert n.value == info["n_chunks"]
+    opt.close()
