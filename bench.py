@@ -238,6 +238,24 @@ def measured_peaks() -> dict:
         return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def host_memory_allows(nbytes: int) -> bool:
+    """True when nbytes of page-locked host memory stay within half of the
+    memory the host has available now (unknown: assume it does)."""
+    try:
+        avail = os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError, AttributeError):
+        return True
+    return nbytes <= avail // 2
+
+
+def e2e_fits(node_bytes: int, world: int, device=None) -> bool:
+    """Whether the end-to-end leg can pin its host gradients on every node,
+    as one decision for all ranks (the leg has barriers and a reduction, so
+    no rank may skip it alone)."""
+    veto = 0.0 if host_memory_allows(node_bytes) else 1.0
+    return max_over_ranks(veto, world, device) == 0.0
+
+
 # ---- CPU baseline (the oracle, as it stands) ----------------------------------
 
 def cpu_oracle_run(n_tensors: int, steps: int, threads: int, numel: int):
@@ -412,7 +430,17 @@ def run_gpu(args):
     clocks = sampler.stop()
 
     e2e = None
-    if "e2e" in variants:
+    host_bytes = sum(g.numel() * g.element_size() for g in shard.grads)
+    ranks_here = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    fits = e2e_fits(ranks_here * host_bytes, world, device)
+    if "e2e" in variants and not fits:
+        # every rank of the node pins its own copy of the gradients: leave
+        # the leg out rather than exhaust the host
+        e2e = {"value": None, "unit": "GB/s", "h2d_bytes_per_step": host_bytes,
+               "d2h_bytes_per_step": 4 * len(groups),
+               "skipped": f"{ranks_here} ranks x {host_bytes / 1e9:.1f} GB of pinned host "
+                          "gradients exceed half of the node's available memory"}
+    elif "e2e" in variants:
         host = [shard.grads[i].cpu().pin_memory() for i in shard.plan_order()]
         for _ in range(max(1, args.warmup // 2)):
             cap.step_from_host(host)

@@ -56,6 +56,40 @@ def test_two_ranks_take_the_slowest_rank_and_sum_the_work():
         assert gps == pytest.approx(2 * 1e8 / 0.020 / 1e9)
 
 
+def _fits_worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    bench.init_dist(world, "gloo")
+    # rank 1 sees a host too small for its pinned gradients
+    if rank == 1:
+        bench.host_memory_allows = lambda nbytes: False
+    out[rank] = bench.e2e_fits(1 << 30, world)
+    dist.destroy_process_group()
+
+
+def test_end_to_end_leg_is_skipped_by_all_ranks_or_none():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    manager = ctx.Manager()
+    out = manager.dict()
+    procs = [ctx.Process(target=_fits_worker, args=(r, world, port, out)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    assert out[0] is False and out[1] is False
+
+
+def test_host_memory_check(monkeypatch):
+    monkeypatch.setattr(bench.os, "sysconf",
+                        lambda name: {"SC_AVPHYS_PAGES": 1000, "SC_PAGE_SIZE": 4096}[name])
+    assert bench.host_memory_allows(2_048_000)
+    assert not bench.host_memory_allows(2_048_001)
+    assert bench.e2e_fits(2_048_000, 1) and not bench.e2e_fits(3_000_000, 1)
+
+
 def test_single_rank_needs_no_process_group():
     assert bench.max_over_ranks(0.5, 1) == 0.5
     assert bench.aggregate(28.0, 1.0, 1, 1.0) == {"gbs": 28e-9, "gparams_per_s": 1e-9}
