@@ -344,6 +344,8 @@ def run_gpu(args):
         spec = workloads.scaled_state_shard(layers=args.layers or 8, seed=1241 + 1000 * rank)
     elif args.workload == "exchange_shard":
         spec = workloads.exchange_shard(layers=args.layers or 8, seed=1240 + 1000 * rank)
+    elif args.workload == "remainder_shard" and args.total:
+        spec = workloads.remainder_shard(total=args.total, seed=1238 + 1000 * rank)
     elif args.workload == "capturable_l2" and args.layers:
         spec = workloads.capturable_l2(layers=args.layers, seed=1236 + 1000 * rank)
     elif args.workload == "many_small" and args.n_tensors:
@@ -518,6 +520,8 @@ def main(argv=None):
     ap.add_argument("--n-tensors", type=int, default=None,
                     help="tensor count of large_uniform[_bf16_state] (201) or many_small (20000)")
     ap.add_argument("--numel", type=int, default=320 * 65536)
+    ap.add_argument("--total", type=int, default=None,
+                    help="elements of the remainder_shard bucket (1,200,000,000)")
     ap.add_argument("--layers", type=int, default=None,
                     help="layers of the capturable_l2 / exchange_shard / scaled_state_shard "
                          "layer list (8)")
