@@ -111,8 +111,11 @@ class Report:
         got = got.astype(np.float64)
         want = want.astype(np.float64)
         both_nan = np.isnan(got) & np.isnan(want)
-        d = np.where(both_nan, 0.0, np.abs(got - want))
-        lim = np.where(both_nan, 0.0, RTOL * np.abs(want) + ATOL)
+        same = (got == want) | both_nan  # equal infinities included
+        with np.errstate(invalid="ignore"):
+            d = np.where(same, 0.0, np.abs(got - want))
+            # a non-finite expected value must be matched exactly
+            lim = np.where(same | ~np.isfinite(want), 0.0, RTOL * np.abs(want) + ATOL)
         bad = ~(d <= lim)
         if bad.any():
             k = int(np.argmax(bad))
@@ -158,7 +161,8 @@ def compare(shard: workloads.Shard, osh: oracle.Shard, idx=None, elems=None,
             if spec.out_dtype == torch.float32:
                 report.f32(to_np(sel(shard.params_out[i])), t.p_out, f"tensor {i} p_out")
             elif spec.out_dtype is not None:
-                report.ulp16(to_np(sel(shard.params_out[i])), t.p_out, f"tensor {i} p_out")
+                report.ulp16(to_np(sel(shard.params_out[i])), t.p_out, f"tensor {i} p_out",
+                             spec.out_dtype)
             continue
         report.f32(to_np(sel(shard.exp_avgs[i])), t.m, f"tensor {i} m")
         report.f32(to_np(sel(shard.exp_avg_sqs[i])), t.v, f"tensor {i} v")
@@ -168,13 +172,14 @@ def compare(shard: workloads.Shard, osh: oracle.Shard, idx=None, elems=None,
             got = oracle.rem_pack(hi, rem).view(np.float32)
             want = oracle.rem_pack(t.p_hi, t.rem).view(np.float32)
             report.f32(got, want, f"tensor {i} fp32 master (bf16 + remainder)")
-            report.ulp16(hi, t.p_hi, f"tensor {i} bf16 high half")
+            report.ulp16(hi, t.p_hi, f"tensor {i} bf16 high half", torch.bfloat16)
         else:
             report.f32(to_np(sel(shard.params[i])), t.p, f"tensor {i} p")
             if spec.out_dtype == torch.float32:
                 report.f32(to_np(sel(shard.params_out[i])), t.p_out, f"tensor {i} p_out")
             elif spec.out_dtype is not None:
-                report.ulp16(to_np(sel(shard.params_out[i])), t.p_out, f"tensor {i} p_out")
+                report.ulp16(to_np(sel(shard.params_out[i])), t.p_out, f"tensor {i} p_out",
+                             spec.out_dtype)
     return report
 
 

@@ -431,3 +431,54 @@ def test_plan_work_lists_match_the_host_dry_runs(name):
                              65536, None, 0, ctypes.byref(n)) == _abi.OK, L.fadam_last_error()
     assert n.value == info["n_chunks"]
     opt.close()
+
+
+_SPECIAL = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-45, -1e-45, 1.1754944e-38,
+                     3.4e38, -3.4e38, 1e-20, 65504.0, 1.0, -1.0], dtype=np.float32)
+
+
+def _sprinkle(t: torch.Tensor, gen: np.random.Generator, every: int) -> None:
+    """Put the special values at every `every`-th element (from a random start)."""
+    n = t.numel()
+    pos = np.arange(int(gen.integers(0, every)), n, every)
+    vals = _SPECIAL[gen.integers(0, len(_SPECIAL), size=len(pos))]
+    t.view(-1)[torch.as_tensor(pos, device=t.device)] = torch.as_tensor(vals, device=t.device)
+
+
+@pytest.mark.parametrize("start_step", [0, 9998])
+def test_special_values_and_extreme_hyper_parameters(start_step):
+    # infinities, NaNs, signed zeros, subnormals and values near overflow in
+    # p, m, v and g (no screen: they flow through the arithmetic), and groups
+    # with lr 0, betas 0, eps 0, large and negative decay, bias correction
+    # off, and a late step where 1 - beta^step rounds to 1: every value as
+    # the oracle's IEEE sequence gives it (NaN where it gives NaN)
+    groups = [
+        workloads.GroupSpec(adam_w_mode=True, lr=1e-3, betas=(0.9, 0.999), eps=1e-8,
+                            weight_decay=0.1),
+        workloads.GroupSpec(adam_w_mode=False, lr=0.0, betas=(0.0, 0.0), eps=0.0,
+                            weight_decay=0.0),
+        workloads.GroupSpec(adam_w_mode=True, lr=10.0, betas=(0.99, 0.9999), eps=1e-30,
+                            weight_decay=1e-4, bias_correction=False),
+        workloads.GroupSpec(adam_w_mode=False, lr=3e-4, betas=(0.5, 0.75), eps=1e-6,
+                            weight_decay=-0.1),
+    ]
+    sizes = [37, 4099, 5, 70003]
+    shard = _custom_shard(sizes * 2, [0, 1, 0, 3] * 2, [0, 1, 0, 3] * 2,
+                          [0, 1, 2, 3, 3, 2, 1, 0], groups, out_dtype=torch.bfloat16)
+    gen = np.random.default_rng(5)
+    for i in range(len(shard.params)):
+        shard.exp_avgs[i].copy_(torch.randn_like(shard.exp_avgs[i]) * 1e-2)
+        shard.exp_avg_sqs[i].copy_(torch.rand_like(shard.exp_avg_sqs[i]) * 1e-4)
+        for t, every in ((shard.params[i], 7), (shard.exp_avgs[i], 11),
+                         (shard.exp_avg_sqs[i], 13), (shard.grads[i], 5)):
+            _sprinkle(t, gen, every)
+    opt = FusedAdamShard(shard.param_groups(), capturable=False)
+    opt.host_steps = [start_step] * len(groups)
+    osh = helpers.oracle_shard(shard)
+    osh.steps = [start_step] * len(groups)
+    for _ in range(3):
+        opt.step()
+        oracle.shard_step(osh, capturable=False)
+    torch.cuda.synchronize()
+    rep = helpers.compare(shard, osh)
+    assert rep.exact_fraction == 1.0
