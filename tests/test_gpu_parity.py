@@ -442,7 +442,7 @@ def _sprinkle(t: torch.Tensor, gen: np.random.Generator, every: int) -> None:
     n = t.numel()
     pos = np.arange(int(gen.integers(0, every)), n, every)
     vals = _SPECIAL[gen.integers(0, len(_SPECIAL), size=len(pos))]
-    t.view(-1)[torch.as_tensor(pos, device=t.device)] = torch.as_tensor(vals, device=t.device)
+    t.view(-1)[torch.as_tensor(pos, device=t.device)] = torch.as_tensor(vals, device=t.device).to(t.dtype)
 
 
 @pytest.mark.parametrize("start_step", [0, 9998])
@@ -479,6 +479,38 @@ def test_special_values_and_extreme_hyper_parameters(start_step):
     for _ in range(3):
         opt.step()
         oracle.shard_step(osh, capturable=False)
+    torch.cuda.synchronize()
+    rep = helpers.compare(shard, osh)
+    assert rep.exact_fraction == 1.0
+
+
+@pytest.mark.parametrize("form", ["bf16_state_fp16_grads", "remainders"])
+def test_special_values_in_16bit_and_remainder_forms(form):
+    # the special values again, stored in the 16-bit state (bf16, with fp16
+    # gradients, so 3.4e38 becomes an fp16 infinity) or in the bf16 high
+    # halves of the remainder form
+    if form == "remainders":
+        spec = workloads.small_versions()["remainder_shard"]
+    else:
+        spec = workloads.large_uniform(n_tensors=3, numel=40_003, state_dtype=torch.bfloat16,
+                                       g_dtype=torch.float16)
+        spec.out_dtype = torch.float16
+    shard = workloads.materialize(spec, DEV)
+    gen = np.random.default_rng(6)
+    for i in range(len(shard.params)):
+        for t, every in ((shard.params[i], 7), (shard.grads[i], 5)):
+            _sprinkle(t, gen, every)
+        if form != "remainders":
+            shard.exp_avgs[i].copy_(torch.randn_like(shard.exp_avgs[i]) * 1e-2)
+            shard.exp_avg_sqs[i].copy_(torch.rand_like(shard.exp_avg_sqs[i]) * 1e-4)
+            _sprinkle(shard.exp_avgs[i], gen, 11)
+            _sprinkle(shard.exp_avg_sqs[i], gen, 13)
+    opt = FusedAdamShard(shard.param_groups(), capturable=spec.capturable,
+                         remainders=spec.remainders, grad_scale=spec.grad_scale)
+    osh = helpers.oracle_shard(shard)
+    for _ in range(3):
+        opt.step()
+        oracle.shard_step(osh, capturable=spec.capturable)
     torch.cuda.synchronize()
     rep = helpers.compare(shard, osh)
     assert rep.exact_fraction == 1.0
