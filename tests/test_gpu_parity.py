@@ -514,3 +514,34 @@ def test_special_values_in_16bit_and_remainder_forms(form):
     torch.cuda.synchronize()
     rep = helpers.compare(shard, osh)
     assert rep.exact_fraction == 1.0
+
+
+@pytest.mark.parametrize("name", ["tiny_adamw", "remainder_shard"])
+def test_two_hundred_graph_replays_stay_bit_identical(name):
+    # a long run: 200 steps of a captured capturable step, new gradients
+    # before each replay (written into the same buffers the graph reads);
+    # the counters reach 200, beta1^step underflows the bias correction to
+    # 1, and every value still equals the oracle's
+    spec = workloads.small_versions()[name]
+    shard = workloads.materialize(spec, DEV)
+    opt = FusedAdamShard(shard.param_groups(), capturable=True, remainders=spec.remainders,
+                         grad_scale=spec.grad_scale)
+    osh = helpers.oracle_shard(shard)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # one eager step on the side stream before capture
+        opt.step()
+    torch.cuda.current_stream().wait_stream(s)
+    oracle.shard_step(osh, capturable=True)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        opt.step()
+    for k in range(2, 201):
+        workloads.fresh_grads(shard, k)
+        helpers.refresh_grads(osh, shard)
+        graph.replay()
+        oracle.shard_step(osh, capturable=True)
+    torch.cuda.synchronize()
+    assert opt.group_steps() == [200] * len(spec.groups)
+    rep = helpers.compare(shard, osh)
+    assert rep.exact_fraction == 1.0
