@@ -545,3 +545,40 @@ def test_two_hundred_graph_replays_stay_bit_identical(name):
     assert opt.group_steps() == [200] * len(spec.groups)
     rep = helpers.compare(shard, osh)
     assert rep.exact_fraction == 1.0
+
+
+def test_learning_rate_and_grad_scale_schedules_under_graph_replay():
+    # the capturable step reads lr and grad_scale from device memory at each
+    # launch: a schedule written between replays (a warm-up ramp and a decay
+    # per group, a loss-scale change) reaches every replay without a new
+    # capture
+    spec = workloads.small_versions()["many_small"]
+    shard = workloads.materialize(spec, DEV)
+    opt = FusedAdamShard(shard.param_groups(), capturable=True, grad_scale=spec.grad_scale)
+    osh = helpers.oracle_shard(shard)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        opt.step()
+    torch.cuda.current_stream().wait_stream(s)
+    oracle.shard_step(osh, capturable=True)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        opt.step()
+    for k in range(2, 9):
+        for gi, g in enumerate(spec.groups):
+            lr = np.float32(g.lr * min(1.0, k / 4) * 0.9 ** max(0, k - 4) * (gi + 1))
+            opt.set_lr(gi, float(lr))
+            osh.groups[gi].lr = float(lr)
+        scale = float(np.float32(2.0 ** (k % 3) * spec.grad_scale))
+        opt.set_grad_scale(scale)
+        for grp in osh.groups:
+            grp.grad_scale = scale
+        workloads.fresh_grads(shard, k)
+        helpers.refresh_grads(osh, shard)
+        graph.replay()
+        oracle.shard_step(osh, capturable=True)
+    torch.cuda.synchronize()
+    assert opt.group_steps() == [8] * len(spec.groups)
+    rep = helpers.compare(shard, osh)
+    assert rep.exact_fraction == 1.0
