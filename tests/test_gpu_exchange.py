@@ -188,3 +188,27 @@ def test_exchange_argument_checks():
         out = torch.zeros(4096, dtype=torch.bfloat16, device=DEV)
         lopt.set_exchange(lsh.grads[0], [], out_shard=out, dests=[out.clone()])
     lopt.close()
+
+
+@pytest.mark.parametrize("ranks,average", [(2, True), (4, False), (8, True), (7, True)])
+def test_unrolled_and_generic_reduce_tiles(ranks, average):
+    # 2, 4 and 8 sources take the reduce tiles unrolled for that count, 7 the
+    # generic loop; each sums in rank order and gives the oracle's shard
+    # bit for bit, and the fused step the oracle's state
+    spec = workloads.exchange_shard(layers=1, hidden=256, ffn=688, ranks=ranks, dests=1)
+    spec.exchange_average = average
+    shard = workloads.materialize(spec, DEV)
+    opt = FusedAdamShard(shard.param_groups(), capturable=True)
+    opt.set_exchange(shard.buckets["g"], list(shard.sources), average=average,
+                     out_shard=shard.buckets["p_out"], dests=list(shard.dests))
+    osh = helpers.oracle_shard(shard)
+    src = _oracle_sources(shard)
+    for _ in range(2):
+        opt.step_reduce()
+        oracle.exchange_step(osh, src, average=average, capturable=True)
+    torch.cuda.synchronize()
+    _check_reduced(shard, osh)
+    rep = helpers.compare(shard, osh)
+    _check_dests(shard)
+    assert rep.exact_fraction == 1.0
+    opt.close()
