@@ -10,7 +10,9 @@ import ctypes
 import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_build", "libfadam.so")
+# FADAM_LIBRARY selects another build of the library (e.g. one compiled with
+# different tuning defines by build.build(defines=..., lib=...))
+LIB_PATH = os.environ.get("FADAM_LIBRARY") or os.path.join(_PKG, "_build", "libfadam.so")
 
 # status codes
 OK, EINVAL, EDTYPE, EALIGN, ECUDA, ETIMEOUT, ELIMIT = 0, 1, 2, 3, 4, 5, 6

@@ -14,6 +14,8 @@ namespace fadam {
 #define FADAM_BLOCK 1024
 #endif
 constexpr int kBlock = FADAM_BLOCK;
+static_assert(kBlock % 32 == 0 && kBlock >= 32 && kBlock <= 1024,
+              "threads per CTA: whole warps, at most 1024");
 // Elements per vector access (one 16-byte fp32 vector).
 constexpr int kVec = 4;
 // Largest work item, in elements (keeps in-item indices in 32 bits).

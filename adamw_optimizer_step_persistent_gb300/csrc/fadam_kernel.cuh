@@ -965,11 +965,12 @@ __device__ __forceinline__ void norm_warp_close(NormAcc& na, const NormBuf& buf,
 
 // Warp 0, after a CTA barrier that follows every warp's norm_warp_close.
 __device__ __forceinline__ void norm_publish(const NormBuf& buf, float gs, double* slot) {
+  constexpr int W = kBlock / 32;  // warp partials (lanes past them add zeros)
   if (threadIdx.x < 32) {
-    float y = buf.f[threadIdx.x];
+    float y = threadIdx.x < W ? buf.f[threadIdx.x] : 0.0f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) y = __fadd_rn(y, __shfl_xor_sync(0xffffffffu, y, o));
-    double yd = buf.d[threadIdx.x];
+    double yd = threadIdx.x < W ? buf.d[threadIdx.x] : 0.0;
     if (__any_sync(0xffffffffu, __double_as_longlong(yd) != 0)) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) yd += __shfl_xor_sync(0xffffffffu, yd, o);
