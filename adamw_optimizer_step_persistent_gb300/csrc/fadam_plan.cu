@@ -32,7 +32,7 @@ constexpr double kMinCtaCost = 64.0 * 1024.0;
 constexpr double kItemOverhead = 4096.0;
 // Most chunks a plan's work list holds (chunks grow past kChunkTiles tiles
 // beyond that).
-constexpr int64_t kPlanMaxChunks = 65536;
+constexpr int64_t kPlanMaxChunks = 131072;
 // Smallest chunk of the tapered end of a chunk list, in tiles.
 #ifndef FADAM_TAPER_MIN_TILES
 #define FADAM_TAPER_MIN_TILES 4

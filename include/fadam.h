@@ -444,7 +444,7 @@ fadam_status fadam_pack_dry(const fadam_tensor* tensors, int64_t n_tensors, int3
  * GPU and dereferences no tensor pointer.  Packs `tensors` for a grid of
  * `grid` CTAs as fadam_pack_dry does, then builds the list of bulk-tile
  * chunks the CTAs of a launch take in order, at most `max_chunks` long (a
- * plan uses 65536, fadam_step_noalloc 4096): 16 tiles a chunk (more when
+ * plan uses 131072, fadam_step_noalloc 4096): 16 tiles a chunk (more when
  * that keeps the list within max_chunks), tapering at the end of the list
  * to about R / (2 grid) tiles, at least 4, for a chunk that starts with R
  * tiles left; the tapered list is used when it fits max_chunks.  A tile

@@ -326,7 +326,7 @@ def test_pack_16bit_state_aligns_every_stream_to_16_bytes():
 
 # ---- the chunk list -------------------------------------------------------------
 
-PLAN_MAX_CHUNKS = 65536
+PLAN_MAX_CHUNKS = 131072
 NOALLOC_MAX_CHUNKS = 4096
 TAPER_MIN = 4
 
@@ -422,3 +422,15 @@ def test_chunk_dry_rejects_bad_arguments():
     arr = (_abi.Tensor * 1)(*tensors)
     assert L.fadam_chunk_dry(arr, 1, 1, _abi.DT_F32, _abi.DT_F32, _abi.DT_NONE, 0, 4, 16, out, 1,
                              ctypes.byref(n)) == _abi.ELIMIT
+
+
+def test_chunk_list_keeps_its_taper_beyond_the_headline_shard():
+    # 260 tensors of 20,971,520 (30 % more than the 201-tensor shard) still
+    # fit the plan's chunk limit with 16-tile chunks and the tapered end
+    spec = workloads.large_uniform(n_tensors=260)
+    tensors = _aligned_tensors(spec.sizes)
+    items, _ = _dry(tensors, 152)
+    chunks = _chunks(tensors, 152, PLAN_MAX_CHUNKS)
+    _check_chunk_cover(items, chunks)
+    sizes = [nt for _, _, nt in chunks]
+    assert max(sizes) == 16 and max(sizes[-152:]) <= TAPER_MIN

@@ -428,7 +428,7 @@ def test_plan_work_lists_match_the_host_dry_runs(name):
                             None, 0, None, ctypes.byref(n)) == _abi.OK, L.fadam_last_error()
     assert n.value == info["n_items"]
     assert L.fadam_chunk_dry(arr, len(descs), len(groups), p_dt, g_dt, o_dt, flags, info["grid"],
-                             65536, None, 0, ctypes.byref(n)) == _abi.OK, L.fadam_last_error()
+                             131072, None, 0, ctypes.byref(n)) == _abi.OK, L.fadam_last_error()
     assert n.value == info["n_chunks"]
     opt.close()
 
