@@ -63,6 +63,10 @@ def lib():
         L.oracle_adam_state.argtypes = [_i64, ctypes.c_int, ctypes.c_int, _i32, _f32, _f32,
                                         _f32, _f32, _f32, _f32, _vp, _vp, _vp, ctypes.c_int,
                                         _vp, ctypes.c_int, _vp, ctypes.c_int]
+        L.oracle_adam_moments.restype = None
+        L.oracle_adam_moments.argtypes = [_i64, ctypes.c_int, ctypes.c_int, _i32, _f32, _f32,
+                                          _f32, _f32, _f32, _f32, _vp, _vp, _vp, ctypes.c_int,
+                                          _vp, ctypes.c_int, _vp, ctypes.c_int]
         L.oracle_adam_f64.restype = None
         L.oracle_adam_f64.argtypes = [_i64, ctypes.c_int, ctypes.c_int, _i32, _f32, _f32,
                                       _f32, _f32, _f32, _f32, _vp, _vp, _vp, _vp]
@@ -194,6 +198,23 @@ def adam_state(group: Group, step: int, p, m, v, state_dtype, g, g_dtype=DT_F32,
                             g_dtype, _ptr(p_out) if out_dtype != DT_NONE else None, out_dtype)
 
 
+def adam_moments(group: Group, step: int, p, m, v, moment_dtype, g, g_dtype=DT_F32, p_out=None,
+                 out_dtype=DT_NONE) -> None:
+    """Update one tensor with an fp32 master p and 16-bit moments m, v of
+    `moment_dtype` (uint16 bits), in place."""
+    n = p.size
+    _check(p, np.float32, n, "p")
+    for a, w in ((m, "m"), (v, "v")):
+        _check(a, np.uint16, n, w)
+    _check(g, _G_NP[g_dtype], n, "g")
+    if out_dtype != DT_NONE:
+        _check(p_out, np.float32 if out_dtype == DT_F32 else np.uint16, n, "p_out")
+    lib().oracle_adam_moments(n, group.mode, group.bias_correction, step, group.beta1,
+                              group.beta2, group.eps, group.weight_decay, group.lr,
+                              group.grad_scale, _ptr(p), _ptr(m), _ptr(v), moment_dtype, _ptr(g),
+                              g_dtype, _ptr(p_out) if out_dtype != DT_NONE else None, out_dtype)
+
+
 def adam_rem(group: Group, step: int, p_hi, rem, m, v, g, g_dtype, p_out) -> None:
     """Update one tensor whose master is bf16 high half + int16 remainder."""
     n = p_hi.size
@@ -237,7 +258,8 @@ class Tensor:
     """One tensor of the shard, as numpy arrays updated in place.
 
     For an fp32 master set ``p``; for 16-bit state set ``p``, ``m``, ``v`` as
-    uint16 bits and ``state_dtype``; for the remainder form set ``p_hi``
+    uint16 bits and ``state_dtype``; for an fp32 master with 16-bit moments
+    set ``m``, ``v`` as uint16 bits and ``moment_dtype``; for the remainder form set ``p_hi``
     (bf16 bits) and ``rem`` and give ``p_out`` (bf16 bits, may be ``p_hi``).
     """
     group: int
@@ -251,6 +273,7 @@ class Tensor:
     p_out: Optional[np.ndarray] = None
     out_dtype: int = DT_NONE
     state_dtype: int = DT_F32  # dtype of p, m and v (fp32 master form)
+    moment_dtype: int = DT_NONE  # bf16 or fp16: m, v in it, fp32 p (else the state dtype)
     scales: Optional[np.ndarray] = None  # scaled 16-bit state: float32[3] (p, m, v)
 
 
@@ -299,6 +322,9 @@ def shard_step(shard: Shard, *, capturable: bool, noop: bool = False,
         elif t.scales is not None:
             adam_scaled(grp, step, t.p, t.m, t.v, t.scales, t.state_dtype, t.g, t.g_dtype,
                         t.p_out, t.out_dtype)
+        elif t.moment_dtype != DT_NONE:
+            adam_moments(grp, step, t.p, t.m, t.v, t.moment_dtype, t.g, t.g_dtype, t.p_out,
+                         t.out_dtype)
         elif t.state_dtype != DT_F32:
             adam_state(grp, step, t.p, t.m, t.v, t.state_dtype, t.g, t.g_dtype, t.p_out,
                        t.out_dtype)

@@ -265,6 +265,33 @@ void oracle_adam_state(int64_t n, int mode, int bias_correction, int32_t step, f
   }
 }
 
+/* One tensor with an fp32 master and moments of `moment_dtype` (bf16 or
+ * fp16): TransformerEngine's FusedAdam exp_avg_dtype and exp_avg_sq_dtype
+ * (constructor arguments of the "[Performance] FusedAdam capturable kernel"
+ * issue's adam_bench.py), taken equal.  m and v are widened to float, the
+ * update runs in float as above, p keeps the float result and m, v are
+ * rounded back to their dtype (to nearest, ties to even) when stored. */
+void oracle_adam_moments(int64_t n, int mode, int bias_correction, int32_t step, float beta1,
+                         float beta2, float eps, float wd, float lr, float grad_scale, float* p,
+                         void* m, void* v, int moment_dtype, const void* g, int g_dtype,
+                         void* p_out, int out_dtype) {
+  float bc1 = 1.0f, bc2 = 1.0f;
+  if (bias_correction == 1) {
+    bc1 = oracle_bias_correction(beta1, step);
+    bc2 = oracle_bias_correction(beta2, step);
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    float mi = value_at(m, moment_dtype, i);
+    float vi = value_at(v, moment_dtype, i);
+    float x = update_one(mode, beta1, beta2, eps, wd, lr, grad_scale, bc1, bc2, p[i], &mi, &vi,
+                         grad_at(g, g_dtype, i));
+    p[i] = x;
+    put_out(m, moment_dtype, i, mi);
+    put_out(v, moment_dtype, i, vi);
+    if (p_out) put_out(p_out, out_dtype, i, x);
+  }
+}
+
 /* One tensor whose fp32 master is held as a bf16 high half plus an int16
  * remainder.  p_hi is read (it is not written unless p_out aliases it),
  * rem, m and v are updated in place, p_out (bf16 bits) gets the new high

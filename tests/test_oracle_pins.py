@@ -555,6 +555,80 @@ def test_16bit_state_is_widen_update_round(state_dtype):
     assert np.array_equal(out, ref_out.view(np.uint16))
 
 
+# ---- fp32 master with 16-bit moments (exp_avg_dtype = exp_avg_sq_dtype) ---------
+
+@pytest.mark.parametrize("moment_dtype", [DT_BF16, DT_F16])
+@pytest.mark.parametrize("name,d", _worked_examples(), ids=[r[0] for r in _worked_examples()])
+def test_worked_example_16bit_moments_exact(name, d, moment_dtype):
+    """The worked examples' moments are exact in bf16 and fp16, so an fp32
+    master with 16-bit moments must reproduce them bit for bit too."""
+    mode = MODE_ADAMW if d["mode"] == "adamw" else MODE_L2
+    grp = Group(mode=mode, bias_correction=int(d["bc"]), beta1=float(d["beta1"]),
+                beta2=float(d["beta2"]), eps=float(d["eps"]), weight_decay=float(d["wd"]),
+                lr=float(d["lr"]), grad_scale=float(d["gs"]))
+    conv = oracle.f32_to_bf16 if moment_dtype == DT_BF16 else oracle.f32_to_f16
+    back = oracle.bf16_to_f32 if moment_dtype == DT_BF16 else oracle.f16_to_f32
+    p = np.array([float(d["p"])], np.float32)
+    m, v = (conv(np.array([float(d[k])], np.float32)) for k in ("m", "v"))
+    g = np.array([float(d["g"])], np.float32)
+    oracle.adam_moments(grp, int(d["step"]), p, m, v, moment_dtype, g, DT_F32)
+    assert p[0] == np.float32(d["p_new"]), name
+    assert back(m)[0] == np.float32(d["m_new"]), name
+    assert back(v)[0] == np.float32(d["v_new"]), name
+
+
+@pytest.mark.parametrize("moment_dtype", [DT_BF16, DT_F16])
+def test_16bit_moments_are_widen_update_round(moment_dtype):
+    """With 16-bit moments the fp32 master gets exactly the fp32 update of
+    the widened moments, and the new moments are that update's moments
+    rounded by torch's own conversion."""
+    n = 20_000
+    rng = np.random.default_rng(15)
+    tdt = torch.bfloat16 if moment_dtype == DT_BF16 else torch.float16
+
+    def to16(x):
+        return torch.from_numpy(np.asarray(x, np.float32)).to(tdt).view(torch.int16).numpy().view(np.uint16)
+
+    def to32(b):
+        return torch.from_numpy(b.view(np.int16).copy()).view(tdt).float().numpy()
+
+    p = rng.standard_normal(n).astype(np.float32)
+    m = to16(rng.standard_normal(n) * 1e-3)
+    v = to16(np.abs(rng.standard_normal(n)) * 1e-6)
+    g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    grp = Group(mode=MODE_ADAMW, weight_decay=0.1, beta1=0.9, beta2=0.95, lr=1e-3)
+    p32, m32, v32 = p.copy(), to32(m), to32(v)
+    out = np.zeros(n, np.uint16)
+    oracle.adam_moments(grp, 3, p, m, v, moment_dtype, g, DT_F32, out, DT_BF16)
+    oracle.adam_f32(grp, 3, p32, m32, v32, g, DT_F32)
+    assert p.tobytes() == p32.tobytes()
+    assert np.array_equal(m, to16(m32)) and np.array_equal(v, to16(v32))
+    ref_out = torch.from_numpy(p32.copy()).to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(out, ref_out.view(np.uint16))
+
+
+def test_16bit_moments_in_a_shard_step():
+    """shard_step takes the moments path for a tensor that names a moment dtype."""
+    n = 300
+    rng = np.random.default_rng(16)
+    p = rng.standard_normal(n).astype(np.float32)
+    g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    m = np.zeros(n, np.uint16)
+    v = np.zeros(n, np.uint16)
+    sh = oracle.Shard(groups=[Group(mode=MODE_ADAMW, weight_decay=0.1, lr=1e-3)],
+                      tensors=[oracle.Tensor(group=0, p=p, m=m, v=v, g=g,
+                                             moment_dtype=DT_BF16)])
+    ref = [p.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)]
+    for k in (1, 2):
+        oracle.shard_step(sh, capturable=False)
+        oracle.adam_f32(sh.groups[0], k, *ref, g, DT_F32)
+        ref[1] = oracle.bf16_to_f32(oracle.f32_to_bf16(ref[1]))
+        ref[2] = oracle.bf16_to_f32(oracle.f32_to_bf16(ref[2]))
+    assert p.tobytes() == ref[0].tobytes()
+    assert np.array_equal(oracle.bf16_to_f32(m), ref[1])
+    assert np.array_equal(oracle.bf16_to_f32(v), ref[2])
+
+
 def test_fp32_state_through_the_generic_path_matches_adam_f32():
     n = 5000
     p0, g = _rand_problem(n, 13)
