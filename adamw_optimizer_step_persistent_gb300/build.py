@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libfadam.so")
 
-SOURCES = ["fadam_plan.cu"] + [f"fadam_kernels_s{s}_g{g}.cu" for s in ("f32", "bf16", "f16")
+SOURCES = ["fadam_plan.cu"] + [f"fadam_kernels_s{s}_g{g}.cu"
+                               for s in ("f32", "bf16", "f16", "f32mbf16", "f32mf16")
                                for g in ("f32", "bf16", "f16")] + [
     f"fadam_kernels_scaled_s{s}_g{g}.cu" for s in ("bf16", "f16") for g in ("f32", "bf16", "f16")]
 HEADERS = ["fadam_internal.h", "fadam_kernel.cuh"]

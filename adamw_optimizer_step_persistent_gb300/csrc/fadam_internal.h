@@ -16,6 +16,18 @@ namespace fadam {
 constexpr int kBlock = FADAM_BLOCK;
 static_assert(kBlock % 32 == 0 && kBlock >= 32 && kBlock <= 1024,
               "threads per CTA: whole warps, at most 1024");
+// State forms of the kernel's ST template argument: FADAM_DT_F32, _BF16 or
+// _F16 mean p, m and v all of that dtype; these two mean an fp32 master with
+// m and v in bf16 or fp16 (exp_avg_dtype = exp_avg_sq_dtype).
+constexpr int kStateF32MomBF16 = 4;
+constexpr int kStateF32MomF16 = 5;
+__host__ __device__ constexpr int p_dtype_of(int st) {
+  return st == kStateF32MomBF16 || st == kStateF32MomF16 ? FADAM_DT_F32 : st;
+}
+__host__ __device__ constexpr int mv_dtype_of(int st) {
+  return st == kStateF32MomBF16 ? FADAM_DT_BF16 : st == kStateF32MomF16 ? FADAM_DT_F16 : st;
+}
+
 // Elements per vector access (one 16-byte fp32 vector).
 constexpr int kVec = 4;
 // Largest work item, in elements (keeps in-item indices in 32 bits).
@@ -158,6 +170,12 @@ FADAM_DECLARE_KERNELS(bf16, f16)
 FADAM_DECLARE_KERNELS(f16, f32)
 FADAM_DECLARE_KERNELS(f16, bf16)
 FADAM_DECLARE_KERNELS(f16, f16)
+FADAM_DECLARE_KERNELS(f32mbf16, f32)
+FADAM_DECLARE_KERNELS(f32mbf16, bf16)
+FADAM_DECLARE_KERNELS(f32mbf16, f16)
+FADAM_DECLARE_KERNELS(f32mf16, f32)
+FADAM_DECLARE_KERNELS(f32mf16, bf16)
+FADAM_DECLARE_KERNELS(f32mf16, f16)
 #undef FADAM_DECLARE_KERNELS
 
 // Scaled 16-bit state instances (state dtype bf16 or fp16), one function per

@@ -279,18 +279,19 @@ __device__ __forceinline__ void rem_split(float x, unsigned short& hi, unsigned 
 // folds |p'|, |m'|, |v'| into the thread's maxima `mx` (bit patterns), pass
 // B only the state, each new value times its new reciprocal scale.
 template <bool ADAMW, int ST, int GT, int OT, Pass PASS = Pass::kUpdate>
-__device__ __forceinline__ void update4_state(const typename Raw4<ST>::T& P,
-                                              const typename Raw4<ST>::T& M,
-                                              const typename Raw4<ST>::T& V,
+__device__ __forceinline__ void update4_state(const typename Raw4<p_dtype_of(ST)>::T& P,
+                                              const typename Raw4<mv_dtype_of(ST)>::T& M,
+                                              const typename Raw4<mv_dtype_of(ST)>::T& V,
                                               const typename Raw4<GT>::T& G, const Scal& s, void* p,
                                               void* m, void* v, void* out, int i, const Dests& d,
                                               const StateScale* sc = nullptr,
                                               unsigned* mx = nullptr) {
   float g[4], x[4], mm[4], vv[4];
   widen4<GT>(G, g);
-  widen4<ST>(P, x);
-  widen4<ST>(M, mm);
-  widen4<ST>(V, vv);
+  constexpr int PT = p_dtype_of(ST), MT = mv_dtype_of(ST);
+  widen4<PT>(P, x);
+  widen4<MT>(M, mm);
+  widen4<MT>(V, vv);
   if constexpr (PASS == Pass::kScaledA || PASS == Pass::kScaledB) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -316,13 +317,13 @@ __device__ __forceinline__ void update4_state(const typename Raw4<ST>::T& P,
       mm[e] = __fmul_rn(mm[e], sc->r[1]);
       vv[e] = __fmul_rn(vv[e], sc->r[2]);
     }
-    store_out4<ST>(p, i, x);
-    store_out4<ST>(m, i, mm);
-    store_out4<ST>(v, i, vv);
+    store_out4<PT>(p, i, x);
+    store_out4<MT>(m, i, mm);
+    store_out4<MT>(v, i, vv);
   } else {
-    store_out4<ST>(p, i, x);
-    store_out4<ST>(m, i, mm);
-    store_out4<ST>(v, i, vv);
+    store_out4<PT>(p, i, x);
+    store_out4<MT>(m, i, mm);
+    store_out4<MT>(v, i, vv);
     store_out4<OT>(out, i, x, &d);
   }
 }
@@ -393,9 +394,9 @@ __host__ __device__ constexpr int vec_bytes() { return DT == FADAM_DT_F32 ? 16 :
 // int16 remainders with fp32 m and v) and g of dtype GT.
 template <int ST, int GT, bool REM>
 struct Layout {
-  static constexpr int kP = REM ? 8 : vec_bytes<ST>();    // bytes per vector of p
+  static constexpr int kP = REM ? 8 : vec_bytes<p_dtype_of(ST)>();  // bytes per vector of p
   static constexpr int kR = REM ? 8 : 0;                  // ... of the remainders
-  static constexpr int kMV = REM ? 16 : vec_bytes<ST>();  // ... of m and of v
+  static constexpr int kMV = REM ? 16 : vec_bytes<mv_dtype_of(ST)>();  // ... of m and of v
   static constexpr int kG = vec_bytes<GT>();              // ... of g
   static constexpr unsigned per_vector = kP + kR + 2 * kMV + kG;
   // vectors of an update tile: two per thread when a vector carries at most
@@ -689,10 +690,11 @@ __device__ __forceinline__ void update_tile(const Item& it, const Scal& s, const
                              reinterpret_cast<float4*>(it.m), reinterpret_cast<float4*>(it.v),
                              reinterpret_cast<uint2*>(it.p_out), i, d);
     } else {
-      using S4 = typename Raw4<ST>::T;
-      const S4 P = reinterpret_cast<const S4*>(st)[t];
-      const S4 M = reinterpret_cast<const S4*>(st + L::off_m)[t];
-      const S4 V = reinterpret_cast<const S4*>(st + L::off_v)[t];
+      using P4 = typename Raw4<p_dtype_of(ST)>::T;
+      using M4 = typename Raw4<mv_dtype_of(ST)>::T;
+      const P4 P = reinterpret_cast<const P4*>(st)[t];
+      const M4 M = reinterpret_cast<const M4*>(st + L::off_m)[t];
+      const M4 V = reinterpret_cast<const M4*>(st + L::off_v)[t];
       update4_state<ADAMW, ST, GT, OT, PASS>(P, M, V, G, s, it.p, it.m, it.v, it.p_out, i, d, sc,
                                              mx);
     }
@@ -1160,7 +1162,8 @@ template <bool ADAMW, int ST, int GT, int OT, Pass PASS>
 __device__ __forceinline__ void update_elem_state(const Item& it, const Scal& s, int i,
                                                   const Dests& d, const StateScale* sc,
                                                   unsigned* mx) {
-  float m = load1<ST>(it.m, i), v = load1<ST>(it.v, i), x0 = load1<ST>(it.p, i);
+  constexpr int PT = p_dtype_of(ST), MT = mv_dtype_of(ST);
+  float m = load1<MT>(it.m, i), v = load1<MT>(it.v, i), x0 = load1<PT>(it.p, i);
   if constexpr (PASS == Pass::kScaledA || PASS == Pass::kScaledB) {
     x0 = __fmul_rn(x0, sc->s[0]);
     m = __fmul_rn(m, sc->s[1]);
@@ -1173,13 +1176,13 @@ __device__ __forceinline__ void update_elem_state(const Item& it, const Scal& s,
     mx[1] = max(mx[1], abs_bits(m));
     mx[2] = max(mx[2], abs_bits(v));
   } else if constexpr (PASS == Pass::kScaledB) {
-    store_out1<ST>(it.p, i, __fmul_rn(x, sc->r[0]));
-    store_out1<ST>(it.m, i, __fmul_rn(m, sc->r[1]));
-    store_out1<ST>(it.v, i, __fmul_rn(v, sc->r[2]));
+    store_out1<PT>(it.p, i, __fmul_rn(x, sc->r[0]));
+    store_out1<MT>(it.m, i, __fmul_rn(m, sc->r[1]));
+    store_out1<MT>(it.v, i, __fmul_rn(v, sc->r[2]));
   } else {
-    store_out1<ST>(it.p, i, x);
-    store_out1<ST>(it.m, i, m);
-    store_out1<ST>(it.v, i, v);
+    store_out1<PT>(it.p, i, x);
+    store_out1<MT>(it.m, i, m);
+    store_out1<MT>(it.v, i, v);
     store_out1<OT>(it.p_out, i, x, &d);
   }
 }
@@ -1247,15 +1250,16 @@ __device__ __forceinline__ void simt_item(const Item& it, const Scal& s, const D
           if (i < nv) update4_rem<ADAMW, GT>(H[u], R[u], M[u], V[u], G[u], s, r4, m4, v4, o4, i, d);
         }
       } else {
-        typename Raw4<ST>::T P[kUnroll], M[kUnroll], V[kUnroll];
+        typename Raw4<p_dtype_of(ST)>::T P[kUnroll];
+        typename Raw4<mv_dtype_of(ST)>::T M[kUnroll], V[kUnroll];
         typename Raw4<GT>::T G[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int i = base + u * kBlock;
           if (i < nv) {
-            P[u] = load4<ST>(it.p, i);
-            M[u] = load4<ST>(it.m, i);
-            V[u] = load4<ST>(it.v, i);
+            P[u] = load4<p_dtype_of(ST)>(it.p, i);
+            M[u] = load4<mv_dtype_of(ST)>(it.m, i);
+            V[u] = load4<mv_dtype_of(ST)>(it.v, i);
             G[u] = load4<GT>(it.g, i);
           }
         }
@@ -1665,9 +1669,14 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
 template <int ST, int GT>
 KernelEntry kernel_for(int out_dtype, bool remainders) {
   if (remainders) {
-    if (ST != FADAM_DT_F32 || out_dtype != FADAM_DT_BF16) return {nullptr, 0};
-    return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_BF16, true>),
-            smem_bytes<ST, GT, true>()};
+    // only the fp32 state form has a remainder instance
+    if constexpr (ST == FADAM_DT_F32) {
+      if (out_dtype != FADAM_DT_BF16) return {nullptr, 0};
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_BF16, true>),
+              smem_bytes<ST, GT, true>()};
+    } else {
+      return {nullptr, 0};
+    }
   }
   const size_t smem = smem_bytes<ST, GT, false>();
   switch (out_dtype) {

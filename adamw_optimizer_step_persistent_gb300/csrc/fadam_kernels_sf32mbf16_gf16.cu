@@ -1,0 +1,12 @@
+// Kernel instances for an fp32 master with bf16 moments (m, v) and
+// gradient dtype fp16: every param-out dtype.  One translation unit per
+// (state form, gradient) pair keeps the build parallel.
+#include "fadam_kernel.cuh"
+
+namespace fadam {
+
+KernelEntry kernel_sf32mbf16_gf16(int out_dtype, bool remainders) {
+  return kernel_for<kStateF32MomBF16, FADAM_DT_F16>(out_dtype, remainders);
+}
+
+}  // namespace fadam

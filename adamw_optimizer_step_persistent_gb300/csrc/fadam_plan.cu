@@ -87,15 +87,33 @@ struct DeviceGuard {
 struct Dtypes {
   int32_t p, g, out;  // p: the state dtype of p, m, v (bf16 high half in remainder form)
   bool rem;
+  int32_t mv = FADAM_DT_NONE;  // 16-bit moments under an fp32 master (FADAM_MOMENTS_*)
 };
 
-// Element size of m and v: the state dtype, or fp32 in the remainder form.
-int mv_size(const Dtypes& d) { return d.rem ? 4 : elem_size(d.p); }
+Dtypes make_dtypes(int32_t p, int32_t g, int32_t out, uint32_t flags) {
+  Dtypes d{p, g, out, (flags & FADAM_REMAINDERS) != 0};
+  if (flags & FADAM_MOMENTS_BF16) d.mv = FADAM_DT_BF16;
+  if (flags & FADAM_MOMENTS_F16) d.mv = FADAM_DT_F16;
+  return d;
+}
+
+// Element size of m and v: the state dtype, the moments' own dtype, or fp32
+// in the remainder form.
+int mv_size(const Dtypes& d) {
+  return d.rem ? 4 : elem_size(d.mv != FADAM_DT_NONE ? d.mv : d.p);
+}
 
 fadam_status check_dtypes(const Dtypes& d, uint32_t flags) {
   const uint32_t known = FADAM_CAPTURABLE | FADAM_REMAINDERS | FADAM_CHECK_FINITE |
-                         FADAM_STEP_PREADVANCED | FADAM_TEST_BARRIER_TIMEOUT | FADAM_SCALED_STATES;
+                         FADAM_STEP_PREADVANCED | FADAM_TEST_BARRIER_TIMEOUT |
+                         FADAM_SCALED_STATES | FADAM_MOMENTS_BF16 | FADAM_MOMENTS_F16;
   if (flags & ~known) return fail(FADAM_EINVAL, "unknown flag bits 0x%x", flags & ~known);
+  if ((flags & FADAM_MOMENTS_BF16) && (flags & FADAM_MOMENTS_F16))
+    return fail(FADAM_EINVAL, "FADAM_MOMENTS_BF16 and FADAM_MOMENTS_F16 exclude each other");
+  if (d.mv != FADAM_DT_NONE &&
+      (d.p != FADAM_DT_F32 || d.rem || (flags & FADAM_SCALED_STATES)))
+    return fail(FADAM_EDTYPE, "16-bit moments need an fp32 master (no remainders, no scaled "
+                              "states)");
   if ((flags & FADAM_STEP_PREADVANCED) && !(flags & FADAM_CAPTURABLE))
     return fail(FADAM_EINVAL, "FADAM_STEP_PREADVANCED needs FADAM_CAPTURABLE");
   if ((flags & FADAM_TEST_BARRIER_TIMEOUT) && !(flags & FADAM_CHECK_FINITE))
@@ -196,7 +214,8 @@ fadam_status check_tensors(const fadam_tensor* ts, int64_t n, int32_t n_groups, 
 double bytes_per_elem(const Dtypes& d) {
   const int gsz = elem_size(d.g);
   if (d.rem) return 2 + 2 + 2 + 2 + 8 + 8 + gsz;  // p_hi R, p_out W, rem R+W, m, v, g
-  return 6.0 * elem_size(d.p) + gsz + elem_size(d.out);  // p, m, v R+W, g R, p_out W
+  // p, m, v read and written, g read, p_out written
+  return 2.0 * elem_size(d.p) + 4.0 * mv_size(d) + gsz + elem_size(d.out);
 }
 
 struct PackItem {
@@ -329,6 +348,22 @@ KernelEntry select_kernel(const Dtypes& d, bool scaled) {
   // the remainder form keeps fp32 m and v: its kernels sit with fp32 state
   const int32_t st = d.rem ? FADAM_DT_F32 : d.p;
   const int key = st * 4 + d.g;
+  if (d.mv == FADAM_DT_BF16) {
+    switch (d.g) {
+      case FADAM_DT_F32: return kernel_sf32mbf16_gf32(d.out, false);
+      case FADAM_DT_BF16: return kernel_sf32mbf16_gbf16(d.out, false);
+      case FADAM_DT_F16: return kernel_sf32mbf16_gf16(d.out, false);
+      default: return {nullptr, 0};
+    }
+  }
+  if (d.mv == FADAM_DT_F16) {
+    switch (d.g) {
+      case FADAM_DT_F32: return kernel_sf32mf16_gf32(d.out, false);
+      case FADAM_DT_BF16: return kernel_sf32mf16_gbf16(d.out, false);
+      case FADAM_DT_F16: return kernel_sf32mf16_gf16(d.out, false);
+      default: return {nullptr, 0};
+    }
+  }
   if (scaled) {
     switch (key) {
       case FADAM_DT_BF16 * 4 + FADAM_DT_F32: return scaled_kernel_sbf16_gf32(d.out);
@@ -611,7 +646,7 @@ fadam_status fadam_plan_create(const fadam_tensor* tensors, int64_t n_tensors,
   t_last_error.clear();
   if (!plan_out) return fail(FADAM_EINVAL, "plan_out is NULL");
   *plan_out = nullptr;
-  const Dtypes d{p_dtype, g_dtype, out_dtype, (flags & FADAM_REMAINDERS) != 0};
+  const Dtypes d = make_dtypes(p_dtype, g_dtype, out_dtype, flags);
   fadam_plan* plan = new (std::nothrow) fadam_plan();
   if (!plan) return fail(FADAM_EINVAL, "out of host memory");
   // the host step of a regular plan is per-step data: checked at launch
@@ -1114,7 +1149,7 @@ fadam_status fadam_pack_dry(const fadam_tensor* tensors, int64_t n_tensors, int3
                             int32_t grid, fadam_pack_item* items_out, int64_t max_items,
                             int32_t* cta_begin_out, int64_t* n_items_out) {
   t_last_error.clear();
-  const Dtypes d{p_dtype, g_dtype, out_dtype, (flags & FADAM_REMAINDERS) != 0};
+  const Dtypes d = make_dtypes(p_dtype, g_dtype, out_dtype, flags);
   fadam_status st = check_dtypes(d, flags);
   if (st) return st;
   if (n_groups < 1 || n_groups > FADAM_MAX_GROUPS)
@@ -1148,7 +1183,7 @@ fadam_status fadam_chunk_dry(const fadam_tensor* tensors, int64_t n_tensors, int
                              int32_t grid, int64_t max_chunks, int32_t* chunks_out,
                              int64_t max_out, int64_t* n_chunks_out) {
   t_last_error.clear();
-  const Dtypes d{p_dtype, g_dtype, out_dtype, (flags & FADAM_REMAINDERS) != 0};
+  const Dtypes d = make_dtypes(p_dtype, g_dtype, out_dtype, flags);
   fadam_status st = check_dtypes(d, flags);
   if (st) return st;
   if (n_groups < 1 || n_groups > FADAM_MAX_GROUPS)
@@ -1257,7 +1292,7 @@ extern "C" fadam_status fadam_step_noalloc(const fadam_tensor* tensors, int64_t 
                                            uint32_t flags, int32_t* noop_dev,
                                            fadam_stream stream) {
   t_last_error.clear();
-  const Dtypes d{p_dtype, g_dtype, out_dtype, (flags & FADAM_REMAINDERS) != 0};
+  const Dtypes d = make_dtypes(p_dtype, g_dtype, out_dtype, flags);
   if (flags & FADAM_SCALED_STATES)
     return fail(FADAM_EINVAL, "scaled states need a plan (fadam_plan_set_state_scales)");
   if ((flags & FADAM_CHECK_FINITE) && !noop_dev)

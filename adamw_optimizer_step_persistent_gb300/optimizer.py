@@ -51,7 +51,8 @@ class FusedAdamShard:
     A group with empty lists is allowed; its step counter still advances.
     ``params`` are the masters and set the state dtype: fp32, bf16 or fp16,
     with ``exp_avgs`` and ``exp_avg_sqs`` of the same dtype (updated in
-    float, rounded back on store); in remainder mode they are the bf16 high
+    float, rounded back on store), or, under an fp32 master, both bf16 or
+    both fp16 (TransformerEngine's exp_avg_dtype and exp_avg_sq_dtype); in remainder mode they are the bf16 high
     halves (``remainders`` then holds the int16 low halves, the moments are
     fp32, and ``params_out`` the bf16 tensors that receive the new high
     halves; they may be ``params``).
@@ -81,6 +82,7 @@ class FusedAdamShard:
         descs = []
         g_dtype = out_dtype = None
         p_dtype = torch.bfloat16 if remainders else None
+        mv_dtype = None
         for gi, g in enumerate(self.groups):
             ps, ms, vs, gs = g["params"], g["exp_avgs"], g["exp_avg_sqs"], g["grads"]
             outs = g.get("params_out") or [None] * len(ps)
@@ -92,7 +94,12 @@ class FusedAdamShard:
                     if t is not None and (not t.is_contiguous() or t.device != self.device):
                         raise ValueError("tensors must be contiguous and on the shard's device")
                 p_dtype = p_dtype or p.dtype
-                mv_dtype = torch.float32 if remainders else p_dtype
+                # m and v: the state dtype, fp32 in remainder mode, or one
+                # 16-bit dtype under an fp32 master (exp_avg_dtype =
+                # exp_avg_sq_dtype)
+                if mv_dtype is None:
+                    mv_dtype = torch.float32 if remainders else (
+                        m.dtype if p_dtype == torch.float32 else p_dtype)
                 if p.dtype != p_dtype or m.dtype != mv_dtype or v.dtype != mv_dtype:
                     raise TypeError(f"group {gi}: p must be {p_dtype}, m and v {mv_dtype}")
                 g_dtype = g_dtype or gr.dtype
@@ -110,6 +117,13 @@ class FusedAdamShard:
         self.n_tensors = len(descs)
         p_dtype = p_dtype or torch.float32
         self.state_dtype = p_dtype
+        self.moment_dtype = None
+        if not remainders and p_dtype == torch.float32 and mv_dtype not in (None, torch.float32):
+            if mv_dtype not in (torch.bfloat16, torch.float16):
+                raise TypeError(f"moments of dtype {mv_dtype} under an fp32 master")
+            self.moment_dtype = mv_dtype
+            flags |= _abi.MOMENTS_BF16 if mv_dtype == torch.bfloat16 else _abi.MOMENTS_F16
+            self.flags = flags
         self.g_dtype = g_dtype or torch.float32
         self.out_dtype = out_dtype
 

@@ -336,6 +336,9 @@ def run_gpu(args):
     if args.workload == "large_uniform":
         spec = workloads.large_uniform(n_tensors=args.n_tensors or 201, numel=args.numel,
                                        seed=1237 + 1000 * rank)
+    elif args.workload == "large_uniform_bf16_moments":
+        spec = workloads.large_uniform(n_tensors=args.n_tensors or 201, numel=args.numel,
+                                       seed=1237 + 1000 * rank, moment_dtype=torch.bfloat16)
     elif args.workload == "large_uniform_bf16_state" and args.n_tensors:
         spec = workloads.large_uniform(n_tensors=args.n_tensors, numel=args.numel,
                                        seed=1237 + 1000 * rank, state_dtype=torch.bfloat16,
@@ -516,9 +519,11 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="large_uniform",
                     choices=["large_uniform", "capturable_l2", "remainder_shard", "many_small",
-                             "large_uniform_bf16_state", "exchange_shard", "scaled_state_shard"])
+                             "large_uniform_bf16_state", "large_uniform_bf16_moments",
+                             "exchange_shard", "scaled_state_shard"])
     ap.add_argument("--n-tensors", type=int, default=None,
-                    help="tensor count of large_uniform[_bf16_state] (201) or many_small (20000)")
+                    help="tensor count of large_uniform[_bf16_state|_bf16_moments] (201) or "
+                         "many_small (20000)")
     ap.add_argument("--numel", type=int, default=320 * 65536)
     ap.add_argument("--total", type=int, default=None,
                     help="elements of the remainder_shard bucket (1,200,000,000)")

@@ -90,6 +90,16 @@ typedef int32_t fadam_status;
                                      caller; use it as is and do not write it */
 #define FADAM_SCALED_STATES 16u /* 16-bit p, m, v stored with one fp32 scale each
                                    per tensor (fadam_plan_set_state_scales) */
+/* An fp32 master (p_dtype FADAM_DT_F32) with both moments, m and v, in bf16
+ * or in fp16: TransformerEngine's FusedAdam exp_avg_dtype and
+ * exp_avg_sq_dtype (constructor arguments in the adam_bench.py script of
+ * "[Performance] FusedAdam capturable kernel is ~1.9x slower than regular
+ * Adam on GB300"), taken equal.  m and v are widened to float, the update
+ * runs in float as for an fp32 state, p keeps the float result and m, v are
+ * rounded to nearest-even when stored.  Not with FADAM_REMAINDERS or
+ * FADAM_SCALED_STATES. */
+#define FADAM_MOMENTS_BF16 32u
+#define FADAM_MOMENTS_F16 64u
 /* Diagnostic, for testing the failure path: with FADAM_CHECK_FINITE, the
  * grid barrier after the inf/nan screen waits for one more CTA than the
  * launch has, so every CTA's wait runs out after its limit (about 2 s).
@@ -112,7 +122,8 @@ typedef int32_t fadam_status;
  *          updated in place; in FADAM_REMAINDERS mode the bf16 high half of
  *          the master (read only, unless p_out aliases it)
  *   m, v   first and second moments (exp_avg, exp_avg_sq) in the state
- *          dtype (fp32 in FADAM_REMAINDERS mode), in place
+ *          dtype (fp32 in FADAM_REMAINDERS mode; bf16 or fp16 with
+ *          FADAM_MOMENTS_BF16 / _F16), in place
  *   g      gradient in the plan's g dtype, read only
  *   p_out  param-out copy in the plan's out dtype; NULL iff the out dtype
  *          is FADAM_DT_NONE; may alias p; required (bf16) in remainder mode
@@ -192,7 +203,9 @@ typedef struct {
  *   flags               FADAM_CAPTURABLE | FADAM_REMAINDERS |
  *                       FADAM_CHECK_FINITE | FADAM_STEP_PREADVANCED |
  *                       FADAM_SCALED_STATES (bf16 or fp16 state only; set
- *                       the scales with fadam_plan_set_state_scales)
+ *                       the scales with fadam_plan_set_state_scales) |
+ *                       FADAM_MOMENTS_BF16 or FADAM_MOMENTS_F16 (fp32 master
+ *                       with m and v in that dtype)
  *   *plan_out           receives the plan (owned by the caller; free with
  *                       fadam_plan_destroy)
  * Errors: FADAM_EINVAL, FADAM_EDTYPE, FADAM_EALIGN, FADAM_ELIMIT, FADAM_ECUDA;

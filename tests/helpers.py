@@ -68,6 +68,8 @@ def oracle_shard(shard: workloads.Shard, idx: List[int] = None, elems: Dict[int,
         else:
             t.p = to_np(sel(shard.params[i]))
             t.state_dtype = _ODT[spec.state_dtype]
+            if spec.moment_dtype is not None:
+                t.moment_dtype = _ODT[spec.moment_dtype]
             if scales is not None:  # [n, 3] in the order of idx
                 t.scales = to_np(scales[len(tensors)]).copy()
             if spec.out_dtype is not None:
@@ -164,8 +166,13 @@ def compare(shard: workloads.Shard, osh: oracle.Shard, idx=None, elems=None,
                 report.ulp16(to_np(sel(shard.params_out[i])), t.p_out, f"tensor {i} p_out",
                              spec.out_dtype)
             continue
-        report.f32(to_np(sel(shard.exp_avgs[i])), t.m, f"tensor {i} m")
-        report.f32(to_np(sel(shard.exp_avg_sqs[i])), t.v, f"tensor {i} v")
+        if spec.moment_dtype is not None:  # 16-bit moments under an fp32 master
+            mdt = spec.moment_dtype
+            report.ulp16(to_np(sel(shard.exp_avgs[i])), t.m, f"tensor {i} m", mdt)
+            report.ulp16(to_np(sel(shard.exp_avg_sqs[i])), t.v, f"tensor {i} v", mdt)
+        else:
+            report.f32(to_np(sel(shard.exp_avgs[i])), t.m, f"tensor {i} m")
+            report.f32(to_np(sel(shard.exp_avg_sqs[i])), t.v, f"tensor {i} v")
         if spec.remainders:
             hi = to_np(sel(shard.params[i]))
             rem = to_np(sel(shard.remainders[i]))

@@ -88,6 +88,9 @@ def _create(tensors, groups, p=_abi.DT_F32, g=_abi.DT_F32, out=_abi.DT_NONE, fla
     ("negative_eps", _abi.EINVAL), ("nan_lr", _abi.EINVAL),
     ("capturable_without_step_dev", _abi.EINVAL), ("capturable_without_lr_dev", _abi.EINVAL),
     ("misaligned_step_dev", _abi.EALIGN),
+    ("both_moment_flags", _abi.EINVAL), ("moments_need_fp32_master", _abi.EDTYPE),
+    ("moments_not_with_remainders", _abi.EDTYPE), ("moments_not_with_scaled", _abi.EDTYPE),
+    ("misaligned_16bit_moment", _abi.EALIGN),
 ])
 def test_plan_create_rejects(case, want):
     t, g, kw = [_tensor()], [_group()], {}
@@ -104,7 +107,19 @@ def test_plan_create_rejects(case, want):
     elif case == "rem_needs_bf16_out":
         kw.update(flags=_abi.REMAINDERS, p=_abi.DT_BF16, out=_abi.DT_F32)
     elif case == "unknown_flag":
-        kw["flags"] = 64
+        kw["flags"] = 1 << 10
+    elif case == "both_moment_flags":
+        kw["flags"] = _abi.MOMENTS_BF16 | _abi.MOMENTS_F16
+    elif case == "moments_need_fp32_master":
+        kw.update(flags=_abi.MOMENTS_BF16, p=_abi.DT_BF16)
+    elif case == "moments_not_with_remainders":
+        kw.update(flags=_abi.MOMENTS_BF16 | _abi.REMAINDERS, p=_abi.DT_BF16, out=_abi.DT_BF16)
+        t = [_tensor(rem=FAKE + (6 << 28), out=FAKE + (5 << 28))]
+    elif case == "moments_not_with_scaled":
+        kw.update(flags=_abi.MOMENTS_F16 | _abi.SCALED_STATES)
+    elif case == "misaligned_16bit_moment":
+        t = [_tensor(v=FAKE + 1)]
+        kw["flags"] = _abi.MOMENTS_F16
     elif case == "preadvanced_needs_capturable":
         kw["flags"] = _abi.STEP_PREADVANCED
     elif case == "group_out_of_range":

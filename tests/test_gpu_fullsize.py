@@ -70,6 +70,14 @@ def test_large_uniform_full_size():
     print(f"large_uniform: {rep.n} sampled values, {rep.exact_fraction:.6f} bit-identical")
 
 
+def test_large_uniform_bf16_moments_full_size():
+    # the 201-tensor shard with an fp32 master and bf16 moments, capturable
+    spec = workloads.large_uniform(moment_dtype=torch.bfloat16)
+    rep, steps, want = _sampled_run(spec, 2, per_tensor=2048, capturable=True)
+    assert steps == want == [2]
+    assert rep.exact_fraction == 1.0
+
+
 def test_capturable_l2_full_size_with_inf_step():
     spec = workloads.capturable_l2()
     rep, steps, want = _sampled_run(spec, 5, per_tensor=4096, inf_step=spec.inf_at_step)

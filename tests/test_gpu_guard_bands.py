@@ -92,14 +92,14 @@ def _group(lists, **kw):
     return d
 
 
-def _update_lists(arena, state_dtype, g_dtype, out_dtype):
+def _update_lists(arena, state_dtype, g_dtype, out_dtype, moment_dtype=None):
     gen = torch.Generator(device=DEV)
     gen.manual_seed(7)
     L = {"params": [], "exp_avgs": [], "exp_avg_sqs": [], "grads": [], "params_out": []}
     for n, sp, sq, so in zip(SIZES, SHIFT_P, SHIFT_Q, SHIFT_O):
         p = arena.view(n, state_dtype, sp)
-        m = arena.view(n, state_dtype, sq)
-        v = arena.view(n, state_dtype, sq)
+        m = arena.view(n, moment_dtype or state_dtype, sq)
+        v = arena.view(n, moment_dtype or state_dtype, sq)
         g = arena.view(n, g_dtype, sq)
         _fill(p, m, v, g, gen)
         L["params"].append(p)
@@ -129,6 +129,18 @@ def test_update_writes_only_its_tensors(state_dtype, g_dtype, out_dtype, captura
     for _ in range(3):
         opt.step()
     opt.grad_norm_sq()
+    arena.check()
+    opt.close()
+
+
+@pytest.mark.parametrize("moment_dtype", [torch.bfloat16, torch.float16])
+def test_16bit_moments_write_only_their_tensors(moment_dtype):
+    arena = Arena(16)
+    L = _update_lists(arena, torch.float32, torch.bfloat16, torch.bfloat16, moment_dtype)
+    opt = FusedAdamShard([_group(L)], capturable=True, check_finite=True)
+    arena.seal()
+    for _ in range(3):
+        opt.step()
     arena.check()
     opt.close()
 

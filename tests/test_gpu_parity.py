@@ -388,6 +388,61 @@ def test_16bit_state_matches_oracle(state_dtype, g_dtype, out_dtype):
         assert rep.exact_fraction == 1.0, rep.exact_fraction
 
 
+@pytest.mark.parametrize("moment_dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("g_dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("out_dtype", [None, torch.bfloat16])
+def test_16bit_moments_match_oracle(moment_dtype, g_dtype, out_dtype):
+    """An fp32 master with m and v in one 16-bit dtype (exp_avg_dtype =
+    exp_avg_sq_dtype), several steps, ragged sizes, both modes and bias
+    corrections, regular and capturable."""
+    spec = workloads.large_uniform(n_tensors=3, numel=40_003, g_dtype=g_dtype,
+                                   moment_dtype=moment_dtype)
+    spec.sizes = [40_003, 7, 131_072 + 5]
+    spec.group_of = [0, 1, 1]
+    spec.groups = [spec.groups[0], workloads.GroupSpec(adam_w_mode=False, weight_decay=0.05,
+                                                       bias_correction=False)]
+    spec.out_dtype = out_dtype
+    for capturable in (False, True):
+        shard, opt, osh = _run(spec, 4, capturable=capturable)
+        assert opt.moment_dtype == moment_dtype
+        rep = helpers.compare(shard, osh)
+        assert opt.group_steps() == [4, 4]
+        assert rep.exact_fraction == 1.0, rep.exact_fraction
+
+
+def test_16bit_moments_regular_capturable_and_graph_are_bit_identical():
+    spec = workloads.small_versions()["many_small"]
+    spec.moment_dtype = torch.bfloat16
+    outs = []
+    for mode in ("regular", "capturable", "graph"):
+        shard = workloads.materialize(spec, DEV)
+        opt = FusedAdamShard(shard.param_groups(), capturable=mode != "regular",
+                             grad_scale=spec.grad_scale)
+        if mode == "graph":
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                opt.step()
+            torch.cuda.current_stream().wait_stream(s)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                opt.step()
+            for _ in range(2):
+                graph.replay()
+        else:
+            for _ in range(3):
+                opt.step()
+        torch.cuda.synchronize()
+        outs.append([t.clone() for t in shard.params + shard.exp_avgs + shard.exp_avg_sqs])
+        opt.close()
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a.view(torch.int16) if a.dtype != torch.float32 else a.view(torch.int32),
+                           b.view(torch.int16) if b.dtype != torch.float32 else b.view(torch.int32))
+    for a, c in zip(outs[1], outs[2]):
+        assert torch.equal(a.view(torch.int16) if a.dtype != torch.float32 else a.view(torch.int32),
+                           c.view(torch.int16) if c.dtype != torch.float32 else c.view(torch.int32))
+
+
 def test_16bit_state_shard_full_oracle_and_graph():
     spec = workloads.small_versions()["many_small"]
     spec.state_dtype = torch.bfloat16
@@ -484,13 +539,17 @@ def test_special_values_and_extreme_hyper_parameters(start_step):
     assert rep.exact_fraction == 1.0
 
 
-@pytest.mark.parametrize("form", ["bf16_state_fp16_grads", "remainders"])
+@pytest.mark.parametrize("form", ["bf16_state_fp16_grads", "remainders", "fp16_moments"])
 def test_special_values_in_16bit_and_remainder_forms(form):
     # the special values again, stored in the 16-bit state (bf16, with fp16
     # gradients, so 3.4e38 becomes an fp16 infinity) or in the bf16 high
     # halves of the remainder form
     if form == "remainders":
         spec = workloads.small_versions()["remainder_shard"]
+    elif form == "fp16_moments":
+        spec = workloads.large_uniform(n_tensors=3, numel=40_003, g_dtype=torch.bfloat16,
+                                       moment_dtype=torch.float16)
+        spec.out_dtype = torch.bfloat16
     else:
         spec = workloads.large_uniform(n_tensors=3, numel=40_003, state_dtype=torch.bfloat16,
                                        g_dtype=torch.float16)

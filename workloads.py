@@ -96,6 +96,7 @@ class ShardSpec:
     exchange_average: bool = True  # ReduceOp.AVG (else SUM)
     exchange_align: int = 64   # fragment starts rounded up to this many elements
     scaled_state: bool = False  # p, m, v in state_dtype with one fp32 scale each per tensor
+    moment_dtype: Optional[torch.dtype] = None  # m, v in bf16 or fp16 under an fp32 master
     scale_of: tuple = (1e-3, 1e-6, 1e-9)  # the scales drawn states are stored with
     notes: Dict = field(default_factory=dict)
 
@@ -126,11 +127,13 @@ def capturable_l2(layers: int = 8, hidden: int = 4096, ffn: int = 11008,
 
 def large_uniform(n_tensors: int = 201, numel: int = 320 * 65536, seed: int = 1237,
                   state_dtype: torch.dtype = torch.float32,
-                  g_dtype: torch.dtype = torch.float32) -> ShardSpec:
+                  g_dtype: torch.dtype = torch.float32,
+                  moment_dtype: Optional[torch.dtype] = None) -> ShardSpec:
     g = GroupSpec(adam_w_mode=True, lr=1.6e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1)
-    name = "large_uniform" if state_dtype == torch.float32 else "large_uniform_16bit_state"
+    name = ("large_uniform_16bit_moments" if moment_dtype is not None else
+            "large_uniform" if state_dtype == torch.float32 else "large_uniform_16bit_state")
     return ShardSpec(name, [g], [numel] * n_tensors, [0] * n_tensors, g_dtype=g_dtype,
-                     state_dtype=state_dtype, grad_std=1e-3, seed=seed)
+                     state_dtype=state_dtype, grad_std=1e-3, seed=seed, moment_dtype=moment_dtype)
 
 
 def remainder_shard(total: int = 1_200_000_000, n_views: int = 512, lo: int = 4096,
@@ -331,10 +334,11 @@ def materialize(spec: ShardSpec, device="cuda") -> Shard:
             g = buckets["g"][o:o + s]
         else:
             sdt = torch.float32 if spec.remainders else spec.state_dtype
+            mdt = spec.moment_dtype if spec.moment_dtype is not None else sdt
             p = torch.empty(s, dtype=torch.bfloat16 if spec.remainders else sdt, device=dev)
             r = torch.empty(s, dtype=torch.int16, device=dev) if spec.remainders else None
-            m = torch.zeros(s, dtype=sdt, device=dev)
-            v = torch.zeros(s, dtype=sdt, device=dev)
+            m = torch.zeros(s, dtype=mdt, device=dev)
+            v = torch.zeros(s, dtype=mdt, device=dev)
             g = torch.empty(s, dtype=spec.g_dtype, device=dev)
             if xoff is not None:
                 g = buckets["g"][xoff[i]:xoff[i] + s]
