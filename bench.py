@@ -336,6 +336,9 @@ def run_gpu(args):
     if args.workload == "large_uniform":
         spec = workloads.large_uniform(n_tensors=args.n_tensors or 201, numel=args.numel,
                                        seed=1237 + 1000 * rank)
+    elif args.workload == "large_uniform_bf16_out":
+        spec = workloads.large_uniform(n_tensors=args.n_tensors or 201, numel=args.numel,
+                                       seed=1237 + 1000 * rank, out_dtype=torch.bfloat16)
     elif args.workload == "large_uniform_bf16_moments":
         spec = workloads.large_uniform(n_tensors=args.n_tensors or 201, numel=args.numel,
                                        seed=1237 + 1000 * rank, moment_dtype=torch.bfloat16)
@@ -520,9 +523,10 @@ def main(argv=None):
     ap.add_argument("--workload", default="large_uniform",
                     choices=["large_uniform", "capturable_l2", "remainder_shard", "many_small",
                              "large_uniform_bf16_state", "large_uniform_bf16_moments",
+                             "large_uniform_bf16_out",
                              "exchange_shard", "scaled_state_shard"])
     ap.add_argument("--n-tensors", type=int, default=None,
-                    help="tensor count of large_uniform[_bf16_state|_bf16_moments] (201) or "
+                    help="tensor count of large_uniform[_bf16_state|_bf16_moments|_bf16_out] (201) or "
                          "many_small (20000)")
     ap.add_argument("--numel", type=int, default=320 * 65536)
     ap.add_argument("--total", type=int, default=None,

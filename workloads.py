@@ -128,12 +128,16 @@ def capturable_l2(layers: int = 8, hidden: int = 4096, ffn: int = 11008,
 def large_uniform(n_tensors: int = 201, numel: int = 320 * 65536, seed: int = 1237,
                   state_dtype: torch.dtype = torch.float32,
                   g_dtype: torch.dtype = torch.float32,
-                  moment_dtype: Optional[torch.dtype] = None) -> ShardSpec:
+                  moment_dtype: Optional[torch.dtype] = None,
+                  out_dtype: Optional[torch.dtype] = None) -> ShardSpec:
     g = GroupSpec(adam_w_mode=True, lr=1.6e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1)
     name = ("large_uniform_16bit_moments" if moment_dtype is not None else
             "large_uniform" if state_dtype == torch.float32 else "large_uniform_16bit_state")
+    if out_dtype is not None:
+        name += "_param_out"
     return ShardSpec(name, [g], [numel] * n_tensors, [0] * n_tensors, g_dtype=g_dtype,
-                     state_dtype=state_dtype, grad_std=1e-3, seed=seed, moment_dtype=moment_dtype)
+                     out_dtype=out_dtype, state_dtype=state_dtype, grad_std=1e-3, seed=seed,
+                     moment_dtype=moment_dtype)
 
 
 def remainder_shard(total: int = 1_200_000_000, n_views: int = 512, lo: int = 4096,
