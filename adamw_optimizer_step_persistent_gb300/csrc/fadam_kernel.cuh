@@ -43,6 +43,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "fadam_internal.h"
 
 namespace fadam {
@@ -239,16 +241,23 @@ __device__ __forceinline__ unsigned abs_bits(float x) { return __float_as_uint(x
 
 // ---- the update of one element ---------------------------------------------
 
+// Bias corrections equal to 1 in float: with bias correction off, and once
+// beta^step has fallen below half an ulp of 1 (from step 165 for beta 0.9,
+// 338 for 0.95, 17,321 for 0.999), the division by the correction is
+// an IEEE identity.  A UNIT mask names the divisions an instance leaves out;
+// the result is the same bits either way.
+enum : int { kUnitBc1 = 1, kUnitBc2 = 2 };
+
 // p' for the fp32 master x; m and v are updated in place.
-template <bool ADAMW>
+template <bool ADAMW, int UNIT = 0>
 __device__ __forceinline__ float adam_elem(float x, float& m, float& v, float g, const Scal& s) {
   float sg = __fmul_rn(g, s.gs);
   if constexpr (!ADAMW) sg = __fadd_rn(sg, __fmul_rn(s.wd, x));
   const float sq = __fmul_rn(sg, sg);
   const float m_next = __fadd_rn(__fmul_rn(s.beta1, m), __fmul_rn(s.omb1, sg));
   const float v_next = __fadd_rn(__fmul_rn(s.beta2, v), __fmul_rn(s.omb2, sq));
-  const float m_hat = __fdiv_rn(m_next, s.bc1);
-  const float v_hat = __fdiv_rn(v_next, s.bc2);
+  const float m_hat = (UNIT & kUnitBc1) ? m_next : __fdiv_rn(m_next, s.bc1);
+  const float v_hat = (UNIT & kUnitBc2) ? v_next : __fdiv_rn(v_next, s.bc2);
   const float denom = __fadd_rn(__fsqrt_rn(v_hat), s.eps);
   float upd = __fdiv_rn(m_hat, denom);
   if constexpr (ADAMW) upd = __fadd_rn(upd, __fmul_rn(s.wd, x));
@@ -278,7 +287,7 @@ __device__ __forceinline__ void rem_split(float x, unsigned short& hi, unsigned 
 // multiplied by the tensor's scales; pass A then writes only param-out and
 // folds |p'|, |m'|, |v'| into the thread's maxima `mx` (bit patterns), pass
 // B only the state, each new value times its new reciprocal scale.
-template <bool ADAMW, int ST, int GT, int OT, Pass PASS = Pass::kUpdate>
+template <bool ADAMW, int ST, int GT, int OT, Pass PASS = Pass::kUpdate, int UNIT = 0>
 __device__ __forceinline__ void update4_state(const typename Raw4<p_dtype_of(ST)>::T& P,
                                               const typename Raw4<mv_dtype_of(ST)>::T& M,
                                               const typename Raw4<mv_dtype_of(ST)>::T& V,
@@ -301,7 +310,7 @@ __device__ __forceinline__ void update4_state(const typename Raw4<p_dtype_of(ST)
     }
   }
 #pragma unroll
-  for (int e = 0; e < 4; ++e) x[e] = adam_elem<ADAMW>(x[e], mm[e], vv[e], g[e], s);
+  for (int e = 0; e < 4; ++e) x[e] = adam_elem<ADAMW, UNIT>(x[e], mm[e], vv[e], g[e], s);
   if constexpr (PASS == Pass::kScaledA) {
     store_out4<OT>(out, i, x, &d);
 #pragma unroll
@@ -666,7 +675,8 @@ __device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, un
 // Consume one tile from shared memory: thread t takes vectors t, t + kTile,
 // ... of it.  DESTS: param-out also goes to the exchange destinations (a
 // separate instance, so the plain step carries no destination loop).
-template <bool ADAMW, int ST, int GT, int OT, bool REM, bool DESTS, Pass PASS = Pass::kUpdate>
+template <bool ADAMW, int ST, int GT, int OT, bool REM, bool DESTS, Pass PASS = Pass::kUpdate,
+          int UNIT = 0>
 __device__ __forceinline__ void update_tile(const Item& it, const Scal& s, const unsigned char* st,
                                             int v0, int len, const Dests& d0,
                                             const StateScale* sc = nullptr, unsigned* mx = nullptr) {
@@ -695,11 +705,23 @@ __device__ __forceinline__ void update_tile(const Item& it, const Scal& s, const
       const P4 P = reinterpret_cast<const P4*>(st)[t];
       const M4 M = reinterpret_cast<const M4*>(st + L::off_m)[t];
       const M4 V = reinterpret_cast<const M4*>(st + L::off_v)[t];
-      update4_state<ADAMW, ST, GT, OT, PASS>(P, M, V, G, s, it.p, it.m, it.v, it.p_out, i, d, sc,
-                                             mx);
+      update4_state<ADAMW, ST, GT, OT, PASS, UNIT>(P, M, V, G, s, it.p, it.m, it.v, it.p_out, i,
+                                                   d, sc, mx);
     }
   }
 }
+
+// The 16-bit state forms are bound by instruction issue, not by memory:
+// their update passes have instances without the divisions by bias
+// corrections equal to 1 in every group (a launch-wide choice, so that each
+// instance is a loop of its own).  Every other form keeps one instance (its
+// divisions issue within the memory time).
+template <int ST, bool REM>
+__host__ __device__ constexpr bool unit_bc_instances() {
+  return !REM && (ST == FADAM_DT_BF16 || ST == FADAM_DT_F16);
+}
+
+
 
 // ---- the reduce-scatter stand-in ---------------------------------------------
 //
@@ -1050,7 +1072,7 @@ __device__ __forceinline__ void norm_tile(const unsigned char* st, const TileTag
 // of the next chunk start while the current one is consumed).  `bad`
 // collects the scan's finding; a wait that gives up sets `timed_out` and
 // ends the pass for the CTA.
-template <int ST, int GT, int OT, bool REM, Pass PASS, int NS>
+template <int ST, int GT, int OT, bool REM, Pass PASS, int NS, int UNIT = 0>
 __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp, unsigned* counter,
                                           unsigned char* smem, uint64_t* full, TileTag* tags,
                                           Producer& pr, double* red, unsigned& stage, bool& bad,
@@ -1107,17 +1129,20 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
         } else if constexpr (PASS == Pass::kScaledA || PASS == Pass::kScaledB) {
           const StateScale sc = tag.sc;
           if (G.bits & kGroupAdamW)
-            update_tile<true, ST, GT, OT, REM, true, PASS>(it, s, st, tag.v0, tag.len, dst, &sc, mx);
+            update_tile<true, ST, GT, OT, REM, true, PASS, UNIT>(it, s, st, tag.v0, tag.len, dst,
+                                                                 &sc, mx);
           else
-            update_tile<false, ST, GT, OT, REM, true, PASS>(it, s, st, tag.v0, tag.len, dst, &sc, mx);
+            update_tile<false, ST, GT, OT, REM, true, PASS, UNIT>(it, s, st, tag.v0, tag.len, dst,
+                                                                  &sc, mx);
         } else {
           const bool aw = (G.bits & kGroupAdamW) != 0;
+          constexpr Pass U = Pass::kUpdate;
           if (dst.n == 0) {
-            if (aw) update_tile<true, ST, GT, OT, REM, false>(it, s, st, tag.v0, tag.len, dst);
-            else update_tile<false, ST, GT, OT, REM, false>(it, s, st, tag.v0, tag.len, dst);
+            if (aw) update_tile<true, ST, GT, OT, REM, false, U, UNIT>(it, s, st, tag.v0, tag.len, dst);
+            else update_tile<false, ST, GT, OT, REM, false, U, UNIT>(it, s, st, tag.v0, tag.len, dst);
           } else {
-            if (aw) update_tile<true, ST, GT, OT, REM, true>(it, s, st, tag.v0, tag.len, dst);
-            else update_tile<false, ST, GT, OT, REM, true>(it, s, st, tag.v0, tag.len, dst);
+            if (aw) update_tile<true, ST, GT, OT, REM, true, U, UNIT>(it, s, st, tag.v0, tag.len, dst);
+            else update_tile<false, ST, GT, OT, REM, true, U, UNIT>(it, s, st, tag.v0, tag.len, dst);
           }
         }
       }
@@ -1419,7 +1444,7 @@ __device__ __forceinline__ bool rest_pass(const KParams& kp, const SGroup* sgrp,
 
 // One full pass: the bulk tiles of the shard (dynamically shared), then
 // the rest of this CTA's items.
-template <int ST, int GT, int OT, bool REM, Pass PASS, int NS>
+template <int ST, int GT, int OT, bool REM, Pass PASS, int NS, int UNIT = 0>
 __device__ __forceinline__ void run_pass(const KParams& kp, const SGroup* sgrp, int item_begin,
                                          int item_end, unsigned* counter, unsigned* tail_counter,
                                          int n_items, unsigned char* smem, uint64_t* full,
@@ -1427,8 +1452,8 @@ __device__ __forceinline__ void run_pass(const KParams& kp, const SGroup* sgrp, 
                                          unsigned& stage, bool& bad, bool& timed_out) {
   const bool bulk = FADAM_BULK && !(kp.flags & kHostGrads);
   if (bulk && kp.n_chunks > 0 && !timed_out)
-    bulk_pass<ST, GT, OT, REM, PASS, NS>(kp, sgrp, counter, smem, full, tags, pr, red, stage, bad,
-                                     timed_out);
+    bulk_pass<ST, GT, OT, REM, PASS, NS, UNIT>(kp, sgrp, counter, smem, full, tags, pr, red, stage,
+                                               bad, timed_out);
   if (bulk) bad |= tail_pass<ST, GT, OT, REM, PASS>(kp, sgrp, tail_counter, n_items);
   bad |= rest_pass<ST, GT, OT, REM, PASS>(kp, sgrp, item_begin, item_end, red);
 }
@@ -1587,27 +1612,47 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
   //    barrier, the rescale pass)
   bool scaled_done = false;
   if (updates && !s_noop && barrier_ok) {
+    // bias corrections that are 1 in every group: the same for every CTA
+    int unit = 0;
+    if constexpr (unit_bc_instances<ST, REM>()) {
+      unit = kUnitBc1 | kUnitBc2;
+      for (int k = 0; k < kp.n_groups; ++k) {
+        if (sgrp[k].bc1 != 1.0f) unit &= ~kUnitBc1;
+        if (sgrp[k].bc2 != 1.0f) unit &= ~kUnitBc2;
+      }
+    }
     bool unused = false;
-    if constexpr (SCALED) {
-      run_pass<ST, GT, OT, REM, Pass::kScaledA, NS>(kp, sgrp, item_begin, item_end,
-                                                &kp.scratch->next_update,
-                                                &kp.scratch->next_tail_update, n_items, s_tiles,
-                                                s_full, s_tags, s_prod, s_red, stage, unused,
-                                                timed_out);
-      barrier_ok = grid_barrier(kp.scratch, 0u);
-      if (barrier_ok)
-        run_pass<ST, GT, OT, REM, Pass::kScaledB, NS>(kp, sgrp, item_begin, item_end,
-                                                  &kp.scratch->next_rescale,
-                                                  &kp.scratch->next_tail_rescale, n_items, s_tiles,
-                                                  s_full, s_tags, s_prod, s_red, stage, unused,
-                                                  timed_out);
-      scaled_done = barrier_ok;
+    // the update passes for a compile-time unit mask U
+    auto passes = [&](auto unit_c) {
+      constexpr int U = decltype(unit_c)::value;
+      if constexpr (SCALED) {
+        run_pass<ST, GT, OT, REM, Pass::kScaledA, NS, U>(kp, sgrp, item_begin, item_end,
+                                                         &kp.scratch->next_update,
+                                                         &kp.scratch->next_tail_update, n_items,
+                                                         s_tiles, s_full, s_tags, s_prod, s_red,
+                                                         stage, unused, timed_out);
+        barrier_ok = grid_barrier(kp.scratch, 0u);
+        if (barrier_ok)
+          run_pass<ST, GT, OT, REM, Pass::kScaledB, NS, U>(kp, sgrp, item_begin, item_end,
+                                                           &kp.scratch->next_rescale,
+                                                           &kp.scratch->next_tail_rescale, n_items,
+                                                           s_tiles, s_full, s_tags, s_prod, s_red,
+                                                           stage, unused, timed_out);
+        scaled_done = barrier_ok;
+      } else {
+        run_pass<ST, GT, OT, REM, Pass::kUpdate, NS, U>(kp, sgrp, item_begin, item_end,
+                                                        &kp.scratch->next_update,
+                                                        &kp.scratch->next_tail_update, n_items,
+                                                        s_tiles, s_full, s_tags, s_prod, s_red,
+                                                        stage, unused, timed_out);
+      }
+    };
+    if constexpr (unit_bc_instances<ST, REM>()) {
+      if (unit == (kUnitBc1 | kUnitBc2)) passes(std::integral_constant<int, kUnitBc1 | kUnitBc2>{});
+      else if (unit == kUnitBc1) passes(std::integral_constant<int, kUnitBc1>{});
+      else passes(std::integral_constant<int, 0>{});
     } else {
-      run_pass<ST, GT, OT, REM, Pass::kUpdate, NS>(kp, sgrp, item_begin, item_end,
-                                               &kp.scratch->next_update,
-                                               &kp.scratch->next_tail_update, n_items, s_tiles,
-                                               s_full, s_tags, s_prod, s_red, stage, unused,
-                                               timed_out);
+      passes(std::integral_constant<int, 0>{});
     }
   }
   if (__syncthreads_or(timed_out) && tid == 0) atomicExch(&kp.scratch->status, FADAM_ETIMEOUT);

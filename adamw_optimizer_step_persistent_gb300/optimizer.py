@@ -335,6 +335,26 @@ class FusedAdamShard:
 
     # ---- state -------------------------------------------------------------------
 
+    def set_group_steps(self, steps: Sequence[int]) -> None:
+        """Set each group's counter to the steps already taken, as when a
+        shard resumes from a checkpoint: the next step of group i is
+        ``steps[i] + 1`` (with ``step_preadvanced`` the counter is what the
+        next launch uses, as always).  Capturable shards get a device write
+        on the current stream; a shared counter takes one value for all
+        groups."""
+        steps = [int(s) for s in steps]
+        if len(steps) != len(self.groups) or any(s < 0 or s >= 2**31 - 1 for s in steps):
+            raise ValueError("one step count in [0, 2^31 - 1) per group")
+        if self.capturable:
+            if len({t.data_ptr() for t in self.step_dev}) == 1 and len(set(steps)) > 1:
+                raise ValueError("the groups share one step counter")
+            for t, s in zip(self.step_dev, steps):
+                t.fill_(s)
+        self.host_steps = steps
+        self._fill_groups()
+        _abi.check(_abi.lib().fadam_plan_set_groups(self._plan, self._groups_c, len(self.groups)),
+                   "fadam_plan_set_groups")
+
     def group_steps(self) -> List[int]:
         """Each group's step counter (reads the device when capturable)."""
         if self.capturable:

@@ -22,14 +22,19 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _run(spec, steps, *, capturable=None, check_finite=False, fresh=True, shared_step=False):
-    """Run `steps` steps on the GPU and on the oracle from the same inputs."""
+def _run(spec, steps, *, capturable=None, check_finite=False, fresh=True, shared_step=False,
+         start_step=0):
+    """Run `steps` steps on the GPU and on the oracle from the same inputs
+    (every group's counter starting at `start_step` steps taken)."""
     capturable = spec.capturable if capturable is None else capturable
     shard = workloads.materialize(spec, DEV)
     opt = FusedAdamShard(shard.param_groups(), capturable=capturable, check_finite=check_finite,
                          remainders=spec.remainders, grad_scale=spec.grad_scale,
                          shared_step=shared_step)
     osh = helpers.oracle_shard(shard, step_slot=[0] * len(spec.groups) if shared_step else None)
+    if start_step:
+        opt.set_group_steps([start_step] * len(spec.groups))
+        osh.steps = [start_step] * len(osh.steps)
     for k in range(1, steps + 1):
         if fresh and k > 1:
             workloads.fresh_grads(shard, k)
@@ -408,6 +413,55 @@ def test_16bit_moments_match_oracle(moment_dtype, g_dtype, out_dtype):
         rep = helpers.compare(shard, osh)
         assert opt.group_steps() == [4, 4]
         assert rep.exact_fraction == 1.0, rep.exact_fraction
+
+
+@pytest.mark.parametrize("state_dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("start", [162, 336, 20000])
+def test_16bit_state_late_steps_match_oracle(state_dtype, start):
+    """Late steps, where a bias correction rounds to 1 in float (bc1 from
+    step 165 with beta1 0.9, bc2 from 338 with beta2 0.95 and 17,321 with
+    0.999): the 16-bit state takes tile instances without those divisions,
+    and every step across each switch point equals the oracle bit for
+    bit."""
+    spec = workloads.large_uniform(n_tensors=3, numel=40_003, state_dtype=state_dtype,
+                                   g_dtype=torch.bfloat16)
+    spec.sizes = [40_003, 7, 131_072 + 5]
+    spec.group_of = [0, 1, 1]
+    spec.groups = [spec.groups[0], workloads.GroupSpec(adam_w_mode=False, weight_decay=0.05,
+                                                       betas=(0.9, 0.999))]
+    spec.out_dtype = torch.bfloat16
+    # the steps run are start + 1 .. start + 5: 163-167 cross bc1's switch,
+    # 337-341 bc2's (beta2 0.95), 20001-20005 have both at 1 in both groups
+    bc = {(b, k): float(oracle.bias_correction(b, k)) for b in (0.9, 0.95, 0.999)
+          for k in (start + 1, start + 5)}
+    if start == 162:
+        assert bc[0.9, 163] < 1.0 and bc[0.9, 167] == 1.0
+    if start == 336:
+        assert bc[0.95, 337] < 1.0 and bc[0.95, 341] == 1.0
+    if start == 20000:
+        assert all(v == 1.0 for v in bc.values())
+    for capturable in (False, True):
+        shard, opt, osh = _run(spec, 5, capturable=capturable, start_step=start)
+        rep = helpers.compare(shard, osh)
+        assert opt.group_steps() == [start + 5, start + 5]
+        assert rep.exact_fraction == 1.0, rep.exact_fraction
+        opt.close()
+
+
+def test_set_group_steps_checks_and_shared_counter():
+    spec = workloads.small_versions()["many_small"]
+    shard = workloads.materialize(spec, DEV)
+    opt = FusedAdamShard(shard.param_groups(), capturable=True, shared_step=True)
+    with pytest.raises(ValueError):
+        opt.set_group_steps([1, 2, 3])
+    with pytest.raises(ValueError):
+        opt.set_group_steps([1, 1])
+    with pytest.raises(ValueError):
+        opt.set_group_steps([-1, -1, -1])
+    opt.set_group_steps([7, 7, 7])
+    opt.step()
+    assert opt.group_steps() == [8, 8, 8]
+    opt.close()
 
 
 def test_16bit_moments_regular_capturable_and_graph_are_bit_identical():

@@ -63,6 +63,29 @@ def test_scaled_steps_match_oracle(name, capturable):
     opt.close()
 
 
+@pytest.mark.parametrize("start", [163, 20000])
+def test_scaled_late_steps_match_oracle(start):
+    """The scaled passes at steps where the bias corrections round to 1
+    (their tile instances leave those divisions out): bits and scales equal
+    the oracle's across the switch at step 165 and far beyond it."""
+    spec, shard, opt, osh, _ = _make("scaled_state_shard", capturable=True)
+    opt.set_group_steps([start])
+    osh.steps = [start] * len(osh.steps)
+    rep = helpers.Report()
+    for k in range(1, 4):
+        if k > 1:
+            workloads.fresh_grads(shard, k)
+            helpers.refresh_grads(osh, shard)
+        opt.step()
+        oracle.shard_step(osh, capturable=True)
+        torch.cuda.synchronize()
+        helpers.compare(shard, osh, report=rep)
+        _check_scales(opt, osh)
+    assert rep.exact_fraction == 1.0, rep.exact_fraction
+    assert opt.group_steps() == [start + 3]
+    opt.close()
+
+
 def test_bf16_overflowing_reciprocals_as_the_oracle():
     spec, shard, opt, osh, _ = _make("scaled_bf16_small_moments")
     opt.step()
