@@ -52,10 +52,10 @@ class FusedAdamShard:
     ``params`` are the masters and set the state dtype: fp32, bf16 or fp16,
     with ``exp_avgs`` and ``exp_avg_sqs`` of the same dtype (updated in
     float, rounded back on store), or, under an fp32 master, both bf16 or
-    both fp16 (TransformerEngine's exp_avg_dtype and exp_avg_sq_dtype); in remainder mode they are the bf16 high
-    halves (``remainders`` then holds the int16 low halves, the moments are
-    fp32, and ``params_out`` the bf16 tensors that receive the new high
-    halves; they may be ``params``).
+    both fp16 (TransformerEngine's exp_avg_dtype and exp_avg_sq_dtype).  In
+    remainder mode ``params`` are the bf16 high halves (``remainders`` then
+    holds the int16 low halves, the moments are fp32, and ``params_out`` the
+    bf16 tensors that receive the new high halves; they may be ``params``).
     """
 
     def __init__(self, param_groups: Sequence[Dict], *, capturable: bool = False,
@@ -354,6 +354,37 @@ class FusedAdamShard:
         self._fill_groups()
         _abi.check(_abi.lib().fadam_plan_set_groups(self._plan, self._groups_c, len(self.groups)),
                    "fadam_plan_set_groups")
+
+    def state_dict(self) -> Dict:
+        """The shard's scalar state for a checkpoint: an int step counter for
+        every group, empty groups included ("[PyTorch] Advance FusedAdam step
+        counter for empty param groups": a checkpoint whose empty group holds
+        no step resumes wrongly), each group's learning rate and the grad
+        scale.  Reads the device when capturable.  The tensors (p, m, v,
+        remainders, state scales) belong to the caller, who saves them."""
+        if self.capturable:
+            lr = [float(t.item()) for t in self.lr_dev]
+            grad_scale = float(self.grad_scale_dev.item())
+        else:
+            lr, grad_scale = list(self.host_lr), self.host_grad_scale
+        return {"step": self.group_steps(), "lr": lr, "grad_scale": grad_scale}
+
+    def load_state_dict(self, state: Dict) -> None:
+        """Restore what ``state_dict`` returned (the same number of groups)."""
+        steps, lr = list(state["step"]), list(state["lr"])
+        if len(steps) != len(self.groups) or len(lr) != len(self.groups):
+            raise ValueError("the checkpoint has a different number of param groups")
+        if any(s is None for s in steps):
+            raise ValueError("the checkpoint lacks the step counter of a group")
+        self.set_group_steps(steps)
+        for i, x in enumerate(lr):
+            self.set_lr(i, x)
+        self.set_grad_scale(state["grad_scale"])
+        if not self.capturable:
+            self._fill_groups()
+            _abi.check(_abi.lib().fadam_plan_set_groups(self._plan, self._groups_c,
+                                                        len(self.groups)),
+                       "fadam_plan_set_groups")
 
     def group_steps(self) -> List[int]:
         """Each group's step counter (reads the device when capturable)."""
