@@ -298,6 +298,31 @@ def test_host_gradients_entry_point_matches_device_gradients(name):
         assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("form", ["bf16_state", "f16_state", "bf16_moments", "f16_moments"])
+def test_host_gradients_in_the_16bit_forms(form):
+    """The in-place host-gradient path with a 16-bit state or 16-bit
+    moments, over the many-small shard's ragged and unaligned tensors:
+    the same bits as two steps with the gradients on the device."""
+    spec = workloads.small_versions()["many_small"]
+    dt = torch.bfloat16 if form.startswith("bf16") else torch.float16
+    if form.endswith("state"):
+        spec.state_dtype = dt
+    else:
+        spec.moment_dtype = dt
+    a, _, _ = _run(spec, 2, capturable=True, fresh=False)
+    b = workloads.materialize(spec, DEV)
+    ob = FusedAdamShard(b.param_groups(), capturable=True, grad_scale=spec.grad_scale)
+    host = [g.cpu().pin_memory() for g in (b.grads[i] for i in b.plan_order())]
+    for gr in b.grads:
+        gr.zero_()
+    steps = [ob.step_from_host(host) for _ in range(2)]
+    assert steps == [[1] * len(spec.groups), [2] * len(spec.groups)]
+    for x, y in zip(helpers.snapshot(a), helpers.snapshot(b)):
+        assert torch.equal(x.view(torch.int16) if x.element_size() == 2 else x.view(torch.int32),
+                           y.view(torch.int16) if y.element_size() == 2 else y.view(torch.int32))
+    ob.close()
+
+
 @pytest.mark.parametrize("memory", ["pageable", "misaligned_pinned"])
 def test_host_gradients_copy_path(memory):
     """Host gradients that cannot be read in place (pageable, or pinned at
