@@ -298,6 +298,48 @@ def test_host_gradients_entry_point_matches_device_gradients(name):
         assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("state_dtype,start", [(torch.float32, 0), (torch.bfloat16, 0),
+                                               (torch.bfloat16, 20000)])
+def test_largest_group_table_each_group_its_own_hyperparameters(state_dtype, start):
+    """32 groups (the most a plan takes), each with its own mode, betas,
+    eps, weight decay, lr and bias correction, two of them empty, ragged
+    tensors of 1 to 70,000 elements: every value equals the oracle bit for
+    bit and every counter advances, regular and capturable.  20,000 steps
+    in, some groups' bias corrections are 1 and others' not (beta2 up to
+    0.9999), so the 16-bit state's launch-wide choice of update loop must
+    keep the divisions that any group needs."""
+    rng = np.random.default_rng(5)
+    groups = [workloads.GroupSpec(adam_w_mode=bool(k % 2), lr=float(10 ** rng.uniform(-4, -2)),
+                                  betas=(float(rng.uniform(0.8, 0.95)),
+                                         float(rng.uniform(0.95, 0.9999))),
+                                  eps=float(10 ** rng.uniform(-10, -6)),
+                                  weight_decay=float(rng.uniform(0.0, 0.2)),
+                                  bias_correction=k % 5 != 0)
+              for k in range(_abi.MAX_GROUPS)]
+    for k in (3, 11):  # beta2 near 1: bias correction 2 stays below 1 long after step 20,000
+        groups[k].betas = (groups[k].betas[0], 0.9999)
+    sizes, group_of = [], []
+    for k in range(_abi.MAX_GROUPS):
+        if k in (7, 19):
+            continue  # empty groups
+        for _ in range(1 + k % 3):
+            sizes.append(int(rng.integers(1, 70_000)))
+            group_of.append(k)
+    spec = workloads.ShardSpec("groups32", groups, sizes, group_of, g_dtype=torch.bfloat16,
+                               out_dtype=torch.bfloat16, grad_std=1e-2, seed=1300,
+                               state_dtype=state_dtype)
+    if start:
+        unit2 = [not g.bias_correction or oracle.bias_correction(g.betas[1], start + 1) == 1.0
+                 for g in groups]
+        assert any(unit2) and not all(unit2)
+    for capturable in (False, True):
+        shard, opt, osh = _run(spec, 3, capturable=capturable, start_step=start)
+        rep = helpers.compare(shard, osh)
+        assert rep.exact_fraction == 1.0, rep.exact_fraction
+        assert opt.group_steps() == oracle.group_steps(osh) == [start + 3] * _abi.MAX_GROUPS
+        opt.close()
+
+
 @pytest.mark.parametrize("form", ["bf16_state", "f16_state", "bf16_moments", "f16_moments"])
 def test_host_gradients_in_the_16bit_forms(form):
     """The in-place host-gradient path with a 16-bit state or 16-bit
