@@ -404,6 +404,34 @@ def run_gpu(args):
         r = summarise(per, reduce_bytes, elems, world, device)
         r["bytes_per_step"] = reduce_bytes
         res["reduce"] = r
+    if spec.exchange_ranks and "clip_pipeline" in variants:
+        # the data-parallel step with gradient clipping, captured as one
+        # graph: the grad scale reset (the loss scaler's value), the
+        # reduce-scatter stand-in, the shard's squared norm, the clip folded
+        # into the grad scale, the step writing every destination
+        gs0 = float(spec.grad_scale)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+
+        def pipeline():
+            cap.set_grad_scale(gs0)
+            cap.grad_reduce()
+            cap.clip_apply(cap.grad_norm_sq(), 1.0)
+            cap.step()
+
+        with torch.cuda.stream(s):
+            pipeline()
+        torch.cuda.current_stream().wait_stream(s)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            pipeline()
+        per, _ = time_launches(graph.replay, args.steps, args.warmup, world)
+        pipe_bytes = reduce_bytes + elems * gsz + bytes_step
+        r = summarise(per, pipe_bytes, elems, world, device)
+        r["bytes_per_step"] = pipe_bytes
+        r["launches"] = "grad scale fill, fadam_grad_reduce, fadam_grad_sumsq, fadam_clip_apply, fadam_step"
+        res["clip_pipeline"] = r
+        del graph
     if "capturable" in variants:
         per, _ = time_launches(cap.step, args.steps, args.warmup, world)
         res["capturable"] = summarise(per, bytes_step, elems, world, device)
@@ -538,7 +566,7 @@ def main(argv=None):
                     help="layers of the capturable_l2 / exchange_shard / scaled_state_shard "
                          "layer list (8)")
     ap.add_argument("--variants", default="capturable,regular,graph,check_finite,norm,e2e",
-                    help="also exchange,reduce on the exchange_shard workload")
+                    help="also exchange,reduce,clip_pipeline on the exchange_shard workload")
     ap.add_argument("--start-step", type=int, default=0,
                     help="steps already taken by every group when timing starts (0: a fresh "
                          "shard; from 165 / 338 / 17,321 the bias corrections of beta 0.9 / "
