@@ -77,6 +77,25 @@ struct alignas(16) KGroup {
 };
 static_assert(sizeof(KGroup) == 64, "KGroup is one 64-byte record");
 
+// Bias corrections of one group for one step, kept between launches.  The
+// double-precision pow behind them takes microseconds on this GPU's narrow
+// FP64 pipe, on the path of every CTA; instead one CTA of each launch
+// computes the next step's corrections and the next launch reads them.  It
+// is a memo of a pure function of (beta1, beta2, step): an entry serves only
+// when all three match and its tag is set, else the launch computes the
+// corrections itself.  Two entries per group, chosen by the step's parity,
+// so that a launch never writes an entry its own CTAs read.
+struct alignas(16) BcMemo {
+  uint32_t beta1_bits, beta2_bits;
+  int32_t step;
+  uint32_t tag;  // kMemoTag once written
+  float bc1, bc2;
+  int32_t reserved[2];
+};
+static_assert(sizeof(BcMemo) == 32, "BcMemo is two 16-byte words");
+constexpr uint32_t kMemoTag = 0x62634d4du;
+constexpr int kMemoEntries = 2 * FADAM_MAX_GROUPS;
+
 // Per-plan device status block.
 // One chunk of bulk tiles: tiles [tile0, tile0 + ntiles) of item `item`.
 struct alignas(16) Chunk {
@@ -125,6 +144,7 @@ struct alignas(16) KParams {
   const Chunk* chunks;       // bulk tiles, pulled dynamically by the CTAs
   double* partials;          // norm launches: weighted sums of squares, one per chunk then one per item
   double* sumsq_out;         // norm launches: sum_g grad_scale_g^2 * sum g^2
+  BcMemo* memo;              // kMemoEntries bias-correction entries, or null
   int32_t n_chunks;
   int32_t n_groups;
   uint32_t flags;

@@ -76,8 +76,42 @@ struct SGroup {
   float beta1, omb1, beta2, omb2;  // omb = 1 - beta, rounded once
   float bc1, bc2, eps, wd, lr, gs;
   int32_t step_old;                // counter as read (capturable) or the host step
+  int32_t step;                    // the step this launch applies
   uint32_t bits;
 };
+
+// 1 - beta^step in double, rounded once to float.
+__device__ __forceinline__ float bias_correction(float beta, int32_t step) {
+  return static_cast<float>(1.0 - pow(static_cast<double>(beta), static_cast<double>(step)));
+}
+
+// The memo entry of group g for `step`, if it holds that step's corrections
+// for these betas.
+__device__ __forceinline__ bool memo_lookup(const BcMemo* memo, int g, float beta1, float beta2,
+                                            int32_t step, float& bc1, float& bc2) {
+  const BcMemo* e = memo + 2 * g + (step & 1);
+  const uint4 a = __ldcg(reinterpret_cast<const uint4*>(e));
+  const uint4 b = __ldcg(reinterpret_cast<const uint4*>(e) + 1);
+  if (a.w != kMemoTag || a.x != __float_as_uint(beta1) || a.y != __float_as_uint(beta2) ||
+      static_cast<int32_t>(a.z) != step)
+    return false;
+  bc1 = __uint_as_float(b.x);
+  bc2 = __uint_as_float(b.y);
+  return true;
+}
+
+// Group g's corrections for `step` into its memo entry (the other parity's
+// entry than the one this launch reads).
+__device__ __forceinline__ void memo_store(BcMemo* memo, int g, float beta1, float beta2,
+                                           int32_t step) {
+  BcMemo* e = memo + 2 * g + (step & 1);
+  const uint4 b = make_uint4(__float_as_uint(bias_correction(beta1, step)),
+                             __float_as_uint(bias_correction(beta2, step)), 0u, 0u);
+  const uint4 a = make_uint4(__float_as_uint(beta1), __float_as_uint(beta2),
+                             static_cast<unsigned>(step), kMemoTag);
+  __stcg(reinterpret_cast<uint4*>(e) + 1, b);
+  __stcg(reinterpret_cast<uint4*>(e), a);
+}
 
 struct Scal {
   float beta1, omb1, beta2, omb2, bc1, bc2, eps, wd, lr, gs;
@@ -1540,18 +1574,27 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
       s.step_old = G.step;
       step = G.step;
     }
-    // launches that only read g (norm, reduction) skip the double pow:
-    // this GPU's FP64 rate makes it a few microseconds per CTA
-    if ((G.bits & kGroupBiasCorr) && !(kp.flags & (kNormOnly | kReduceOnly))) {
-      s.bc1 = static_cast<float>(1.0 - pow(static_cast<double>(G.beta1), static_cast<double>(step)));
-      s.bc2 = static_cast<float>(1.0 - pow(static_cast<double>(G.beta2), static_cast<double>(step)));
-    } else {
-      s.bc1 = 1.0f;
-      s.bc2 = 1.0f;
+    s.step = step;
+    // launches that only read g (norm, reduction) skip the corrections; the
+    // others take them from the memo the previous launch left, or compute
+    // the double pow (a few microseconds on this GPU's FP64 pipe)
+    s.bc1 = 1.0f;
+    s.bc2 = 1.0f;
+    if ((G.bits & kGroupBiasCorr) && !(kp.flags & (kNormOnly | kReduceOnly)) &&
+        !(kp.memo && memo_lookup(kp.memo, tid, G.beta1, G.beta2, step, s.bc1, s.bc2))) {
+      s.bc1 = bias_correction(G.beta1, step);
+      s.bc2 = bias_correction(G.beta2, step);
     }
     sgrp[tid] = s;
   }
   __syncthreads();
+  // the next step's corrections, for the next launch: one warp of the last
+  // CTA pays the pow while the other CTAs start on the shard's tiles
+  if (kp.memo && blockIdx.x == gridDim.x - 1 && !(kp.flags & (kNormOnly | kReduceOnly)) &&
+      tid >= 32 && tid < 32 + kp.n_groups) {
+    const SGroup& g = sgrp[tid - 32];
+    if (g.bits & kGroupBiasCorr) memo_store(kp.memo, tid - 32, g.beta1, g.beta2, g.step + 1);
+  }
 
   const int item_begin = __ldg(kp.cta_begin + blockIdx.x);
   const int item_end = __ldg(kp.cta_begin + blockIdx.x + 1);

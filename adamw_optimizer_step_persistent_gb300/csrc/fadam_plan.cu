@@ -560,6 +560,7 @@ struct fadam_plan {
   Chunk* d_chunks = nullptr;
   int32_t* d_cta = nullptr;
   KScratch* d_scratch = nullptr;
+  BcMemo* d_memo = nullptr;      // bias corrections carried from one launch to the next
   double* d_partials = nullptr;  // gradient-norm launches: per-chunk and per-item partials
   // the data-parallel exchange (fadam_plan_set_exchange): byte offsets
   int32_t n_sources = 0, average = 0, n_dests = 0;
@@ -587,6 +588,7 @@ void free_plan_memory(fadam_plan* p) {
   if (p->d_chunks) cudaFree(p->d_chunks);
   if (p->d_cta) cudaFree(p->d_cta);
   if (p->d_scratch) cudaFree(p->d_scratch);
+  if (p->d_memo) cudaFree(p->d_memo);
   if (p->d_partials) cudaFree(p->d_partials);
   p->d_items = nullptr;
   p->d_chunks = nullptr;
@@ -679,6 +681,9 @@ fadam_status fadam_plan_create(const fadam_tensor* tensors, int64_t n_tensors,
                    cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMalloc(&plan->d_scratch, sizeof(KScratch));
   if (e == cudaSuccess) e = cudaMemset(plan->d_scratch, 0, sizeof(KScratch));
+  // no memo entry is valid until a launch writes it (tag 0)
+  if (e == cudaSuccess) e = cudaMalloc(&plan->d_memo, kMemoEntries * sizeof(BcMemo));
+  if (e == cudaSuccess) e = cudaMemset(plan->d_memo, 0, kMemoEntries * sizeof(BcMemo));
   // gradient-norm launches: one partial per tile chunk and per item
   if (e == cudaSuccess)
     e = cudaMalloc(&plan->d_partials, (hp.chunks.size() + hp.items.size() + 1) * sizeof(double));
@@ -758,6 +763,7 @@ fadam_status step_launch(fadam_plan* plan, int32_t* noop_dev, fadam_stream strea
               hp.flags | extra_flags);
   fill_exchange(kp, plan);
   fill_scaled(kp, plan);
+  kp.memo = plan->d_memo;
   kp.n_sources = 0;  // the plain step reads g as it stands
   kp.host_g = plan->d_host_g;
   kp.dev_g = plan->d_dev_g;
@@ -859,6 +865,7 @@ fadam_status fadam_step_reduce(fadam_plan* plan, int32_t* noop_dev, fadam_stream
               hp.flags | kReduceFirst);
   fill_exchange(kp, plan);
   fill_scaled(kp, plan);
+  kp.memo = plan->d_memo;
   return launch(hp.kernel, hp.smem, kp, hp.grid, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -1256,7 +1263,8 @@ constexpr size_t kArenaCtaOff = 256;
 constexpr size_t kArenaItemsOff =
     kArenaCtaOff + ((size_t(kNoAllocMaxCtas) + 1) * sizeof(int32_t) + 255) / 256 * 256;
 constexpr size_t kArenaChunksOff = kArenaItemsOff + size_t(kNoAllocMaxItems) * sizeof(Item);
-constexpr size_t kArenaBytes = kArenaChunksOff + size_t(kNoAllocMaxChunks) * sizeof(Chunk);
+constexpr size_t kArenaMemoOff = kArenaChunksOff + size_t(kNoAllocMaxChunks) * sizeof(Chunk);
+constexpr size_t kArenaBytes = kArenaMemoOff + size_t(kMemoEntries) * sizeof(BcMemo);
 static_assert(sizeof(KScratch) <= kArenaCtaOff, "status block fits its slot");
 
 constexpr int kMaxDevices = 64;
@@ -1338,5 +1346,8 @@ extern "C" fadam_status fadam_step_noalloc(const fadam_tensor* tensors, int64_t 
   KParams kp;
   fill_params(kp, items, cta, chunks, static_cast<int32_t>(hp.chunks.size()), noop_dev, scratch,
               groups, n_groups, flags);
+  // the memo is shared by every call: its entries are keyed by betas and
+  // step, so any entry that matches holds the corrections this call needs
+  kp.memo = reinterpret_cast<BcMemo*>(arena + kArenaMemoOff);
   return launch(hp.kernel, hp.smem, kp, hp.grid, (flags & FADAM_CHECK_FINITE) != 0, s);
 }

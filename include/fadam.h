@@ -406,7 +406,7 @@ fadam_status fadam_step_once(const fadam_tensor* tensors, int64_t n_tensors, int
  * cudaMalloc/cudaFree could synchronise the device.  This call packs the
  * shard on the host, as fadam_plan_create does, and runs one step as
  * fadam_step does, but keeps the work list and the status block in a
- * static device array instead of allocated memory: about 330 KB that every
+ * static device array instead of allocated memory: about 340 KB that every
  * GPU which loads this library holds until the process exits.  It calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *

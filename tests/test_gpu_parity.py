@@ -515,6 +515,49 @@ def test_16bit_state_late_steps_match_oracle(state_dtype, start):
         opt.close()
 
 
+@pytest.mark.parametrize("capturable", [False, True])
+def test_carried_bias_corrections_follow_betas_and_steps(capturable):
+    """Each launch computes the next step's bias corrections for the next
+    launch to read, keyed by betas and step.  New betas, a counter set back
+    to an earlier step and a counter moved far ahead must each take freshly
+    computed corrections, and the steps after them the carried ones: every
+    value bit-identical to the oracle throughout."""
+    spec = workloads.small_versions()["tiny_adamw"]
+    spec.groups = [workloads.GroupSpec(adam_w_mode=True, lr=1e-3, betas=(0.9, 0.999),
+                                       weight_decay=0.01),
+                   workloads.GroupSpec(adam_w_mode=False, lr=2e-3, betas=(0.85, 0.99),
+                                       weight_decay=0.02)]
+    spec.group_of = [0, 1, 0, 1]
+    shard = workloads.materialize(spec, DEV)
+    opt = FusedAdamShard(shard.param_groups(), capturable=capturable)
+    osh = helpers.oracle_shard(shard)
+    lib = _abi.lib()
+
+    def steps(n):
+        for _ in range(n):
+            opt.step()
+            oracle.shard_step(osh, capturable=capturable)
+        torch.cuda.synchronize()
+        rep = helpers.compare(shard, osh)
+        assert rep.exact_fraction == 1.0, rep.exact_fraction
+
+    steps(3)
+    opt.groups[0]["betas"] = (0.8, 0.99)  # read by the next launch's group table
+    osh.groups[0].beta1, osh.groups[0].beta2 = 0.8, 0.99
+    if capturable:  # a capturable plan's table changes only through set_groups
+        opt._fill_groups()
+        _abi.check(lib.fadam_plan_set_groups(opt._plan, opt._groups_c, len(opt.groups)), "set")
+    steps(2)
+    opt.set_group_steps([1, 1])  # back: the next step is 2 again
+    osh.steps = [1] * len(osh.steps)
+    steps(2)
+    opt.set_group_steps([5000, 77])  # far ahead, one group at a time
+    osh.steps = [5000, 77]
+    steps(2)
+    assert opt.group_steps() == [5002, 79]
+    opt.close()
+
+
 def test_set_group_steps_checks_and_shared_counter():
     spec = workloads.small_versions()["many_small"]
     shard = workloads.materialize(spec, DEV)
