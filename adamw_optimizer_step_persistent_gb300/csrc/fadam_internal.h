@@ -134,6 +134,11 @@ constexpr uint32_t kReduceFirst = 1u << 28;
 // tensor t's g lives at host_g[t] instead of dev_g[t], every item goes the
 // element-wise way (plain loads; no bulk copies from host memory).
 constexpr uint32_t kHostGrads = 1u << 27;
+// Launch-only, from the plan's shape: no bulk item has an element-wise tail
+// (every bulk item's length is a multiple of 8), and no item is off the
+// bulk path.  They let a launch skip the tail and rest passes.
+constexpr uint32_t kNoTails = 1u << 26;
+constexpr uint32_t kAllBulk = 1u << 25;
 
 // Everything one launch needs, passed as a __grid_constant__ parameter.
 struct alignas(16) KParams {

@@ -1488,8 +1488,14 @@ __device__ __forceinline__ void run_pass(const KParams& kp, const SGroup* sgrp, 
   if (bulk && kp.n_chunks > 0 && !timed_out)
     bulk_pass<ST, GT, OT, REM, PASS, NS, UNIT>(kp, sgrp, counter, smem, full, tags, pr, red, stage,
                                                bad, timed_out);
-  if (bulk) bad |= tail_pass<ST, GT, OT, REM, PASS>(kp, sgrp, tail_counter, n_items);
-  bad |= rest_pass<ST, GT, OT, REM, PASS>(kp, sgrp, item_begin, item_end, red);
+  // a shard without element-wise tails skips the tail pass, one whose items
+  // all go through the tiles the rest pass: a global round trip each on
+  // every CTA's path (the norm writes every bulk item's slot in its tail
+  // pass, so it keeps it)
+  if (bulk && (PASS == Pass::kNorm || !(kp.flags & kNoTails)))
+    bad |= tail_pass<ST, GT, OT, REM, PASS>(kp, sgrp, tail_counter, n_items);
+  if (!bulk || !(kp.flags & kAllBulk))
+    bad |= rest_pass<ST, GT, OT, REM, PASS>(kp, sgrp, item_begin, item_end, red);
 }
 
 // Grid-wide barrier for a cooperative launch.  The wait is bounded: after

@@ -472,6 +472,7 @@ struct HostPlan {
   std::vector<Chunk> chunks;
   int64_t n_elements = 0;
   double bytes = 0, check_bytes = 0;
+  uint32_t shape = 0;  // kNoTails, kAllBulk
 };
 
 // Checks, device query and packing shared by fadam_plan_create and
@@ -515,6 +516,13 @@ fadam_status prepare(const fadam_tensor* tensors, int64_t n_tensors, const fadam
   hp.items.reserve(pitems.size());
   for (const PackItem& pi : pitems) hp.items.push_back(to_item(tensors[pi.tensor], pi, d));
   build_chunks(hp.items, max_chunks, hp.grid, hp.chunks);
+  // a bulk item takes a multiple of 8 elements through the tiles and the
+  // rest element-wise in the tail pass
+  hp.shape = kNoTails | kAllBulk;
+  for (const Item& it : hp.items) {
+    if (!(it.flags & kItemBulk)) hp.shape &= ~kAllBulk;
+    else if (it.n % 8 != 0) hp.shape &= ~kNoTails;
+  }
   const double bpe = bytes_per_elem(d);
   for (int64_t i = 0; i < n_tensors; ++i) {
     const int64_t ne = std::max<int64_t>(tensors[i].numel, 0);
@@ -760,7 +768,7 @@ fadam_status step_launch(fadam_plan* plan, int32_t* noop_dev, fadam_stream strea
   KParams kp;
   fill_params(kp, plan->d_items, plan->d_cta, plan->d_chunks, static_cast<int32_t>(hp.chunks.size()),
               noop_dev, plan->d_scratch, plan->groups.data(), plan->n_groups,
-              hp.flags | extra_flags);
+              hp.flags | hp.shape | extra_flags);
   fill_exchange(kp, plan);
   fill_scaled(kp, plan);
   kp.memo = plan->d_memo;
@@ -835,7 +843,7 @@ fadam_status fadam_grad_reduce(fadam_plan* plan, fadam_stream stream) {
   KParams kp;
   fill_params(kp, plan->d_items, plan->d_cta, plan->d_chunks, static_cast<int32_t>(hp.chunks.size()),
               nullptr, plan->d_scratch, plan->groups.data(), plan->n_groups,
-              (hp.flags & FADAM_CAPTURABLE) | kReduceOnly);
+              (hp.flags & FADAM_CAPTURABLE) | hp.shape | kReduceOnly);
   fill_exchange(kp, plan);
   return launch(hp.kernel, hp.smem, kp, hp.grid, false, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -862,7 +870,7 @@ fadam_status fadam_step_reduce(fadam_plan* plan, int32_t* noop_dev, fadam_stream
   KParams kp;
   fill_params(kp, plan->d_items, plan->d_cta, plan->d_chunks, static_cast<int32_t>(hp.chunks.size()),
               noop_dev, plan->d_scratch, plan->groups.data(), plan->n_groups,
-              hp.flags | kReduceFirst);
+              hp.flags | hp.shape | kReduceFirst);
   fill_exchange(kp, plan);
   fill_scaled(kp, plan);
   kp.memo = plan->d_memo;
@@ -1041,7 +1049,7 @@ fadam_status fadam_step_once(const fadam_tensor* tensors, int64_t n_tensors, int
   if (e == cudaSuccess) {
     KParams kp;
     fill_params(kp, d_items, d_cta, d_chunks, static_cast<int32_t>(hp.chunks.size()), noop_dev,
-                d_scratch, &grp, 1, flags);
+                d_scratch, &grp, 1, flags | hp.shape);
     st = launch(hp.kernel, hp.smem, kp, hp.grid, false, s);
   } else {
     st = cuda_fail(e, "one-shot upload");
@@ -1103,7 +1111,7 @@ fadam_status fadam_grad_sumsq(fadam_plan* plan, double* sumsq_dev, fadam_stream 
   KParams kp;
   fill_params(kp, plan->d_items, plan->d_cta, plan->d_chunks, static_cast<int32_t>(hp.chunks.size()),
               nullptr, plan->d_scratch, plan->groups.data(), plan->n_groups,
-              (hp.flags & FADAM_CAPTURABLE) | kNormOnly);
+              (hp.flags & FADAM_CAPTURABLE) | hp.shape | kNormOnly);
   kp.partials = plan->d_partials;
   kp.sumsq_out = sumsq_dev;
   return launch(hp.kernel, hp.smem, kp, hp.grid, false, reinterpret_cast<cudaStream_t>(stream));
@@ -1345,7 +1353,7 @@ extern "C" fadam_status fadam_step_noalloc(const fadam_tensor* tensors, int64_t 
   if (e != cudaSuccess) return cuda_fail(e, "fadam_step_noalloc upload");
   KParams kp;
   fill_params(kp, items, cta, chunks, static_cast<int32_t>(hp.chunks.size()), noop_dev, scratch,
-              groups, n_groups, flags);
+              groups, n_groups, flags | hp.shape);
   // the memo is shared by every call: its entries are keyed by betas and
   // step, so any entry that matches holds the corrections this call needs
   kp.memo = reinterpret_cast<BcMemo*>(arena + kArenaMemoOff);
