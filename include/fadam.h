@@ -190,7 +190,10 @@ typedef struct {
 /* Build a plan for a shard: validates every descriptor, packs the ragged
  * tensor list into a balanced work list for a persistent grid sized to the
  * current device, uploads it (synchronously) and allocates the plan's
- * device status block.  Call it before any stream capture.
+ * device status block and a 2 KB memo through which each launch hands the
+ * next step's bias corrections to the next launch (keyed by betas and
+ * step; a launch that finds no matching entry computes them, so results do
+ * not depend on it).  Call it before any stream capture.
  *   tensors[n_tensors]  descriptors (host array, copied; n_tensors >= 0)
  *   groups[n_groups]    1 <= n_groups <= FADAM_MAX_GROUPS (host array, copied)
  *   p_dtype             state dtype of p, m and v: FADAM_DT_F32, _BF16 or
