@@ -80,6 +80,12 @@ struct SGroup {
   uint32_t bits;
 };
 
+// Step counters advance modulo 2^32, as an int32 tensor's += does (no
+// signed overflow in the kernel's own arithmetic).
+__device__ __forceinline__ int32_t step_add(int32_t a, int32_t b) {
+  return static_cast<int32_t>(static_cast<uint32_t>(a) + static_cast<uint32_t>(b));
+}
+
 // 1 - beta^step in double, rounded once to float.
 __device__ __forceinline__ float bias_correction(float beta, int32_t step) {
   return static_cast<float>(1.0 - pow(static_cast<double>(beta), static_cast<double>(step)));
@@ -1573,7 +1579,7 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
       s.lr = G.lr_dev ? __ldcg(G.lr_dev) : 0.0f;
       s.gs = G.gs_dev ? __ldcg(G.gs_dev) : 0.0f;
       s.step_old = __ldcg(G.step_dev);
-      step = (kp.flags & kPreadvanced) ? s.step_old : s.step_old + 1;
+      step = (kp.flags & kPreadvanced) ? s.step_old : step_add(s.step_old, 1);
     } else {
       s.lr = G.lr;
       s.gs = G.grad_scale;
@@ -1599,7 +1605,8 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
   if (kp.memo && blockIdx.x == gridDim.x - 1 && !(kp.flags & (kNormOnly | kReduceOnly)) &&
       tid >= 32 && tid < 32 + kp.n_groups) {
     const SGroup& g = sgrp[tid - 32];
-    if (g.bits & kGroupBiasCorr) memo_store(kp.memo, tid - 32, g.beta1, g.beta2, g.step + 1);
+    if (g.bits & kGroupBiasCorr)
+      memo_store(kp.memo, tid - 32, g.beta1, g.beta2, step_add(g.step, 1));
   }
 
   const int item_begin = __ldg(kp.cta_begin + blockIdx.x);
@@ -1745,7 +1752,8 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
       if (updates && capturable && !(kp.flags & kPreadvanced)) {
         const int adv = (s_noop || !barrier_ok) ? 0 : 1;
         for (int g = 0; g < kp.n_groups; ++g)
-          if (sgrp[g].bits & kGroupOwnsStep) *kp.groups[g].step_dev = sgrp[g].step_old + adv;
+          if (sgrp[g].bits & kGroupOwnsStep)
+            *kp.groups[g].step_dev = step_add(sgrp[g].step_old, adv);
       }
       atomicExch(&kp.scratch->next_update, 0u);
       atomicExch(&kp.scratch->next_scan, 0u);

@@ -70,6 +70,25 @@ def test_resume_from_state_dict_is_bit_identical(capturable):
     fresh.close()
 
 
+@pytest.mark.parametrize("capturable", [False, True])
+def test_empty_group_step_in_state_dict_after_three_steps(capturable):
+    """The check the TransformerEngine fix describes: one populated group
+    and one empty group, three steps, both groups at step 3 in the state
+    dict (before the fix the empty group had no step)."""
+    p = torch.randn(1000, device=DEV)
+    groups = [{"params": [p], "exp_avgs": [torch.zeros_like(p)],
+               "exp_avg_sqs": [torch.zeros_like(p)], "grads": [torch.randn_like(p) * 1e-3],
+               "lr": 1e-3},
+              {"params": [], "exp_avgs": [], "exp_avg_sqs": [], "grads": [], "lr": 1e-3}]
+    opt = FusedAdamShard(groups, capturable=capturable)
+    for _ in range(3):
+        opt.step()
+    sd = opt.state_dict()
+    assert sd["step"] == [3, 3]
+    assert opt.group_steps() == [3, 3]
+    opt.close()
+
+
 def test_load_state_dict_refuses_a_missing_step():
     spec = workloads.small_versions()["tiny_adamw"]
     shard = workloads.materialize(spec, DEV)
