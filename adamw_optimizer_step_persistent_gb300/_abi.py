@@ -24,6 +24,7 @@ DT_NONE, DT_F32, DT_BF16, DT_F16 = 0, 1, 2, 3
 CAPTURABLE, REMAINDERS, CHECK_FINITE, STEP_PREADVANCED = 1, 2, 4, 8
 SCALED_STATES = 16
 MOMENTS_BF16, MOMENTS_F16 = 32, 64
+RECIP_BC = 128  # 16-bit state forms: multiply by 1/bc1, 1/bc2 instead of dividing
 TEST_BARRIER_TIMEOUT = 0x80000000  # diagnostic: the screen's grid barrier runs out
 MAX_GROUPS = 32
 MAX_SOURCES = 16

@@ -116,6 +116,9 @@ struct KScratch {
   unsigned int next_tail_scan;    // next item whose tail the screen takes
   unsigned int next_rescale;      // scaled state: next chunk of the rescale pass
   unsigned int next_tail_rescale; // ... and next item whose tail it takes
+  unsigned int launch_timeout;    // 1 once a wait of the current launch gave up
+                                  // (status keeps it until read; this one is
+                                  // cleared by the launch's last CTA)
 };
 
 // Kernel flags.
@@ -124,6 +127,7 @@ constexpr uint32_t kCheckFinite = FADAM_CHECK_FINITE;
 constexpr uint32_t kPreadvanced = FADAM_STEP_PREADVANCED;
 constexpr uint32_t kTestBarrierTimeout = FADAM_TEST_BARRIER_TIMEOUT;
 constexpr uint32_t kScaledStates = FADAM_SCALED_STATES;
+constexpr uint32_t kRecipBcFlag = FADAM_RECIP_BC;
 // Launch-only flags (never plan flags): compute the squared gradient norm
 // instead of the update; write the gradient shard from the exchange sources
 // (alone, or before the update with a grid barrier between).

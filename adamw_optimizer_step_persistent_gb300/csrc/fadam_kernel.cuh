@@ -75,6 +75,7 @@ __device__ __forceinline__ unsigned long long global_ns() {
 struct SGroup {
   float beta1, omb1, beta2, omb2;  // omb = 1 - beta, rounded once
   float bc1, bc2, eps, wd, lr, gs;
+  float rbc1, rbc2;                // 1/bc1, 1/bc2 (IEEE reciprocals), for FADAM_RECIP_BC
   int32_t step_old;                // counter as read (capturable) or the host step
   int32_t step;                    // the step this launch applies
   uint32_t bits;
@@ -285,8 +286,11 @@ __device__ __forceinline__ unsigned abs_bits(float x) { return __float_as_uint(x
 // beta^step has fallen below half an ulp of 1 (from step 165 for beta 0.9,
 // 338 for 0.95, 17,321 for 0.999), the division by the correction is
 // an IEEE identity.  A UNIT mask names the divisions an instance leaves out;
-// the result is the same bits either way.
-enum : int { kUnitBc1 = 1, kUnitBc2 = 2 };
+// the result is the same bits either way.  kRecipBc (FADAM_RECIP_BC) turns
+// the remaining divisions by bc1 and bc2 into products with their
+// reciprocals, which the caller then passes in place of bc1 and bc2: a
+// second rounding, within the tolerance, not the same bits.
+enum : int { kUnitBc1 = 1, kUnitBc2 = 2, kRecipBc = 4 };
 
 // p' for the fp32 master x; m and v are updated in place.
 template <bool ADAMW, int UNIT = 0>
@@ -296,8 +300,14 @@ __device__ __forceinline__ float adam_elem(float x, float& m, float& v, float g,
   const float sq = __fmul_rn(sg, sg);
   const float m_next = __fadd_rn(__fmul_rn(s.beta1, m), __fmul_rn(s.omb1, sg));
   const float v_next = __fadd_rn(__fmul_rn(s.beta2, v), __fmul_rn(s.omb2, sq));
-  const float m_hat = (UNIT & kUnitBc1) ? m_next : __fdiv_rn(m_next, s.bc1);
-  const float v_hat = (UNIT & kUnitBc2) ? v_next : __fdiv_rn(v_next, s.bc2);
+  float m_hat = m_next, v_hat = v_next;
+  if constexpr (UNIT & kRecipBc) {  // s.bc1, s.bc2 hold the reciprocals
+    if constexpr (!(UNIT & kUnitBc1)) m_hat = __fmul_rn(m_next, s.bc1);
+    if constexpr (!(UNIT & kUnitBc2)) v_hat = __fmul_rn(v_next, s.bc2);
+  } else {
+    if constexpr (!(UNIT & kUnitBc1)) m_hat = __fdiv_rn(m_next, s.bc1);
+    if constexpr (!(UNIT & kUnitBc2)) v_hat = __fdiv_rn(v_next, s.bc2);
+  }
   const float denom = __fadd_rn(__fsqrt_rn(v_hat), s.eps);
   float upd = __fdiv_rn(m_hat, denom);
   if constexpr (ADAMW) upd = __fadd_rn(upd, __fmul_rn(s.wd, x));
@@ -1158,7 +1168,9 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
         }
         const unsigned char* st = smem + size_t(b) * Layout<ST, GT, REM>::stage;
         const SGroup& G = sgrp[it.group];
-        const Scal s{G.beta1, G.omb1, G.beta2, G.omb2, G.bc1, G.bc2, G.eps, G.wd, G.lr, G.gs};
+        constexpr bool kRecip = (UNIT & kRecipBc) != 0;
+        const Scal s{G.beta1, G.omb1, G.beta2, G.omb2, kRecip ? G.rbc1 : G.bc1,
+                     kRecip ? G.rbc2 : G.bc2, G.eps, G.wd, G.lr, G.gs};
         if constexpr (PASS == Pass::kScan) {
           bad |= scan_tile<Layout<ST, GT, REM>::scan_per_thread, GT>(st, tag.len, s.gs);
         } else if constexpr (PASS == Pass::kNorm) {
@@ -1526,6 +1538,7 @@ __device__ __forceinline__ bool grid_barrier(KScratch* sc, unsigned extra) {
       while (ld_acquire_u32(&sc->bar_gen) == gen) {
         if (global_ns() - t0 > kWaitLimitNs) {
           atomicExch(&sc->status, FADAM_ETIMEOUT);
+          atomicExch(&sc->launch_timeout, 1u);
           ok = 0;
           break;
         }
@@ -1597,6 +1610,8 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
       s.bc1 = bias_correction(G.beta1, step);
       s.bc2 = bias_correction(G.beta2, step);
     }
+    s.rbc1 = __frcp_rn(s.bc1);
+    s.rbc2 = __frcp_rn(s.bc2);
     sgrp[tid] = s;
   }
   __syncthreads();
@@ -1676,6 +1691,9 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
         if (sgrp[k].bc1 != 1.0f) unit &= ~kUnitBc1;
         if (sgrp[k].bc2 != 1.0f) unit &= ~kUnitBc2;
       }
+      // reciprocals: one instance for any correction that is not 1 (the
+      // product by a reciprocal of 1 is exact)
+      if ((kp.flags & kRecipBcFlag) && unit != (kUnitBc1 | kUnitBc2)) unit = kRecipBc;
     }
     bool unused = false;
     // the update passes for a compile-time unit mask U
@@ -1705,13 +1723,17 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
     };
     if constexpr (unit_bc_instances<ST, REM>()) {
       if (unit == (kUnitBc1 | kUnitBc2)) passes(std::integral_constant<int, kUnitBc1 | kUnitBc2>{});
+      else if (unit == kRecipBc) passes(std::integral_constant<int, kRecipBc>{});
       else if (unit == kUnitBc1) passes(std::integral_constant<int, kUnitBc1>{});
       else passes(std::integral_constant<int, 0>{});
     } else {
       passes(std::integral_constant<int, 0>{});
     }
   }
-  if (__syncthreads_or(timed_out) && tid == 0) atomicExch(&kp.scratch->status, FADAM_ETIMEOUT);
+  if (__syncthreads_or(timed_out) && tid == 0) {
+    atomicExch(&kp.scratch->status, FADAM_ETIMEOUT);
+    atomicExch(&kp.scratch->launch_timeout, 1u);
+  }
 
   // 4. the last CTA to finish resets the work counters for the next launch
   //    and, for capturable plans, advances the step counters; for a norm
@@ -1734,10 +1756,10 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
   }
   if (scaled_done && s_last) {
     // the new scales replace the old (tensors that had no element keep
-    // theirs), unless some wait gave up; the absmax slots are cleared for
-    // the next step either way
+    // theirs), unless some wait of this launch gave up; the absmax slots
+    // are cleared for the next step either way
     __threadfence();
-    const bool ok = ld_acquire_s32(&kp.scratch->status) == FADAM_OK;
+    const bool ok = ld_acquire_u32(&kp.scratch->launch_timeout) == 0u;
     for (int j = tid; j < 3 * kp.n_tensors; j += kBlock) {
       const unsigned a = __ldcg(kp.absmax + j);
       if (a) {
@@ -1761,6 +1783,12 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
       atomicExch(&kp.scratch->next_tail_scan, 0u);
       atomicExch(&kp.scratch->next_rescale, 0u);
       atomicExch(&kp.scratch->next_tail_rescale, 0u);
+      // every CTA has left its grid barriers by now: a wait that gave up
+      // leaves its arrival counted, which would stall the next launch's
+      // barrier, so the count starts from zero again (the status word keeps
+      // the timeout until fadam_plan_status reads it)
+      atomicExch(&kp.scratch->bar_count, 0u);
+      atomicExch(&kp.scratch->launch_timeout, 0u);
       atomicExch(&kp.scratch->done, 0u);
     }
   }

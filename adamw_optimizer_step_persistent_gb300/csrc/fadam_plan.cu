@@ -106,7 +106,8 @@ int mv_size(const Dtypes& d) {
 fadam_status check_dtypes(const Dtypes& d, uint32_t flags) {
   const uint32_t known = FADAM_CAPTURABLE | FADAM_REMAINDERS | FADAM_CHECK_FINITE |
                          FADAM_STEP_PREADVANCED | FADAM_TEST_BARRIER_TIMEOUT |
-                         FADAM_SCALED_STATES | FADAM_MOMENTS_BF16 | FADAM_MOMENTS_F16;
+                         FADAM_SCALED_STATES | FADAM_MOMENTS_BF16 | FADAM_MOMENTS_F16 |
+                         FADAM_RECIP_BC;
   if (flags & ~known) return fail(FADAM_EINVAL, "unknown flag bits 0x%x", flags & ~known);
   if ((flags & FADAM_MOMENTS_BF16) && (flags & FADAM_MOMENTS_F16))
     return fail(FADAM_EINVAL, "FADAM_MOMENTS_BF16 and FADAM_MOMENTS_F16 exclude each other");
@@ -582,6 +583,8 @@ struct fadam_plan {
   const char** d_dev_g = nullptr;
   const char** d_host_g = nullptr;
   std::vector<const char*> host_g;
+  // FADAM_TEST_BARRIER_TIMEOUT acts on the plan's first step launch only
+  bool test_timeout_armed = false;
 };
 
 namespace {
@@ -640,6 +643,18 @@ void fill_exchange(KParams& kp, const fadam_plan* plan) {
   for (int d = 0; d < plan->n_dests; ++d) kp.dst_delta[d] = plan->dst_delta[d];
 }
 
+// The plan's flags for a step launch: the barrier-timeout diagnostic goes
+// to the first such launch only, so that the launches after it show that a
+// plan recovers from a wait that gave up.
+uint32_t step_flags(fadam_plan* plan) {
+  uint32_t f = plan->hp.flags & ~kTestBarrierTimeout;
+  if (plan->test_timeout_armed) {
+    f |= kTestBarrierTimeout;
+    plan->test_timeout_armed = false;
+  }
+  return f;
+}
+
 bool needs_launch(const HostPlan& hp) {
   const bool owns_steps = (hp.flags & FADAM_CAPTURABLE) && !(hp.flags & FADAM_STEP_PREADVANCED);
   return !hp.items.empty() || owns_steps;
@@ -669,6 +684,7 @@ fadam_status fadam_plan_create(const fadam_tensor* tensors, int64_t n_tensors,
   plan->tensors.assign(tensors, tensors + n_tensors);
   plan->groups.assign(groups, groups + n_groups);
   plan->n_groups = n_groups;
+  plan->test_timeout_armed = (flags & FADAM_TEST_BARRIER_TIMEOUT) != 0;
   const HostPlan& hp = plan->hp;
   cudaError_t e = cudaSuccess;
   if (!hp.items.empty()) {
@@ -768,7 +784,7 @@ fadam_status step_launch(fadam_plan* plan, int32_t* noop_dev, fadam_stream strea
   KParams kp;
   fill_params(kp, plan->d_items, plan->d_cta, plan->d_chunks, static_cast<int32_t>(hp.chunks.size()),
               noop_dev, plan->d_scratch, plan->groups.data(), plan->n_groups,
-              hp.flags | hp.shape | extra_flags);
+              step_flags(plan) | hp.shape | extra_flags);
   fill_exchange(kp, plan);
   fill_scaled(kp, plan);
   kp.memo = plan->d_memo;
@@ -870,7 +886,7 @@ fadam_status fadam_step_reduce(fadam_plan* plan, int32_t* noop_dev, fadam_stream
   KParams kp;
   fill_params(kp, plan->d_items, plan->d_cta, plan->d_chunks, static_cast<int32_t>(hp.chunks.size()),
               noop_dev, plan->d_scratch, plan->groups.data(), plan->n_groups,
-              hp.flags | hp.shape | kReduceFirst);
+              step_flags(plan) | hp.shape | kReduceFirst);
   fill_exchange(kp, plan);
   fill_scaled(kp, plan);
   kp.memo = plan->d_memo;
@@ -1286,7 +1302,8 @@ static __device__ __align__(256) unsigned char g_noalloc_arena[kArenaBytes];
 namespace {
 
 // Device address of g_noalloc_arena on `dev` (which must be current),
-// looked up on the first call for that device.
+// looked up on the first call for that device and kept for the life of the
+// process (a cudaDeviceReset of that device would make it stale).
 fadam_status arena_address(int dev, unsigned char** out) {
   if (dev < 0 || dev >= kMaxDevices) return fail(FADAM_ELIMIT, "device %d beyond %d", dev, kMaxDevices);
   std::lock_guard<std::mutex> lock(g_arena_mutex);
@@ -1315,6 +1332,20 @@ extern "C" fadam_status fadam_step_noalloc(const fadam_tensor* tensors, int64_t 
     return fail(FADAM_EINVAL, "FADAM_CHECK_FINITE needs a noop_dev flag to write");
   if (noop_dev && reinterpret_cast<uintptr_t>(noop_dev) % 4)
     return fail(FADAM_EALIGN, "noop_dev is not 4-byte aligned");
+  // each call uploads its work list from host vectors that are gone when
+  // it returns, so a captured call would leave a graph replaying garbage:
+  // refuse a capturing stream (the implicit-capture error of the legacy
+  // stream while another stream captures counts as capturing)
+  {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    const cudaError_t ce = cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cap);
+    if (ce == cudaErrorStreamCaptureImplicit || (ce == cudaSuccess && cap != cudaStreamCaptureStatusNone)) {
+      cudaGetLastError();
+      return fail(FADAM_EINVAL, "fadam_step_noalloc is not for stream capture (the stream is "
+                                "capturing); use fadam_plan_create/fadam_step in a graph");
+    }
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamIsCapturing");
+  }
   HostPlan hp;
   fadam_status st = prepare(tensors, n_tensors, groups, n_groups, d, flags, true, kNoAllocMaxChunks,
                             hp);

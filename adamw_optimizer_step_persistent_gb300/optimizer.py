@@ -56,13 +56,16 @@ class FusedAdamShard:
     remainder mode ``params`` are the bf16 high halves (``remainders`` then
     holds the int16 low halves, the moments are fp32, and ``params_out`` the
     bf16 tensors that receive the new high halves; they may be ``params``).
+    ``recip_bc`` (16-bit state only) multiplies the moments by reciprocal
+    bias corrections instead of dividing them (FADAM_RECIP_BC): faster for
+    those issue-bound forms, within the tolerance rather than bit-identical.
     """
 
     def __init__(self, param_groups: Sequence[Dict], *, capturable: bool = False,
                  check_finite: bool = False, remainders: bool = False,
                  shared_step: bool = False, step_preadvanced: bool = False,
                  grad_scale: float = 1.0, device=None, extra_flags: int = 0,
-                 state_scales: Optional[torch.Tensor] = None):
+                 state_scales: Optional[torch.Tensor] = None, recip_bc: bool = False):
         if check_finite and not capturable:
             raise ValueError("check_finite needs capturable=True (the counters live on the device)")
         self.capturable = capturable
@@ -76,6 +79,7 @@ class FusedAdamShard:
         flags |= (_abi.CHECK_FINITE if check_finite else 0)
         flags |= (_abi.STEP_PREADVANCED if step_preadvanced else 0)
         flags |= (_abi.SCALED_STATES if state_scales is not None else 0)
+        flags |= (_abi.RECIP_BC if recip_bc else 0)
         flags |= int(extra_flags)
         self.flags = flags
 

@@ -100,11 +100,29 @@ typedef int32_t fadam_status;
  * FADAM_SCALED_STATES. */
 #define FADAM_MOMENTS_BF16 32u
 #define FADAM_MOMENTS_F16 64u
+/* Reciprocal bias corrections, for the 16-bit state forms (FADAM_DT_BF16 or
+ * FADAM_DT_F16 state, plain or FADAM_SCALED_STATES), whose update is bound
+ * by instruction issue rather than by memory: each CTA computes 1/bc1 and
+ * 1/bc2 once per group (IEEE reciprocals) and the update tiles multiply the
+ * moments by them instead of dividing every element by bc1 and bc2 (the
+ * functor's m/bc1 and v/bc2).  Each bias-corrected moment then carries two
+ * roundings instead of one, so results are no longer bit-identical to the
+ * division: the update u = m_hat / (sqrt(v_hat) + eps) moves by at most a
+ * few float ulps, and a stored 16-bit value by at most one unit in its last
+ * place per step.  Once a correction rounds to 1 in float the multiply is
+ * exact.  Other state forms (fp32 master, remainders, 16-bit moments) are
+ * bound by memory, keep the division and ignore the flag, as do the at most
+ * 7 tail elements of each tensor and tensors not 16-byte aligned. */
+#define FADAM_RECIP_BC 128u
 /* Diagnostic, for testing the failure path: with FADAM_CHECK_FINITE, the
- * grid barrier after the inf/nan screen waits for one more CTA than the
- * launch has, so every CTA's wait runs out after its limit (about 2 s).
- * The step then updates nothing, advances no counter, and
- * fadam_plan_status() reports FADAM_ETIMEOUT.  Never set in normal use. */
+ * grid barrier after the inf/nan screen of the plan's FIRST step launch
+ * (fadam_step, fadam_step_reduce or fadam_step_host_grads) waits for one
+ * more CTA than the launch has, so every CTA's wait runs out after its limit
+ * (about 2 s).  That step then updates nothing, advances no counter, and
+ * fadam_plan_status() reports FADAM_ETIMEOUT; the plan's later launches run
+ * normally, which shows that a plan recovers from a wait that gave up.
+ * fadam_step_noalloc applies it to every call that passes it.  Never set in
+ * normal use. */
 #define FADAM_TEST_BARRIER_TIMEOUT 0x80000000u
 
 /* Maximum number of param groups in one plan. */
@@ -208,7 +226,7 @@ typedef struct {
  *                       FADAM_SCALED_STATES (bf16 or fp16 state only; set
  *                       the scales with fadam_plan_set_state_scales) |
  *                       FADAM_MOMENTS_BF16 or FADAM_MOMENTS_F16 (fp32 master
- *                       with m and v in that dtype)
+ *                       with m and v in that dtype) | FADAM_RECIP_BC
  *   *plan_out           receives the plan (owned by the caller; free with
  *                       fadam_plan_destroy)
  * Errors: FADAM_EINVAL, FADAM_EDTYPE, FADAM_EALIGN, FADAM_ELIMIT, FADAM_ECUDA;
@@ -373,9 +391,13 @@ fadam_status fadam_step_reduce(fadam_plan* plan, int32_t* noop_dev, fadam_stream
 fadam_status fadam_plan_set_state_scales(fadam_plan* plan, float* scales_dev);
 
 /* Read (synchronously) and clear the plan's device status word:
- * *device_status = FADAM_OK, or FADAM_ETIMEOUT when a bounded wait of the
- * FADAM_CHECK_FINITE grid barrier gave up (that step may be partly applied).
- * Clearing also resets the barrier counters.  Errors: FADAM_EINVAL,
+ * *device_status = FADAM_OK, or FADAM_ETIMEOUT when a bounded device wait
+ * (a grid barrier, or a bulk copy's completion) of some launch since the
+ * last read gave up; that launch may be partly applied.  The word is sticky
+ * until read, but it does not block the plan: each launch's last CTA resets
+ * the barrier counters, so the next launch runs normally whether or not
+ * the status was read in between (a scaled-state launch replaces the
+ * scales unless one of its own waits gave up).  Errors: FADAM_EINVAL,
  * FADAM_ECUDA. */
 fadam_status fadam_plan_status(fadam_plan* plan, int32_t* device_status);
 
@@ -408,10 +430,16 @@ fadam_status fadam_step_once(const fadam_tensor* tensors, int64_t n_tensors, int
  * only use memory handed to it, and latency-critical loops where
  * cudaMalloc/cudaFree could synchronise the device.  This call packs the
  * shard on the host, as fadam_plan_create does, and runs one step as
- * fadam_step does, but keeps the work list and the status block in a
- * static device array instead of allocated memory: about 340 KB that every
- * GPU which loads this library holds until the process exits.  It calls no
- * cudaMalloc, cudaFree or other allocating routine.
+ * fadam_step does, but keeps the work list, the status block and the
+ * bias-correction memo in a static device array instead of allocated
+ * memory: about 340 KB that every GPU which loads this library holds until
+ * the process exits.  It calls no cudaMalloc, cudaFree or other allocating
+ * routine.
+ *
+ * Not for stream capture: each call copies its work list from host memory
+ * that is freed when the call returns, which a captured graph could not
+ * replay.  A call on a capturing stream returns FADAM_EINVAL before any
+ * device work; graphs use fadam_plan_create / fadam_step.
  *
  * Limits: at most 4096 work items (roughly one per tensor plus one per CTA
  * of the grid) and 2048 CTAs; a larger shard is rejected with FADAM_ELIMIT
@@ -421,13 +449,16 @@ fadam_status fadam_step_once(const fadam_tensor* tensors, int64_t n_tensors, int
  * Arguments: as fadam_plan_create, plus noop_dev and stream as fadam_step;
  * the step counters behave as in fadam_step.
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any
- * stream capture.  Each call copies its work list into the array and
- * clears the status block on `stream` before the launch.  All calls share
- * the one array and it keeps the last call's contents: calls whose work
- * overlaps on the GPU (unordered streams, or concurrent host threads) race,
- * so issue them in order on one stream.  Errors: as fadam_plan_create and
- * fadam_step, FADAM_ELIMIT beyond the limits above. */
+ * device, with that device current) and keeps it for the life of the
+ * process; it does not survive a cudaDeviceReset() of that device, so do
+ * not call this entry point on a device after resetting it.  Each call
+ * copies its work list into the array and clears the status block on
+ * `stream` before the launch.  All calls share the one array and it keeps
+ * the last call's contents: calls whose work overlaps on the GPU (unordered
+ * streams, or concurrent host threads) race on the work list, the status
+ * block and the memo, so issue them in order on one stream.  Errors: as
+ * fadam_plan_create and fadam_step, FADAM_ELIMIT beyond the limits above,
+ * FADAM_EINVAL on a capturing stream. */
 fadam_status fadam_step_noalloc(const fadam_tensor* tensors, int64_t n_tensors,
                                 const fadam_group* groups, int32_t n_groups, int32_t p_dtype,
                                 int32_t g_dtype, int32_t out_dtype, uint32_t flags,

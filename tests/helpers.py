@@ -8,7 +8,7 @@ Tolerances (GPU vs oracle):
 """
 from __future__ import annotations
 
-from typing import Dict, List
+from typing import Dict, List, Optional
 
 import numpy as np
 import torch
@@ -43,20 +43,33 @@ def oracle_groups(spec: workloads.ShardSpec) -> List[oracle.Group]:
     return out
 
 
+def _selector(elems, i: int, device):
+    """Element selection of tensor i: everything, a contiguous range (a
+    slice) or gathered indices."""
+    if elems is None:
+        return lambda t: t
+    e = elems[i]
+    if isinstance(e, slice):
+        return lambda t: t[e]
+    e = torch.as_tensor(e, device=device)
+    return lambda t: t[e]
+
+
 def oracle_shard(shard: workloads.Shard, idx: List[int] = None, elems: Dict[int, np.ndarray] = None,
                  step_slot=None, scales: torch.Tensor = None) -> oracle.Shard:
     """Snapshot of the shard (or of sampled elements of it) as oracle arrays.
 
     `idx` is the tensor order; `elems[i]`, when given, selects elements of
-    tensor i (the oracle then runs on the gathered samples only, which is
-    exact because every element updates independently).
+    tensor i, as an index array or a slice (the oracle then runs on the
+    selected elements only, which is exact because every element updates
+    independently).
     """
     spec = shard.spec
     idx = shard.plan_order() if idx is None else idx
     g_dt = _ODT[spec.g_dtype]
     tensors = []
     for i in idx:
-        sel = (lambda t: t) if elems is None else (lambda t, e=torch.as_tensor(elems[i], device=shard.params[i].device): t[e])
+        sel = _selector(elems, i, shard.params[i].device)
         t = oracle.Tensor(group=spec.group_of[i], m=to_np(sel(shard.exp_avgs[i])),
                           v=to_np(sel(shard.exp_avg_sqs[i])), g=to_np(sel(shard.grads[i])),
                           g_dtype=g_dt)
@@ -83,10 +96,36 @@ def oracle_shard(shard: workloads.Shard, idx: List[int] = None, elems: Dict[int,
 def refresh_grads(osh: oracle.Shard, shard: workloads.Shard, idx=None, elems=None) -> None:
     idx = shard.plan_order() if idx is None else idx
     for t, i in zip(osh.tensors, idx):
-        g = shard.grads[i]
-        if elems is not None:
-            g = g[torch.as_tensor(elems[i], device=g.device)]
-        t.g = to_np(g)
+        t.g = to_np(_selector(elems, i, shard.grads[i].device)(shard.grads[i]))
+
+
+def put(dst: Optional[torch.Tensor], arr: Optional[np.ndarray]) -> None:
+    """Write an oracle array (fp32 values, 16-bit bit patterns or int16)
+    into a device tensor of the same size."""
+    if dst is None or arr is None:
+        return
+    if dst.dtype == torch.float32:
+        dst.copy_(torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32)))
+    else:
+        dst.view(torch.int16).copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)))
+
+
+def load_oracle_state(shard: workloads.Shard, osh: oracle.Shard, idx=None,
+                      scales: torch.Tensor = None) -> None:
+    """Make the oracle's current state the GPU shard's (p, m, v, the
+    remainders, and the scaled state's scales in the order of idx), so that
+    the next step starts both from the same values."""
+    idx = shard.plan_order() if idx is None else idx
+    for k, (t, i) in enumerate(zip(osh.tensors, idx)):
+        put(shard.exp_avgs[i], t.m)
+        put(shard.exp_avg_sqs[i], t.v)
+        if t.rem is not None:
+            put(shard.params[i], t.p_hi)
+            put(shard.remainders[i], t.rem)
+        else:
+            put(shard.params[i], t.p)
+        if scales is not None and t.scales is not None:
+            scales[k].copy_(torch.from_numpy(np.ascontiguousarray(t.scales, dtype=np.float32)))
 
 
 def _ordered16(bits: np.ndarray) -> np.ndarray:
@@ -109,7 +148,27 @@ class Report:
         self.exact = 0
         self.worst = 0.0
 
+    def _same_bytes(self, got: np.ndarray, want: np.ndarray) -> bool:
+        """Equal bit patterns (the common case): counted as exact, with no
+        need for the tolerance arithmetic."""
+        if got.shape != want.shape or got.dtype.itemsize != want.dtype.itemsize:
+            return False
+        u = {2: np.uint16, 4: np.uint32}.get(got.dtype.itemsize)
+        if u is None or not np.array_equal(np.ascontiguousarray(got).view(u),
+                                           np.ascontiguousarray(want).view(u)):
+            return False
+        self.n += got.size
+        self.exact += got.size
+        return True
+
+    def merge(self, other: "Report") -> None:
+        self.n += other.n
+        self.exact += other.exact
+        self.worst = max(self.worst, other.worst)
+
     def f32(self, got: np.ndarray, want: np.ndarray, what: str) -> None:
+        if self._same_bytes(got, want):
+            return
         got = got.astype(np.float64)
         want = want.astype(np.float64)
         both_nan = np.isnan(got) & np.isnan(want)
@@ -131,6 +190,8 @@ class Report:
             self.worst = max(self.worst, float(rel.max()))
 
     def ulp16(self, got: np.ndarray, want: np.ndarray, what: str, dtype=None) -> None:
+        if self._same_bytes(got, want):
+            return
         d = np.abs(_ordered16(got) - _ordered16(want))
         if dtype is not None:  # two NaNs match whatever their payloads
             d = np.where(_is_nan16(got, dtype) & _is_nan16(want, dtype), 0, d)
@@ -154,7 +215,7 @@ def compare(shard: workloads.Shard, osh: oracle.Shard, idx=None, elems=None,
     idx = shard.plan_order() if idx is None else idx
     state16 = not spec.remainders and spec.state_dtype != torch.float32
     for t, i in zip(osh.tensors, idx):
-        sel = (lambda x: x) if elems is None else (lambda x, e=torch.as_tensor(elems[i], device=shard.params[i].device): x[e])
+        sel = _selector(elems, i, shard.params[i].device)
         if state16:  # 16-bit p, m, v: within one unit in the last place
             sdt = spec.state_dtype
             report.ulp16(to_np(sel(shard.exp_avgs[i])), t.m, f"tensor {i} m", sdt)

@@ -127,6 +127,35 @@ def test_screen_skips_a_scaled_step():
     opt.close()
 
 
+def test_scaled_plan_recovers_from_a_wait_that_gave_up():
+    """The first step's screen barrier runs out (diagnostic flag): nothing is
+    written, scales included.  The next steps on the same plan, its status
+    left unread, store the rescaled state and replace the scales as the
+    oracle does (a timeout of an earlier launch does not hold the new scales
+    back)."""
+    spec, shard, opt, osh, scales = _make("scaled_state_shard", capturable=True, check_finite=True,
+                                          extra_flags=_abi.TEST_BARRIER_TIMEOUT)
+    snap = helpers.snapshot(shard)
+    before = scales.clone()
+    opt.step()
+    torch.cuda.synchronize()
+    assert helpers.state_equal(shard, snap) and torch.equal(before, opt.state_scales)
+    assert opt.group_steps() == [0] and opt.noop.item() == 0
+    rep = helpers.Report()
+    for k in (2, 3):
+        workloads.fresh_grads(shard, k)
+        helpers.refresh_grads(osh, shard)
+        opt.step()
+        oracle.shard_step(osh, capturable=True)
+        torch.cuda.synchronize()
+        helpers.compare(shard, osh, report=rep)
+        _check_scales(opt, osh)
+    assert rep.exact_fraction == 1.0
+    assert opt.group_steps() == [2]
+    assert opt.device_status() == _abi.ETIMEOUT and opt.device_status() == _abi.OK
+    opt.close()
+
+
 def test_graph_replay_equals_eager():
     _, a, oa, _, _ = _make("scaled_state_shard", capturable=True)
     _, b, ob, _, _ = _make("scaled_state_shard", capturable=True)
