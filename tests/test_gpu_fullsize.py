@@ -1,13 +1,24 @@
 """GPU parity at the full workload sizes, in the launch configuration the
-benchmark uses (default plan: persistent grid sized to the device).
+benchmark uses (default plan: persistent grid sized to the device), over
+every element.
 
-The oracle cannot redo 1-4e9 elements per step in seconds, so each test
-samples elements (every tensor's first and last element included), gathers
-their inputs before the steps, and lets the oracle run the same steps on the
-samples only; every element updates independently, so this is exact.  The
-noop step of the capturable L2 shard is checked bit-exactly over the whole
-state, and the step counters over every group.
+The state each tensor starts from is cloned on the device before the GPU
+runs all the steps of a workload (gradients that do not change between
+steps are only read, so the shard's own serve).  The oracle then replays
+the same steps tensor by tensor, each tensor cut into contiguous ranges of
+elements (exact, because every element updates independently; the scaled
+state, whose rescale needs every new value of a tensor, replays whole
+tensors), on a pool of one thread per host core, and every value the GPU
+wrote is compared with the oracle's under the parity tolerances (equal
+bytes are counted without the tolerance arithmetic).  Each test prints how
+many values it compared against how many the shard holds.  The noop step
+of the capturable L2 shard is also checked bit-exactly over the whole state
+on the GPU, and the step counters over every group.
 """
+import os
+from concurrent.futures import ThreadPoolExecutor
+from types import SimpleNamespace
+
 import numpy as np
 import pytest
 import torch
@@ -20,23 +31,79 @@ from tests import helpers
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
+THREADS = max(1, len(os.sched_getaffinity(0)))
+RANGE = 1 << 22  # elements per oracle work unit
+
 
 def _free():
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
 
 
-def _sampled_run(spec, steps, per_tensor, tensor_subset=None, inf_step=None, capturable=None):
+def _clone(lst):
+    return [None if t is None else t.clone() for t in lst]
+
+
+def _inputs(shard, grads=None):
+    """The state every tensor starts from, as device clones, in the shape
+    helpers.oracle_shard reads (param-out is only written, so the shard's
+    own buffers serve)."""
+    return SimpleNamespace(spec=shard.spec, params=_clone(shard.params),
+                           exp_avgs=_clone(shard.exp_avgs), exp_avg_sqs=_clone(shard.exp_avg_sqs),
+                           remainders=_clone(shard.remainders), params_out=shard.params_out,
+                           grads=shard.grads if grads is None else grads)
+
+
+def _units(spec, order, whole=False):
+    """(tensor, element range) work units: every non-empty tensor in ranges
+    of RANGE elements, or whole."""
+    out = []
+    for i in order:
+        n = spec.sizes[i]
+        if n == 0:
+            continue
+        if whole:
+            out.append((i, None))
+        else:
+            out += [(i, slice(a, min(n, a + RANGE))) for a in range(0, n, RANGE)]
+    return out
+
+
+def _replay(shard, init, unit, schedule, capturable):
+    """The oracle's steps on one unit, then the comparison with the GPU."""
+    i, sl = unit
+    elems = None if sl is None else {i: sl}
+    osh = helpers.oracle_shard(init, idx=[i], elems=elems)
+    for noop in schedule:
+        oracle.shard_step(osh, capturable=capturable, noop=noop)
+    return helpers.compare(shard, osh, idx=[i], elems=elems)
+
+
+def _pool_map(fn, units):
+    rep = helpers.Report()
+    with ThreadPoolExecutor(max_workers=THREADS) as ex:
+        for r in ex.map(fn, units):
+            rep.merge(r)
+    return rep
+
+
+def _values_per_element(spec):
+    """Values the comparison reads per element: p (or the packed master and
+    its high half), m, v, and param-out when it is a separate buffer."""
+    if spec.remainders:
+        return 4
+    return 3 + (1 if spec.out_dtype is not None else 0)
+
+
+def _full_run(spec, steps, inf_step=None, capturable=None):
     if capturable is not None:
         spec.capturable = capturable
     shard = workloads.materialize(spec, DEV)
     opt = FusedAdamShard(shard.param_groups(), capturable=spec.capturable,
                          remainders=spec.remainders, grad_scale=spec.grad_scale)
-    order = shard.plan_order()
-    idx = order if tensor_subset is None else [i for i in order if i in tensor_subset]
-    elems = helpers.sample_elements(spec, per_tensor, seed=spec.seed + 5)
-    osh = helpers.oracle_shard(shard, idx=idx, elems=elems)
+    init = _inputs(shard)
     t_inf, e_inf = workloads.inf_position(spec) if inf_step else (None, None)
+    schedule = []
     for k in range(1, steps + 1):
         noop = k == inf_step
         if noop:
@@ -52,54 +119,62 @@ def _sampled_run(spec, steps, per_tensor, tensor_subset=None, inf_step=None, cap
             del before
             shard.grads[t_inf][e_inf] = saved
             opt.noop.zero_()
-        oracle.shard_step(osh, capturable=spec.capturable, noop=noop)
+        schedule.append(noop)
     torch.cuda.synchronize()
-    rep = helpers.compare(shard, osh, idx=idx, elems=elems)
     steps_dev = opt.group_steps()
     opt.close()
-    del shard, opt
+    rep = _pool_map(lambda u: _replay(shard, init, u, schedule, spec.capturable),
+                    _units(spec, shard.plan_order()))
+    total = _values_per_element(spec) * sum(spec.sizes)
+    want_steps = [sum(1 for n in schedule if not n)] * len(spec.groups)
+    del shard, init
     _free()
-    return rep, steps_dev, oracle.group_steps(osh)
+    return rep, total, steps_dev, want_steps
+
+
+def _report(name, rep, total):
+    print(f"{name}: {rep.n} of {total} values compared, {rep.exact} bit-identical, "
+          f"worst {rep.worst:.3g} of tolerance")
+    assert rep.n == total
 
 
 def test_large_uniform_full_size():
+    # the benchmark's headline path: capturable, device scalars; two steps
+    # over all 4,215,275,520 elements
     spec = workloads.large_uniform()
-    # the benchmark's headline path: capturable, device scalars
-    rep, steps, want = _sampled_run(spec, 2, per_tensor=4096, capturable=True)
+    rep, total, steps, want = _full_run(spec, 2, capturable=True)
     assert steps == want == [2]
-    print(f"large_uniform: {rep.n} sampled values, {rep.exact_fraction:.6f} bit-identical")
+    _report("large_uniform", rep, total)
 
 
 def test_large_uniform_bf16_moments_full_size():
     # the 201-tensor shard with an fp32 master and bf16 moments, capturable
     spec = workloads.large_uniform(moment_dtype=torch.bfloat16)
-    rep, steps, want = _sampled_run(spec, 2, per_tensor=2048, capturable=True)
+    rep, total, steps, want = _full_run(spec, 2, capturable=True)
     assert steps == want == [2]
+    _report("large_uniform_bf16_moments", rep, total)
     assert rep.exact_fraction == 1.0
 
 
 def test_capturable_l2_full_size_with_inf_step():
     spec = workloads.capturable_l2()
-    rep, steps, want = _sampled_run(spec, 5, per_tensor=4096, inf_step=spec.inf_at_step)
-    assert steps == want == [4]
-    print(f"capturable_l2: {rep.n} sampled values, {rep.exact_fraction:.6f} bit-identical")
+    rep, total, steps, want = _full_run(spec, 10, inf_step=spec.inf_at_step)
+    assert steps == want == [9]
+    _report("capturable_l2", rep, total)
 
 
 def test_remainder_shard_full_size():
     spec = workloads.remainder_shard()
-    rep, steps, want = _sampled_run(spec, 3, per_tensor=2048)
-    assert steps == want == [3]
-    print(f"remainder_shard: {rep.n} sampled values, {rep.exact_fraction:.6f} bit-identical")
+    rep, total, steps, want = _full_run(spec, 10)
+    assert steps == want == [10]
+    _report("remainder_shard", rep, total)
 
 
 def test_many_small_full_size():
     spec = workloads.many_small()
-    rng = np.random.default_rng(3)
-    subset = set(rng.choice(len(spec.sizes), size=1500, replace=False).tolist())
-    subset |= {0, len(spec.sizes) - 1}
-    rep, steps, want = _sampled_run(spec, 5, per_tensor=256, tensor_subset=subset)
-    assert steps == want == [5, 5, 5]
-    print(f"many_small: {rep.n} sampled values, {rep.exact_fraction:.6f} bit-identical")
+    rep, total, steps, want = _full_run(spec, 10)
+    assert steps == want == [10, 10, 10]
+    _report("many_small", rep, total)
 
 
 def test_tensor_beyond_2_pow_31_elements():
@@ -107,19 +182,15 @@ def test_tensor_beyond_2_pow_31_elements():
     spec = workloads.large_uniform(n_tensors=1, numel=n)
     shard = workloads.materialize(spec, DEV)
     opt = FusedAdamShard(shard.param_groups(), capturable=False)
-    e = np.unique(np.concatenate([np.arange(0, 64), np.arange(n - 4200, n),
-                                  (1 << 31) + np.arange(-64, 64),
-                                  np.random.default_rng(1).choice(n, 100_000, replace=False)]))
-    elems = {0: e.astype(np.int64)}
-    osh = helpers.oracle_shard(shard, elems=elems)
+    init = _inputs(shard)
     opt.step()
-    oracle.shard_step(osh, capturable=False)
     torch.cuda.synchronize()
-    helpers.compare(shard, osh, elems=elems)
     info = opt.info()
     assert info["n_elements"] == n and info["n_items"] >= 32
     opt.close()
-    del shard, opt
+    rep = _pool_map(lambda u: _replay(shard, init, u, [False], False), _units(spec, [0]))
+    _report("one tensor of 2^31 + 4099", rep, 3 * n)
+    del shard, init
     _free()
 
 
@@ -130,8 +201,9 @@ def test_large_uniform_norm_full_size():
     shard = workloads.materialize(spec, DEV)
     opt = FusedAdamShard(shard.param_groups(), capturable=True)
     got = opt.grad_norm_sq().item()
-    want = sum(oracle.sumsq(helpers.to_np(g), oracle.DT_F32) for g in shard.grads)
-    assert got == pytest.approx(want, rel=2e-6)
+    with ThreadPoolExecutor(max_workers=THREADS) as ex:
+        parts = list(ex.map(lambda g: oracle.sumsq(helpers.to_np(g), oracle.DT_F32), shard.grads))
+    assert got == pytest.approx(sum(parts), rel=2e-6)
     opt.close()
     del shard, opt
     _free()
@@ -140,64 +212,75 @@ def test_large_uniform_norm_full_size():
 def test_exchange_shard_full_size():
     """Eight ranks' bf16 gradients averaged into the 1.2e9-element shard and
     stepped in one launch, param-out to the seven other ranks' places, for
-    two steps; sampled elements against the oracle (the reduced gradient
-    bit for bit), destinations byte-equal over the whole shard."""
+    two steps; every element against the oracle (the reduced gradient bit
+    for bit), destinations byte-equal over the whole shard."""
     spec = workloads.exchange_versions(full=True)["exchange_shard"]
     shard = workloads.materialize(spec, DEV)
     opt = FusedAdamShard(shard.param_groups(), capturable=True)
     opt.set_exchange(shard.buckets["g"], list(shard.sources), average=True,
                      out_shard=shard.buckets["p_out"], dests=list(shard.dests))
-    order = shard.plan_order()
-    elems = helpers.sample_elements(spec, 4096, seed=spec.seed + 5)
-    osh = helpers.oracle_shard(shard, elems=elems)
-    src = []
-    for i in order:
-        e = torch.as_tensor(elems[i], device=DEV) + shard.offsets[i]
-        src.append([helpers.to_np(shard.sources[r][e]) for r in range(spec.exchange_ranks)])
+    init = _inputs(shard)
     for _ in range(2):
         opt.step_reduce()
-        oracle.exchange_step(osh, src, average=True, capturable=True)
     torch.cuda.synchronize()
-    for t, i in zip(osh.tensors, order):
-        got = helpers.to_np(shard.grads[i][torch.as_tensor(elems[i], device=DEV)])
-        assert got.tobytes() == t.g.tobytes(), f"tensor {i}: reduced gradient differs"
-    rep = helpers.compare(shard, osh, elems=elems)
+    assert opt.group_steps() == [2]
+    opt.close()
+
+    def unit(u):
+        i, sl = u
+        a = shard.offsets[i] + sl.start
+        b = shard.offsets[i] + sl.stop
+        src = [[helpers.to_np(shard.sources[r][a:b]) for r in range(spec.exchange_ranks)]]
+        osh = helpers.oracle_shard(init, idx=[i], elems={i: sl})
+        for _ in range(2):
+            oracle.exchange_step(osh, src, average=True, capturable=True)
+        got = helpers.to_np(shard.grads[i][sl])
+        assert got.tobytes() == osh.tensors[0].g.tobytes(), f"tensor {i}: reduced gradient differs"
+        return helpers.compare(shard, osh, idx=[i], elems={i: sl})
+
+    rep = _pool_map(unit, _units(spec, shard.plan_order()))
+    _report("exchange_shard", rep, 4 * sum(spec.sizes))
     assert rep.exact_fraction == 1.0
     out = shard.buckets["p_out"].view(torch.int16)
     for d in range(spec.exchange_dests):
         assert torch.equal(shard.dests[d].view(torch.int16), out), f"destination {d}"
-    assert opt.group_steps() == [2]
-    opt.close()
-    del shard, opt
+    del shard, init
     _free()
 
 
 def test_scaled_state_full_size():
-    """The 1.2e9-element fp16 scaled-state shard, two regular steps.  The
-    rescale depends on every element of a tensor, so the oracle runs whole
-    tensors: the first layer's 4096x4096 and 4096x11008 matrices and both
-    norm vectors, against every one of their elements and their scales."""
+    """The 1.2e9-element fp16 scaled-state shard, two regular steps with
+    fresh gradients for the second.  The rescale depends on every element
+    of a tensor, so the oracle replays whole tensors: every element of every
+    tensor, and every tensor's scales, bit for bit."""
     spec = workloads.scaled_versions(full=True)["scaled_state_shard"]
     shard = workloads.materialize(spec, DEV)
     order = shard.plan_order()
     scales = shard.state_scales[order].contiguous()
+    scales0 = scales.clone()
     opt = FusedAdamShard(shard.param_groups(), state_scales=scales)
-    pos = [0, 1, 4, 5]
-    idx = [order[k] for k in pos]
-    osh = helpers.oracle_shard(shard, idx=idx, scales=scales[pos])
-    for k in (1, 2):
-        if k > 1:
-            workloads.fresh_grads(shard, k)
-            helpers.refresh_grads(osh, shard, idx=idx)
-        opt.step()
-        oracle.shard_step(osh, capturable=False)
+    init = _inputs(shard, grads=_clone(shard.grads))
+    opt.step()
+    workloads.fresh_grads(shard, 2)
+    opt.step()
     torch.cuda.synchronize()
-    rep = helpers.compare(shard, osh, idx=idx)
-    assert rep.exact_fraction == 1.0
-    got = helpers.to_np(scales)
-    for k, t in zip(pos, osh.tensors):
-        assert got[k].tobytes() == t.scales.tobytes(), k
     assert opt.group_steps() == [2]
     opt.close()
-    del shard, opt
+    got_scales = helpers.to_np(scales)
+    pos = {i: k for k, i in enumerate(order)}
+
+    def unit(u):
+        i, _ = u
+        k = pos[i]
+        osh = helpers.oracle_shard(init, idx=[i], scales=scales0[k:k + 1])
+        oracle.shard_step(osh, capturable=False)
+        osh.tensors[0].g = helpers.to_np(shard.grads[i])
+        oracle.shard_step(osh, capturable=False)
+        assert got_scales[k].tobytes() == osh.tensors[0].scales.tobytes(), i
+        return helpers.compare(shard, osh, idx=[i])
+
+    rep = _pool_map(unit, _units(spec, order, whole=True))
+    _report("scaled_state_shard", rep, _values_per_element(spec) * sum(spec.sizes))
+    assert rep.exact_fraction == 1.0
+    del shard, init
     _free()
