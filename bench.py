@@ -31,7 +31,6 @@ import subprocess
 import sys
 import threading
 import time
-from concurrent.futures import ThreadPoolExecutor
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -176,7 +175,9 @@ def summarise(per_ms, bytes_per_step, elems, world, device):
             "gbs": agg["gbs"], "gparams_per_s": agg["gparams_per_s"]}
 
 
-PROFILE = os.path.join(ROOT, "profiles", "fadam_update_kernel_large_uniform_8x20971520.md")
+# ncu counters of the headline kernel (one capture of the large_uniform launch,
+# with the hash of the kernel sources it was taken on)
+PROFILE = os.path.join(ROOT, "profiles", "fadam_update_kernel_large_uniform_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "include", "fadam.h")] + sorted(
     os.path.join(ROOT, "adamw_optimizer_step_persistent_gb300", "csrc", f)
     for f in os.listdir(os.path.join(ROOT, "adamw_optimizer_step_persistent_gb300", "csrc"))
@@ -207,25 +208,19 @@ def kernel_source_hash() -> str:
 
 
 def profiled_traffic(elements: int):
-    """DRAM bytes per launch from the committed ncu summary of the headline
-    kernel, scaled from its capture case by elements, or None when the
-    kernel sources changed since the capture."""
+    """DRAM bytes (read + written) per launch from the committed ncu counters
+    of the headline kernel, per element of the captured launch times the
+    elements of this one, or None when the kernel sources changed since the
+    capture (or there is none)."""
     try:
         with open(PROFILE) as fh:
-            text = fh.read()
-    except OSError:
+            d = json.load(fh)
+        if d.get("source_sha256") != kernel_source_hash():
+            return None
+        per_elem = (float(d["dram_bytes_read"]) + float(d["dram_bytes_write"])) / float(d["elements"])
+    except (OSError, KeyError, ValueError, TypeError, ZeroDivisionError):
         return None
-    fields = {}
-    for line in text.splitlines():
-        if ":" in line and line.split(":", 1)[0].strip() in ("source_sha256", "traffic_bytes_per_element"):
-            k, v = line.split(":", 1)
-            fields[k.strip()] = v.strip().strip("`")
-    if fields.get("source_sha256") != kernel_source_hash():
-        return None
-    try:
-        return float(fields["traffic_bytes_per_element"]) * elements
-    except (KeyError, ValueError):
-        return None
+    return per_elem * elements
 
 
 def measured_peaks() -> dict:
@@ -258,57 +253,122 @@ def e2e_fits(node_bytes: int, world: int, device=None) -> bool:
 
 # ---- CPU baseline (the oracle, as it stands) ----------------------------------
 
-def cpu_oracle_run(n_tensors: int, steps: int, threads: int, numel: int):
-    """Time the oracle on `n_tensors` tensors of the large-uniform recipe for
-    `steps` steps, tensors split into `threads` contiguous chunks run by a
-    thread pool (ctypes releases the GIL).  Returns (seconds per step, elems)."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def _np_view(t: torch.Tensor) -> np.ndarray:
+    """Zero-copy numpy view of a CPU tensor (16-bit floats as uint16 bits)."""
+    if t.dtype in (torch.bfloat16, torch.float16):
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+# bounded CPU samples of the four timed workloads: (name, spec factory,
+# bytes per element), each about 0.15-0.35e9 elements
+CPU_SAMPLES = [
+    ("capturable_l2", lambda: workloads.capturable_l2(layers=1), 28),
+    ("large_uniform", lambda: workloads.large_uniform(n_tensors=8), 28),
+    ("remainder_shard", lambda: workloads.remainder_shard(total=150_000_000, n_views=64), 26),
+    ("many_small", lambda: workloads.many_small(n_tensors=2500), 28),
+]
+
+
+def cpu_oracle_steps(spec, steps: int):
+    """Time `steps` steps of the oracle's timed OpenMP build (-O3 -fopenmp;
+    each tensor split across the host cores) on a CPU copy of `spec`.
+    Returns (seconds per step, elements)."""
     import oracle
 
-    spec = workloads.large_uniform(n_tensors=n_tensors, numel=numel)
     shard = workloads.materialize(spec, "cpu")
-    g = spec.groups[0]
-    grp = oracle.Group(mode=oracle.MODE_ADAMW, bias_correction=1, beta1=g.betas[0],
-                       beta2=g.betas[1], eps=g.eps, weight_decay=g.weight_decay, lr=g.lr)
-    arrays = [(p.numpy(), m.numpy(), v.numpy(), gr.numpy())
-              for p, m, v, gr in zip(shard.params, shard.exp_avgs, shard.exp_avg_sqs, shard.grads)]
-    chunks = []
-    for p, m, v, gr in arrays:
-        bounds = np.linspace(0, p.size, threads + 1).astype(np.int64)
-        for a, b in zip(bounds[:-1], bounds[1:]):
-            if b > a:
-                chunks.append((p[a:b], m[a:b], v[a:b], gr[a:b]))
+    gdt = {torch.float32: oracle.DT_F32, torch.bfloat16: oracle.DT_BF16,
+           torch.float16: oracle.DT_F16}
+    groups = [oracle.Group(mode=oracle.MODE_ADAMW if g.adam_w_mode else oracle.MODE_L2,
+                           bias_correction=1 if g.bias_correction else 0, beta1=g.betas[0],
+                           beta2=g.betas[1], eps=g.eps, weight_decay=g.weight_decay, lr=g.lr,
+                           grad_scale=spec.grad_scale) for g in spec.groups]
+    work = []
+    for i in shard.plan_order():
+        if spec.sizes[i] == 0:
+            continue
+        grp = groups[spec.group_of[i]]
+        g = _np_view(shard.grads[i])
+        m, v = _np_view(shard.exp_avgs[i]), _np_view(shard.exp_avg_sqs[i])
+        if spec.remainders:
+            hi, rem = _np_view(shard.params[i]), shard.remainders[i].numpy()
+            work.append(lambda k, a=(hi, rem, m, v, g), grp=grp: oracle.adam_rem(
+                grp, k, a[0], a[1], a[2], a[3], a[4], gdt[spec.g_dtype], a[0], timed=True))
+        else:
+            p = _np_view(shard.params[i])
+            out = _np_view(shard.params_out[i]) if shard.params_out[i] is not None else None
+            odt = gdt[spec.out_dtype] if spec.out_dtype is not None else oracle.DT_NONE
+            work.append(lambda k, a=(p, m, v, g, out), grp=grp, odt=odt: oracle.adam_f32(
+                grp, k, a[0], a[1], a[2], a[3], gdt[spec.g_dtype], a[4], odt, timed=True))
     per_step = []
-    with ThreadPoolExecutor(max_workers=threads) as pool:
-        for k in range(1, steps + 1):
-            t0 = time.perf_counter()
-            list(pool.map(lambda c: oracle.adam_f32(grp, k, *c), chunks))
-            per_step.append(time.perf_counter() - t0)
+    for k in range(1, steps + 1):
+        t0 = time.perf_counter()
+        for w in work:
+            w(k)
+        per_step.append(time.perf_counter() - t0)
     return per_step, spec.n_elements
 
 
-def cpu_baseline(n_tensors=8, steps=10):
-    threads = os.cpu_count() or 1
-    per_step, elems = cpu_oracle_run(n_tensors, steps, threads, 320 * 65536)
-    sec = statistics.mean(per_step)
-    return {"value": elems * 28 / sec / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "gparams_per_s": elems / sec / 1e9,
-            "sample": f"{n_tensors} of the 201 tensors x 20,971,520 fp32 elements "
-                      f"({elems} elements, {elems * 28 / 1e9:.2f} GB per step), {steps} steps, "
-                      f"oracle per-tensor C loop on {threads} threads"}
+def cpu_baseline(steps: int = 3):
+    """The oracle on the host cores: one bounded sample of each of the four
+    timed workloads, a few steps each; the line's value is the large-uniform
+    sample's (its workload)."""
+    import oracle
+
+    threads = oracle.timed_lib().oracle_omp_threads()
+    per = {}
+    for name, make_spec, bpe in CPU_SAMPLES:
+        spec = make_spec()
+        times, elems = cpu_oracle_steps(spec, steps)
+        sec = statistics.median(times)
+        per[name] = {"gbs": elems * bpe / sec / 1e9, "gparams_per_s": elems / sec / 1e9,
+                     "s_per_step": sec, "elements": elems, "bytes_per_element": bpe,
+                     "sample": f"{len(spec.sizes)} tensors of the {name} recipe"}
+    head = per["large_uniform"]
+    return {"value": head["gbs"], "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "cpu_model": cpu_model(), "gparams_per_s": head["gparams_per_s"],
+            "build": "oracle C source, -O3 -fopenmp -ffp-contract=off -fno-math-errno "
+                     "(vectorised; each tensor split across the OpenMP threads)",
+            "sample": (f"8 of the 201 tensors x 20,971,520 fp32 elements "
+                       f"({head['elements']} elements, {head['elements'] * 28 / 1e9:.2f} GB per "
+                       f"step), median of {steps} steps; per-workload samples in 'workloads'"),
+            "workloads": per}
 
 
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    threads = os.cpu_count() or 1
-    per_step, elems = cpu_oracle_run(args.ref_tensors, args.warmup + args.steps, threads,
-                                     320 * 65536)
+    import oracle
+
+    threads = oracle.timed_lib().oracle_omp_threads()
+    spec = workloads.large_uniform(n_tensors=args.ref_tensors)
+    per_step, elems = cpu_oracle_steps(spec, args.warmup + args.steps)
     timed = per_step[args.warmup:]
     sec = statistics.mean(timed)
     gbs = elems * 28 / sec / 1e9
     sample = (f"each step: {args.ref_tensors} of the 201 tensors x 20,971,520 fp32 elements "
-              f"({elems} elements); oracle per-tensor C loop on {threads} threads")
+              f"({elems} elements); the oracle's timed OpenMP build on {threads} threads "
+              f"({cpu_model()})")
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -317,7 +377,7 @@ def run_reference(args):
                                    "(bounded sample per step)", "sample_elements": elems},
             "gparams_per_s": elems / sec / 1e9,
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": sample},
+                             "cpu_model": cpu_model(), "sample": sample},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -361,7 +421,7 @@ def run_gpu(args):
         spec.seed += 1000 * rank
     shard = workloads.materialize(spec, device)
     groups = shard.param_groups()
-    kw = dict(remainders=spec.remainders, grad_scale=spec.grad_scale)
+    kw = dict(remainders=spec.remainders, grad_scale=spec.grad_scale, recip_bc=args.recip_bc)
 
     def make(capturable, **more):
         if spec.scaled_state:  # each plan steps its own copy of the scales
@@ -519,6 +579,7 @@ def run_gpu(args):
                    "block": info["block"], "items": info["n_items"],
                    "l2": "inputs larger than L2 (no flush needed)",
                    "start_step": args.start_step,
+                   "recip_bc": args.recip_bc,
                    "parallelism": f"weak: one shard per GPU x {world}"},
         "fraction_of_peak": head["gbs"] / world / peaks["hbm_gbs"],
         "gparams_per_s": head["gparams_per_s"],
@@ -571,6 +632,9 @@ def main(argv=None):
                     help="steps already taken by every group when timing starts (0: a fresh "
                          "shard; from 165 / 338 / 17,321 the bias corrections of beta 0.9 / "
                          "0.95 / 0.999 are 1 in float)")
+    ap.add_argument("--recip-bc", action="store_true",
+                    help="FADAM_RECIP_BC: the 16-bit state forms multiply by reciprocal bias "
+                         "corrections (within the tolerance, not bit-identical)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tensors", type=int, default=4)
     args = ap.parse_args(argv)

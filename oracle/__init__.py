@@ -32,6 +32,7 @@ from typing import List, Optional
 import numpy as np
 
 from .build import build as _build
+from .build import build_timed as _build_timed
 
 DT_NONE, DT_F32, DT_BF16, DT_F16 = 0, 1, 2, 3
 MODE_L2, MODE_ADAMW = 0, 1
@@ -42,6 +43,10 @@ _i64 = ctypes.c_int64
 _i32 = ctypes.c_int32
 _f32 = ctypes.c_float
 _vp = ctypes.c_void_p
+L_F32_ARGS = [_i64, ctypes.c_int, ctypes.c_int, _i32, _f32, _f32, _f32, _f32, _f32, _f32, _vp,
+              _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_int]
+L_REM_ARGS = [_i64, ctypes.c_int, ctypes.c_int, _i32, _f32, _f32, _f32, _f32, _f32, _f32, _vp,
+              _vp, _vp, _vp, _vp, ctypes.c_int, _vp]
 
 
 def lib():
@@ -52,13 +57,9 @@ def lib():
         L.oracle_bias_correction.restype = _f32
         L.oracle_bias_correction.argtypes = [_f32, _i32]
         L.oracle_adam_f32.restype = None
-        L.oracle_adam_f32.argtypes = [_i64, ctypes.c_int, ctypes.c_int, _i32, _f32, _f32,
-                                      _f32, _f32, _f32, _f32, _vp, _vp, _vp, _vp,
-                                      ctypes.c_int, _vp, ctypes.c_int]
+        L.oracle_adam_f32.argtypes = L_F32_ARGS
         L.oracle_adam_rem.restype = None
-        L.oracle_adam_rem.argtypes = [_i64, ctypes.c_int, ctypes.c_int, _i32, _f32, _f32,
-                                      _f32, _f32, _f32, _f32, _vp, _vp, _vp, _vp, _vp,
-                                      ctypes.c_int, _vp]
+        L.oracle_adam_rem.argtypes = L_REM_ARGS
         L.oracle_adam_state.restype = None
         L.oracle_adam_state.argtypes = [_i64, ctypes.c_int, ctypes.c_int, _i32, _f32, _f32,
                                         _f32, _f32, _f32, _f32, _vp, _vp, _vp, ctypes.c_int,
@@ -84,6 +85,26 @@ def lib():
             getattr(L, name).argtypes = [_i64, _vp, _vp]
         _LIB = L
     return _LIB
+
+
+_TIMED = None
+
+
+def timed_lib():
+    """The timed-only build (-O3 -fopenmp, the same source plus an OpenMP
+    driver that splits each tensor across the threads): for the benchmark's
+    CPU baseline only; the tests use ``lib()``."""
+    global _TIMED
+    if _TIMED is None:
+        L = ctypes.CDLL(_build_timed())
+        L.oracle_omp_threads.restype = ctypes.c_int
+        L.oracle_omp_threads.argtypes = []
+        L.oracle_omp_adam_f32.restype = None
+        L.oracle_omp_adam_f32.argtypes = L_F32_ARGS
+        L.oracle_omp_adam_rem.restype = None
+        L.oracle_omp_adam_rem.argtypes = L_REM_ARGS
+        _TIMED = L
+    return _TIMED
 
 
 def _ptr(a: Optional[np.ndarray]):
@@ -165,8 +186,10 @@ class Group:
 
 
 def adam_f32(group: Group, step: int, p, m, v, g, g_dtype=DT_F32, p_out=None,
-             out_dtype=DT_NONE) -> None:
-    """Update one tensor with an fp32 master in place (p, m, v, p_out)."""
+             out_dtype=DT_NONE, timed: bool = False) -> None:
+    """Update one tensor with an fp32 master in place (p, m, v, p_out).
+    ``timed``: run it through the timed OpenMP build instead (the CPU
+    baseline)."""
     n = p.size
     _check(p, np.float32, n, "p")
     _check(m, np.float32, n, "m")
@@ -174,10 +197,10 @@ def adam_f32(group: Group, step: int, p, m, v, g, g_dtype=DT_F32, p_out=None,
     _check(g, _G_NP[g_dtype], n, "g")
     if out_dtype != DT_NONE:
         _check(p_out, np.float32 if out_dtype == DT_F32 else np.uint16, n, "p_out")
-    lib().oracle_adam_f32(n, group.mode, group.bias_correction, step, group.beta1,
-                          group.beta2, group.eps, group.weight_decay, group.lr,
-                          group.grad_scale, _ptr(p), _ptr(m), _ptr(v), _ptr(g), g_dtype,
-                          _ptr(p_out) if out_dtype != DT_NONE else None, out_dtype)
+    fn = timed_lib().oracle_omp_adam_f32 if timed else lib().oracle_adam_f32
+    fn(n, group.mode, group.bias_correction, step, group.beta1, group.beta2, group.eps,
+       group.weight_decay, group.lr, group.grad_scale, _ptr(p), _ptr(m), _ptr(v), _ptr(g),
+       g_dtype, _ptr(p_out) if out_dtype != DT_NONE else None, out_dtype)
 
 
 _S_NP = {DT_F32: np.float32, DT_BF16: np.uint16, DT_F16: np.uint16}
@@ -215,8 +238,10 @@ def adam_moments(group: Group, step: int, p, m, v, moment_dtype, g, g_dtype=DT_F
                               g_dtype, _ptr(p_out) if out_dtype != DT_NONE else None, out_dtype)
 
 
-def adam_rem(group: Group, step: int, p_hi, rem, m, v, g, g_dtype, p_out) -> None:
-    """Update one tensor whose master is bf16 high half + int16 remainder."""
+def adam_rem(group: Group, step: int, p_hi, rem, m, v, g, g_dtype, p_out,
+             timed: bool = False) -> None:
+    """Update one tensor whose master is bf16 high half + int16 remainder
+    (``timed``: through the timed OpenMP build)."""
     n = p_hi.size
     _check(p_hi, np.uint16, n, "p_hi")
     _check(rem, np.int16, n, "rem")
@@ -224,10 +249,10 @@ def adam_rem(group: Group, step: int, p_hi, rem, m, v, g, g_dtype, p_out) -> Non
     _check(v, np.float32, n, "v")
     _check(g, _G_NP[g_dtype], n, "g")
     _check(p_out, np.uint16, n, "p_out")
-    lib().oracle_adam_rem(n, group.mode, group.bias_correction, step, group.beta1,
-                          group.beta2, group.eps, group.weight_decay, group.lr,
-                          group.grad_scale, _ptr(p_hi), _ptr(rem), _ptr(m), _ptr(v), _ptr(g),
-                          g_dtype, _ptr(p_out))
+    fn = timed_lib().oracle_omp_adam_rem if timed else lib().oracle_adam_rem
+    fn(n, group.mode, group.bias_correction, step, group.beta1, group.beta2, group.eps,
+       group.weight_decay, group.lr, group.grad_scale, _ptr(p_hi), _ptr(rem), _ptr(m), _ptr(v),
+       _ptr(g), g_dtype, _ptr(p_out))
 
 
 def adam_f64(group: Group, step: int, p, m, v, g) -> None:

@@ -1002,3 +1002,38 @@ def test_shard_step_dispatches_scaled_tensors():
                        np.zeros(300, np.uint16), DT_BF16)
     assert t.p.tobytes() == ref[0].tobytes() and t.scales.tobytes() == ref[3].tobytes()
     assert sh.steps == [1] and np.any(t.m)
+
+
+@pytest.mark.parametrize("g_dtype,out_dtype", [(DT_F32, oracle.DT_NONE), (DT_BF16, DT_BF16),
+                                               (DT_F16, DT_F32)])
+@pytest.mark.parametrize("mode", [MODE_L2, MODE_ADAMW])
+def test_timed_build_computes_what_the_parity_build_does(g_dtype, out_dtype, mode):
+    """The benchmark's CPU baseline times a second build of the same oracle
+    source (-O3 -fopenmp, vectorised, each tensor split across threads).  It
+    must be the same function: bit-identical to the parity build, three
+    steps of an odd-sized tensor, fp32 master and remainder forms."""
+    rng = np.random.default_rng(31)
+    n = 100_003
+    grp = Group(mode=mode, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, lr=1.6e-3,
+                grad_scale=0.5)
+    g32 = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    g = {DT_F32: g32, DT_BF16: oracle.f32_to_bf16(g32), DT_F16: oracle.f32_to_f16(g32)}[g_dtype]
+    p0 = rng.standard_normal(n).astype(np.float32)
+    odt = {oracle.DT_NONE: None, DT_F32: np.float32, DT_BF16: np.uint16}[out_dtype]
+    a = [p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)]
+    b = [p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)]
+    oa = np.zeros(n, odt) if odt else None
+    ob = np.zeros(n, odt) if odt else None
+    hi, rem = oracle.rem_split(p0.view(np.uint32))
+    ra = [hi.copy(), rem.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)]
+    rb = [hi.copy(), rem.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)]
+    for k in (1, 2, 3):
+        oracle.adam_f32(grp, k, *a, g, g_dtype, oa, out_dtype)
+        oracle.adam_f32(grp, k, *b, g, g_dtype, ob, out_dtype, timed=True)
+        oracle.adam_rem(grp, k, ra[0], ra[1], ra[2], ra[3], g, g_dtype, ra[0])
+        oracle.adam_rem(grp, k, rb[0], rb[1], rb[2], rb[3], g, g_dtype, rb[0], timed=True)
+    for x, y in zip(a + ra, b + rb):
+        assert x.tobytes() == y.tobytes()
+    if odt:
+        assert oa.tobytes() == ob.tobytes()
+    assert oracle.timed_lib().oracle_omp_threads() >= 1
