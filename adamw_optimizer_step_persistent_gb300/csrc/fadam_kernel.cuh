@@ -72,14 +72,23 @@ __device__ __forceinline__ unsigned long long global_ns() {
 
 // ---- scalar state -----------------------------------------------------------
 
-struct SGroup {
+// One group's scalars in shared memory, read by every tile.  Twelve words,
+// 16-byte aligned, so that a tile loads the ten it needs with three 128-bit
+// loads (a 52-byte record, with no provable vector alignment, took ten
+// 32-bit loads per warp and tile: 1-2 % of the 16-bit forms' instructions).
+// What the tiles do not read lives in the arrays after it.
+struct alignas(16) SGroup {
   float beta1, omb1, beta2, omb2;  // omb = 1 - beta, rounded once
-  float bc1, bc2, eps, wd, lr, gs;
-  float rbc1, rbc2;                // 1/bc1, 1/bc2 (IEEE reciprocals), for FADAM_RECIP_BC
+  float bc1, bc2, eps, wd;
+  float lr, gs;
   int32_t step_old;                // counter as read (capturable) or the host step
-  int32_t step;                    // the step this launch applies
   uint32_t bits;
 };
+static_assert(sizeof(SGroup) == 48, "SGroup is three 16-byte words");
+// Per group: 1/bc1 and 1/bc2 (IEEE reciprocals, read by the FADAM_RECIP_BC
+// tiles in place of bc1 and bc2) and the step this launch applies.
+__shared__ float2 s_group_rbc[FADAM_MAX_GROUPS];
+__shared__ int32_t s_group_step[FADAM_MAX_GROUPS];
 
 // Step counters advance modulo 2^32, as an int32 tensor's += does (no
 // signed overflow in the kernel's own arithmetic).
@@ -1169,8 +1178,9 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
         const unsigned char* st = smem + size_t(b) * Layout<ST, GT, REM>::stage;
         const SGroup& G = sgrp[it.group];
         constexpr bool kRecip = (UNIT & kRecipBc) != 0;
-        const Scal s{G.beta1, G.omb1, G.beta2, G.omb2, kRecip ? G.rbc1 : G.bc1,
-                     kRecip ? G.rbc2 : G.bc2, G.eps, G.wd, G.lr, G.gs};
+        const Scal s{G.beta1, G.omb1, G.beta2, G.omb2,
+                     kRecip ? s_group_rbc[it.group].x : G.bc1,
+                     kRecip ? s_group_rbc[it.group].y : G.bc2, G.eps, G.wd, G.lr, G.gs};
         if constexpr (PASS == Pass::kScan) {
           bad |= scan_tile<Layout<ST, GT, REM>::scan_per_thread, GT>(st, tag.len, s.gs);
         } else if constexpr (PASS == Pass::kNorm) {
@@ -1599,7 +1609,7 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
       s.step_old = G.step;
       step = G.step;
     }
-    s.step = step;
+    s_group_step[tid] = step;
     // launches that only read g (norm, reduction) skip the corrections; the
     // others take them from the memo the previous launch left, or compute
     // the double pow (a few microseconds on this GPU's FP64 pipe)
@@ -1610,8 +1620,7 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
       s.bc1 = bias_correction(G.beta1, step);
       s.bc2 = bias_correction(G.beta2, step);
     }
-    s.rbc1 = __frcp_rn(s.bc1);
-    s.rbc2 = __frcp_rn(s.bc2);
+    s_group_rbc[tid] = make_float2(__frcp_rn(s.bc1), __frcp_rn(s.bc2));
     sgrp[tid] = s;
   }
   __syncthreads();
@@ -1621,7 +1630,7 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
       tid >= 32 && tid < 32 + kp.n_groups) {
     const SGroup& g = sgrp[tid - 32];
     if (g.bits & kGroupBiasCorr)
-      memo_store(kp.memo, tid - 32, g.beta1, g.beta2, step_add(g.step, 1));
+      memo_store(kp.memo, tid - 32, g.beta1, g.beta2, step_add(s_group_step[tid - 32], 1));
   }
 
   const int item_begin = __ldg(kp.cta_begin + blockIdx.x);
