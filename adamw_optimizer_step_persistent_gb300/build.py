@@ -21,7 +21,8 @@ LIB = os.path.join(OUT_DIR, "libfadam.so")
 SOURCES = ["fadam_plan.cu"] + [f"fadam_kernels_s{s}_g{g}.cu"
                                for s in ("f32", "bf16", "f16", "f32mbf16", "f32mf16")
                                for g in ("f32", "bf16", "f16")] + [
-    f"fadam_kernels_scaled_s{s}_g{g}.cu" for s in ("bf16", "f16") for g in ("f32", "bf16", "f16")]
+    f"fadam_kernels_{kind}s{s}_g{g}.cu" for kind in ("scaled_", "recip_", "recip_scaled_")
+    for s in ("bf16", "f16") for g in ("f32", "bf16", "f16")]
 HEADERS = ["fadam_internal.h", "fadam_kernel.cuh"]
 
 NVCC_FLAGS = [

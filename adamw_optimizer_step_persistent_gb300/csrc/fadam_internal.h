@@ -127,7 +127,6 @@ constexpr uint32_t kCheckFinite = FADAM_CHECK_FINITE;
 constexpr uint32_t kPreadvanced = FADAM_STEP_PREADVANCED;
 constexpr uint32_t kTestBarrierTimeout = FADAM_TEST_BARRIER_TIMEOUT;
 constexpr uint32_t kScaledStates = FADAM_SCALED_STATES;
-constexpr uint32_t kRecipBcFlag = FADAM_RECIP_BC;
 // Launch-only flags (never plan flags): compute the squared gradient norm
 // instead of the update; write the gradient shard from the exchange sources
 // (alone, or before the update with a grid barrier between).
@@ -217,5 +216,19 @@ FADAM_DECLARE_SCALED(f16, f32)
 FADAM_DECLARE_SCALED(f16, bf16)
 FADAM_DECLARE_SCALED(f16, f16)
 #undef FADAM_DECLARE_SCALED
+
+// Instances of the 16-bit state forms with reciprocal bias corrections
+// (FADAM_RECIP_BC), plain and scaled, one function per (state, g) pair, in
+// fadam_kernels_recip_s<state>_g<g>.cu and fadam_kernels_recip_scaled_*.cu.
+#define FADAM_DECLARE_RECIP(S, G)                       \
+  KernelEntry recip_kernel_s##S##_g##G(int out_dtype);  \
+  KernelEntry recip_scaled_kernel_s##S##_g##G(int out_dtype);
+FADAM_DECLARE_RECIP(bf16, f32)
+FADAM_DECLARE_RECIP(bf16, bf16)
+FADAM_DECLARE_RECIP(bf16, f16)
+FADAM_DECLARE_RECIP(f16, f32)
+FADAM_DECLARE_RECIP(f16, bf16)
+FADAM_DECLARE_RECIP(f16, f16)
+#undef FADAM_DECLARE_RECIP
 
 }  // namespace fadam

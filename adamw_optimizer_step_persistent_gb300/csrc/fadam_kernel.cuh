@@ -1565,8 +1565,11 @@ __device__ __forceinline__ bool grid_barrier(KScratch* sc, unsigned extra) {
 // ---- the kernel ---------------------------------------------------------------
 
 // SCALED: the scaled 16-bit state instances (their own kernels, so the
-// plain ones carry none of the two-pass code).
-template <int ST, int GT, int OT, bool REM, bool SCALED = false>
+// plain ones carry none of the two-pass code).  RECIP (16-bit state only):
+// multiply by reciprocal bias corrections (FADAM_RECIP_BC) instead of
+// dividing as the functor does; those are instances of their own, so that
+// the default ones keep the register allocation of their own loops.
+template <int ST, int GT, int OT, bool REM, bool SCALED = false, bool RECIP = false>
 __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams kp) {
   __shared__ SGroup sgrp[FADAM_MAX_GROUPS];
   __shared__ int s_noop;
@@ -1665,7 +1668,10 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
     // generic-proxy stores of g before that
     asm volatile("fence.proxy.async.global;" ::: "memory");
     if (reduce_first) {
-      if (__syncthreads_or(bad) && tid == 0) atomicExch(kp.noop, 1);
+      // warp-level OR of the screen: one write of the flag per warp that saw
+      // a value that is not finite (the grid barrier orders it before the
+      // flag is read)
+      if (__any_sync(0xffffffffu, bad) && (tid & 31) == 0) atomicExch(kp.noop, 1);
       barrier_ok = grid_barrier(kp.scratch, (kp.flags & kTestBarrierTimeout) ? 1u : 0u);
       if (tid == 0) {
         s_noop = kp.noop ? (ld_acquire_s32(kp.noop) == 1) : 0;
@@ -1682,7 +1688,10 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
       run_pass<ST, GT, OT, REM, Pass::kScan, NS>(kp, sgrp, item_begin, item_end, &kp.scratch->next_scan,
                                          &kp.scratch->next_tail_scan, n_items, s_tiles, s_full,
                                          s_tags, s_prod, s_red, stage, bad, timed_out);
-    if (__syncthreads_or(bad) && tid == 0) atomicExch(kp.noop, 1);
+    // warp-level OR of the screen, one write of the flag per warp that saw
+    // a value that is not finite; the grid barrier orders the writes before
+    // every CTA reads the flag
+    if (__any_sync(0xffffffffu, bad) && (tid & 31) == 0) atomicExch(kp.noop, 1);
     barrier_ok = grid_barrier(kp.scratch, (kp.flags & kTestBarrierTimeout) ? 1u : 0u);
     if (tid == 0) s_noop = (ld_acquire_s32(kp.noop) == 1);
     __syncthreads();
@@ -1700,9 +1709,6 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
         if (sgrp[k].bc1 != 1.0f) unit &= ~kUnitBc1;
         if (sgrp[k].bc2 != 1.0f) unit &= ~kUnitBc2;
       }
-      // reciprocals: one instance for any correction that is not 1 (the
-      // product by a reciprocal of 1 is exact)
-      if ((kp.flags & kRecipBcFlag) && unit != (kUnitBc1 | kUnitBc2)) unit = kRecipBc;
     }
     bool unused = false;
     // the update passes for a compile-time unit mask U
@@ -1730,9 +1736,13 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
                                                         stage, unused, timed_out);
       }
     };
-    if constexpr (unit_bc_instances<ST, REM>()) {
+    if constexpr (unit_bc_instances<ST, REM>() && RECIP) {
+      // reciprocals: one loop for any correction that is not 1 (the product
+      // by a reciprocal of 1 is exact), one for both corrections at 1
       if (unit == (kUnitBc1 | kUnitBc2)) passes(std::integral_constant<int, kUnitBc1 | kUnitBc2>{});
-      else if (unit == kRecipBc) passes(std::integral_constant<int, kRecipBc>{});
+      else passes(std::integral_constant<int, kRecipBc>{});
+    } else if constexpr (unit_bc_instances<ST, REM>()) {
+      if (unit == (kUnitBc1 | kUnitBc2)) passes(std::integral_constant<int, kUnitBc1 | kUnitBc2>{});
       else if (unit == kUnitBc1) passes(std::integral_constant<int, kUnitBc1>{});
       else passes(std::integral_constant<int, 0>{});
     } else {
@@ -1845,6 +1855,24 @@ KernelEntry scaled_kernel_for(int out_dtype) {
       return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_BF16, false, true>), smem};
     case FADAM_DT_F16:
       return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_F16, false, true>), smem};
+    default: return {nullptr, 0};
+  }
+}
+
+// The instances with reciprocal bias corrections (FADAM_RECIP_BC) of a
+// 16-bit state dtype (ST bf16 or fp16), plain or scaled: every out dtype.
+template <int ST, int GT, bool SCALED>
+KernelEntry recip_kernel_for(int out_dtype) {
+  const size_t smem = smem_bytes<ST, GT, false, SCALED>();
+  switch (out_dtype) {
+    case FADAM_DT_NONE:
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_NONE, false, SCALED, true>), smem};
+    case FADAM_DT_F32:
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_F32, false, SCALED, true>), smem};
+    case FADAM_DT_BF16:
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_BF16, false, SCALED, true>), smem};
+    case FADAM_DT_F16:
+      return {reinterpret_cast<const void*>(&fadam_update_kernel<ST, GT, FADAM_DT_F16, false, SCALED, true>), smem};
     default: return {nullptr, 0};
   }
 }

@@ -1,0 +1,13 @@
+// Plain kernel instances with reciprocal bias corrections
+// (FADAM_RECIP_BC) for state dtype bf16 and gradient dtype bf16: every
+// param-out dtype.  Apart from the default instances so that the build
+// stays parallel.
+#include "fadam_kernel.cuh"
+
+namespace fadam {
+
+KernelEntry recip_kernel_sbf16_gbf16(int out_dtype) {
+  return recip_kernel_for<FADAM_DT_BF16, FADAM_DT_BF16, false>(out_dtype);
+}
+
+}  // namespace fadam

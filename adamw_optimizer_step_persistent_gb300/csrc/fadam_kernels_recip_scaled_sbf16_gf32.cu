@@ -1,0 +1,13 @@
+// Scaled-state kernel instances with reciprocal bias corrections
+// (FADAM_RECIP_BC) for state dtype bf16 and gradient dtype f32: every
+// param-out dtype.  Apart from the default instances so that the build
+// stays parallel.
+#include "fadam_kernel.cuh"
+
+namespace fadam {
+
+KernelEntry recip_scaled_kernel_sbf16_gf32(int out_dtype) {
+  return recip_kernel_for<FADAM_DT_BF16, FADAM_DT_F32, true>(out_dtype);
+}
+
+}  // namespace fadam

@@ -345,10 +345,28 @@ Item to_item(const fadam_tensor& t, const PackItem& pi, const Dtypes& d) {
   return it;
 }
 
-KernelEntry select_kernel(const Dtypes& d, bool scaled) {
+KernelEntry select_kernel(const Dtypes& d, bool scaled, bool recip) {
   // the remainder form keeps fp32 m and v: its kernels sit with fp32 state
   const int32_t st = d.rem ? FADAM_DT_F32 : d.p;
   const int key = st * 4 + d.g;
+  // the reciprocal bias corrections have instances for the 16-bit state
+  // forms only
+  if (recip && !d.rem && d.mv == FADAM_DT_NONE && st != FADAM_DT_F32) {
+    switch (key) {
+#define FADAM_RECIP_PICK(S, SD, G, GD)                                                  \
+      case SD * 4 + GD:                                                                  \
+        return scaled ? recip_scaled_kernel_s##S##_g##G(d.out)                           \
+                      : recip_kernel_s##S##_g##G(d.out);
+      FADAM_RECIP_PICK(bf16, FADAM_DT_BF16, f32, FADAM_DT_F32)
+      FADAM_RECIP_PICK(bf16, FADAM_DT_BF16, bf16, FADAM_DT_BF16)
+      FADAM_RECIP_PICK(bf16, FADAM_DT_BF16, f16, FADAM_DT_F16)
+      FADAM_RECIP_PICK(f16, FADAM_DT_F16, f32, FADAM_DT_F32)
+      FADAM_RECIP_PICK(f16, FADAM_DT_F16, bf16, FADAM_DT_BF16)
+      FADAM_RECIP_PICK(f16, FADAM_DT_F16, f16, FADAM_DT_F16)
+#undef FADAM_RECIP_PICK
+      default: return {nullptr, 0};
+    }
+  }
   if (d.mv == FADAM_DT_BF16) {
     switch (d.g) {
       case FADAM_DT_F32: return kernel_sf32mbf16_gf32(d.out, false);
@@ -493,7 +511,8 @@ fadam_status prepare(const fadam_tensor* tensors, int64_t n_tensors, const fadam
 
   hp.d = d;
   hp.flags = flags;
-  const KernelEntry ke = select_kernel(d, (flags & FADAM_SCALED_STATES) != 0);
+  const KernelEntry ke =
+      select_kernel(d, (flags & FADAM_SCALED_STATES) != 0, (flags & FADAM_RECIP_BC) != 0);
   hp.kernel = ke.fn;
   hp.smem = ke.smem;
   if (!hp.kernel) return fail(FADAM_EDTYPE, "no kernel for this dtype combination");

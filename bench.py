@@ -423,9 +423,15 @@ def run_gpu(args):
     groups = shard.param_groups()
     kw = dict(remainders=spec.remainders, grad_scale=spec.grad_scale, recip_bc=args.recip_bc)
 
+    # scaled state: every plan of the run steps the same p, m, v, so they
+    # share one scales tensor too (a plan with a copy of its own would start
+    # from scales that no longer match the state the previous plan left)
+    scales = (shard.state_scales[shard.plan_order()].contiguous() if spec.scaled_state
+              else None)
+
     def make(capturable, **more):
-        if spec.scaled_state:  # each plan steps its own copy of the scales
-            more["state_scales"] = shard.state_scales[shard.plan_order()].contiguous()
+        if spec.scaled_state:
+            more["state_scales"] = scales
         opt = FusedAdamShard(groups, capturable=capturable, **kw, **more)
         if args.start_step:  # a shard resumed this many steps into training
             opt.set_group_steps([args.start_step] * len(groups))

@@ -101,7 +101,7 @@ def test_recip_16bit_state_each_step_within_one_ulp(state_dtype, g_dtype, out_dt
         assert opt.group_steps() == oracle.group_steps(osh) == [start + 10] * 2
         if start == 20000:
             # both corrections are 1 in float: the instance without any
-            # division runs, bit for bit
+            # division by them runs, bit for bit
             assert rep.exact_fraction == 1.0
         elif start == 0 and out_dtype == torch.float32:
             # the products by reciprocals do run: the fp32 param-out (p' as
@@ -140,5 +140,6 @@ def test_recip_scaled_state_each_step(name, capturable):
             want = t.scales.astype(np.float64)
             assert np.all(np.abs(got[j] - want) <= 2e-6 * np.abs(want)), (k, j, got[j], want)
     assert opt.group_steps() == [10]
-    print(f"{name} capturable {capturable}: {rep.n} values, {rep.exact_fraction:.6f} bit-identical")
+    print(f"{name} capturable {capturable}: {rep.n} values, "
+          f"{rep.exact_fraction:.6f} bit-identical")
     opt.close()
