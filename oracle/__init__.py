@@ -446,16 +446,34 @@ def reduce_sources(sources, g_dtype: int, average: bool) -> np.ndarray:
     return _narrow(acc, g_dtype)
 
 
+def accumulate_grad(g_shard, synced, g_dtype: int) -> np.ndarray:
+    """Gradient accumulation across reduce-scatters (_finish_bucket_grad_sync:
+    after the first, each synced shard is added to the gradient shard with
+    ``grads_shard.add_(sync_grads_shard)``).  Reading: both are in the grad
+    dtype; the sum is taken in float (one IEEE addition of the widened
+    values) and rounded once to the grad dtype."""
+    with np.errstate(over="ignore", invalid="ignore"):
+        acc = _widen(g_shard, g_dtype) + _widen(synced, g_dtype)
+    return _narrow(acc, g_dtype)
+
+
+def reduce_into(g_shard, sources, g_dtype: int, average: bool, accumulate: bool) -> np.ndarray:
+    """This rank's gradient shard after one reduce-scatter: the reduced
+    contributions, or (accumulating) the old shard plus them."""
+    synced = reduce_sources(sources, g_dtype, average)
+    return accumulate_grad(g_shard, synced, g_dtype) if accumulate else synced
+
+
 def exchange_step(shard: Shard, sources, *, average: bool, capturable: bool,
                   noop: bool = False, check_finite: bool = False,
-                  step_preadvanced: bool = False) -> bool:
+                  step_preadvanced: bool = False, accumulate: bool = False) -> bool:
     """Reduce-scatter stand-in, then the shard step.  ``sources[i]`` lists the
-    R contributions for tensor i; each tensor's ``g`` is overwritten with the
-    reduced shard (the exchange happens even if the step is then skipped).
-    Returns the noop flag after the step; the all-gather side is
-    ``gather_param_out``."""
+    R contributions for tensor i; each tensor's ``g`` becomes the reduced
+    shard, or with ``accumulate`` its old value plus the reduced shard (the
+    exchange happens even if the step is then skipped).  Returns the noop
+    flag after the step; the all-gather side is ``gather_param_out``."""
     for t, src in zip(shard.tensors, sources):
-        t.g[...] = reduce_sources(src, t.g_dtype, average)
+        t.g[...] = reduce_into(t.g, src, t.g_dtype, average, accumulate)
     return shard_step(shard, capturable=capturable, noop=noop, check_finite=check_finite,
                       step_preadvanced=step_preadvanced)
 

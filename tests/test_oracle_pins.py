@@ -1037,3 +1037,80 @@ def test_timed_build_computes_what_the_parity_build_does(g_dtype, out_dtype, mod
     if odt:
         assert oa.tobytes() == ob.tobytes()
     assert oracle.timed_lib().oracle_omp_threads() >= 1
+
+
+# ---- gradient accumulation across reduce-scatters ---------------------------------
+
+def _golden_accumulate_rows():
+    rows = []
+    path = os.path.join(os.path.dirname(__file__), "golden", "accumulate_grad.txt")
+    with open(path) as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, vals = line.split("|")
+            dt, expected = head.split()
+            old, synced = (float(x) for x in vals.split())
+            rows.append((dt, float(expected), old, synced))
+    return rows
+
+
+@pytest.mark.parametrize("row", _golden_accumulate_rows(), ids=lambda r: f"{r[0]}-{r[1]}")
+def test_accumulate_grad_golden_rows(row):
+    dts, expected, old, synced = row
+    dt = _DT[dts]
+    a, b = _to_dtype([old], dt), _to_dtype([synced], dt)
+    for x, v in ((a, old), (b, synced)):  # the fixture's inputs are exact in their dtype
+        w = _from_dtype(x, dt)[0]
+        assert w == np.float32(v) or (np.isnan(v) and np.isnan(w))
+    got = _from_dtype(oracle.accumulate_grad(a, b, dt), dt)[0]
+    if np.isnan(expected):
+        assert np.isnan(got)
+    else:
+        assert got == np.float32(expected) and np.signbit(got) == np.signbit(np.float32(expected))
+
+
+@pytest.mark.parametrize("dt", [DT_BF16, DT_F16])
+def test_accumulate_grad_is_torch_add_in_the_grad_dtype(dt):
+    """The page's grads_shard.add_(sync_grads_shard) on 16-bit tensors, run
+    by torch on the CPU, against the oracle's accumulation."""
+    rng = np.random.default_rng(41)
+    tdt = torch.bfloat16 if dt == DT_BF16 else torch.float16
+    a = (rng.standard_normal(20000) * 1e-2).astype(np.float32)
+    b = (rng.standard_normal(20000) * 1e-2).astype(np.float32)
+    ta, tb = torch.from_numpy(a).to(tdt), torch.from_numpy(b).to(tdt)
+    want = ta.clone().add_(tb).view(torch.int16).numpy().view(np.uint16)
+    ab = ta.view(torch.int16).numpy().view(np.uint16).copy()
+    bb = tb.view(torch.int16).numpy().view(np.uint16).copy()
+    assert np.array_equal(oracle.accumulate_grad(ab, bb, dt), want)
+
+
+def test_reduce_into_composes_the_reduction_and_the_accumulation():
+    rng = np.random.default_rng(42)
+    old = oracle.f32_to_bf16(rng.standard_normal(3000).astype(np.float32))
+    srcs = [oracle.f32_to_bf16(rng.standard_normal(3000).astype(np.float32)) for _ in range(3)]
+    synced = oracle.reduce_sources(srcs, DT_BF16, True)
+    assert np.array_equal(oracle.reduce_into(old, srcs, DT_BF16, True, False), synced)
+    acc = oracle.reduce_into(old, srcs, DT_BF16, True, True)
+    assert np.array_equal(acc, oracle.f32_to_bf16(oracle.bf16_to_f32(old) + oracle.bf16_to_f32(synced)))
+    # accumulating a shard of +0 leaves every nonzero value as it was
+    x = rng.standard_normal(3000).astype(np.float32)
+    zero = np.zeros(3000, np.float32)
+    assert oracle.accumulate_grad(x, zero, DT_F32).tobytes() == x.tobytes()
+    # two micro-batches accumulated through the shard step equal the sum fed
+    # to the plain step
+    sh_a, sh_b = _exchange_shard(43), _exchange_shard(43)
+    src1 = [[oracle.f32_to_bf16(rng.standard_normal(t.g.size).astype(np.float32)) for _ in range(2)]
+            for t in sh_a.tensors]
+    src2 = [[oracle.f32_to_bf16(rng.standard_normal(t.g.size).astype(np.float32)) for _ in range(2)]
+            for t in sh_a.tensors]
+    for t, s1 in zip(sh_a.tensors, src1):
+        t.g[...] = oracle.reduce_sources(s1, DT_BF16, True)
+    oracle.exchange_step(sh_a, src2, average=True, capturable=False, accumulate=True)
+    for t, s1, s2 in zip(sh_b.tensors, src1, src2):
+        t.g[...] = oracle.accumulate_grad(oracle.reduce_sources(s1, DT_BF16, True),
+                                          oracle.reduce_sources(s2, DT_BF16, True), DT_BF16)
+    oracle.shard_step(sh_b, capturable=False)
+    for ta, tb in zip(sh_a.tensors, sh_b.tensors):
+        assert ta.g.tobytes() == tb.g.tobytes() and ta.p.tobytes() == tb.p.tobytes()
