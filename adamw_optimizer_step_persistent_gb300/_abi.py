@@ -26,6 +26,7 @@ SCALED_STATES = 16
 MOMENTS_BF16, MOMENTS_F16 = 32, 64
 RECIP_BC = 128  # 16-bit state forms: multiply by 1/bc1, 1/bc2 instead of dividing
 TEST_BARRIER_TIMEOUT = 0x80000000  # diagnostic: the screen's grid barrier runs out
+EXCHANGE_AVERAGE, EXCHANGE_ACCUMULATE = 1, 2  # reduce_flags of fadam_plan_set_exchange
 MAX_GROUPS = 32
 MAX_SOURCES = 16
 MAX_DESTS = 16

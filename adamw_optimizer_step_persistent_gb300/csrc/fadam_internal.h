@@ -143,6 +143,11 @@ constexpr uint32_t kHostGrads = 1u << 27;
 constexpr uint32_t kNoTails = 1u << 26;
 constexpr uint32_t kAllBulk = 1u << 25;
 
+// The exchange's reduction: divide the sum by R (ReduceOp.AVG); add the
+// reduced value to the shard's old g (gradient accumulation).
+constexpr int32_t kExchangeAverage = FADAM_EXCHANGE_AVERAGE;
+constexpr int32_t kExchangeAccumulate = FADAM_EXCHANGE_ACCUMULATE;
+
 // Everything one launch needs, passed as a __grid_constant__ parameter.
 struct alignas(16) KParams {
   const Item* items;
@@ -160,7 +165,7 @@ struct alignas(16) KParams {
   // the data-parallel exchange: byte offsets from the shard's g to each
   // source's, and from p_out to each extra destination
   int32_t n_sources;
-  int32_t average;
+  int32_t average;  // kExchangeAverage | kExchangeAccumulate
   int32_t n_dests;
   float avg_mul;  // 1/R when averaging over a power-of-two R (exact), else 0
   int64_t src_delta[FADAM_MAX_SOURCES];

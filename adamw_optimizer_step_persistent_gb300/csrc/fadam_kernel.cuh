@@ -569,13 +569,20 @@ __device__ __forceinline__ int bulk_tiles(const Item& it) {
 }
 
 
-// Vectors of a reduce tile: as many as the R source slices fit in one stage
-// (at most as many as a screen tile), a multiple of one warp.
+// Vectors of a reduce tile: as many as the R source slices (and, when
+// accumulating, the shard's own g as one slice more) fit in one stage (at
+// most as many as a screen tile), a multiple of one warp.
 template <int ST, int GT, bool REM>
 __host__ __device__ constexpr int reduce_vectors(int n_sources) {
   using L = Layout<ST, GT, REM>;
   const int v = static_cast<int>(L::stage / (static_cast<unsigned>(n_sources) * L::kG));
   return (v < L::scan_vectors ? v : L::scan_vectors) & ~31;
+}
+
+// Slices a reduce tile copies: the sources, and the shard's own g when
+// accumulating.
+__device__ __forceinline__ int reduce_slices(const KParams& kp) {
+  return kp.n_sources + ((kp.average & kExchangeAccumulate) ? 1 : 0);
 }
 
 // Vectors in one tile of a pass (Layout::update_vectors or ::scan_vectors).
@@ -596,12 +603,15 @@ __device__ __forceinline__ void issue_tile(const KParams& kp, const Item& it, in
   uint64_t* bar = full + b;
   const size_t v = static_cast<size_t>(v0);
   if constexpr (PASS == Pass::kReduce) {
-    // source r's slice at r * (vectors of a reduce tile) in the stage
-    const size_t stride = size_t(reduce_vectors<ST, GT, REM>(kp.n_sources)) * L::kG;
-    mbar_expect_tx(bar, static_cast<unsigned>(kp.n_sources) * len * L::kG);
+    // source r's slice at r * (vectors of a reduce tile) in the stage; when
+    // accumulating, the shard's old g after them
+    const int ns = reduce_slices(kp);
+    const size_t stride = size_t(reduce_vectors<ST, GT, REM>(ns)) * L::kG;
+    mbar_expect_tx(bar, static_cast<unsigned>(ns) * len * L::kG);
     const char* g = static_cast<const char*>(it.g) + v * L::kG;
     for (int r = 0; r < kp.n_sources; ++r)
       bulk_load(st + size_t(r) * stride, g + kp.src_delta[r], len * L::kG, bar);
+    if (ns > kp.n_sources) bulk_load(st + size_t(kp.n_sources) * stride, g, len * L::kG, bar);
   } else if constexpr (!update_like(PASS)) {
     mbar_expect_tx(bar, len * L::kG);
     bulk_load(st, static_cast<const char*>(it.g) + v * L::kG, len * L::kG, bar);
@@ -717,7 +727,7 @@ __device__ __forceinline__ void produce_next(Producer& pr, const KParams& kp, un
     pr.vend = min((ch.tile0 + ch.ntiles) * kTile, bulk_vectors(pr.it));
   }
   int tv;
-  if constexpr (PASS == Pass::kReduce) tv = reduce_vectors<ST, GT, REM>(kp.n_sources);
+  if constexpr (PASS == Pass::kReduce) tv = reduce_vectors<ST, GT, REM>(reduce_slices(kp));
   else tv = tile_vectors<ST, GT, REM, PASS>();
   const int len = min(tv, pr.vend - pr.v);
   TileTag& tg = tags[pr.slot % NS];
@@ -787,9 +797,11 @@ __host__ __device__ constexpr bool unit_bc_instances() {
 // "apex/contrib/optimizers/distributed_fused_adam.py", _start_bucket_grad_sync:
 // this rank's shard of g from the R ranks' contributions, widened to float
 // and added in rank order (one IEEE addition each), divided by R for
-// ReduceOp.AVG (one IEEE division), rounded once to the grad dtype.  With
-// the screen on, the reduced g*grad_scale is tested as the update will use
-// it.
+// ReduceOp.AVG (one IEEE division), rounded once to the grad dtype.
+// Accumulating (_finish_bucket_grad_sync's grads_shard.add_ after the first
+// reduce-scatter of a step), that rounded value is added to the shard's old
+// g, both widened, and the sum rounded once more.  With the screen on, the
+// new g*grad_scale is tested as the update will use it.
 
 template <int GT>
 __device__ __forceinline__ float stored_value(float x) {
@@ -798,18 +810,18 @@ __device__ __forceinline__ float stored_value(float x) {
   else return f16_to_f32(narrow<GT>(x));
 }
 
-// One tile: source r's vectors at r * stride in the stage.  R > 0: the
-// number of sources, fixed at compile time (the source loop unrolled, the
-// slice offsets constants); R == 0: kp.n_sources.  Either way the sources
-// are added in rank order.
-template <int ST, int GT, bool REM, int R>
+// One tile: source r's vectors at r * stride in the stage (ACC: the
+// shard's old g after them).  R > 0: the number of sources, fixed at
+// compile time (the source loop unrolled, the slice offsets constants);
+// R == 0: kp.n_sources.  Either way the sources are added in rank order.
+template <int ST, int GT, bool REM, int R, bool ACC>
 __device__ __forceinline__ bool reduce_tile(const KParams& kp, const Item& it,
                                             const unsigned char* st, int v0, int len, float gs,
                                             bool screen) {
   using L = Layout<ST, GT, REM>;
   using G4 = typename Raw4<GT>::T;
   const int nr = R > 0 ? R : kp.n_sources;
-  const size_t stride = size_t(reduce_vectors<ST, GT, REM>(nr)) * L::kG;
+  const size_t stride = size_t(reduce_vectors<ST, GT, REM>(nr + (ACC ? 1 : 0))) * L::kG;
   const float rn = static_cast<float>(nr);
   bool bad = false;
   for (int t = threadIdx.x; t < len; t += kBlock) {
@@ -823,7 +835,7 @@ __device__ __forceinline__ bool reduce_tile(const KParams& kp, const Item& it,
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
     }
-    if (kp.average) {
+    if (kp.average & kExchangeAverage) {
       // dividing by a power of two is multiplying by its exact reciprocal
       // (the same correctly rounded result)
       if (kp.avg_mul != 0.0f) {
@@ -833,6 +845,12 @@ __device__ __forceinline__ bool reduce_tile(const KParams& kp, const Item& it,
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[e] = __fdiv_rn(acc[e], rn);
       }
+    }
+    if constexpr (ACC) {  // the shard's old g, staged after the sources
+      float old[4];
+      widen4<GT>(reinterpret_cast<const G4*>(st + size_t(nr) * stride)[t], old);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[e] = __fadd_rn(old[e], stored_value<GT>(acc[e]));
     }
     const G4 w = pack_out4<GT>(acc);
     __stcs(reinterpret_cast<G4*>(const_cast<void*>(it.g)) + v0 + t, w);
@@ -852,11 +870,19 @@ template <int ST, int GT, bool REM>
 __device__ __forceinline__ bool reduce_tile_any(const KParams& kp, const Item& it,
                                                 const unsigned char* st, int v0, int len, float gs,
                                                 bool screen) {
+  if (kp.average & kExchangeAccumulate) {
+    switch (kp.n_sources) {
+      case 2: return reduce_tile<ST, GT, REM, 2, true>(kp, it, st, v0, len, gs, screen);
+      case 4: return reduce_tile<ST, GT, REM, 4, true>(kp, it, st, v0, len, gs, screen);
+      case 8: return reduce_tile<ST, GT, REM, 8, true>(kp, it, st, v0, len, gs, screen);
+      default: return reduce_tile<ST, GT, REM, 0, true>(kp, it, st, v0, len, gs, screen);
+    }
+  }
   switch (kp.n_sources) {
-    case 2: return reduce_tile<ST, GT, REM, 2>(kp, it, st, v0, len, gs, screen);
-    case 4: return reduce_tile<ST, GT, REM, 4>(kp, it, st, v0, len, gs, screen);
-    case 8: return reduce_tile<ST, GT, REM, 8>(kp, it, st, v0, len, gs, screen);
-    default: return reduce_tile<ST, GT, REM, 0>(kp, it, st, v0, len, gs, screen);
+    case 2: return reduce_tile<ST, GT, REM, 2, false>(kp, it, st, v0, len, gs, screen);
+    case 4: return reduce_tile<ST, GT, REM, 4, false>(kp, it, st, v0, len, gs, screen);
+    case 8: return reduce_tile<ST, GT, REM, 8, false>(kp, it, st, v0, len, gs, screen);
+    default: return reduce_tile<ST, GT, REM, 0, false>(kp, it, st, v0, len, gs, screen);
   }
 }
 
@@ -867,9 +893,10 @@ __device__ __forceinline__ bool reduce_elem(const KParams& kp, const Item& it, i
   const char* g = static_cast<const char*>(it.g);
   float acc = load1<GT>(g + kp.src_delta[0], i);
   for (int r = 1; r < kp.n_sources; ++r) acc = __fadd_rn(acc, load1<GT>(g + kp.src_delta[r], i));
-  if (kp.average)
+  if (kp.average & kExchangeAverage)
     acc = kp.avg_mul != 0.0f ? __fmul_rn(acc, kp.avg_mul)
                              : __fdiv_rn(acc, static_cast<float>(kp.n_sources));
+  if (kp.average & kExchangeAccumulate) acc = __fadd_rn(load1<GT>(g, i), stored_value<GT>(acc));
   store_out1<GT>(const_cast<void*>(it.g), i, acc);
   return screen && !isfinite(__fmul_rn(stored_value<GT>(acc), gs));
 }

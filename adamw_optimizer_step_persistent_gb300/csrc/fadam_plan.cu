@@ -657,7 +657,9 @@ void fill_exchange(KParams& kp, const fadam_plan* plan) {
   kp.average = plan->average;
   kp.n_dests = plan->n_dests;
   const int r_n = plan->n_sources;
-  kp.avg_mul = (plan->average && r_n > 0 && (r_n & (r_n - 1)) == 0) ? 1.0f / static_cast<float>(r_n) : 0.0f;
+  kp.avg_mul = ((plan->average & FADAM_EXCHANGE_AVERAGE) && r_n > 0 && (r_n & (r_n - 1)) == 0)
+                   ? 1.0f / static_cast<float>(r_n)
+                   : 0.0f;
   for (int r = 0; r < plan->n_sources; ++r) kp.src_delta[r] = plan->src_delta[r];
   for (int d = 0; d < plan->n_dests; ++d) kp.dst_delta[d] = plan->dst_delta[d];
 }
@@ -829,7 +831,7 @@ fadam_status fadam_plan_set_state_scales(fadam_plan* plan, float* scales_dev) {
 
 fadam_status fadam_plan_set_exchange(fadam_plan* plan, const void* g_shard,
                                      const void* const* sources, int32_t n_sources,
-                                     int32_t average, const void* out_shard,
+                                     int32_t reduce_flags, const void* out_shard,
                                      void* const* dests, int32_t n_dests) {
   t_last_error.clear();
   if (!plan) return fail(FADAM_EINVAL, "plan is NULL");
@@ -837,7 +839,9 @@ fadam_status fadam_plan_set_exchange(fadam_plan* plan, const void* g_shard,
     return fail(FADAM_EINVAL, "n_sources %d outside 0..%d", n_sources, FADAM_MAX_SOURCES);
   if (n_dests < 0 || n_dests > FADAM_MAX_DESTS)
     return fail(FADAM_EINVAL, "n_dests %d outside 0..%d", n_dests, FADAM_MAX_DESTS);
-  if (average != 0 && average != 1) return fail(FADAM_EINVAL, "average must be 0 or 1");
+  if (reduce_flags & ~(FADAM_EXCHANGE_AVERAGE | FADAM_EXCHANGE_ACCUMULATE))
+    return fail(FADAM_EINVAL, "reduce_flags 0x%x: only FADAM_EXCHANGE_AVERAGE and "
+                              "FADAM_EXCHANGE_ACCUMULATE are defined", reduce_flags);
   int64_t src[FADAM_MAX_SOURCES] = {}, dst[FADAM_MAX_DESTS] = {};
   if (n_sources > 0) {
     if (!g_shard || !sources) return fail(FADAM_EINVAL, "g_shard and sources are needed");
@@ -860,7 +864,7 @@ fadam_status fadam_plan_set_exchange(fadam_plan* plan, const void* g_shard,
     }
   }
   plan->n_sources = n_sources;
-  plan->average = average;
+  plan->average = reduce_flags;
   plan->n_dests = n_dests;
   for (int r = 0; r < FADAM_MAX_SOURCES; ++r) plan->src_delta[r] = src[r];
   for (int d = 0; d < FADAM_MAX_DESTS; ++d) plan->dst_delta[d] = dst[d];

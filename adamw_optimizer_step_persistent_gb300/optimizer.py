@@ -290,12 +290,15 @@ class FusedAdamShard:
 
     def set_exchange(self, g_shard: torch.Tensor, sources: Sequence[torch.Tensor], *,
                      average: bool = True, out_shard: Optional[torch.Tensor] = None,
-                     dests: Sequence[torch.Tensor] = ()) -> None:
+                     dests: Sequence[torch.Tensor] = (), accumulate: bool = False) -> None:
         """Register the reduce-scatter sources and the param all-gather
         destinations (fadam_plan_set_exchange).  Every tensor's gradient is
         a view of ``g_shard`` and each source is laid out like it (same
         dtype, at least as many elements); every param-out copy is a view of
-        ``out_shard`` and each destination is laid out like it."""
+        ``out_shard`` and each destination is laid out like it.
+        ``accumulate``: each reduction adds to the shard's gradient instead
+        of replacing it (gradient accumulation: the second and later
+        reduce-scatters of a step; see ``set_accumulate``)."""
         for s in sources:
             if s.dtype != g_shard.dtype or s.numel() < g_shard.numel() or s.device != g_shard.device:
                 raise ValueError("each source needs g_shard's dtype, device and at least its size")
@@ -306,11 +309,21 @@ class FusedAdamShard:
                 raise ValueError("each destination needs out_shard's dtype, device and at least its size")
         src = (ctypes.c_void_p * max(1, len(sources)))(*[s.data_ptr() for s in sources])
         dst = (ctypes.c_void_p * max(1, len(dests)))(*[d.data_ptr() for d in dests])
+        flags = ((_abi.EXCHANGE_AVERAGE if average else 0)
+                 | (_abi.EXCHANGE_ACCUMULATE if accumulate else 0))
         _abi.check(_abi.lib().fadam_plan_set_exchange(
-            self._plan, g_shard.data_ptr() if sources else None, src, len(sources), int(average),
+            self._plan, g_shard.data_ptr() if sources else None, src, len(sources), flags,
             out_shard.data_ptr() if dests else None, dst, len(dests)), "fadam_plan_set_exchange")
         # the plan holds raw pointers: keep the buffers alive with it
-        self._exchange = (g_shard, list(sources), out_shard, list(dests))
+        self._exchange = (g_shard, list(sources), out_shard, list(dests), bool(average))
+
+    def set_accumulate(self, accumulate: bool) -> None:
+        """Switch gradient accumulation of the registered exchange on (the
+        second and later reduce-scatters of a step) or off (a step's first).
+        Host only: may be called between captured launches."""
+        g_shard, sources, out_shard, dests, average = self._exchange
+        self.set_exchange(g_shard, sources, average=average, out_shard=out_shard, dests=dests,
+                          accumulate=accumulate)
 
     def grad_reduce(self) -> None:
         """The reduce-scatter stand-in alone: every tensor's gradient from the

@@ -470,6 +470,16 @@ def run_gpu(args):
         r = summarise(per, reduce_bytes, elems, world, device)
         r["bytes_per_step"] = reduce_bytes
         res["reduce"] = r
+    if spec.exchange_ranks and "accumulate" in variants:
+        # a later micro-batch's reduce-scatter: the R sources read, the
+        # shard's g read, added to and written back
+        cap.set_accumulate(True)
+        per, _ = time_launches(cap.grad_reduce, args.steps, args.warmup, world)
+        cap.set_accumulate(False)
+        acc_bytes = elems * (spec.exchange_ranks + 2) * gsz
+        r = summarise(per, acc_bytes, elems, world, device)
+        r["bytes_per_step"] = acc_bytes
+        res["reduce_accumulate"] = r
     if spec.exchange_ranks and "clip_pipeline" in variants:
         # the data-parallel step with gradient clipping, captured as one
         # graph: the grad scale reset (the loss scaler's value), the
@@ -633,7 +643,8 @@ def main(argv=None):
                     help="layers of the capturable_l2 / exchange_shard / scaled_state_shard "
                          "layer list (8)")
     ap.add_argument("--variants", default="capturable,regular,graph,check_finite,norm,e2e",
-                    help="also exchange,reduce,clip_pipeline on the exchange_shard workload")
+                    help="also exchange,reduce,accumulate,clip_pipeline on the exchange_shard "
+                         "workload")
     ap.add_argument("--start-step", type=int, default=0,
                     help="steps already taken by every group when timing starts (0: a fresh "
                          "shard; from 165 / 338 / 17,321 the bias corrections of beta 0.9 / "

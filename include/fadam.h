@@ -130,6 +130,9 @@ typedef int32_t fadam_status;
 
 /* Maximum numbers of gradient sources and extra param-out destinations of
  * the data-parallel exchange (fadam_plan_set_exchange). */
+/* reduce_flags of fadam_plan_set_exchange. */
+#define FADAM_EXCHANGE_AVERAGE 1    /* divide the sum by R (ReduceOp.AVG) */
+#define FADAM_EXCHANGE_ACCUMULATE 2 /* add the reduced value to the shard's g */
 #define FADAM_MAX_SOURCES 16
 #define FADAM_MAX_DESTS 16
 
@@ -326,8 +329,18 @@ fadam_status fadam_clip_apply(fadam_plan* plan, const double* sumsq_dev, float m
  *                                 (host array of device pointers, copied);
  *                                 every sources[r] - g_shard a multiple of 16
  *                                 bytes.  The sources are only read.
- *   average                       1: the sum divided by R (ReduceOp.AVG);
- *                                 0: the sum.
+ *   reduce_flags                  FADAM_EXCHANGE_AVERAGE: the sum divided by
+ *                                 R (ReduceOp.AVG), else the sum;
+ *                                 FADAM_EXCHANGE_ACCUMULATE: gradient
+ *                                 accumulation across reduce-scatters
+ *                                 (_finish_bucket_grad_sync: the second and
+ *                                 later reduce-scatters of a step add their
+ *                                 shard to the gradient shard,
+ *                                 grads_shard.add_): the shard's g becomes
+ *                                 its old value plus the reduced value
+ *                                 rounded to the grad dtype, both widened,
+ *                                 one IEEE addition, rounded once to the grad
+ *                                 dtype; without it g is overwritten.
  *   out_shard, dests[n_dests]     0 <= n_dests <= FADAM_MAX_DESTS, each
  *                                 dests[d] - out_shard a multiple of 16
  *                                 bytes; needs a param-out dtype.
@@ -338,12 +351,15 @@ fadam_status fadam_clip_apply(fadam_plan* plan, const double* sumsq_dev, float m
  * while the plan is used; the pointers are copied on the host (no device
  * memory is touched, so this may be called between captured launches;
  * captured launches keep the pointers they were captured with).
- * n_sources = 0 and n_dests = 0 remove the exchange.  Errors: FADAM_EINVAL
+ * n_sources = 0 and n_dests = 0 remove the exchange.  Set the flags again
+ * (with the same buffers) to switch accumulation on after a step's first
+ * reduce-scatter and off for the next step's first.  Errors: FADAM_EINVAL
  * (counts out of range, NULL pointers, destinations without a param-out
- * dtype), FADAM_EALIGN (a difference not a multiple of 16 bytes). */
+ * dtype, unknown reduce_flags bits), FADAM_EALIGN (a difference not a
+ * multiple of 16 bytes). */
 fadam_status fadam_plan_set_exchange(fadam_plan* plan, const void* g_shard,
                                      const void* const* sources, int32_t n_sources,
-                                     int32_t average, const void* out_shard,
+                                     int32_t reduce_flags, const void* out_shard,
                                      void* const* dests, int32_t n_dests);
 
 /* The reduce-scatter stand-in alone: one launch that writes this rank's

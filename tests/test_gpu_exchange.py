@@ -212,3 +212,124 @@ def test_unrolled_and_generic_reduce_tiles(ranks, average):
     _check_dests(shard)
     assert rep.exact_fraction == 1.0
     opt.close()
+
+
+def _rotated(shard, k):
+    """The ranks' buffers in rank order rotated by k: each micro-batch's
+    contributions arrive in another order, so their sums differ."""
+    src = list(shard.sources)
+    k %= len(src)
+    return src[k:] + src[:k]
+
+
+def _set_micro_batch(opt, shard, spec, k, accumulate):
+    opt.set_exchange(shard.buckets["g"], _rotated(shard, k), average=spec.exchange_average,
+                     out_shard=shard.buckets["p_out"], dests=list(shard.dests),
+                     accumulate=accumulate)
+
+
+def _oracle_micro_batch(shard, k):
+    """Per tensor: the rotated ranks' contributions to its fragment."""
+    out = []
+    R = shard.sources.shape[0]
+    for i in shard.plan_order():
+        o, n = shard.offsets[i], shard.spec.sizes[i]
+        out.append([helpers.to_np(shard.sources[(r + k) % R, o:o + n]) for r in range(R)])
+    return out
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_gradient_accumulation_over_three_micro_batches(name):
+    """Two steps of three micro-batches each: the first reduce-scatter of a
+    step writes the shard, the second adds to it (fadam_grad_reduce with
+    FADAM_EXCHANGE_ACCUMULATE), the third adds to it fused with the step
+    (fadam_step_reduce).  The shard's g bit for bit after every micro-batch,
+    the state and every destination against the oracle after each step."""
+    spec, shard, opt = _make(name)
+    osh = helpers.oracle_shard(shard)
+    rep = helpers.Report()
+    k = 0
+    for step in range(2):
+        for mb in range(3):
+            _set_micro_batch(opt, shard, spec, k, accumulate=mb > 0)
+            src = _oracle_micro_batch(shard, k)
+            if mb < 2:
+                opt.grad_reduce()
+                for t, s in zip(osh.tensors, src):
+                    t.g[...] = oracle.reduce_into(t.g, s, t.g_dtype, spec.exchange_average, mb > 0)
+            else:
+                opt.step_reduce()
+                oracle.exchange_step(osh, src, average=spec.exchange_average, capturable=True,
+                                     accumulate=True)
+            torch.cuda.synchronize()
+            _check_reduced(shard, osh)
+            k += 1
+        helpers.compare(shard, osh, report=rep)
+        _check_dests(shard)
+    assert opt.group_steps() == [2]
+    assert rep.exact_fraction == 1.0, rep.exact_fraction
+    opt.close()
+
+
+def test_screen_sees_an_inf_that_arrives_by_accumulation():
+    """The first micro-batch is finite; the second carries an inf in one
+    rank's contribution: the accumulated shard holds the inf, the fused step
+    is skipped, and the state is left as it was."""
+    spec, shard, opt = _make("exchange_shard", check_finite=True)
+    _set_micro_batch(opt, shard, spec, 0, accumulate=False)
+    opt.grad_reduce()
+    i = shard.plan_order()[2]
+    shard.sources[2, shard.offsets[i] + 5] = float("inf")
+    _set_micro_batch(opt, shard, spec, 1, accumulate=True)
+    snap = helpers.snapshot(shard)
+    opt.step_reduce()
+    torch.cuda.synchronize()
+    assert opt.noop.item() == 1 and opt.group_steps() == [0]
+    assert helpers.state_equal(shard, snap)
+    assert torch.isinf(shard.grads[i][5].float())
+    opt.close()
+
+
+def test_accumulating_step_captured_in_one_graph():
+    """A whole step of two micro-batches (the flags switched on the host
+    between the captured launches, which keep the flags they were captured
+    with) replayed three times equals three eager steps."""
+    spec, a, oa = _make("exchange_shard")
+    _, b, ob = _make("exchange_shard")
+
+    def step(opt, shard):
+        _set_micro_batch(opt, shard, spec, 0, accumulate=False)
+        opt.grad_reduce()
+        _set_micro_batch(opt, shard, spec, 1, accumulate=True)
+        opt.step_reduce()
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step(ob, b)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(ob, b)
+    for _ in range(4):
+        step(oa, a)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    for x, y in zip(helpers.snapshot(a), helpers.snapshot(b)):
+        assert torch.equal(x.view(torch.int8), y.view(torch.int8))
+    assert torch.equal(a.buckets["g"], b.buckets["g"]) and torch.equal(a.dests, b.dests)
+    assert oa.group_steps() == ob.group_steps() == [4]
+    oa.close()
+    ob.close()
+
+
+def test_unknown_reduce_flag_bits_are_refused():
+    spec, shard, opt = _make("exchange_shard")
+    from adamw_optimizer_step_persistent_gb300 import _abi
+    import ctypes
+    src = (ctypes.c_void_p * 1)(shard.sources[0].data_ptr())
+    st = _abi.lib().fadam_plan_set_exchange(opt._plan, shard.buckets["g"].data_ptr(), src, 1, 4,
+                                            None, None, 0)
+    assert st == _abi.EINVAL and b"reduce_flags" in _abi.lib().fadam_last_error()
+    opt.close()

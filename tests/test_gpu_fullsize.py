@@ -210,17 +210,28 @@ def test_large_uniform_norm_full_size():
 
 
 def test_exchange_shard_full_size():
-    """Eight ranks' bf16 gradients averaged into the 1.2e9-element shard and
-    stepped in one launch, param-out to the seven other ranks' places, for
-    two steps; every element against the oracle (the reduced gradient bit
-    for bit), destinations byte-equal over the whole shard."""
+    """Eight ranks' bf16 gradients averaged into the 1.2e9-element shard,
+    param-out to the seven other ranks' places, two steps of two
+    micro-batches each: the first reduce-scatter writes the shard, the
+    second (the ranks' buffers in another order) adds to it fused with the
+    step.  Every element against the oracle (the reduced gradient bit for
+    bit), destinations byte-equal over the whole shard."""
     spec = workloads.exchange_versions(full=True)["exchange_shard"]
     shard = workloads.materialize(spec, DEV)
     opt = FusedAdamShard(shard.param_groups(), capturable=True)
-    opt.set_exchange(shard.buckets["g"], list(shard.sources), average=True,
-                     out_shard=shard.buckets["p_out"], dests=list(shard.dests))
+    R = spec.exchange_ranks
+    srcs = list(shard.sources)
+
+    def micro_batch(k, accumulate):
+        opt.set_exchange(shard.buckets["g"], srcs[k:] + srcs[:k], average=True,
+                         out_shard=shard.buckets["p_out"], dests=list(shard.dests),
+                         accumulate=accumulate)
+
     init = _inputs(shard)
     for _ in range(2):
+        micro_batch(0, False)
+        opt.grad_reduce()
+        micro_batch(1, True)
         opt.step_reduce()
     torch.cuda.synchronize()
     assert opt.group_steps() == [2]
@@ -230,12 +241,15 @@ def test_exchange_shard_full_size():
         i, sl = u
         a = shard.offsets[i] + sl.start
         b = shard.offsets[i] + sl.stop
-        src = [[helpers.to_np(shard.sources[r][a:b]) for r in range(spec.exchange_ranks)]]
+        raw = [helpers.to_np(shard.sources[r][a:b]) for r in range(R)]
+        src0, src1 = [raw], [raw[1:] + raw[:1]]
         osh = helpers.oracle_shard(init, idx=[i], elems={i: sl})
+        t = osh.tensors[0]
         for _ in range(2):
-            oracle.exchange_step(osh, src, average=True, capturable=True)
+            t.g[...] = oracle.reduce_into(t.g, src0[0], t.g_dtype, True, False)
+            oracle.exchange_step(osh, src1, average=True, capturable=True, accumulate=True)
         got = helpers.to_np(shard.grads[i][sl])
-        assert got.tobytes() == osh.tensors[0].g.tobytes(), f"tensor {i}: reduced gradient differs"
+        assert got.tobytes() == t.g.tobytes(), f"tensor {i}: reduced gradient differs"
         return helpers.compare(shard, osh, idx=[i], elems={i: sl})
 
     rep = _pool_map(unit, _units(spec, shard.plan_order()))
