@@ -13,6 +13,8 @@ array instead of allocated scratch.  These tests call it through the C ABI:
 * twice in a row with host scalars (regular), each result against the
   oracle directly;
 * with the noop flag set (nothing written, no counter moved), then clear;
+* with a bf16 state and reciprocal bias corrections, against the plan path
+  with the same flag;
 * on two shards with different betas at the same step indices, in turn,
   and with a counter moved by the caller: the bias-correction memo in the
   shared array must never serve an entry made for other betas or another
@@ -209,6 +211,32 @@ def test_noalloc_memo_serves_only_matching_betas_and_steps():
     assert scal["A"].steps() == [6, 6, 6] and scal["B"].steps() == [3]
     for p in plans.values():
         p.close()
+
+
+def test_noalloc_16bit_state_with_reciprocal_corrections():
+    """A bf16 state with FADAM_RECIP_BC (its own kernel instances): two
+    capturable calls bit-identical to the plan path with the same flag."""
+    spec = workloads.large_uniform(n_tensors=3, numel=40_003, state_dtype=torch.bfloat16,
+                                   g_dtype=torch.bfloat16)
+    spec.sizes = [40_003, 7, 131_072 + 5]
+    ref = workloads.materialize(spec, DEV)
+    out = workloads.materialize(spec, DEV)
+    plan_opt = FusedAdamShard(ref.param_groups(), capturable=True, recip_bc=True)
+    ds = _DeviceScalars(spec)
+    noop = torch.zeros(1, dtype=torch.int32, device=DEV)
+    arr, n, groups = _c_args(out, ds.lr, ds.gs, ds.step)
+    L = _abi.lib()
+    for call in (1, 2):
+        plan_opt.step()
+        st = L.fadam_step_noalloc(arr, n, groups, len(spec.groups), _abi.DT_BF16, _abi.DT_BF16,
+                                  _abi.DT_NONE, _abi.CAPTURABLE | _abi.RECIP_BC, noop.data_ptr(),
+                                  torch.cuda.current_stream().cuda_stream)
+        assert st == _abi.OK, L.fadam_last_error()
+        torch.cuda.synchronize()
+        for x, y in zip(helpers.snapshot(out), helpers.snapshot(ref)):
+            assert torch.equal(x.view(torch.int16), y.view(torch.int16)), f"call {call}"
+        assert ds.steps() == plan_opt.group_steps() == [call]
+    plan_opt.close()
 
 
 def test_noalloc_refuses_a_capturing_stream():
