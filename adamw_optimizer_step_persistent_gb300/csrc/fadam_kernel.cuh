@@ -1814,6 +1814,9 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
       }
     }
   }
+  // every thread of the last CTA has read this launch's timeout flag before
+  // thread 0 clears it below
+  __syncthreads();
   if (tid == 0) {
     if (s_last) {
       __threadfence();

@@ -58,7 +58,7 @@ class FusedAdamShard:
     bf16 tensors that receive the new high halves; they may be ``params``).
     ``recip_bc`` (16-bit state only) multiplies the moments by reciprocal
     bias corrections instead of dividing them (FADAM_RECIP_BC): faster for
-    those issue-bound forms, within the tolerance rather than bit-identical.
+    those issue-bound forms, within a derived bound rather than bit-identical.
     """
 
     def __init__(self, param_groups: Sequence[Dict], *, capturable: bool = False,

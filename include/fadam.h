@@ -108,9 +108,12 @@ typedef int32_t fadam_status;
  * functor's m/bc1 and v/bc2).  Each bias-corrected moment then carries two
  * roundings instead of one, so results are no longer bit-identical to the
  * division: the update u = m_hat / (sqrt(v_hat) + eps) moves by at most a
- * few float ulps, and a stored 16-bit value by at most one unit in its last
- * place per step.  Once a correction rounds to 1 in float the multiply is
- * exact.  Other state forms (fp32 master, remainders, 16-bit moments) are
+ * few float ulps; m and v do not move (they precede any division); p' =
+ * p - lr*u moves by a few ulps of lr*u <= |p| + |p'|, so a stored p (or
+ * param-out) lands within one unit in its last place plus
+ * 2e-6 * max(|p|, |p'|) of the divided result per step (more than one ulp
+ * only where the step nearly cancels p).  Once a correction rounds to 1 in
+ * float the multiply is exact.  Other state forms (fp32 master, remainders, 16-bit moments) are
  * bound by memory, keep the division and ignore the flag, as do the at most
  * 7 tail elements of each tensor and tensors not 16-byte aligned. */
 #define FADAM_RECIP_BC 128u

@@ -128,6 +128,90 @@ def load_oracle_state(shard: workloads.Shard, osh: oracle.Shard, idx=None,
             scales[k].copy_(torch.from_numpy(np.ascontiguousarray(t.scales, dtype=np.float32)))
 
 
+def widen16(bits: np.ndarray, dtype) -> np.ndarray:
+    """16-bit bit patterns of `dtype` as float64 values."""
+    if dtype == torch.bfloat16:
+        return oracle.bf16_to_f32(bits).astype(np.float64)
+    return oracle.f16_to_f32(bits).astype(np.float64)
+
+
+def ulp16(values: np.ndarray, dtype) -> np.ndarray:
+    """Spacing of the 16-bit dtype at each (finite) value."""
+    mant, emin = (7, -133) if dtype == torch.bfloat16 else (10, -24)
+    a = np.abs(values)
+    _, e = np.frexp(np.where(a > 0, a, 1.0))  # a = m * 2^e, m in [0.5, 1)
+    return np.ldexp(1.0, np.maximum(e - 1 - mant, emin))
+
+
+def check_recip_p16(got_bits, want_bits, dtype, x_before, what, report,
+                    got_scale=1.0, want_scale=1.0):
+    """A 16-bit p (or param-out) of a step with reciprocal bias corrections:
+    the value (times its scale, for a scaled state) within one ulp of its
+    dtype plus 2e-6 * max(|p before the step|, |p'|) + 1e-9.  The
+    reciprocal's extra rounding is relative to lr*u <= |p| + |p'|, which can
+    exceed |p'| many times where the step nearly cancels p, so a small p'
+    may land several of its own ulps away; m and v need no such allowance."""
+    g = widen16(got_bits, dtype) * np.float64(got_scale)
+    w = widen16(want_bits, dtype) * np.float64(want_scale)
+    x = np.abs(np.asarray(x_before, np.float64))
+    both_nan = np.isnan(g) & np.isnan(w)
+    same = (g == w) | both_nan
+    with np.errstate(invalid="ignore", over="ignore"):
+        lim = (ulp16(widen16(want_bits, dtype), dtype) * abs(np.float64(want_scale))
+               + 2e-6 * np.maximum(x, np.abs(w)) + 1e-9)
+        bad = ~same & ~(np.abs(g - w) <= lim)
+    if bad.any():
+        k = int(np.argmax(bad))
+        raise AssertionError(f"{what}: {int(bad.sum())} of {g.size} outside the bound; first at "
+                             f"{k}: got {g[k]!r} want {w[k]!r} p before {x[k]!r}")
+    report.n += g.size
+    report.exact += int(np.sum(np.asarray(got_bits) == np.asarray(want_bits)))
+
+
+def compare_recip(shard: workloads.Shard, osh: oracle.Shard, x_before, report: Report,
+                  idx=None, elems=None, got_scales: np.ndarray = None) -> Report:
+    """GPU vs oracle after one step of a 16-bit state with reciprocal bias
+    corrections (FADAM_RECIP_BC): m and v within one ulp of their dtype, p
+    and a 16-bit param-out under check_recip_p16, an fp32 param-out within
+    2e-6 * max(|p before|, |p'|) + 1e-9.  x_before[k]: tensor k's fp32
+    master before the step (for a scaled state, unscaled); got_scales[k]:
+    the GPU's new scales of tensor k (scaled state)."""
+    spec = shard.spec
+    sdt = spec.state_dtype
+    idx = shard.plan_order() if idx is None else idx
+    for k, (t, i, x0) in enumerate(zip(osh.tensors, idx, x_before)):
+        sel = _selector(elems, i, shard.params[i].device)
+        report.ulp16(to_np(sel(shard.exp_avgs[i])), t.m, f"tensor {i} m", sdt)
+        report.ulp16(to_np(sel(shard.exp_avg_sqs[i])), t.v, f"tensor {i} v", sdt)
+        gs = 1.0 if got_scales is None else got_scales[k][0]
+        ws = 1.0 if t.scales is None else t.scales[0]
+        check_recip_p16(to_np(sel(shard.params[i])), t.p, sdt, x0, f"tensor {i} p", report, gs, ws)
+        if spec.out_dtype == torch.float32:
+            got = to_np(sel(shard.params_out[i])).astype(np.float64)
+            want = t.p_out.astype(np.float64)
+            lim = 2e-6 * np.maximum(np.abs(want), np.abs(np.asarray(x0, np.float64))) + 1e-9
+            bad = ~(np.abs(got - want) <= lim) & ~(np.isnan(got) & np.isnan(want)) & (got != want)
+            assert not bad.any(), f"tensor {i} p_out: {int(bad.sum())} outside; first at {int(np.argmax(bad))}"
+            report.n += got.size
+            report.exact += int(np.sum(got == want))
+        elif spec.out_dtype is not None:
+            check_recip_p16(to_np(sel(shard.params_out[i])), t.p_out, spec.out_dtype, x0,
+                            f"tensor {i} p_out", report)
+    return report
+
+
+def unscaled_p(osh: oracle.Shard, state_dtype) -> List[np.ndarray]:
+    """Each oracle tensor's master p as float64 values (times its p scale for
+    a scaled state): the state a step starts from."""
+    out = []
+    for t in osh.tensors:
+        x = widen16(t.p, state_dtype)
+        if t.scales is not None:
+            x = x * np.float64(t.scales[0])
+        out.append(x)
+    return out
+
+
 def _ordered16(bits: np.ndarray) -> np.ndarray:
     b = bits.astype(np.int32)
     return np.where(b & 0x8000, -(b & 0x7FFF), b)

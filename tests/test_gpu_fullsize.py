@@ -95,12 +95,12 @@ def _values_per_element(spec):
     return 3 + (1 if spec.out_dtype is not None else 0)
 
 
-def _full_run(spec, steps, inf_step=None, capturable=None):
+def _full_run(spec, steps, inf_step=None, capturable=None, recip_bc=False):
     if capturable is not None:
         spec.capturable = capturable
     shard = workloads.materialize(spec, DEV)
     opt = FusedAdamShard(shard.param_groups(), capturable=spec.capturable,
-                         remainders=spec.remainders, grad_scale=spec.grad_scale)
+                         remainders=spec.remainders, grad_scale=spec.grad_scale, recip_bc=recip_bc)
     init = _inputs(shard)
     t_inf, e_inf = workloads.inf_position(spec) if inf_step else (None, None)
     schedule = []
@@ -154,6 +154,42 @@ def test_large_uniform_bf16_moments_full_size():
     assert steps == want == [2]
     _report("large_uniform_bf16_moments", rep, total)
     assert rep.exact_fraction == 1.0
+
+
+def test_large_uniform_bf16_state_full_size():
+    # the 201-tensor shard with p, m, v and g in bf16 (IEEE division): every
+    # element of two capturable steps, bit for bit in bf16 units
+    spec = workloads.large_uniform(state_dtype=torch.bfloat16, g_dtype=torch.bfloat16)
+    rep, total, steps, want = _full_run(spec, 2, capturable=True)
+    assert steps == want == [2]
+    _report("large_uniform_bf16_state", rep, total)
+    assert rep.exact_fraction == 1.0
+
+
+def test_large_uniform_bf16_state_recip_full_size():
+    # the benchmark's FADAM_RECIP_BC row: one step over all 4,215,275,520
+    # elements, m and v within one bf16 ulp of the oracle's, p under the
+    # reciprocal bound (helpers.check_recip_p16)
+    spec = workloads.large_uniform(state_dtype=torch.bfloat16, g_dtype=torch.bfloat16)
+    shard = workloads.materialize(spec, DEV)
+    opt = FusedAdamShard(shard.param_groups(), capturable=True, recip_bc=True)
+    init = _inputs(shard)
+    opt.step()
+    torch.cuda.synchronize()
+    assert opt.group_steps() == [1]
+    opt.close()
+
+    def unit(u):
+        i, sl = u
+        osh = helpers.oracle_shard(init, idx=[i], elems={i: sl})
+        x0 = helpers.unscaled_p(osh, spec.state_dtype)
+        oracle.shard_step(osh, capturable=True)
+        return helpers.compare_recip(shard, osh, x0, helpers.Report(), idx=[i], elems={i: sl})
+
+    rep = _pool_map(unit, _units(spec, shard.plan_order()))
+    _report("large_uniform_bf16_state, reciprocal corrections", rep, 3 * sum(spec.sizes))
+    del shard, init
+    _free()
 
 
 def test_capturable_l2_full_size_with_inf_step():
@@ -258,6 +294,43 @@ def test_exchange_shard_full_size():
     out = shard.buckets["p_out"].view(torch.int16)
     for d in range(spec.exchange_dests):
         assert torch.equal(shard.dests[d].view(torch.int16), out), f"destination {d}"
+    del shard, init
+    _free()
+
+
+def test_scaled_state_recip_full_size():
+    """The benchmark's scaled-state row with FADAM_RECIP_BC: one step, every
+    element of every tensor: m and v within one fp16 ulp, p and the bf16
+    param-out under the reciprocal bound (helpers.check_recip_p16, values
+    after the scales), every scale within 2e-6 relative."""
+    spec = workloads.scaled_versions(full=True)["scaled_state_shard"]
+    shard = workloads.materialize(spec, DEV)
+    order = shard.plan_order()
+    scales = shard.state_scales[order].contiguous()
+    scales0 = scales.clone()
+    opt = FusedAdamShard(shard.param_groups(), state_scales=scales, recip_bc=True)
+    init = _inputs(shard)
+    opt.step()
+    torch.cuda.synchronize()
+    assert opt.group_steps() == [1]
+    opt.close()
+    got_scales = helpers.to_np(scales).astype(np.float64)
+    pos = {i: k for k, i in enumerate(order)}
+
+    def unit(u):
+        i, _ = u
+        k = pos[i]
+        osh = helpers.oracle_shard(init, idx=[i], scales=scales0[k:k + 1])
+        x0 = helpers.unscaled_p(osh, spec.state_dtype)
+        oracle.shard_step(osh, capturable=False)
+        want = osh.tensors[0].scales.astype(np.float64)
+        assert np.all(np.abs(got_scales[k] - want) <= 2e-6 * np.abs(want)), (i, got_scales[k], want)
+        return helpers.compare_recip(shard, osh, x0, helpers.Report(), idx=[i],
+                                     got_scales=got_scales[k:k + 1])
+
+    rep = _pool_map(unit, _units(spec, order, whole=True))
+    _report("scaled_state_shard, reciprocal corrections", rep,
+            _values_per_element(spec) * sum(spec.sizes))
     del shard, init
     _free()
 

@@ -4,23 +4,17 @@ the oracle.
 With the flag, the 16-bit state forms multiply the moments by 1/bc1 and
 1/bc2 (one IEEE reciprocal per group and CTA) instead of dividing every
 element: each bias-corrected moment carries one more rounding, so the
-update u moves by a few float ulps and a value stored in 16 bits by at most
-one unit in its last place.  That bound holds for one step from a given
-state; over many free-running steps the two paths may drift apart the way
-two 16-bit trajectories do, so each step here starts from the oracle's
-state, written into the GPU tensors, and the step's results are compared:
-p, m, v and a 16-bit param-out within one 16-bit ulp (m and v come out
-exact, being computed before any division), and the scaled state's new
-scales within 2e-6 relative.
-
-An fp32 param-out is p' = p - lr*u unrounded.  The reciprocal's extra
-rounding is relative to lr*u, which exceeds |p'| when the two terms nearly
-cancel (a 16-bit v that underflowed can leave u well above 1), so the
-error bound follows the larger of the terms: |d| <= 2e-6 * max(|p|, |p'|)
-+ 1e-9, the fp32 tolerance's relative form taken against the step's input
-as well as its result (a few float ulps of lr*u <= |p| + |p'| stay far
-inside it).  Ten steps each, at the start of training and across the
-steps where a correction becomes 1, regular and capturable.
+update u moves by a few float ulps.  m and v are computed before any
+division and do not move.  p' = p - lr*u moves by a few ulps of lr*u, and
+lr*u <= |p| + |p'|: where the step nearly cancels p, that is many ulps of a
+small p', so p (and a param-out copy) is held to one ulp of its dtype plus
+2e-6 * max(|p|, |p'|) + 1e-9 (helpers.check_recip_p16), values compared
+after the scale for a scaled state, whose new scales must be within 2e-6
+relative.  That bound holds for one step from a given state; over many
+free-running steps the two paths may drift apart the way two 16-bit
+trajectories do, so each step here starts from the oracle's state, written
+into the GPU tensors.  Ten steps each, at the start of training and across
+the steps where a correction becomes 1, regular and capturable.
 """
 import numpy as np
 import pytest
@@ -33,34 +27,6 @@ from tests import helpers
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-
-
-def _widen16(bits, dtype):
-    return oracle.bf16_to_f32(bits) if dtype == torch.bfloat16 else oracle.f16_to_f32(bits)
-
-
-def _compare_recip(shard, osh, p_before, rep):
-    """16-bit p, m, v and param-out within one ulp; an fp32 param-out within
-    2e-6 * max(|p before the step|, |p'|) + 1e-9."""
-    spec = shard.spec
-    sdt = spec.state_dtype
-    for t, i, x0 in zip(osh.tensors, shard.plan_order(), p_before):
-        rep.ulp16(helpers.to_np(shard.exp_avgs[i]), t.m, f"tensor {i} m", sdt)
-        rep.ulp16(helpers.to_np(shard.exp_avg_sqs[i]), t.v, f"tensor {i} v", sdt)
-        rep.ulp16(helpers.to_np(shard.params[i]), t.p, f"tensor {i} p", sdt)
-        if spec.out_dtype == torch.float32:
-            got = helpers.to_np(shard.params_out[i]).astype(np.float64)
-            want = t.p_out.astype(np.float64)
-            lim = 2e-6 * np.maximum(np.abs(want), np.abs(x0.astype(np.float64))) + 1e-9
-            d = np.abs(got - want)
-            bad = ~(d <= lim)
-            assert not bad.any(), (f"tensor {i} p_out: {int(bad.sum())} outside; first at "
-                                   f"{int(np.argmax(bad))}")
-            rep.n += got.size
-            rep.exact += int(np.sum(got == want))
-        elif spec.out_dtype is not None:
-            rep.ulp16(helpers.to_np(shard.params_out[i]), t.p_out, f"tensor {i} p_out",
-                      spec.out_dtype)
 
 
 def _state_spec(state_dtype, g_dtype, out_dtype):
@@ -93,11 +59,11 @@ def test_recip_16bit_state_each_step_within_one_ulp(state_dtype, g_dtype, out_dt
                 workloads.fresh_grads(shard, k)
                 helpers.refresh_grads(osh, shard)
                 helpers.load_oracle_state(shard, osh)
-            p_before = [_widen16(t.p, state_dtype) for t in osh.tensors]
+            p_before = helpers.unscaled_p(osh, state_dtype)
             opt.step()
             oracle.shard_step(osh, capturable=capturable)
             torch.cuda.synchronize()
-            _compare_recip(shard, osh, p_before, rep)
+            helpers.compare_recip(shard, osh, p_before, rep)
         assert opt.group_steps() == oracle.group_steps(osh) == [start + 10] * 2
         if start == 20000:
             # both corrections are 1 in float: the instance without any
@@ -131,10 +97,11 @@ def test_recip_scaled_state_each_step(name, capturable):
             workloads.fresh_grads(shard, k)
             helpers.refresh_grads(osh, shard)
             helpers.load_oracle_state(shard, osh, scales=scales)
+        p_before = helpers.unscaled_p(osh, spec.state_dtype)
         opt.step()
         oracle.shard_step(osh, capturable=capturable)
         torch.cuda.synchronize()
-        helpers.compare(shard, osh, report=rep)
+        helpers.compare_recip(shard, osh, p_before, rep, got_scales=helpers.to_np(scales))
         got = helpers.to_np(scales).astype(np.float64)
         for j, t in enumerate(osh.tensors):
             want = t.scales.astype(np.float64)
