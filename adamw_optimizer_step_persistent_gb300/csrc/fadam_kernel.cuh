@@ -1747,7 +1747,9 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
                                                          &kp.scratch->next_tail_update, n_items,
                                                          s_tiles, s_full, s_tags, s_prod, s_red,
                                                          stage, unused, timed_out);
-        barrier_ok = grid_barrier(kp.scratch, 0u);
+        // the timeout diagnostic of a plan without the screen acts here
+        barrier_ok = grid_barrier(
+            kp.scratch, ((kp.flags & kTestBarrierTimeout) && !(kp.flags & kCheckFinite)) ? 1u : 0u);
         if (barrier_ok)
           run_pass<ST, GT, OT, REM, Pass::kScaledB, NS, U>(kp, sgrp, item_begin, item_end,
                                                            &kp.scratch->next_rescale,
@@ -1800,12 +1802,13 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
     const double total = cta_sum(x, s_red);
     if (tid == 0) *kp.sumsq_out = total;
   }
-  if (scaled_done && s_last) {
+  if (SCALED && updates && s_last) {
     // the new scales replace the old (tensors that had no element keep
     // theirs), unless some wait of this launch gave up; the absmax slots
-    // are cleared for the next step either way
+    // are cleared for the next step either way, also when this CTA's own
+    // wait between the passes gave up (other CTAs may have filled them)
     __threadfence();
-    const bool ok = ld_acquire_u32(&kp.scratch->launch_timeout) == 0u;
+    const bool ok = scaled_done && ld_acquire_u32(&kp.scratch->launch_timeout) == 0u;
     for (int j = tid; j < 3 * kp.n_tensors; j += kBlock) {
       const unsigned a = __ldcg(kp.absmax + j);
       if (a) {

@@ -117,8 +117,9 @@ fadam_status check_dtypes(const Dtypes& d, uint32_t flags) {
                               "states)");
   if ((flags & FADAM_STEP_PREADVANCED) && !(flags & FADAM_CAPTURABLE))
     return fail(FADAM_EINVAL, "FADAM_STEP_PREADVANCED needs FADAM_CAPTURABLE");
-  if ((flags & FADAM_TEST_BARRIER_TIMEOUT) && !(flags & FADAM_CHECK_FINITE))
-    return fail(FADAM_EINVAL, "FADAM_TEST_BARRIER_TIMEOUT needs FADAM_CHECK_FINITE");
+  if ((flags & FADAM_TEST_BARRIER_TIMEOUT) && !(flags & (FADAM_CHECK_FINITE | FADAM_SCALED_STATES)))
+    return fail(FADAM_EINVAL, "FADAM_TEST_BARRIER_TIMEOUT needs FADAM_CHECK_FINITE or "
+                              "FADAM_SCALED_STATES (a grid barrier to run out)");
   if (d.g != FADAM_DT_F32 && d.g != FADAM_DT_BF16 && d.g != FADAM_DT_F16)
     return fail(FADAM_EDTYPE, "g dtype %d is not fp32, bf16 or fp16", d.g);
   if (d.out != FADAM_DT_NONE && elem_size(d.out) == 0)

@@ -117,13 +117,15 @@ typedef int32_t fadam_status;
  * bound by memory, keep the division and ignore the flag, as do the at most
  * 7 tail elements of each tensor and tensors not 16-byte aligned. */
 #define FADAM_RECIP_BC 128u
-/* Diagnostic, for testing the failure path: with FADAM_CHECK_FINITE, the
- * grid barrier after the inf/nan screen of the plan's FIRST step launch
- * (fadam_step, fadam_step_reduce or fadam_step_host_grads) waits for one
- * more CTA than the launch has, so every CTA's wait runs out after its limit
- * (about 2 s).  That step then updates nothing, advances no counter, and
- * fadam_plan_status() reports FADAM_ETIMEOUT; the plan's later launches run
- * normally, which shows that a plan recovers from a wait that gave up.
+/* Diagnostic, for testing the failure path: the grid barrier after the
+ * inf/nan screen (FADAM_CHECK_FINITE), or else the one between the two
+ * passes of a scaled state (FADAM_SCALED_STATES), of the plan's FIRST step
+ * launch (fadam_step, fadam_step_reduce or fadam_step_host_grads) waits for
+ * one more CTA than the launch has, so every CTA's wait runs out after its
+ * limit (about 2 s).  That step then writes no p, m, v or scales (after the
+ * scaled state's first pass, param-out is written), advances no counter,
+ * and fadam_plan_status() reports FADAM_ETIMEOUT; the plan's later launches
+ * run normally, which shows that a plan recovers from a wait that gave up.
  * fadam_step_noalloc applies it to every call that passes it.  Never set in
  * normal use. */
 #define FADAM_TEST_BARRIER_TIMEOUT 0x80000000u

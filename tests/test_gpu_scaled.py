@@ -156,6 +156,38 @@ def test_scaled_plan_recovers_from_a_wait_that_gave_up():
     opt.close()
 
 
+def test_scaled_barrier_runs_out_then_the_next_step_is_exact():
+    """The first step's wait between the two scaled passes runs out in every
+    CTA (diagnostic flag, a plan without the screen): p, m, v, the scales and
+    the counter stay as they were.  The absmax slots the first pass filled
+    are cleared all the same, so the next step, on fresh gradients, gets
+    exactly the oracle's state and new scales (stale maxima would show in
+    the scales)."""
+    spec, shard, opt, osh, scales = _make("scaled_state_shard", capturable=True,
+                                          extra_flags=_abi.TEST_BARRIER_TIMEOUT)
+    order = shard.plan_order()
+    state = [t.clone() for lst in (shard.params, shard.exp_avgs, shard.exp_avg_sqs)
+             for t in (lst[i] for i in order)]
+    before = scales.clone()
+    opt.step()
+    torch.cuda.synchronize()
+    after = [t for lst in (shard.params, shard.exp_avgs, shard.exp_avg_sqs)
+             for t in (lst[i] for i in order)]
+    assert all(torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(after, state))
+    assert torch.equal(before, opt.state_scales) and opt.group_steps() == [0]
+    assert opt.device_status() == _abi.ETIMEOUT
+    workloads.fresh_grads(shard, 2)
+    helpers.refresh_grads(osh, shard)
+    opt.step()
+    oracle.shard_step(osh, capturable=True)
+    torch.cuda.synchronize()
+    rep = helpers.compare(shard, osh)
+    _check_scales(opt, osh)
+    assert rep.exact_fraction == 1.0 and opt.group_steps() == [1]
+    assert opt.device_status() == _abi.OK
+    opt.close()
+
+
 def test_graph_replay_equals_eager():
     _, a, oa, _, _ = _make("scaled_state_shard", capturable=True)
     _, b, ob, _, _ = _make("scaled_state_shard", capturable=True)
