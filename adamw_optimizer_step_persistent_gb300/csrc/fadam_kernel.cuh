@@ -76,7 +76,7 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // 16-byte aligned, so that a tile loads the ten it needs with three 128-bit
 // loads (a 52-byte record, with no provable vector alignment, took ten
 // 32-bit loads per warp and tile: 1-2 % of the 16-bit forms' instructions).
-// What the tiles do not read lives in the arrays after it.
+// What the tiles do not read lives in the array after it.
 struct alignas(16) SGroup {
   float beta1, omb1, beta2, omb2;  // omb = 1 - beta, rounded once
   float bc1, bc2, eps, wd;
@@ -85,9 +85,7 @@ struct alignas(16) SGroup {
   uint32_t bits;
 };
 static_assert(sizeof(SGroup) == 48, "SGroup is three 16-byte words");
-// Per group: 1/bc1 and 1/bc2 (IEEE reciprocals, read by the FADAM_RECIP_BC
-// tiles in place of bc1 and bc2) and the step this launch applies.
-__shared__ float2 s_group_rbc[FADAM_MAX_GROUPS];
+// Per group: the step this launch applies.
 __shared__ int32_t s_group_step[FADAM_MAX_GROUPS];
 
 // Step counters advance modulo 2^32, as an int32 tensor's += does (no
@@ -1204,10 +1202,7 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
         }
         const unsigned char* st = smem + size_t(b) * Layout<ST, GT, REM>::stage;
         const SGroup& G = sgrp[it.group];
-        constexpr bool kRecip = (UNIT & kRecipBc) != 0;
-        const Scal s{G.beta1, G.omb1, G.beta2, G.omb2,
-                     kRecip ? s_group_rbc[it.group].x : G.bc1,
-                     kRecip ? s_group_rbc[it.group].y : G.bc2, G.eps, G.wd, G.lr, G.gs};
+        const Scal s{G.beta1, G.omb1, G.beta2, G.omb2, G.bc1, G.bc2, G.eps, G.wd, G.lr, G.gs};
         if constexpr (PASS == Pass::kScan) {
           bad |= scan_tile<Layout<ST, GT, REM>::scan_per_thread, GT>(st, tag.len, s.gs);
         } else if constexpr (PASS == Pass::kNorm) {
@@ -1272,7 +1267,7 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
 
 // ---- element-wise paths (tails, runs not 16-byte aligned) -------------------
 
-template <bool ADAMW, int ST, int GT, int OT, Pass PASS>
+template <bool ADAMW, int ST, int GT, int OT, Pass PASS, int UNIT = 0>
 __device__ __forceinline__ void update_elem_state(const Item& it, const Scal& s, int i,
                                                   const Dests& d, const StateScale* sc,
                                                   unsigned* mx) {
@@ -1283,7 +1278,7 @@ __device__ __forceinline__ void update_elem_state(const Item& it, const Scal& s,
     m = __fmul_rn(m, sc->s[1]);
     v = __fmul_rn(v, sc->s[2]);
   }
-  const float x = adam_elem<ADAMW>(x0, m, v, load1<GT>(it.g, i), s);
+  const float x = adam_elem<ADAMW, UNIT>(x0, m, v, load1<GT>(it.g, i), s);
   if constexpr (PASS == Pass::kScaledA) {
     store_out1<OT>(it.p_out, i, x, &d);
     mx[0] = max(mx[0], abs_bits(x));
@@ -1320,17 +1315,17 @@ __device__ __forceinline__ void update_elem_rem(const Item& it, const Scal& s, i
   store_all(op, i, oh, &d);
 }
 
-template <bool ADAMW, int ST, int GT, int OT, bool REM, Pass PASS = Pass::kUpdate>
+template <bool ADAMW, int ST, int GT, int OT, bool REM, Pass PASS = Pass::kUpdate, int UNIT = 0>
 __device__ __forceinline__ void update_elem(const Item& it, const Scal& s, int i, const Dests& d,
                                             const StateScale* sc = nullptr, unsigned* mx = nullptr) {
   if constexpr (REM) update_elem_rem<ADAMW, GT>(it, s, i, d);
-  else update_elem_state<ADAMW, ST, GT, OT, PASS>(it, s, i, d, sc, mx);
+  else update_elem_state<ADAMW, ST, GT, OT, PASS, UNIT>(it, s, i, d, sc, mx);
 }
 
 // A whole item not aligned for bulk copies, by the whole CTA: 128-bit
 // streaming loads when every stream is vector-aligned, then element by
 // element for the rest.
-template <bool ADAMW, int ST, int GT, int OT, bool REM, Pass PASS = Pass::kUpdate>
+template <bool ADAMW, int ST, int GT, int OT, bool REM, Pass PASS = Pass::kUpdate, int UNIT = 0>
 __device__ __forceinline__ void simt_item(const Item& it, const Scal& s, const Dests& d,
                                           const StateScale* sc = nullptr, unsigned* mx = nullptr) {
   const int n = it.n;
@@ -1381,15 +1376,15 @@ __device__ __forceinline__ void simt_item(const Item& it, const Scal& s, const D
         for (int u = 0; u < kUnroll; ++u) {
           const int i = base + u * kBlock;
           if (i < nv)
-            update4_state<ADAMW, ST, GT, OT, PASS>(P[u], M[u], V[u], G[u], s, it.p, it.m, it.v,
-                                                   it.p_out, i, d, sc, mx);
+            update4_state<ADAMW, ST, GT, OT, PASS, UNIT>(P[u], M[u], V[u], G[u], s, it.p, it.m,
+                                                         it.v, it.p_out, i, d, sc, mx);
         }
       }
     }
     scalar_from = nv * kVec;
   }
   for (int i = scalar_from + threadIdx.x; i < n; i += kBlock)
-    update_elem<ADAMW, ST, GT, OT, REM, PASS>(it, s, i, d, sc, mx);
+    update_elem<ADAMW, ST, GT, OT, REM, PASS, UNIT>(it, s, i, d, sc, mx);
 }
 
 // True when this thread saw a non-finite g*grad_scale in the item (by the
@@ -1418,7 +1413,7 @@ __device__ __forceinline__ bool simt_scan(const Item& it, float gs) {
 // Warps pull 32 items at a time from a launch-wide counter and each lane
 // takes one item's tail, so the many small latencies overlap across the
 // whole GPU.
-template <int ST, int GT, int OT, bool REM, Pass PASS>
+template <int ST, int GT, int OT, bool REM, Pass PASS, int UNIT = 0>
 __device__ __forceinline__ bool tail_pass(const KParams& kp, const SGroup* sgrp, unsigned* counter,
                                           int n_items) {
   const int lane = threadIdx.x % 32;
@@ -1450,11 +1445,11 @@ __device__ __forceinline__ bool tail_pass(const KParams& kp, const SGroup* sgrp,
       } else if constexpr (PASS == Pass::kReduce) {
         bad |= reduce_elem<GT>(kp, it, i, s.gs, screen);
       } else if constexpr (PASS == Pass::kScaledA || PASS == Pass::kScaledB) {
-        if (G.bits & kGroupAdamW) update_elem<true, ST, GT, OT, REM, PASS>(it, s, i, dst, &sc, mx);
-        else update_elem<false, ST, GT, OT, REM, PASS>(it, s, i, dst, &sc, mx);
+        if (G.bits & kGroupAdamW) update_elem<true, ST, GT, OT, REM, PASS, UNIT>(it, s, i, dst, &sc, mx);
+        else update_elem<false, ST, GT, OT, REM, PASS, UNIT>(it, s, i, dst, &sc, mx);
       } else {
-        if (G.bits & kGroupAdamW) update_elem<true, ST, GT, OT, REM>(it, s, i, dst);
-        else update_elem<false, ST, GT, OT, REM>(it, s, i, dst);
+        if (G.bits & kGroupAdamW) update_elem<true, ST, GT, OT, REM, Pass::kUpdate, UNIT>(it, s, i, dst);
+        else update_elem<false, ST, GT, OT, REM, Pass::kUpdate, UNIT>(it, s, i, dst);
       }
     }
     if constexpr (PASS == Pass::kScaledA) {  // this lane's item alone: no warp reduction
@@ -1474,7 +1469,7 @@ __device__ __forceinline__ bool tail_pass(const KParams& kp, const SGroup* sgrp,
 // element).  Without the bulk pipeline every item goes this way.  The
 // threads first test kBlock items' flags at once, so a range of bulk items
 // is skipped in a few loads.
-template <int ST, int GT, int OT, bool REM, Pass PASS>
+template <int ST, int GT, int OT, bool REM, Pass PASS, int UNIT = 0>
 __device__ __forceinline__ bool rest_pass(const KParams& kp, const SGroup* sgrp, int item_begin,
                                           int item_end, double* red) {
   __shared__ int s_count;
@@ -1518,12 +1513,12 @@ __device__ __forceinline__ bool rest_pass(const KParams& kp, const SGroup* sgrp,
       } else if constexpr (PASS == Pass::kScaledA || PASS == Pass::kScaledB) {
         const StateScale sc = tensor_scales(kp, it.tensor, PASS == Pass::kScaledB);
         unsigned mx[3] = {0u, 0u, 0u};
-        if (G.bits & kGroupAdamW) simt_item<true, ST, GT, OT, REM, PASS>(it, s, dst, &sc, mx);
-        else simt_item<false, ST, GT, OT, REM, PASS>(it, s, dst, &sc, mx);
+        if (G.bits & kGroupAdamW) simt_item<true, ST, GT, OT, REM, PASS, UNIT>(it, s, dst, &sc, mx);
+        else simt_item<false, ST, GT, OT, REM, PASS, UNIT>(it, s, dst, &sc, mx);
         if constexpr (PASS == Pass::kScaledA) flush_absmax(kp, it.tensor, mx);
       } else {
-        if (G.bits & kGroupAdamW) simt_item<true, ST, GT, OT, REM>(it, s, dst);
-        else simt_item<false, ST, GT, OT, REM>(it, s, dst);
+        if (G.bits & kGroupAdamW) simt_item<true, ST, GT, OT, REM, Pass::kUpdate, UNIT>(it, s, dst);
+        else simt_item<false, ST, GT, OT, REM, Pass::kUpdate, UNIT>(it, s, dst);
       }
     }
     __syncthreads();  // s_list is reused
@@ -1547,10 +1542,14 @@ __device__ __forceinline__ void run_pass(const KParams& kp, const SGroup* sgrp, 
   // all go through the tiles the rest pass: a global round trip each on
   // every CTA's path (the norm writes every bulk item's slot in its tail
   // pass, so it keeps it)
+  // the element-wise paths multiply by reciprocal corrections where the
+  // tiles do (the group record then holds reciprocals); the divisions by
+  // corrections of 1 they keep (identities)
+  constexpr int EU = UNIT & kRecipBc;
   if (bulk && (PASS == Pass::kNorm || !(kp.flags & kNoTails)))
-    bad |= tail_pass<ST, GT, OT, REM, PASS>(kp, sgrp, tail_counter, n_items);
+    bad |= tail_pass<ST, GT, OT, REM, PASS, EU>(kp, sgrp, tail_counter, n_items);
   if (!bulk || !(kp.flags & kAllBulk))
-    bad |= rest_pass<ST, GT, OT, REM, PASS>(kp, sgrp, item_begin, item_end, red);
+    bad |= rest_pass<ST, GT, OT, REM, PASS, EU>(kp, sgrp, item_begin, item_end, red);
 }
 
 // Grid-wide barrier for a cooperative launch.  The wait is bounded: after
@@ -1650,7 +1649,13 @@ __global__ void FADAM_BOUNDS fadam_update_kernel(const __grid_constant__ KParams
       s.bc1 = bias_correction(G.beta1, step);
       s.bc2 = bias_correction(G.beta2, step);
     }
-    s_group_rbc[tid] = make_float2(__frcp_rn(s.bc1), __frcp_rn(s.bc2));
+    if constexpr (RECIP) {
+      // the reciprocal instances keep 1/bc1 and 1/bc2 in their place (IEEE
+      // reciprocals; 1 stays 1, so the launch-wide test for corrections of
+      // 1 below reads the same)
+      s.bc1 = __frcp_rn(s.bc1);
+      s.bc2 = __frcp_rn(s.bc2);
+    }
     sgrp[tid] = s;
   }
   __syncthreads();

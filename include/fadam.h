@@ -103,8 +103,8 @@ typedef int32_t fadam_status;
 /* Reciprocal bias corrections, for the 16-bit state forms (FADAM_DT_BF16 or
  * FADAM_DT_F16 state, plain or FADAM_SCALED_STATES), whose update is bound
  * by instruction issue rather than by memory: each CTA computes 1/bc1 and
- * 1/bc2 once per group (IEEE reciprocals) and the update tiles multiply the
- * moments by them instead of dividing every element by bc1 and bc2 (the
+ * 1/bc2 once per group (IEEE reciprocals) and the update multiplies the
+ * moments of every element by them instead of dividing by bc1 and bc2 (the
  * functor's m/bc1 and v/bc2).  Each bias-corrected moment then carries two
  * roundings instead of one, so results are no longer bit-identical to the
  * division: the update u = m_hat / (sqrt(v_hat) + eps) moves by at most a
@@ -113,9 +113,9 @@ typedef int32_t fadam_status;
  * param-out) lands within one unit in its last place plus
  * 2e-6 * max(|p|, |p'|) of the divided result per step (more than one ulp
  * only where the step nearly cancels p).  Once a correction rounds to 1 in
- * float the multiply is exact.  Other state forms (fp32 master, remainders, 16-bit moments) are
- * bound by memory, keep the division and ignore the flag, as do the at most
- * 7 tail elements of each tensor and tensors not 16-byte aligned. */
+ * float the multiply is exact.  Other state forms (fp32 master, remainders,
+ * 16-bit moments) are bound by memory, keep the division and ignore the
+ * flag. */
 #define FADAM_RECIP_BC 128u
 /* Diagnostic, for testing the failure path: the grid barrier after the
  * inf/nan screen (FADAM_CHECK_FINITE), or else the one between the two
