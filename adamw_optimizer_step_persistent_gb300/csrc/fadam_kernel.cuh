@@ -404,6 +404,29 @@ __device__ __forceinline__ void flush_absmax(const KParams& kp, int t, unsigned 
   }
 }
 
+// Pass A, bulk tiles: a warp's maxima into the CTA's shared slots (1 + bits,
+// 0 = none yet); thread 0 takes them to the tensor's global slots with
+// push_absmax once every warp has added its own.
+__device__ __forceinline__ void gather_absmax(unsigned* sm, unsigned (&mx)[3]) {
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const unsigned w = __reduce_max_sync(0xffffffffu, mx[k]);
+    if ((threadIdx.x & 31) == 0) atomicMax(sm + k, w + 1u);
+    mx[k] = 0u;
+  }
+}
+
+// Thread 0: the CTA's maxima of tensor t into its global slots, and the
+// shared slots cleared for a later item.
+__device__ __forceinline__ void push_absmax(const KParams& kp, int t, unsigned* sm) {
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const unsigned a = sm[k];
+    if (a) atomicMax(kp.absmax + 3 * t + k, a);
+    sm[k] = 0u;
+  }
+}
+
 // One 4-element vector of the remainder form: H the bf16 high halves, R the
 // remainders; the new remainders go to rem, the new high halves to out.
 template <bool ADAMW, int GT>
@@ -1164,6 +1187,18 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
   const Dests dst{kp.n_dests, kp.dst_delta};
   const bool screen = (kp.flags & kCheckFinite) != 0;  // reduce pass: screen the result
   unsigned mx[3] = {0u, 0u, 0u};                        // scaled pass A: |new value| maxima
+  // scaled pass A: when the tiles move on to another item, the warps' maxima
+  // of the one they leave meet in shared memory and thread 0 takes them to
+  // the global slots after the tile's barrier (three global atomics per CTA
+  // and item, not three per warp: with 152 CTAs on neighbouring chunks of
+  // one tensor, those land on the same three words).  Two buffers: the
+  // warps may fill the next one while thread 0 empties the last.
+  __shared__ unsigned s_amax[2][3];
+  int amax_tensor = -1;  // tensor whose maxima wait in s_amax[amax_buf ^ 1]
+  unsigned amax_buf = 0;  // the buffer the next gather fills
+  if constexpr (PASS == Pass::kScaledA) {
+    if (threadIdx.x < 6) s_amax[threadIdx.x / 3][threadIdx.x % 3] = 0u;  // read after a tile's barrier
+  }
   NormAcc na{0.0f, 0.0f, false, -1, 0};
   NormPending pend{-1, 0.0f};
   double* dpart = nullptr;
@@ -1195,8 +1230,13 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
       tag = tags[b];
       if (tag.item >= 0) {
         if (tag.item != cur_item) {
-          if constexpr (PASS == Pass::kScaledA)
-            if (cur_item >= 0) flush_absmax(kp, it.tensor, mx);
+          if constexpr (PASS == Pass::kScaledA) {
+            if (cur_item >= 0) {
+              gather_absmax(s_amax[amax_buf], mx);
+              amax_tensor = it.tensor;
+              amax_buf ^= 1u;
+            }
+          }
           cur_item = tag.item;
           it = load_item(kp.items, tag.item);
         }
@@ -1243,10 +1283,21 @@ __device__ __forceinline__ void bulk_pass(const KParams& kp, const SGroup* sgrp,
         pend.chunk = -1;
       }
     }
+    if constexpr (PASS == Pass::kScaledA) {
+      if (amax_tensor >= 0) {  // every warp's gather came before the barrier
+        if (threadIdx.x == 0) push_absmax(kp, amax_tensor, s_amax[amax_buf ^ 1u]);
+        amax_tensor = -1;
+      }
+    }
     if (tag.item < 0) {  // the end marker (the same for every thread)
       ++stage;
-      if constexpr (PASS == Pass::kScaledA)
-        if (cur_item >= 0) flush_absmax(kp, it.tensor, mx);
+      if constexpr (PASS == Pass::kScaledA) {
+        if (cur_item >= 0) {
+          gather_absmax(s_amax[amax_buf], mx);
+          __syncthreads();
+          if (threadIdx.x == 0) push_absmax(kp, it.tensor, s_amax[amax_buf]);
+        }
+      }
       if constexpr (PASS == Pass::kNorm) {
         if (na.chunk >= 0) {
           const NormBuf buf = norm_buf(red, closes);
