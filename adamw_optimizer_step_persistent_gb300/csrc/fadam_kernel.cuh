@@ -394,7 +394,8 @@ __device__ __forceinline__ void update4_state(const typename Raw4<p_dtype_of(ST)
   }
 }
 
-// Pass A: a warp's maxima into the tensor's absmax slots (1 + bits).
+// Pass A, items off the tiles (the rest pass, a CTA at a time): a warp's
+// maxima into the tensor's absmax slots (1 + bits).
 __device__ __forceinline__ void flush_absmax(const KParams& kp, int t, unsigned (&mx)[3]) {
 #pragma unroll
   for (int k = 0; k < 3; ++k) {
