@@ -214,6 +214,36 @@ def test_unrolled_and_generic_reduce_tiles(ranks, average):
     opt.close()
 
 
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_sixteen_sources_and_sixteen_destinations(accumulate):
+    """The exchange at its limits (FADAM_MAX_SOURCES, FADAM_MAX_DESTS): 16
+    ranks' slices through the generic reduce loop (17 slices per tile when
+    the shard's old g is added to them), param-out written to 16
+    destinations; the reduced shard bit for bit, the state and every
+    destination against the oracle over two steps."""
+    spec = workloads.exchange_shard(layers=1, hidden=256, ffn=688, ranks=16, dests=16)
+    shard = workloads.materialize(spec, DEV)
+    opt = FusedAdamShard(shard.param_groups(), capturable=True)
+    opt.set_exchange(shard.buckets["g"], list(shard.sources), average=spec.exchange_average,
+                     out_shard=shard.buckets["p_out"], dests=list(shard.dests),
+                     accumulate=accumulate)
+    osh = helpers.oracle_shard(shard)
+    src = _oracle_sources(shard)
+    rep = helpers.Report()
+    for _ in range(2):
+        opt.step_reduce()
+        oracle.exchange_step(osh, src, average=spec.exchange_average, capturable=True,
+                             accumulate=accumulate)
+        torch.cuda.synchronize()
+        _check_reduced(shard, osh)
+        helpers.compare(shard, osh, report=rep)
+        _check_dests(shard)
+    assert shard.dests.shape[0] == 16 and shard.sources.shape[0] == 16
+    assert rep.exact_fraction == 1.0, rep.exact_fraction
+    assert opt.group_steps() == [2]
+    opt.close()
+
+
 def _rotated(shard, k):
     """The ranks' buffers in rank order rotated by k: each micro-batch's
     contributions arrive in another order, so their sums differ."""
