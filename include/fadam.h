@@ -113,9 +113,12 @@ typedef int32_t fadam_status;
  * param-out) lands within one unit in its last place plus
  * 2e-6 * max(|p|, |p'|) of the divided result per step (more than one ulp
  * only where the step nearly cancels p).  Once a correction rounds to 1 in
- * float the multiply is exact.  Other state forms (fp32 master, remainders,
- * 16-bit moments) are bound by memory, keep the division and ignore the
- * flag. */
+ * float the multiply is exact.  Infinite and NaN inputs give the same
+ * non-finite results as the division; the bound holds while m/bc1 and
+ * v/bc2 stay finite (where m is within a few ulps of FLT_MAX * bc1, m/bc1
+ * may be infinite in one form and finite in the other; likewise v).  Other
+ * state forms (fp32 master, remainders, 16-bit moments) are bound by memory,
+ * keep the division and ignore the flag. */
 #define FADAM_RECIP_BC 128u
 /* Diagnostic, for testing the failure path: the grid barrier after the
  * inf/nan screen (FADAM_CHECK_FINITE), or else the one between the two
