@@ -110,3 +110,58 @@ def test_recip_scaled_state_each_step(name, capturable):
     print(f"{name} capturable {capturable}: {rep.n} values, "
           f"{rep.exact_fraction:.6f} bit-identical")
     opt.close()
+
+
+@pytest.mark.parametrize("start", [0, 160])
+def test_recip_special_values(start):
+    """Infinities, NaNs, signed zeros, subnormals and values near overflow in
+    p, m, v and g of a bf16 state with fp16 gradients and an fp16 param-out,
+    with FADAM_RECIP_BC, one step from the same state on both sides: m and v
+    bit-identical to the oracle (no division precedes them), every p or
+    param-out value that is infinite or NaN on either side the same on the
+    other (NaN where the oracle gives NaN, the same infinity), and the
+    finite ones within the derived bound."""
+    from tests.test_gpu_parity import _sprinkle
+    spec = workloads.large_uniform(n_tensors=3, numel=40_003, state_dtype=torch.bfloat16,
+                                   g_dtype=torch.float16)
+    spec.out_dtype = torch.float16
+    shard = workloads.materialize(spec, DEV)
+    gen = np.random.default_rng(16)
+    for i in range(len(shard.params)):
+        shard.exp_avgs[i].copy_(torch.randn_like(shard.exp_avgs[i]) * 1e-2)
+        shard.exp_avg_sqs[i].copy_(torch.rand_like(shard.exp_avg_sqs[i]) * 1e-4)
+        for t, every in ((shard.params[i], 7), (shard.exp_avgs[i], 11),
+                         (shard.exp_avg_sqs[i], 13), (shard.grads[i], 5)):
+            _sprinkle(t, gen, every)
+    opt = FusedAdamShard(shard.param_groups(), capturable=True, recip_bc=True)
+    osh = helpers.oracle_shard(shard)
+    if start:
+        opt.set_group_steps([start] * len(spec.groups))
+        osh.steps = [start] * len(osh.steps)
+    p_before = helpers.unscaled_p(osh, spec.state_dtype)
+    opt.step()
+    oracle.shard_step(osh, capturable=True)
+    torch.cuda.synchronize()
+    rep = helpers.Report()
+    n_nonfinite = 0
+    for t, i, x0 in zip(osh.tensors, shard.plan_order(), p_before):
+        for got_t, want, what in ((shard.exp_avgs[i], t.m, "m"), (shard.exp_avg_sqs[i], t.v, "v")):
+            got = helpers.to_np(got_t)
+            nan = np.isnan(helpers.widen16(got, spec.state_dtype))
+            want_nan = np.isnan(helpers.widen16(want, spec.state_dtype))
+            # the same bits, any two NaNs alike (payloads are not compared)
+            assert ((got == want) | (nan & want_nan)).all(), f"tensor {i} {what}"
+        for got_t, want, dt, what in ((shard.params[i], t.p, spec.state_dtype, "p"),
+                                      (shard.params_out[i], t.p_out, spec.out_dtype, "p_out")):
+            got = helpers.to_np(got_t)
+            g = helpers.widen16(got, dt)
+            w = helpers.widen16(want, dt)
+            special = ~np.isfinite(g) | ~np.isfinite(w) | ~np.isfinite(x0)
+            same = (g == w) | (np.isnan(g) & np.isnan(w))
+            assert same[~np.isfinite(g) | ~np.isfinite(w)].all(), f"tensor {i} {what}: non-finite"
+            n_nonfinite += int(special.sum())
+            helpers.check_recip_p16(got[~special], want[~special], dt, x0[~special],
+                                    f"tensor {i} {what}", rep)
+    assert n_nonfinite > 0 and rep.n > 0
+    print(f"start {start}: {n_nonfinite} non-finite values matched, {rep.n} finite within the bound, "
+          f"{rep.exact_fraction:.6f} of those bit-identical")
