@@ -156,10 +156,13 @@ def check_recip_p16(got_bits, want_bits, dtype, x_before, what, report,
     x = np.abs(np.asarray(x_before, np.float64))
     both_nan = np.isnan(g) & np.isnan(w)
     same = (g == w) | both_nan
+    # a value that is infinite or NaN on either side must be the same on
+    # the other (the bound's terms are infinite there)
+    nonfinite = ~np.isfinite(g) | ~np.isfinite(w)
     with np.errstate(invalid="ignore", over="ignore"):
         lim = (ulp16(widen16(want_bits, dtype), dtype) * abs(np.float64(want_scale))
                + 2e-6 * np.maximum(x, np.abs(w)) + 1e-9)
-        bad = ~same & ~(np.abs(g - w) <= lim)
+        bad = ~same & (nonfinite | ~(np.abs(g - w) <= lim))
     if bad.any():
         k = int(np.argmax(bad))
         raise AssertionError(f"{what}: {int(bad.sum())} of {g.size} outside the bound; first at "
@@ -190,7 +193,10 @@ def compare_recip(shard: workloads.Shard, osh: oracle.Shard, x_before, report: R
             got = to_np(sel(shard.params_out[i])).astype(np.float64)
             want = t.p_out.astype(np.float64)
             lim = 2e-6 * np.maximum(np.abs(want), np.abs(np.asarray(x0, np.float64))) + 1e-9
-            bad = ~(np.abs(got - want) <= lim) & ~(np.isnan(got) & np.isnan(want)) & (got != want)
+            nonfinite = ~np.isfinite(got) | ~np.isfinite(want)  # must be the same there
+            with np.errstate(invalid="ignore"):
+                bad = ((nonfinite | ~(np.abs(got - want) <= lim))
+                       & ~(np.isnan(got) & np.isnan(want)) & (got != want))
             assert not bad.any(), f"tensor {i} p_out: {int(bad.sum())} outside; first at {int(np.argmax(bad))}"
             report.n += got.size
             report.exact += int(np.sum(got == want))
