@@ -8,3 +8,10 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+
+# the property tests need hypothesis, which not every machine that runs the
+# suite has; without it the module is left out rather than reported skipped
+try:
+    import hypothesis  # noqa: F401
+except ImportError:
+    collect_ignore = ["test_pack_properties.py"]

@@ -223,6 +223,12 @@ def _ordered16(bits: np.ndarray) -> np.ndarray:
     return np.where(b & 0x8000, -(b & 0x7FFF), b)
 
 
+def _is_inf_or_nan16(bits: np.ndarray, dtype) -> np.ndarray:
+    b = bits.astype(np.int32)
+    e = 0x7F80 if dtype == torch.bfloat16 else 0x7C00
+    return (b & e) == e
+
+
 def _is_nan16(bits: np.ndarray, dtype) -> np.ndarray:
     b = bits.astype(np.int32)
     if dtype == torch.bfloat16:
@@ -283,8 +289,14 @@ class Report:
         if self._same_bytes(got, want):
             return
         d = np.abs(_ordered16(got) - _ordered16(want))
-        if dtype is not None:  # two NaNs match whatever their payloads
-            d = np.where(_is_nan16(got, dtype) & _is_nan16(want, dtype), 0, d)
+        if dtype is not None:
+            # an infinity sits one step from the largest finite value in this
+            # order: a value that is infinite or NaN on either side must be
+            # the same on the other; two NaNs match whatever their payloads
+            both_nan = _is_nan16(got, dtype) & _is_nan16(want, dtype)
+            nonfinite = _is_inf_or_nan16(got, dtype) | _is_inf_or_nan16(want, dtype)
+            d = np.where(nonfinite & (np.asarray(got) != np.asarray(want)), 1 << 20, d)
+            d = np.where(both_nan, 0, d)
         if (d > 1).any():
             k = int(np.argmax(d > 1))
             raise AssertionError(f"{what}: {int((d > 1).sum())} values beyond 1 ulp; first at "
