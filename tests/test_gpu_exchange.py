@@ -39,9 +39,18 @@ def _oracle_sources(shard, idx=None):
 
 
 def _check_reduced(shard, osh):
+    """The reduced shard bit for bit (any two NaNs alike: their payloads
+    are not compared)."""
     for t, i in zip(osh.tensors, shard.plan_order()):
         got = helpers.to_np(shard.grads[i])
-        assert got.tobytes() == t.g.tobytes(), f"tensor {i}: reduced gradient differs"
+        if got.tobytes() == t.g.tobytes():
+            continue
+        dt = shard.grads[i].dtype
+        if dt == torch.float32:
+            nan = np.isnan(got) & np.isnan(t.g)
+        else:
+            nan = np.isnan(helpers.widen16(got, dt)) & np.isnan(helpers.widen16(t.g, dt))
+        assert ((got == t.g) | nan).all(), f"tensor {i}: reduced gradient differs"
 
 
 def _check_dests(shard):
@@ -151,6 +160,34 @@ def test_norm_of_the_reduced_shard():
     osh = helpers.oracle_shard(shard)
     want = oracle.shard_sumsq(osh)
     assert got == pytest.approx(want, rel=2e-6)
+    opt.close()
+
+
+@pytest.mark.parametrize("case", ["inf", "nan", "overflow"])
+def test_reduce_special_values(case):
+    """An infinity or NaN in one rank's contribution, and contributions
+    whose float sum overflows, reach the reduced shard as the oracle's
+    reduction gives them (a NaN's payload aside: the GPU writes its own)."""
+    spec, shard, opt = _make("exchange_shard")
+    i = shard.plan_order()[2]
+    o = shard.offsets[i]
+    if case == "inf":
+        shard.sources[2, o + 5] = float("inf")
+    elif case == "nan":
+        shard.sources[1, o + 77] = float("nan")
+    else:
+        shard.sources[:, o:o + 3000] = 2e38
+    osh = helpers.oracle_shard(shard)
+    for t, src in zip(osh.tensors, _oracle_sources(shard)):
+        t.g[...] = oracle.reduce_into(t.g, src, t.g_dtype, spec.exchange_average, False)
+    opt.grad_reduce()
+    torch.cuda.synchronize()
+    _check_reduced(shard, osh)
+    g = shard.grads[i].float()
+    if case == "nan":
+        assert torch.isnan(g[77])
+    else:
+        assert torch.isinf(g[5] if case == "inf" else g[0])
     opt.close()
 
 
